@@ -1,0 +1,451 @@
+// SIMT forward of the Lizard token mixer (fp32 path, and every shape the tensor-core
+// path does not cover).
+//
+// Lizard summary (gist.science/ko/paper/2507.09025): sec. 2-A-1 gated linear
+// attention over the tokens that have left the window, sec. 2-A-2 sliding-window
+// softmax with meta-memory scalars in the denominator, sec. 2-C Hedgehog feature
+// map and gates in log space.  Decays are exp of differences of cumulative
+// log-gates, always arranged as exp(non-positive), so nothing overflows.
+//
+// Three launches:
+//   1. seglocal: every segment but the last computes its own state contribution
+//      dH = sum_t e^{B_end - B_t} phi(k_{t-w}) v_{t-w}^T (and dz) and its total
+//      log-decay dLam, starting from a zero state;
+//   2. scan: an fp32 scan over segments turns those into each segment's
+//      starting state H_p = e^{dLam_{p-1}} H_{p-1} + dH_{p-1};
+//   3. main: one CTA per (query head, segment) walks its segment 32 tokens at a
+//      time: state readout, intra-sub-chunk state term, window softmax with
+//      sinks, shared-normaliser epilogue, state update.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lz {
+namespace {
+
+constexpr int NT = 256;  // threads per CTA
+constexpr int TS = 32;   // tokens per sub-chunk
+constexpr int KT = 16;   // window keys per smem tile
+
+template <int DH, int DF>
+struct Lay {
+    static constexpr int PF = DF + 1;  // padded row strides (rows are read across lanes)
+    static constexpr int PH = DH + 1;
+    static constexpr int oH = 0;
+    static constexpr int oz = oH + DF * DH;
+    static constexpr int oW = oz + DF;
+    static constexpr int ob = oW + DH * (DF / 2);
+    static constexpr int ophk = ob + TS * PF;
+    static constexpr int ov = ophk + TS * PF;
+    static constexpr int oq = ov + TS * DH;
+    static constexpr int ophq = oq + TS * PH;
+    static constexpr int oA = ophq + TS * PF;
+    static constexpr int oR = oA + TS * (TS + 1);
+    static constexpr int RSZ = (TS * PF > KT * PH + KT * DH) ? TS * PF : KT * PH + KT * DH;
+    static constexpr int oP = oR + RSZ;
+    static constexpr int total = oP + TS * KT;
+    static constexpr size_t bytes = sizeof(float) * (size_t)total;
+};
+
+// Rows t in [rlo, rhi) of x (token tok0 + t, head hx) into s[t][*] (stride sst); zeros elsewhere.
+template <typename T, int DH>
+__device__ __forceinline__ void load_rows(const T* x, int64_t b, int64_t L, int64_t Hx,
+                                          int64_t hx, int64_t tok0, int rlo, int rhi, float* s,
+                                          int sst) {
+    for (int e = threadIdx.x; e < TS * DH; e += NT) {
+        const int t = e / DH, c = e % DH;
+        float val = 0.0f;
+        if (t >= rlo && t < rhi) val = ld(x + ((b * L + tok0 + t) * Hx + hx) * DH + c);
+        s[t * sst + c] = val;
+    }
+}
+
+// Hedgehog map of TS rows: sout[t] = [softmax(x_t Wf), softmax(-x_t Wf)] for t in
+// [rlo, rhi), zeros elsewhere.  Eight lanes per row.
+template <int DH, int DF, bool FAST>
+__device__ __forceinline__ void phi_rows(const float* sx, const float* sW, float* sout, int rlo,
+                                         int rhi) {
+    constexpr int H = DF / 2, PH = DH + 1, PF = DF + 1, NJ = H / 8;
+    const int r = threadIdx.x >> 3, sub = threadIdx.x & 7;
+    float u[NJ];
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) u[j] = 0.0f;
+    const float* x = sx + r * PH;
+    for (int c = 0; c < DH; ++c) {
+        const float xc = x[c];
+        const float* wr = sW + c * H + sub;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) u[j] = fmaf(xc, wr[8 * j], u[j]);
+    }
+    float mx = u[0], mn = u[0];
+#pragma unroll
+    for (int j = 1; j < NJ; ++j) {
+        mx = fmaxf(mx, u[j]);
+        mn = fminf(mn, u[j]);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+    }
+    float ep[NJ], en[NJ], sp = 0.0f, sn = 0.0f;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        ep[j] = ex<FAST>(u[j] - mx);
+        en[j] = ex<FAST>(mn - u[j]);
+        sp += ep[j];
+        sn += en[j];
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+        sp += __shfl_xor_sync(0xffffffffu, sp, o);
+        sn += __shfl_xor_sync(0xffffffffu, sn, o);
+    }
+    const bool valid = r >= rlo && r < rhi;
+    const float ip = valid ? 1.0f / sp : 0.0f, in = valid ? 1.0f / sn : 0.0f;
+    float* o = sout + r * PF;
+#pragma unroll
+    for (int j = 0; j < NJ; ++j) {
+        o[sub + 8 * j] = ep[j] * ip;
+        o[H + sub + 8 * j] = en[j] * in;
+    }
+}
+
+// sb[t][f] = sum_{s<=t} log sigmoid(g_{i0+s, f}) for the n valid rows; rows >= n add 0.
+template <typename T, int DF, bool FAST>
+__device__ __forceinline__ void gates_cumsum(const T* g, int64_t b, int64_t L, int64_t Hkv,
+                                             int64_t kv, int64_t i0, int n, float* sb) {
+    constexpr int PF = DF + 1;
+    for (int e = threadIdx.x; e < TS * DF; e += NT) {
+        const int t = e / DF, f = e % DF;
+        float lam = 0.0f;
+        if (t < n) lam = log_sigmoid<FAST>(ld(g + ((b * L + i0 + t) * Hkv + kv) * DF + f));
+        sb[t * PF + f] = lam;
+    }
+    __syncthreads();
+    if (threadIdx.x < DF) {
+        const int f = threadIdx.x;
+        float acc = 0.0f;
+        for (int t = 0; t < TS; ++t) {
+            acc += sb[t * PF + f];
+            sb[t * PF + f] = acc;
+        }
+    }
+    __syncthreads();
+}
+
+// H <- e^{b_last} (.) H + sum_t (phk_t e^{b_last - b_t}) v_t^T, z likewise.
+// Overwrites sphk with the decayed keys.
+template <int DH, int DF, bool FAST>
+__device__ __forceinline__ void state_update(float* sH, float* sz, float* sphk, const float* sv,
+                                             const float* sb) {
+    constexpr int PF = DF + 1;
+    for (int e = threadIdx.x; e < TS * DF; e += NT) {
+        const int t = e / DF, f = e % DF;
+        sphk[t * PF + f] *= ex<FAST>(sb[(TS - 1) * PF + f] - sb[t * PF + f]);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < DF * DH; e += NT) {
+        const int f = e / DH, c = e % DH;
+        float acc = ex<FAST>(sb[(TS - 1) * PF + f]) * sH[e];
+#pragma unroll 8
+        for (int t = 0; t < TS; ++t) acc = fmaf(sphk[t * PF + f], sv[t * DH + c], acc);
+        sH[e] = acc;
+    }
+    if (threadIdx.x < DF) {
+        const int f = threadIdx.x;
+        float acc = ex<FAST>(sb[(TS - 1) * PF + f]) * sz[f];
+        for (int t = 0; t < TS; ++t) acc += sphk[t * PF + f];
+        sz[f] = acc;
+    }
+    __syncthreads();
+}
+
+template <typename T, int DH, int DF, bool FAST>
+__global__ void __launch_bounds__(NT, 1) fwd_simt_seglocal(Plan p, FwdArgs a) {
+    using Ly = Lay<DH, DF>;
+    extern __shared__ float sm[];
+    float *sH = sm + Ly::oH, *sz = sm + Ly::oz, *sW = sm + Ly::oW, *sb = sm + Ly::ob;
+    float *sphk = sm + Ly::ophk, *sv = sm + Ly::ov, *sq = sm + Ly::oq;
+    const int64_t unit = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t s0 = seg * p.seg_len, s1 = min64(p.L, s0 + p.seg_len);
+    const T* W = (const T*)a.Wf + kv * DH * (DF / 2);
+    for (int e = threadIdx.x; e < DH * (DF / 2); e += NT) sW[e] = ld(W + e);
+    for (int e = threadIdx.x; e < DF * DH; e += NT) sH[e] = 0.0f;
+    if (threadIdx.x < DF) sz[threadIdx.x] = 0.0f;
+    float lam_tot = 0.0f;  // thread f < DF: total log-decay of the segment
+    __syncthreads();
+    for (int64_t i0 = s0; i0 < s1; i0 += TS) {
+        const int n = (int)min64(TS, s1 - i0);
+        gates_cumsum<T, DF, FAST>((const T*)a.g, b, p.L, p.Hkv, kv, i0, n, sb);
+        const int rlo = (int)min64(n, max64(0, p.w - i0));
+        load_rows<T, DH>((const T*)a.k, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n, sq, Ly::PH);
+        load_rows<T, DH>((const T*)a.v, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n, sv, DH);
+        __syncthreads();
+        phi_rows<DH, DF, FAST>(sq, sW, sphk, rlo, n);
+        if (threadIdx.x < DF) lam_tot += sb[(TS - 1) * Ly::PF + threadIdx.x];
+        __syncthreads();
+        state_update<DH, DF, FAST>(sH, sz, sphk, sv, sb);
+    }
+    float* rec = a.seg + ((size_t)seg * (size_t)(p.B * p.Hkv) + (size_t)unit) * p.rec_floats;
+    for (int e = threadIdx.x; e < DF * DH; e += NT) rec[e] = sH[e];
+    if (threadIdx.x < DF) {
+        rec[DF * DH + threadIdx.x] = sz[threadIdx.x];
+        rec[DF * DH + DF + threadIdx.x] = lam_tot;
+    }
+}
+
+// Exclusive scan over segments, in place: record p becomes the state before segment p.
+__global__ void fwd_seg_scan(Plan p, float* seg) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int64_t unit = blockIdx.y;
+    const int64_t nE = p.D * p.d + p.D;
+    if (e >= nE) return;
+    const int64_t f = e < p.D * p.d ? e / p.d : e - p.D * p.d;
+    const int64_t U = p.B * p.Hkv;
+    float carry = 0.0f;
+    for (int64_t s = 0; s < p.P; ++s) {
+        float* rec = seg + ((size_t)s * U + unit) * p.rec_floats;
+        float dH = 0.0f, lam = 0.0f;
+        if (s < p.P - 1) {
+            dH = rec[e];
+            lam = rec[p.D * p.d + p.D + f];
+        }
+        rec[e] = carry;
+        carry = expf(lam) * carry + dH;
+    }
+}
+
+template <typename T, int DH, int DF, bool FAST>
+__global__ void __launch_bounds__(NT, 1) fwd_simt_main(Plan p, FwdArgs a) {
+    using Ly = Lay<DH, DF>;
+    constexpr int PF = Ly::PF, PH = Ly::PH, NC = DH / 8;
+    extern __shared__ float sm[];
+    float *sH = sm + Ly::oH, *sz = sm + Ly::oz, *sW = sm + Ly::oW, *sb = sm + Ly::ob;
+    float *sphk = sm + Ly::ophk, *sv = sm + Ly::ov, *sq = sm + Ly::oq, *sphq = sm + Ly::ophq;
+    float *sA = sm + Ly::oA, *sR = sm + Ly::oR, *sP = sm + Ly::oP;
+    const int64_t bh = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = bh / p.Hq, h = bh % p.Hq, kv = h / p.G;
+    const int64_t s0 = seg * p.seg_len;
+    if (s0 >= p.L) return;
+    const int64_t s1 = min64(p.L, s0 + p.seg_len);
+    const int64_t unit = b * p.Hkv + kv;
+    const int tid = threadIdx.x;
+    const T* W = (const T*)a.Wf + kv * DH * (DF / 2);
+    for (int e = tid; e < DH * (DF / 2); e += NT) sW[e] = ld(W + e);
+    if (seg == 0) {
+        for (int e = tid; e < DF * DH; e += NT) sH[e] = 0.0f;
+        if (tid < DF) sz[tid] = 0.0f;
+    } else {
+        const float* rec = a.seg + ((size_t)seg * (size_t)(p.B * p.Hkv) + (size_t)unit) *
+                                       p.rec_floats;
+        for (int e = tid; e < DF * DH; e += NT) sH[e] = rec[e];
+        if (tid < DF) sz[tid] = rec[DF * DH + tid];
+    }
+    float tmax = kMinShift;
+    for (int m = 0; m < p.M; ++m) tmax = fmaxf(tmax, a.sinks[h * p.M + m]);
+    __syncthreads();
+
+    const int r = tid >> 3, cs = tid & 7;
+    const T* q = (const T*)a.q;
+    const T* kk = (const T*)a.k;
+    const T* vv = (const T*)a.v;
+    for (int64_t i0 = s0; i0 < s1; i0 += TS) {
+        const int n = (int)min64(TS, s1 - i0);
+        gates_cumsum<T, DF, FAST>((const T*)a.g, b, p.L, p.Hkv, kv, i0, n, sb);
+        // delayed stream: row t carries key/value i0 + t - w (absent before token w)
+        const int rlo = (int)min64(n, max64(0, p.w - i0));
+        load_rows<T, DH>(kk, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n, sq, PH);
+        load_rows<T, DH>(vv, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n, sv, DH);
+        __syncthreads();
+        phi_rows<DH, DF, FAST>(sq, sW, sphk, rlo, n);
+        __syncthreads();
+        load_rows<T, DH>(q, b, p.L, p.Hq, h, i0, 0, n, sq, PH);
+        __syncthreads();
+        phi_rows<DH, DF, FAST>(sq, sW, sphq, 0, n);
+        __syncthreads();
+        for (int e = tid; e < TS * DF; e += NT) {
+            const int t = e / DF, f = e % DF;
+            sR[t * PF + f] = sphq[t * PF + f] * ex<FAST>(sb[t * PF + f]);
+        }
+        __syncthreads();
+        // state readout: phi(q_i) e^{b_i} . [H | z]
+        float acc[NC], gden = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NC; ++j) acc[j] = 0.0f;
+        for (int f = 0; f < DF; ++f) {
+            const float qt = sR[r * PF + f];
+#pragma unroll
+            for (int j = 0; j < NC; ++j) acc[j] = fmaf(qt, sH[f * DH + cs + 8 * j], acc[j]);
+            gden = fmaf(qt, sz[f], gden);
+        }
+        // intra-sub-chunk state term: A_it = sum_f phq_if phk_tf e^{b_if - b_tf}, t <= i
+        for (int e = tid; e < TS * TS; e += NT) {
+            const int i = e / TS, t = e % TS;
+            float val = 0.0f;
+            if (t <= i && i < n && t >= rlo) {
+                const float* qi = sphq + i * PF;
+                const float* kt = sphk + t * PF;
+                const float* bi = sb + i * PF;
+                const float* bt = sb + t * PF;
+                for (int f = 0; f < DF; ++f) val = fmaf(qi[f] * kt[f], ex<FAST>(bi[f] - bt[f]), val);
+            }
+            sA[i * (TS + 1) + t] = val;
+        }
+        __syncthreads();
+        for (int t = 0; t < TS; ++t) {
+            const float at = sA[r * (TS + 1) + t];
+            gden += at;
+#pragma unroll
+            for (int j = 0; j < NC; ++j) acc[j] = fmaf(at, sv[t * DH + cs + 8 * j], acc[j]);
+        }
+        // window softmax over keys (i-w, i], online max, tiles of KT keys
+        float mrun = tmax, l = 0.0f, wacc[NC];
+#pragma unroll
+        for (int j = 0; j < NC; ++j) wacc[j] = 0.0f;
+        const int64_t i = i0 + r;
+        const int64_t jlo = max64(0, i0 - p.w + 1), jhi = i0 + n - 1;
+        float* sk = sR;
+        float* sv2 = sR + KT * PH;
+        for (int64_t j0 = jlo; j0 <= jhi; j0 += KT) {
+            __syncthreads();
+            for (int e = tid; e < KT * DH; e += NT) {
+                const int t = e / DH, c = e % DH;
+                const int64_t j = j0 + t;
+                float kx = 0.0f, vx = 0.0f;
+                if (j <= jhi) {
+                    kx = ld(kk + ((b * p.L + j) * p.Hkv + kv) * DH + c);
+                    vx = ld(vv + ((b * p.L + j) * p.Hkv + kv) * DH + c);
+                }
+                sk[t * PH + c] = kx;
+                sv2[t * DH + c] = vx;
+            }
+            __syncthreads();
+            float s[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const int kx = cs + 8 * u;
+                const int64_t j = j0 + kx;
+                const bool valid = (r < n) && (j <= i) && (j > i - p.w) && (j <= jhi);
+                float dot = 0.0f;
+                const float* qr = sq + r * PH;
+                const float* kr = sk + kx * PH;
+                for (int c = 0; c < DH; ++c) dot = fmaf(qr[c], kr[c], dot);
+                s[u] = valid ? dot * p.scale : -INFINITY;
+            }
+            float tm = fmaxf(s[0], s[1]);
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, o));
+            const float mnew = fmaxf(mrun, tm);
+            const float corr = ex<FAST>(mrun - mnew);
+            const float p0 = (s[0] == -INFINITY) ? 0.0f : ex<FAST>(s[0] - mnew);
+            const float p1 = (s[1] == -INFINITY) ? 0.0f : ex<FAST>(s[1] - mnew);
+            sP[r * KT + cs] = p0;
+            sP[r * KT + cs + 8] = p1;
+            float ps = p0 + p1;
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            l = l * corr + ps;
+#pragma unroll
+            for (int j = 0; j < NC; ++j) wacc[j] *= corr;
+            mrun = mnew;
+            __syncwarp();
+            for (int t = 0; t < KT; ++t) {
+                const float pk = sP[r * KT + t];
+#pragma unroll
+                for (int j = 0; j < NC; ++j) wacc[j] = fmaf(pk, sv2[t * DH + cs + 8 * j], wacc[j]);
+            }
+        }
+        // shared normaliser: y = (e^{-m} N_gla + N_win) / (e^{-m} D_gla + E_win + sum e^{t-m})
+        if (r < n) {
+            float ssum = 0.0f;
+            for (int m = 0; m < p.M; ++m) ssum += ex<FAST>(a.sinks[h * p.M + m] - mrun);
+            const float e = ex<FAST>(-mrun);
+            const float den = e * gden + l + ssum;
+            const float inv = 1.0f / den;
+            T* yr = (T*)a.y + ((b * p.L + i) * p.Hq + h) * DH;
+#pragma unroll
+            for (int j = 0; j < NC; ++j) st(yr + cs + 8 * j, (e * acc[j] + wacc[j]) * inv);
+            if (a.lse != nullptr && cs == 0) a.lse[(b * p.L + i) * p.Hq + h] = mrun + logf(den);
+        }
+        __syncthreads();
+        state_update<DH, DF, FAST>(sH, sz, sphk, sv, sb);
+    }
+    if (a.S_out != nullptr && s1 == p.L && (h % p.G) == 0) {
+        for (int e = tid; e < DF * DH; e += NT) a.S_out[unit * DF * DH + e] = sH[e];
+        if (tid < DF && a.z_out != nullptr) a.z_out[unit * DF + tid] = sz[tid];
+    }
+}
+
+template <typename T>
+__global__ void ring_fill_kernel(Plan p, const T* k, const T* v, T* kc, T* vc) {
+    const int64_t nt = min64(p.L, p.w);
+    const int64_t t = p.L - nt + blockIdx.x;
+    const int64_t unit = blockIdx.y, b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t slot = t % (p.w + 1);
+    for (int64_t c = threadIdx.x; c < p.d; c += blockDim.x) {
+        const int64_t src = ((b * p.L + t) * p.Hkv + kv) * p.d + c;
+        const int64_t dst = (unit * (p.w + 1) + slot) * p.d + c;
+        if (kc != nullptr) kc[dst] = k[src];
+        if (vc != nullptr) vc[dst] = v[src];
+    }
+}
+
+template <typename T, int DH, int DF, bool FAST>
+cudaError_t launch_impl(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+    using Ly = Lay<DH, DF>;
+    const size_t smem = Ly::bytes;
+    cudaError_t err;
+    err = cudaFuncSetAttribute(fwd_simt_main<T, DH, DF, FAST>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    err = cudaFuncSetAttribute(fwd_simt_seglocal<T, DH, DF, FAST>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    const unsigned U = (unsigned)(p.B * p.Hkv);
+    if (p.P > 1) {
+        fwd_simt_seglocal<T, DH, DF, FAST><<<dim3(U, (unsigned)(p.P - 1)), NT, smem, s>>>(p, a);
+        const unsigned nE = (unsigned)(p.D * p.d + p.D);
+        fwd_seg_scan<<<dim3((nE + 255) / 256, U), 256, 0, s>>>(p, a.seg);
+    }
+    if (a.ev_before) cudaEventRecord(a.ev_before, s);
+    fwd_simt_main<T, DH, DF, FAST>
+        <<<dim3((unsigned)(p.B * p.Hq), (unsigned)p.P), NT, smem, s>>>(p, a);
+    if (a.ev_after) cudaEventRecord(a.ev_after, s);
+    return cudaGetLastError();
+}
+
+template <typename T, bool FAST>
+cudaError_t dispatch_dims(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+    if (p.d == 128 && p.D == 128) return launch_impl<T, 128, 128, FAST>(p, a, s);
+    if (p.d == 128 && p.D == 64) return launch_impl<T, 128, 64, FAST>(p, a, s);
+    if (p.d == 64 && p.D == 128) return launch_impl<T, 64, 128, FAST>(p, a, s);
+    if (p.d == 64 && p.D == 64) return launch_impl<T, 64, 64, FAST>(p, a, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_simt(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+    if (p.dtype == LIZARD_F32) return dispatch_dims<float, false>(p, a, s);
+    return dispatch_dims<__nv_bfloat16, true>(p, a, s);
+}
+
+cudaError_t launch_ring_fill(const Plan& p, const void* k, const void* v, void* kc, void* vc,
+                             cudaStream_t s) {
+    const int64_t nt = p.L < p.w ? p.L : p.w;
+    if (nt <= 0) return cudaSuccess;
+    dim3 grid((unsigned)nt, (unsigned)(p.B * p.Hkv));
+    if (p.dtype == LIZARD_F32)
+        ring_fill_kernel<float><<<grid, 128, 0, s>>>(p, (const float*)k, (const float*)v,
+                                                     (float*)kc, (float*)vc);
+    else
+        ring_fill_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(
+            p, (const __nv_bfloat16*)k, (const __nv_bfloat16*)v, (__nv_bfloat16*)kc,
+            (__nv_bfloat16*)vc);
+    return cudaGetLastError();
+}
+
+}  // namespace lz

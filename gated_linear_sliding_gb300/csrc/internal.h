@@ -1,0 +1,75 @@
+// Internal host-side interface between the C-ABI entry points and the kernels.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "lizard.h"
+
+namespace lz {
+
+constexpr int kChunk = 64;            // GLA chunk (tokens); segments are whole chunks
+constexpr size_t kHeaderBytes = 256;  // device status word and padding
+constexpr int kTargetUnits = 304;     // 2 x 152 SMs: (batch, KV head, segment) CTAs wanted
+
+// Segment plan of a forward/backward call.  The sequence of each (batch, KV head)
+// unit is cut into P segments of seg_chunks chunks; the segment count never
+// exceeds Pmax, which depends on B and Hkv only, so the workspace does not grow
+// with L.
+struct Plan {
+    int64_t B, L, Hq, Hkv, d, D, w, M, G;
+    float scale;
+    int dtype;
+    int64_t nchunks, seg_chunks, seg_len, P, Pmax;
+    size_t rec_floats;   // floats per (segment, unit) record: D*d + D + D
+};
+
+bool make_plan(const lizard_dims* dims, Plan* p);
+size_t fwd_workspace_bytes(const Plan& p);
+
+struct FwdArgs {
+    const void *q, *k, *v, *g, *Wf;
+    const float* sinks;
+    void* y;
+    float* lse;
+    float *S_out, *z_out;
+    void *kcache_out, *vcache_out;
+    float* seg;   // (Pmax, B*Hkv, rec_floats) segment records
+    void* header;
+    cudaEvent_t ev_before, ev_after;  // optional: bracket the dominant kernel
+};
+
+cudaError_t launch_fwd_simt(const Plan& p, const FwdArgs& a, cudaStream_t s);
+bool fwd_tc_supported(const Plan& p);
+cudaError_t launch_fwd_tc(const Plan& p, const FwdArgs& a, cudaStream_t s);
+cudaError_t launch_ring_fill(const Plan& p, const void* k, const void* v, void* kc, void* vc,
+                             cudaStream_t s);
+
+struct DecodeArgs {
+    int64_t pos;
+    const void *q, *k, *v, *g, *Wf;
+    const float* sinks;
+    void* y;
+    float *S, *z;
+    void *kc, *vc;
+    void* header;
+};
+cudaError_t launch_decode(const Plan& p, const DecodeArgs& a, cudaStream_t s);
+
+struct BwdArgs {
+    const void *q, *k, *v, *g, *Wf;
+    const float* sinks;
+    const void* y;
+    const float* lse;
+    const void* dy;
+    void *dq, *dk, *dv, *dg;
+    float *dWf, *dsinks;
+    void* ws;
+    size_t ws_bytes;
+    cudaEvent_t ev_before, ev_after;
+};
+size_t bwd_workspace_bytes(const Plan& p);
+cudaError_t launch_bwd(const Plan& p, const BwdArgs& a, cudaStream_t s);
+
+}  // namespace lz

@@ -1,0 +1,267 @@
+// C-ABI entry points of the Lizard token-mixer library: argument validation,
+// segment planning, workspace sizes and kernel dispatch.  Every check runs on the
+// host before any launch; there is no CPU fallback.
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lz {
+
+bool make_plan(const lizard_dims* dims, Plan* p) {
+    if (dims == nullptr) return false;
+    const lizard_dims& d = *dims;
+    if (d.B < 1 || d.L < 1 || d.Hq < 1 || d.Hkv < 1 || d.Hq % d.Hkv != 0) return false;
+    if (d.w < 1 || d.M < 0 || d.M > 64) return false;
+    if (d.D < 2 || d.D % 2 != 0 || d.d < 1) return false;
+    if (!(d.chunk == 0 || d.chunk == kChunk)) return false;
+    if (!(d.dtype == LIZARD_F32 || d.dtype == LIZARD_BF16)) return false;
+    if (!(d.scale >= 0.0f) || !isfinite(d.scale)) return false;
+    p->B = d.B;
+    p->L = d.L;
+    p->Hq = d.Hq;
+    p->Hkv = d.Hkv;
+    p->d = d.d;
+    p->D = d.D;
+    p->w = d.w;
+    p->M = d.M;
+    p->G = d.Hq / d.Hkv;
+    p->scale = d.scale > 0.0f ? d.scale : 1.0f / sqrtf((float)d.d);
+    p->dtype = d.dtype;
+    const int64_t U = d.B * d.Hkv;
+    p->nchunks = (d.L + kChunk - 1) / kChunk;
+    int64_t pmax = (kTargetUnits + U - 1) / U;
+    if (pmax < 1) pmax = 1;
+    if (pmax > 64) pmax = 64;
+    p->Pmax = pmax;
+    p->seg_chunks = (p->nchunks + pmax - 1) / pmax;
+    p->seg_len = p->seg_chunks * kChunk;
+    p->P = (p->nchunks + p->seg_chunks - 1) / p->seg_chunks;
+    p->rec_floats = (size_t)(d.D * d.d + 2 * d.D);
+    return true;
+}
+
+static bool shapes_compiled(const Plan& p) {
+    return (p.d == 64 || p.d == 128) && (p.D == 64 || p.D == 128) && p.B * p.Hkv <= 65535 &&
+           p.B * p.Hq <= (int64_t)1 << 30;
+}
+
+size_t fwd_workspace_bytes(const Plan& p) {
+    return kHeaderBytes + sizeof(float) * (size_t)p.Pmax * (size_t)(p.B * p.Hkv) * p.rec_floats;
+}
+
+static bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+
+// 1 if the current device is sm_103, 0 if not, -1 if the query failed.
+static int device_ok() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    static int cache[64];  // 0 unknown, 1 ok, 2 not ok
+    if (dev >= 0 && dev < 64 && cache[dev] != 0) return cache[dev] == 1 ? 1 : 0;
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+        return -1;
+    const int ok = (major == 10 && minor == 3) ? 1 : 0;
+    if (dev >= 0 && dev < 64) cache[dev] = ok ? 1 : 2;
+    return ok;
+}
+
+static lizard_status device_status() {
+    const int ok = device_ok();
+    if (ok < 0) {
+        cudaGetLastError();
+        return LIZARD_ERR_CUDA;
+    }
+    return ok ? LIZARD_OK : LIZARD_ERR_UNSUPPORTED;
+}
+
+static cudaEvent_t g_ev_before = nullptr, g_ev_after = nullptr;
+
+static lizard_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA; }
+
+}  // namespace lz
+
+using namespace lz;
+
+extern "C" {
+
+size_t lizard_attn_fwd_workspace(const lizard_dims* dims) {
+    Plan p;
+    if (!make_plan(dims, &p)) return 0;
+    return fwd_workspace_bytes(p);
+}
+
+lizard_status lizard_workspace_init(void* workspace, size_t ws_bytes, void* stream) {
+    if (workspace == nullptr || !aligned16(workspace)) return LIZARD_ERR_INVALID_ARG;
+    if (ws_bytes < kHeaderBytes) return LIZARD_ERR_WORKSPACE;
+    return from_cuda(cudaMemsetAsync(workspace, 0, kHeaderBytes, (cudaStream_t)stream));
+}
+
+lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void* k,
+                              const void* v, const void* g, const void* Wf, const float* sinks,
+                              void* y, float* lse, float* S_out, float* z_out, void* kcache_out,
+                              void* vcache_out, void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    if (!make_plan(dims, &p)) return LIZARD_ERR_INVALID_ARG;
+    if (!q || !k || !v || !g || !Wf || !y || (p.M > 0 && !sinks)) return LIZARD_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, Wf, sinks, y, lse, S_out, z_out, kcache_out, vcache_out,
+                          workspace};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return LIZARD_ERR_INVALID_ARG;
+    if ((S_out == nullptr) != (z_out == nullptr)) return LIZARD_ERR_INVALID_ARG;
+    if ((kcache_out == nullptr) != (vcache_out == nullptr)) return LIZARD_ERR_INVALID_ARG;
+    if (!shapes_compiled(p)) return LIZARD_ERR_UNSUPPORTED;
+    if (workspace == nullptr || ws_bytes < fwd_workspace_bytes(p)) return LIZARD_ERR_WORKSPACE;
+    lizard_status st = device_status();
+    if (st != LIZARD_OK) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    FwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.Wf = Wf;
+    a.sinks = sinks;
+    a.y = y;
+    a.lse = lse;
+    a.S_out = S_out;
+    a.z_out = z_out;
+    a.kcache_out = kcache_out;
+    a.vcache_out = vcache_out;
+    a.header = workspace;
+    a.seg = (float*)((char*)workspace + kHeaderBytes);
+    a.ev_before = g_ev_before;
+    a.ev_after = g_ev_after;
+    cudaError_t e = fwd_tc_supported(p) ? launch_fwd_tc(p, a, s) : launch_fwd_simt(p, a, s);
+    if (e == cudaSuccess && kcache_out != nullptr)
+        e = launch_ring_fill(p, k, v, kcache_out, vcache_out, s);
+    return from_cuda(e);
+}
+
+size_t lizard_attn_bwd_workspace(const lizard_dims* dims) {
+    Plan p;
+    if (!make_plan(dims, &p)) return 0;
+    return bwd_workspace_bytes(p);
+}
+
+lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* q, const void* k,
+                              const void* v, const void* g, const void* Wf, const float* sinks,
+                              const void* y, const float* lse, const void* dy, void* dq, void* dk,
+                              void* dv, void* dg, float* dWf, float* dsinks, void* workspace,
+                              size_t ws_bytes, void* stream) {
+    Plan p;
+    if (!make_plan(dims, &p)) return LIZARD_ERR_INVALID_ARG;
+    const void* req[] = {q, k, v, g, Wf, y, lse, dy, dq, dk, dv, dg, dWf};
+    for (const void* ptr : req)
+        if (ptr == nullptr || !aligned16(ptr)) return LIZARD_ERR_INVALID_ARG;
+    if (p.M > 0 && (!sinks || !dsinks || !aligned16(sinks) || !aligned16(dsinks)))
+        return LIZARD_ERR_INVALID_ARG;
+    if (!shapes_compiled(p)) return LIZARD_ERR_UNSUPPORTED;
+    if (workspace == nullptr || !aligned16(workspace) || ws_bytes < bwd_workspace_bytes(p))
+        return LIZARD_ERR_WORKSPACE;
+    lizard_status st = device_status();
+    if (st != LIZARD_OK) return st;
+    BwdArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.Wf = Wf;
+    a.sinks = sinks;
+    a.y = y;
+    a.lse = lse;
+    a.dy = dy;
+    a.dq = dq;
+    a.dk = dk;
+    a.dv = dv;
+    a.dg = dg;
+    a.dWf = dWf;
+    a.dsinks = dsinks;
+    a.ws = workspace;
+    a.ws_bytes = ws_bytes;
+    a.ev_before = g_ev_before;
+    a.ev_after = g_ev_after;
+    return from_cuda(launch_bwd(p, a, (cudaStream_t)stream));
+}
+
+size_t lizard_decode_workspace(const lizard_dims* dims) {
+    lizard_dims d1 = dims ? *dims : lizard_dims{};
+    d1.L = 1;
+    Plan p;
+    if (!make_plan(&d1, &p)) return 0;
+    return kHeaderBytes;
+}
+
+lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const void* q,
+                                 const void* k, const void* v, const void* g, const void* Wf,
+                                 const float* sinks, void* y, float* S, float* z, void* kcache,
+                                 void* vcache, void* workspace, size_t ws_bytes, void* stream) {
+    if (dims == nullptr) return LIZARD_ERR_INVALID_ARG;
+    lizard_dims d1 = *dims;
+    d1.L = 1;
+    Plan p;
+    if (!make_plan(&d1, &p) || pos < 0) return LIZARD_ERR_INVALID_ARG;
+    const void* req[] = {q, k, v, g, Wf, y, S, z, kcache, vcache};
+    for (const void* ptr : req)
+        if (ptr == nullptr || !aligned16(ptr)) return LIZARD_ERR_INVALID_ARG;
+    if (p.M > 0 && (!sinks || !aligned16(sinks))) return LIZARD_ERR_INVALID_ARG;
+    if (!shapes_compiled(p) || p.G > 8 || p.w > 256) return LIZARD_ERR_UNSUPPORTED;
+    if (workspace == nullptr || !aligned16(workspace) || ws_bytes < kHeaderBytes)
+        return LIZARD_ERR_WORKSPACE;
+    lizard_status st = device_status();
+    if (st != LIZARD_OK) return st;
+    DecodeArgs a;
+    a.pos = pos;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.g = g;
+    a.Wf = Wf;
+    a.sinks = sinks;
+    a.y = y;
+    a.S = S;
+    a.z = z;
+    a.kc = kcache;
+    a.vc = vcache;
+    a.header = workspace;
+    return from_cuda(launch_decode(p, a, (cudaStream_t)stream));
+}
+
+lizard_status lizard_read_device_status(void* workspace, void* stream) {
+    if (workspace == nullptr || !aligned16(workspace)) return LIZARD_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return LIZARD_ERR_CUDA;
+    unsigned int word = 0;
+    if (cudaMemcpy(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    if (word != 0 && cudaMemset(workspace, 0, kHeaderBytes) != cudaSuccess)
+        return LIZARD_ERR_CUDA;
+    if (word > (unsigned)LIZARD_ERR_TIMEOUT) return LIZARD_ERR_CUDA;
+    return (lizard_status)word;
+}
+
+const char* lizard_status_string(lizard_status s) {
+    switch (s) {
+        case LIZARD_OK: return "ok";
+        case LIZARD_ERR_INVALID_ARG: return "invalid argument";
+        case LIZARD_ERR_UNSUPPORTED: return "unsupported sizes or device";
+        case LIZARD_ERR_WORKSPACE: return "workspace missing or too small";
+        case LIZARD_ERR_CUDA: return "CUDA error";
+        case LIZARD_ERR_TIMEOUT: return "device-side wait timed out";
+    }
+    return "unknown status";
+}
+
+lizard_status lizard_profile_events(void* before, void* after) {
+    if ((before == nullptr) != (after == nullptr)) return LIZARD_ERR_INVALID_ARG;
+    g_ev_before = (cudaEvent_t)before;
+    g_ev_after = (cudaEvent_t)after;
+    return LIZARD_OK;
+}
+
+const char* lizard_version(void) { return "lizard-gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

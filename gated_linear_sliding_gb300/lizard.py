@@ -1,0 +1,267 @@
+"""Python binding of liblizard.so: argument marshalling only.
+
+Every function here checks tensor shapes, dtypes and contiguity, then calls the
+C entry point of the same name with raw device pointers and the current CUDA
+stream.  All arithmetic runs in the library's CUDA kernels; there is no CPU
+path.  If the library has not been built, loading it raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+LIZARD_OK = 0
+LIZARD_ERR_INVALID_ARG = 1
+LIZARD_ERR_UNSUPPORTED = 2
+LIZARD_ERR_WORKSPACE = 3
+LIZARD_ERR_CUDA = 4
+LIZARD_ERR_TIMEOUT = 5
+LIZARD_F32 = 0
+LIZARD_BF16 = 1
+
+EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_fwd",
+            "lizard_attn_bwd_workspace", "lizard_attn_bwd", "lizard_decode_workspace",
+            "lizard_decode_step", "lizard_read_device_status", "lizard_status_string",
+            "lizard_profile_events", "lizard_version"]
+
+
+class lizard_dims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("L", ctypes.c_int64), ("Hq", ctypes.c_int64),
+                ("Hkv", ctypes.c_int64), ("d", ctypes.c_int64), ("D", ctypes.c_int64),
+                ("w", ctypes.c_int64), ("M", ctypes.c_int64), ("chunk", ctypes.c_int64),
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+
+
+class LizardError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+_lib = None
+_VP = ctypes.c_void_p
+_DP = ctypes.POINTER(lizard_dims)
+
+
+def load(path: str | None = None) -> ctypes.CDLL:
+    """Load liblizard.so; raises if it is missing (build it with __graft_entry__.build())."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: the CUDA library must be built first "
+                           "(python -c 'import __graft_entry__ as g; g.build()')")
+    lib = ctypes.CDLL(path)
+    lib.lizard_attn_fwd_workspace.argtypes = [_DP]
+    lib.lizard_attn_fwd_workspace.restype = ctypes.c_size_t
+    lib.lizard_attn_bwd_workspace.argtypes = [_DP]
+    lib.lizard_attn_bwd_workspace.restype = ctypes.c_size_t
+    lib.lizard_decode_workspace.argtypes = [_DP]
+    lib.lizard_decode_workspace.restype = ctypes.c_size_t
+    lib.lizard_workspace_init.argtypes = [_VP, ctypes.c_size_t, _VP]
+    lib.lizard_workspace_init.restype = ctypes.c_int
+    lib.lizard_attn_fwd.argtypes = [_DP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
+    lib.lizard_attn_fwd.restype = ctypes.c_int
+    lib.lizard_attn_bwd.argtypes = [_DP] + [_VP] * 16 + [ctypes.c_size_t, _VP]
+    lib.lizard_attn_bwd.restype = ctypes.c_int
+    lib.lizard_decode_step.argtypes = [_DP, ctypes.c_int64] + [_VP] * 12 + [ctypes.c_size_t, _VP]
+    lib.lizard_decode_step.restype = ctypes.c_int
+    lib.lizard_read_device_status.argtypes = [_VP, _VP]
+    lib.lizard_read_device_status.restype = ctypes.c_int
+    lib.lizard_status_string.argtypes = [ctypes.c_int]
+    lib.lizard_status_string.restype = ctypes.c_char_p
+    lib.lizard_profile_events.argtypes = [_VP, _VP]
+    lib.lizard_profile_events.restype = ctypes.c_int
+    lib.lizard_version.argtypes = []
+    lib.lizard_version.restype = ctypes.c_char_p
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().lizard_status_string(status).decode()
+
+
+def lizard_version() -> str:
+    return load().lizard_version().decode()
+
+
+def _check(status: int, where: str):
+    if status != LIZARD_OK:
+        raise LizardError(status, where)
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return LIZARD_F32
+    if t.dtype == torch.bfloat16:
+        return LIZARD_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def make_dims(B, L, Hq, Hkv, d, D, w, M, dtype, scale: float = 0.0, chunk: int = 0) -> lizard_dims:
+    code = dtype if isinstance(dtype, int) else _dtype_code(torch.empty(0, dtype=dtype))
+    return lizard_dims(B, L, Hq, Hkv, d, D, w, M, chunk, float(scale), code)
+
+
+def dims_of(q, k, g, sinks, w: int, scale: float = 0.0) -> lizard_dims:
+    B, L, Hq, d = q.shape
+    Hkv = k.shape[2]
+    D = g.shape[-1]
+    M = sinks.shape[1]
+    return lizard_dims(B, L, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+
+
+def _need(t, name, shape, dtype):
+    if t is None:
+        raise ValueError(f"{name} is required")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name}: shape {tuple(t.shape)} != {tuple(shape)}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name}: dtype {t.dtype} != {dtype}")
+    if not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name} must be a contiguous CUDA tensor")
+
+
+def lizard_attn_fwd_workspace(dims: lizard_dims) -> int:
+    return int(load().lizard_attn_fwd_workspace(ctypes.byref(dims)))
+
+
+def lizard_attn_bwd_workspace(dims: lizard_dims) -> int:
+    return int(load().lizard_attn_bwd_workspace(ctypes.byref(dims)))
+
+
+def lizard_decode_workspace(dims: lizard_dims) -> int:
+    return int(load().lizard_decode_workspace(ctypes.byref(dims)))
+
+
+def new_workspace(nbytes: int, device, stream=None) -> torch.Tensor:
+    """Allocate a workspace (torch owns the memory) and zero its status word."""
+    ws = torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+    _check(load().lizard_workspace_init(_p(ws), ws.numel(), _stream(stream)),
+           "lizard_workspace_init")
+    return ws
+
+
+def lizard_profile_events(before=None, after=None):
+    """Bracket the dominant kernel of later forward/backward calls with two
+    torch.cuda.Event objects (None, None turns it off)."""
+    handles = []
+    for ev in (before, after):
+        if ev is None:
+            handles.append(None)
+            continue
+        if not ev.cuda_event:
+            ev.record()  # torch creates the underlying cudaEvent_t on first record
+        handles.append(ctypes.c_void_p(ev.cuda_event))
+    _check(load().lizard_profile_events(*handles), "lizard_profile_events")
+
+
+def lizard_read_device_status(workspace: torch.Tensor, stream=None) -> int:
+    return int(load().lizard_read_device_status(_p(workspace), _stream(stream)))
+
+
+def lizard_attn_fwd(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0, y=None, lse=None,
+                    S_out=None, z_out=None, kcache_out=None, vcache_out=None, workspace=None,
+                    stream=None):
+    """Forward over L tokens.  Returns y [B, L, Hq, d] (allocated if not given)."""
+    B, L, Hq, d = q.shape
+    Hkv, D, M = k.shape[2], g.shape[-1], sinks.shape[1]
+    dt = q.dtype
+    _need(q, "q", (B, L, Hq, d), dt)
+    _need(k, "k", (B, L, Hkv, d), dt)
+    _need(v, "v", (B, L, Hkv, d), dt)
+    _need(g, "g", (B, L, Hkv, D), dt)
+    _need(Wf, "Wf", (Hkv, d, D // 2), dt)
+    _need(sinks, "sinks", (Hq, M), torch.float32)
+    if y is None:
+        y = torch.empty_like(q)
+    _need(y, "y", (B, L, Hq, d), dt)
+    if lse is not None:
+        _need(lse, "lse", (B, L, Hq), torch.float32)
+    if S_out is not None:
+        _need(S_out, "S_out", (B, Hkv, D, d), torch.float32)
+        _need(z_out, "z_out", (B, Hkv, D), torch.float32)
+    if kcache_out is not None:
+        _need(kcache_out, "kcache_out", (B, Hkv, w + 1, d), dt)
+        _need(vcache_out, "vcache_out", (B, Hkv, w + 1, d), dt)
+    dims = dims_of(q, k, g, sinks, w, scale)
+    if workspace is None:
+        workspace = new_workspace(lizard_attn_fwd_workspace(dims), q.device, stream)
+    st = load().lizard_attn_fwd(ctypes.byref(dims), _p(q), _p(k), _p(v), _p(g), _p(Wf),
+                                _p(sinks), _p(y), _p(lse), _p(S_out), _p(z_out), _p(kcache_out),
+                                _p(vcache_out), _p(workspace), workspace.numel(),
+                                _stream(stream))
+    _check(st, "lizard_attn_fwd")
+    return y
+
+
+def lizard_attn_bwd(q, k, v, g, Wf, sinks, y, lse, dy, w: int, *, scale: float = 0.0,
+                    dq=None, dk=None, dv=None, dg=None, dWf=None, dsinks=None, workspace=None,
+                    stream=None):
+    """Gradients (dq, dk, dv, dg, dWf, dsinks) of y against dy."""
+    B, L, Hq, d = q.shape
+    Hkv, D, M = k.shape[2], g.shape[-1], sinks.shape[1]
+    dt = q.dtype
+    for t, n, shp in ((q, "q", (B, L, Hq, d)), (k, "k", (B, L, Hkv, d)), (v, "v", (B, L, Hkv, d)),
+                      (g, "g", (B, L, Hkv, D)), (Wf, "Wf", (Hkv, d, D // 2)),
+                      (y, "y", (B, L, Hq, d)), (dy, "dy", (B, L, Hq, d))):
+        _need(t, n, shp, dt)
+    _need(sinks, "sinks", (Hq, M), torch.float32)
+    _need(lse, "lse", (B, L, Hq), torch.float32)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    dg = torch.empty_like(g) if dg is None else dg
+    dWf = torch.empty(Hkv, d, D // 2, dtype=torch.float32, device=q.device) if dWf is None else dWf
+    dsinks = torch.empty(Hq, M, dtype=torch.float32, device=q.device) if dsinks is None else dsinks
+    dims = dims_of(q, k, g, sinks, w, scale)
+    if workspace is None:
+        workspace = new_workspace(lizard_attn_bwd_workspace(dims), q.device, stream)
+    st = load().lizard_attn_bwd(ctypes.byref(dims), _p(q), _p(k), _p(v), _p(g), _p(Wf),
+                                _p(sinks), _p(y), _p(lse), _p(dy), _p(dq), _p(dk), _p(dv),
+                                _p(dg), _p(dWf), _p(dsinks), _p(workspace), workspace.numel(),
+                                _stream(stream))
+    _check(st, "lizard_attn_bwd")
+    return dict(dq=dq, dk=dk, dv=dv, dg=dg, dWf=dWf, dsinks=dsinks)
+
+
+def lizard_decode_step(pos: int, q, k, v, g, Wf, sinks, S, z, kcache, vcache, w: int, *,
+                       scale: float = 0.0, y=None, workspace=None, stream=None):
+    """One decode step at position pos; S, z, kcache, vcache are updated in place."""
+    B, Hq, d = q.shape
+    Hkv, D, M = k.shape[1], g.shape[-1], sinks.shape[1]
+    dt = q.dtype
+    _need(k, "k", (B, Hkv, d), dt)
+    _need(v, "v", (B, Hkv, d), dt)
+    _need(g, "g", (B, Hkv, D), dt)
+    _need(Wf, "Wf", (Hkv, d, D // 2), dt)
+    _need(sinks, "sinks", (Hq, M), torch.float32)
+    _need(S, "S", (B, Hkv, D, d), torch.float32)
+    _need(z, "z", (B, Hkv, D), torch.float32)
+    _need(kcache, "kcache", (B, Hkv, w + 1, d), dt)
+    _need(vcache, "vcache", (B, Hkv, w + 1, d), dt)
+    y = torch.empty_like(q) if y is None else y
+    dims = lizard_dims(B, 1, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    if workspace is None:
+        workspace = new_workspace(lizard_decode_workspace(dims), q.device, stream)
+    st = load().lizard_decode_step(ctypes.byref(dims), int(pos), _p(q), _p(k), _p(v), _p(g),
+                                   _p(Wf), _p(sinks), _p(y), _p(S), _p(z), _p(kcache),
+                                   _p(vcache), _p(workspace), workspace.numel(), _stream(stream))
+    _check(st, "lizard_decode_step")
+    return y

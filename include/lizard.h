@@ -1,0 +1,152 @@
+/*
+ * lizard.h - C ABI of the GB300 (sm_103a) Lizard hybrid token mixer.
+ *
+ * The mixer (Lizard summary, gist.science/ko/paper/2507.09025):
+ *   sec. 2-A-1  gated linear attention: a data-dependent gate
+ *               Gamma_i = sigmoid(g_i) (per token, per feature) decays a
+ *               constant-size state S_i updated token by token;
+ *   sec. 2-A-2  sliding-window softmax attention whose denominator also holds
+ *               learnable meta-memory scalars t_m ("sinks");
+ *   sec. 2-C    the non-negative Hedgehog feature map
+ *               phi(x) = [softmax(x Wf), softmax(-x Wf)], which lets the gates
+ *               move to log space and fold into the query/key sides.
+ * Both parts share one normaliser:
+ *   y_i = [phi(q_i) S_i + sum_{j in (i-w, i]} e^{s q_i.k_j} v_j]
+ *       / [phi(q_i).z_i + sum_{j in (i-w, i]} e^{s q_i.k_j} + sum_m e^{t_m}],
+ *   S_i = Gamma_i (.) S_{i-1} + [i >= w] phi(k_{i-w}) v_{i-w}^T,
+ *   z_i = Gamma_i (.) z_{i-1} + [i >= w] phi(k_{i-w}),
+ * i.e. a key enters the state, undecayed, at the step it leaves the window and
+ * is decayed by every later gate.  Query head h uses KV head h / (Hq / Hkv),
+ * which owns Wf, the gate logits, S and z.
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers to contiguous row-major arrays,
+ *     16-byte aligned.  The caller allocates and owns every buffer, workspace
+ *     included.  The library never allocates, frees or synchronises (except
+ *     lizard_read_device_status) and enqueues all work on `stream` (a
+ *     cudaStream_t; NULL = legacy default stream).
+ *   - Arguments are validated on the host before any launch; on any error the
+ *     call returns a status and launches nothing.
+ *   - Element type `dtype` (LIZARD_F32 or LIZARD_BF16) applies to q, k, v, g,
+ *     Wf, y, the ring caches and the gradients dq, dk, dv, dg.  sinks, S, z,
+ *     lse, dWf and dsinks are always fp32.
+ *   - Positions are 0-based.  There is no CPU fallback: on a device other than
+ *     sm_103 every call returns LIZARD_ERR_UNSUPPORTED.
+ *
+ * Layouts:
+ *   q, y, dy, dq  [B, L, Hq, d]        k, v, dk, dv  [B, L, Hkv, d]
+ *   g, dg         [B, L, Hkv, D]       Wf, dWf       [Hkv, d, D/2]
+ *   sinks, dsinks [Hq, M] (fp32)       lse           [B, L, Hq] (fp32)
+ *   S             [B, Hkv, D, d] fp32  z             [B, Hkv, D] fp32
+ *   kcache/vcache [B, Hkv, w+1, d]     token t lives in slot t mod (w+1)
+ */
+#ifndef LIZARD_H
+#define LIZARD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LIZARD_OK = 0,
+    LIZARD_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, inconsistent sizes      */
+    LIZARD_ERR_UNSUPPORTED = 2,  /* sizes outside the compiled kernels, or not sm_103 */
+    LIZARD_ERR_WORKSPACE = 3,    /* workspace NULL or smaller than the query says     */
+    LIZARD_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed               */
+    LIZARD_ERR_TIMEOUT = 5       /* a bounded device-side wait gave up (device status) */
+} lizard_status;
+
+typedef enum { LIZARD_F32 = 0, LIZARD_BF16 = 1 } lizard_dtype;
+
+/* Problem sizes.  d, D in {64, 128}; D is the phi width (Wf is d x D/2);
+ * Hq % Hkv == 0; w >= 1 (window of the w most recent tokens, self included);
+ * 0 <= M <= 64 sinks per query head; chunk is 0 (default) or 64;
+ * scale is the softmax scale applied to q.k, 0 selects 1/sqrt(d). */
+typedef struct {
+    int64_t B, L, Hq, Hkv, d, D, w, M;
+    int64_t chunk;
+    float scale;
+    int32_t dtype; /* lizard_dtype */
+} lizard_dims;
+
+/* Bytes of device workspace lizard_attn_fwd needs.  It depends on B, Hkv, d and
+ * D only, never on L (the per-segment boundary states, sec. 2-A-1 constant
+ * memory).  Returns 0 for invalid dims. */
+size_t lizard_attn_fwd_workspace(const lizard_dims* dims);
+
+/* Zero the device status word at the head of a workspace (async on stream).
+ * Call once after allocating a workspace; kernels only ever set the word. */
+lizard_status lizard_workspace_init(void* workspace, size_t ws_bytes, void* stream);
+
+/* Prefill / training forward over L tokens (sec. 2-A-1, 2-A-2, 2-C).
+ *   q, k, v, g, Wf, sinks   inputs as laid out above (read only);
+ *   y                       output [B, L, Hq, d];
+ *   lse                     optional (NULL to skip) [B, L, Hq] fp32: natural log
+ *                           of each row's full denominator, kept for the backward;
+ *   S_out, z_out            optional final state after token L-1 (decode hand-off);
+ *   kcache_out, vcache_out  optional ring caches: the last min(L, w) tokens are
+ *                           written to slot t mod (w+1), other slots untouched;
+ *   workspace, ws_bytes     >= lizard_attn_fwd_workspace(dims) bytes. */
+lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void* k,
+                              const void* v, const void* g, const void* Wf, const float* sinks,
+                              void* y, float* lse, float* S_out, float* z_out, void* kcache_out,
+                              void* vcache_out, void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace lizard_attn_bwd needs (independent of L). */
+size_t lizard_attn_bwd_workspace(const lizard_dims* dims);
+
+/* Exact gradient of lizard_attn_fwd's y against an upstream gradient dy.  The
+ * pages give no backward; this is the adjoint of the forward definition.
+ *   y, lse        the forward's y and lse for the same inputs;
+ *   dq, dk, dv, dg outputs in dtype; dWf [Hkv, d, D/2] and dsinks [Hq, M] fp32;
+ *   every output is overwritten.  Reductions use a fixed order (deterministic). */
+lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* q, const void* k,
+                              const void* v, const void* g, const void* Wf, const float* sinks,
+                              const void* y, const float* lse, const void* dy, void* dq, void* dk,
+                              void* dv, void* dg, float* dWf, float* dsinks, void* workspace,
+                              size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace lizard_decode_step needs (the status word only). */
+size_t lizard_decode_workspace(const lizard_dims* dims);
+
+/* One constant-memory generation step for every sequence of the batch
+ * (sec. 2-A-1: the state is updated incrementally, no growing KV cache;
+ * sec. 4: generation at 32K keeps constant memory).
+ *   dims.L is ignored; pos is the 0-based position of the new token (the same
+ *   for the whole batch);
+ *   q [B, Hq, d], k, v [B, Hkv, d], g [B, Hkv, D]: the new token;
+ *   S, z: the state after token pos-1, updated IN PLACE to the state after pos
+ *   (decay by Gamma_pos, then admit token pos-w read from the ring);
+ *   kcache, vcache: ring caches holding tokens pos-w .. pos-1; the new k, v are
+ *   written to slot pos mod (w+1) IN PLACE;
+ *   y [B, Hq, d]: the output of token pos. */
+lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const void* q,
+                                 const void* k, const void* v, const void* g, const void* Wf,
+                                 const float* sinks, void* y, float* S, float* z, void* kcache,
+                                 void* vcache, void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, read the device status word of `workspace` and clear it.
+ * Returns LIZARD_OK or the first error a kernel recorded (e.g. LIZARD_ERR_TIMEOUT). */
+lizard_status lizard_read_device_status(void* workspace, void* stream);
+
+/* Static description of a status code. */
+const char* lizard_status_string(lizard_status s);
+
+/* Measurement hook.  While set (non-NULL cudaEvent_t handles), every later
+ * lizard_attn_fwd / lizard_attn_bwd call records `before` on its stream right
+ * before its dominant kernel (the chunk walk) and `after` right after it, so a
+ * caller can time that kernel alone with cudaEventElapsedTime.  NULL, NULL turns
+ * it off.  Process-wide; not for concurrent use from several threads. */
+lizard_status lizard_profile_events(void* before, void* after);
+
+/* Library version string. */
+const char* lizard_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIZARD_H */

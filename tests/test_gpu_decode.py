@@ -1,0 +1,117 @@
+"""Decode parity: lizard_decode_step (through the C ABI) against the float64 oracle.
+
+Sec. 2-A-1 of the Lizard summary (gist.science 2507.09025): generation updates a
+constant-size state token by token.  Each step must reproduce, token by token, the
+output of a prefill over the whole sequence.
+"""
+import numpy as np
+import pytest
+
+from gated_linear_sliding_gb300 import inputs as I
+from helpers import assert_parity, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def lz():
+    from gated_linear_sliding_gb300 import lizard
+
+    lizard.load()
+    return lizard
+
+
+def decode_all(lz, t, wl, pos0, npos, S, z, kc, vc):
+    ys = []
+    dims = lz.make_dims(wl.B, 1, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, t["q"].dtype)
+    ws = lz.new_workspace(lz.lizard_decode_workspace(dims), "cuda")
+    for pos in range(pos0, pos0 + npos):
+        y = lz.lizard_decode_step(pos, t["q"][:, pos].contiguous(), t["k"][:, pos].contiguous(),
+                                  t["v"][:, pos].contiguous(), t["g"][:, pos].contiguous(),
+                                  t["Wf"], t["sinks"], S, z, kc, vc, wl.w, workspace=ws)
+        ys.append(y)
+    torch.cuda.synchronize()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    return to_np(torch.stack(ys, 1))
+
+
+@pytest.mark.parametrize("dtype,d,D,G,w", [("f32", 64, 64, 2, 8), ("f32", 128, 128, 4, 5),
+                                           ("bf16", 128, 128, 4, 64), ("bf16", 64, 128, 8, 3)])
+def test_decode_from_scratch(lz, oracle_mod, dtype, d, D, G, w):
+    wl = I.TINY_F32.replace(dtype=dtype, B=3, L=150, d=d, D=D, Hkv=2, Hq=2 * G, w=w)
+    inp = I.make_inputs(wl)
+    ref = oracle_mod.fwd(**inp, w=wl.w)["y"]
+    t = to_dev(inp, dtype)
+    tdt = t["q"].dtype
+    S = torch.zeros(wl.B, wl.Hkv, D, d, dtype=torch.float32, device="cuda")
+    z = torch.zeros(wl.B, wl.Hkv, D, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(wl.B, wl.Hkv, w + 1, d, dtype=tdt, device="cuda")
+    vc = torch.zeros_like(kc)
+    y = decode_all(lz, t, wl, 0, wl.L, S, z, kc, vc)
+    assert_parity(y, ref, dtype, "decode y")
+    fin = oracle_mod.fwd(**inp, w=wl.w, state=True)
+    assert_parity(to_np(S), fin["S"], dtype, "S")
+    assert_parity(to_np(z), fin["z"], dtype, "z")
+
+
+def test_prefill_then_decode_matches_longer_prefill(lz, oracle_mod):
+    """The forward hands off (S, z, ring caches); decode continues; the result equals the
+    oracle prefill of the whole sequence, token by token."""
+    wl = I.DECODE_B64.replace(B=4)
+    L0, steps = 2048, 96
+    inp = I.make_inputs(wl.replace(L=L0 + steps))
+    ref = oracle_mod.fwd(**inp, w=wl.w)["y"]
+    t = to_dev(inp, wl.dtype)
+    tdt = t["q"].dtype
+    S = torch.empty(wl.B, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.empty(wl.B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(wl.B, wl.Hkv, wl.w + 1, wl.d, dtype=tdt, device="cuda")
+    vc = torch.zeros_like(kc)
+    pre = {n: (a[:, :L0].contiguous() if n in ("q", "k", "v", "g") else a) for n, a in t.items()}
+    lz.lizard_attn_fwd(pre["q"], pre["k"], pre["v"], pre["g"], pre["Wf"], pre["sinks"], wl.w,
+                       S_out=S, z_out=z, kcache_out=kc, vcache_out=vc)
+    y = decode_all(lz, t, wl, L0, steps, S, z, kc, vc)
+    assert_parity(y, ref[:, L0:], wl.dtype, "decode after prefill")
+
+
+def test_decode_gla_sensitive(lz, oracle_mod):
+    wl = I.gla_sensitive(I.DECODE_B64.replace(B=2))
+    L0, steps = 1024, 64
+    inp = I.make_inputs(wl.replace(L=L0 + steps))
+    ref = oracle_mod.fwd(**inp, w=wl.w, scale=wl.scale)["y"]
+    t = to_dev(inp, wl.dtype)
+    S = torch.empty(wl.B, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.empty(wl.B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(wl.B, wl.Hkv, wl.w + 1, wl.d, dtype=t["q"].dtype, device="cuda")
+    vc = torch.zeros_like(kc)
+    pre = {n: (a[:, :L0].contiguous() if n in ("q", "k", "v", "g") else a) for n, a in t.items()}
+    lz.lizard_attn_fwd(pre["q"], pre["k"], pre["v"], pre["g"], pre["Wf"], pre["sinks"], wl.w,
+                       S_out=S, z_out=z, kcache_out=kc, vcache_out=vc)
+    y = decode_all(lz, t, wl, L0, steps, S, z, kc, vc)
+    assert_parity(y, ref[:, L0:], wl.dtype, "decode gla-sensitive")
+
+
+def test_decode_state_checkpoint_resume(lz):
+    """The decode state (S, z, caches, pos) is the whole memory: copying it out and back
+    in, then continuing, reproduces the uninterrupted run bit for bit."""
+    wl = I.DECODE_B64.replace(B=2)
+    inp = I.make_inputs(wl.replace(L=80))
+    t = to_dev(inp, wl.dtype)
+    tdt = t["q"].dtype
+
+    def fresh():
+        return (torch.zeros(wl.B, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda"),
+                torch.zeros(wl.B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda"),
+                torch.zeros(wl.B, wl.Hkv, wl.w + 1, wl.d, dtype=tdt, device="cuda"),
+                torch.zeros(wl.B, wl.Hkv, wl.w + 1, wl.d, dtype=tdt, device="cuda"))
+
+    st = fresh()
+    y_all = decode_all(lz, t, wl, 0, 80, *st)
+    st = fresh()
+    decode_all(lz, t, wl, 0, 50, *st)
+    saved = [x.cpu() for x in st]
+    st2 = [x.to("cuda") for x in saved]
+    y_tail = decode_all(lz, t, wl, 50, 30, *st2)
+    np.testing.assert_array_equal(y_tail, y_all[:, 50:])

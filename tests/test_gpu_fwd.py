@@ -1,0 +1,170 @@
+"""Forward parity: lizard_attn_fwd (through the C ABI) against the float64 oracle.
+
+The oracle is the token recurrence of the Lizard summary (gist.science 2507.09025,
+sec. 2-A-1 and 2-A-2, shared normaliser); inputs come from the seeded generators.
+"""
+import numpy as np
+import pytest
+
+from gated_linear_sliding_gb300 import inputs as I
+from helpers import assert_parity, rel_l2, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def lz():
+    from gated_linear_sliding_gb300 import lizard
+
+    lizard.load()
+    return lizard
+
+
+def gpu_fwd(lz, inp, wl, scale=0.0, state=False, cache=False, lse=False):
+    t = to_dev(inp, wl.dtype)
+    B, L, Hq, d = inp["q"].shape
+    Hkv, D = wl.Hkv, wl.D
+    kw = {}
+    if lse:
+        kw["lse"] = torch.empty(B, L, Hq, dtype=torch.float32, device="cuda")
+    if state:
+        kw["S_out"] = torch.empty(B, Hkv, D, d, dtype=torch.float32, device="cuda")
+        kw["z_out"] = torch.empty(B, Hkv, D, dtype=torch.float32, device="cuda")
+    if cache:
+        kw["kcache_out"] = torch.zeros(B, Hkv, wl.w + 1, d, dtype=t["q"].dtype, device="cuda")
+        kw["vcache_out"] = torch.zeros(B, Hkv, wl.w + 1, d, dtype=t["q"].dtype, device="cuda")
+    y = lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w,
+                           scale=scale, **kw)
+    torch.cuda.synchronize()
+    out = {"y": to_np(y)}
+    for n, v in kw.items():
+        out[n] = to_np(v)
+    return out
+
+
+def oracle_fwd(oracle_mod, inp, wl, **kw):
+    return oracle_mod.fwd(**inp, w=wl.w, scale=wl.scale, **kw)
+
+
+def test_tiny_f32(lz, oracle_mod):
+    wl = I.TINY_F32
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl, lse=True, state=True)
+    ref = oracle_fwd(oracle_mod, inp, wl, parts=True, state=True)
+    assert_parity(out["y"], ref["y"], "f32", "y")
+    assert rel_l2(out["lse"], np.log(ref["den"])) < 1e-5
+    assert_parity(out["S_out"], ref["S"], "f32", "S")
+    assert_parity(out["z_out"], ref["z"], "f32", "z")
+
+
+def test_tiny_f32_gla_sensitive(lz, oracle_mod):
+    wl = I.gla_sensitive(I.TINY_F32.replace(L=640, Hq=4, Hkv=2))
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl)
+    assert_parity(out["y"], oracle_fwd(oracle_mod, inp, wl)["y"], "f32", "y")
+
+
+@pytest.mark.parametrize("L,w", [(1, 32), (31, 32), (33, 32), (65, 1), (200, 5), (130, 300),
+                                 (517, 64), (1100, 100)])
+def test_f32_ragged_lengths_and_windows(lz, oracle_mod, L, w):
+    wl = I.TINY_F32.replace(L=L, w=w, Hq=4, Hkv=2, B=2)
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl, state=True)
+    ref = oracle_fwd(oracle_mod, inp, wl, state=True)
+    assert_parity(out["y"], ref["y"], "f32", "y")
+    assert_parity(out["S_out"], ref["S"], "f32", "S")
+
+
+@pytest.mark.parametrize("d,D,G", [(128, 64, 1), (64, 128, 8), (128, 128, 4), (64, 64, 3)])
+def test_f32_shapes(lz, oracle_mod, d, D, G):
+    wl = I.TINY_F32.replace(L=300, d=d, D=D, Hkv=2, Hq=2 * G, w=16)
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl)
+    assert_parity(out["y"], oracle_fwd(oracle_mod, inp, wl)["y"], "f32", "y")
+
+
+def test_f32_no_sinks(lz, oracle_mod):
+    wl = I.TINY_F32.replace(M=0, L=300)
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl)
+    assert_parity(out["y"], oracle_fwd(oracle_mod, inp, wl)["y"], "f32", "y")
+
+
+def test_llama3_8b_shape_full(lz, oracle_mod):
+    wl = I.LLAMA3_8B_L8K
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl, lse=True, state=True, cache=True)
+    ref = oracle_fwd(oracle_mod, inp, wl, parts=True, state=True)
+    assert_parity(out["y"], ref["y"], "bf16", "y")
+    assert rel_l2(out["lse"], np.log(ref["den"])) < 1e-3
+    assert_parity(out["S_out"], ref["S"], "bf16", "S")
+    assert_parity(out["z_out"], ref["z"], "bf16", "z")
+    # ring caches hold the last w tokens at slot t mod (w+1)
+    L, w = wl.L, wl.w
+    for t in range(L - w, L):
+        np.testing.assert_array_equal(out["kcache_out"][:, :, t % (w + 1)], inp["k"][:, t])
+        np.testing.assert_array_equal(out["vcache_out"][:, :, t % (w + 1)], inp["v"][:, t])
+
+
+@pytest.mark.parametrize("L", [64, 1000, 3000])
+def test_llama3_8b_shape_ragged(lz, oracle_mod, L):
+    wl = I.LLAMA3_8B_L8K
+    inp = I.make_inputs(wl, L=L)
+    out = gpu_fwd(lz, inp, wl)
+    assert_parity(out["y"], oracle_fwd(oracle_mod, inp, wl)["y"], "bf16", "y")
+
+
+def test_llama3_8b_gla_sensitive(lz, oracle_mod):
+    wl = I.gla_sensitive(I.LLAMA3_8B_L8K)
+    inp = I.make_inputs(wl, L=4096)
+    out = gpu_fwd(lz, inp, wl, state=True)
+    ref = oracle_fwd(oracle_mod, inp, wl, state=True, parts=True)
+    assert np.median(ref["den_gla"][:, 2048:] / ref["den"][:, 2048:]) > 0.1
+    assert_parity(out["y"], ref["y"], "bf16", "y")
+    assert_parity(out["S_out"], ref["S"], "bf16", "S")
+
+
+def test_stress_gates_underflow(lz, oracle_mod):
+    """Gate mixture whose chunk products underflow: the log-space path stays finite."""
+    wl = I.STRESS_L64K
+    inp = I.make_inputs(wl, L=8192)
+    out = gpu_fwd(lz, inp, wl)
+    assert_parity(out["y"], oracle_fwd(oracle_mod, inp, wl)["y"], "bf16", "y")
+
+
+def test_stress_full_length_sampled_heads(lz, oracle_mod):
+    """L = 65536: the GPU runs all heads; the oracle checks two KV groups (the units are
+    independent, so a head subset is an exact sub-problem)."""
+    wl = I.STRESS_L64K
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl)
+    G = wl.G
+    for kv in (0, 5):
+        sub = dict(q=inp["q"][:, :, kv * G:(kv + 1) * G], k=inp["k"][:, :, kv:kv + 1],
+                   v=inp["v"][:, :, kv:kv + 1], g=inp["g"][:, :, kv:kv + 1],
+                   Wf=inp["Wf"][kv:kv + 1], sinks=inp["sinks"][kv * G:(kv + 1) * G])
+        ref = oracle_mod.fwd(**sub, w=wl.w, scale=wl.scale)["y"]
+        assert_parity(out["y"][:, :, kv * G:(kv + 1) * G], ref, "bf16", f"y kv{kv}")
+
+
+def test_mistral_7b_train_shape(lz, oracle_mod):
+    wl = I.MISTRAL_7B_TRAIN
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl)
+    assert_parity(out["y"], oracle_fwd(oracle_mod, inp, wl)["y"], "bf16", "y")
+
+
+def test_workspace_reuse_and_determinism(lz):
+    wl = I.LLAMA3_8B_L8K
+    t = to_dev(I.make_inputs(wl, L=2048), wl.dtype)
+    dims = lz.dims_of(t["q"], t["k"], t["g"], t["sinks"], wl.w)
+    ws = lz.new_workspace(lz.lizard_attn_fwd_workspace(dims), "cuda")
+    y1 = lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w,
+                            workspace=ws)
+    y2 = lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w,
+                            workspace=ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
