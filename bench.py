@@ -86,13 +86,21 @@ def load_peaks():
         return 6800.0, 1900.0, "fallback"
 
 
-def load_traffic():
+def load_traffic(key: str):
+    """DRAM bytes per launch of the dominant kernel from a committed ncu capture, or None when
+    the kernel's source has changed since the counters were taken."""
+    import hashlib
+
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
-            return json.load(f)
+            ent = json.load(f)[key]
+        with open(os.path.join(ROOT, ent["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != ent["sha256"]:
+                return None
+        return ent["dram_bytes_per_launch"]
     except Exception:
-        return {}
+        return None
 
 
 def smi_id(local: int) -> str:
@@ -341,7 +349,7 @@ def run_ours(args, rank, world, device):
     value = world * tokens / (step_ms * 1e-3)
     alg_bytes = fwd_algorithmic_bytes(wl)
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = load_traffic().get("fwd_main", {}).get("dram_bytes_per_launch")
+    traffic = load_traffic("fwd_main")
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
