@@ -349,7 +349,9 @@ def run_ours(args, rank, world, device):
     value = world * tokens / (step_ms * 1e-3)
     alg_bytes = fwd_algorithmic_bytes(wl)
     achieved = alg_bytes / (kern_ms * 1e-3) / 1e9
-    traffic = load_traffic("fwd_main")
+    path = lz.lizard_attn_fwd_kernel(dims)
+    key = "fwd_main_tc" if path == 1 else "fwd_main_simt"
+    traffic = load_traffic(key)
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
@@ -359,7 +361,9 @@ def run_ours(args, rank, world, device):
                                        "parallelism": "replicas" if world > 1 else "1 GPU"}),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
-                     "kernel": "chunk walk (fwd main)", "kernel_ms": kern_ms,
+                     "kernel": ("fwd_tc_kernel<main> (tcgen05 chunk walk)" if path == 1
+                                else "fwd_simt_main (SIMT chunk walk)"),
+                     "kernel_ms": kern_ms,
                      "algorithmic_bytes": alg_bytes, "peak_source": peak_src,
                      "flops": fwd_algorithmic_flops(wl),
                      "tflops_achieved": fwd_algorithmic_flops(wl) / (kern_ms * 1e-3) / 1e12},

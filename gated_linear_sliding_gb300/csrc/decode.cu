@@ -8,11 +8,14 @@
 //      / [phi(q).z + sum_j e^{s q.k_j} + sum_m e^{t_m}],
 // with k_{pos-w}, v_{pos-w} and the window read from a (w+1)-slot ring cache.
 //
-// The step is bound by HBM traffic on the fp32 state (read and write of
-// D x d x 4 bytes per (batch, KV head)).  Each (batch, KV head) unit is one
-// cluster of NS CTAs; CTA r owns columns [r d/NS, (r+1) d/NS) of S and of the
-// outputs.  Every CTA reads the old z, so the cluster barrier orders those reads
-// before CTA 0 writes the new z.
+// The step is bound by HBM traffic on the fp32 state (read and write of D x d x 4
+// bytes per (batch, KV head)).  Each (batch, KV head) unit is one cluster of NS CTAs;
+// CTA r owns columns [r d/NS, (r+1) d/NS) of S, of the value window and of the
+// outputs.  At entry every thread issues its share of all loads at once (state slice
+// into registers; Wf, the key window, the value slice, the token and z into shared
+// memory with cp.async), so the CTA pays one memory latency, then computes from
+// on-chip data.  Every CTA reads the old z, so the cluster barrier orders those
+// reads before CTA 0 writes the new z.
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -25,73 +28,67 @@ namespace lz {
 namespace {
 
 constexpr int NT = 256;
-constexpr int NS = 4;  // CTAs (column slices) per unit = cluster size
+constexpr int NS = 4;      // CTAs (column slices) per unit = cluster size
+constexpr int GMAX = 8;    // query heads per KV head
 
-template <typename T, int DH, int DF>
-struct DecLay {
-    static constexpr int CW = DH / NS;       // columns per CTA
-    static constexpr int NRG = NT / CW;      // row groups
-    static constexpr int RPT = DF / NRG;     // state rows per thread
-    static constexpr int GMAX = 8;
-    static constexpr int WMAX = 256;         // window keys staged per step
-};
-
-// phi of one row x (smem, DH floats) with Wf [DH, DF/2] from global; one warp.
-template <typename T, int DH, int DF>
-__device__ __forceinline__ void phi_warp(const float* x, const T* Wk, float* out) {
-    constexpr int H = DF / 2, NJ = H / 32;
-    const int lane = threadIdx.x & 31;
-    float u[NJ];
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) u[j] = 0.0f;
-    for (int c = 0; c < DH; ++c) {
-        const float xc = x[c];
-#pragma unroll
-        for (int j = 0; j < NJ; ++j) u[j] = fmaf(xc, ld(Wk + c * H + lane + 32 * j), u[j]);
-    }
-    float mx = u[0], mn = u[0];
-#pragma unroll
-    for (int j = 1; j < NJ; ++j) {
-        mx = fmaxf(mx, u[j]);
-        mn = fminf(mn, u[j]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-    }
-    float ep[NJ], en[NJ], sp = 0.0f, sn = 0.0f;
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        ep[j] = expf(u[j] - mx);
-        en[j] = expf(mn - u[j]);
-        sp += ep[j];
-        sn += en[j];
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        sp += __shfl_xor_sync(0xffffffffu, sp, o);
-        sn += __shfl_xor_sync(0xffffffffu, sn, o);
-    }
-#pragma unroll
-    for (int j = 0; j < NJ; ++j) {
-        out[lane + 32 * j] = ep[j] / sp;
-        out[H + lane + 32 * j] = en[j] / sn;
-    }
+__device__ __forceinline__ void cp16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 
-template <typename T, int DH, int DF>
+template <typename T, int DH, int DF, int WMAX>
+struct DecLay {
+    static constexpr int CW = DH / NS;        // columns per CTA
+    static constexpr int NRG = NT / CW;       // row groups of the state slice
+    static constexpr int RPT = DF / NRG;      // state rows per thread
+    static constexpr int E = (int)sizeof(T);  // bytes per element
+    static constexpr int KROW = DH * E + 16;  // padded key row (bytes)
+    // byte offsets of the dynamic shared memory
+    static constexpr int oW = 0;                              // Wf [DH][DF/2]
+    static constexpr int oK = oW + DH * (DF / 2) * E;         // key window [WMAX][KROW]
+    static constexpr int oV = oK + WMAX * KROW;               // value slice [WMAX][CW]
+    static constexpr int oQ = oV + WMAX * CW * E;             // raw q rows, k_{pos-w} [G+1][DH]
+    static constexpr int oVE = oQ + (GMAX + 1) * DH * E;      // v_{pos-w} slice [CW]
+    static constexpr int oG = oVE + ((CW * E + 15) / 16) * 16;  // gate logits [DF]
+    static constexpr int oZ = oG + ((DF * E + 15) / 16) * 16;   // old z [DF] fp32
+    static constexpr int oX = oZ + DF * 4;                    // fp32 rows [G+1][DH]
+    static constexpr int oPhi = oX + (GMAX + 1) * DH * 4;     // phi rows [G+1][DF]
+    static constexpr int oU = oPhi + (GMAX + 1) * DF * 4;     // u rows [G+1][DF/2]
+    static constexpr int oGam = oU + (GMAX + 1) * (DF / 2) * 4;
+    static constexpr int oS = oGam + DF * 4;                  // window scores [G][WMAX]
+    static constexpr int oRed = oS + GMAX * WMAX * 4;         // readout partials [NRG][G][CW]
+    static constexpr int oRow = oRed + NRG * GMAX * CW * 4;   // per head m, l, den_gla, sinks
+    static constexpr int bytes = oRow + GMAX * 4 * 4;
+};
+
+template <typename T>
+__device__ __forceinline__ float ldv(const T* p, int i) {
+    return ld(p + i);
+}
+
+template <typename T, int DH, int DF, int WMAX>
 __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     decode_kernel(Plan p, DecodeArgs a) {
-    using Ly = DecLay<T, DH, DF>;
-    constexpr int CW = Ly::CW, NRG = Ly::NRG, RPT = Ly::RPT;
-    __shared__ float sx[(Ly::GMAX + 1) * DH];
-    __shared__ float sphi[(Ly::GMAX + 1) * DF];
-    __shared__ float sgam[DF];
-    __shared__ float sz[DF];
-    __shared__ float sred[NRG * Ly::GMAX * CW];
-    __shared__ float ss[Ly::GMAX * Ly::WMAX];
-    __shared__ float srow[Ly::GMAX * 4];
+    using Ly = DecLay<T, DH, DF, WMAX>;
+    constexpr int CW = Ly::CW, NRG = Ly::NRG, RPT = Ly::RPT, E = Ly::E, H2 = DF / 2;
+    extern __shared__ __align__(16) unsigned char sm[];
+    T* sW = (T*)(sm + Ly::oW);
+    T* sQ = (T*)(sm + Ly::oQ);
+    T* sVE = (T*)(sm + Ly::oVE);
+    T* sG = (T*)(sm + Ly::oG);
+    float* sZ = (float*)(sm + Ly::oZ);
+    float* sX = (float*)(sm + Ly::oX);
+    float* sPhi = (float*)(sm + Ly::oPhi);
+    float* sU = (float*)(sm + Ly::oU);
+    float* sGam = (float*)(sm + Ly::oGam);
+    float* sS = (float*)(sm + Ly::oS);
+    float* sRed = (float*)(sm + Ly::oRed);
+    float* sRow = (float*)(sm + Ly::oRow);
 
     cg::cluster_group cluster = cg::this_cluster();
     const int sl = (int)cluster.block_rank();
@@ -102,99 +99,167 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = tid % CW, rg = tid / CW, c0 = sl * CW;
     const bool admit = pos >= w;
+    const int64_t nkeys = min64(w, pos + 1);
+    const int64_t jstart = pos - nkeys + 1;
+    const T* kc = (const T*)a.kc;
+    const T* vc = (const T*)a.vc;
+    const T* knew = (const T*)a.k + unit * DH;
+    const T* vnew = (const T*)a.v + unit * DH;
 
-    // 1. this CTA's state slice, into registers
+    // 1. issue every load: state slice to registers, the rest to shared memory
     float* Sg = a.S + unit * DF * DH;
     float sreg[RPT];
 #pragma unroll
     for (int i = 0; i < RPT; ++i) sreg[i] = Sg[(rg + NRG * i) * DH + c0 + c];
-
-    // 2. the new token's q heads, the key leaving the window, gates, old z
-    const T* kc = (const T*)a.kc;
-    const T* vc = (const T*)a.vc;
-    for (int e = tid; e < G * DH; e += NT) {
-        const int hh = e / DH, cc = e % DH;
-        sx[e] = ld((const T*)a.q + (b * p.Hq + kv * G + hh) * DH + cc);
+    {
+        const T* Wk = (const T*)a.Wf + kv * DH * H2;
+        constexpr int nW = DH * H2 * E / 16;
+        for (int e = tid; e < nW; e += NT) cp16((char*)sW + 16 * e, (const char*)Wk + 16 * e);
+        constexpr int cpr = DH * E / 16;  // 16-byte chunks per key row
+        for (int e = tid; e < nkeys * cpr; e += NT) {
+            const int64_t jj = e / cpr, ch = e % cpr;
+            const int64_t j = jstart + jj;
+            const T* src = (j == pos) ? knew : kc + (unit * R + j % R) * DH;
+            cp16(sm + Ly::oK + jj * Ly::KROW + 16 * ch, (const char*)src + 16 * ch);
+        }
+        constexpr int cpv = CW * E / 16;  // chunks per value-slice row
+        for (int e = tid; e < nkeys * cpv; e += NT) {
+            const int64_t jj = e / cpv, ch = e % cpv;
+            const int64_t j = jstart + jj;
+            const T* src = (j == pos) ? vnew : vc + (unit * R + j % R) * DH;
+            cp16(sm + Ly::oV + (jj * CW) * E + 16 * ch, (const char*)(src + c0) + 16 * ch);
+        }
+        const T* qrow = (const T*)a.q + (b * p.Hq + kv * G) * DH;
+        for (int e = tid; e < G * cpr; e += NT) cp16((char*)sQ + 16 * e, (const char*)qrow + 16 * e);
+        if (admit) {
+            const T* ke = kc + (unit * R + (pos - w) % R) * DH;
+            const T* ve = vc + (unit * R + (pos - w) % R) * DH + c0;
+            for (int e = tid; e < cpr; e += NT)
+                cp16((char*)(sQ + G * DH) + 16 * e, (const char*)ke + 16 * e);
+            for (int e = tid; e < cpv; e += NT) cp16((char*)sVE + 16 * e, (const char*)ve + 16 * e);
+        }
+        const T* gr = (const T*)a.g + unit * DF;
+        for (int e = tid; e < DF * E / 16; e += NT) cp16((char*)sG + 16 * e, (const char*)gr + 16 * e);
+        const float* zr = a.z + unit * DF;
+        for (int e = tid; e < DF * 4 / 16; e += NT) cp16((char*)sZ + 16 * e, (const char*)zr + 16 * e);
     }
-    for (int e = tid; e < DH; e += NT)
-        sx[G * DH + e] = admit ? ld(kc + (unit * R + (pos - w) % R) * DH + e) : 0.0f;
-    for (int f = tid; f < DF; f += NT) {
-        sgam[f] = sigmoidf_(ld((const T*)a.g + unit * DF + f));
-        sz[f] = a.z[unit * DF + f];
-    }
+    cp_wait_all();
     __syncthreads();
     // every CTA of the cluster has read the old z before CTA 0 may overwrite it
     cluster.sync();
 
-    // 3. feature maps of the G query heads and of the admitted key (one warp per row)
-    const T* Wk = (const T*)a.Wf + kv * DH * (DF / 2);
-    for (int row = warp; row <= G; row += NT / 32) {
-        if (row == G && !admit) {
-            for (int f = lane; f < DF; f += 32) sphi[G * DF + f] = 0.0f;
-        } else {
-            phi_warp<T, DH, DF>(sx + row * DH, Wk, sphi + row * DF);
+    // 2. token rows to fp32, gates
+    for (int e = tid; e < (G + 1) * DH; e += NT) {
+        const int r = e / DH;
+        sX[e] = (r < G || admit) ? ld(sQ + e) : 0.0f;
+    }
+    for (int f = tid; f < DF; f += NT) sGam[f] = sigmoidf_(ld(sG + f));
+    __syncthreads();
+
+    // 3. u = x Wf for the G query rows and the admitted key: 4 threads per output
+    for (int r = 0; r <= G; ++r) {
+        for (int o = tid; o < H2 * 4; o += NT) {
+            const int f = o >> 2, part = o & 3;
+            float acc = 0.0f;
+            const float* x = sX + r * DH;
+#pragma unroll 8
+            for (int cc = part * (DH / 4); cc < (part + 1) * (DH / 4); ++cc)
+                acc = fmaf(x[cc], ld(sW + cc * H2 + f), acc);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (part == 0) sU[r * H2 + f] = acc;
+        }
+    }
+    __syncthreads();
+    // phi rows: one warp per row, [softmax(u), softmax(-u)]
+    for (int r = warp; r <= G; r += NT / 32) {
+        constexpr int NJ = H2 / 32;
+        float u[NJ];
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) u[j] = sU[r * H2 + lane + 32 * j];
+        float mx = u[0], mn = u[0];
+#pragma unroll
+        for (int j = 1; j < NJ; ++j) {
+            mx = fmaxf(mx, u[j]);
+            mn = fminf(mn, u[j]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        }
+        float ep[NJ], en[NJ], sp = 0.0f, sn = 0.0f;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            ep[j] = expf(u[j] - mx);
+            en[j] = expf(mn - u[j]);
+            sp += ep[j];
+            sn += en[j];
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sp += __shfl_xor_sync(0xffffffffu, sp, o);
+            sn += __shfl_xor_sync(0xffffffffu, sn, o);
+        }
+        const bool zero = (r == G) && !admit;
+#pragma unroll
+        for (int j = 0; j < NJ; ++j) {
+            sPhi[r * DF + lane + 32 * j] = zero ? 0.0f : ep[j] / sp;
+            sPhi[r * DF + H2 + lane + 32 * j] = zero ? 0.0f : en[j] / sn;
         }
     }
     __syncthreads();
 
     // 4. state update of this slice (in place) and partial readouts phi(q).S
-    const float ve = admit ? ld(vc + (unit * R + (pos - w) % R) * DH + c0 + c) : 0.0f;
+    const float ve = admit ? ld(sVE + c) : 0.0f;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         const int f = rg + NRG * i;
-        const float sv = fmaf(sgam[f], sreg[i], sphi[G * DF + f] * ve);
+        const float sv = fmaf(sGam[f], sreg[i], sPhi[G * DF + f] * ve);
         sreg[i] = sv;
         Sg[f * DH + c0 + c] = sv;
     }
     for (int hh = 0; hh < G; ++hh) {
         float part = 0.0f;
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) part = fmaf(sphi[hh * DF + rg + NRG * i], sreg[i], part);
-        sred[(rg * G + hh) * CW + c] = part;
+        for (int i = 0; i < RPT; ++i) part = fmaf(sPhi[hh * DF + rg + NRG * i], sreg[i], part);
+        sRed[(rg * G + hh) * CW + c] = part;
     }
-    __syncthreads();
+    // new z (this CTA's copy in shared memory; CTA 0 writes it back)
     for (int f = tid; f < DF; f += NT) {
-        const float zn = fmaf(sgam[f], sz[f], sphi[G * DF + f]);
-        sz[f] = zn;
+        const float zn = fmaf(sGam[f], sZ[f], sPhi[G * DF + f]);
+        sZ[f] = zn;
         if (sl == 0) a.z[unit * DF + f] = zn;
     }
 
-    // 5. window scores s_hj = scale q_h.k_j, j in (pos-w, pos]; the newest key is the input
-    const int64_t nkeys = min64(w, pos + 1);
-    const int64_t jstart = pos - nkeys + 1;
-    for (int64_t jj = warp; jj < nkeys; jj += NT / 32) {
-        const int64_t j = jstart + jj;
-        const T* krow = (j == pos) ? (const T*)a.k + unit * DH : kc + (unit * R + j % R) * DH;
-        float kr[DH / 32];
-#pragma unroll
-        for (int e = 0; e < DH / 32; ++e) kr[e] = ld(krow + lane + 32 * e);
-        for (int hh = 0; hh < G; ++hh) {
-            float part = 0.0f;
-#pragma unroll
-            for (int e = 0; e < DH / 32; ++e) part = fmaf(sx[hh * DH + lane + 32 * e], kr[e], part);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-            if (lane == 0) ss[hh * Ly::WMAX + jj] = part * p.scale;
-        }
+    // 5. window scores s_hj = scale q_h.k_j from the staged key rows
+    for (int e = tid; e < G * nkeys; e += NT) {
+        const int hh = e / (int)nkeys, jj = e % (int)nkeys;
+        const T* kr = (const T*)(sm + Ly::oK + jj * Ly::KROW);
+        const float* x = sX + hh * DH;
+        float acc = 0.0f;
+#pragma unroll 8
+        for (int cc = 0; cc < DH; ++cc) acc = fmaf(x[cc], ld(kr + cc), acc);
+        sS[hh * WMAX + jj] = acc * p.scale;
     }
     __syncthreads();
 
-    // 6. per head: shift m, window weights, state denominator, sink sum
+    // 6. per head: shift m, window weights, state denominator, sink sum (one warp per head)
     for (int hh = warp; hh < G; hh += NT / 32) {
         const int64_t h = kv * G + hh;
         float m = kMinShift;
         for (int mm = 0; mm < p.M; ++mm) m = fmaxf(m, a.sinks[h * p.M + mm]);
-        for (int64_t jj = lane; jj < nkeys; jj += 32) m = fmaxf(m, ss[hh * Ly::WMAX + jj]);
+        for (int jj = lane; jj < nkeys; jj += 32) m = fmaxf(m, sS[hh * WMAX + jj]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.0f;
-        for (int64_t jj = lane; jj < nkeys; jj += 32) {
-            const float pw = expf(ss[hh * Ly::WMAX + jj] - m);
-            ss[hh * Ly::WMAX + jj] = pw;
+        for (int jj = lane; jj < nkeys; jj += 32) {
+            const float pw = expf(sS[hh * WMAX + jj] - m);
+            sS[hh * WMAX + jj] = pw;
             l += pw;
         }
         float gd = 0.0f;
-        for (int f = lane; f < DF; f += 32) gd = fmaf(sphi[hh * DF + f], sz[f], gd);
+        for (int f = lane; f < DF; f += 32) gd = fmaf(sPhi[hh * DF + f], sZ[f], gd);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             l += __shfl_xor_sync(0xffffffffu, l, o);
@@ -203,29 +268,27 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
         float ssum = 0.0f;
         for (int mm = 0; mm < p.M; ++mm) ssum += expf(a.sinks[h * p.M + mm] - m);
         if (lane == 0) {
-            srow[hh * 4 + 0] = m;
-            srow[hh * 4 + 1] = l;
-            srow[hh * 4 + 2] = gd;
-            srow[hh * 4 + 3] = ssum;
+            sRow[hh * 4 + 0] = m;
+            sRow[hh * 4 + 1] = l;
+            sRow[hh * 4 + 2] = gd;
+            sRow[hh * 4 + 3] = ssum;
         }
     }
     __syncthreads();
 
     // 7. outputs of this slice's columns
+    const T* sV = (const T*)(sm + Ly::oV);
     for (int e = tid; e < G * CW; e += NT) {
         const int hh = e / CW, cc = e % CW;
         float num = 0.0f;
-        for (int r2 = 0; r2 < NRG; ++r2) num += sred[(r2 * G + hh) * CW + cc];
+#pragma unroll
+        for (int r2 = 0; r2 < NRG; ++r2) num += sRed[(r2 * G + hh) * CW + cc];
         float wv = 0.0f;
-        for (int64_t jj = 0; jj < nkeys; ++jj) {
-            const int64_t j = jstart + jj;
-            const T* vrow = (j == pos) ? (const T*)a.v + unit * DH : vc + (unit * R + j % R) * DH;
-            wv = fmaf(ss[hh * Ly::WMAX + jj], ld(vrow + c0 + cc), wv);
-        }
-        const float m = srow[hh * 4 + 0];
-        const float E = expf(-m);
-        const float den = E * srow[hh * 4 + 2] + srow[hh * 4 + 1] + srow[hh * 4 + 3];
-        st((T*)a.y + (b * p.Hq + kv * G + hh) * DH + c0 + cc, (E * num + wv) / den);
+        for (int jj = 0; jj < nkeys; ++jj) wv = fmaf(sS[hh * WMAX + jj], ld(sV + jj * CW + cc), wv);
+        const float m = sRow[hh * 4 + 0];
+        const float Em = expf(-m);
+        const float den = Em * sRow[hh * 4 + 2] + sRow[hh * 4 + 1] + sRow[hh * 4 + 3];
+        st((T*)a.y + (b * p.Hq + kv * G + hh) * DH + c0 + cc, (Em * num + wv) / den);
     }
 
     // 8. the new token joins the ring (slot pos mod (w+1), never read in this step)
@@ -233,16 +296,26 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     T* vco = (T*)a.vc;
     for (int cc = tid; cc < CW; cc += NT) {
         const int64_t dst = (unit * R + pos % R) * DH + c0 + cc;
-        kco[dst] = ((const T*)a.k)[unit * DH + c0 + cc];
-        vco[dst] = ((const T*)a.v)[unit * DH + c0 + cc];
+        kco[dst] = knew[c0 + cc];
+        vco[dst] = vnew[c0 + cc];
     }
 }
 
+template <typename T, int DH, int DF, int WMAX>
+cudaError_t launch_w(const Plan& p, const DecodeArgs& a, cudaStream_t s) {
+    using Ly = DecLay<T, DH, DF, WMAX>;
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, DH, DF, WMAX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::bytes);
+    if (e != cudaSuccess) return e;
+    const unsigned grid = (unsigned)(p.B * p.Hkv * NS);
+    decode_kernel<T, DH, DF, WMAX><<<grid, NT, Ly::bytes, s>>>(p, a);
+    return cudaGetLastError();
+}
+
+// window capacity 64 keys for the usual w <= 64 (smaller shared-memory footprint), 256 otherwise
 template <typename T, int DH, int DF>
 cudaError_t launch_t(const Plan& p, const DecodeArgs& a, cudaStream_t s) {
-    const unsigned grid = (unsigned)(p.B * p.Hkv * NS);
-    decode_kernel<T, DH, DF><<<grid, NT, 0, s>>>(p, a);
-    return cudaGetLastError();
+    return p.w <= 64 ? launch_w<T, DH, DF, 64>(p, a, s) : launch_w<T, DH, DF, 256>(p, a, s);
 }
 
 template <typename T>

@@ -1,12 +1,690 @@
-// Tensor-core (tcgen05 / TMEM / TMA) forward of the Lizard token mixer: not built yet.
+// Tensor-core forward of the Lizard token mixer on sm_103a: tcgen05 MMAs with TMEM
+// accumulators, operands staged by TMA in 128-byte-swizzled shared memory.
+//
+// Covers the LLaMA-3-8B / Mistral-7B-shaped layers: bf16, d = D = 128, four query
+// heads per KV head, window w = 64.  Other shapes take the SIMT path.
+//
+// Lizard summary (gist.science/ko/paper/2507.09025):
+//   sec. 2-A-1  gated linear attention, state S_i = Gamma_i (.) S_{i-1} + phi(k) v^T
+//               (here the key that leaves the window enters the state);
+//   sec. 2-A-2  sliding-window softmax with meta-memory scalars in the denominator;
+//   sec. 2-C    the Hedgehog map is non-negative, so the gate products move to log
+//               space and fold into the query and key sides, which turns the chunk
+//               into plain low-precision GEMMs on the tensor cores.
+//
+// One CTA per (batch, KV head, segment); it walks its segment 32 tokens at a time.
+// The 128 query rows of a step are (token, head) pairs, row = 4 * token + head, so
+// the four heads of a group share every key-side operand.  Per step:
+//   b_t   = sum_{s<=t} log sigmoid(g_s)  (fp32, chunk-local), reference r = b_15
+//   q~_i  = phi(q_i) e^{b_i - r} e^{-m_i}          m_i = row shift (window, sinks)
+//   k~_t  = phi(k_{t-w}) e^{r - b_t}                (delayed key of stream step t)
+//   O_i   = q~_i (e^{r} (.) H) + P_win V_ring + [q~ k~^T (.) causal] V_delayed
+//   H    <- e^{b_31} (.) H + (phi(k_{t-w}) e^{b_31 - b_t})^T V_delayed
+//   y_i   = O_i / (sum P_win + sum P_intra + q~_i.(e^{r} z) + sum_m e^{t_m - m_i})
+// Every gate factor is e^{difference of cumulative log-gates}; relative to the
+// sub-chunk midpoint r each factor stays within the log-decay of 16 tokens, so no
+// factor leaves the fp32/bf16 range unless 16 consecutive gates decay by more than
+// e^-80 (exponents are clamped to +-80 there).
+//
+// TMEM columns: H [0,128)  scores S [128,256)  U_q [256,320)  U_k [320,384)
+//               O [256,384) (reuses U)  intra scores A [384,416).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+
+#include "common.cuh"
 #include "internal.h"
+#include "sm100.cuh"
 
 namespace lz {
+namespace {
 
-bool fwd_tc_supported(const Plan&) { return false; }
+using namespace sm100;
 
-cudaError_t launch_fwd_tc(const Plan&, const FwdArgs&, cudaStream_t) {
-    return cudaErrorNotSupported;
+constexpr int NT = 256;   // 8 warps: warp w owns TMEM lanes 32(w%4).. ; w/4 picks a column half
+constexpr int CT = 32;    // tokens per step
+constexpr int GQ = 4;     // query heads per KV head
+constexpr int DH = 128;   // head dim
+constexpr int DF = 128;   // phi dim
+constexpr int WIN = 64;   // window
+constexpr int MMAX = 64;  // sinks per head
+constexpr long long kTimeout = 2000000000LL;  // SM cycles (about one second)
+
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr uint32_t oQ = 0;         // q tile, K-major [128 rows][128 d]; then P_win [128][128 keys]
+constexpr uint32_t oQt = 32768;    // q~, K-major [128 rows][128 features]
+constexpr uint32_t oK = 65536;     // key ring: 4 slots x 32 keys, K-major over d
+constexpr uint32_t oV = 98304;     // value ring: same bytes, read MN-major (N = d)
+constexpr uint32_t oW = 131072;    // Wf [128 d rows][64 features], MN-major B
+constexpr uint32_t oHs = 147456;   // e^{r} (.) H in bf16, [128 feature rows][128 d], MN-major B
+constexpr uint32_t oKi = 180224;   // k~ (intra), K-major [32 keys][128 features]
+constexpr uint32_t oKu = 188416;   // k~ (state update), MN-major A, same byte layout
+constexpr uint32_t oE = 196608;    // Eq, Ek tables (bf16 [32][128] each); then P_intra
+constexpr uint32_t oSmall = 212992;
+
+struct Small {
+    uint64_t bar_tma, bar_mma;
+    uint32_t tmem;
+    volatile int abort;
+    float z[DF], zs[DF], eref[DF], elast[DF], cf[DF];
+    float m[128], den[128];
+    float pm[2][128], ps[2][128], pg[2][128];
+    float tmax[GQ];
+    float sinks[GQ][MMAX];
+};
+constexpr uint32_t kSmemBytes = oSmall + (uint32_t)sizeof(Small) + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// TMEM column bases
+constexpr uint32_t cH = 0, cS = 128, cUq = 256, cUk = 320, cO = 256, cA = 384;
+
+__device__ __forceinline__ float clamp80(float x) { return fminf(fmaxf(x, -80.0f), 80.0f); }
+
+__device__ __forceinline__ float bf16r(float x) {
+    return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+__device__ __forceinline__ void unpack8(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                        float* o) {
+    const uint32_t w[4] = {w0, w1, w2, w3};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
+        float2 f = __bfloat1622float2(h);
+        o[2 * k] = f.x;
+        o[2 * k + 1] = f.y;
+    }
+}
+
+// Wait for a barrier phase with a time limit; all threads return the same verdict.
+__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t& ph, Small& S, WsHeader* hdr,
+                                         unsigned where) {
+    if (!mbar_wait(bar, ph, kTimeout)) {
+        S.abort = 1;
+        report(hdr, LIZARD_ERR_TIMEOUT, where);
+    } else {
+        ph ^= 1u;
+    }
+    __syncthreads();
+    return S.abort == 0;
+}
+
+// K-major (or MN-major) descriptor helpers for the 128-byte-swizzled tiles.
+__device__ __forceinline__ uint64_t kdesc(uint32_t addr) {
+    return make_sdesc(addr, 16, 1024, kSwizzle128);
+}
+__device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
+    return make_sdesc(addr, lbo, 1024, kSwizzle128);
+}
+
+template <bool MAIN>
+__global__ void __launch_bounds__(NT, 1)
+    fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmW,
+                  Plan p, FwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    Small& S = *reinterpret_cast<Small*>(sm + oSmall);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, half = warp >> 2;
+    const int row = 32 * quad + lane;
+    const int64_t unit = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t U = p.B * p.Hkv;
+    const int64_t s0 = seg * p.seg_len;
+    const int64_t s1 = min64(p.L, s0 + p.seg_len);
+    WsHeader* hdr = (WsHeader*)a.header;
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    const __nv_bfloat16* gptr = (const __nv_bfloat16*)a.g;
+
+    if (warp == 0) {
+        tmem_alloc(&S.tmem, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&S.bar_tma, 1);
+        mbar_init(&S.bar_mma, 1);
+        fence_mbar_init();
+        S.abort = 0;
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmW);
+        if (MAIN) prefetch_tmap(&tmQ);
+    }
+    if (MAIN) {
+        for (int e = tid; e < GQ * MMAX; e += NT) {
+            const int hh = e / MMAX, mm = e % MMAX;
+            S.sinks[hh][mm] = mm < p.M ? a.sinks[(kv * GQ + hh) * p.M + mm] : 0.0f;
+        }
+        if (tid < GQ) {
+            float tm = kMinShift;
+            for (int mm = 0; mm < p.M; ++mm) tm = fmaxf(tm, a.sinks[(kv * GQ + tid) * p.M + mm]);
+            S.tmax[tid] = tm;
+        }
+    }
+    // zero both rings: P_win is 0 on masked keys, but 0 times non-finite stale bits is NaN
+    for (int e = tid; e < 65536 / 16; e += NT) st_shared_v4(base + oK + e * 16, 0u, 0u, 0u, 0u);
+    fence_async_smem();
+    const float* rec = (MAIN && seg > 0)
+                           ? a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats
+                           : nullptr;
+    if (tid < DF) S.z[tid] = rec ? rec[DF * DH + tid] : 0.0f;
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = S.tmem;
+
+    // starting state H into TMEM (fp32 master copy), lane = feature f, column = d
+    {
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int col = 64 * half + 32 * j;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + col + k] : 0.0f;
+            tmem_st32(tb + lane_off + cH + col, v);
+        }
+        tmem_wait_st();
+    }
+
+    uint32_t ph_tma = 0, ph_mma = 0;
+    bool tma_pending = false, mma_pending = false;
+    const int64_t c_begin = s0 / CT, c_end = (s1 + CT - 1) / CT;
+    float lam_tot = 0.0f;
+    bool ok = true;
+
+    // Wf and the two chunks before the segment (zero-filled before the sequence start)
+    if (tid == 0) {
+        mbar_arrive_expect_tx(&S.bar_tma, 16384u + 2u * 16384u);
+        tma_load_3d(sm + oW, &tmW, &S.bar_tma, 0, 0, (int)kv);
+        for (int64_t cc = c_begin - 2; cc < c_begin; ++cc) {
+            const int slot = (int)(cc & 3);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_4d(sm + oK + kb * 16384 + slot * 4096, &tmK, &S.bar_tma, 64 * kb, (int)kv,
+                            (int)(cc * CT), (int)b);
+                tma_load_4d(sm + oV + kb * 16384 + slot * 4096, &tmV, &S.bar_tma, 64 * kb, (int)kv,
+                            (int)(cc * CT), (int)b);
+            }
+        }
+    }
+    tma_pending = true;
+    ok = wait_bar(&S.bar_tma, ph_tma, S, hdr, 1);
+    if (ok) tma_pending = false;
+
+    for (int64_t c = c_begin; ok && c < c_end; ++c) {
+        const int64_t t0 = c * CT;
+        const int n = (int)min64(CT, s1 - t0);
+        const int slot_c = (int)(c & 3), slot_d = (int)((c - 2) & 3);
+
+        // (1) this step's keys, values (and queries) into the rings
+        if (tid == 0) {
+            mbar_arrive_expect_tx(&S.bar_tma, MAIN ? 16384u + 32768u : 16384u);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_4d(sm + oK + kb * 16384 + slot_c * 4096, &tmK, &S.bar_tma, 64 * kb,
+                            (int)kv, (int)t0, (int)b);
+                tma_load_4d(sm + oV + kb * 16384 + slot_c * 4096, &tmV, &S.bar_tma, 64 * kb,
+                            (int)kv, (int)t0, (int)b);
+                if (MAIN)
+                    tma_load_4d(sm + oQ + kb * 16384, &tmQ, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                                (int)t0, (int)b);
+            }
+        }
+        tma_pending = true;
+
+        // (2) gates: cumulative log-sigmoid per feature, decay tables around r = b_15
+        if (tid < DF) {
+            const int f = tid;
+            float bt[CT];
+            float run = 0.0f;
+#pragma unroll
+            for (int t = 0; t < CT; ++t) {
+                float lam = 0.0f;
+                if (t < n)
+                    lam = log_sigmoid<true>(
+                        __bfloat162float(gptr[((b * p.L + t0 + t) * p.Hkv + kv) * DF + f]));
+                run += lam;
+                bt[t] = run;
+            }
+            const float bref = bt[15], blast = bt[CT - 1];
+            __nv_bfloat16* Eq = (__nv_bfloat16*)(sm + oE);
+            __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + oE + 8192);
+#pragma unroll
+            for (int t = 0; t < CT; ++t) {
+                Eq[t * DF + f] = __float2bfloat16_rn(__expf(clamp80(bt[t] - bref)));
+                Ek[t * DF + f] = __float2bfloat16_rn(__expf(clamp80(bref - bt[t])));
+            }
+            const float er = __expf(bref);
+            S.eref[f] = er;
+            S.elast[f] = __expf(blast);
+            S.cf[f] = __expf(blast - bref);
+            S.zs[f] = er * S.z[f];
+            lam_tot += blast;
+        }
+        __syncthreads();
+
+        // (3) state: bf16 copy scaled by e^{r} for the readout; decay the master by e^{b_31}
+        {
+            const int f = row;
+            const float er = S.eref[f], el = S.elast[f];
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = 64 * half + 32 * j;
+                tmem_ld32(tb + lane_off + cH + col, v);
+                tmem_wait_ld();
+                if (MAIN) {
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const int nchunk = (col & 63) / 8 + ch;
+                        st_shared_v4(base + oHs + (col / 64) * 16384 + sw128(f, nchunk),
+                                     pack_bf16(er * v[8 * ch], er * v[8 * ch + 1]),
+                                     pack_bf16(er * v[8 * ch + 2], er * v[8 * ch + 3]),
+                                     pack_bf16(er * v[8 * ch + 4], er * v[8 * ch + 5]),
+                                     pack_bf16(er * v[8 * ch + 6], er * v[8 * ch + 7]));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] *= el;
+                tmem_st32(tb + lane_off + cH + col, v);
+            }
+            tmem_wait_st();
+        }
+
+        // (4) operands have landed
+        ok = wait_bar(&S.bar_tma, ph_tma, S, hdr, 2);
+        if (!ok) break;
+        tma_pending = false;
+
+        // (5) feature-map projections and window scores
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t koff = (j >> 2) * 16384 + (j & 3) * 32;
+                const uint64_t bw = mndesc(base + oW + j * 2048, 16384);
+                mma_bf16(tb + cUk, kdesc(base + oK + koff), bw, idesc_bf16(128, 64, false, true),
+                         j > 0);
+                if (MAIN) {
+                    const uint64_t aq = kdesc(base + oQ + koff);
+                    mma_bf16(tb + cUq, aq, bw, idesc_bf16(128, 64, false, true), j > 0);
+                    mma_bf16(tb + cS, aq, kdesc(base + oK + koff), idesc_bf16(128, 128, false, false),
+                             j > 0);
+                }
+            }
+            mma_commit(&S.bar_mma);
+        }
+        mma_pending = true;
+        ok = wait_bar(&S.bar_mma, ph_mma, S, hdr, 3);
+        if (!ok) break;
+        mma_pending = false;
+        tc_fence_after();
+
+        // (6) window softmax (all rows, two column halves) and the query feature map
+        const int i = row >> 2, hh = row & 3;
+        const int64_t qa = t0 + i;
+        const bool qv = i < n;
+        float m_row = 0.0f;
+        if (MAIN) {
+            float sv[64];
+            tmem_ld32(tb + lane_off + cS + 64 * half, sv);
+            tmem_ld32(tb + lane_off + cS + 64 * half + 32, sv + 32);
+            tmem_wait_ld();
+            float pmax = -INFINITY;
+            uint64_t vm = 0;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+                const int kr = 64 * half + k;
+                const int slot = kr >> 5, u = kr & 31;
+                const int64_t age = (c - slot) & 3;
+                const int64_t key = (c - age) * CT + u;
+                const bool valid = qv && age <= 2 && key <= qa && key > qa - WIN && key >= 0;
+                sv[k] *= p.scale;
+                if (valid) {
+                    pmax = fmaxf(pmax, sv[k]);
+                    vm |= (1ull << k);
+                }
+            }
+            S.pm[half][row] = pmax;
+            __syncthreads();
+            m_row = fmaxf(fmaxf(S.pm[0][row], S.pm[1][row]), S.tmax[hh]);
+            float psum = 0.0f;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                float pv[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int k = 8 * ch + e;
+                    pv[e] = ((vm >> k) & 1ull) ? bf16r(__expf(sv[k] - m_row)) : 0.0f;
+                    psum += pv[e];
+                }
+                st_shared_v4(base + oQ + half * 16384 + sw128(row, ch), pack_bf16(pv[0], pv[1]),
+                             pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
+                             pack_bf16(pv[6], pv[7]));
+            }
+            S.ps[half][row] = psum;
+
+            // phi(q): half 0 takes softmax(u), half 1 softmax(-u), u = q Wf (64 values)
+            float uv[64];
+            tmem_ld32(tb + lane_off + cUq, uv);
+            tmem_ld32(tb + lane_off + cUq + 32, uv + 32);
+            tmem_wait_ld();
+            float ref = uv[0];
+#pragma unroll
+            for (int k = 1; k < 64; ++k) ref = half ? fminf(ref, uv[k]) : fmaxf(ref, uv[k]);
+            float sum = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+                uv[k] = __expf(half ? (ref - uv[k]) : (uv[k] - ref));
+                sum += uv[k];
+            }
+            const float sc = __expf(-m_row) / sum;
+            float pg = 0.0f;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const int f0 = 64 * half + 8 * ch;
+                uint32_t w0, w1, w2, w3;
+                ld_shared_v4(base + oE + (uint32_t)(i * DF + f0) * 2u, w0, w1, w2, w3);
+                float eq[8], qv8[8];
+                unpack8(w0, w1, w2, w3, eq);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    qv8[e] = bf16r(uv[8 * ch + e] * sc * eq[e]);
+                    pg = fmaf(qv8[e], S.zs[f0 + e], pg);
+                }
+                st_shared_v4(base + oQt + half * 16384 + sw128(row, ch), pack_bf16(qv8[0], qv8[1]),
+                             pack_bf16(qv8[2], qv8[3]), pack_bf16(qv8[4], qv8[5]),
+                             pack_bf16(qv8[6], qv8[7]));
+            }
+            S.pg[half][row] = pg;
+        }
+
+        // phi of the delayed keys (the ring slot two steps back) -> k~ for intra and update
+        if (quad == slot_d) {
+            const int t = lane;
+            const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
+            float uv[64];
+            tmem_ld32(tb + lane_off + cUk, uv);
+            tmem_ld32(tb + lane_off + cUk + 32, uv + 32);
+            tmem_wait_ld();
+            float ref = uv[0];
+#pragma unroll
+            for (int k = 1; k < 64; ++k) ref = half ? fminf(ref, uv[k]) : fmaxf(ref, uv[k]);
+            float sum = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 64; ++k) {
+                uv[k] = __expf(half ? (ref - uv[k]) : (uv[k] - ref));
+                sum += uv[k];
+            }
+            const float inv = dvalid ? 1.0f / sum : 0.0f;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const int f0 = 64 * half + 8 * ch;
+                uint32_t w0, w1, w2, w3;
+                ld_shared_v4(base + oE + 8192u + (uint32_t)(t * DF + f0) * 2u, w0, w1, w2, w3);
+                float ek[8], ki[8], ku[8];
+                unpack8(w0, w1, w2, w3, ek);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float phk = uv[8 * ch + e] * inv;
+                    ki[e] = phk * ek[e];
+                    ku[e] = ki[e] * S.cf[f0 + e];
+                }
+                if (MAIN)
+                    st_shared_v4(base + oKi + half * 4096 + sw128(t, ch), pack_bf16(ki[0], ki[1]),
+                                 pack_bf16(ki[2], ki[3]), pack_bf16(ki[4], ki[5]),
+                                 pack_bf16(ki[6], ki[7]));
+                st_shared_v4(base + oKu + half * 4096 + sw128(t, ch), pack_bf16(ku[0], ku[1]),
+                             pack_bf16(ku[2], ku[3]), pack_bf16(ku[4], ku[5]),
+                             pack_bf16(ku[6], ku[7]));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+
+        // (7) intra-step scores A = q~ k~^T
+        if (MAIN && tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t qoff = (j >> 2) * 16384 + (j & 3) * 32;
+                const uint32_t koff = (j >> 2) * 4096 + (j & 3) * 32;
+                mma_bf16(tb + cA, kdesc(base + oQt + qoff), kdesc(base + oKi + koff),
+                         idesc_bf16(128, 32, false, false), j > 0);
+            }
+            mma_commit(&S.bar_mma);
+        }
+        // z <- e^{b_31} z + sum_t k~u_t (read back from the bf16 tile the MMA uses)
+        if (tid < DF) {
+            const int f = tid;
+            float zsum = 0.0f;
+            const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + oKu);
+            for (int t = 0; t < CT; ++t) {
+                const uint32_t off = (f >> 6) * 4096 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
+                zsum += __bfloat162float(ku[off / 2]);
+            }
+            S.z[f] = fmaf(S.elast[f], S.z[f], zsum);
+        }
+        if (MAIN) {
+            mma_pending = true;
+            ok = wait_bar(&S.bar_mma, ph_mma, S, hdr, 4);
+            if (!ok) break;
+            mma_pending = false;
+            tc_fence_after();
+            if (half == 0) {
+                float av[32];
+                tmem_ld32(tb + lane_off + cA, av);
+                tmem_wait_ld();
+                float ps2 = 0.0f;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    float pv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int t = 8 * ch + e;
+                        const bool valid = qv && t <= i && (t0 + t - WIN >= 0);
+                        pv[e] = valid ? bf16r(av[t]) : 0.0f;
+                        ps2 += pv[e];
+                    }
+                    st_shared_v4(base + oE + sw128(row, ch), pack_bf16(pv[0], pv[1]),
+                                 pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
+                                 pack_bf16(pv[6], pv[7]));
+                }
+                float ssum = 0.0f;
+                for (int mm = 0; mm < p.M; ++mm) ssum += __expf(S.sinks[hh][mm] - m_row);
+                S.m[row] = m_row;
+                S.den[row] = S.ps[0][row] + S.ps[1][row] + S.pg[0][row] + S.pg[1][row] + ps2 + ssum;
+            }
+            fence_async_smem();
+            tc_fence_before();
+            __syncthreads();
+        }
+
+        // (8) outputs and the state update
+        if (tid == 0) {
+            tc_fence_after();
+            if (MAIN) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t qoff = (j >> 2) * 16384 + (j & 3) * 32;
+                    mma_bf16(tb + cO, kdesc(base + oQt + qoff), mndesc(base + oHs + j * 2048, 16384),
+                             idesc_bf16(128, 128, false, true), j > 0);
+                }
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const uint32_t poff = (j >> 2) * 16384 + (j & 3) * 32;
+                    mma_bf16(tb + cO, kdesc(base + oQ + poff), mndesc(base + oV + j * 2048, 16384),
+                             idesc_bf16(128, 128, false, true), 1);
+                }
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+                    mma_bf16(tb + cO, kdesc(base + oE + j * 32),
+                             mndesc(base + oV + slot_d * 4096 + j * 2048, 16384),
+                             idesc_bf16(128, 128, false, true), 1);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                mma_bf16(tb + cH, mndesc(base + oKu + j * 2048, 4096),
+                         mndesc(base + oV + slot_d * 4096 + j * 2048, 16384),
+                         idesc_bf16(128, 128, true, true), 1);
+            mma_commit(&S.bar_mma);
+        }
+        mma_pending = true;
+        ok = wait_bar(&S.bar_mma, ph_mma, S, hdr, 5);
+        if (!ok) break;
+        mma_pending = false;
+        tc_fence_after();
+
+        // (9) epilogue: y = O / den, 16-byte bf16 stores
+        if (MAIN) {
+            float ov[32];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = 64 * half + 32 * j;
+                tmem_ld32(tb + lane_off + cO + col, ov);
+                tmem_wait_ld();
+                if (qv) {
+                    const float inv = 1.0f / S.den[row];
+                    __nv_bfloat16* yr = (__nv_bfloat16*)a.y +
+                                        ((b * p.L + qa) * p.Hq + kv * GQ + hh) * DH + col;
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint4 w;
+                        w.x = pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv);
+                        w.y = pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv);
+                        w.z = pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv);
+                        w.w = pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv);
+                        *reinterpret_cast<uint4*>(yr + 8 * ch) = w;
+                    }
+                }
+            }
+            if (qv && half == 0 && a.lse != nullptr)
+                a.lse[(b * p.L + qa) * p.Hq + kv * GQ + hh] = S.m[row] + logf(S.den[row]);
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+
+    if (ok) {
+        // final state of the segment: the local record (segment pass) or the decode hand-off
+        float* dstH = nullptr;
+        float* dstz = nullptr;
+        if (!MAIN) {
+            float* r = a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats;
+            dstH = r;
+            dstz = r + DF * DH;
+            if (tid < DF) r[DF * DH + DF + tid] = lam_tot;
+        } else if (a.S_out != nullptr && s1 == p.L) {
+            dstH = a.S_out + unit * DF * DH;
+            dstz = a.z_out + unit * DF;
+        }
+        if (dstH != nullptr) {
+            tc_fence_after();
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = 64 * half + 32 * j;
+                tmem_ld32(tb + lane_off + cH + col, v);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(dstH + row * DH + col + k) =
+                        make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+            }
+            if (tid < DF) dstz[tid] = S.z[tid];
+        }
+    } else {
+        // a wait gave up: let copies and MMAs still in flight land before leaving
+        if (tid == 0) {
+            if (tma_pending) mbar_wait(&S.bar_tma, ph_tma, kTimeout);
+            if (mma_pending) mbar_wait(&S.bar_mma, ph_mma, kTimeout);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
+    }
+    return fn;
+}
+
+bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
+              const cuuint64_t* strides, const cuuint32_t* box) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
+              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool fwd_tc_supported(const Plan& p) {
+    return p.dtype == LIZARD_BF16 && p.d == DH && p.D == DF && p.G == GQ && p.w == WIN &&
+           p.M <= MMAX && p.L < ((int64_t)1 << 30) && encode_fn() != nullptr;
+}
+
+cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
+    Plan p = p0;
+    plan_segments(&p, 152);
+    alignas(64) CUtensorMap mq, mk, mv, mw;
+    const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
+                     Hkv = (cuuint64_t)p.Hkv;
+    {
+        const cuuint64_t dims[4] = {DH, Hq, L, B};
+        const cuuint64_t str[3] = {DH * 2, Hq * DH * 2, L * Hq * DH * 2};
+        const cuuint32_t box[4] = {64, GQ, CT, 1};
+        if (!make_map(&mq, a.q, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {DH, Hkv, L, B};
+        const cuuint64_t str[3] = {DH * 2, Hkv * DH * 2, L * Hkv * DH * 2};
+        const cuuint32_t box[4] = {64, 1, CT, 1};
+        if (!make_map(&mk, a.k, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!make_map(&mv, a.v, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {DF / 2, DH, Hkv};
+        const cuuint64_t str[2] = {(DF / 2) * 2, DH * (DF / 2) * 2};
+        const cuuint32_t box[3] = {DF / 2, DH, 1};
+        if (!make_map(&mw, a.Wf, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e;
+    e = cudaFuncSetAttribute(fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)kSmemBytes);
+    if (e != cudaSuccess) return e;
+    const unsigned U = (unsigned)(p.B * p.Hkv);
+    if (p.P > 1) {
+        fwd_tc_kernel<false><<<dim3(U, (unsigned)(p.P - 1)), NT, kSmemBytes, s>>>(mq, mk, mv, mw,
+                                                                                 p, a);
+        e = launch_seg_scan(p, a.seg, s);
+        if (e != cudaSuccess) return e;
+    }
+    if (a.ev_before) cudaEventRecord(a.ev_before, s);
+    fwd_tc_kernel<true><<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, p, a);
+    if (a.ev_after) cudaEventRecord(a.ev_after, s);
+    return cudaGetLastError();
 }
 
 }  // namespace lz

@@ -26,6 +26,9 @@ struct Plan {
 };
 
 bool make_plan(const lizard_dims* dims, Plan* p);
+// Re-cut the segments for a kernel that wants about `target` (unit, segment) CTAs;
+// never more than Pmax segments, so the workspace size stays valid.
+void plan_segments(Plan* p, int64_t target);
 size_t fwd_workspace_bytes(const Plan& p);
 
 struct FwdArgs {
@@ -41,6 +44,10 @@ struct FwdArgs {
 };
 
 cudaError_t launch_fwd_simt(const Plan& p, const FwdArgs& a, cudaStream_t s);
+// Segment-start states only (segment pass + scan into a.seg), for the backward.
+cudaError_t launch_fwd_states(const Plan& p, const FwdArgs& a, cudaStream_t s);
+// fp32 exclusive scan over the segment records (in place).
+cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s);
 bool fwd_tc_supported(const Plan& p);
 cudaError_t launch_fwd_tc(const Plan& p, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_ring_fill(const Plan& p, const void* k, const void* v, void* kc, void* vc,

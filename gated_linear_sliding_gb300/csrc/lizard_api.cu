@@ -36,11 +36,19 @@ bool make_plan(const lizard_dims* dims, Plan* p) {
     if (pmax < 1) pmax = 1;
     if (pmax > 64) pmax = 64;
     p->Pmax = pmax;
-    p->seg_chunks = (p->nchunks + pmax - 1) / pmax;
+    p->rec_floats = (size_t)(d.D * d.d + 2 * d.D);
+    plan_segments(p, kTargetUnits);
+    return true;
+}
+
+void plan_segments(Plan* p, int64_t target) {
+    const int64_t U = p->B * p->Hkv;
+    int64_t want = (target + U - 1) / U;
+    if (want < 1) want = 1;
+    if (want > p->Pmax) want = p->Pmax;
+    p->seg_chunks = (p->nchunks + want - 1) / want;
     p->seg_len = p->seg_chunks * kChunk;
     p->P = (p->nchunks + p->seg_chunks - 1) / p->seg_chunks;
-    p->rec_floats = (size_t)(d.D * d.d + 2 * d.D);
-    return true;
 }
 
 static bool shapes_compiled(const Plan& p) {
@@ -92,6 +100,12 @@ size_t lizard_attn_fwd_workspace(const lizard_dims* dims) {
     Plan p;
     if (!make_plan(dims, &p)) return 0;
     return fwd_workspace_bytes(p);
+}
+
+int lizard_attn_fwd_kernel(const lizard_dims* dims) {
+    Plan p;
+    if (!make_plan(dims, &p)) return -1;
+    return fwd_tc_supported(p) ? 1 : 0;
 }
 
 lizard_status lizard_workspace_init(void* workspace, size_t ws_bytes, void* stream) {

@@ -26,7 +26,8 @@ LIZARD_BF16 = 1
 EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_fwd",
             "lizard_attn_bwd_workspace", "lizard_attn_bwd", "lizard_decode_workspace",
             "lizard_decode_step", "lizard_read_device_status", "lizard_status_string",
-            "lizard_profile_events", "lizard_version"]
+            "lizard_profile_events", "lizard_version",
+            "lizard_attn_fwd_kernel"]
 
 
 class lizard_dims(ctypes.Structure):
@@ -63,6 +64,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_attn_bwd_workspace.restype = ctypes.c_size_t
     lib.lizard_decode_workspace.argtypes = [_DP]
     lib.lizard_decode_workspace.restype = ctypes.c_size_t
+    lib.lizard_attn_fwd_kernel.argtypes = [_DP]
+    lib.lizard_attn_fwd_kernel.restype = ctypes.c_int
     lib.lizard_workspace_init.argtypes = [_VP, ctypes.c_size_t, _VP]
     lib.lizard_workspace_init.restype = ctypes.c_int
     lib.lizard_attn_fwd.argtypes = [_DP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
@@ -140,6 +143,11 @@ def _need(t, name, shape, dtype):
 
 def lizard_attn_fwd_workspace(dims: lizard_dims) -> int:
     return int(load().lizard_attn_fwd_workspace(ctypes.byref(dims)))
+
+
+def lizard_attn_fwd_kernel(dims: lizard_dims) -> int:
+    """1 if the tensor-core chunk walk serves these sizes, 0 for the SIMT walk, -1 invalid."""
+    return int(load().lizard_attn_fwd_kernel(ctypes.byref(dims)))
 
 
 def lizard_attn_bwd_workspace(dims: lizard_dims) -> int:

@@ -77,6 +77,11 @@ typedef struct {
  * memory).  Returns 0 for invalid dims. */
 size_t lizard_attn_fwd_workspace(const lizard_dims* dims);
 
+/* Which forward kernel serves these sizes: 1 = the tensor-core (tcgen05) chunk walk
+ * (bf16, d = D = 128, Hq = 4 Hkv, w = 64), 0 = the SIMT walk (fp32 and every other
+ * shape), -1 = invalid sizes.  Pure host query. */
+int lizard_attn_fwd_kernel(const lizard_dims* dims);
+
 /* Zero the device status word at the head of a workspace (async on stream).
  * Call once after allocating a workspace; kernels only ever set the word. */
 lizard_status lizard_workspace_init(void* workspace, size_t ws_bytes, void* stream);
@@ -95,7 +100,9 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
                               void* y, float* lse, float* S_out, float* z_out, void* kcache_out,
                               void* vcache_out, void* workspace, size_t ws_bytes, void* stream);
 
-/* Bytes of device workspace lizard_attn_bwd needs (independent of L). */
+/* Bytes of device workspace lizard_attn_bwd needs: segment records whose size depends on
+ * B, Hkv, d and D only, plus one fp32 per gate element (B * L * Hkv * D * 4 bytes) holding
+ * the per-position gate gradient before its reverse cumulative sum. */
 size_t lizard_attn_bwd_workspace(const lizard_dims* dims);
 
 /* Exact gradient of lizard_attn_fwd's y against an upstream gradient dy.  The

@@ -1,0 +1,113 @@
+"""Backward parity: lizard_attn_bwd (through the C ABI) against the float64 oracle's exact
+reverse pass (itself pinned by central finite differences).  The pages give no backward;
+the reference is the adjoint of the forward definition (Lizard summary,
+gist.science 2507.09025, sec. 2-A and 2-C)."""
+import numpy as np
+import pytest
+
+from gated_linear_sliding_gb300 import inputs as I
+from helpers import assert_grad, to_dev, to_np
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def lz():
+    from gated_linear_sliding_gb300 import lizard
+
+    lizard.load()
+    return lizard
+
+
+def gpu_fwd_bwd(lz, inp, wl):
+    t = to_dev(inp, wl.dtype)
+    B, L, Hq, d = inp["q"].shape
+    lse = torch.empty(B, L, Hq, dtype=torch.float32, device="cuda")
+    y = lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w, lse=lse)
+    g = lz.lizard_attn_bwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], y, lse, t["dy"],
+                           wl.w)
+    torch.cuda.synchronize()
+    return {n: to_np(v) for n, v in g.items()}
+
+
+def check(out, ref, dtype, names=("dq", "dk", "dv", "dg", "dWf", "dsinks")):
+    for n in names:
+        assert_grad(out[n], ref[n], dtype, n)
+
+
+@pytest.mark.parametrize("L,w", [(100, 8), (300, 32), (40, 64), (257, 5)])
+def test_bwd_f32_small(lz, oracle_mod, L, w):
+    wl = I.TINY_F32.replace(L=L, w=w, B=2, Hq=4, Hkv=2)
+    inp = I.make_inputs(wl, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "f32")
+
+
+def test_bwd_f32_tiny_workload(lz, oracle_mod):
+    wl = I.TINY_F32
+    inp = I.make_inputs(wl, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "f32")
+
+
+def test_bwd_f32_gla_sensitive(lz, oracle_mod):
+    wl = I.gla_sensitive(I.TINY_F32.replace(L=400, Hq=4, Hkv=2, w=16))
+    inp = I.make_inputs(wl, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w,
+                         scale=wl.scale)
+    out = gpu_fwd_bwd(lz, inp, wl)
+    check(out, ref, "f32")
+    assert np.abs(ref["dg"]).max() > 1e-3  # the state carries gradient here
+
+
+@pytest.mark.parametrize("d,D,G", [(128, 64, 2), (64, 128, 8)])
+def test_bwd_f32_shapes(lz, oracle_mod, d, D, G):
+    wl = I.TINY_F32.replace(L=200, d=d, D=D, Hkv=2, Hq=2 * G, w=16)
+    inp = I.make_inputs(wl, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "f32")
+
+
+def test_bwd_mistral_shape_reduced(lz, oracle_mod):
+    wl = I.MISTRAL_7B_TRAIN
+    inp = I.make_inputs(wl, L=512, B=2, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16")
+
+
+def test_bwd_mistral_gla_sensitive(lz, oracle_mod):
+    wl = I.gla_sensitive(I.MISTRAL_7B_TRAIN)
+    inp = I.make_inputs(wl, L=640, B=1, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w,
+                         scale=wl.scale)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16")
+
+
+def test_bwd_mistral_full_sampled_batch(lz, oracle_mod):
+    """B=8, L=2048: the GPU runs the whole batch; the oracle checks two sequences (the
+    batch entries are independent, except dWf and dsinks, which sum over the batch and are
+    checked against the oracle over the same two sequences run alone)."""
+    wl = I.MISTRAL_7B_TRAIN
+    inp = I.make_inputs(wl, with_dy=True)
+    out = gpu_fwd_bwd(lz, inp, wl)
+    for b in (0, 5):
+        sub = {n: (a[b:b + 1] if n in ("q", "k", "v", "g", "dy") else a) for n, a in inp.items()}
+        ref = oracle_mod.bwd(**{n: a for n, a in sub.items() if n != "dy"}, dy=sub["dy"], w=wl.w)
+        for n in ("dq", "dk", "dv", "dg"):
+            assert_grad(out[n][b:b + 1], ref[n], "bf16", f"{n} b{b}")
+    sub = {n: (a[[0, 5]] if n in ("q", "k", "v", "g", "dy") else a) for n, a in inp.items()}
+    sub_out = gpu_fwd_bwd(lz, sub, wl)
+    ref = oracle_mod.bwd(**{n: a for n, a in sub.items() if n != "dy"}, dy=sub["dy"], w=wl.w)
+    assert_grad(sub_out["dWf"], ref["dWf"], "bf16", "dWf")
+    assert_grad(sub_out["dsinks"], ref["dsinks"], "bf16", "dsinks")
+
+
+def test_bwd_deterministic(lz):
+    wl = I.MISTRAL_7B_TRAIN
+    inp = I.make_inputs(wl, L=700, B=2, with_dy=True)
+    a = gpu_fwd_bwd(lz, inp, wl)
+    b = gpu_fwd_bwd(lz, inp, wl)
+    for n in a:
+        np.testing.assert_array_equal(a[n], b[n], err_msg=n)
