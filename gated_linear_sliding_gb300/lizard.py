@@ -26,7 +26,7 @@ LIZARD_BF16 = 1
 EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_fwd",
             "lizard_attn_bwd_workspace", "lizard_attn_bwd", "lizard_decode_workspace",
             "lizard_decode_step", "lizard_read_device_status", "lizard_status_string",
-            "lizard_profile_events", "lizard_version",
+            "lizard_profile_events", "lizard_version", "lizard_attn_fwd_noalloc",
             "lizard_attn_fwd_kernel"]
 
 
@@ -70,6 +70,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_workspace_init.restype = ctypes.c_int
     lib.lizard_attn_fwd.argtypes = [_DP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_fwd.restype = ctypes.c_int
+    lib.lizard_attn_fwd_noalloc.argtypes = [_DP] + [_VP] * 13
+    lib.lizard_attn_fwd_noalloc.restype = ctypes.c_int
     lib.lizard_attn_bwd.argtypes = [_DP] + [_VP] * 16 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_bwd.restype = ctypes.c_int
     lib.lizard_decode_step.argtypes = [_DP, ctypes.c_int64] + [_VP] * 12 + [ctypes.c_size_t, _VP]
@@ -216,6 +218,34 @@ def lizard_attn_fwd(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0, y=None
                                 _p(vcache_out), _p(workspace), workspace.numel(),
                                 _stream(stream))
     _check(st, "lizard_attn_fwd")
+    return y
+
+
+def lizard_attn_fwd_noalloc(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0, y=None,
+                            lse=None, S_out=None, z_out=None, kcache_out=None, vcache_out=None,
+                            stream=None):
+    """The forward without a workspace, for callers that cannot allocate device memory.
+
+    Same arguments and result as lizard_attn_fwd; the library keeps the scratch in a
+    fixed 32 MiB device array (see include/lizard.h for the limit and the sharing rules).
+    `y` is allocated here only for the Python caller's convenience when not given."""
+    B, L, Hq, d = q.shape
+    Hkv, D, M = k.shape[2], g.shape[-1], sinks.shape[1]
+    dt = q.dtype
+    _need(q, "q", (B, L, Hq, d), dt)
+    _need(k, "k", (B, L, Hkv, d), dt)
+    _need(v, "v", (B, L, Hkv, d), dt)
+    _need(g, "g", (B, L, Hkv, D), dt)
+    _need(Wf, "Wf", (Hkv, d, D // 2), dt)
+    _need(sinks, "sinks", (Hq, M), torch.float32)
+    if y is None:
+        y = torch.empty_like(q)
+    _need(y, "y", (B, L, Hq, d), dt)
+    dims = dims_of(q, k, g, sinks, w, scale)
+    st = load().lizard_attn_fwd_noalloc(ctypes.byref(dims), _p(q), _p(k), _p(v), _p(g), _p(Wf),
+                                        _p(sinks), _p(y), _p(lse), _p(S_out), _p(z_out),
+                                        _p(kcache_out), _p(vcache_out), _stream(stream))
+    _check(st, "lizard_attn_fwd_noalloc")
     return y
 
 

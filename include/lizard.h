@@ -100,6 +100,32 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
                               void* y, float* lse, float* S_out, float* z_out, void* kcache_out,
                               void* vcache_out, void* workspace, size_t ws_bytes, void* stream);
 
+/* The forward for callers that cannot allocate device memory.  The Lizard pages have
+ * no counterpart to this entry point; it exists for the integration.
+ *
+ * Some callers hold only pointers to their inputs and outputs: a plugin handed tensors
+ * by a host framework that owns every device allocation, or a latency-critical loop that
+ * must not call cudaMalloc/cudaFree because those can synchronise the whole device.  This
+ * call takes no workspace.  It computes exactly what lizard_attn_fwd computes, with the
+ * same arguments minus the workspace, and allocates nothing: its scratch (the status
+ * word and the per-segment boundary states) is one 32 MiB array in device memory that
+ * the library defines at file scope, so every GPU that loads the library holds those
+ * 32 MiB until the process exits.
+ *   - A problem whose scratch exceeds 32 MiB (256 bytes plus, when the sequence is cut
+ *     into P > 1 segments, P * B * Hkv * (D*d + 2*D) * 4 bytes) is rejected with
+ *     LIZARD_ERR_WORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current) and caches it; make that first call before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents (each call
+ *     clears the status word on `stream` before its kernels).  Calls whose work overlaps
+ *     on the GPU (different streams, or different host threads) race on the array:
+ *     order them on one stream. */
+lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const void* q, const void* k,
+                                      const void* v, const void* g, const void* Wf,
+                                      const float* sinks, void* y, float* lse, float* S_out,
+                                      float* z_out, void* kcache_out, void* vcache_out,
+                                      void* stream);
+
 /* Bytes of device workspace lizard_attn_bwd needs: segment records whose size depends on
  * B, Hkv, d and D only, plus one fp32 per gate element (B * L * Hkv * D * 4 bytes) holding
  * the per-position gate gradient before its reverse cumulative sum. */
