@@ -27,7 +27,7 @@ EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_f
             "lizard_attn_bwd_workspace", "lizard_attn_bwd", "lizard_decode_workspace",
             "lizard_decode_step", "lizard_read_device_status", "lizard_status_string",
             "lizard_profile_events", "lizard_version", "lizard_attn_fwd_noalloc",
-            "lizard_attn_fwd_kernel"]
+            "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout"]
 
 
 class lizard_dims(ctypes.Structure):
@@ -64,6 +64,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_attn_bwd_workspace.restype = ctypes.c_size_t
     lib.lizard_decode_workspace.argtypes = [_DP]
     lib.lizard_decode_workspace.restype = ctypes.c_size_t
+    lib.lizard_selftest_wait_timeout.argtypes = [_VP, ctypes.c_size_t, ctypes.c_longlong, _VP]
+    lib.lizard_selftest_wait_timeout.restype = ctypes.c_int
     lib.lizard_attn_fwd_kernel.argtypes = [_DP]
     lib.lizard_attn_fwd_kernel.restype = ctypes.c_int
     lib.lizard_workspace_init.argtypes = [_VP, ctypes.c_size_t, _VP]
@@ -180,6 +182,12 @@ def lizard_profile_events(before=None, after=None):
             ev.record()  # torch creates the underlying cudaEvent_t on first record
         handles.append(ctypes.c_void_p(ev.cuda_event))
     _check(load().lizard_profile_events(*handles), "lizard_profile_events")
+
+
+def lizard_selftest_wait_timeout(workspace: torch.Tensor, limit_cycles: int, stream=None):
+    """Run the bounded-wait failure path once (see include/lizard.h)."""
+    _check(load().lizard_selftest_wait_timeout(_p(workspace), workspace.numel(), int(limit_cycles),
+                                               _stream(stream)), "lizard_selftest_wait_timeout")
 
 
 def lizard_read_device_status(workspace: torch.Tensor, stream=None) -> int:

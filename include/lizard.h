@@ -165,6 +165,14 @@ lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const voi
  * Returns LIZARD_OK or the first error a kernel recorded (e.g. LIZARD_ERR_TIMEOUT). */
 lizard_status lizard_read_device_status(void* workspace, void* stream);
 
+/* Failure-path self-test: one CTA holds TMEM, waits on a barrier that never completes,
+ * gives up after limit_cycles SM cycles (at most 4e9, about two seconds) exactly like the
+ * tensor-core kernels' waits, records LIZARD_ERR_TIMEOUT in the workspace status word,
+ * frees its TMEM and returns.  No fault, no hang: the context stays usable.  Read the
+ * result with lizard_read_device_status. */
+lizard_status lizard_selftest_wait_timeout(void* workspace, size_t ws_bytes,
+                                           long long limit_cycles, void* stream);
+
 /* Static description of a status code. */
 const char* lizard_status_string(lizard_status s);
 
