@@ -8,28 +8,22 @@
 //      / [phi(q).z + sum_j e^{s q.k_j} + sum_m e^{t_m}],
 // with k_{pos-w}, v_{pos-w} and the window read from a (w+1)-slot ring cache.
 //
-// The step is bound by HBM traffic on the fp32 state (read and write of D x d x 4
-// bytes per (batch, KV head)).  Each (batch, KV head) unit is one cluster of NS CTAs;
-// CTA r owns columns [r d/NS, (r+1) d/NS) of S, of the value window and of the
-// outputs.  At entry every thread issues its share of all loads at once (state slice
-// into registers; Wf, the key window, the value slice, the token and z into shared
-// memory with cp.async), so the CTA pays one memory latency, then computes from
-// on-chip data.  Every CTA reads the old z, so the cluster barrier orders those
-// reads before CTA 0 writes the new z.
-#include <cooperative_groups.h>
+// The step is bound by HBM traffic on the fp32 state (read and write of D x d x 4 bytes
+// per (batch, KV head)).  One CTA owns one (batch, KV head) unit: at entry every thread
+// issues its share of all loads at once (its slice of the state into registers; Wf, the
+// key and value windows, the token and z into shared memory with cp.async), so the CTA
+// pays one memory latency, then computes the feature maps, the state update and readout,
+// the window softmax and the outputs from on-chip data, and writes the state back.
 #include <math.h>
 
 #include "common.cuh"
 #include "internal.h"
 
-namespace cg = cooperative_groups;
-
 namespace lz {
 namespace {
 
 constexpr int NT = 256;
-constexpr int NS = 4;      // CTAs (column slices) per unit = cluster size
-constexpr int GMAX = 8;    // query heads per KV head
+constexpr int GMAX = 8;  // query heads per KV head
 
 __device__ __forceinline__ void cp16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
@@ -43,39 +37,32 @@ __device__ __forceinline__ void cp_wait_all() {
 
 template <typename T, int DH, int DF, int WMAX>
 struct DecLay {
-    static constexpr int CW = DH / NS;        // columns per CTA
-    static constexpr int NRG = NT / CW;       // row groups of the state slice
+    static constexpr int NRG = NT / DH;       // row groups of the state
     static constexpr int RPT = DF / NRG;      // state rows per thread
     static constexpr int E = (int)sizeof(T);  // bytes per element
     static constexpr int KROW = DH * E + 16;  // padded key row (bytes)
     // byte offsets of the dynamic shared memory
-    static constexpr int oW = 0;                              // Wf [DH][DF/2]
-    static constexpr int oK = oW + DH * (DF / 2) * E;         // key window [WMAX][KROW]
-    static constexpr int oV = oK + WMAX * KROW;               // value slice [WMAX][CW]
-    static constexpr int oQ = oV + WMAX * CW * E;             // raw q rows, k_{pos-w} [G+1][DH]
-    static constexpr int oVE = oQ + (GMAX + 1) * DH * E;      // v_{pos-w} slice [CW]
-    static constexpr int oG = oVE + ((CW * E + 15) / 16) * 16;  // gate logits [DF]
-    static constexpr int oZ = oG + ((DF * E + 15) / 16) * 16;   // old z [DF] fp32
-    static constexpr int oX = oZ + DF * 4;                    // fp32 rows [G+1][DH]
-    static constexpr int oPhi = oX + (GMAX + 1) * DH * 4;     // phi rows [G+1][DF]
-    static constexpr int oU = oPhi + (GMAX + 1) * DF * 4;     // u rows [G+1][DF/2]
-    static constexpr int oGam = oU + (GMAX + 1) * (DF / 2) * 4;
-    static constexpr int oS = oGam + DF * 4;                  // window scores [G][WMAX]
-    static constexpr int oRed = oS + GMAX * WMAX * 4;         // readout partials [NRG][G][CW]
-    static constexpr int oRow = oRed + NRG * GMAX * CW * 4;   // per head m, l, den_gla, sinks
+    static constexpr int oW = 0;                                 // Wf [DH][DF/2]
+    static constexpr int oK = oW + DH * (DF / 2) * E;            // key window [WMAX][KROW]
+    static constexpr int oV = oK + WMAX * KROW;                  // value window [WMAX][DH]
+    static constexpr int oQ = oV + WMAX * DH * E;                // q rows, k_{pos-w} [G+1][DH]
+    static constexpr int oVE = oQ + (GMAX + 1) * DH * E;         // v_{pos-w} [DH]
+    static constexpr int oG = oVE + ((DH * E + 15) / 16) * 16;   // gate logits [DF]
+    static constexpr int oZ = oG + ((DF * E + 15) / 16) * 16;    // old z [DF] fp32
+    static constexpr int oX = oZ + DF * 4;                       // fp32 rows [G+1][DH]
+    static constexpr int oPhi = oX + (GMAX + 1) * DH * 4;        // phi rows [G+1][DF]
+    static constexpr int oU = oPhi + (GMAX + 1) * DF * 4;        // u rows [G+1][DF/2]
+    static constexpr int oGam = oU + (GMAX + 1) * (DF / 2) * 4;  // gates [DF]
+    static constexpr int oS = oGam + DF * 4;                     // window scores [G][WMAX]
+    static constexpr int oRed = oS + GMAX * WMAX * 4;            // partials [NRG][G][DH]
+    static constexpr int oRow = oRed + NRG * GMAX * DH * 4;      // per head m, l, den_gla, sinks
     static constexpr int bytes = oRow + GMAX * 4 * 4;
 };
 
-template <typename T>
-__device__ __forceinline__ float ldv(const T* p, int i) {
-    return ld(p + i);
-}
-
 template <typename T, int DH, int DF, int WMAX>
-__global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
-    decode_kernel(Plan p, DecodeArgs a) {
+__global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
     using Ly = DecLay<T, DH, DF, WMAX>;
-    constexpr int CW = Ly::CW, NRG = Ly::NRG, RPT = Ly::RPT, E = Ly::E, H2 = DF / 2;
+    constexpr int NRG = Ly::NRG, RPT = Ly::RPT, E = Ly::E, H2 = DF / 2;
     extern __shared__ __align__(16) unsigned char sm[];
     T* sW = (T*)(sm + Ly::oW);
     T* sQ = (T*)(sm + Ly::oQ);
@@ -90,14 +77,12 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     float* sRed = (float*)(sm + Ly::oRed);
     float* sRow = (float*)(sm + Ly::oRow);
 
-    cg::cluster_group cluster = cg::this_cluster();
-    const int sl = (int)cluster.block_rank();
-    const int64_t unit = blockIdx.x / NS;
+    const int64_t unit = blockIdx.x;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
     const int G = (int)p.G;
     const int64_t w = p.w, R = w + 1, pos = a.pos;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = tid % CW, rg = tid / CW, c0 = sl * CW;
+    const int c = tid % DH, rg = tid / DH;
     const bool admit = pos >= w;
     const int64_t nkeys = min64(w, pos + 1);
     const int64_t jstart = pos - nkeys + 1;
@@ -106,37 +91,34 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     const T* knew = (const T*)a.k + unit * DH;
     const T* vnew = (const T*)a.v + unit * DH;
 
-    // 1. issue every load: state slice to registers, the rest to shared memory
+    // 1. issue every load: the state rows of this thread to registers, the rest to shared memory
     float* Sg = a.S + unit * DF * DH;
     float sreg[RPT];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) sreg[i] = Sg[(rg + NRG * i) * DH + c0 + c];
+    for (int i = 0; i < RPT; ++i) sreg[i] = Sg[(rg + NRG * i) * DH + c];
     {
         const T* Wk = (const T*)a.Wf + kv * DH * H2;
         constexpr int nW = DH * H2 * E / 16;
         for (int e = tid; e < nW; e += NT) cp16((char*)sW + 16 * e, (const char*)Wk + 16 * e);
-        constexpr int cpr = DH * E / 16;  // 16-byte chunks per key row
+        constexpr int cpr = DH * E / 16;  // 16-byte chunks per row
         for (int e = tid; e < nkeys * cpr; e += NT) {
             const int64_t jj = e / cpr, ch = e % cpr;
             const int64_t j = jstart + jj;
-            const T* src = (j == pos) ? knew : kc + (unit * R + j % R) * DH;
-            cp16(sm + Ly::oK + jj * Ly::KROW + 16 * ch, (const char*)src + 16 * ch);
-        }
-        constexpr int cpv = CW * E / 16;  // chunks per value-slice row
-        for (int e = tid; e < nkeys * cpv; e += NT) {
-            const int64_t jj = e / cpv, ch = e % cpv;
-            const int64_t j = jstart + jj;
-            const T* src = (j == pos) ? vnew : vc + (unit * R + j % R) * DH;
-            cp16(sm + Ly::oV + (jj * CW) * E + 16 * ch, (const char*)(src + c0) + 16 * ch);
+            const bool cur = j == pos;
+            const T* ks = cur ? knew : kc + (unit * R + j % R) * DH;
+            const T* vs = cur ? vnew : vc + (unit * R + j % R) * DH;
+            cp16(sm + Ly::oK + jj * Ly::KROW + 16 * ch, (const char*)ks + 16 * ch);
+            cp16(sm + Ly::oV + jj * DH * E + 16 * ch, (const char*)vs + 16 * ch);
         }
         const T* qrow = (const T*)a.q + (b * p.Hq + kv * G) * DH;
         for (int e = tid; e < G * cpr; e += NT) cp16((char*)sQ + 16 * e, (const char*)qrow + 16 * e);
         if (admit) {
             const T* ke = kc + (unit * R + (pos - w) % R) * DH;
-            const T* ve = vc + (unit * R + (pos - w) % R) * DH + c0;
-            for (int e = tid; e < cpr; e += NT)
+            const T* ve = vc + (unit * R + (pos - w) % R) * DH;
+            for (int e = tid; e < cpr; e += NT) {
                 cp16((char*)(sQ + G * DH) + 16 * e, (const char*)ke + 16 * e);
-            for (int e = tid; e < cpv; e += NT) cp16((char*)sVE + 16 * e, (const char*)ve + 16 * e);
+                cp16((char*)sVE + 16 * e, (const char*)ve + 16 * e);
+            }
         }
         const T* gr = (const T*)a.g + unit * DF;
         for (int e = tid; e < DF * E / 16; e += NT) cp16((char*)sG + 16 * e, (const char*)gr + 16 * e);
@@ -145,8 +127,6 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     }
     cp_wait_all();
     __syncthreads();
-    // every CTA of the cluster has read the old z before CTA 0 may overwrite it
-    cluster.sync();
 
     // 2. token rows to fp32, gates
     for (int e = tid; e < (G + 1) * DH; e += NT) {
@@ -156,18 +136,35 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     for (int f = tid; f < DF; f += NT) sGam[f] = sigmoidf_(ld(sG + f));
     __syncthreads();
 
-    // 3. u = x Wf for the G query rows and the admitted key: 4 threads per output
-    for (int r = 0; r <= G; ++r) {
-        for (int o = tid; o < H2 * 4; o += NT) {
-            const int f = o >> 2, part = o & 3;
-            float acc = 0.0f;
-            const float* x = sX + r * DH;
-#pragma unroll 8
-            for (int cc = part * (DH / 4); cc < (part + 1) * (DH / 4); ++cc)
-                acc = fmaf(x[cc], ld(sW + cc * H2 + f), acc);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-            if (part == 0) sU[r * H2 + f] = acc;
+    // 3. u = x Wf for the G query rows and the admitted key.  Lanes run over features, so a
+    //    warp reads one contiguous row of Wf per column cc; the NQ thread groups split cc and
+    //    their partial sums are added in a fixed order.
+    {
+        constexpr int NQ = NT / H2, CQ = DH / NQ;
+        const int f = tid % H2, qd = tid / H2;
+        float acc[GMAX + 1];
+#pragma unroll
+        for (int r = 0; r <= GMAX; ++r) acc[r] = 0.0f;
+        for (int cc = qd * CQ; cc < (qd + 1) * CQ; ++cc) {
+            const float wv = ld(sW + cc * H2 + f);
+#pragma unroll
+            for (int r = 0; r <= GMAX; ++r)
+                if (r <= G) acc[r] = fmaf(sX[r * DH + cc], wv, acc[r]);
+        }
+        // partials [NQ][G+1][H2] in the score and readout-partial buffers (contiguous, both
+        // unused until step 4)
+        static_assert(GMAX * WMAX + NRG * GMAX * DH >= (GMAX + 1) * NT, "partials fit");
+        static_assert(Ly::oRed == Ly::oS + GMAX * WMAX * 4, "contiguous");
+        float* sUp = sS;
+#pragma unroll
+        for (int r = 0; r <= GMAX; ++r)
+            if (r <= G) sUp[(qd * (G + 1) + r) * H2 + f] = acc[r];
+        __syncthreads();
+        for (int e = tid; e < (G + 1) * H2; e += NT) {
+            float u = 0.0f;
+#pragma unroll
+            for (int q2 = 0; q2 < NQ; ++q2) u += sUp[q2 * (G + 1) * H2 + e];
+            sU[e] = u;
         }
     }
     __syncthreads();
@@ -210,36 +207,43 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     }
     __syncthreads();
 
-    // 4. state update of this slice (in place) and partial readouts phi(q).S
+    // 4. state update (this thread's rows of column c) and partial readouts phi(q).S
     const float ve = admit ? ld(sVE + c) : 0.0f;
 #pragma unroll
     for (int i = 0; i < RPT; ++i) {
         const int f = rg + NRG * i;
-        const float sv = fmaf(sGam[f], sreg[i], sPhi[G * DF + f] * ve);
-        sreg[i] = sv;
-        Sg[f * DH + c0 + c] = sv;
+        sreg[i] = fmaf(sGam[f], sreg[i], sPhi[G * DF + f] * ve);
     }
     for (int hh = 0; hh < G; ++hh) {
         float part = 0.0f;
 #pragma unroll
         for (int i = 0; i < RPT; ++i) part = fmaf(sPhi[hh * DF + rg + NRG * i], sreg[i], part);
-        sRed[(rg * G + hh) * CW + c] = part;
+        sRed[(rg * G + hh) * DH + c] = part;
     }
-    // new z (this CTA's copy in shared memory; CTA 0 writes it back)
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) Sg[(rg + NRG * i) * DH + c] = sreg[i];
+    // new z (written back by the CTA, which owns the unit)
     for (int f = tid; f < DF; f += NT) {
         const float zn = fmaf(sGam[f], sZ[f], sPhi[G * DF + f]);
         sZ[f] = zn;
-        if (sl == 0) a.z[unit * DF + f] = zn;
+        a.z[unit * DF + f] = zn;
     }
 
-    // 5. window scores s_hj = scale q_h.k_j from the staged key rows
+    // 5. window scores s_hj = scale q_h.k_j: one key per lane, 16-byte reads of the padded
+    //    key rows (consecutive lanes land in distinct bank groups), q broadcast
     for (int e = tid; e < G * nkeys; e += NT) {
         const int hh = e / (int)nkeys, jj = e % (int)nkeys;
-        const T* kr = (const T*)(sm + Ly::oK + jj * Ly::KROW);
+        const unsigned char* kr = sm + Ly::oK + jj * Ly::KROW;
         const float* x = sX + hh * DH;
         float acc = 0.0f;
-#pragma unroll 8
-        for (int cc = 0; cc < DH; ++cc) acc = fmaf(x[cc], ld(kr + cc), acc);
+        constexpr int EPC = 16 / E;  // elements per 16-byte chunk
+#pragma unroll 4
+        for (int ch = 0; ch < DH / EPC; ++ch) {
+            const uint4 wv = *reinterpret_cast<const uint4*>(kr + 16 * ch);
+            const T* kv8 = reinterpret_cast<const T*>(&wv);
+#pragma unroll
+            for (int e2 = 0; e2 < EPC; ++e2) acc = fmaf(x[ch * EPC + e2], ld(kv8 + e2), acc);
+        }
         sS[hh * WMAX + jj] = acc * p.scale;
     }
     __syncthreads();
@@ -276,28 +280,28 @@ __global__ void __cluster_dims__(NS, 1, 1) __launch_bounds__(NT)
     }
     __syncthreads();
 
-    // 7. outputs of this slice's columns
+    // 7. outputs
     const T* sV = (const T*)(sm + Ly::oV);
-    for (int e = tid; e < G * CW; e += NT) {
-        const int hh = e / CW, cc = e % CW;
+    for (int e = tid; e < G * DH; e += NT) {
+        const int hh = e / DH, cc = e % DH;
         float num = 0.0f;
 #pragma unroll
-        for (int r2 = 0; r2 < NRG; ++r2) num += sRed[(r2 * G + hh) * CW + cc];
+        for (int r2 = 0; r2 < NRG; ++r2) num += sRed[(r2 * G + hh) * DH + cc];
         float wv = 0.0f;
-        for (int jj = 0; jj < nkeys; ++jj) wv = fmaf(sS[hh * WMAX + jj], ld(sV + jj * CW + cc), wv);
+        for (int jj = 0; jj < nkeys; ++jj) wv = fmaf(sS[hh * WMAX + jj], ld(sV + jj * DH + cc), wv);
         const float m = sRow[hh * 4 + 0];
         const float Em = expf(-m);
         const float den = Em * sRow[hh * 4 + 2] + sRow[hh * 4 + 1] + sRow[hh * 4 + 3];
-        st((T*)a.y + (b * p.Hq + kv * G + hh) * DH + c0 + cc, (Em * num + wv) / den);
+        st((T*)a.y + (b * p.Hq + kv * G + hh) * DH + cc, (Em * num + wv) / den);
     }
 
     // 8. the new token joins the ring (slot pos mod (w+1), never read in this step)
     T* kco = (T*)a.kc;
     T* vco = (T*)a.vc;
-    for (int cc = tid; cc < CW; cc += NT) {
-        const int64_t dst = (unit * R + pos % R) * DH + c0 + cc;
-        kco[dst] = knew[c0 + cc];
-        vco[dst] = vnew[c0 + cc];
+    for (int cc = tid; cc < DH; cc += NT) {
+        const int64_t dst = (unit * R + pos % R) * DH + cc;
+        kco[dst] = knew[cc];
+        vco[dst] = vnew[cc];
     }
 }
 
@@ -307,8 +311,7 @@ cudaError_t launch_w(const Plan& p, const DecodeArgs& a, cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, DH, DF, WMAX>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Ly::bytes);
     if (e != cudaSuccess) return e;
-    const unsigned grid = (unsigned)(p.B * p.Hkv * NS);
-    decode_kernel<T, DH, DF, WMAX><<<grid, NT, Ly::bytes, s>>>(p, a);
+    decode_kernel<T, DH, DF, WMAX><<<(unsigned)(p.B * p.Hkv), NT, Ly::bytes, s>>>(p, a);
     return cudaGetLastError();
 }
 

@@ -41,7 +41,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int NT = 256;   // 8 warps: warp w owns TMEM lanes 32(w%4).. ; w/4 picks a column half
+constexpr int NT = 512;   // 16 warps: warp w owns TMEM lanes 32(w%4).., w/4 picks a 32-column part
 constexpr int CT = 32;    // tokens per step
 constexpr int GQ = 4;     // query heads per KV head
 constexpr int DH = 128;   // head dim
@@ -50,25 +50,26 @@ constexpr int WIN = 64;   // window
 constexpr int MMAX = 64;  // sinks per head
 constexpr long long kTimeout = 2000000000LL;  // SM cycles (about one second)
 
-// shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t oQ = 0;         // q tile, K-major [128 rows][128 d]; then P_win [128][128 keys]
-constexpr uint32_t oQt = 32768;    // q~, K-major [128 rows][128 features]
+// shared-memory map (bytes from a 1024-aligned base); later uses of a region in a step follow
+// the arrow
+constexpr uint32_t oQ = 0;         // q tile, K-major [128 rows][128 d] -> P_win [128][128 keys]
+constexpr uint32_t oQt = 32768;    // gate partial sums [4][128] fp32 -> q~, K-major [128][128]
 constexpr uint32_t oK = 65536;     // key ring: 4 slots x 32 keys, K-major over d
 constexpr uint32_t oV = 98304;     // value ring: same bytes, read MN-major (N = d)
 constexpr uint32_t oW = 131072;    // Wf [128 d rows][64 features], MN-major B
 constexpr uint32_t oHs = 147456;   // e^{r} (.) H in bf16, [128 feature rows][128 d], MN-major B
-constexpr uint32_t oKi = 180224;   // k~ (intra), K-major [32 keys][128 features]
-constexpr uint32_t oKu = 188416;   // k~ (state update), MN-major A, same byte layout
-constexpr uint32_t oE = 196608;    // Eq, Ek tables (bf16 [32][128] each); then P_intra
-constexpr uint32_t oSmall = 212992;
+constexpr uint32_t oKi = 180224;   // k~ (intra), K-major [32 keys][128] -> P_intra sums [4][128]
+constexpr uint32_t oKu = 188416;   // row exchange (max, u-extreme, u-sum) [3][4][128] -> k~ (update)
+constexpr uint32_t oE = 196608;    // Eq, Ek tables (bf16 [32][128] each) -> P_intra
+constexpr uint32_t oG = 212992;    // gate logits [32][128] bf16 -> staged U_k rows [32][64] fp32
+constexpr uint32_t oSmall = 221184;
 
 struct Small {
     uint64_t bar_tma, bar_mma;
     uint32_t tmem;
     volatile int abort;
-    float z[DF], zs[DF], eref[DF], elast[DF], cf[DF];
-    float m[128], den[128];
-    float pm[2][128], ps[2][128], pg[2][128];
+    float z[DF], zs[DF], cf[DF];
+    float ps[4][128], pg[4][128];  // per-part window and state denominators of each row
     float tmax[GQ];
     float sinks[GQ][MMAX];
 };
@@ -82,6 +83,11 @@ __device__ __forceinline__ float clamp80(float x) { return fminf(fmaxf(x, -80.0f
 
 __device__ __forceinline__ float bf16r(float x) {
     return __bfloat162float(__float2bfloat16_rn(x));
+}
+
+// log sigmoid(x) = min(x, 0) - log(1 + e^{-|x|}); the argument of the log is in (1, 2].
+__device__ __forceinline__ float log_sigmoid_fast(float x) {
+    return fminf(x, 0.0f) - __logf(1.0f + __expf(-fabsf(x)));
 }
 
 __device__ __forceinline__ void unpack8(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
@@ -109,6 +115,30 @@ __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t& ph, Small& S, 
     return S.abort == 0;
 }
 
+// One step's operands: key/value slot of chunk c, the gate tile (and the query tile).
+template <bool MAIN>
+__device__ __forceinline__ void issue_step_loads(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmQ,
+                                                 const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                                 const CUtensorMap* tmG, int64_t c, int64_t kv,
+                                                 int64_t b) {
+    const int slot = (int)(c & 3);
+    const int t0 = (int)(c * 32);
+    sm100::mbar_arrive_expect_tx(bar, MAIN ? 16384u + 8192u + 32768u : 16384u + 8192u);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb) {
+        sm100::tma_load_4d(sm + oK + kb * 16384 + slot * 4096, tmK, bar, 64 * kb, (int)kv, t0, (int)b);
+        sm100::tma_load_4d(sm + oV + kb * 16384 + slot * 4096, tmV, bar, 64 * kb, (int)kv, t0, (int)b);
+        if (MAIN)
+            sm100::tma_load_4d(sm + oQ + kb * 16384, tmQ, bar, 64 * kb, (int)(kv * 4), t0, (int)b);
+    }
+    sm100::tma_load_4d(sm + oG, tmG, bar, 0, (int)kv, t0, (int)b);
+}
+
+// Barrier among the 128 threads (4 warps) that share one TMEM lane quadrant.
+__device__ __forceinline__ void quad_sync(int quad) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + quad) : "memory");
+}
+
 // K-major (or MN-major) descriptor helpers for the 128-byte-swizzled tiles.
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) {
     return make_sdesc(addr, 16, 1024, kSwizzle128);
@@ -121,15 +151,21 @@ template <bool MAIN>
 __global__ void __launch_bounds__(NT, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmW,
-                  Plan p, FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmG, Plan p, FwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
     Small& S = *reinterpret_cast<Small*>(sm + oSmall);
+    float* gpart = reinterpret_cast<float*>(sm + oQt);       // [4][DF], gates phase only
+    float* xpm = reinterpret_cast<float*>(sm + oKu);         // [4][128] window partial max
+    float* xum = xpm + 512;                                   // [4][128] u partial extreme
+    float* xus = xpm + 1024;                                  // [4][128] u partial sum
+    float* spi = reinterpret_cast<float*>(sm + oKi);         // [4][128] P_intra partial sums
+    float* suk = reinterpret_cast<float*>(sm + oG);          // [32][64] staged U_k rows
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, half = warp >> 2;
+    const int quad = warp & 3, part = warp >> 2;
     const int row = 32 * quad + lane;
     const int64_t unit = blockIdx.x, seg = blockIdx.y;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
@@ -138,7 +174,6 @@ __global__ void __launch_bounds__(NT, 1)
     const int64_t s1 = min64(p.L, s0 + p.seg_len);
     WsHeader* hdr = (WsHeader*)a.header;
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
-    const __nv_bfloat16* gptr = (const __nv_bfloat16*)a.g;
 
     if (warp == 0) {
         tmem_alloc(&S.tmem, 512);
@@ -152,6 +187,7 @@ __global__ void __launch_bounds__(NT, 1)
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmW);
+        prefetch_tmap(&tmG);
         if (MAIN) prefetch_tmap(&tmQ);
     }
     if (MAIN) {
@@ -175,17 +211,20 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = S.tmem;
+    // operand descriptors at the tile bases; the start-address field (bits 0-13, in 16-byte
+    // units) advances by (byte offset >> 4) for each K step
+    const uint64_t dQ = kdesc(base + oQ), dQt = kdesc(base + oQt), dK = kdesc(base + oK),
+                   dKi = kdesc(base + oKi), dE = kdesc(base + oE);
+    const uint64_t dW = mndesc(base + oW, 16384), dHs = mndesc(base + oHs, 16384),
+                   dV = mndesc(base + oV, 16384), dKu = mndesc(base + oKu, 4096);
 
     // starting state H into TMEM (fp32 master copy), lane = feature f, column = d
     {
         float v[32];
+        const int col = 32 * part;
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int col = 64 * half + 32 * j;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + col + k] : 0.0f;
-            tmem_st32(tb + lane_off + cH + col, v);
-        }
+        for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + col + k] : 0.0f;
+        tmem_st32(tb + lane_off + cH + col, v);
         tmem_wait_st();
     }
 
@@ -213,109 +252,103 @@ __global__ void __launch_bounds__(NT, 1)
     tma_pending = true;
     ok = wait_bar(&S.bar_tma, ph_tma, S, hdr, 1);
     if (ok) tma_pending = false;
+    // the first step's operands; every later step's are issued at the end of the step before
+    if (ok && tid == 0 && c_begin < c_end)
+        issue_step_loads<MAIN>(sm, &S.bar_tma, &tmQ, &tmK, &tmV, &tmG, c_begin, kv, b);
+    tma_pending = c_begin < c_end;
 
     for (int64_t c = c_begin; ok && c < c_end; ++c) {
         const int64_t t0 = c * CT;
         const int n = (int)min64(CT, s1 - t0);
-        const int slot_c = (int)(c & 3), slot_d = (int)((c - 2) & 3);
+        const int slot_d = (int)((c - 2) & 3);
 
-        // (1) this step's keys, values (and queries) into the rings
-        if (tid == 0) {
-            mbar_arrive_expect_tx(&S.bar_tma, MAIN ? 16384u + 32768u : 16384u);
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                tma_load_4d(sm + oK + kb * 16384 + slot_c * 4096, &tmK, &S.bar_tma, 64 * kb,
-                            (int)kv, (int)t0, (int)b);
-                tma_load_4d(sm + oV + kb * 16384 + slot_c * 4096, &tmV, &S.bar_tma, 64 * kb,
-                            (int)kv, (int)t0, (int)b);
-                if (MAIN)
-                    tma_load_4d(sm + oQ + kb * 16384, &tmQ, &S.bar_tma, 64 * kb, (int)(kv * GQ),
-                                (int)t0, (int)b);
-            }
-        }
-        tma_pending = true;
-
-        // (2) gates: cumulative log-sigmoid per feature, decay tables around r = b_15
-        if (tid < DF) {
-            const int f = tid;
-            float bt[CT];
-            float run = 0.0f;
-#pragma unroll
-            for (int t = 0; t < CT; ++t) {
-                float lam = 0.0f;
-                if (t < n)
-                    lam = log_sigmoid<true>(
-                        __bfloat162float(gptr[((b * p.L + t0 + t) * p.Hkv + kv) * DF + f]));
-                run += lam;
-                bt[t] = run;
-            }
-            const float bref = bt[15], blast = bt[CT - 1];
-            __nv_bfloat16* Eq = (__nv_bfloat16*)(sm + oE);
-            __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + oE + 8192);
-#pragma unroll
-            for (int t = 0; t < CT; ++t) {
-                Eq[t * DF + f] = __float2bfloat16_rn(__expf(clamp80(bt[t] - bref)));
-                Ek[t * DF + f] = __float2bfloat16_rn(__expf(clamp80(bref - bt[t])));
-            }
-            const float er = __expf(bref);
-            S.eref[f] = er;
-            S.elast[f] = __expf(blast);
-            S.cf[f] = __expf(blast - bref);
-            S.zs[f] = er * S.z[f];
-            lam_tot += blast;
-        }
-        __syncthreads();
-
-        // (3) state: bf16 copy scaled by e^{r} for the readout; decay the master by e^{b_31}
-        {
-            const int f = row;
-            const float er = S.eref[f], el = S.elast[f];
-            float v[32];
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int col = 64 * half + 32 * j;
-                tmem_ld32(tb + lane_off + cH + col, v);
-                tmem_wait_ld();
-                if (MAIN) {
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const int nchunk = (col & 63) / 8 + ch;
-                        st_shared_v4(base + oHs + (col / 64) * 16384 + sw128(f, nchunk),
-                                     pack_bf16(er * v[8 * ch], er * v[8 * ch + 1]),
-                                     pack_bf16(er * v[8 * ch + 2], er * v[8 * ch + 3]),
-                                     pack_bf16(er * v[8 * ch + 4], er * v[8 * ch + 5]),
-                                     pack_bf16(er * v[8 * ch + 6], er * v[8 * ch + 7]));
-                    }
-                }
-#pragma unroll
-                for (int k = 0; k < 32; ++k) v[k] *= el;
-                tmem_st32(tb + lane_off + cH + col, v);
-            }
-            tmem_wait_st();
-        }
-
-        // (4) operands have landed
+        // (1) this step's keys, values, gates (and queries) have landed
         ok = wait_bar(&S.bar_tma, ph_tma, S, hdr, 2);
         if (!ok) break;
         tma_pending = false;
 
-        // (5) feature-map projections and window scores
+        // (2) feature-map projections and window scores on the tensor cores; they need only
+        //     this step's operands, so they run while the threads fold the gates
         if (tid == 0) {
             tc_fence_after();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint32_t koff = (j >> 2) * 16384 + (j & 3) * 32;
-                const uint64_t bw = mndesc(base + oW + j * 2048, 16384);
-                mma_bf16(tb + cUk, kdesc(base + oK + koff), bw, idesc_bf16(128, 64, false, true),
-                         j > 0);
+                const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                const uint64_t bw = dW + ((j * 2048) >> 4);
+                mma_bf16(tb + cUk, dK + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
                 if (MAIN) {
-                    const uint64_t aq = kdesc(base + oQ + koff);
-                    mma_bf16(tb + cUq, aq, bw, idesc_bf16(128, 64, false, true), j > 0);
-                    mma_bf16(tb + cS, aq, kdesc(base + oK + koff), idesc_bf16(128, 128, false, false),
+                    mma_bf16(tb + cUq, dQ + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
+                    mma_bf16(tb + cS, dQ + koff, dK + koff, idesc_bf16(128, 128, false, false),
                              j > 0);
                 }
             }
             mma_commit(&S.bar_mma);
+        }
+
+        // (3) gates: cumulative log-sigmoid per feature; four threads per feature, one per
+        //     8-token quarter; the reference r = b_15 is the first two quarters' total
+        const int gf = tid & (DF - 1), gq = tid >> 7;
+        float bt[CT / 4];
+        {
+            const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + oG);
+            float run = 0.0f;
+#pragma unroll
+            for (int t = 0; t < CT / 4; ++t) {
+                const int tt = (CT / 4) * gq + t;
+                const float lam = tt < n ? log_sigmoid_fast(__bfloat162float(sg[tt * DF + gf])) : 0.0f;
+                run += lam;
+                bt[t] = run;
+            }
+            gpart[gq * DF + gf] = run;
+        }
+        __syncthreads();
+        {
+            const float g0 = gpart[gf], g1 = gpart[DF + gf], g2 = gpart[2 * DF + gf],
+                        g3 = gpart[3 * DF + gf];
+            const float bref = g0 + g1, blast = bref + g2 + g3;
+            const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? bref : bref + g2;
+            __nv_bfloat16* Eq = (__nv_bfloat16*)(sm + oE);
+            __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + oE + 8192);
+#pragma unroll
+            for (int t = 0; t < CT / 4; ++t) {
+                const int tt = (CT / 4) * gq + t;
+                const float btt = bt[t] + off;
+                if (MAIN) Eq[tt * DF + gf] = __float2bfloat16_rn(__expf(clamp80(btt - bref)));
+                Ek[tt * DF + gf] = __float2bfloat16_rn(__expf(clamp80(bref - btt)));
+            }
+            if (gq == 0) {
+                S.cf[gf] = __expf(blast - bref);
+                S.zs[gf] = __expf(bref) * S.z[gf];
+                lam_tot += blast;
+            }
+        }
+
+        // (4) ... while the threads make the state's bf16 copy scaled by e^{r} for the readout
+        //     and decay the fp32 master by e^{b_31} (TMEM columns the MMAs do not touch)
+        {
+            const int f = row;
+            const float g0 = gpart[f], g1 = gpart[DF + f], g2 = gpart[2 * DF + f],
+                        g3 = gpart[3 * DF + f];
+            const float er = __expf(g0 + g1), el = __expf(g0 + g1 + g2 + g3);
+            const int col = 32 * part;
+            float v[32];
+            tmem_ld32(tb + lane_off + cH + col, v);
+            tmem_wait_ld();
+            if (MAIN) {
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const int nchunk = (col & 63) / 8 + ch;
+                    st_shared_v4(base + oHs + (col / 64) * 16384 + sw128(f, nchunk),
+                                 pack_bf16(er * v[8 * ch], er * v[8 * ch + 1]),
+                                 pack_bf16(er * v[8 * ch + 2], er * v[8 * ch + 3]),
+                                 pack_bf16(er * v[8 * ch + 4], er * v[8 * ch + 5]),
+                                 pack_bf16(er * v[8 * ch + 6], er * v[8 * ch + 7]));
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= el;
+            tmem_st32(tb + lane_off + cH + col, v);
+            tmem_wait_st();
         }
         mma_pending = true;
         ok = wait_bar(&S.bar_mma, ph_mma, S, hdr, 3);
@@ -323,69 +356,91 @@ __global__ void __launch_bounds__(NT, 1)
         mma_pending = false;
         tc_fence_after();
 
-        // (6) window softmax (all rows, two column halves) and the query feature map
+        // (5) window softmax over the ring slot `part`, the query feature map, U_k staging
         const int i = row >> 2, hh = row & 3;
         const int64_t qa = t0 + i;
         const bool qv = i < n;
         float m_row = 0.0f;
+        float sv[32], uv[32];
+        int ulo = 1, uhi = 0;
         if (MAIN) {
-            float sv[64];
-            tmem_ld32(tb + lane_off + cS + 64 * half, sv);
-            tmem_ld32(tb + lane_off + cS + 64 * half + 32, sv + 32);
+            tmem_ld32(tb + lane_off + cS + 32 * part, sv);
+            tmem_ld32(tb + lane_off + cUq + 32 * (part & 1), uv);
+        }
+        if (quad == slot_d && part < 2) {
+            float w[32];
+            tmem_ld32(tb + lane_off + cUk + 32 * part, w);
             tmem_wait_ld();
-            float pmax = -INFINITY;
-            uint64_t vm = 0;
 #pragma unroll
-            for (int k = 0; k < 64; ++k) {
-                const int kr = 64 * half + k;
-                const int slot = kr >> 5, u = kr & 31;
-                const int64_t age = (c - slot) & 3;
-                const int64_t key = (c - age) * CT + u;
-                const bool valid = qv && age <= 2 && key <= qa && key > qa - WIN && key >= 0;
-                sv[k] *= p.scale;
-                if (valid) {
-                    pmax = fmaxf(pmax, sv[k]);
-                    vm |= (1ull << k);
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(suk + lane * 64 + 32 * part + k) =
+                    make_float4(w[k], w[k + 1], w[k + 2], w[k + 3]);
+        }
+        if (MAIN) {
+            tmem_wait_ld();
+            // keys of ring slot `part` are tokens 32 (c - age) + u; the valid u form one interval
+            {
+                const int64_t age = (c - part) & 3;
+                const int64_t kbase = (c - age) * CT;
+                const int64_t lo = max64(max64(0, qa - WIN + 1 - kbase), -kbase);
+                const int64_t hi = min64(31, qa - kbase);
+                if (qv && age <= 2) {
+                    ulo = (int)lo;
+                    uhi = (int)hi;
                 }
             }
-            S.pm[half][row] = pmax;
-            __syncthreads();
-            m_row = fmaxf(fmaxf(S.pm[0][row], S.pm[1][row]), S.tmax[hh]);
+            float pmax = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                sv[k] *= p.scale;
+                if (k >= ulo && k <= uhi) pmax = fmaxf(pmax, sv[k]);
+            }
+            float uext = uv[0];
+#pragma unroll
+            for (int k = 1; k < 32; ++k) uext = part < 2 ? fmaxf(uext, uv[k]) : fminf(uext, uv[k]);
+            xpm[part * 128 + row] = pmax;
+            xum[part * 128 + row] = uext;
+        }
+        // the exchanges below stay within the 4 warps of a lane quadrant (one row per lane);
+        // the staged U_k rows are read after the full barrier at the end of this phase
+        if (MAIN) quad_sync(quad);
+        if (MAIN) {
+            m_row = fmaxf(fmaxf(fmaxf(xpm[row], xpm[128 + row]), fmaxf(xpm[256 + row], xpm[384 + row])),
+                          S.tmax[hh]);
             float psum = 0.0f;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
+            for (int ch = 0; ch < 4; ++ch) {
                 float pv[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int k = 8 * ch + e;
-                    pv[e] = ((vm >> k) & 1ull) ? bf16r(__expf(sv[k] - m_row)) : 0.0f;
+                    pv[e] = (k >= ulo && k <= uhi) ? bf16r(__expf(sv[k] - m_row)) : 0.0f;
                     psum += pv[e];
                 }
-                st_shared_v4(base + oQ + half * 16384 + sw128(row, ch), pack_bf16(pv[0], pv[1]),
-                             pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
-                             pack_bf16(pv[6], pv[7]));
+                st_shared_v4(base + oQ + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                             pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
+                             pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
             }
-            S.ps[half][row] = psum;
-
-            // phi(q): half 0 takes softmax(u), half 1 softmax(-u), u = q Wf (64 values)
-            float uv[64];
-            tmem_ld32(tb + lane_off + cUq, uv);
-            tmem_ld32(tb + lane_off + cUq + 32, uv + 32);
-            tmem_wait_ld();
-            float ref = uv[0];
+            S.ps[part][row] = psum;
+            const int sib = part ^ 1;
+            const float uext = part < 2 ? fmaxf(xum[part * 128 + row], xum[sib * 128 + row])
+                                        : fminf(xum[part * 128 + row], xum[sib * 128 + row]);
+            float usum = 0.0f;
 #pragma unroll
-            for (int k = 1; k < 64; ++k) ref = half ? fminf(ref, uv[k]) : fmaxf(ref, uv[k]);
-            float sum = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 64; ++k) {
-                uv[k] = __expf(half ? (ref - uv[k]) : (uv[k] - ref));
-                sum += uv[k];
+            for (int k = 0; k < 32; ++k) {
+                uv[k] = __expf(part < 2 ? (uv[k] - uext) : (uext - uv[k]));
+                usum += uv[k];
             }
-            const float sc = __expf(-m_row) / sum;
+            xus[part * 128 + row] = usum;
+        }
+        if (MAIN) quad_sync(quad);
+        if (MAIN) {
+            // q~ = phi(q) e^{b_i - r} e^{-m}: features [32 part, 32 part + 32)
+            const float sc = __expf(-m_row) / (xus[part * 128 + row] + xus[(part ^ 1) * 128 + row]);
             float pg = 0.0f;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const int f0 = 64 * half + 8 * ch;
+            for (int ch = 0; ch < 4; ++ch) {
+                const int f0 = 32 * part + 8 * ch;
                 uint32_t w0, w1, w2, w3;
                 ld_shared_v4(base + oE + (uint32_t)(i * DF + f0) * 2u, w0, w1, w2, w3);
                 float eq[8], qv8[8];
@@ -395,51 +450,64 @@ __global__ void __launch_bounds__(NT, 1)
                     qv8[e] = bf16r(uv[8 * ch + e] * sc * eq[e]);
                     pg = fmaf(qv8[e], S.zs[f0 + e], pg);
                 }
-                st_shared_v4(base + oQt + half * 16384 + sw128(row, ch), pack_bf16(qv8[0], qv8[1]),
-                             pack_bf16(qv8[2], qv8[3]), pack_bf16(qv8[4], qv8[5]),
-                             pack_bf16(qv8[6], qv8[7]));
+                st_shared_v4(base + oQt + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                             pack_bf16(qv8[0], qv8[1]), pack_bf16(qv8[2], qv8[3]),
+                             pack_bf16(qv8[4], qv8[5]), pack_bf16(qv8[6], qv8[7]));
             }
-            S.pg[half][row] = pg;
+            S.pg[part][row] = pg;
         }
+        __syncthreads();
 
-        // phi of the delayed keys (the ring slot two steps back) -> k~ for intra and update
-        if (quad == slot_d) {
-            const int t = lane;
+        // (6) phi of the delayed keys (the ring slot two steps back) from the staged U_k rows:
+        //     16 threads per key, 4 u-values each -> k~ for the intra scores and the update
+        {
+            const int t = tid >> 4, sub = tid & 15;
             const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
-            float uv[64];
-            tmem_ld32(tb + lane_off + cUk, uv);
-            tmem_ld32(tb + lane_off + cUk + 32, uv + 32);
-            tmem_wait_ld();
-            float ref = uv[0];
+            const float4 u4 = *reinterpret_cast<const float4*>(suk + t * 64 + 4 * sub);
+            const float u[4] = {u4.x, u4.y, u4.z, u4.w};
+            float mx = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
+            float mn = fminf(fminf(u[0], u[1]), fminf(u[2], u[3]));
 #pragma unroll
-            for (int k = 1; k < 64; ++k) ref = half ? fminf(ref, uv[k]) : fmaxf(ref, uv[k]);
-            float sum = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 64; ++k) {
-                uv[k] = __expf(half ? (ref - uv[k]) : (uv[k] - ref));
-                sum += uv[k];
+            for (int o = 1; o < 16; o <<= 1) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
             }
-            const float inv = dvalid ? 1.0f / sum : 0.0f;
+            float ep[4], en[4], sp = 0.0f, sn = 0.0f;
 #pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const int f0 = 64 * half + 8 * ch;
-                uint32_t w0, w1, w2, w3;
-                ld_shared_v4(base + oE + 8192u + (uint32_t)(t * DF + f0) * 2u, w0, w1, w2, w3);
-                float ek[8], ki[8], ku[8];
-                unpack8(w0, w1, w2, w3, ek);
+            for (int e = 0; e < 4; ++e) {
+                ep[e] = __expf(u[e] - mx);
+                en[e] = __expf(mn - u[e]);
+                sp += ep[e];
+                sn += en[e];
+            }
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float phk = uv[8 * ch + e] * inv;
-                    ki[e] = phk * ek[e];
+            for (int o = 1; o < 16; o <<= 1) {
+                sp += __shfl_xor_sync(0xffffffffu, sp, o);
+                sn += __shfl_xor_sync(0xffffffffu, sn, o);
+            }
+            const float ip = dvalid ? 1.0f / sp : 0.0f, in = dvalid ? 1.0f / sn : 0.0f;
+            const __nv_bfloat16* Ek = (const __nv_bfloat16*)(sm + oE + 8192);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                const int f0 = 64 * kb + 4 * sub;  // features f0..f0+3 (kb 0: softmax(u), 1: -u)
+                float ki[4], ku[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float ph = kb == 0 ? ep[e] * ip : en[e] * in;
+                    ki[e] = ph * __bfloat162float(Ek[t * DF + f0 + e]);
                     ku[e] = ki[e] * S.cf[f0 + e];
                 }
-                if (MAIN)
-                    st_shared_v4(base + oKi + half * 4096 + sw128(t, ch), pack_bf16(ki[0], ki[1]),
-                                 pack_bf16(ki[2], ki[3]), pack_bf16(ki[4], ki[5]),
-                                 pack_bf16(ki[6], ki[7]));
-                st_shared_v4(base + oKu + half * 4096 + sw128(t, ch), pack_bf16(ku[0], ku[1]),
-                             pack_bf16(ku[2], ku[3]), pack_bf16(ku[4], ku[5]),
-                             pack_bf16(ku[6], ku[7]));
+                const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
+                if (MAIN) {
+                    const uint32_t a0 = pack_bf16(ki[0], ki[1]), a1 = pack_bf16(ki[2], ki[3]);
+                    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + oKi + off), "r"(a0),
+                                 "r"(a1)
+                                 : "memory");
+                }
+                const uint32_t b0 = pack_bf16(ku[0], ku[1]), b1 = pack_bf16(ku[2], ku[3]);
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + oKu + off), "r"(b0),
+                             "r"(b1)
+                             : "memory");
             }
         }
         fence_async_smem();
@@ -451,10 +519,9 @@ __global__ void __launch_bounds__(NT, 1)
             tc_fence_after();
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint32_t qoff = (j >> 2) * 16384 + (j & 3) * 32;
-                const uint32_t koff = (j >> 2) * 4096 + (j & 3) * 32;
-                mma_bf16(tb + cA, kdesc(base + oQt + qoff), kdesc(base + oKi + koff),
-                         idesc_bf16(128, 32, false, false), j > 0);
+                const uint32_t qoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                const uint32_t koff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + cA, dQt + qoff, dKi + koff, idesc_bf16(128, 32, false, false), j > 0);
             }
             mma_commit(&S.bar_mma);
         }
@@ -467,38 +534,30 @@ __global__ void __launch_bounds__(NT, 1)
                 const uint32_t off = (f >> 6) * 4096 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
                 zsum += __bfloat162float(ku[off / 2]);
             }
-            S.z[f] = fmaf(S.elast[f], S.z[f], zsum);
+            S.z[f] = fmaf(S.cf[f] * S.zs[f], 1.0f, zsum);  // e^{b_31} z = e^{b_31-r} e^{r} z
         }
+        float pi_row = 0.0f;
         if (MAIN) {
             mma_pending = true;
             ok = wait_bar(&S.bar_mma, ph_mma, S, hdr, 4);
             if (!ok) break;
             mma_pending = false;
             tc_fence_after();
-            if (half == 0) {
-                float av[32];
-                tmem_ld32(tb + lane_off + cA, av);
-                tmem_wait_ld();
-                float ps2 = 0.0f;
+            // P_intra: columns t in [8 part, 8 part + 8)
+            float av[8];
+            tmem_ld8(tb + lane_off + cA + 8 * part, av);
+            tmem_wait_ld();
+            float pv[8];
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    float pv[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int t = 8 * ch + e;
-                        const bool valid = qv && t <= i && (t0 + t - WIN >= 0);
-                        pv[e] = valid ? bf16r(av[t]) : 0.0f;
-                        ps2 += pv[e];
-                    }
-                    st_shared_v4(base + oE + sw128(row, ch), pack_bf16(pv[0], pv[1]),
-                                 pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]),
-                                 pack_bf16(pv[6], pv[7]));
-                }
-                float ssum = 0.0f;
-                for (int mm = 0; mm < p.M; ++mm) ssum += __expf(S.sinks[hh][mm] - m_row);
-                S.m[row] = m_row;
-                S.den[row] = S.ps[0][row] + S.ps[1][row] + S.pg[0][row] + S.pg[1][row] + ps2 + ssum;
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * part + e;
+                const bool valid = qv && t <= i && (t0 + t - WIN >= 0);
+                pv[e] = valid ? bf16r(av[e]) : 0.0f;
+                pi_row += pv[e];
             }
+            st_shared_v4(base + oE + sw128(row, part), pack_bf16(pv[0], pv[1]),
+                         pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
+            spi[part * 128 + row] = pi_row;
             fence_async_smem();
             tc_fence_before();
             __syncthreads();
@@ -507,29 +566,28 @@ __global__ void __launch_bounds__(NT, 1)
         // (8) outputs and the state update
         if (tid == 0) {
             tc_fence_after();
+            const uint64_t dVd = dV + ((slot_d * 4096) >> 4);
             if (MAIN) {
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const uint32_t qoff = (j >> 2) * 16384 + (j & 3) * 32;
-                    mma_bf16(tb + cO, kdesc(base + oQt + qoff), mndesc(base + oHs + j * 2048, 16384),
+                    const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                    mma_bf16(tb + cO, dQt + aoff, dHs + ((j * 2048) >> 4),
                              idesc_bf16(128, 128, false, true), j > 0);
                 }
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
-                    const uint32_t poff = (j >> 2) * 16384 + (j & 3) * 32;
-                    mma_bf16(tb + cO, kdesc(base + oQ + poff), mndesc(base + oV + j * 2048, 16384),
+                    const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                    mma_bf16(tb + cO, dQ + aoff, dV + ((j * 2048) >> 4),
                              idesc_bf16(128, 128, false, true), 1);
                 }
 #pragma unroll
                 for (int j = 0; j < 2; ++j)
-                    mma_bf16(tb + cO, kdesc(base + oE + j * 32),
-                             mndesc(base + oV + slot_d * 4096 + j * 2048, 16384),
+                    mma_bf16(tb + cO, dE + ((j * 32) >> 4), dVd + ((j * 2048) >> 4),
                              idesc_bf16(128, 128, false, true), 1);
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
-                mma_bf16(tb + cH, mndesc(base + oKu + j * 2048, 4096),
-                         mndesc(base + oV + slot_d * 4096 + j * 2048, 16384),
+                mma_bf16(tb + cH, dKu + ((j * 2048) >> 4), dVd + ((j * 2048) >> 4),
                          idesc_bf16(128, 128, true, true), 1);
             mma_commit(&S.bar_mma);
         }
@@ -538,32 +596,40 @@ __global__ void __launch_bounds__(NT, 1)
         if (!ok) break;
         mma_pending = false;
         tc_fence_after();
+        // the next step's operands fly during the epilogue: the query tile (P_win), the ring
+        // slot (chunk c-3) and the gate tile (U_k staging) are no longer read
+        if (tid == 0 && c + 1 < c_end)
+            issue_step_loads<MAIN>(sm, &S.bar_tma, &tmQ, &tmK, &tmV, &tmG, c + 1, kv, b);
+        tma_pending = c + 1 < c_end;
 
-        // (9) epilogue: y = O / den, 16-byte bf16 stores
+        // (9) epilogue: y = O / den over columns [32 part, 32 part + 32), 16-byte bf16 stores
         if (MAIN) {
             float ov[32];
+            const int col = 32 * part;
+            tmem_ld32(tb + lane_off + cO + col, ov);
+            tmem_wait_ld();
+            if (qv) {
+                float ssum = 0.0f;
+                for (int mm = 0; mm < p.M; ++mm) ssum += __expf(S.sinks[hh][mm] - m_row);
+                const float den = (S.ps[0][row] + S.ps[1][row]) + (S.ps[2][row] + S.ps[3][row]) +
+                                  (S.pg[0][row] + S.pg[1][row]) + (S.pg[2][row] + S.pg[3][row]) +
+                                  (spi[row] + spi[128 + row]) + (spi[256 + row] + spi[384 + row]) +
+                                  ssum;
+                const float inv = 1.0f / den;
+                __nv_bfloat16* yr = (__nv_bfloat16*)a.y +
+                                    ((b * p.L + qa) * p.Hq + kv * GQ + hh) * DH + col;
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int col = 64 * half + 32 * j;
-                tmem_ld32(tb + lane_off + cO + col, ov);
-                tmem_wait_ld();
-                if (qv) {
-                    const float inv = 1.0f / S.den[row];
-                    __nv_bfloat16* yr = (__nv_bfloat16*)a.y +
-                                        ((b * p.L + qa) * p.Hq + kv * GQ + hh) * DH + col;
-#pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint4 w;
-                        w.x = pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv);
-                        w.y = pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv);
-                        w.z = pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv);
-                        w.w = pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv);
-                        *reinterpret_cast<uint4*>(yr + 8 * ch) = w;
-                    }
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint4 w;
+                    w.x = pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv);
+                    w.y = pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv);
+                    w.z = pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv);
+                    w.w = pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv);
+                    *reinterpret_cast<uint4*>(yr + 8 * ch) = w;
                 }
+                if (part == 0 && a.lse != nullptr)
+                    a.lse[(b * p.L + qa) * p.Hq + kv * GQ + hh] = m_row + __logf(den);
             }
-            if (qv && half == 0 && a.lse != nullptr)
-                a.lse[(b * p.L + qa) * p.Hq + kv * GQ + hh] = S.m[row] + logf(S.den[row]);
         }
         tc_fence_before();
         __syncthreads();
@@ -585,16 +651,13 @@ __global__ void __launch_bounds__(NT, 1)
         if (dstH != nullptr) {
             tc_fence_after();
             float v[32];
+            const int col = 32 * part;
+            tmem_ld32(tb + lane_off + cH + col, v);
+            tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int col = 64 * half + 32 * j;
-                tmem_ld32(tb + lane_off + cH + col, v);
-                tmem_wait_ld();
-#pragma unroll
-                for (int k = 0; k < 32; k += 4)
-                    *reinterpret_cast<float4*>(dstH + row * DH + col + k) =
-                        make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-            }
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(dstH + row * DH + col + k) =
+                    make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
             if (tid < DF) dstz[tid] = S.z[tid];
         }
     } else {
@@ -626,12 +689,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box) {
+              const cuuint64_t* strides, const cuuint32_t* box, bool swizzle = true) {
     auto fn = encode_fn();
     if (fn == nullptr) return false;
     const cuuint32_t es[5] = {1, 1, 1, 1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
-              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -661,6 +725,13 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
         if (!make_map(&mk, a.k, 4, dims, str, box)) return cudaErrorInvalidValue;
         if (!make_map(&mv, a.v, 4, dims, str, box)) return cudaErrorInvalidValue;
     }
+    alignas(64) CUtensorMap mg;
+    {
+        const cuuint64_t dims[4] = {DF, Hkv, L, B};
+        const cuuint64_t str[3] = {DF * 2, Hkv * DF * 2, L * Hkv * DF * 2};
+        const cuuint32_t box[4] = {DF, 1, CT, 1};
+        if (!make_map(&mg, a.g, 4, dims, str, box, false)) return cudaErrorInvalidValue;
+    }
     {
         const cuuint64_t dims[3] = {DF / 2, DH, Hkv};
         const cuuint64_t str[2] = {(DF / 2) * 2, DH * (DF / 2) * 2};
@@ -677,12 +748,12 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     const unsigned U = (unsigned)(p.B * p.Hkv);
     if (p.P > 1) {
         fwd_tc_kernel<false><<<dim3(U, (unsigned)(p.P - 1)), NT, kSmemBytes, s>>>(mq, mk, mv, mw,
-                                                                                 p, a);
+                                                                                 mg, p, a);
         e = launch_seg_scan(p, a.seg, s);
         if (e != cudaSuccess) return e;
     }
     if (a.ev_before) cudaEventRecord(a.ev_before, s);
-    fwd_tc_kernel<true><<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, p, a);
+    fwd_tc_kernel<true><<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, p, a);
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
     return cudaGetLastError();
 }

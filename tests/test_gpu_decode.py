@@ -115,3 +115,38 @@ def test_decode_state_checkpoint_resume(lz):
     st2 = [x.to("cuda") for x in saved]
     y_tail = decode_all(lz, t, wl, 50, 30, *st2)
     np.testing.assert_array_equal(y_tail, y_all[:, 50:])
+
+
+def test_decode_b64_full_size_sampled(lz, oracle_mod):
+    """The decode workload at full size: B=64 sequences prefilled with 32768 tokens, then 1024
+    single-token steps.  Inputs are drawn on the device (host generation of 15 G values would
+    take minutes); two sampled sequences are copied back and checked against the oracle's
+    prefill of all 33792 tokens, token by token."""
+    wl = I.DECODE_B64
+    T0, steps = wl.prefill, wl.steps
+    B, Hq, Hkv, d, D, w = wl.B, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w
+    pre = I.make_device_inputs(wl, "cuda", L=T0, B=B)
+    S = torch.empty(B, Hkv, D, d, dtype=torch.float32, device="cuda")
+    z = torch.empty(B, Hkv, D, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(B, Hkv, w + 1, d, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    lz.lizard_attn_fwd(pre["q"], pre["k"], pre["v"], pre["g"], pre["Wf"], pre["sinks"], w,
+                       S_out=S, z_out=z, kcache_out=kc, vcache_out=vc)
+    nxt = I.make_device_inputs(wl, "cuda", L=steps, B=B, seed_offset=1)
+    qs, ks, vs, gs = (nxt[n].transpose(0, 1).contiguous() for n in ("q", "k", "v", "g"))
+    dims = lz.make_dims(B, 1, Hq, Hkv, d, D, w, wl.M, torch.bfloat16)
+    ws = lz.new_workspace(lz.lizard_decode_workspace(dims), "cuda")
+    Y = torch.empty(steps, B, Hq, d, dtype=torch.bfloat16, device="cuda")
+    for i in range(steps):
+        lz.lizard_decode_step(T0 + i, qs[i], ks[i], vs[i], gs[i], pre["Wf"], pre["sinks"], S, z,
+                              kc, vc, w, y=Y[i], workspace=ws)
+    torch.cuda.synchronize()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    for b in (0, 37):
+        seq = {n: torch.cat([pre[n][b:b + 1], nxt[n][b:b + 1]], dim=1).float().cpu().numpy()
+               for n in ("q", "k", "v", "g")}
+        seq["Wf"] = pre["Wf"].float().cpu().numpy()
+        seq["sinks"] = pre["sinks"].cpu().numpy()
+        ref = oracle_mod.fwd(**seq, w=w)["y"][0, T0:]          # [steps, Hq, d]
+        got = Y[:, b].float().cpu().numpy().astype(np.float64)
+        assert_parity(got, ref, "bf16", f"decode b{b}")
