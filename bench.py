@@ -37,6 +37,7 @@ def parse():
     ap.add_argument("--decode-steps", type=int, default=1024)
     ap.add_argument("--decode-prefill", type=int, default=32768)
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-train", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -175,6 +176,18 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(busy)}
 
 
+def reduce_max(x: float, world: int, device) -> float:
+    """Max of a per-rank float over all ranks (the job's time is its slowest rank's)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def run_reference(args, rank, world):
     """The oracle (float64 C recurrence, OpenMP over batch x KV head) on host cores."""
     from gated_linear_sliding_gb300 import inputs as I
@@ -248,11 +261,7 @@ def run_ours(args, rank, world, device):
             dist.barrier()
 
     def max_over_ranks(x: float) -> float:
-        if world == 1:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return reduce_max(x, world, device)
 
     # --- inputs: seeded host arrays, pinned, copied once to HBM
     inp = I.make_inputs(wl)
@@ -343,6 +352,9 @@ def run_ours(args, rank, world, device):
     decode = None
     if not args.no_decode:
         decode = run_decode(args, device, lz, I, hbm_peak, peak_src)
+    train = None
+    if not args.no_train:
+        train = run_train(args, device, lz, I)
     clocks = sampler.stop()
 
     tokens = wl.B * wl.L
@@ -374,7 +386,55 @@ def run_ours(args, rank, world, device):
     }
     if decode is not None:
         out["decode"] = decode
+    if train is not None:
+        out["train"] = train
     return out
+
+
+def run_train(args, device, lz, I):
+    """Forward + backward of the Mistral-7B-shaped layer (B=8, L=2048), L2 flushed per step."""
+    import torch
+
+    wl = I.MISTRAL_7B_TRAIN
+    t = I.make_device_inputs(wl, device, with_dy=True)
+    B, L, Hq = wl.B, wl.L, wl.Hq
+    y = torch.empty_like(t["q"])
+    lse = torch.empty(B, L, Hq, dtype=torch.float32, device=device)
+    dims = lz.dims_of(t["q"], t["k"], t["g"], t["sinks"], wl.w)
+    wsf = lz.new_workspace(lz.lizard_attn_fwd_workspace(dims), device)
+    wsb = lz.new_workspace(lz.lizard_attn_bwd_workspace(dims), device)
+    grads = dict(dq=torch.empty_like(t["q"]), dk=torch.empty_like(t["k"]),
+                 dv=torch.empty_like(t["v"]), dg=torch.empty_like(t["g"]),
+                 dWf=torch.empty(wl.Hkv, wl.d, wl.D // 2, device=device),
+                 dsinks=torch.empty(Hq, wl.M, device=device))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def step():
+        lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w, y=y,
+                           lse=lse, workspace=wsf)
+        lz.lizard_attn_bwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], y, lse, t["dy"],
+                           wl.w, workspace=wsb, **grads)
+
+    step()
+    torch.cuda.synchronize()
+    n = 3
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for e0, e1, e2 in evs:
+        flush.zero_()
+        e0.record()
+        lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w, y=y,
+                           lse=lse, workspace=wsf)
+        e1.record()
+        lz.lizard_attn_bwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], y, lse, t["dy"],
+                           wl.w, workspace=wsb, **grads)
+        e2.record()
+    torch.cuda.synchronize()
+    fwd_ms = sum(a.elapsed_time(b) for a, b, _ in evs) / n
+    bwd_ms = sum(b.elapsed_time(c) for _, b, c in evs) / n
+    return {"workload": wl.name, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "step_ms": fwd_ms + bwd_ms, "tokens_per_s": B * L / ((fwd_ms + bwd_ms) * 1e-3),
+            "timing": "CUDA events, 512 MiB L2 flush before each step, mean of 3"}
 
 
 def run_decode(args, device, lz, I, hbm_peak, peak_src):
