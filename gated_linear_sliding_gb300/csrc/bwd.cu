@@ -36,7 +36,7 @@ constexpr int KB = 16;  // window keys per tile in the query-side walk
 
 // Workspace regions (floats, each 64-float aligned)
 struct BwdWs {
-    size_t fwd_rec, rev_rec, dB, tot, dW, dt, total;
+    size_t fwd_rec, rev_rec, dB, tot, dW, dt, rows, total;
 };
 
 inline size_t al64(size_t x) { return (x + 63) & ~(size_t)63; }
@@ -57,6 +57,8 @@ BwdWs bwd_layout(const Plan& p) {
     off += al64((size_t)2 * p.Pmax * U * (size_t)(p.d * (p.D / 2)));
     w.dt = off;
     off += al64((size_t)p.Pmax * U * (size_t)p.G);
+    w.rows = off;  // per query row: a = e^{-lse}, delta = dy . y   [2][B*L*Hq]
+    off += al64((size_t)2 * (size_t)(p.B * p.L * p.Hq));
     w.total = off * sizeof(float);
     return w;
 }
@@ -174,24 +176,38 @@ __device__ __forceinline__ void load_rows_p(const T* x, int64_t b, int64_t L, in
     }
 }
 
-// a_i = e^{-lse_i}, delta_i = dy_i . y_i for the n valid rows of one head (row stats).
-template <typename T, int DH>
-__device__ __forceinline__ void row_stats(const BwdArgs& a, const Plan& p, int64_t b, int64_t h,
-                                          int64_t i0, int n, float* srow) {
-    const int r = threadIdx.x / LPR, sub = threadIdx.x % LPR;
-    float dl = 0.0f;
-    if (r < n) {
-        const T* yr = (const T*)a.y + ((b * p.L + i0 + r) * p.Hq + h) * DH;
-        const T* dr = (const T*)a.dy + ((b * p.L + i0 + r) * p.Hq + h) * DH;
-        for (int c = sub; c < DH; c += LPR) dl = fmaf(ld(yr + c), ld(dr + c), dl);
+// a_i = e^{-lse_i}, delta_i = dy_i . y_i, lse_i for the n valid rows of one head, from the
+// per-row table the first backward kernel fills.
+__device__ __forceinline__ void row_stats(const BwdArgs& a, const Plan& p, const BwdWs& ws,
+                                          int64_t b, int64_t h, int64_t i0, int n, float* srow) {
+    const int r = threadIdx.x;
+    if (r < TS) {
+        const int64_t idx = (b * p.L + i0 + r) * p.Hq + h;
+        const int64_t nrow = p.B * p.L * p.Hq;
+        const float* rows = (const float*)a.ws + ws.rows;
+        srow[r] = r < n ? rows[idx] : 0.0f;
+        srow[TS + r] = r < n ? rows[nrow + idx] : 0.0f;
+        srow[2 * TS + r] = r < n ? a.lse[idx] : 0.0f;
     }
+}
+
+// Per query row: a = e^{-lse}, delta = dy . y (one warp per row, fixed order).
+template <typename T, int DH>
+__global__ void bwd_row_table(Plan p, BwdArgs a, BwdWs ws) {
+    const int64_t nrow = p.B * p.L * p.Hq;
+    const int64_t r = (int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31;
+    if (r >= nrow) return;
+    const T* yr = (const T*)a.y + r * DH;
+    const T* dr = (const T*)a.dy + r * DH;
+    float dl = 0.0f;
+    for (int c = lane; c < DH; c += 32) dl = fmaf(ld(yr + c), ld(dr + c), dl);
 #pragma unroll
-    for (int o = 1; o < LPR; o <<= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
-    if (sub == 0) {
-        const float lse = r < n ? a.lse[(b * p.L + i0 + r) * p.Hq + h] : 0.0f;
-        srow[r] = r < n ? expf(-lse) : 0.0f;
-        srow[TS + r] = r < n ? dl : 0.0f;
-        srow[2 * TS + r] = lse;
+    for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+    if (lane == 0) {
+        float* rows = (float*)a.ws + ws.rows;
+        rows[r] = expf(-a.lse[r]);
+        rows[nrow + r] = dl;
     }
 }
 
@@ -313,7 +329,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_forward_walk(Plan p, BwdArgs a, Bwd
             const int64_t h = kv * p.G + hh;
             load_rows_p<T, DH>((const T*)a.q, b, p.L, p.Hq, h, i0, 0, n, sq);
             load_rows_p<T, DH>((const T*)a.dy, b, p.L, p.Hq, h, i0, 0, n, sdy);
-            row_stats<T, DH>(a, p, b, h, i0, n, srow);
+            row_stats(a, p, ws, b, h, i0, n, srow);
             __syncthreads();
             phi_rows_p<DH, DF, FAST>(sq, sW, sphq, 0, n);
             // c_it = a_i (v'_t . dy_i - delta_i), t <= i
@@ -479,7 +495,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_local(Plan p, BwdArgs a, Bw
             const int64_t h = kv * p.G + hh;
             load_rows_p<T, DH>((const T*)a.q, b, p.L, p.Hq, h, i0, 0, n, sq);
             load_rows_p<T, DH>((const T*)a.dy, b, p.L, p.Hq, h, i0, 0, n, sdy);
-            row_stats<T, DH>(a, p, b, h, i0, n, srow);
+            row_stats(a, p, ws, b, h, i0, n, srow);
             __syncthreads();
             phi_rows_p<DH, DF, FAST>(sq, sW, sphq, 0, n);
             __syncthreads();
@@ -594,7 +610,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
             const int64_t h = kv * p.G + hh;
             load_rows_p<T, DH>((const T*)a.q, b, p.L, p.Hq, h, i0, 0, n, sq);
             load_rows_p<T, DH>((const T*)a.dy, b, p.L, p.Hq, h, i0, 0, n, sdy);
-            row_stats<T, DH>(a, p, b, h, i0, n, srow);
+            row_stats(a, p, ws, b, h, i0, n, srow);
             __syncthreads();
             phi_rows_p<DH, DF, FAST>(sq, sW, sphq, 0, n);
             __syncthreads();
@@ -687,7 +703,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
 // Window part of dk, dv, key-centric: keys j of a 32-key tile, queries i in [j, j + w).
 // Keys with j + w < L already hold their state parts; the window part is added to them.
 template <typename T, int DH, bool FAST>
-__global__ void __launch_bounds__(NT) bwd_window_keys(Plan p, BwdArgs a) {
+__global__ void __launch_bounds__(NT) bwd_window_keys(Plan p, BwdArgs a, BwdWs ws) {
     constexpr int PH = DH + 1, QT = 8;  // query tokens per tile
     extern __shared__ float sm[];
     float* sk = sm;                  // [32][PH]
@@ -734,8 +750,7 @@ __global__ void __launch_bounds__(NT) bwd_window_keys(Plan p, BwdArgs a) {
             if (i < ihi) {
                 const int64_t off = ((b * p.L + i) * p.Hq + kv * G + hh);
                 lse = a.lse[off];
-                for (int c = 0; c < DH; ++c)
-                    dl = fmaf(ld((const T*)a.y + off * DH + c), ld((const T*)a.dy + off * DH + c), dl);
+                dl = ((const float*)a.ws)[ws.rows + p.B * p.L * p.Hq + off];
             }
             srow[rr] = lse;
             srow[RQ + rr] = dl;
@@ -848,6 +863,11 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const unsigned U = (unsigned)(p.B * p.Hkv);
     float* wsf = (float*)a.ws;
+    // 0. per-row a = e^{-lse} and delta = dy . y
+    {
+        const int64_t nrow = p.B * p.L * p.Hq;
+        bwd_row_table<T, DH><<<(unsigned)((nrow + 7) / 8), 256, 0, s>>>(p, a, ws);
+    }
     // 1. forward segment states (segment pass + scan) into the first record region
     if (p.P > 1) {
         FwdArgs fa{};
@@ -875,7 +895,7 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     // 4. reverse-direction walk
     bwd_reverse_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
     // 5. window parts of dk, dv
-    bwd_window_keys<T, DH, FAST><<<dim3((unsigned)((p.L + 31) / 32), U), NT, wsmem, s>>>(p, a);
+    bwd_window_keys<T, DH, FAST><<<dim3((unsigned)((p.L + 31) / 32), U), NT, wsmem, s>>>(p, a, ws);
     // 6. dg, then the reductions
     const int64_t ng = p.B * p.L * p.Hkv * p.D;
     bwd_gates<T><<<(unsigned)((ng + 255) / 256), 256, 0, s>>>(p, a, ws);

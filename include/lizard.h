@@ -128,7 +128,8 @@ lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const void* q, co
 
 /* Bytes of device workspace lizard_attn_bwd needs: segment records whose size depends on
  * B, Hkv, d and D only, plus one fp32 per gate element (B * L * Hkv * D * 4 bytes) holding
- * the per-position gate gradient before its reverse cumulative sum. */
+ * the per-position gate gradient before its reverse cumulative sum, plus two fp32 per query
+ * row (e^{-lse} and dy . y, B * L * Hq * 8 bytes). */
 size_t lizard_attn_bwd_workspace(const lizard_dims* dims);
 
 /* Exact gradient of lizard_attn_fwd's y against an upstream gradient dy.  The

@@ -56,10 +56,10 @@ def test_workspace_constant_in_L(lib):
     boundary states whose count depends on B and Hkv only."""
     sizes = {L: lz.lizard_attn_fwd_workspace(dims(L=L)) for L in (64, 1000, 8192, 65536)}
     assert len(set(sizes.values())) == 1 and sizes[8192] > 0
-    # backward: only the per-gate-element fp32 scratch grows with L
+    # backward: only the per-gate-element and per-query-row fp32 scratch grows with L
     b1 = lz.lizard_attn_bwd_workspace(dims(L=2048, B=8))
     b2 = lz.lizard_attn_bwd_workspace(dims(L=4096, B=8))
-    assert b2 - b1 == 8 * 2048 * 8 * 128 * 4
+    assert b2 - b1 == 8 * 2048 * 8 * 128 * 4 + 2 * 8 * 2048 * 32 * 4
 
 
 @pytest.mark.parametrize("bad", [dict(Hq=30), dict(D=127), dict(w=0), dict(M=-1), dict(M=65),
