@@ -12,7 +12,10 @@
 //               space and fold into the query and key sides, which turns the chunk
 //               into plain low-precision GEMMs on the tensor cores.
 //
-// One CTA per (batch, KV head, segment); it walks its segment 32 tokens at a time.
+// One CTA per (batch, KV head, segment); it walks its segment 32 tokens at a time.  Sixteen
+// math warps do the softmaxes, masks and decay tables; one control warp issues every TMA
+// copy and MMA and hands results over through mbarriers, so the next step's projections run
+// while the math warps finish the current step.
 // The 128 query rows of a step are (token, head) pairs, row = 4 * token + head, so
 // the four heads of a group share every key-side operand.  Per step:
 //   b_t   = sum_{s<=t} log sigmoid(g_s)  (fp32, chunk-local), reference r = b_15
@@ -26,8 +29,8 @@
 // factor leaves the fp32/bf16 range unless 16 consecutive gates decay by more than
 // e^-80 (exponents are clamped to +-80 there).
 //
-// TMEM columns: H [0,128)  scores S [128,256)  U_q [256,320)  U_k [320,384)
-//               O [256,384) (reuses U)  intra scores A [384,416).
+// TMEM columns: H [0,128)  scores S [128,256) (intra scores A reuse [128,160))
+//               U_q [256,320)  U_k [320,384)  O [384,512).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -41,19 +44,23 @@ namespace {
 
 using namespace sm100;
 
-constexpr int NT = 512;   // 16 warps: warp w owns TMEM lanes 32(w%4).., w/4 picks a 32-column part
-constexpr int CT = 32;    // tokens per step
-constexpr int GQ = 4;     // query heads per KV head
-constexpr int DH = 128;   // head dim
-constexpr int DF = 128;   // phi dim
-constexpr int WIN = 64;   // window
-constexpr int MMAX = 64;  // sinks per head
+constexpr int NW = 16;        // math warps: warp w owns TMEM lanes 32(w%4).., w/4 picks a 32-column part
+constexpr int NS = 32 * NW;   // math threads
+constexpr int NT = NS + 32;   // plus one control warp that issues every TMA copy and MMA
+constexpr int CT = 32;        // tokens per step
+constexpr int GQ = 4;         // query heads per KV head
+constexpr int DH = 128;       // head dim
+constexpr int DF = 128;       // phi dim
+constexpr int WIN = 64;       // window
+constexpr int MMAX = 64;      // sinks per head
 constexpr long long kTimeout = 2000000000LL;  // SM cycles (about one second)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
 
 // shared-memory map (bytes from a 1024-aligned base); later uses of a region in a step follow
 // the arrow
 constexpr uint32_t oQ = 0;         // q tile, K-major [128 rows][128 d] -> P_win [128][128 keys]
-constexpr uint32_t oQt = 32768;    // gate partial sums [4][128] fp32 -> q~, K-major [128][128]
+constexpr uint32_t oQt = 32768;    // q~, K-major [128][128]
 constexpr uint32_t oK = 65536;     // key ring: 4 slots x 32 keys, K-major over d
 constexpr uint32_t oV = 98304;     // value ring: same bytes, read MN-major (N = d)
 constexpr uint32_t oW = 131072;    // Wf [128 d rows][64 features], MN-major B
@@ -65,10 +72,17 @@ constexpr uint32_t oG = 212992;    // gate logits [32][128] bf16 -> staged U_k r
 constexpr uint32_t oSmall = 221184;
 
 struct Small {
-    uint64_t bar_tma, bar_mma;
+    uint64_t bar_tma;  // copies landed
+    uint64_t bar_u;    // U_k (U_q, window scores) in TMEM
+    uint64_t bar_q;    // q~, k~ in shared memory (math warps -> control)
+    uint64_t bar_a;    // intra scores in TMEM
+    uint64_t bar_p;    // P_intra in shared memory (math warps -> control)
+    uint64_t bar_o;    // outputs and state update done
+    uint64_t bar_fin;  // drain after an abort
     uint32_t tmem;
     volatile int abort;
     float z[DF], zs[DF], cf[DF];
+    float gpart[4][DF];            // per-quarter gate sums of each feature
     float ps[4][128], pg[4][128];  // per-part window and state denominators of each row
     float tmax[GQ];
     float sinks[GQ][MMAX];
@@ -76,13 +90,18 @@ struct Small {
 constexpr uint32_t kSmemBytes = oSmall + (uint32_t)sizeof(Small) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-// TMEM column bases
-constexpr uint32_t cH = 0, cS = 128, cUq = 256, cUk = 320, cO = 256, cA = 384;
+// TMEM column bases: H [0,128), window scores S [128,256) (the intra scores A reuse its first
+// 32 columns once S is read), U_q [256,320), U_k [320,384), O [384,512).  O has columns of its
+// own so the next step's projections can run while the epilogue still reads O.
+constexpr uint32_t cH = 0, cS = 128, cA = 128, cUq = 256, cUk = 320, cO = 384;
 
 __device__ __forceinline__ float clamp80(float x) { return fminf(fmaxf(x, -80.0f), 80.0f); }
 
-__device__ __forceinline__ float bf16r(float x) {
-    return __bfloat162float(__float2bfloat16_rn(x));
+// 2^x on the special-function unit (inputs here are finite or -inf, which gives +0)
+__device__ __forceinline__ float ex2f(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 // log sigmoid(x) = min(x, 0) - log(1 + e^{-|x|}); the argument of the log is in (1, 2].
@@ -90,40 +109,91 @@ __device__ __forceinline__ float log_sigmoid_fast(float x) {
     return fminf(x, 0.0f) - __logf(1.0f + __expf(-fabsf(x)));
 }
 
+// Round a pair to bf16 (nearest even) in place and return it packed (lo in the low half).
+__device__ __forceinline__ uint32_t round_pair(float& lo, float& hi) {
+    const uint32_t w = pack_bf16(lo, hi);
+    lo = __uint_as_float(w << 16);
+    hi = __uint_as_float(w & 0xFFFF0000u);
+    return w;
+}
+
 __device__ __forceinline__ void unpack8(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
                                         float* o) {
     const uint32_t w[4] = {w0, w1, w2, w3};
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-        __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[k]);
-        float2 f = __bfloat1622float2(h);
-        o[2 * k] = f.x;
-        o[2 * k + 1] = f.y;
+        o[2 * k] = __uint_as_float(w[k] << 16);
+        o[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
     }
 }
 
-// Wait for a barrier phase with a time limit; all threads return the same verdict.
-__device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t& ph, Small& S, WsHeader* hdr,
-                                         unsigned where) {
-    if (!mbar_wait(bar, ph, kTimeout)) {
+// Barrier among the 128 math threads (4 warps) that share one TMEM lane quadrant.
+__device__ __forceinline__ void quad_sync(int quad) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + quad) : "memory");
+}
+// Barrier among the math threads (the control warp never joins it).
+__device__ __forceinline__ void math_sync() { asm volatile("bar.sync 5, 512;" ::: "memory"); }
+// Barrier among the math threads that also returns whether any of them passed `pred`.
+__device__ __forceinline__ bool math_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 6, 512, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// Bounded wait for a barrier phase that also gives up as soon as another thread aborted.
+__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, Small& S) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (S.abort) return false;
+        if (clock64() - t0 > kTimeout) return false;
+    }
+    return true;
+}
+
+// Math threads: every one of them calls this; all return the same verdict.
+__device__ __forceinline__ bool math_wait(uint64_t* bar, uint32_t& ph, Small& S, WsHeader* hdr,
+                                          unsigned where) {
+    const bool fail = !wait_or_abort(bar, ph, S);
+    if (fail && !S.abort) {
         S.abort = 1;
         report(hdr, LIZARD_ERR_TIMEOUT, where);
-    } else {
-        ph ^= 1u;
     }
-    __syncthreads();
-    return S.abort == 0;
+    ph ^= 1u;
+    return !math_any(fail);
 }
 
-// One step's operands: key/value slot of chunk c, the gate tile (and the query tile).
+// Control thread.
+__device__ __forceinline__ bool ctl_wait(uint64_t* bar, uint32_t& ph, Small& S, WsHeader* hdr,
+                                         unsigned where) {
+    if (!wait_or_abort(bar, ph, S)) {
+        if (!S.abort) {
+            S.abort = 1;
+            report(hdr, LIZARD_ERR_TIMEOUT, where);
+        }
+        return false;
+    }
+    ph ^= 1u;
+    return true;
+}
+
+// One step's operands: key/value slot of chunk c, the gate tile (and the query tile); the
+// barrier expects `extra` more bytes from copies the caller issues on the same phase.
 template <bool MAIN>
 __device__ __forceinline__ void issue_step_loads(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmQ,
                                                  const CUtensorMap* tmK, const CUtensorMap* tmV,
                                                  const CUtensorMap* tmG, int64_t c, int64_t kv,
-                                                 int64_t b) {
+                                                 int64_t b, uint32_t extra) {
     const int slot = (int)(c & 3);
     const int t0 = (int)(c * 32);
-    sm100::mbar_arrive_expect_tx(bar, MAIN ? 16384u + 8192u + 32768u : 16384u + 8192u);
+    sm100::mbar_arrive_expect_tx(bar, (MAIN ? 16384u + 8192u + 32768u : 16384u + 8192u) + extra);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
         sm100::tma_load_4d(sm + oK + kb * 16384 + slot * 4096, tmK, bar, 64 * kb, (int)kv, t0, (int)b);
@@ -134,17 +204,119 @@ __device__ __forceinline__ void issue_step_loads(uint8_t* sm, uint64_t* bar, con
     sm100::tma_load_4d(sm + oG, tmG, bar, 0, (int)kv, t0, (int)b);
 }
 
-// Barrier among the 128 threads (4 warps) that share one TMEM lane quadrant.
-__device__ __forceinline__ void quad_sync(int quad) {
-    asm volatile("bar.sync %0, 128;" ::"r"(1 + quad) : "memory");
-}
-
 // K-major (or MN-major) descriptor helpers for the 128-byte-swizzled tiles.
 __device__ __forceinline__ uint64_t kdesc(uint32_t addr) {
     return make_sdesc(addr, 16, 1024, kSwizzle128);
 }
 __device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
     return make_sdesc(addr, lbo, 1024, kSwizzle128);
+}
+
+// The control warp: lane 0 issues the copies and the three MMA groups of every step and
+// hands each result to the math warps through an mbarrier.
+template <bool MAIN>
+__device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_t tb, Small& S,
+                                             WsHeader* hdr, const CUtensorMap* tmQ,
+                                             const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                             const CUtensorMap* tmW, const CUtensorMap* tmG,
+                                             int64_t c_begin, int64_t c_end, int64_t kv, int64_t b) {
+    const uint64_t dQ = kdesc(base + oQ), dQt = kdesc(base + oQt), dK = kdesc(base + oK),
+                   dKi = kdesc(base + oKi), dE = kdesc(base + oE);
+    const uint64_t dW = mndesc(base + oW, 16384), dHs = mndesc(base + oHs, 16384),
+                   dV = mndesc(base + oV, 16384), dKu = mndesc(base + oKu, 4096);
+    uint32_t ph_tma = 0, ph_q = 0, ph_p = 0, ph_o = 0;
+    bool tma_out = false, mma_out = false;
+    if (c_begin < c_end) {
+        // the first step's operands, Wf and the two chunks before the segment (zero-filled
+        // before the sequence start), all on one phase
+        issue_step_loads<MAIN>(sm, &S.bar_tma, tmQ, tmK, tmV, tmG, c_begin, kv, b,
+                               16384u + 2u * 16384u);
+        tma_load_3d(sm + oW, tmW, &S.bar_tma, 0, 0, (int)kv);
+        for (int64_t cc = c_begin - 2; cc < c_begin; ++cc) {
+            const int slot = (int)(cc & 3);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                tma_load_4d(sm + oK + kb * 16384 + slot * 4096, tmK, &S.bar_tma, 64 * kb, (int)kv,
+                            (int)(cc * CT), (int)b);
+                tma_load_4d(sm + oV + kb * 16384 + slot * 4096, tmV, &S.bar_tma, 64 * kb, (int)kv,
+                            (int)(cc * CT), (int)b);
+            }
+        }
+        tma_out = true;
+    }
+    for (int64_t c = c_begin; c < c_end; ++c) {
+        const int slot_d = (int)((c - 2) & 3);
+        if (!ctl_wait(&S.bar_tma, ph_tma, S, hdr, 2)) break;
+        tma_out = false;
+        tc_fence_after();
+        // feature-map projections (and window scores) of this step
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+            const uint64_t bw = dW + ((j * 2048) >> 4);
+            mma_bf16(tb + cUk, dK + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
+            if (MAIN) {
+                mma_bf16(tb + cUq, dQ + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
+                mma_bf16(tb + cS, dQ + koff, dK + koff, idesc_bf16(128, 128, false, false), j > 0);
+            }
+        }
+        mma_commit(&S.bar_u);
+        mma_out = true;
+        if (!ctl_wait(&S.bar_q, ph_q, S, hdr, 6)) break;
+        tc_fence_after();
+        const uint64_t dVd = dV + ((slot_d * 4096) >> 4);
+        if (MAIN) {
+            // intra-step scores A = q~ k~^T
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t qoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                const uint32_t koff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + cA, dQt + qoff, dKi + koff, idesc_bf16(128, 32, false, false), j > 0);
+            }
+            mma_commit(&S.bar_a);
+            if (!ctl_wait(&S.bar_p, ph_p, S, hdr, 7)) break;
+            tc_fence_after();
+            // O = q~ H_s + P_win V_ring + P_intra V_delayed
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + cO, dQt + aoff, dHs + ((j * 2048) >> 4),
+                         idesc_bf16(128, 128, false, true), j > 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + cO, dQ + aoff, dV + ((j * 2048) >> 4),
+                         idesc_bf16(128, 128, false, true), 1);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                mma_bf16(tb + cO, dE + ((j * 32) >> 4), dVd + ((j * 2048) >> 4),
+                         idesc_bf16(128, 128, false, true), 1);
+        }
+        // H += k~u^T V_delayed
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            mma_bf16(tb + cH, dKu + ((j * 2048) >> 4), dVd + ((j * 2048) >> 4),
+                     idesc_bf16(128, 128, true, true), 1);
+        mma_commit(&S.bar_o);
+        if (!ctl_wait(&S.bar_o, ph_o, S, hdr, 8)) break;
+        mma_out = false;
+        // the query tile (P_win), the ring slot of chunk c-3 and the gate tile (staged U_k)
+        // are free now
+        if (c + 1 < c_end) {
+            issue_step_loads<MAIN>(sm, &S.bar_tma, tmQ, tmK, tmV, tmG, c + 1, kv, b, 0u);
+            tma_out = true;
+        }
+    }
+    if (S.abort) {
+        // let copies and MMAs still in flight land before the CTA exits
+        if (mma_out) {
+            mma_commit(&S.bar_fin);
+            mbar_wait(&S.bar_fin, 0, kTimeout);
+        }
+        if (tma_out) mbar_wait(&S.bar_tma, ph_tma, kTimeout);
+    }
 }
 
 template <bool MAIN>
@@ -157,7 +329,6 @@ __global__ void __launch_bounds__(NT, 1)
     const uint32_t base = (raw + 1023u) & ~1023u;
     uint8_t* sm = smem_raw + (base - raw);
     Small& S = *reinterpret_cast<Small*>(sm + oSmall);
-    float* gpart = reinterpret_cast<float*>(sm + oQt);       // [4][DF], gates phase only
     float* xpm = reinterpret_cast<float*>(sm + oKu);         // [4][128] window partial max
     float* xum = xpm + 512;                                   // [4][128] u partial extreme
     float* xus = xpm + 1024;                                  // [4][128] u partial sum
@@ -165,7 +336,7 @@ __global__ void __launch_bounds__(NT, 1)
     float* suk = reinterpret_cast<float*>(sm + oG);          // [32][64] staged U_k rows
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quad = warp & 3, part = warp >> 2;
+    const int quad = warp & 3, part = (warp >> 2) & 3;
     const int row = 32 * quad + lane;
     const int64_t unit = blockIdx.x, seg = blockIdx.y;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
@@ -174,6 +345,7 @@ __global__ void __launch_bounds__(NT, 1)
     const int64_t s1 = min64(p.L, s0 + p.seg_len);
     WsHeader* hdr = (WsHeader*)a.header;
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    const int64_t c_begin = s0 / CT, c_end = (s1 + CT - 1) / CT;
 
     if (warp == 0) {
         tmem_alloc(&S.tmem, 512);
@@ -181,9 +353,16 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (tid == 0) {
         mbar_init(&S.bar_tma, 1);
-        mbar_init(&S.bar_mma, 1);
+        mbar_init(&S.bar_u, 1);
+        mbar_init(&S.bar_q, 1);
+        mbar_init(&S.bar_a, 1);
+        mbar_init(&S.bar_p, 1);
+        mbar_init(&S.bar_o, 1);
+        mbar_init(&S.bar_fin, 1);
         fence_mbar_init();
         S.abort = 0;
+    }
+    if (warp == NW && lane == 0) {
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmW);
@@ -198,7 +377,7 @@ __global__ void __launch_bounds__(NT, 1)
         if (tid < GQ) {
             float tm = kMinShift;
             for (int mm = 0; mm < p.M; ++mm) tm = fmaxf(tm, a.sinks[(kv * GQ + tid) * p.M + mm]);
-            S.tmax[tid] = tm;
+            S.tmax[tid] = tm * kLog2e;
         }
     }
     // zero both rings: P_win is 0 on masked keys, but 0 times non-finite stale bits is NaN
@@ -211,460 +390,396 @@ __global__ void __launch_bounds__(NT, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = S.tmem;
-    // operand descriptors at the tile bases; the start-address field (bits 0-13, in 16-byte
-    // units) advances by (byte offset >> 4) for each K step
-    const uint64_t dQ = kdesc(base + oQ), dQt = kdesc(base + oQt), dK = kdesc(base + oK),
-                   dKi = kdesc(base + oKi), dE = kdesc(base + oE);
-    const uint64_t dW = mndesc(base + oW, 16384), dHs = mndesc(base + oHs, 16384),
-                   dV = mndesc(base + oV, 16384), dKu = mndesc(base + oKu, 4096);
 
-    // starting state H into TMEM (fp32 master copy), lane = feature f, column = d
-    {
-        float v[32];
-        const int col = 32 * part;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + col + k] : 0.0f;
-        tmem_st32(tb + lane_off + cH + col, v);
-        tmem_wait_st();
-    }
-
-    uint32_t ph_tma = 0, ph_mma = 0;
-    bool tma_pending = false, mma_pending = false;
-    const int64_t c_begin = s0 / CT, c_end = (s1 + CT - 1) / CT;
-    float lam_tot = 0.0f;
-    bool ok = true;
-
-    // Wf and the two chunks before the segment (zero-filled before the sequence start)
-    if (tid == 0) {
-        mbar_arrive_expect_tx(&S.bar_tma, 16384u + 2u * 16384u);
-        tma_load_3d(sm + oW, &tmW, &S.bar_tma, 0, 0, (int)kv);
-        for (int64_t cc = c_begin - 2; cc < c_begin; ++cc) {
-            const int slot = (int)(cc & 3);
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                tma_load_4d(sm + oK + kb * 16384 + slot * 4096, &tmK, &S.bar_tma, 64 * kb, (int)kv,
-                            (int)(cc * CT), (int)b);
-                tma_load_4d(sm + oV + kb * 16384 + slot * 4096, &tmV, &S.bar_tma, 64 * kb, (int)kv,
-                            (int)(cc * CT), (int)b);
-            }
-        }
-    }
-    tma_pending = true;
-    ok = wait_bar(&S.bar_tma, ph_tma, S, hdr, 1);
-    if (ok) tma_pending = false;
-    // the first step's operands; every later step's are issued at the end of the step before
-    if (ok && tid == 0 && c_begin < c_end)
-        issue_step_loads<MAIN>(sm, &S.bar_tma, &tmQ, &tmK, &tmV, &tmG, c_begin, kv, b);
-    tma_pending = c_begin < c_end;
-
-    for (int64_t c = c_begin; ok && c < c_end; ++c) {
-        const int64_t t0 = c * CT;
-        const int n = (int)min64(CT, s1 - t0);
-        const int slot_d = (int)((c - 2) & 3);
-
-        // (1) this step's keys, values, gates (and queries) have landed
-        ok = wait_bar(&S.bar_tma, ph_tma, S, hdr, 2);
-        if (!ok) break;
-        tma_pending = false;
-
-        // (2) feature-map projections and window scores on the tensor cores; they need only
-        //     this step's operands, so they run while the threads fold the gates
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
-                const uint64_t bw = dW + ((j * 2048) >> 4);
-                mma_bf16(tb + cUk, dK + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
-                if (MAIN) {
-                    mma_bf16(tb + cUq, dQ + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
-                    mma_bf16(tb + cS, dQ + koff, dK + koff, idesc_bf16(128, 128, false, false),
-                             j > 0);
-                }
-            }
-            mma_commit(&S.bar_mma);
-        }
-
-        // (3) gates: cumulative log-sigmoid per feature; four threads per feature, one per
-        //     8-token quarter; the reference r = b_15 is the first two quarters' total
-        const int gf = tid & (DF - 1), gq = tid >> 7;
-        float bt[CT / 4];
+    if (warp == NW) {
+        if (lane == 0)
+            control_loop<MAIN>(sm, base, tb, S, hdr, &tmQ, &tmK, &tmV, &tmW, &tmG, c_begin, c_end,
+                               kv, b);
+        __syncwarp();
+    } else {
+        // starting state H into TMEM (fp32 master copy), lane = feature f, column = d
         {
-            const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + oG);
-            float run = 0.0f;
-#pragma unroll
-            for (int t = 0; t < CT / 4; ++t) {
-                const int tt = (CT / 4) * gq + t;
-                const float lam = tt < n ? log_sigmoid_fast(__bfloat162float(sg[tt * DF + gf])) : 0.0f;
-                run += lam;
-                bt[t] = run;
-            }
-            gpart[gq * DF + gf] = run;
-        }
-        __syncthreads();
-        {
-            const float g0 = gpart[gf], g1 = gpart[DF + gf], g2 = gpart[2 * DF + gf],
-                        g3 = gpart[3 * DF + gf];
-            const float bref = g0 + g1, blast = bref + g2 + g3;
-            const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? bref : bref + g2;
-            __nv_bfloat16* Eq = (__nv_bfloat16*)(sm + oE);
-            __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + oE + 8192);
-#pragma unroll
-            for (int t = 0; t < CT / 4; ++t) {
-                const int tt = (CT / 4) * gq + t;
-                const float btt = bt[t] + off;
-                if (MAIN) Eq[tt * DF + gf] = __float2bfloat16_rn(__expf(clamp80(btt - bref)));
-                Ek[tt * DF + gf] = __float2bfloat16_rn(__expf(clamp80(bref - btt)));
-            }
-            if (gq == 0) {
-                S.cf[gf] = __expf(blast - bref);
-                S.zs[gf] = __expf(bref) * S.z[gf];
-                lam_tot += blast;
-            }
-        }
-
-        // (4) ... while the threads make the state's bf16 copy scaled by e^{r} for the readout
-        //     and decay the fp32 master by e^{b_31} (TMEM columns the MMAs do not touch)
-        {
-            const int f = row;
-            const float g0 = gpart[f], g1 = gpart[DF + f], g2 = gpart[2 * DF + f],
-                        g3 = gpart[3 * DF + f];
-            const float er = __expf(g0 + g1), el = __expf(g0 + g1 + g2 + g3);
-            const int col = 32 * part;
             float v[32];
-            tmem_ld32(tb + lane_off + cH + col, v);
-            tmem_wait_ld();
-            if (MAIN) {
+            const int col = 32 * part;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const int nchunk = (col & 63) / 8 + ch;
-                    st_shared_v4(base + oHs + (col / 64) * 16384 + sw128(f, nchunk),
-                                 pack_bf16(er * v[8 * ch], er * v[8 * ch + 1]),
-                                 pack_bf16(er * v[8 * ch + 2], er * v[8 * ch + 3]),
-                                 pack_bf16(er * v[8 * ch + 4], er * v[8 * ch + 5]),
-                                 pack_bf16(er * v[8 * ch + 6], er * v[8 * ch + 7]));
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] *= el;
+            for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + col + k] : 0.0f;
             tmem_st32(tb + lane_off + cH + col, v);
             tmem_wait_st();
         }
-        mma_pending = true;
-        ok = wait_bar(&S.bar_mma, ph_mma, S, hdr, 3);
-        if (!ok) break;
-        mma_pending = false;
-        tc_fence_after();
+        uint32_t ph_tma = 0, ph_u = 0, ph_a = 0, ph_o = 0;
+        float lam_tot = 0.0f;
+        bool ok = true;
 
-        // (5) window softmax over the ring slot `part`, the query feature map, U_k staging
-        const int i = row >> 2, hh = row & 3;
-        const int64_t qa = t0 + i;
-        const bool qv = i < n;
-        float m_row = 0.0f;
-        float sv[32], uv[32];
-        int ulo = 1, uhi = 0;
-        if (MAIN) {
-            tmem_ld32(tb + lane_off + cS + 32 * part, sv);
-            tmem_ld32(tb + lane_off + cUq + 32 * (part & 1), uv);
-        }
-        if (quad == slot_d && part < 2) {
-            float w[32];
-            tmem_ld32(tb + lane_off + cUk + 32 * part, w);
-            tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 32; k += 4)
-                *reinterpret_cast<float4*>(suk + lane * 64 + 32 * part + k) =
-                    make_float4(w[k], w[k + 1], w[k + 2], w[k + 3]);
-        }
-        if (MAIN) {
-            tmem_wait_ld();
-            // keys of ring slot `part` are tokens 32 (c - age) + u; the valid u form one interval
+        for (int64_t c = c_begin; c < c_end; ++c) {
+            const int64_t t0 = c * CT;
+            const int n = (int)min64(CT, s1 - t0);
+            const int slot_d = (int)((c - 2) & 3);
+
+            // (1) this step's keys, values, gates (and queries) have landed; the control warp
+            //     has started the feature-map projections and window scores
+            ok = math_wait(&S.bar_tma, ph_tma, S, hdr, 2);
+            if (!ok) break;
+
+            // (2) gates: cumulative log-sigmoid per feature; four threads per feature, one per
+            //     8-token quarter; the reference r = b_15 is the first two quarters' total
+            const int gf = tid & (DF - 1), gq = tid >> 7;
+            float bt[CT / 4];
             {
-                const int64_t age = (c - part) & 3;
-                const int64_t kbase = (c - age) * CT;
-                const int64_t lo = max64(max64(0, qa - WIN + 1 - kbase), -kbase);
-                const int64_t hi = min64(31, qa - kbase);
-                if (qv && age <= 2) {
-                    ulo = (int)lo;
-                    uhi = (int)hi;
+                const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + oG);
+                float run = 0.0f;
+#pragma unroll
+                for (int t = 0; t < CT / 4; ++t) {
+                    const int tt = (CT / 4) * gq + t;
+                    const float lam =
+                        tt < n ? log_sigmoid_fast(__bfloat162float(sg[tt * DF + gf])) : 0.0f;
+                    run += lam;
+                    bt[t] = run;
+                }
+                S.gpart[gq][gf] = run;
+            }
+            math_sync();
+            {
+                const float g0 = S.gpart[0][gf], g1 = S.gpart[1][gf], g2 = S.gpart[2][gf],
+                            g3 = S.gpart[3][gf];
+                const float bref = g0 + g1, blast = bref + g2 + g3;
+                const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? bref : bref + g2;
+                __nv_bfloat16* Eq = (__nv_bfloat16*)(sm + oE);
+                __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + oE + 8192);
+#pragma unroll
+                for (int t = 0; t < CT / 4; ++t) {
+                    const int tt = (CT / 4) * gq + t;
+                    const float btt = bt[t] + off;
+                    if (MAIN) Eq[tt * DF + gf] = __float2bfloat16_rn(__expf(clamp80(btt - bref)));
+                    Ek[tt * DF + gf] = __float2bfloat16_rn(__expf(clamp80(bref - btt)));
+                }
+                if (gq == 0) {
+                    S.cf[gf] = __expf(blast - bref);
+                    S.zs[gf] = __expf(bref) * S.z[gf];
+                    lam_tot += blast;
                 }
             }
-            float pmax = -INFINITY;
+
+            // (3) the state's bf16 copy scaled by e^{r} for the readout, and the fp32 master
+            //     decayed by e^{b_31} (TMEM columns no MMA in flight touches)
+            {
+                const int f = row;
+                const float g0 = S.gpart[0][f], g1 = S.gpart[1][f], g2 = S.gpart[2][f],
+                            g3 = S.gpart[3][f];
+                const float er = __expf(g0 + g1), el = __expf(g0 + g1 + g2 + g3);
+                const int col = 32 * part;
+                float v[32];
+                tmem_ld32(tb + lane_off + cH + col, v);
+                tmem_wait_ld();
+                if (MAIN) {
 #pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                sv[k] *= p.scale;
-                if (k >= ulo && k <= uhi) pmax = fmaxf(pmax, sv[k]);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        const int nchunk = (col & 63) / 8 + ch;
+                        st_shared_v4(base + oHs + (col / 64) * 16384 + sw128(f, nchunk),
+                                     pack_bf16(er * v[8 * ch], er * v[8 * ch + 1]),
+                                     pack_bf16(er * v[8 * ch + 2], er * v[8 * ch + 3]),
+                                     pack_bf16(er * v[8 * ch + 4], er * v[8 * ch + 5]),
+                                     pack_bf16(er * v[8 * ch + 6], er * v[8 * ch + 7]));
+                    }
+                }
+#pragma unroll
+                for (int k = 0; k < 32; ++k) v[k] *= el;
+                tmem_st32(tb + lane_off + cH + col, v);
+                tmem_wait_st();
             }
-            float uext = uv[0];
+            ok = math_wait(&S.bar_u, ph_u, S, hdr, 3);
+            if (!ok) break;
+            tc_fence_after();
+
+            // (4) window softmax over the ring slot `part`, the query feature map, U_k staging.
+            //     Exponents are kept in base 2: m2 = m log2(e).
+            const int i = row >> 2, hh = row & 3;
+            const int64_t qa = t0 + i;
+            const bool qv = i < n;
+            float m2 = 0.0f;
+            if (quad == slot_d && part < 2) {
+                float w[32];
+                tmem_ld32(tb + lane_off + cUk + 32 * part, w);
+                tmem_wait_ld();
 #pragma unroll
-            for (int k = 1; k < 32; ++k) uext = part < 2 ? fmaxf(uext, uv[k]) : fminf(uext, uv[k]);
-            xpm[part * 128 + row] = pmax;
-            xum[part * 128 + row] = uext;
-        }
-        // the exchanges below stay within the 4 warps of a lane quadrant (one row per lane);
-        // the staged U_k rows are read after the full barrier at the end of this phase
-        if (MAIN) quad_sync(quad);
-        if (MAIN) {
-            m_row = fmaxf(fmaxf(fmaxf(xpm[row], xpm[128 + row]), fmaxf(xpm[256 + row], xpm[384 + row])),
-                          S.tmax[hh]);
-            float psum = 0.0f;
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(suk + lane * 64 + 32 * part + k) =
+                        make_float4(w[k], w[k + 1], w[k + 2], w[k + 3]);
+            }
+            if (MAIN) {
+                // keys of ring slot `part` are tokens 32 (c - age) + u; the slot that is three
+                // steps old, and slots before the sequence start, hold no key of the window
+                const int age = (int)((c - part) & 3);
+                const bool live = age <= 2 && c >= age;  // same for the whole warp
+                const int sib = part ^ 1;
+                const float s2 = p.scale * kLog2e;
+                uint32_t vm = 0;  // bit u: key u of the slot is in this row's window
+                if (live && qv) {
+                    const int64_t kbase = (c - age) * CT;
+                    const int64_t lo = max64(0, qa - WIN + 1 - kbase);
+                    const int64_t hi = min64(31, qa - kbase);
+                    if (hi >= lo) vm = (uint32_t)(((2ull << hi) - 1ull) & ~((1ull << lo) - 1ull));
+                }
+                // first pass: row maxima (scores and u); the rows are read again from TMEM
+                // after the exchange rather than held in registers across it
+                {
+                    float pmax = -INFINITY;
+                    if (live) {
+                        float sv[32];
+                        tmem_ld32(tb + lane_off + cS + 32 * part, sv);
+                        tmem_wait_ld();
 #pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
+                        for (int k = 0; k < 32; ++k)
+                            pmax = fmaxf(pmax, ((vm >> k) & 1u) ? sv[k] * s2 : -INFINITY);
+                    }
+                    float uv[32];
+                    tmem_ld32(tb + lane_off + cUq + 32 * (part & 1), uv);
+                    tmem_wait_ld();
+                    // parts 0, 1 take softmax(+u) over features [0, 64), parts 2, 3 softmax(-u)
+                    float uext = -INFINITY;
+                    if (part < 2) {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) uext = fmaxf(uext, uv[k]);
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) uext = fmaxf(uext, -uv[k]);
+                    }
+                    xpm[part * 128 + row] = pmax;
+                    xum[part * 128 + row] = uext;
+                }
+                // the exchanges below stay within the 4 warps of a lane quadrant (one row per
+                // lane); the staged U_k rows are read after the barrier at the end of this phase
+                quad_sync(quad);
+                m2 = fmaxf(fmaxf(fmaxf(xpm[row], xpm[128 + row]), fmaxf(xpm[256 + row], xpm[384 + row])),
+                           S.tmax[hh]);
+                float psum = 0.0f;
+                if (live) {
+                    float sv[32];
+                    tmem_ld32(tb + lane_off + cS + 32 * part, sv);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
+                        float pv[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const int k = 8 * ch + e;
+                            pv[e] = ex2f(((vm >> k) & 1u) ? fmaf(sv[k], s2, -m2) : -INFINITY);
+                        }
+                        const uint32_t w0 = round_pair(pv[0], pv[1]), w1 = round_pair(pv[2], pv[3]),
+                                       w2 = round_pair(pv[4], pv[5]), w3 = round_pair(pv[6], pv[7]);
+                        psum += ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
+                        st_shared_v4(base + oQ + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                                     w0, w1, w2, w3);
+                    }
+                } else {
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
+                        st_shared_v4(base + oQ + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                                     0u, 0u, 0u, 0u);
+                }
+                S.ps[part][row] = psum;
+                const float f2 = part < 2 ? kLog2e : -kLog2e;
+                const float cst = -fmaxf(xum[part * 128 + row], xum[sib * 128 + row]) * kLog2e;
+                float uv[32];
+                tmem_ld32(tb + lane_off + cUq + 32 * (part & 1), uv);
+                tmem_wait_ld();
+                float usum = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    uv[k] = ex2f(fmaf(uv[k], f2, cst));
+                    usum += uv[k];
+                }
+                xus[part * 128 + row] = usum;
+                quad_sync(quad);
+                // q~ = phi(q) e^{b_i - r} e^{-m}: features [32 part, 32 part + 32)
+                const float sc = ex2f(-m2) / (xus[part * 128 + row] + xus[sib * 128 + row]);
+                float pg = 0.0f;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    const int f0 = 32 * part + 8 * ch;
+                    uint32_t w0, w1, w2, w3;
+                    ld_shared_v4(base + oE + (uint32_t)(i * DF + f0) * 2u, w0, w1, w2, w3);
+                    float eq[8], qv8[8];
+                    unpack8(w0, w1, w2, w3, eq);
+                    const float4 za = *reinterpret_cast<const float4*>(&S.zs[f0]);
+                    const float4 zb = *reinterpret_cast<const float4*>(&S.zs[f0 + 4]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) qv8[e] = uv[8 * ch + e] * sc * eq[e];
+                    const uint32_t q0 = round_pair(qv8[0], qv8[1]), q1 = round_pair(qv8[2], qv8[3]),
+                                   q2 = round_pair(qv8[4], qv8[5]), q3 = round_pair(qv8[6], qv8[7]);
+                    pg = fmaf(qv8[0], za.x, pg);
+                    pg = fmaf(qv8[1], za.y, pg);
+                    pg = fmaf(qv8[2], za.z, pg);
+                    pg = fmaf(qv8[3], za.w, pg);
+                    pg = fmaf(qv8[4], zb.x, pg);
+                    pg = fmaf(qv8[5], zb.y, pg);
+                    pg = fmaf(qv8[6], zb.z, pg);
+                    pg = fmaf(qv8[7], zb.w, pg);
+                    st_shared_v4(base + oQt + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                                 q0, q1, q2, q3);
+                }
+                S.pg[part][row] = pg;
+            }
+            math_sync();
+
+            // (5) phi of the delayed keys (the ring slot two steps back) from the staged U_k
+            //     rows: 16 threads per key, 4 u-values each -> k~ for the intra scores and the
+            //     update
+            {
+                const int t = tid >> 4, sub = tid & 15;
+                const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
+                const float4 u4 = *reinterpret_cast<const float4*>(suk + t * 64 + 4 * sub);
+                const float u[4] = {u4.x, u4.y, u4.z, u4.w};
+                float mx = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
+                float mn = fminf(fminf(u[0], u[1]), fminf(u[2], u[3]));
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                }
+                const float cmx = -mx * kLog2e, cmn = mn * kLog2e;
+                float ep[4], en[4], sp = 0.0f, sn = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    ep[e] = ex2f(fmaf(u[e], kLog2e, cmx));
+                    en[e] = ex2f(fmaf(u[e], -kLog2e, cmn));
+                    sp += ep[e];
+                    sn += en[e];
+                }
+#pragma unroll
+                for (int o = 1; o < 16; o <<= 1) {
+                    sp += __shfl_xor_sync(0xffffffffu, sp, o);
+                    sn += __shfl_xor_sync(0xffffffffu, sn, o);
+                }
+                const float ip = dvalid ? 1.0f / sp : 0.0f, in = dvalid ? 1.0f / sn : 0.0f;
+                const __nv_bfloat16* Ek = (const __nv_bfloat16*)(sm + oE + 8192);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    const int f0 = 64 * kb + 4 * sub;  // features f0..f0+3 (kb 0: softmax(u), 1: -u)
+                    float ki[4], ku[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float ph = kb == 0 ? ep[e] * ip : en[e] * in;
+                        ki[e] = ph * __bfloat162float(Ek[t * DF + f0 + e]);
+                        ku[e] = ki[e] * S.cf[f0 + e];
+                    }
+                    const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
+                    if (MAIN) {
+                        const uint32_t a0 = pack_bf16(ki[0], ki[1]), a1 = pack_bf16(ki[2], ki[3]);
+                        asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + oKi + off),
+                                     "r"(a0), "r"(a1)
+                                     : "memory");
+                    }
+                    const uint32_t b0 = pack_bf16(ku[0], ku[1]), b1 = pack_bf16(ku[2], ku[3]);
+                    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + oKu + off), "r"(b0),
+                                 "r"(b1)
+                                 : "memory");
+                }
+            }
+            fence_async_smem();
+            tc_fence_before();
+            math_sync();
+            if (tid == 0) mbar_arrive(&S.bar_q);
+
+            // z <- e^{b_31} z + sum_t k~u_t (read back from the bf16 tile the MMA uses)
+            if (tid < DF) {
+                const int f = tid;
+                float zsum = 0.0f;
+                const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + oKu);
+                for (int t = 0; t < CT; ++t) {
+                    const uint32_t off = (f >> 6) * 4096 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
+                    zsum += __bfloat162float(ku[off / 2]);
+                }
+                S.z[f] = fmaf(S.cf[f] * S.zs[f], 1.0f, zsum);  // e^{b_31} z = e^{b_31-r} e^{r} z
+            }
+            float inv = 0.0f;
+            if (MAIN) {
+                ok = math_wait(&S.bar_a, ph_a, S, hdr, 4);
+                if (!ok) break;
+                tc_fence_after();
+                // (6) P_intra: columns t in [8 part, 8 part + 8)
+                float av[8];
+                tmem_ld8(tb + lane_off + cA + 8 * part, av);
+                tmem_wait_ld();
                 float pv[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    const int k = 8 * ch + e;
-                    pv[e] = (k >= ulo && k <= uhi) ? bf16r(__expf(sv[k] - m_row)) : 0.0f;
-                    psum += pv[e];
+                    const int t = 8 * part + e;
+                    const bool valid = qv && t <= i && (t0 + t - WIN >= 0);
+                    pv[e] = valid ? av[e] : 0.0f;
                 }
-                st_shared_v4(base + oQ + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
-                             pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
-                             pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
-            }
-            S.ps[part][row] = psum;
-            const int sib = part ^ 1;
-            const float uext = part < 2 ? fmaxf(xum[part * 128 + row], xum[sib * 128 + row])
-                                        : fminf(xum[part * 128 + row], xum[sib * 128 + row]);
-            float usum = 0.0f;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) {
-                uv[k] = __expf(part < 2 ? (uv[k] - uext) : (uext - uv[k]));
-                usum += uv[k];
-            }
-            xus[part * 128 + row] = usum;
-        }
-        if (MAIN) quad_sync(quad);
-        if (MAIN) {
-            // q~ = phi(q) e^{b_i - r} e^{-m}: features [32 part, 32 part + 32)
-            const float sc = __expf(-m_row) / (xus[part * 128 + row] + xus[(part ^ 1) * 128 + row]);
-            float pg = 0.0f;
-#pragma unroll
-            for (int ch = 0; ch < 4; ++ch) {
-                const int f0 = 32 * part + 8 * ch;
-                uint32_t w0, w1, w2, w3;
-                ld_shared_v4(base + oE + (uint32_t)(i * DF + f0) * 2u, w0, w1, w2, w3);
-                float eq[8], qv8[8];
-                unpack8(w0, w1, w2, w3, eq);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    qv8[e] = bf16r(uv[8 * ch + e] * sc * eq[e]);
-                    pg = fmaf(qv8[e], S.zs[f0 + e], pg);
+                const uint32_t w0 = round_pair(pv[0], pv[1]), w1 = round_pair(pv[2], pv[3]),
+                               w2 = round_pair(pv[4], pv[5]), w3 = round_pair(pv[6], pv[7]);
+                st_shared_v4(base + oE + sw128(row, part), w0, w1, w2, w3);
+                spi[part * 128 + row] =
+                    ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
+                fence_async_smem();
+                tc_fence_before();
+                math_sync();
+                if (tid == 0) mbar_arrive(&S.bar_p);
+                // the shared normaliser of this row, while the output MMAs run
+                if (qv) {
+                    float ssum = 0.0f;
+                    for (int mm = 0; mm < p.M; ++mm)
+                        ssum += ex2f(fmaf(S.sinks[hh][mm], kLog2e, -m2));
+                    const float den = (S.ps[0][row] + S.ps[1][row]) + (S.ps[2][row] + S.ps[3][row]) +
+                                      (S.pg[0][row] + S.pg[1][row]) + (S.pg[2][row] + S.pg[3][row]) +
+                                      (spi[row] + spi[128 + row]) + (spi[256 + row] + spi[384 + row]) +
+                                      ssum;
+                    inv = 1.0f / den;
+                    if (part == 0 && a.lse != nullptr)
+                        a.lse[(b * p.L + qa) * p.Hq + kv * GQ + hh] = m2 * kLn2 + __logf(den);
                 }
-                st_shared_v4(base + oQt + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
-                             pack_bf16(qv8[0], qv8[1]), pack_bf16(qv8[2], qv8[3]),
-                             pack_bf16(qv8[4], qv8[5]), pack_bf16(qv8[6], qv8[7]));
             }
-            S.pg[part][row] = pg;
-        }
-        __syncthreads();
-
-        // (6) phi of the delayed keys (the ring slot two steps back) from the staged U_k rows:
-        //     16 threads per key, 4 u-values each -> k~ for the intra scores and the update
-        {
-            const int t = tid >> 4, sub = tid & 15;
-            const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
-            const float4 u4 = *reinterpret_cast<const float4*>(suk + t * 64 + 4 * sub);
-            const float u[4] = {u4.x, u4.y, u4.z, u4.w};
-            float mx = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
-            float mn = fminf(fminf(u[0], u[1]), fminf(u[2], u[3]));
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) {
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            }
-            float ep[4], en[4], sp = 0.0f, sn = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                ep[e] = __expf(u[e] - mx);
-                en[e] = __expf(mn - u[e]);
-                sp += ep[e];
-                sn += en[e];
-            }
-#pragma unroll
-            for (int o = 1; o < 16; o <<= 1) {
-                sp += __shfl_xor_sync(0xffffffffu, sp, o);
-                sn += __shfl_xor_sync(0xffffffffu, sn, o);
-            }
-            const float ip = dvalid ? 1.0f / sp : 0.0f, in = dvalid ? 1.0f / sn : 0.0f;
-            const __nv_bfloat16* Ek = (const __nv_bfloat16*)(sm + oE + 8192);
-#pragma unroll
-            for (int kb = 0; kb < 2; ++kb) {
-                const int f0 = 64 * kb + 4 * sub;  // features f0..f0+3 (kb 0: softmax(u), 1: -u)
-                float ki[4], ku[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float ph = kb == 0 ? ep[e] * ip : en[e] * in;
-                    ki[e] = ph * __bfloat162float(Ek[t * DF + f0 + e]);
-                    ku[e] = ki[e] * S.cf[f0 + e];
-                }
-                const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
-                if (MAIN) {
-                    const uint32_t a0 = pack_bf16(ki[0], ki[1]), a1 = pack_bf16(ki[2], ki[3]);
-                    asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + oKi + off), "r"(a0),
-                                 "r"(a1)
-                                 : "memory");
-                }
-                const uint32_t b0 = pack_bf16(ku[0], ku[1]), b1 = pack_bf16(ku[2], ku[3]);
-                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + oKu + off), "r"(b0),
-                             "r"(b1)
-                             : "memory");
-            }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // (7) intra-step scores A = q~ k~^T
-        if (MAIN && tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t qoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
-                const uint32_t koff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
-                mma_bf16(tb + cA, dQt + qoff, dKi + koff, idesc_bf16(128, 32, false, false), j > 0);
-            }
-            mma_commit(&S.bar_mma);
-        }
-        // z <- e^{b_31} z + sum_t k~u_t (read back from the bf16 tile the MMA uses)
-        if (tid < DF) {
-            const int f = tid;
-            float zsum = 0.0f;
-            const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + oKu);
-            for (int t = 0; t < CT; ++t) {
-                const uint32_t off = (f >> 6) * 4096 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
-                zsum += __bfloat162float(ku[off / 2]);
-            }
-            S.z[f] = fmaf(S.cf[f] * S.zs[f], 1.0f, zsum);  // e^{b_31} z = e^{b_31-r} e^{r} z
-        }
-        float pi_row = 0.0f;
-        if (MAIN) {
-            mma_pending = true;
-            ok = wait_bar(&S.bar_mma, ph_mma, S, hdr, 4);
+            ok = math_wait(&S.bar_o, ph_o, S, hdr, 5);
             if (!ok) break;
-            mma_pending = false;
             tc_fence_after();
-            // P_intra: columns t in [8 part, 8 part + 8)
-            float av[8];
-            tmem_ld8(tb + lane_off + cA + 8 * part, av);
-            tmem_wait_ld();
-            float pv[8];
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int t = 8 * part + e;
-                const bool valid = qv && t <= i && (t0 + t - WIN >= 0);
-                pv[e] = valid ? bf16r(av[e]) : 0.0f;
-                pi_row += pv[e];
-            }
-            st_shared_v4(base + oE + sw128(row, part), pack_bf16(pv[0], pv[1]),
-                         pack_bf16(pv[2], pv[3]), pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
-            spi[part * 128 + row] = pi_row;
-            fence_async_smem();
-            tc_fence_before();
-            __syncthreads();
-        }
 
-        // (8) outputs and the state update
-        if (tid == 0) {
-            tc_fence_after();
-            const uint64_t dVd = dV + ((slot_d * 4096) >> 4);
+            // (7) epilogue: y = O / den over columns [32 part, 32 part + 32), 16-byte bf16 stores
             if (MAIN) {
+                float ov[32];
+                const int col = 32 * part;
+                tmem_ld32(tb + lane_off + cO + col, ov);
+                tmem_wait_ld();
+                if (qv) {
+                    __nv_bfloat16* yr = (__nv_bfloat16*)a.y +
+                                        ((b * p.L + qa) * p.Hq + kv * GQ + hh) * DH + col;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
-                    mma_bf16(tb + cO, dQt + aoff, dHs + ((j * 2048) >> 4),
-                             idesc_bf16(128, 128, false, true), j > 0);
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint4 w;
+                        w.x = pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv);
+                        w.y = pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv);
+                        w.z = pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv);
+                        w.w = pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv);
+                        *reinterpret_cast<uint4*>(yr + 8 * ch) = w;
+                    }
                 }
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
-                    mma_bf16(tb + cO, dQ + aoff, dV + ((j * 2048) >> 4),
-                             idesc_bf16(128, 128, false, true), 1);
-                }
-#pragma unroll
-                for (int j = 0; j < 2; ++j)
-                    mma_bf16(tb + cO, dE + ((j * 32) >> 4), dVd + ((j * 2048) >> 4),
-                             idesc_bf16(128, 128, false, true), 1);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-                mma_bf16(tb + cH, dKu + ((j * 2048) >> 4), dVd + ((j * 2048) >> 4),
-                         idesc_bf16(128, 128, true, true), 1);
-            mma_commit(&S.bar_mma);
-        }
-        mma_pending = true;
-        ok = wait_bar(&S.bar_mma, ph_mma, S, hdr, 5);
-        if (!ok) break;
-        mma_pending = false;
-        tc_fence_after();
-        // the next step's operands fly during the epilogue: the query tile (P_win), the ring
-        // slot (chunk c-3) and the gate tile (U_k staging) are no longer read
-        if (tid == 0 && c + 1 < c_end)
-            issue_step_loads<MAIN>(sm, &S.bar_tma, &tmQ, &tmK, &tmV, &tmG, c + 1, kv, b);
-        tma_pending = c + 1 < c_end;
-
-        // (9) epilogue: y = O / den over columns [32 part, 32 part + 32), 16-byte bf16 stores
-        if (MAIN) {
-            float ov[32];
-            const int col = 32 * part;
-            tmem_ld32(tb + lane_off + cO + col, ov);
-            tmem_wait_ld();
-            if (qv) {
-                float ssum = 0.0f;
-                for (int mm = 0; mm < p.M; ++mm) ssum += __expf(S.sinks[hh][mm] - m_row);
-                const float den = (S.ps[0][row] + S.ps[1][row]) + (S.ps[2][row] + S.ps[3][row]) +
-                                  (S.pg[0][row] + S.pg[1][row]) + (S.pg[2][row] + S.pg[3][row]) +
-                                  (spi[row] + spi[128 + row]) + (spi[256 + row] + spi[384 + row]) +
-                                  ssum;
-                const float inv = 1.0f / den;
-                __nv_bfloat16* yr = (__nv_bfloat16*)a.y +
-                                    ((b * p.L + qa) * p.Hq + kv * GQ + hh) * DH + col;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint4 w;
-                    w.x = pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv);
-                    w.y = pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv);
-                    w.z = pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv);
-                    w.w = pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv);
-                    *reinterpret_cast<uint4*>(yr + 8 * ch) = w;
-                }
-                if (part == 0 && a.lse != nullptr)
-                    a.lse[(b * p.L + qa) * p.Hq + kv * GQ + hh] = m_row + __logf(den);
             }
         }
-        tc_fence_before();
-        __syncthreads();
-    }
 
-    if (ok) {
-        // final state of the segment: the local record (segment pass) or the decode hand-off
-        float* dstH = nullptr;
-        float* dstz = nullptr;
-        if (!MAIN) {
-            float* r = a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats;
-            dstH = r;
-            dstz = r + DF * DH;
-            if (tid < DF) r[DF * DH + DF + tid] = lam_tot;
-        } else if (a.S_out != nullptr && s1 == p.L) {
-            dstH = a.S_out + unit * DF * DH;
-            dstz = a.z_out + unit * DF;
-        }
-        if (dstH != nullptr) {
-            tc_fence_after();
-            float v[32];
-            const int col = 32 * part;
-            tmem_ld32(tb + lane_off + cH + col, v);
-            tmem_wait_ld();
+        if (ok) {
+            // final state of the segment: the local record (segment pass) or the decode hand-off
+            float* dstH = nullptr;
+            float* dstz = nullptr;
+            if (!MAIN) {
+                float* r = a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats;
+                dstH = r;
+                dstz = r + DF * DH;
+                if (tid < DF) r[DF * DH + DF + tid] = lam_tot;
+            } else if (a.S_out != nullptr && s1 == p.L) {
+                dstH = a.S_out + unit * DF * DH;
+                dstz = a.z_out + unit * DF;
+            }
+            if (dstH != nullptr) {
+                float v[32];
+                const int col = 32 * part;
+                tmem_ld32(tb + lane_off + cH + col, v);
+                tmem_wait_ld();
 #pragma unroll
-            for (int k = 0; k < 32; k += 4)
-                *reinterpret_cast<float4*>(dstH + row * DH + col + k) =
-                    make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
-            if (tid < DF) dstz[tid] = S.z[tid];
-        }
-    } else {
-        // a wait gave up: let copies and MMAs still in flight land before leaving
-        if (tid == 0) {
-            if (tma_pending) mbar_wait(&S.bar_tma, ph_tma, kTimeout);
-            if (mma_pending) mbar_wait(&S.bar_mma, ph_mma, kTimeout);
+                for (int k = 0; k < 32; k += 4)
+                    *reinterpret_cast<float4*>(dstH + row * DH + col + k) =
+                        make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+                if (tid < DF) dstz[tid] = S.z[tid];
+            }
         }
     }
     tc_fence_before();
