@@ -30,7 +30,7 @@
 // e^-80 (exponents are clamped to +-80 there).
 //
 // TMEM columns: H [0,128)  scores S [128,256) (intra scores A reuse [128,160))
-//               U_q [256,320)  U_k [320,384)  O [384,512).
+//               U_q [256,320)  U_k [320,384) (then P_win, bf16 pairs)  O [384,512).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <math.h>
@@ -59,8 +59,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // shared-memory map (bytes from a 1024-aligned base); later uses of a region in a step follow
 // the arrow
-constexpr uint32_t oQ = 0;         // q tile, K-major [128 rows][128 d] -> P_win [128][128 keys]
-constexpr uint32_t oQt = 32768;    // q~, K-major [128][128]
+constexpr uint32_t oQ = 0;         // q tile, K-major [128 rows][128 d]
+constexpr uint32_t oQt = 32768;    // q~, K-major [128][128] -> y tile for the TMA store
 constexpr uint32_t oK = 65536;     // key ring: 4 slots x 32 keys, K-major over d
 constexpr uint32_t oV = 98304;     // value ring: same bytes, read MN-major (N = d)
 constexpr uint32_t oW = 131072;    // Wf [128 d rows][64 features], MN-major B
@@ -91,9 +91,11 @@ constexpr uint32_t kSmemBytes = oSmall + (uint32_t)sizeof(Small) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // TMEM column bases: H [0,128), window scores S [128,256) (the intra scores A reuse its first
-// 32 columns once S is read), U_q [256,320), U_k [320,384), O [384,512).  O has columns of its
-// own so the next step's projections can run while the epilogue still reads O.
-constexpr uint32_t cH = 0, cS = 128, cA = 128, cUq = 256, cUk = 320, cO = 384;
+// 32 columns once S is read), U_q [256,320), U_k [320,384), O [384,512).  Once the delayed
+// keys' U_k rows are staged, the window probabilities P_win (128 rows x 128 keys, bf16 pairs)
+// take U_k's columns and feed the output MMA from TMEM.  O has columns of its own so the next
+// step's projections can run while the epilogue still reads O.
+constexpr uint32_t cH = 0, cS = 128, cA = 128, cUq = 256, cUk = 320, cPw = 320, cO = 384;
 
 __device__ __forceinline__ float clamp80(float x) { return fminf(fmaxf(x, -80.0f), 80.0f); }
 
@@ -184,16 +186,21 @@ __device__ __forceinline__ bool ctl_wait(uint64_t* bar, uint32_t& ph, Small& S, 
     return true;
 }
 
-// One step's operands: key/value slot of chunk c, the gate tile (and the query tile); the
-// barrier expects `extra` more bytes from copies the caller issues on the same phase.
+// Bytes one step's copies bring: key and value slots, the gate tile (and the query tile).
 template <bool MAIN>
-__device__ __forceinline__ void issue_step_loads(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmQ,
-                                                 const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                                 const CUtensorMap* tmG, int64_t c, int64_t kv,
-                                                 int64_t b, uint32_t extra) {
+constexpr uint32_t step_bytes() {
+    return MAIN ? 16384u + 8192u + 32768u : 16384u + 8192u;
+}
+
+// Key/value slot of chunk c (and its query tile), on a barrier phase that expects `expect`
+// bytes in all (the gate tile follows separately).
+template <bool MAIN>
+__device__ __forceinline__ void issue_kvq_loads(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmQ,
+                                                const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                                int64_t c, int64_t kv, int64_t b, uint32_t expect) {
     const int slot = (int)(c & 3);
     const int t0 = (int)(c * 32);
-    sm100::mbar_arrive_expect_tx(bar, (MAIN ? 16384u + 8192u + 32768u : 16384u + 8192u) + extra);
+    sm100::mbar_arrive_expect_tx(bar, expect);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
         sm100::tma_load_4d(sm + oK + kb * 16384 + slot * 4096, tmK, bar, 64 * kb, (int)kv, t0, (int)b);
@@ -201,7 +208,11 @@ __device__ __forceinline__ void issue_step_loads(uint8_t* sm, uint64_t* bar, con
         if (MAIN)
             sm100::tma_load_4d(sm + oQ + kb * 16384, tmQ, bar, 64 * kb, (int)(kv * 4), t0, (int)b);
     }
-    sm100::tma_load_4d(sm + oG, tmG, bar, 0, (int)kv, t0, (int)b);
+}
+
+__device__ __forceinline__ void issue_gate_load(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmG,
+                                                int64_t c, int64_t kv, int64_t b) {
+    sm100::tma_load_4d(sm + oG, tmG, bar, 0, (int)kv, (int)(c * 32), (int)b);
 }
 
 // K-major (or MN-major) descriptor helpers for the 128-byte-swizzled tiles.
@@ -213,7 +224,9 @@ __device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
 }
 
 // The control warp: lane 0 issues the copies and the three MMA groups of every step and
-// hands each result to the math warps through an mbarrier.
+// hands each result to the math warps through an mbarrier.  The next step's query tile and
+// ring slot are loaded as soon as this step's projections have read theirs, its gate tile
+// once the delayed keys' feature map has consumed the staged U_k rows.
 template <bool MAIN>
 __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_t tb, Small& S,
                                              WsHeader* hdr, const CUtensorMap* tmQ,
@@ -224,13 +237,15 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
                    dKi = kdesc(base + oKi), dE = kdesc(base + oE);
     const uint64_t dW = mndesc(base + oW, 16384), dHs = mndesc(base + oHs, 16384),
                    dV = mndesc(base + oV, 16384), dKu = mndesc(base + oKu, 4096);
-    uint32_t ph_tma = 0, ph_q = 0, ph_p = 0, ph_o = 0;
+    uint32_t ph_tma = 0, ph_u = 0, ph_q = 0, ph_p = 0, ph_o = 0;
     bool tma_out = false, mma_out = false;
+    int64_t gate_due = -1;  // chunk whose gate tile its barrier phase still waits for
     if (c_begin < c_end) {
         // the first step's operands, Wf and the two chunks before the segment (zero-filled
         // before the sequence start), all on one phase
-        issue_step_loads<MAIN>(sm, &S.bar_tma, tmQ, tmK, tmV, tmG, c_begin, kv, b,
-                               16384u + 2u * 16384u);
+        issue_kvq_loads<MAIN>(sm, &S.bar_tma, tmQ, tmK, tmV, c_begin, kv, b,
+                              step_bytes<MAIN>() + 16384u + 2u * 16384u);
+        issue_gate_load(sm, &S.bar_tma, tmG, c_begin, kv, b);
         tma_load_3d(sm + oW, tmW, &S.bar_tma, 0, 0, (int)kv);
         for (int64_t cc = c_begin - 2; cc < c_begin; ++cc) {
             const int slot = (int)(cc & 3);
@@ -246,6 +261,8 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
     }
     for (int64_t c = c_begin; c < c_end; ++c) {
         const int slot_d = (int)((c - 2) & 3);
+        const int slot_x = (int)((c + 1) & 3);  // three steps old: no key of the window
+        const bool more = c + 1 < c_end;
         if (!ctl_wait(&S.bar_tma, ph_tma, S, hdr, 2)) break;
         tma_out = false;
         tc_fence_after();
@@ -262,8 +279,19 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
         }
         mma_commit(&S.bar_u);
         mma_out = true;
+        if (!ctl_wait(&S.bar_u, ph_u, S, hdr, 9)) break;
+        // the query tile and the ring slot of chunk c-3 are free: next step's copies start
+        if (more) {
+            issue_kvq_loads<MAIN>(sm, &S.bar_tma, tmQ, tmK, tmV, c + 1, kv, b, step_bytes<MAIN>());
+            tma_out = true;
+            gate_due = c + 1;
+        }
         if (!ctl_wait(&S.bar_q, ph_q, S, hdr, 6)) break;
         tc_fence_after();
+        if (more) {
+            issue_gate_load(sm, &S.bar_tma, tmG, c + 1, kv, b);
+            gate_due = -1;
+        }
         const uint64_t dVd = dV + ((slot_d * 4096) >> 4);
         if (MAIN) {
             // intra-step scores A = q~ k~^T
@@ -285,9 +313,9 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
             }
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
-                mma_bf16(tb + cO, dQ + aoff, dV + ((j * 2048) >> 4),
-                         idesc_bf16(128, 128, false, true), 1);
+                if ((j >> 1) == slot_x) continue;  // P_win is zero there; the slot is reloading
+                mma_bf16_ts(tb + cO, tb + cPw + 8 * j, dV + ((j * 2048) >> 4),
+                            idesc_bf16(128, 128, false, true), 1);
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j)
@@ -302,12 +330,6 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
         mma_commit(&S.bar_o);
         if (!ctl_wait(&S.bar_o, ph_o, S, hdr, 8)) break;
         mma_out = false;
-        // the query tile (P_win), the ring slot of chunk c-3 and the gate tile (staged U_k)
-        // are free now
-        if (c + 1 < c_end) {
-            issue_step_loads<MAIN>(sm, &S.bar_tma, tmQ, tmK, tmV, tmG, c + 1, kv, b, 0u);
-            tma_out = true;
-        }
     }
     if (S.abort) {
         // let copies and MMAs still in flight land before the CTA exits
@@ -315,7 +337,10 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
             mma_commit(&S.bar_fin);
             mbar_wait(&S.bar_fin, 0, kTimeout);
         }
-        if (tma_out) mbar_wait(&S.bar_tma, ph_tma, kTimeout);
+        if (tma_out) {
+            if (gate_due >= 0) issue_gate_load(sm, &S.bar_tma, tmG, gate_due, kv, b);
+            mbar_wait(&S.bar_tma, ph_tma, kTimeout);
+        }
     }
 }
 
@@ -323,7 +348,8 @@ template <bool MAIN>
 __global__ void __launch_bounds__(NT, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmW,
-                  const __grid_constant__ CUtensorMap tmG, Plan p, FwdArgs a) {
+                  const __grid_constant__ CUtensorMap tmG, const __grid_constant__ CUtensorMap tmY,
+                  Plan p, FwdArgs a) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -367,7 +393,10 @@ __global__ void __launch_bounds__(NT, 1)
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmG);
-        if (MAIN) prefetch_tmap(&tmQ);
+        if (MAIN) {
+            prefetch_tmap(&tmQ);
+            prefetch_tmap(&tmY);
+        }
     }
     if (MAIN) {
         for (int e = tid; e < GQ * MMAX; e += NT) {
@@ -437,6 +466,8 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 S.gpart[gq][gf] = run;
             }
+            // the previous step's y tile has left the q~ buffer before anyone writes q~ again
+            if (MAIN && tid == 0) bulk_wait_read();
             math_sync();
             {
                 const float g0 = S.gpart[0][gf], g1 = S.gpart[1][gf], g2 = S.gpart[2][gf],
@@ -548,10 +579,13 @@ __global__ void __launch_bounds__(NT, 1)
                 }
                 // the exchanges below stay within the 4 warps of a lane quadrant (one row per
                 // lane); the staged U_k rows are read after the barrier at the end of this phase
+                tc_fence_before();
                 quad_sync(quad);
                 m2 = fmaxf(fmaxf(fmaxf(xpm[row], xpm[128 + row]), fmaxf(xpm[256 + row], xpm[384 + row])),
                            S.tmax[hh]);
                 float psum = 0.0f;
+                tc_fence_after();  // the staged U_k reads of this quad precede the P_win writes
+                uint32_t pw[16];
                 if (live) {
                     float sv[32];
                     tmem_ld32(tb + lane_off + cS + 32 * part, sv);
@@ -564,18 +598,18 @@ __global__ void __launch_bounds__(NT, 1)
                             const int k = 8 * ch + e;
                             pv[e] = ex2f(((vm >> k) & 1u) ? fmaf(sv[k], s2, -m2) : -INFINITY);
                         }
-                        const uint32_t w0 = round_pair(pv[0], pv[1]), w1 = round_pair(pv[2], pv[3]),
-                                       w2 = round_pair(pv[4], pv[5]), w3 = round_pair(pv[6], pv[7]);
+                        pw[4 * ch] = round_pair(pv[0], pv[1]);
+                        pw[4 * ch + 1] = round_pair(pv[2], pv[3]);
+                        pw[4 * ch + 2] = round_pair(pv[4], pv[5]);
+                        pw[4 * ch + 3] = round_pair(pv[6], pv[7]);
                         psum += ((pv[0] + pv[1]) + (pv[2] + pv[3])) + ((pv[4] + pv[5]) + (pv[6] + pv[7]));
-                        st_shared_v4(base + oQ + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
-                                     w0, w1, w2, w3);
                     }
                 } else {
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch)
-                        st_shared_v4(base + oQ + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
-                                     0u, 0u, 0u, 0u);
+                    for (int e = 0; e < 16; ++e) pw[e] = 0u;
                 }
+                // keys 32 part + u of this row -> P_win columns 16 part + u / 2
+                tmem_st16(tb + lane_off + cPw + 16 * part, pw);
                 S.ps[part][row] = psum;
                 const float f2 = part < 2 ? kLog2e : -kLog2e;
                 const float cst = -fmaxf(xum[part * 128 + row], xum[sib * 128 + row]) * kLog2e;
@@ -618,6 +652,7 @@ __global__ void __launch_bounds__(NT, 1)
                                  q0, q1, q2, q3);
                 }
                 S.pg[part][row] = pg;
+                tmem_wait_st();
             }
             math_sync();
 
@@ -734,27 +769,31 @@ __global__ void __launch_bounds__(NT, 1)
             if (!ok) break;
             tc_fence_after();
 
-            // (7) epilogue: y = O / den over columns [32 part, 32 part + 32), 16-byte bf16 stores
+            // (7) epilogue: y = O / den over columns [32 part, 32 part + 32) into the y tile
+            //     (q~'s buffer, free once the output MMAs are done), then one TMA store
             if (MAIN) {
                 float ov[32];
                 const int col = 32 * part;
                 tmem_ld32(tb + lane_off + cO + col, ov);
                 tmem_wait_ld();
-                if (qv) {
-                    __nv_bfloat16* yr = (__nv_bfloat16*)a.y +
-                                        ((b * p.L + qa) * p.Hq + kv * GQ + hh) * DH + col;
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        uint4 w;
-                        w.x = pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv);
-                        w.y = pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv);
-                        w.z = pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv);
-                        w.w = pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv);
-                        *reinterpret_cast<uint4*>(yr + 8 * ch) = w;
-                    }
+                for (int ch = 0; ch < 4; ++ch)
+                    st_shared_v4(base + oQt + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                                 pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv),
+                                 pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv),
+                                 pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv),
+                                 pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv));
+                fence_async_smem();
+                math_sync();
+                if (tid == 0) {
+                    // rows past the end of the sequence fall outside the tensor and are dropped
+                    tma_store_4d(&tmY, sm + oQt, 0, (int)(kv * GQ), (int)t0, (int)b);
+                    tma_store_4d(&tmY, sm + oQt + 16384, 64, (int)(kv * GQ), (int)t0, (int)b);
+                    bulk_commit();
                 }
             }
         }
+        if (MAIN && tid == 0) bulk_wait_all();
 
         if (ok) {
             // final state of the segment: the local record (segment pass) or the decode hand-off
@@ -824,7 +863,7 @@ bool fwd_tc_supported(const Plan& p) {
 cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     Plan p = p0;
     plan_segments(&p, 152);
-    alignas(64) CUtensorMap mq, mk, mv, mw;
+    alignas(64) CUtensorMap mq, mk, mv, mw, my;
     const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
                      Hkv = (cuuint64_t)p.Hkv;
     {
@@ -832,6 +871,7 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
         const cuuint64_t str[3] = {DH * 2, Hq * DH * 2, L * Hq * DH * 2};
         const cuuint32_t box[4] = {64, GQ, CT, 1};
         if (!make_map(&mq, a.q, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!make_map(&my, a.y, 4, dims, str, box)) return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t dims[4] = {DH, Hkv, L, B};
@@ -863,12 +903,13 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     const unsigned U = (unsigned)(p.B * p.Hkv);
     if (p.P > 1) {
         fwd_tc_kernel<false><<<dim3(U, (unsigned)(p.P - 1)), NT, kSmemBytes, s>>>(mq, mk, mv, mw,
-                                                                                 mg, p, a);
+                                                                                 mg, my, p, a);
         e = launch_seg_scan(p, a.seg, s);
         if (e != cudaSuccess) return e;
     }
     if (a.ev_before) cudaEventRecord(a.ev_before, s);
-    fwd_tc_kernel<true><<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, p, a);
+    fwd_tc_kernel<true><<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, my, p,
+                                                                        a);
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
     return cudaGetLastError();
 }
