@@ -70,16 +70,27 @@ __global__ void fwd_seg_scan(Plan p, float* seg) {
     if (e >= nE) return;
     const int64_t f = e < p.D * p.d ? e / p.d : e - p.D * p.d;
     const int64_t U = p.B * p.Hkv;
+    // records are read eight at a time before any is overwritten, so the loads of a group
+    // are in flight together instead of one memory round trip per segment
+    constexpr int KG = 8;
     float carry = 0.0f;
-    for (int64_t s = 0; s < p.P; ++s) {
-        float* rec = seg + ((size_t)s * U + unit) * p.rec_floats;
-        float dH = 0.0f, lam = 0.0f;
-        if (s < p.P - 1) {
-            dH = rec[e];
-            lam = rec[p.D * p.d + p.D + f];
+    for (int64_t s0 = 0; s0 < p.P; s0 += KG) {
+        float dH[KG], lam[KG];
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+            const int64_t s = s0 + k;
+            const float* rec = seg + ((size_t)s * U + unit) * p.rec_floats;
+            dH[k] = s < p.P - 1 ? rec[e] : 0.0f;
+            lam[k] = s < p.P - 1 ? rec[p.D * p.d + p.D + f] : 0.0f;
         }
-        rec[e] = carry;
-        carry = expf(lam) * carry + dH;
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+            const int64_t s = s0 + k;
+            if (s < p.P) {
+                seg[((size_t)s * U + unit) * p.rec_floats + e] = carry;
+                carry = expf(lam[k]) * carry + dH[k];
+            }
+        }
     }
 }
 
