@@ -919,8 +919,12 @@ size_t bwd_workspace_bytes(const Plan& p) { return bwd_layout(p).total; }
 
 cudaError_t launch_bwd(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     if (p.G > 8) return cudaErrorInvalidValue;
-    if (p.dtype == LIZARD_F32) return bwd_dims<float, false>(p, a, s);
-    return bwd_dims<__nv_bfloat16, true>(p, a, s);
+    // the walks run one CTA per (unit, segment), one CTA per SM: cut the segments so the
+    // last wave is as full as the others
+    Plan q = p;
+    plan_segments_waves(&q, 152);
+    if (q.dtype == LIZARD_F32) return bwd_dims<float, false>(q, a, s);
+    return bwd_dims<__nv_bfloat16, true>(q, a, s);
 }
 
 }  // namespace lz

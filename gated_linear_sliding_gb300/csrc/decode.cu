@@ -38,7 +38,8 @@ __device__ __forceinline__ void cp_wait_all() {
 template <typename T, int DH, int DF, int WMAX>
 struct DecLay {
     static constexpr int NRG = NT / DH;       // row groups of the state
-    static constexpr int RPT = DF / NRG;      // state rows per thread
+    static constexpr int RPT = DF / NRG;      // consecutive state rows per thread
+    static_assert(RPT % 4 == 0, "rows are read four at a time");
     static constexpr int E = (int)sizeof(T);  // bytes per element
     static constexpr int KROW = DH * E + 16;  // padded key row (bytes)
     // byte offsets of the dynamic shared memory
@@ -95,7 +96,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
     float* Sg = a.S + unit * DF * DH;
     float sreg[RPT];
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) sreg[i] = Sg[(rg + NRG * i) * DH + c];
+    for (int i = 0; i < RPT; ++i) sreg[i] = Sg[(rg * RPT + i) * DH + c];
     {
         const T* Wk = (const T*)a.Wf + kv * DH * H2;
         constexpr int nW = DH * H2 * E / 16;
@@ -145,11 +146,15 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
         float acc[GMAX + 1];
 #pragma unroll
         for (int r = 0; r <= GMAX; ++r) acc[r] = 0.0f;
-        for (int cc = qd * CQ; cc < (qd + 1) * CQ; ++cc) {
-            const float wv = ld(sW + cc * H2 + f);
+        for (int cc = qd * CQ; cc < (qd + 1) * CQ; cc += 4) {
+            const float w0 = ld(sW + cc * H2 + f), w1 = ld(sW + (cc + 1) * H2 + f),
+                        w2 = ld(sW + (cc + 2) * H2 + f), w3 = ld(sW + (cc + 3) * H2 + f);
 #pragma unroll
             for (int r = 0; r <= GMAX; ++r)
-                if (r <= G) acc[r] = fmaf(sX[r * DH + cc], wv, acc[r]);
+                if (r <= G) {
+                    const float4 x = *reinterpret_cast<const float4*>(sX + r * DH + cc);
+                    acc[r] = fmaf(x.x, w0, fmaf(x.y, w1, fmaf(x.z, w2, fmaf(x.w, w3, acc[r]))));
+                }
         }
         // partials [NQ][G+1][H2] in the score and readout-partial buffers (contiguous, both
         // unused until step 4)
@@ -207,21 +212,32 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
     }
     __syncthreads();
 
-    // 4. state update (this thread's rows of column c) and partial readouts phi(q).S
+    // 4. state update (rows [rg RPT, rg RPT + RPT) of column c) and partial readouts phi(q).S
     const float ve = admit ? ld(sVE + c) : 0.0f;
+    const int f0 = rg * RPT;
 #pragma unroll
-    for (int i = 0; i < RPT; ++i) {
-        const int f = rg + NRG * i;
-        sreg[i] = fmaf(sGam[f], sreg[i], sPhi[G * DF + f] * ve);
+    for (int i = 0; i < RPT; i += 4) {
+        const float4 gm = *reinterpret_cast<const float4*>(sGam + f0 + i);
+        const float4 pk = *reinterpret_cast<const float4*>(sPhi + G * DF + f0 + i);
+        sreg[i] = fmaf(gm.x, sreg[i], pk.x * ve);
+        sreg[i + 1] = fmaf(gm.y, sreg[i + 1], pk.y * ve);
+        sreg[i + 2] = fmaf(gm.z, sreg[i + 2], pk.z * ve);
+        sreg[i + 3] = fmaf(gm.w, sreg[i + 3], pk.w * ve);
     }
+#pragma unroll
+    for (int i = 0; i < RPT; ++i) Sg[(f0 + i) * DH + c] = sreg[i];
     for (int hh = 0; hh < G; ++hh) {
         float part = 0.0f;
 #pragma unroll
-        for (int i = 0; i < RPT; ++i) part = fmaf(sPhi[hh * DF + rg + NRG * i], sreg[i], part);
+        for (int i = 0; i < RPT; i += 4) {
+            const float4 ph = *reinterpret_cast<const float4*>(sPhi + hh * DF + f0 + i);
+            part = fmaf(ph.x, sreg[i], part);
+            part = fmaf(ph.y, sreg[i + 1], part);
+            part = fmaf(ph.z, sreg[i + 2], part);
+            part = fmaf(ph.w, sreg[i + 3], part);
+        }
         sRed[(rg * G + hh) * DH + c] = part;
     }
-#pragma unroll
-    for (int i = 0; i < RPT; ++i) Sg[(rg + NRG * i) * DH + c] = sreg[i];
     // new z (written back by the CTA, which owns the unit)
     for (int f = tid; f < DF; f += NT) {
         const float zn = fmaf(sGam[f], sZ[f], sPhi[G * DF + f]);
@@ -242,7 +258,13 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
             const uint4 wv = *reinterpret_cast<const uint4*>(kr + 16 * ch);
             const T* kv8 = reinterpret_cast<const T*>(&wv);
 #pragma unroll
-            for (int e2 = 0; e2 < EPC; ++e2) acc = fmaf(x[ch * EPC + e2], ld(kv8 + e2), acc);
+            for (int e2 = 0; e2 < EPC; e2 += 4) {
+                const float4 x4 = *reinterpret_cast<const float4*>(x + ch * EPC + e2);
+                acc = fmaf(x4.x, ld(kv8 + e2), acc);
+                acc = fmaf(x4.y, ld(kv8 + e2 + 1), acc);
+                acc = fmaf(x4.z, ld(kv8 + e2 + 2), acc);
+                acc = fmaf(x4.w, ld(kv8 + e2 + 3), acc);
+            }
         }
         sS[hh * WMAX + jj] = acc * p.scale;
     }
@@ -280,19 +302,38 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
     }
     __syncthreads();
 
-    // 7. outputs
+    // 7. outputs: two adjacent columns of one head per item
     const T* sV = (const T*)(sm + Ly::oV);
-    for (int e = tid; e < G * DH; e += NT) {
-        const int hh = e / DH, cc = e % DH;
-        float num = 0.0f;
+    for (int e = tid; e < G * (DH / 2); e += NT) {
+        const int hh = e / (DH / 2), cc = 2 * (e % (DH / 2));
+        float num0 = 0.0f, num1 = 0.0f;
 #pragma unroll
-        for (int r2 = 0; r2 < NRG; ++r2) num += sRed[(r2 * G + hh) * DH + cc];
-        float wv = 0.0f;
-        for (int jj = 0; jj < nkeys; ++jj) wv = fmaf(sS[hh * WMAX + jj], ld(sV + jj * DH + cc), wv);
+        for (int r2 = 0; r2 < NRG; ++r2) {
+            num0 += sRed[(r2 * G + hh) * DH + cc];
+            num1 += sRed[(r2 * G + hh) * DH + cc + 1];
+        }
+        float wv0 = 0.0f, wv1 = 0.0f;
+        const float* ps = sS + hh * WMAX;
+        int jj = 0;
+        for (; jj + 4 <= nkeys; jj += 4) {
+            const float4 p4 = *reinterpret_cast<const float4*>(ps + jj);
+            const float pj[4] = {p4.x, p4.y, p4.z, p4.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                wv0 = fmaf(pj[k], ld(sV + (jj + k) * DH + cc), wv0);
+                wv1 = fmaf(pj[k], ld(sV + (jj + k) * DH + cc + 1), wv1);
+            }
+        }
+        for (; jj < nkeys; ++jj) {
+            wv0 = fmaf(ps[jj], ld(sV + jj * DH + cc), wv0);
+            wv1 = fmaf(ps[jj], ld(sV + jj * DH + cc + 1), wv1);
+        }
         const float m = sRow[hh * 4 + 0];
         const float Em = expf(-m);
-        const float den = Em * sRow[hh * 4 + 2] + sRow[hh * 4 + 1] + sRow[hh * 4 + 3];
-        st((T*)a.y + (b * p.Hq + kv * G + hh) * DH + cc, (Em * num + wv) / den);
+        const float inv = 1.0f / (Em * sRow[hh * 4 + 2] + sRow[hh * 4 + 1] + sRow[hh * 4 + 3]);
+        T* yo = (T*)a.y + (b * p.Hq + kv * G + hh) * DH + cc;
+        st(yo, (Em * num0 + wv0) * inv);
+        st(yo + 1, (Em * num1 + wv1) * inv);
     }
 
     // 8. the new token joins the ring (slot pos mod (w+1), never read in this step)

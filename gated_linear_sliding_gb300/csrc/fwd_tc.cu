@@ -829,6 +829,340 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Segment pass: the state a segment leaves behind when it starts from zero,
+//   H_seg = sum_t e^{b_end - b_t} (.) phi(k_{t-w}) v_{t-w}^T,   z_seg likewise,
+// (b = cumulative log-sigmoid gate from the segment start) and its total log-decay, for
+// every segment but the last.  Steps of 128 tokens: the delayed keys of a step fill one
+// 128-row MMA tile, so U_k = k Wf and the update H += k~^T v are one MMA group each, and the
+// state is decayed once per 128 tokens.
+constexpr int LT = 128;  // tokens per segment-pass step
+constexpr uint32_t lK = 0;         // delayed keys [2 halves][128 rows][64 d], K-major
+constexpr uint32_t lV = 32768;     // delayed values, same layout, read MN-major
+constexpr uint32_t lG = 65536;     // gate logits [128 tokens][128 features] bf16
+constexpr uint32_t lW = 98304;     // Wf, MN-major B
+constexpr uint32_t lKu = 114688;   // k~ = phi(k) e^{b_end - b_t}, [2 halves][128 tokens][64 f]
+constexpr uint32_t lE = 147456;    // e^{b_end - b_t} bf16 [128 tokens][EKR] (padded rows)
+constexpr int EKR = DF + 8;        // row pitch of lE: rows land in distinct bank groups
+constexpr uint32_t lX = lE + 128 * EKR * 2;  // exchanges: u-extreme, u-sum, gate and z quarters
+constexpr uint32_t lSmall = lX + 8192;
+
+struct LSmall {
+    uint64_t bar_k, bar_v, bar_g, bar_u, bar_h, bar_fin;
+    uint32_t tmem;
+    volatile int abort;
+    float z[DF], el[DF];
+};
+constexpr uint32_t kLocalSmem = lSmall + (uint32_t)sizeof(LSmall) + 1024;
+static_assert(kLocalSmem <= 232448, "shared memory budget");
+constexpr int NL = 512;  // threads of the segment pass
+
+// Bounded wait by every thread of the segment pass; all return the same verdict.
+__device__ __forceinline__ bool local_wait(uint64_t* bar, uint32_t& ph, LSmall& S, WsHeader* hdr,
+                                           unsigned where) {
+    bool fail = false;
+    if (!mbar_try_wait(bar, ph)) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, ph)) {
+            if (S.abort || clock64() - t0 > kTimeout) {
+                fail = true;
+                break;
+            }
+        }
+    }
+    if (fail && !S.abort) {
+        S.abort = 1;
+        report(hdr, LIZARD_ERR_TIMEOUT, where);
+    }
+    if (!fail) ph ^= 1u;
+    return !__syncthreads_or(fail);
+}
+
+__device__ __forceinline__ void local_load(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar,
+                                           int64_t kv, int64_t t, int64_t b) {
+    mbar_arrive_expect_tx(bar, 32768u);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+        tma_load_4d(dst + kb * 16384, tm, bar, 64 * kb, (int)kv, (int)t, (int)b);
+}
+
+__global__ void __launch_bounds__(NL, 1)
+    fwd_tc_local(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
+                 Plan p, FwdArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    LSmall& S = *reinterpret_cast<LSmall*>(sm + lSmall);
+    float* xum = reinterpret_cast<float*>(sm + lX);  // [4][128] u extreme per (part, key)
+    float* xus = xum + 512;                          // [4][128] u sums
+    float* gpart = xum + 1024;                       // [4][128] gate quarter sums
+    float* zq = xum + 1536;                          // [4][128] z quarter sums
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, part = warp >> 2;
+    const int row = 32 * quad + lane;
+    const int64_t unit = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t U = p.B * p.Hkv;
+    const int64_t s0 = seg * p.seg_len;
+    const int64_t s1 = min64(p.L, s0 + p.seg_len);
+    const int64_t nsteps = (s1 - s0 + LT - 1) / LT;
+    WsHeader* hdr = (WsHeader*)a.header;
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+
+    if (warp == 0) {
+        tmem_alloc(&S.tmem, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&S.bar_k, 1);
+        mbar_init(&S.bar_v, 1);
+        mbar_init(&S.bar_g, 1);
+        mbar_init(&S.bar_u, 1);
+        mbar_init(&S.bar_h, 1);
+        mbar_init(&S.bar_fin, 1);
+        fence_mbar_init();
+        S.abort = 0;
+    }
+    if (tid < DF) S.z[tid] = 0.0f;
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = S.tmem;
+    const uint32_t cHl = 0, cUl = 128;  // TMEM: H [0,128), U_k [128,192)
+    const uint64_t dK = kdesc(base + lK);
+    const uint64_t dW = mndesc(base + lW, 16384), dV = mndesc(base + lV, 16384),
+                   dKu = mndesc(base + lKu, 16384);
+    {
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+        tmem_st32(tb + lane_off + cHl + 32 * part, v);
+        tmem_wait_st();
+    }
+    bool k_out = false, v_out = false, g_out = false, mma_out = false;
+    if (tid == 0 && nsteps > 0) {
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmG);
+        mbar_arrive_expect_tx(&S.bar_k, 32768u + 16384u);
+        tma_load_3d(sm + lW, &tmW, &S.bar_k, 0, 0, (int)kv);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+            tma_load_4d(sm + lK + kb * 16384, &tmK, &S.bar_k, 64 * kb, (int)kv, (int)(s0 - WIN), (int)b);
+        mbar_arrive_expect_tx(&S.bar_g, 32768u);
+        tma_load_4d(sm + lG, &tmG, &S.bar_g, 0, (int)kv, (int)s0, (int)b);
+        local_load(sm + lV, &tmV, &S.bar_v, kv, s0 - WIN, b);
+        k_out = v_out = g_out = true;
+    }
+    tc_fence_before();
+    __syncthreads();
+    uint32_t ph_k = 0, ph_v = 0, ph_g = 0, ph_u = 0, ph_h = 0;
+    float lam_tot = 0.0f;
+    bool ok = true;
+
+    for (int64_t c = 0; c < nsteps; ++c) {
+        const int64_t t0 = s0 + c * LT;
+        const int n = (int)min64(LT, s1 - t0);
+        const bool more = c + 1 < nsteps;
+        // (1) U_k = k Wf for the 128 delayed keys of the step
+        ok = local_wait(&S.bar_k, ph_k, S, hdr, 20);
+        if (!ok) break;
+        if (tid == 0) {
+            k_out = false;
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + cUl, dK + koff, dW + ((j * 2048) >> 4), idesc_bf16(128, 64, false, true),
+                         j > 0);
+            }
+            mma_commit(&S.bar_u);
+            mma_out = true;
+        }
+        // (2) gates: four threads per feature, 32 tokens each; decay of each token's key to the
+        //     step end, e^{b_last - b_t} (at most 1), and of the old state, e^{b_last}
+        ok = local_wait(&S.bar_g, ph_g, S, hdr, 21);
+        if (!ok) break;
+        if (tid == 0) g_out = false;
+        {
+            const int gf = tid & (DF - 1), gq = tid >> 7;
+            const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + lG);
+            float bt[32];
+            float run = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int tt = 32 * gq + j;
+                run += tt < n ? log_sigmoid_fast(__bfloat162float(sg[tt * DF + gf])) : 0.0f;
+                bt[j] = run;
+            }
+            gpart[gq * DF + gf] = run;
+            __syncthreads();
+            const float g0 = gpart[gf], g1 = gpart[DF + gf], g2 = gpart[2 * DF + gf],
+                        g3 = gpart[3 * DF + gf];
+            const float blast = (g0 + g1) + (g2 + g3);
+            const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? g0 + g1 : (g0 + g1) + g2;
+            const float cst = (blast - off) * kLog2e;
+            __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + lE);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                Ek[(32 * gq + j) * EKR + gf] = __float2bfloat16_rn(ex2f(fmaf(-bt[j], kLog2e, cst)));
+            if (gq == 0) {
+                S.el[gf] = ex2f(blast * kLog2e);
+                lam_tot += blast;
+            }
+        }
+        __syncthreads();
+        // the gate tile is consumed: the next step's gates start loading
+        if (tid == 0 && more) {
+            mbar_arrive_expect_tx(&S.bar_g, 32768u);
+            tma_load_4d(sm + lG, &tmG, &S.bar_g, 0, (int)kv, (int)(t0 + LT), (int)b);
+            g_out = true;
+        }
+        // (3) decay the state by e^{b_last} (lane = feature, 32 columns per part)
+        {
+            float v[32];
+            tmem_ld32(tb + lane_off + cHl + 32 * part, v);
+            tmem_wait_ld();
+            const float el = S.el[row];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= el;
+            tmem_st32(tb + lane_off + cHl + 32 * part, v);
+            tmem_wait_st();
+        }
+        // (4) phi of the delayed keys (lane = key): parts 0, 1 softmax(+u) over features
+        //     [0, 64), parts 2, 3 softmax(-u) over [64, 128); k~ = phi e^{b_last - b_t}
+        ok = local_wait(&S.bar_u, ph_u, S, hdr, 22);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0) {
+            mma_out = false;
+            // the key tile is consumed: the next step's keys start loading
+            if (more) {
+                local_load(sm + lK, &tmK, &S.bar_k, kv, t0 + LT - WIN, b);
+                k_out = true;
+            }
+        }
+        {
+            const int t = row, sib = part ^ 1;
+            float uv[32];
+            tmem_ld32(tb + lane_off + cUl + 32 * (part & 1), uv);
+            tmem_wait_ld();
+            float uext = -INFINITY;
+            if (part < 2) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) uext = fmaxf(uext, uv[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) uext = fmaxf(uext, -uv[k]);
+            }
+            xum[part * 128 + t] = uext;
+            quad_sync(quad);
+            const float f2 = part < 2 ? kLog2e : -kLog2e;
+            const float cst = -fmaxf(xum[part * 128 + t], xum[sib * 128 + t]) * kLog2e;
+            float usum = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                uv[k] = ex2f(fmaf(uv[k], f2, cst));
+                usum += uv[k];
+            }
+            xus[part * 128 + t] = usum;
+            quad_sync(quad);
+            const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
+            const float inv = dvalid ? 1.0f / (xus[part * 128 + t] + xus[sib * 128 + t]) : 0.0f;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const int f0 = 32 * part + 8 * ch;
+                uint32_t w0, w1, w2, w3;
+                ld_shared_v4(base + lE + (uint32_t)(t * EKR + f0) * 2u, w0, w1, w2, w3);
+                float ek[8], kv8[8];
+                unpack8(w0, w1, w2, w3, ek);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) kv8[e] = uv[8 * ch + e] * inv * ek[e];
+                st_shared_v4(base + lKu + (part >> 1) * 16384 + sw128(t, 4 * (part & 1) + ch),
+                             pack_bf16(kv8[0], kv8[1]), pack_bf16(kv8[2], kv8[3]),
+                             pack_bf16(kv8[4], kv8[5]), pack_bf16(kv8[6], kv8[7]));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // (5) H += k~^T v on the tensor cores while the threads sum z
+        if (tid == 0) {
+            if (!mbar_wait(&S.bar_v, ph_v, kTimeout)) {
+                S.abort = 1;
+                report(hdr, LIZARD_ERR_TIMEOUT, 23);
+            } else {
+                ph_v ^= 1u;
+                v_out = false;
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    mma_bf16(tb + cHl, dKu + ((j * 2048) >> 4), dV + ((j * 2048) >> 4),
+                             idesc_bf16(128, 128, true, true), 1);
+                mma_commit(&S.bar_h);
+                mma_out = true;
+            }
+        }
+        {
+            // z <- e^{b_last} z + sum_t k~_t, from the bf16 tile the MMA reads
+            const int f = tid & (DF - 1), gq = tid >> 7;
+            const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + lKu);
+            float zs = 0.0f;
+            for (int t = 32 * gq; t < 32 * gq + 32; ++t) {
+                const uint32_t off = (f >> 6) * 16384 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
+                zs += __bfloat162float(ku[off / 2]);
+            }
+            zq[gq * DF + f] = zs;
+        }
+        __syncthreads();
+        if (tid < DF)
+            S.z[tid] = fmaf(S.el[tid], S.z[tid], (zq[tid] + zq[DF + tid]) + (zq[2 * DF + tid] + zq[3 * DF + tid]));
+        ok = local_wait(&S.bar_h, ph_h, S, hdr, 24);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0) {
+            mma_out = false;
+            // values and k~ are consumed: the next step's values start loading
+            if (more) {
+                local_load(sm + lV, &tmV, &S.bar_v, kv, t0 + LT - WIN, b);
+                v_out = true;
+            }
+        }
+    }
+
+    if (ok) {
+        float* r = a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats;
+        float v[32];
+        tmem_ld32(tb + lane_off + cHl + 32 * part, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(r + row * DH + 32 * part + k) =
+                make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+        if (tid < DF) {
+            r[DF * DH + tid] = S.z[tid];
+            r[DF * DH + DF + tid] = lam_tot;
+        }
+    } else if (tid == 0) {
+        // let copies and MMAs still in flight land before the CTA exits
+        if (mma_out) {
+            mma_commit(&S.bar_fin);
+            mbar_wait(&S.bar_fin, 0, kTimeout);
+        }
+        if (k_out) mbar_wait(&S.bar_k, ph_k, kTimeout);
+        if (g_out) mbar_wait(&S.bar_g, ph_g, kTimeout);
+        if (v_out) mbar_wait(&S.bar_v, ph_v, kTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 256);
+    }
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (fn == nullptr) {
@@ -897,13 +1231,27 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     e = cudaFuncSetAttribute(fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(fwd_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
-    if (e != cudaSuccess) return e;
     const unsigned U = (unsigned)(p.B * p.Hkv);
     if (p.P > 1) {
-        fwd_tc_kernel<false><<<dim3(U, (unsigned)(p.P - 1)), NT, kSmemBytes, s>>>(mq, mk, mv, mw,
-                                                                                 mg, my, p, a);
+        // segment pass: 128-token tiles of the delayed keys, values and gates
+        alignas(64) CUtensorMap lk, lv, lg;
+        {
+            const cuuint64_t dims[4] = {DH, Hkv, L, B};
+            const cuuint64_t str[3] = {DH * 2, Hkv * DH * 2, L * Hkv * DH * 2};
+            const cuuint32_t box[4] = {64, 1, LT, 1};
+            if (!make_map(&lk, a.k, 4, dims, str, box)) return cudaErrorInvalidValue;
+            if (!make_map(&lv, a.v, 4, dims, str, box)) return cudaErrorInvalidValue;
+        }
+        {
+            const cuuint64_t dims[4] = {DF, Hkv, L, B};
+            const cuuint64_t str[3] = {DF * 2, Hkv * DF * 2, L * Hkv * DF * 2};
+            const cuuint32_t box[4] = {DF, 1, LT, 1};
+            if (!make_map(&lg, a.g, 4, dims, str, box, false)) return cudaErrorInvalidValue;
+        }
+        e = cudaFuncSetAttribute(fwd_tc_local, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)kLocalSmem);
+        if (e != cudaSuccess) return e;
+        fwd_tc_local<<<dim3(U, (unsigned)(p.P - 1)), NL, kLocalSmem, s>>>(lk, lv, mw, lg, p, a);
         e = launch_seg_scan(p, a.seg, s);
         if (e != cudaSuccess) return e;
     }

@@ -29,6 +29,9 @@ bool make_plan(const lizard_dims* dims, Plan* p);
 // Re-cut the segments for a kernel that wants about `target` (unit, segment) CTAs;
 // never more than Pmax segments, so the workspace size stays valid.
 void plan_segments(Plan* p, int64_t target);
+// Re-cut the segments of a kernel that runs one CTA per (unit, segment) on `slots` resident
+// CTAs: the segment count (at most Pmax) that minimises waves x segment length.
+void plan_segments_waves(Plan* p, int64_t slots);
 size_t fwd_workspace_bytes(const Plan& p);
 
 struct FwdArgs {

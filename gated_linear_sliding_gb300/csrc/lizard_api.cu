@@ -32,13 +32,30 @@ bool make_plan(const lizard_dims* dims, Plan* p) {
     p->dtype = d.dtype;
     const int64_t U = d.B * d.Hkv;
     p->nchunks = (d.L + kChunk - 1) / kChunk;
-    int64_t pmax = (kTargetUnits + U - 1) / U;
+    int64_t pmax = (2 * kTargetUnits + U - 1) / U;
     if (pmax < 1) pmax = 1;
     if (pmax > 64) pmax = 64;
     p->Pmax = pmax;
     p->rec_floats = (size_t)(d.D * d.d + 2 * d.D);
     plan_segments(p, kTargetUnits);
     return true;
+}
+
+void plan_segments_waves(Plan* p, int64_t slots) {
+    const int64_t U = p->B * p->Hkv;
+    int64_t best_cost = -1, best = 1;
+    for (int64_t want = 1; want <= p->Pmax; ++want) {
+        const int64_t sc = (p->nchunks + want - 1) / want;
+        const int64_t P = (p->nchunks + sc - 1) / sc;
+        const int64_t cost = ((U * P + slots - 1) / slots) * sc;
+        if (best_cost < 0 || cost < best_cost) {
+            best_cost = cost;
+            best = want;
+        }
+    }
+    p->seg_chunks = (p->nchunks + best - 1) / best;
+    p->seg_len = p->seg_chunks * kChunk;
+    p->P = (p->nchunks + p->seg_chunks - 1) / p->seg_chunks;
 }
 
 void plan_segments(Plan* p, int64_t target) {
