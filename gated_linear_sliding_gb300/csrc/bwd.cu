@@ -400,7 +400,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_forward_walk(Plan p, BwdArgs a, Bwd
             const float dl = srow[TS + r], lse = srow[2 * TS + r];
             const int64_t i = i0 + r;
             const int64_t jlo = max64(0, i0 - p.w + 1), jhi = i0 + n - 1;
-            for (int64_t j0 = jlo; j0 <= jhi; j0 += KB) {
+            // (the tensor-core window kernel adds the window part afterwards when it runs)
+            for (int64_t j0 = jlo; !a.win_tc && j0 <= jhi; j0 += KB) {
                 __syncthreads();
                 for (int e = tid; e < KB * DH; e += NT) {
                     const int t = e / DH, c = e % DH;
@@ -886,6 +887,11 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     if (a.ev_before) cudaEventRecord(a.ev_before, s);
     bwd_forward_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
+    // window part of dq on the tensor cores (the walk above wrote the state part)
+    if (a.win_tc) {
+        e = launch_bwd_win_tc(p, a, wsf + ws.rows, false, s);
+        if (e != cudaSuccess) return e;
+    }
     // 3. reverse segment pass and scan
     if (p.P > 1) {
         bwd_reverse_local<T, DH, DF, FAST><<<dim3(U, (unsigned)(p.P - 1)), NT, smem, s>>>(p, a, ws);
@@ -895,7 +901,12 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     // 4. reverse-direction walk
     bwd_reverse_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
     // 5. window parts of dk, dv
-    bwd_window_keys<T, DH, FAST><<<dim3((unsigned)((p.L + 31) / 32), U), NT, wsmem, s>>>(p, a, ws);
+    if (a.win_tc) {
+        e = launch_bwd_win_tc(p, a, wsf + ws.rows, true, s);
+        if (e != cudaSuccess) return e;
+    } else {
+        bwd_window_keys<T, DH, FAST><<<dim3((unsigned)((p.L + 31) / 32), U), NT, wsmem, s>>>(p, a, ws);
+    }
     // 6. dg, then the reductions
     const int64_t ng = p.B * p.L * p.Hkv * p.D;
     bwd_gates<T><<<(unsigned)((ng + 255) / 256), 256, 0, s>>>(p, a, ws);
@@ -923,8 +934,10 @@ cudaError_t launch_bwd(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     // last wave is as full as the others
     Plan q = p;
     plan_segments_waves(&q, 152);
-    if (q.dtype == LIZARD_F32) return bwd_dims<float, false>(q, a, s);
-    return bwd_dims<__nv_bfloat16, true>(q, a, s);
+    BwdArgs b = a;
+    b.win_tc = bwd_win_tc_supported(q) ? 1 : 0;
+    if (q.dtype == LIZARD_F32) return bwd_dims<float, false>(q, b, s);
+    return bwd_dims<__nv_bfloat16, true>(q, b, s);
 }
 
 }  // namespace lz

@@ -38,11 +38,13 @@
 #include "common.cuh"
 #include "internal.h"
 #include "sm100.cuh"
+#include "tc_util.cuh"
 
 namespace lz {
 namespace {
 
 using namespace sm100;
+using namespace tc;
 
 constexpr int NW = 16;        // math warps: warp w owns TMEM lanes 32(w%4).., w/4 picks a 32-column part
 constexpr int NS = 32 * NW;   // math threads
@@ -53,9 +55,6 @@ constexpr int DH = 128;       // head dim
 constexpr int DF = 128;       // phi dim
 constexpr int WIN = 64;       // window
 constexpr int MMAX = 64;      // sinks per head
-constexpr long long kTimeout = 2000000000LL;  // SM cycles (about one second)
-constexpr float kLog2e = 1.4426950408889634f;
-constexpr float kLn2 = 0.6931471805599453f;
 
 // shared-memory map (bytes from a 1024-aligned base); later uses of a region in a step follow
 // the arrow
@@ -99,34 +98,9 @@ constexpr uint32_t cH = 0, cS = 128, cA = 128, cUq = 256, cUk = 320, cPw = 320, 
 
 __device__ __forceinline__ float clamp80(float x) { return fminf(fmaxf(x, -80.0f), 80.0f); }
 
-// 2^x on the special-function unit (inputs here are finite or -inf, which gives +0)
-__device__ __forceinline__ float ex2f(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
 // log sigmoid(x) = min(x, 0) - log(1 + e^{-|x|}); the argument of the log is in (1, 2].
 __device__ __forceinline__ float log_sigmoid_fast(float x) {
     return fminf(x, 0.0f) - __logf(1.0f + __expf(-fabsf(x)));
-}
-
-// Round a pair to bf16 (nearest even) in place and return it packed (lo in the low half).
-__device__ __forceinline__ uint32_t round_pair(float& lo, float& hi) {
-    const uint32_t w = pack_bf16(lo, hi);
-    lo = __uint_as_float(w << 16);
-    hi = __uint_as_float(w & 0xFFFF0000u);
-    return w;
-}
-
-__device__ __forceinline__ void unpack8(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
-                                        float* o) {
-    const uint32_t w[4] = {w0, w1, w2, w3};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        o[2 * k] = __uint_as_float(w[k] << 16);
-        o[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
-    }
 }
 
 // Barrier among the 128 math threads (4 warps) that share one TMEM lane quadrant.
@@ -213,14 +187,6 @@ __device__ __forceinline__ void issue_kvq_loads(uint8_t* sm, uint64_t* bar, cons
 __device__ __forceinline__ void issue_gate_load(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmG,
                                                 int64_t c, int64_t kv, int64_t b) {
     sm100::tma_load_4d(sm + oG, tmG, bar, 0, (int)kv, (int)(c * 32), (int)b);
-}
-
-// K-major (or MN-major) descriptor helpers for the 128-byte-swizzled tiles.
-__device__ __forceinline__ uint64_t kdesc(uint32_t addr) {
-    return make_sdesc(addr, 16, 1024, kSwizzle128);
-}
-__device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
-    return make_sdesc(addr, lbo, 1024, kSwizzle128);
 }
 
 // The control warp: lane 0 issues the copies and the three MMA groups of every step and
@@ -1161,30 +1127,6 @@ __global__ void __launch_bounds__(NL, 1)
         tc_fence_after();
         tmem_dealloc(tb, 256);
     }
-}
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (PFN_cuTensorMapEncodeTiled_v12000)ptr;
-    }
-    return fn;
-}
-
-bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t* dims,
-              const cuuint64_t* strides, const cuuint32_t* box, bool swizzle = true) {
-    auto fn = encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint32_t es[5] = {1, 1, 1, 1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(ptr), dims,
-              strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-              swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace

@@ -78,8 +78,14 @@ struct BwdArgs {
     void* ws;
     size_t ws_bytes;
     cudaEvent_t ev_before, ev_after;
+    int win_tc;  // window parts of dq, dk, dv on the tensor cores (set by launch_bwd)
 };
 size_t bwd_workspace_bytes(const Plan& p);
+bool bwd_win_tc_supported(const Plan& p);
+// Window parts of the gradients on the tensor cores: dk, dv (keys) or dq; `rows` is the
+// per-row table [e^{-lse}; dy . y].
+cudaError_t launch_bwd_win_tc(const Plan& p, const BwdArgs& a, const float* rows, bool keys,
+                              cudaStream_t s);
 cudaError_t launch_bwd(const Plan& p, const BwdArgs& a, cudaStream_t s);
 
 }  // namespace lz
