@@ -880,7 +880,7 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
         fa.sinks = a.sinks;
         fa.seg = wsf + ws.fwd_rec;
         fa.header = a.ws;
-        e = launch_fwd_states(p, fa, s);
+        e = fwd_tc_supported(p) ? launch_fwd_states_tc(p, fa, s) : launch_fwd_states(p, fa, s);
         if (e != cudaSuccess) return e;
     }
     // 2. forward-direction walk
@@ -894,7 +894,12 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     }
     // 3. reverse segment pass and scan
     if (p.P > 1) {
-        bwd_reverse_local<T, DH, DF, FAST><<<dim3(U, (unsigned)(p.P - 1)), NT, smem, s>>>(p, a, ws);
+        if (a.win_tc && bwd_rev_local_tc_supported(p)) {
+            e = launch_bwd_rev_local_tc(p, a, wsf + ws.rows, wsf + ws.rev_rec, s);
+            if (e != cudaSuccess) return e;
+        } else {
+            bwd_reverse_local<T, DH, DF, FAST><<<dim3(U, (unsigned)(p.P - 1)), NT, smem, s>>>(p, a, ws);
+        }
         const unsigned nE = (unsigned)(p.D * p.d + p.D);
         bwd_reverse_scan<<<dim3((nE + 255) / 256, U), 256, 0, s>>>(p, wsf + ws.rev_rec);
     }

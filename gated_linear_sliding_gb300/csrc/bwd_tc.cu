@@ -487,11 +487,380 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Reverse segment pass: what a segment adds to the state adjoint at its start,
+//   [dH | dz] = sum_i e^{b_i} (.) phi(q_i) a_i [dy_i, -delta_i]
+// (b_i = cumulative log-sigmoid gate from the segment start to token i), and its total
+// log-decay, walking the segment backwards in 32-token steps of 128 query rows.  The
+// weighted feature rows q^ = phi(q) e^{b} a form the A operand (features are the MMA rows)
+// of dH += q^^T dY.
+constexpr uint32_t rQ = 0, rD = 32768, rQh = 65536, rW = 98304, rG = 114688,
+                   rE = rG + 8192;                 // e^{b_t} bf16 [32][EPR]
+constexpr int EPR = 136;                           // padded row pitch of the decay table
+constexpr uint32_t rX = rE + 32 * EPR * 2;         // exchanges [4][128] x 4, -delta [128]
+constexpr uint32_t rBars = rX + 9216;
+struct RSmall {
+    uint64_t bar_q, bar_d, bar_g, bar_u, bar_h, bar_fin;
+    uint32_t tmem;
+    volatile int abort;
+    float dz[128], el[128];
+};
+constexpr uint32_t kSmemRev = rBars + (uint32_t)sizeof(RSmall) + 1024;
+static_assert(kSmemRev <= 232448, "shared memory budget");
+
+__device__ __forceinline__ bool rev_wait(uint64_t* bar, uint32_t& ph, RSmall& S, WsHeader* hdr,
+                                         unsigned where) {
+    bool fail = false;
+    if (!mbar_try_wait(bar, ph)) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, ph)) {
+            if (S.abort || clock64() - t0 > kTimeout) {
+                fail = true;
+                break;
+            }
+        }
+    }
+    if (fail && !S.abort) {
+        S.abort = 1;
+        report(hdr, LIZARD_ERR_TIMEOUT, where);
+    }
+    if (!fail) ph ^= 1u;
+    return !__syncthreads_or(fail);
+}
+
+__device__ __forceinline__ void load_tile(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar,
+                                          int64_t kv, int64_t c, int64_t b) {
+    mbar_arrive_expect_tx(bar, kTile);
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+        tma_load_4d(dst + kb * 16384, tm, bar, 64 * kb, (int)(kv * GQ), (int)(c * CT), (int)b);
+}
+
+__device__ __forceinline__ float log_sigmoid_f(float x) {
+    return fminf(x, 0.0f) - __logf(1.0f + __expf(-fabsf(x)));
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    bwd_rev_local_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmD,
+                     const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
+                     Plan p, BwdArgs a, const float* rows, float* rev_rec) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    RSmall& S = *reinterpret_cast<RSmall*>(sm + rBars);
+    float* xum = reinterpret_cast<float*>(sm + rX);  // [4][128]
+    float* xus = xum + 512;                          // [4][128]
+    float* gpart = xum + 1024;                       // [4][128]
+    float* zq = xum + 1536;                          // [4][128]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, part = warp >> 2;
+    const int row = 32 * quad + lane;
+    const int64_t unit = blockIdx.x, seg = blockIdx.y + 1;
+    const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t U = p.B * p.Hkv;
+    const int64_t s0 = seg * p.seg_len, s1 = min64(p.L, s0 + p.seg_len);
+    const int64_t c_first = s0 / CT, c_last = (s1 - 1) / CT;
+    const int64_t nrow = p.B * p.L * p.Hq;
+    WsHeader* hdr = (WsHeader*)a.ws;
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    constexpr uint32_t cH = 0, cU = 128;
+
+    if (warp == 0) {
+        tmem_alloc(&S.tmem, 256);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&S.bar_q, 1);
+        mbar_init(&S.bar_d, 1);
+        mbar_init(&S.bar_g, 1);
+        mbar_init(&S.bar_u, 1);
+        mbar_init(&S.bar_h, 1);
+        mbar_init(&S.bar_fin, 1);
+        fence_mbar_init();
+        S.abort = 0;
+    }
+    if (tid < 128) S.dz[tid] = 0.0f;
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = S.tmem;
+    {
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = 0.0f;
+        tmem_st32(tb + lane_off + cH + 32 * part, v);
+        tmem_wait_st();
+    }
+    bool q_out = false, d_out = false, g_out = false, mma_out = false;
+    if (tid == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmD);
+        prefetch_tmap(&tmG);
+        mbar_arrive_expect_tx(&S.bar_q, kTile + 16384u);
+        tma_load_3d(sm + rW, &tmW, &S.bar_q, 0, 0, (int)kv);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+            tma_load_4d(sm + rQ + kb * 16384, &tmQ, &S.bar_q, 64 * kb, (int)(kv * GQ),
+                        (int)(c_last * CT), (int)b);
+        load_tile(sm + rD, &tmD, &S.bar_d, kv, c_last, b);
+        mbar_arrive_expect_tx(&S.bar_g, 8192u);
+        tma_load_4d(sm + rG, &tmG, &S.bar_g, 0, (int)kv, (int)(c_last * CT), (int)b);
+        q_out = d_out = g_out = true;
+    }
+    tc_fence_before();
+    __syncthreads();
+    const uint64_t dQ = kdesc(base + rQ), dW = mndesc(base + rW, 16384);
+    const uint64_t dQh = mndesc(base + rQh, 16384), dD = mndesc(base + rD, 16384);
+    uint32_t ph_q = 0, ph_d = 0, ph_g = 0, ph_u = 0, ph_h = 0;
+    float lam_tot = 0.0f;
+    bool ok = true;
+
+    for (int64_t c = c_last; c >= c_first; --c) {
+        const int64_t q0 = c * CT;
+        const int n = (int)min64(CT, s1 - q0);
+        const bool more = c > c_first;
+        // (1) U_q = q Wf
+        ok = rev_wait(&S.bar_q, ph_q, S, hdr, 50);
+        if (!ok) break;
+        if (tid == 0) {
+            q_out = false;
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t off = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + cU, dQ + off, dW + ((j * 2048) >> 4), idesc_bf16(128, 64, false, true),
+                         j > 0);
+            }
+            mma_commit(&S.bar_u);
+            mma_out = true;
+        }
+        // (2) gates: e^{b_t} per token and feature (at most 1), e^{b_31} for the decay
+        ok = rev_wait(&S.bar_g, ph_g, S, hdr, 51);
+        if (!ok) break;
+        {
+            const int gf = tid & 127, gq = tid >> 7;
+            const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + rG);
+            float bt[8];
+            float run = 0.0f;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int tt = 8 * gq + j;
+                run += tt < n ? log_sigmoid_f(__bfloat162float(sg[tt * 128 + gf])) : 0.0f;
+                bt[j] = run;
+            }
+            gpart[gq * 128 + gf] = run;
+            __syncthreads();
+            const float g0 = gpart[gf], g1 = gpart[128 + gf], g2 = gpart[256 + gf],
+                        g3 = gpart[384 + gf];
+            const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? g0 + g1 : (g0 + g1) + g2;
+            __nv_bfloat16* Eb = (__nv_bfloat16*)(sm + rE);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                Eb[(8 * gq + j) * EPR + gf] = __float2bfloat16_rn(ex2f((bt[j] + off) * kLog2e));
+            if (gq == 0) {
+                const float blast = (g0 + g1) + (g2 + g3);
+                S.el[gf] = ex2f(blast * kLog2e);
+                lam_tot += blast;
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            g_out = false;
+            if (more) {
+                mbar_arrive_expect_tx(&S.bar_g, 8192u);
+                tma_load_4d(sm + rG, &tmG, &S.bar_g, 0, (int)kv, (int)((c - 1) * CT), (int)b);
+                g_out = true;
+            }
+        }
+        // (3) the adjoint from later steps decays over this step: dH, dz *= e^{b_31}
+        {
+            float v[32];
+            tmem_ld32(tb + lane_off + cH + 32 * part, v);
+            tmem_wait_ld();
+            const float el = S.el[row];
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= el;
+            tmem_st32(tb + lane_off + cH + 32 * part, v);
+            tmem_wait_st();
+        }
+        // (4) q^ = phi(q) e^{b_t} a for row = 4 t + head
+        ok = rev_wait(&S.bar_u, ph_u, S, hdr, 52);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0) {
+            mma_out = false;
+            if (more) {
+                mbar_arrive_expect_tx(&S.bar_q, kTile);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+                    tma_load_4d(sm + rQ + kb * 16384, &tmQ, &S.bar_q, 64 * kb, (int)(kv * GQ),
+                                (int)((c - 1) * CT), (int)b);
+                q_out = true;
+            }
+        }
+        {
+            const int t = row >> 2, sib = part ^ 1;
+            const int64_t i = q0 + t;
+            const int64_t idx = (b * p.L + i) * p.Hq + kv * GQ + (row & 3);
+            const float ar = t < n ? rows[idx] : 0.0f;
+            if (part == 0) zq[512 + row] = t < n ? -rows[nrow + idx] : 0.0f;  // -delta per row
+            float uv[32];
+            tmem_ld32(tb + lane_off + cU + 32 * (part & 1), uv);
+            tmem_wait_ld();
+            float uext = -INFINITY;
+            if (part < 2) {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) uext = fmaxf(uext, uv[k]);
+            } else {
+#pragma unroll
+                for (int k = 0; k < 32; ++k) uext = fmaxf(uext, -uv[k]);
+            }
+            xum[part * 128 + row] = uext;
+            quad_sync(quad);
+            const float f2 = part < 2 ? kLog2e : -kLog2e;
+            const float cst = -fmaxf(xum[part * 128 + row], xum[sib * 128 + row]) * kLog2e;
+            float usum = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 32; ++k) {
+                uv[k] = ex2f(fmaf(uv[k], f2, cst));
+                usum += uv[k];
+            }
+            xus[part * 128 + row] = usum;
+            quad_sync(quad);
+            const float sc = ar / (xus[part * 128 + row] + xus[sib * 128 + row]);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const int f0 = 32 * part + 8 * ch;
+                uint32_t w0, w1, w2, w3;
+                ld_shared_v4(base + rE + (uint32_t)(t * EPR + f0) * 2u, w0, w1, w2, w3);
+                float eb[8], qh[8];
+                unpack8(w0, w1, w2, w3, eb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) qh[e] = uv[8 * ch + e] * sc * eb[e];
+                st_shared_v4(base + rQh + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                             pack_bf16(qh[0], qh[1]), pack_bf16(qh[2], qh[3]),
+                             pack_bf16(qh[4], qh[5]), pack_bf16(qh[6], qh[7]));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        // (5) dH += q^^T dY on the tensor cores while the threads sum dz
+        if (tid == 0) {
+            if (!mbar_wait(&S.bar_d, ph_d, kTimeout)) {
+                S.abort = 1;
+                report(hdr, LIZARD_ERR_TIMEOUT, 53);
+            } else {
+                ph_d ^= 1u;
+                d_out = false;
+                tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    mma_bf16(tb + cH, dQh + ((j * 2048) >> 4), dD + ((j * 2048) >> 4),
+                             idesc_bf16(128, 128, true, true), 1);
+                mma_commit(&S.bar_h);
+                mma_out = true;
+            }
+        }
+        {
+            // dz_f += sum_rows q^[row][f] (-delta_row), from the bf16 tile the MMA reads
+            const int f = tid & 127, gq = tid >> 7;
+            const __nv_bfloat16* qh = (const __nv_bfloat16*)(sm + rQh);
+            float zs = 0.0f;
+            for (int r = 32 * gq; r < 32 * gq + 32; ++r) {
+                const uint32_t off = (f >> 6) * 16384 + sw128(r, (f & 63) >> 3) + (f & 7) * 2;
+                zs = fmaf(__bfloat162float(qh[off / 2]), zq[512 + r], zs);
+            }
+            zq[gq * 128 + f] = zs;
+        }
+        __syncthreads();
+        if (tid < 128)
+            S.dz[tid] = fmaf(S.el[tid], S.dz[tid], (zq[tid] + zq[128 + tid]) + (zq[256 + tid] + zq[384 + tid]));
+        ok = rev_wait(&S.bar_h, ph_h, S, hdr, 54);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0) {
+            mma_out = false;
+            if (more) {
+                load_tile(sm + rD, &tmD, &S.bar_d, kv, c - 1, b);
+                d_out = true;
+            }
+        }
+    }
+
+    if (ok) {
+        float* r = rev_rec + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats;
+        float v[32];
+        tmem_ld32(tb + lane_off + cH + 32 * part, v);
+        tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; k += 4)
+            *reinterpret_cast<float4*>(r + row * DH + 32 * part + k) =
+                make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+        if (tid < 128) {
+            r[128 * DH + tid] = S.dz[tid];
+            r[128 * DH + 128 + tid] = lam_tot;
+        }
+    } else if (tid == 0) {
+        if (mma_out) {
+            mma_commit(&S.bar_fin);
+            mbar_wait(&S.bar_fin, 0, kTimeout);
+        }
+        if (q_out) mbar_wait(&S.bar_q, ph_q, kTimeout);
+        if (g_out) mbar_wait(&S.bar_g, ph_g, kTimeout);
+        if (d_out) mbar_wait(&S.bar_d, ph_d, kTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 256);
+    }
+}
+
 }  // namespace
 
 bool bwd_win_tc_supported(const Plan& p) {
     return p.dtype == LIZARD_BF16 && p.d == DH && p.G == GQ && p.w == WIN &&
            p.L < ((int64_t)1 << 30) && p.B * p.Hkv <= 65535 && tc::encode_fn() != nullptr;
+}
+
+bool bwd_rev_local_tc_supported(const Plan& p) {
+    return bwd_win_tc_supported(p) && p.D == 128;
+}
+
+cudaError_t launch_bwd_rev_local_tc(const Plan& p, const BwdArgs& a, const float* rows,
+                                    float* rev_rec, cudaStream_t s) {
+    if (p.P <= 1) return cudaSuccess;
+    alignas(64) CUtensorMap mq, md, mw, mg;
+    const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
+                     Hkv = (cuuint64_t)p.Hkv;
+    {
+        const cuuint64_t dims[4] = {DH, Hq, L, B};
+        const cuuint64_t str[3] = {DH * 2, Hq * DH * 2, L * Hq * DH * 2};
+        const cuuint32_t box[4] = {64, GQ, CT, 1};
+        if (!tc::make_map(&mq, a.q, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!tc::make_map(&md, a.dy, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {128, Hkv, L, B};
+        const cuuint64_t str[3] = {128 * 2, Hkv * 128 * 2, L * Hkv * 128 * 2};
+        const cuuint32_t box[4] = {128, 1, CT, 1};
+        if (!tc::make_map(&mg, a.g, 4, dims, str, box, false)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {64, DH, Hkv};
+        const cuuint64_t str[2] = {64 * 2, DH * 64 * 2};
+        const cuuint32_t box[3] = {64, DH, 1};
+        if (!tc::make_map(&mw, a.Wf, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(bwd_rev_local_tc,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemRev);
+    if (e != cudaSuccess) return e;
+    bwd_rev_local_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)(p.P - 1)), NT, kSmemRev, s>>>(
+        mq, md, mw, mg, p, a, rows, rev_rec);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_win_tc(const Plan& p, const BwdArgs& a, const float* rows, bool keys,

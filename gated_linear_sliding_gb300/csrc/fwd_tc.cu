@@ -1129,11 +1129,53 @@ __global__ void __launch_bounds__(NL, 1)
     }
 }
 
+// Segment pass (fwd_tc_local) over every segment but the last, then the exclusive scan:
+// a.seg receives the state each segment starts from.
+cudaError_t launch_local_and_scan(const Plan& p, const FwdArgs& a, const CUtensorMap& mw,
+                                  cudaStream_t s) {
+    const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hkv = (cuuint64_t)p.Hkv;
+    const unsigned U = (unsigned)(p.B * p.Hkv);
+    // 128-token tiles of the delayed keys, values and gates
+    alignas(64) CUtensorMap lk, lv, lg;
+    {
+        const cuuint64_t dims[4] = {DH, Hkv, L, B};
+        const cuuint64_t str[3] = {DH * 2, Hkv * DH * 2, L * Hkv * DH * 2};
+        const cuuint32_t box[4] = {64, 1, LT, 1};
+        if (!make_map(&lk, a.k, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!make_map(&lv, a.v, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {DF, Hkv, L, B};
+        const cuuint64_t str[3] = {DF * 2, Hkv * DF * 2, L * Hkv * DF * 2};
+        const cuuint32_t box[4] = {DF, 1, LT, 1};
+        if (!make_map(&lg, a.g, 4, dims, str, box, false)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(fwd_tc_local, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kLocalSmem);
+    if (e != cudaSuccess) return e;
+    fwd_tc_local<<<dim3(U, (unsigned)(p.P - 1)), NL, kLocalSmem, s>>>(lk, lv, mw, lg, p, a);
+    return launch_seg_scan(p, a.seg, s);
+}
+
+bool make_wf_map(CUtensorMap* mw, const void* Wf, int64_t Hkv) {
+    const cuuint64_t dims[3] = {DF / 2, DH, (cuuint64_t)Hkv};
+    const cuuint64_t str[2] = {(DF / 2) * 2, DH * (DF / 2) * 2};
+    const cuuint32_t box[3] = {DF / 2, DH, 1};
+    return make_map(mw, Wf, 3, dims, str, box);
+}
+
 }  // namespace
 
 bool fwd_tc_supported(const Plan& p) {
     return p.dtype == LIZARD_BF16 && p.d == DH && p.D == DF && p.G == GQ && p.w == WIN &&
            p.M <= MMAX && p.L < ((int64_t)1 << 30) && encode_fn() != nullptr;
+}
+
+cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+    if (p.P <= 1) return cudaSuccess;
+    alignas(64) CUtensorMap mw;
+    if (!make_wf_map(&mw, a.Wf, p.Hkv)) return cudaErrorInvalidValue;
+    return launch_local_and_scan(p, a, mw, s);
 }
 
 cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
@@ -1175,26 +1217,7 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const unsigned U = (unsigned)(p.B * p.Hkv);
     if (p.P > 1) {
-        // segment pass: 128-token tiles of the delayed keys, values and gates
-        alignas(64) CUtensorMap lk, lv, lg;
-        {
-            const cuuint64_t dims[4] = {DH, Hkv, L, B};
-            const cuuint64_t str[3] = {DH * 2, Hkv * DH * 2, L * Hkv * DH * 2};
-            const cuuint32_t box[4] = {64, 1, LT, 1};
-            if (!make_map(&lk, a.k, 4, dims, str, box)) return cudaErrorInvalidValue;
-            if (!make_map(&lv, a.v, 4, dims, str, box)) return cudaErrorInvalidValue;
-        }
-        {
-            const cuuint64_t dims[4] = {DF, Hkv, L, B};
-            const cuuint64_t str[3] = {DF * 2, Hkv * DF * 2, L * Hkv * DF * 2};
-            const cuuint32_t box[4] = {DF, 1, LT, 1};
-            if (!make_map(&lg, a.g, 4, dims, str, box, false)) return cudaErrorInvalidValue;
-        }
-        e = cudaFuncSetAttribute(fwd_tc_local, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)kLocalSmem);
-        if (e != cudaSuccess) return e;
-        fwd_tc_local<<<dim3(U, (unsigned)(p.P - 1)), NL, kLocalSmem, s>>>(lk, lv, mw, lg, p, a);
-        e = launch_seg_scan(p, a.seg, s);
+        e = launch_local_and_scan(p, a, mw, s);
         if (e != cudaSuccess) return e;
     }
     if (a.ev_before) cudaEventRecord(a.ev_before, s);

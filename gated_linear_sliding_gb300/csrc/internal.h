@@ -53,6 +53,8 @@ cudaError_t launch_fwd_states(const Plan& p, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s);
 bool fwd_tc_supported(const Plan& p);
 cudaError_t launch_fwd_tc(const Plan& p, const FwdArgs& a, cudaStream_t s);
+// Segment-start states only (tensor-core segment pass + scan into a.seg), for the backward.
+cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_ring_fill(const Plan& p, const void* k, const void* v, void* kc, void* vc,
                              cudaStream_t s);
 
@@ -82,6 +84,11 @@ struct BwdArgs {
 };
 size_t bwd_workspace_bytes(const Plan& p);
 bool bwd_win_tc_supported(const Plan& p);
+bool bwd_rev_local_tc_supported(const Plan& p);
+// Reverse segment pass on the tensor cores: each segment's contribution to the state adjoint
+// at its start (records as the forward's) into rev_rec.
+cudaError_t launch_bwd_rev_local_tc(const Plan& p, const BwdArgs& a, const float* rows,
+                                    float* rev_rec, cudaStream_t s);
 // Window parts of the gradients on the tensor cores: dk, dv (keys) or dq; `rows` is the
 // per-row table [e^{-lse}; dy . y].
 cudaError_t launch_bwd_win_tc(const Plan& p, const BwdArgs& a, const float* rows, bool keys,
