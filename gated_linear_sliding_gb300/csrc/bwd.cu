@@ -885,7 +885,12 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     }
     // 2. forward-direction walk
     if (a.ev_before) cudaEventRecord(a.ev_before, s);
-    bwd_forward_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
+    if (a.win_tc && bwd_rev_local_tc_supported(p)) {
+        e = launch_bwd_fwalk_tc(p, a, wsf, ws.rows, ws.fwd_rec, ws.dB, ws.dW, ws.dt, s);
+        if (e != cudaSuccess) return e;
+    } else {
+        bwd_forward_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
+    }
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
     // window part of dq on the tensor cores (the walk above wrote the state part)
     if (a.win_tc) {

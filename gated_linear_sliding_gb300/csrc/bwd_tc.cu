@@ -819,11 +819,641 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Forward-direction walk of the backward on the tensor cores: the state part of dq, the
+// phi(q)-side of dB, the dWf and dt partials of a segment, walking it in 32-token steps of
+// 128 query rows (row = 4 token + head) with the forward's state recurrence.  With
+// a_i = e^{-lse_i}, delta_i = dy_i . y_i and the forward's decay reference r of a step:
+//   D    = dY (e^{r} (.) H)^T + c k~i            c_it = dy_i . v'_t - delta_i,  t <= i
+//   dphi(q)_i = a_i e^{b_i - r} (.) (D_i - delta_i e^{r} (.) z)
+//   du   = phi+ (.) (dphi+ - phi+ . dphi+) - phi- (.) (dphi- - phi- . dphi-)
+//   dq   = du Wf^T,   dWf += q^T du,   dB_i += sum_heads phi(q_i) (.) dphi(q_i)
+// and the state moves on as in the forward: H <- e^{b_31} (.) H + k~u^T V_d.
+// dB feeds a reverse cumulative sum whose terms nearly cancel, so the operands of D that
+// are not exact in bf16 (the state copy, c, k~i) go in as a high and a low bf16 part, and
+// the decay factors stay in fp32.  Each thread owns 16 u-values of its row and both
+// feature-map halves built from them, so the feature-map backward needs no exchange of
+// feature values.
+constexpr uint32_t wQ = 0, wD = 32768, wK = 65536, wV = 73728, wW = 81920, wHh = 98304,
+                   wHl = 131072, wKih = 163840, wKil = 172032, wKu = 180224, wB = 188416,
+                   wG = 204800, wX = 212992, wSm = 217088;
+struct WSmall {
+    uint64_t bar_tma, bar_u, bar_d1, bar_d2, bar_q, bar_fin;
+    uint32_t tmem;
+    volatile int abort;
+    float z[128], zs[128], cf[128], bref[128];
+    float dts[4][4];
+};
+constexpr uint32_t kSmemFW = wSm + (uint32_t)sizeof(WSmall) + 1024;
+static_assert(kSmemFW <= 232448, "shared memory budget");
+// TMEM: H [0,128), D [128,256), U_q [256,320) and U_k [320,384) -> dq [256,384),
+// C [384,416) -> du (bf16 pairs) [384,416), c high [416,432), c low [432,448), dWf [448,512)
+constexpr uint32_t fH = 0, fD = 128, fUq = 256, fUk = 320, fDQ = 256, fC = 384, fDU = 384,
+                   fCh = 416, fCl = 432, fDW = 448;
+
+__device__ __forceinline__ bool fw_wait(uint64_t* bar, uint32_t& ph, WSmall& S, WsHeader* hdr,
+                                        unsigned where) {
+    bool fail = false;
+    if (!mbar_try_wait(bar, ph)) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, ph)) {
+            if (S.abort || clock64() - t0 > kTimeout) {
+                fail = true;
+                break;
+            }
+        }
+    }
+    if (fail && !S.abort) {
+        S.abort = 1;
+        report(hdr, LIZARD_ERR_TIMEOUT, where);
+    }
+    if (!fail) ph ^= 1u;
+    return !__syncthreads_or(fail);
+}
+
+__device__ __forceinline__ float clamp80f(float x) { return fminf(fmaxf(x, -80.0f), 80.0f); }
+
+// Split x into a bf16 high part and the bf16 rounding of the remainder.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    float h0 = x0, h1 = x1;
+    hi = round_pair(h0, h1);
+    lo = pack_bf16(x0 - h0, x1 - h1);
+}
+
+// Delayed keys or values of chunk c (two 64-column halves of 32 rows, 4 KB apart).
+__device__ __forceinline__ void load_delayed(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar,
+                                             int64_t kv, int64_t c, int64_t b) {
+#pragma unroll
+    for (int kb = 0; kb < 2; ++kb)
+        tma_load_4d(dst + kb * 4096, tm, bar, 64 * kb, (int)kv, (int)((c - 2) * CT), (int)b);
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    bwd_fwalk_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDY,
+                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
+                 Plan p, BwdArgs a, const float* rows, const float* fwd_rec, float* dB, float* dWp,
+                 float* dtp) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    WSmall& S = *reinterpret_cast<WSmall*>(sm + wSm);
+    float* xa = reinterpret_cast<float*>(sm + wX);   // [4][128]
+    float* xb = xa + 512;                            // [4][128]
+    float* suk = reinterpret_cast<float*>(sm + wG);  // staged U_k rows [32][64]
+    float* btab = reinterpret_cast<float*>(sm + wB); // cumulative log-gates [32][128]
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, part = warp >> 2;
+    const int row = 32 * quad + lane;
+    const int64_t unit = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t U = p.B * p.Hkv;
+    const int64_t s0 = seg * p.seg_len, s1 = min64(p.L, s0 + p.seg_len);
+    const int64_t c_begin = s0 / CT, c_end = (s1 + CT - 1) / CT;
+    const int64_t nrow = p.B * p.L * p.Hq;
+    WsHeader* hdr = (WsHeader*)a.ws;
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    constexpr uint32_t kStepBytes = 2 * kTile + 8192u + 8192u + 8192u;  // q, dY, k', v', gates
+
+    if (warp == 0) {
+        tmem_alloc(&S.tmem, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&S.bar_tma, 1);
+        mbar_init(&S.bar_u, 1);
+        mbar_init(&S.bar_d1, 1);
+        mbar_init(&S.bar_d2, 1);
+        mbar_init(&S.bar_q, 1);
+        mbar_init(&S.bar_fin, 1);
+        fence_mbar_init();
+        S.abort = 0;
+    }
+    const float* rec = seg > 0 ? fwd_rec + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats
+                               : nullptr;
+    if (tid < 128) S.z[tid] = rec ? rec[128 * DH + tid] : 0.0f;
+    if (tid < 16) S.dts[tid >> 2][tid & 3] = 0.0f;
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = S.tmem;
+    {
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + 32 * part + k] : 0.0f;
+        tmem_st32(tb + lane_off + fH + 32 * part, v);
+        tmem_wait_st();
+    }
+    bool tma_out = false, mma_out = false;
+    if (tid == 0 && c_begin < c_end) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmDY);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmG);
+        mbar_arrive_expect_tx(&S.bar_tma, kStepBytes + 16384u);
+        tma_load_3d(sm + wW, &tmW, &S.bar_tma, 0, 0, (int)kv);
+        load_delayed(sm + wK, &tmK, &S.bar_tma, kv, c_begin, b);
+        load_delayed(sm + wV, &tmV, &S.bar_tma, kv, c_begin, b);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_4d(sm + wQ + kb * 16384, &tmQ, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                        (int)(c_begin * CT), (int)b);
+            tma_load_4d(sm + wD + kb * 16384, &tmDY, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                        (int)(c_begin * CT), (int)b);
+        }
+        tma_load_4d(sm + wG, &tmG, &S.bar_tma, 0, (int)kv, (int)(c_begin * CT), (int)b);
+        tma_out = true;
+    }
+    tc_fence_before();
+    __syncthreads();
+    const uint64_t dQk = kdesc(base + wQ), dDk = kdesc(base + wD), dKk = kdesc(base + wK),
+                   dVk = kdesc(base + wV), dHh = kdesc(base + wHh), dHl = kdesc(base + wHl),
+                   dWk = kdesc(base + wW);
+    const uint64_t dWm = mndesc(base + wW, 16384), dVm = mndesc(base + wV, 4096),
+                   dKih = mndesc(base + wKih, 4096), dKil = mndesc(base + wKil, 4096),
+                   dKum = mndesc(base + wKu, 4096), dQm = mndesc(base + wQ, 16384),
+                   dDUm = mndesc(base + wKih, 16384);
+    uint32_t ph_tma = 0, ph_u = 0, ph_d1 = 0, ph_d2 = 0, ph_q = 0;
+    bool ok = true, dw_init = false;
+    float dts_acc = 0.0f;
+
+    for (int64_t c = c_begin; c < c_end; ++c) {
+        const int64_t t0 = c * CT;
+        const int n = (int)min64(CT, s1 - t0);
+        const bool more = c + 1 < c_end;
+        ok = fw_wait(&S.bar_tma, ph_tma, S, hdr, 60);
+        if (!ok) break;
+        if (tid == 0) {
+            tma_out = false;
+            tc_fence_after();
+            // (1) projections: U_k of the delayed keys (rows 0..31 of the tile; the MMA's other
+            //     rows read the neighbouring tiles and are never used), U_q
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                const uint32_t kdoff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+                const uint64_t bw = dWm + ((j * 2048) >> 4);
+                mma_bf16(tb + fUk, dKk + kdoff, bw, idesc_bf16(128, 64, false, true), j > 0);
+                mma_bf16(tb + fUq, dQk + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
+            }
+            mma_commit(&S.bar_u);
+            mma_out = true;
+        }
+        // (2) gates: cumulative log-sigmoid b (fp32 table), reference r = b_15
+        const int gf = tid & 127, gq = tid >> 7;
+        {
+            const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + wG);
+            float bt[8];
+            float run = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int tt = 8 * gq + t;
+                run += tt < n ? log_sigmoid_f(__bfloat162float(sg[tt * 128 + gf])) : 0.0f;
+                bt[t] = run;
+            }
+            xa[gq * 128 + gf] = run;
+            __syncthreads();
+            const float g0 = xa[gf], g1 = xa[128 + gf], g2 = xa[256 + gf], g3 = xa[384 + gf];
+            const float bref = g0 + g1, blast = bref + g2 + g3;
+            const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? bref : bref + g2;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) btab[(8 * gq + t) * 128 + gf] = bt[t] + off;
+            if (gq == 0) {
+                S.cf[gf] = __expf(blast - bref);
+                S.zs[gf] = __expf(bref) * S.z[gf];
+                S.bref[gf] = bref;
+            }
+        }
+        // (3) state copy e^{r} (.) H as high and low bf16 parts; master decayed by e^{b_31}
+        {
+            const int f = row;
+            const float g0 = xa[f], g1 = xa[128 + f], g2 = xa[256 + f], g3 = xa[384 + f];
+            const float er = __expf(g0 + g1), el = __expf(g0 + g1 + g2 + g3);
+            const int col = 32 * part;
+            float v[32];
+            tmem_ld32(tb + lane_off + fH + col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const uint32_t off = (col / 64) * 16384 + sw128(f, (col & 63) / 8 + ch);
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    split2(er * v[8 * ch + 2 * e], er * v[8 * ch + 2 * e + 1], hi[e], lo[e]);
+                st_shared_v4(base + wHh + off, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(base + wHl + off, lo[0], lo[1], lo[2], lo[3]);
+            }
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= el;
+            tmem_st32(tb + lane_off + fH + col, v);
+            tmem_wait_st();
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // (4) D = dY H_s^T (high + low parts), C = dY V_d^T
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                const uint32_t kdoff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + fD, dDk + koff, dHh + koff, idesc_bf16(128, 128, false, false), j > 0);
+                mma_bf16(tb + fD, dDk + koff, dHl + koff, idesc_bf16(128, 128, false, false), 1);
+                mma_bf16(tb + fC, dDk + koff, dVk + kdoff, idesc_bf16(128, 32, false, false), j > 0);
+            }
+            mma_commit(&S.bar_d1);
+        }
+        // (5) phi(q): this thread's 16 u-values give features f = 16 part + k of both halves
+        ok = fw_wait(&S.bar_u, ph_u, S, hdr, 61);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && more) {
+            // the delayed-key tile is consumed: the next step's copies start
+            mbar_arrive_expect_tx(&S.bar_tma, kStepBytes);
+            load_delayed(sm + wK, &tmK, &S.bar_tma, kv, c + 1, b);
+            tma_out = true;
+        }
+        if (quad == 0 && part < 2) {
+            float w[32];
+            tmem_ld32(tb + lane_off + fUk + 32 * part, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(suk + lane * 64 + 32 * part + k) =
+                    make_float4(w[k], w[k + 1], w[k + 2], w[k + 3]);
+        }
+        float php[16], phn[16];
+        {
+            float u[16];
+            tmem_ld8(tb + lane_off + fUq + 16 * part, u);
+            tmem_ld8(tb + lane_off + fUq + 16 * part + 8, u + 8);
+            tmem_wait_ld();
+            float mx = -INFINITY, mn = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                mx = fmaxf(mx, u[k]);
+                mn = fmaxf(mn, -u[k]);
+            }
+            xa[part * 128 + row] = mx;
+            xb[part * 128 + row] = mn;
+            quad_sync(quad);
+            mx = fmaxf(fmaxf(xa[row], xa[128 + row]), fmaxf(xa[256 + row], xa[384 + row]));
+            mn = fmaxf(fmaxf(xb[row], xb[128 + row]), fmaxf(xb[256 + row], xb[384 + row]));
+            float sp = 0.0f, sn = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                php[k] = __expf(u[k] - mx);
+                phn[k] = __expf(-u[k] - mn);
+                sp += php[k];
+                sn += phn[k];
+            }
+            quad_sync(quad);
+            xa[part * 128 + row] = sp;
+            xb[part * 128 + row] = sn;
+            quad_sync(quad);
+            sp = (xa[row] + xa[128 + row]) + (xa[256 + row] + xa[384 + row]);
+            sn = (xb[row] + xb[128 + row]) + (xb[256 + row] + xb[384 + row]);
+            const float ip = 1.0f / sp, in = 1.0f / sn;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                php[k] *= ip;
+                phn[k] *= in;
+            }
+        }
+        __syncthreads();
+        // (6) phi of the delayed keys -> k~i = phi e^{r - b_t} (high, low), k~u = k~i e^{b_31 - r}
+        {
+            const int t = tid >> 4, sub = tid & 15;
+            const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
+            const float4 u4 = *reinterpret_cast<const float4*>(suk + t * 64 + 4 * sub);
+            const float u[4] = {u4.x, u4.y, u4.z, u4.w};
+            float mx = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
+            float mn = fminf(fminf(u[0], u[1]), fminf(u[2], u[3]));
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            }
+            float ep[4], en[4], sp = 0.0f, sn = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                ep[e] = __expf(u[e] - mx);
+                en[e] = __expf(mn - u[e]);
+                sp += ep[e];
+                sn += en[e];
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                sp += __shfl_xor_sync(0xffffffffu, sp, o);
+                sn += __shfl_xor_sync(0xffffffffu, sn, o);
+            }
+            const float ip = dvalid ? 1.0f / sp : 0.0f, in = dvalid ? 1.0f / sn : 0.0f;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                const int f0 = 64 * kb + 4 * sub;
+                float ki[4], ku[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float ph = kb == 0 ? ep[e] * ip : en[e] * in;
+                    ki[e] = ph * __expf(clamp80f(S.bref[f0 + e] - btab[t * 128 + f0 + e]));
+                    ku[e] = ki[e] * S.cf[f0 + e];
+                }
+                const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
+                uint32_t h0, l0, h1, l1;
+                split2(ki[0], ki[1], h0, l0);
+                split2(ki[2], ki[3], h1, l1);
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + wKih + off), "r"(h0),
+                             "r"(h1)
+                             : "memory");
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + wKil + off), "r"(l0),
+                             "r"(l1)
+                             : "memory");
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + wKu + off),
+                             "r"(pack_bf16(ku[0], ku[1])), "r"(pack_bf16(ku[2], ku[3]))
+                             : "memory");
+            }
+        }
+        fence_async_smem();
+        __syncthreads();
+        if (tid == 0 && more) {
+            // the gate tile and the staged U_k rows are consumed
+            tma_load_4d(sm + wG, &tmG, &S.bar_tma, 0, (int)kv, (int)((c + 1) * CT), (int)b);
+        }
+        // z <- e^{b_31} z + sum_t k~u_t
+        if (tid < 128) {
+            const int f = tid;
+            float zsum = 0.0f;
+            const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + wKu);
+            for (int t = 0; t < CT; ++t) {
+                const uint32_t off = (f >> 6) * 4096 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
+                zsum += __bfloat162float(ku[off / 2]);
+            }
+            S.z[f] = fmaf(S.cf[f] * S.zs[f], 1.0f, zsum);
+        }
+        // (7) c_it = C_it - delta_i for delayed keys t <= i (8 keys per part), high and low
+        const int ti = row >> 2;
+        const int64_t ridx = (b * p.L + t0 + ti) * p.Hq + kv * GQ + (row & 3);
+        const bool rv = ti < n;
+        const float ar = rv ? rows[ridx] : 0.0f, dl = rv ? rows[nrow + ridx] : 0.0f;
+        ok = fw_wait(&S.bar_d1, ph_d1, S, hdr, 62);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && more) {
+            // dY is consumed
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+                tma_load_4d(sm + wD + kb * 16384, &tmDY, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                            (int)((c + 1) * CT), (int)b);
+        }
+        {
+            float cv[8];
+            tmem_ld8(tb + lane_off + fC + 8 * part, cv);
+            tmem_wait_ld();
+            uint32_t ch[4], cl[4];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2) {
+                float x2[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int t = 8 * part + e + h;
+                    const bool valid = rv && t <= ti && (t0 + t - WIN >= 0);
+                    x2[h] = valid ? cv[e + h] - dl : 0.0f;
+                }
+                split2(x2[0], x2[1], ch[e / 2], cl[e / 2]);
+            }
+            tmem_st4(tb + lane_off + fCh + 4 * part, ch);
+            tmem_st4(tb + lane_off + fCl + 4 * part, cl);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // (8) D += c k~i (high x high, high x low, low x high); H += k~u^T V_d
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const uint32_t bo = (j * 2048) >> 4;
+                mma_bf16_ts(tb + fD, tb + fCh + 8 * j, dKih + bo, idesc_bf16(128, 128, false, true), 1);
+                mma_bf16_ts(tb + fD, tb + fCh + 8 * j, dKil + bo, idesc_bf16(128, 128, false, true), 1);
+                mma_bf16_ts(tb + fD, tb + fCl + 8 * j, dKih + bo, idesc_bf16(128, 128, false, true), 1);
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                mma_bf16(tb + fH, dKum + ((j * 2048) >> 4), dVm + ((j * 2048) >> 4),
+                         idesc_bf16(128, 128, true, true), 1);
+            mma_commit(&S.bar_d2);
+        }
+        ok = fw_wait(&S.bar_d2, ph_d2, S, hdr, 63);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0 && more) {
+            // the delayed values are consumed
+            load_delayed(sm + wV, &tmV, &S.bar_tma, kv, c + 1, b);
+        }
+        // (9) dphi(q), the phi(q)-side of dB, du
+        {
+            float Dp[16], Dn[16];
+            tmem_ld8(tb + lane_off + fD + 16 * part, Dp);
+            tmem_ld8(tb + lane_off + fD + 16 * part + 8, Dp + 8);
+            tmem_ld8(tb + lane_off + fD + 64 + 16 * part, Dn);
+            tmem_ld8(tb + lane_off + fD + 64 + 16 * part + 8, Dn + 8);
+            tmem_wait_ld();
+            const int fp = 16 * part, fn = 64 + 16 * part;
+            float spd = 0.0f, snd = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                const float eqp = __expf(clamp80f(btab[ti * 128 + fp + k] - S.bref[fp + k]));
+                const float eqn = __expf(clamp80f(btab[ti * 128 + fn + k] - S.bref[fn + k]));
+                Dp[k] = ar * eqp * (Dp[k] - dl * S.zs[fp + k]);  // dphi+
+                Dn[k] = ar * eqn * (Dn[k] - dl * S.zs[fn + k]);  // dphi-
+                spd = fmaf(php[k], Dp[k], spd);
+                snd = fmaf(phn[k], Dn[k], snd);
+            }
+            // dB over the group's heads: rows 4 t .. 4 t + 3 are lanes of this warp
+            {
+                float bp[16], bn[16];
+#pragma unroll
+                for (int k = 0; k < 16; ++k) {
+                    float x = php[k] * Dp[k], y = phn[k] * Dn[k];
+                    x += __shfl_xor_sync(0xffffffffu, x, 1);
+                    y += __shfl_xor_sync(0xffffffffu, y, 1);
+                    x += __shfl_xor_sync(0xffffffffu, x, 2);
+                    y += __shfl_xor_sync(0xffffffffu, y, 2);
+                    bp[k] = x;
+                    bn[k] = y;
+                }
+                if ((lane & 3) == 0 && rv) {
+                    float* dst = dB + ((b * p.L + t0 + ti) * p.Hkv + kv) * 128;
+#pragma unroll
+                    for (int k = 0; k < 16; k += 4) {
+                        *reinterpret_cast<float4*>(dst + fp + k) =
+                            make_float4(bp[k], bp[k + 1], bp[k + 2], bp[k + 3]);
+                        *reinterpret_cast<float4*>(dst + fn + k) =
+                            make_float4(bn[k], bn[k + 1], bn[k + 2], bn[k + 3]);
+                    }
+                }
+            }
+            xa[part * 128 + row] = spd;
+            xb[part * 128 + row] = snd;
+            quad_sync(quad);
+            const float Sp = (xa[row] + xa[128 + row]) + (xa[256 + row] + xa[384 + row]);
+            const float Sn = (xb[row] + xb[128 + row]) + (xb[256 + row] + xb[384 + row]);
+            uint32_t dw8[8];
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+                float d2[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    d2[h] = php[k + h] * (Dp[k + h] - Sp) - phn[k + h] * (Dn[k + h] - Sn);
+                dw8[k / 2] = pack_bf16(d2[0], d2[1]);
+            }
+            // du as the A operand of dq (TMEM) and the B operand of dWf (shared memory)
+            tmem_st8(tb + lane_off + fDU + 8 * part, dw8);
+            st_shared_v4(base + wKih + sw128(row, 2 * part), dw8[0], dw8[1], dw8[2], dw8[3]);
+            st_shared_v4(base + wKih + sw128(row, 2 * part + 1), dw8[4], dw8[5], dw8[6], dw8[7]);
+            tmem_wait_st();
+        }
+        if (rv) dts_acc = fmaf(ar, dl, dts_acc);  // rows of one head are summed at the end
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // (10) dq = du Wf^T; dWf += q^T du
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mma_bf16_ts(tb + fDQ, tb + fDU + 8 * j, dWk + ((j * 32) >> 4),
+                            idesc_bf16(128, 128, false, false), j > 0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                mma_bf16(tb + fDW, dQm + ((j * 2048) >> 4), dDUm + ((j * 2048) >> 4),
+                         idesc_bf16(128, 64, true, true), (dw_init || j > 0) ? 1u : 0u);
+            mma_commit(&S.bar_q);
+        }
+        dw_init = true;
+        ok = fw_wait(&S.bar_q, ph_q, S, hdr, 64);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0) {
+            mma_out = false;
+            if (more) {
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+                    tma_load_4d(sm + wQ + kb * 16384, &tmQ, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                                (int)((c + 1) * CT), (int)b);
+            }
+        }
+        {
+            float v[32];
+            tmem_ld32(tb + lane_off + fDQ + 32 * part, v);
+            tmem_wait_ld();
+            if (rv) {
+                __nv_bfloat16* dq = (__nv_bfloat16*)a.dq + ridx * DH + 32 * part;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint4 w;
+                    w.x = pack_bf16(v[8 * ch], v[8 * ch + 1]);
+                    w.y = pack_bf16(v[8 * ch + 2], v[8 * ch + 3]);
+                    w.z = pack_bf16(v[8 * ch + 4], v[8 * ch + 5]);
+                    w.w = pack_bf16(v[8 * ch + 6], v[8 * ch + 7]);
+                    *reinterpret_cast<uint4*>(dq + 8 * ch) = w;
+                }
+            }
+        }
+        tc_fence_before();
+        __syncthreads();
+    }
+
+    if (ok) {
+        // dWf partial of the segment (lane = d, 16 feature columns per part) and dt partials
+        float v[16];
+        tmem_ld8(tb + lane_off + fDW + 16 * part, v);
+        tmem_ld8(tb + lane_off + fDW + 16 * part + 8, v + 8);
+        tmem_wait_ld();
+        float* dst = dWp + ((size_t)seg * (size_t)U + (size_t)unit) * (size_t)(DH * 64) + row * 64 +
+                     16 * part;
+#pragma unroll
+        for (int k = 0; k < 16; k += 4)
+            *reinterpret_cast<float4*>(dst + k) =
+                dw_init ? make_float4(v[k], v[k + 1], v[k + 2], v[k + 3])
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        // dt partial: sum of a delta over the segment's rows of each head (head = row % 4),
+        // in a fixed order: lanes of a warp, then the four lane quadrants
+        if (part == 0) {
+            float x = dts_acc;
+            x += __shfl_xor_sync(0xffffffffu, x, 4);
+            x += __shfl_xor_sync(0xffffffffu, x, 8);
+            x += __shfl_xor_sync(0xffffffffu, x, 16);
+            if (lane < 4) S.dts[quad][lane] = x;
+        }
+        __syncthreads();
+        if (tid < GQ)
+            dtp[((size_t)seg * (size_t)U + (size_t)unit) * GQ + tid] =
+                (S.dts[0][tid] + S.dts[1][tid]) + (S.dts[2][tid] + S.dts[3][tid]);
+    } else if (tid == 0) {
+        if (mma_out) {
+            mma_commit(&S.bar_fin);
+            mbar_wait(&S.bar_fin, 0, kTimeout);
+        }
+        if (tma_out) mbar_wait(&S.bar_tma, ph_tma, kTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
 }  // namespace
 
 bool bwd_win_tc_supported(const Plan& p) {
     return p.dtype == LIZARD_BF16 && p.d == DH && p.G == GQ && p.w == WIN &&
            p.L < ((int64_t)1 << 30) && p.B * p.Hkv <= 65535 && tc::encode_fn() != nullptr;
+}
+
+cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
+                                size_t o_fwd, size_t o_dB, size_t o_dW, size_t o_dt,
+                                cudaStream_t s) {
+    alignas(64) CUtensorMap mq, md, mk, mv, mw, mg;
+    const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
+                     Hkv = (cuuint64_t)p.Hkv;
+    {
+        const cuuint64_t dims[4] = {DH, Hq, L, B};
+        const cuuint64_t str[3] = {DH * 2, Hq * DH * 2, L * Hq * DH * 2};
+        const cuuint32_t box[4] = {64, GQ, CT, 1};
+        if (!tc::make_map(&mq, a.q, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!tc::make_map(&md, a.dy, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {DH, Hkv, L, B};
+        const cuuint64_t str[3] = {DH * 2, Hkv * DH * 2, L * Hkv * DH * 2};
+        const cuuint32_t box[4] = {64, 1, CT, 1};
+        if (!tc::make_map(&mk, a.k, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!tc::make_map(&mv, a.v, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {128, Hkv, L, B};
+        const cuuint64_t str[3] = {128 * 2, Hkv * 128 * 2, L * Hkv * 128 * 2};
+        const cuuint32_t box[4] = {128, 1, CT, 1};
+        if (!tc::make_map(&mg, a.g, 4, dims, str, box, false)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {64, DH, Hkv};
+        const cuuint64_t str[2] = {64 * 2, DH * 64 * 2};
+        const cuuint32_t box[3] = {64, DH, 1};
+        if (!tc::make_map(&mw, a.Wf, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(bwd_fwalk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemFW);
+    if (e != cudaSuccess) return e;
+    bwd_fwalk_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemFW, s>>>(
+        mq, md, mk, mv, mw, mg, p, a, wsf + o_rows, wsf + o_fwd, wsf + o_dB, wsf + o_dW,
+        wsf + o_dt);
+    return cudaGetLastError();
 }
 
 bool bwd_rev_local_tc_supported(const Plan& p) {
