@@ -260,26 +260,44 @@ __device__ __forceinline__ void state_step(float* sH, float* sz, float* sphk, co
 }
 
 // Adjoint accumulation: [dH | dz] += sum_t (e^{b_t} phq_t a_t) [dy_t, -delta_t].
-// Overwrites sphq with the scaled rows.
+// Overwrites sphq with the scaled rows.  Each thread accumulates a block of DF/8 features x
+// DH/32 columns in registers (columns lane + 32 k, features of its warp), so a step reads
+// each scaled feature once per warp and each dy value once per thread.
 template <int DH, int DF, bool FAST>
 __device__ __forceinline__ void adjoint_add(float* sH, float* sz, float* sphq, const float* sdy,
                                             const float* sb, const float* srow, int n) {
     constexpr int PF = DF + 1, PH = DH + 1;
+    constexpr int NWARP = NT / 32, FB = DF / NWARP, NCC = DH / 32;
     for (int e = threadIdx.x; e < TS * DF; e += NT) {
         const int t = e / DF, f = e % DF;
         sphq[t * PF + f] *= ex<FAST>(sb[t * PF + f]) * srow[t];
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < DF * DH; e += NT) {
-        const int f = e / DH, c = e % DH;
-        float acc = sH[f * PH + c];
-        for (int t = 0; t < n; ++t) acc = fmaf(sphq[t * PF + f], sdy[t * PH + c], acc);
-        sH[f * PH + c] = acc;
+    const int lane = threadIdx.x & 31, wf = (threadIdx.x >> 5) * FB;
+    float acc[FB][NCC];
+#pragma unroll
+    for (int j = 0; j < FB; ++j)
+#pragma unroll
+        for (int k = 0; k < NCC; ++k) acc[j][k] = sH[(wf + j) * PH + lane + 32 * k];
+    for (int t = 0; t < n; ++t) {
+        float dyv[NCC];
+#pragma unroll
+        for (int k = 0; k < NCC; ++k) dyv[k] = sdy[t * PH + lane + 32 * k];
+#pragma unroll
+        for (int j = 0; j < FB; ++j) {
+            const float ph = sphq[t * PF + wf + j];
+#pragma unroll
+            for (int k = 0; k < NCC; ++k) acc[j][k] = fmaf(ph, dyv[k], acc[j][k]);
+        }
     }
+#pragma unroll
+    for (int j = 0; j < FB; ++j)
+#pragma unroll
+        for (int k = 0; k < NCC; ++k) sH[(wf + j) * PH + lane + 32 * k] = acc[j][k];
     if (threadIdx.x < DF) {
-        float acc = sz[threadIdx.x];
-        for (int t = 0; t < n; ++t) acc = fmaf(-sphq[t * PF + threadIdx.x], srow[TS + t], acc);
-        sz[threadIdx.x] = acc;
+        float za = sz[threadIdx.x];
+        for (int t = 0; t < n; ++t) za = fmaf(-sphq[t * PF + threadIdx.x], srow[TS + t], za);
+        sz[threadIdx.x] = za;
     }
     __syncthreads();
 }
@@ -591,10 +609,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
                 const float dec = ex<FAST>(sb[(TS - 1) * PF + f] - sb[r * PF + f]);
                 dk_acc[j] = dec * (dk_acc[j] + sz[f]);
             }
+            // weights e^{bl - b_t} phk_t of the end term, once per (row, feature) (sdp is free)
+            for (int e = tid; e < TS * DF; e += NT) {
+                const int t = e / DF, f = e % DF;
+                sdp[t * PF + f] = ex<FAST>(sb[(TS - 1) * PF + f] - sb[t * PF + f]) * sphk[t * PF + f];
+            }
+            __syncthreads();
 #pragma unroll
             for (int j = 0; j < NC; ++j) dv_acc[j] = 0.0f;
             for (int f = 0; f < DF; ++f) {
-                const float w_ = ex<FAST>(sb[(TS - 1) * PF + f] - sb[r * PF + f]) * sphk[r * PF + f];
+                const float w_ = sdp[r * PF + f];
 #pragma unroll
                 for (int j = 0; j < NC; ++j) dv_acc[j] = fmaf(sH[f * PH + cs + LPR * j], w_, dv_acc[j]);
             }
