@@ -82,7 +82,11 @@ struct BLay {
     static constexpr int oA2 = oA + TS * (TS + 1);  // second pair matrix [TS][TS+1]
     static constexpr int orow = oA2 + TS * (TS + 1);  // a_i, delta_i, lse_i [3][TS]
     static constexpr int otile = orow + 3 * TS;     // window key/value tiles [2][KB][PH], ds [TS][KB]
-    static constexpr int total = otile + 2 * KB * PH + TS * KB;
+                                                    // (reverse walk: decay tables [2][TS][PF], [2][DF])
+    static constexpr int ntile = 2 * KB * PH + TS * KB > 2 * TS * PF + 2 * DF
+                                     ? 2 * KB * PH + TS * KB
+                                     : 2 * TS * PF + 2 * DF;
+    static constexpr int total = otile + ntile;
     static constexpr size_t bytes = sizeof(float) * (size_t)total;
 };
 
@@ -265,12 +269,15 @@ __device__ __forceinline__ void state_step(float* sH, float* sz, float* sphk, co
 // each scaled feature once per warp and each dy value once per thread.
 template <int DH, int DF, bool FAST>
 __device__ __forceinline__ void adjoint_add(float* sH, float* sz, float* sphq, const float* sdy,
-                                            const float* sb, const float* srow, int n) {
+                                            const float* sb, const float* srow, int n,
+                                            const float* ser = nullptr) {
     constexpr int PF = DF + 1, PH = DH + 1;
     constexpr int NWARP = NT / 32, FB = DF / NWARP, NCC = DH / 32;
+    // rows become e^{b_t} phi(q_t) a_t; when ser is given the rows already carry e^{b_t - r}
+    // and ser[f] = e^{r_f} completes the factor
     for (int e = threadIdx.x; e < TS * DF; e += NT) {
         const int t = e / DF, f = e % DF;
-        sphq[t * PF + f] *= ex<FAST>(sb[t * PF + f]) * srow[t];
+        sphq[t * PF + f] *= (ser ? ser[f] : ex<FAST>(sb[t * PF + f])) * srow[t];
     }
     __syncthreads();
     const int lane = threadIdx.x & 31, wf = (threadIdx.x >> 5) * FB;
@@ -564,6 +571,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
     float *sphk = sm + Ly::ophk, *sv = sm + Ly::ov, *sq = sm + Ly::oq, *sphq = sm + Ly::ophq;
     float *sdp = sm + Ly::odp, *sdy = sm + Ly::ody, *sA = sm + Ly::oA, *sA2 = sm + Ly::oA2;
     float* srow = sm + Ly::orow;
+    // decay tables in the window-tile area (unused by this walk)
+    float* sE = sm + Ly::otile;           // [TS][PF]
+    float* sK = sE + TS * PF;             // [TS][PF]
+    float* ser = sK + TS * PF;            // [DF]
+    float* sel = ser + DF;                // [DF]
+    static_assert(2 * TS * (DF + 1) + 2 * DF <= Ly::ntile, "tables fit");
     const int64_t unit = blockIdx.x, seg = blockIdx.y;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
     const int64_t U = p.B * p.Hkv;
@@ -591,6 +604,19 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
         load_rows_p<T, DH>((const T*)a.v, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n, sv);
         __syncthreads();
         phi_rows_p<DH, DF, FAST>(sq, sW, sphk, rlo, n);
+        // decay tables around the step's midpoint r = b_{TS/2-1}: sE = e^{b_t - r},
+        // sK = e^{r - b_t}, so e^{b_i - b_t} = sE_i sK_t without an exponential per pair;
+        // ser = e^{r}, sel = e^{bl - r}
+        for (int e = tid; e < TS * DF; e += NT) {
+            const int t = e / DF, f = e % DF;
+            const float d = sb[t * PF + f] - sb[(TS / 2 - 1) * PF + f];
+            sE[t * PF + f] = ex<FAST>(fminf(fmaxf(d, -80.0f), 80.0f));
+            sK[t * PF + f] = ex<FAST>(fminf(fmaxf(-d, -80.0f), 80.0f));
+        }
+        if (tid < DF) {
+            ser[tid] = ex<FAST>(sb[(TS / 2 - 1) * PF + tid]);
+            sel[tid] = ex<FAST>(sb[(TS - 1) * PF + tid] - sb[(TS / 2 - 1) * PF + tid]);
+        }
         __syncthreads();
         // terms through the step's end: dphk_t = e^{bl - b_t} (.) (dH v'_t + dz),
         // dv'_t = sum_f e^{bl_f - b_tf} phk_tf dH[f][.]   (row t = r, in registers)
@@ -603,16 +629,16 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
 #pragma unroll
                 for (int j = 0; j < NF; ++j) dk_acc[j] = fmaf(sH[(cs + LPR * j) * PH + c], vc, dk_acc[j]);
             }
+            // dk_acc holds e^{r - b_t} times the sum; the common factor sK is applied at the end
 #pragma unroll
             for (int j = 0; j < NF; ++j) {
                 const int f = cs + LPR * j;
-                const float dec = ex<FAST>(sb[(TS - 1) * PF + f] - sb[r * PF + f]);
-                dk_acc[j] = dec * (dk_acc[j] + sz[f]);
+                dk_acc[j] = sel[f] * (dk_acc[j] + sz[f]);
             }
             // weights e^{bl - b_t} phk_t of the end term, once per (row, feature) (sdp is free)
             for (int e = tid; e < TS * DF; e += NT) {
                 const int t = e / DF, f = e % DF;
-                sdp[t * PF + f] = ex<FAST>(sb[(TS - 1) * PF + f] - sb[t * PF + f]) * sphk[t * PF + f];
+                sdp[t * PF + f] = sel[f] * sK[t * PF + f] * sphk[t * PF + f];
             }
             __syncthreads();
 #pragma unroll
@@ -639,6 +665,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
             __syncthreads();
             phi_rows_p<DH, DF, FAST>(sq, sW, sphq, 0, n);
             __syncthreads();
+            // phq rows carry e^{b_i - r} from here on
+            for (int e = tid; e < TS * DF; e += NT) {
+                const int t = e / DF, f = e % DF;
+                sphq[t * PF + f] *= sE[t * PF + f];
+            }
+            __syncthreads();
             // c_it = a_i (v'_t.dy_i - delta_i); A_it a_i = a_i sum_f phq_if phk_tf e^{b_if - b_tf}
             {
                 const int i = r, t = cs;
@@ -649,8 +681,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
                     cv = srow[i] * (d - srow[TS + i]);
                     float s = 0.0f;
                     for (int f = 0; f < DF; ++f)
-                        s = fmaf(sphq[i * PF + f] * sphk[t * PF + f],
-                                 ex<FAST>(sb[i * PF + f] - sb[t * PF + f]), s);
+                        s = fmaf(sphq[i * PF + f], sphk[t * PF + f] * sK[t * PF + f], s);
                     av = s * srow[i];
                 }
                 sA[i * (TS + 1) + t] = cv;
@@ -661,10 +692,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
 #pragma unroll
             for (int j = 0; j < NF; ++j) {
                 const int f = cs + LPR * j;
-                const float bt = sb[r * PF + f];
                 float v = 0.0f;
-                for (int i = r; i < n; ++i)
-                    v = fmaf(ex<FAST>(sb[i * PF + f] - bt) * sphq[i * PF + f], sA[i * (TS + 1) + r], v);
+                for (int i = r; i < n; ++i) v = fmaf(sphq[i * PF + f], sA[i * (TS + 1) + r], v);
                 dk_acc[j] += v;
             }
 #pragma unroll
@@ -675,12 +704,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
                 dv_acc[j] += v;
             }
             __syncthreads();
-            adjoint_add<DH, DF, FAST>(sH, sz, sphq, sdy, sb, srow, n);
+            adjoint_add<DH, DF, FAST>(sH, sz, sphq, sdy, sb, srow, n, ser);
         }
-        // dphk into sdp (rows outside [rlo, n) are zero)
+        // dphk into sdp (rows outside [rlo, n) are zero), with the factor e^{r - b_t}
 #pragma unroll
         for (int j = 0; j < NF; ++j)
-            sdp[r * PF + cs + LPR * j] = (r >= rlo && r < n) ? dk_acc[j] : 0.0f;
+            sdp[r * PF + cs + LPR * j] =
+                (r >= rlo && r < n) ? sK[r * PF + cs + LPR * j] * dk_acc[j] : 0.0f;
         __syncthreads();
         // dB = (phi(q)-side, from the forward walk) - phk (.) dphk; reverse cumsum in place
         if (tid < DF) {
