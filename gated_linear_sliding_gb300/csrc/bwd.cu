@@ -963,7 +963,12 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
         bwd_reverse_scan<<<dim3((nE + 255) / 256, U), 256, 0, s>>>(p, wsf + ws.rev_rec);
     }
     // 4. reverse-direction walk
-    bwd_reverse_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
+    if (a.win_tc && bwd_rev_local_tc_supported(p)) {
+        e = launch_bwd_rwalk_tc(p, a, wsf, ws.rows, ws.rev_rec, ws.dB, ws.dW, ws.tot, s);
+        if (e != cudaSuccess) return e;
+    } else {
+        bwd_reverse_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
+    }
     // 5. window parts of dk, dv
     if (a.win_tc) {
         e = launch_bwd_win_tc(p, a, wsf + ws.rows, true, s);

@@ -1408,6 +1408,637 @@ __global__ void __launch_bounds__(NT, 1)
     }
 }
 
+// ---------------------------------------------------------------------------------------
+// Reverse-direction walk of the backward on the tensor cores: the state parts of dk, dv of
+// the delayed keys, the phi(k')-side of dB with its reverse cumulative sum inside the
+// segment, and the dWf partial of the key side.  The segment is walked backwards in 32-token
+// steps of 128 query rows (row = 4 token + head) and 32 delayed keys.  With the step's
+// cumulative log-gates b (from its start), a reference rho = max(b_15, -60) per feature,
+// a_i = e^{-lse_i}, delta_i = dy_i . y_i and the stored adjoint S (dH at the step start is
+// e^{rho} (.) S):
+//   S'   = e^{bl - rho + rho_next} (.) S_next             (the adjoint at the step end)
+//   q^_i = phi(q_i) a_i e^{b_i - rho},   k^_t = phi(k'_t) e^{rho - b_t}
+//   dphi(k')_t = e^{rho - b_t} (.) (S' v'_t + z' + sum_{i >= t} q^_i (dy_i . v'_t - delta_i))
+//   dv'_t = S'^T k^_t + sum_{i >= t} (q^_i . k^_t) dy_i
+//   S    = S' + q^^T dY,  z = z' - q^^T delta
+// then dk' = du' Wf^T and dWf += k'^T du' from the feature-map backward du'.  The terms of
+// dphi(k') that feed dB go in as high and low bf16 parts (dB feeds a nearly cancelling
+// reverse cumulative sum); the decay factors stay in fp32.  Lanes hold features for the
+// key-side accumulators ([f x keys]) and d for the outputs ([d x keys]).
+constexpr uint32_t vR1 = 0, vR2 = 65536, vR3 = 98304, vK = 131072, vV = 139264, vW = 147456,
+                   vG = 163840, vB = 172032, vPK = 188416, vDU = 204800, vX = 208896,
+                   vSm = 221696;
+struct VSmall {
+    uint64_t bar_tma, bar_u, bar_g, bar_a, bar_v, bar_k, bar_fin;
+    uint32_t tmem;
+    volatile int abort;
+    float z[128], rho_next[128], carry[128], rho[128];
+};
+constexpr uint32_t kSmemRW = vSm + (uint32_t)sizeof(VSmall) + 1024;
+static_assert(kSmemRW <= 232448, "shared memory budget");
+// TMEM: S [0,128), G [128,160) (dphi(k') sums), C [160,192), A [192,224), dv'^T [224,256),
+// dk'^T [256,288), dWf [288,352), U_q [352,416), U_k [416,480)
+constexpr uint32_t vS = 0, vGc = 128, vC = 160, vA = 192, vDV = 224, vDK = 256, vDW = 288,
+                   vUq = 352, vUk = 416;
+
+// Byte offset of element (key t, row i) in a [32 keys x 128 rows] bf16 tile stored K-major
+// over rows (two 64-row halves of 4 KB, 128-byte swizzle).
+__device__ __forceinline__ uint32_t kt_off(int t, int i) {
+    return (uint32_t)(i >> 6) * 4096u + sw128(t, (i & 63) >> 3) + (i & 7) * 2;
+}
+
+__device__ __forceinline__ bool fw_wait2(uint64_t* bar, uint32_t& ph, volatile int& abort,
+                                         WsHeader* hdr, unsigned where) {
+    bool fail = false;
+    if (!mbar_try_wait(bar, ph)) {
+        const long long t0 = clock64();
+        while (!mbar_try_wait(bar, ph)) {
+            if (abort || clock64() - t0 > kTimeout) {
+                fail = true;
+                break;
+            }
+        }
+    }
+    if (fail && !abort) {
+        abort = 1;
+        report(hdr, LIZARD_ERR_TIMEOUT, where);
+    }
+    if (!fail) ph ^= 1u;
+    return !__syncthreads_or(fail);
+}
+
+__global__ void __launch_bounds__(NT, 1)
+    bwd_rwalk_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDY,
+                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                 const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
+                 Plan p, BwdArgs a, const float* rows, const float* rev_rec, float* dB,
+                 float* dWp, float* totp) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    uint8_t* sm = smem_raw + (base - raw);
+    VSmall& S = *reinterpret_cast<VSmall*>(sm + vSm);
+    float* xa = reinterpret_cast<float*>(sm + vX);    // [4][128]
+    float* xb = xa + 512;                             // [4][128]
+    float* tn = xb + 512;                             // [64 f][32 keys]
+    static_assert(vX + 4 * (512 + 512 + 2048 + 128) <= vSm, "exchange area");
+    float* suk = reinterpret_cast<float*>(sm + vG);   // staged U_k rows [32][64]
+    float* btab = reinterpret_cast<float*>(sm + vB);  // cumulative log-gates [32][128]
+    float* pk = reinterpret_cast<float*>(sm + vPK);   // phi(k') [32][128] fp32
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quad = warp & 3, part = warp >> 2;
+    const int row = 32 * quad + lane;
+    const int64_t unit = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t U = p.B * p.Hkv;
+    const int64_t s0 = seg * p.seg_len, s1 = min64(p.L, s0 + p.seg_len);
+    const int64_t c_first = s0 / CT, c_last = (s1 - 1) / CT;
+    const int64_t nrow = p.B * p.L * p.Hq;
+    WsHeader* hdr = (WsHeader*)a.ws;
+    const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
+    constexpr uint32_t kStepBytes = 2 * kTile + 8192u + 8192u + 8192u;  // q, dY, k', v', gates
+
+    if (warp == 0) {
+        tmem_alloc(&S.tmem, 512);
+        tmem_relinquish();
+    }
+    if (tid == 0) {
+        mbar_init(&S.bar_tma, 1);
+        mbar_init(&S.bar_u, 1);
+        mbar_init(&S.bar_g, 1);
+        mbar_init(&S.bar_a, 1);
+        mbar_init(&S.bar_v, 1);
+        mbar_init(&S.bar_k, 1);
+        mbar_init(&S.bar_fin, 1);
+        fence_mbar_init();
+        S.abort = 0;
+    }
+    const bool last = seg == p.P - 1;
+    const float* rec = last ? nullptr : rev_rec + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats;
+    if (tid < 128) {
+        S.z[tid] = rec ? rec[128 * DH + tid] : 0.0f;
+        S.rho_next[tid] = 0.0f;
+        S.carry[tid] = 0.0f;
+    }
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tb = S.tmem;
+    {
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + 32 * part + k] : 0.0f;
+        tmem_st32(tb + lane_off + vS + 32 * part, v);
+        tmem_wait_st();
+    }
+    bool tma_out = false, mma_out = false;
+    if (tid == 0) {
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmDY);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+        prefetch_tmap(&tmG);
+        mbar_arrive_expect_tx(&S.bar_tma, kStepBytes + 16384u);
+        tma_load_3d(sm + vW, &tmW, &S.bar_tma, 0, 0, (int)kv);
+        load_delayed(sm + vK, &tmK, &S.bar_tma, kv, c_last, b);
+        load_delayed(sm + vV, &tmV, &S.bar_tma, kv, c_last, b);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb) {
+            tma_load_4d(sm + vR2 + kb * 16384, &tmQ, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                        (int)(c_last * CT), (int)b);
+            tma_load_4d(sm + vR3 + kb * 16384, &tmDY, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                        (int)(c_last * CT), (int)b);
+        }
+        tma_load_4d(sm + vG, &tmG, &S.bar_tma, 0, (int)kv, (int)(c_last * CT), (int)b);
+        tma_out = true;
+    }
+    tc_fence_before();
+    __syncthreads();
+    const uint64_t dQk = kdesc(base + vR2), dDk = kdesc(base + vR3), dKk = kdesc(base + vK),
+                   dVk = kdesc(base + vV), dWk = kdesc(base + vW);
+    const uint64_t dWm = mndesc(base + vW, 16384), dDm = mndesc(base + vR3, 16384),
+                   dKm = mndesc(base + vK, 4096);
+    // R1 as the adjoint copy S' (K-major over d / MN-major over d), then as q^ (MN-major over f
+    // for the f-row products, K-major over f for A = q^ k^^T)
+    const uint64_t dS1h = kdesc(base + vR1), dS1l = kdesc(base + vR1 + 32768),
+                   dS1hm = mndesc(base + vR1, 16384);
+    const uint64_t dQhm = mndesc(base + vR1, 16384), dQlm = mndesc(base + vR1 + 32768, 16384),
+                   dQhk = kdesc(base + vR1);
+    // R2 after the query tile: k^ [32 keys][128 f] (8 KB), c high, c low, A^ (transposed tiles)
+    const uint64_t dKh = kdesc(base + vR2), dCh = kdesc(base + vR2 + 8192),
+                   dCl = kdesc(base + vR2 + 16384), dAh = kdesc(base + vR2 + 24576);
+    const uint64_t dDUk = kdesc(base + vDU), dDUm = mndesc(base + vDU, 4096);
+    uint32_t ph_tma = 0, ph_u = 0, ph_g = 0, ph_a = 0, ph_v = 0, ph_k = 0;
+    bool ok = true, dw_init = false;
+
+    for (int64_t c = c_last; c >= c_first; --c) {
+        const int64_t t0 = c * CT;
+        const int n = (int)min64(CT, s1 - t0);
+        const bool more = c > c_first;
+        ok = fw_wait2(&S.bar_tma, ph_tma, S.abort, hdr, 70);
+        if (!ok) break;
+        if (tid == 0) {
+            tma_out = false;
+            tc_fence_after();
+            // (1) U_q, U_k of the delayed keys (rows 0..31), C = dY V_d^T
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                const uint32_t kdoff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+                const uint64_t bw = dWm + ((j * 2048) >> 4);
+                mma_bf16(tb + vUq, dQk + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
+                mma_bf16(tb + vUk, dKk + kdoff, bw, idesc_bf16(128, 64, false, true), j > 0);
+                mma_bf16(tb + vC, dDk + koff, dVk + kdoff, idesc_bf16(128, 32, false, false), j > 0);
+            }
+            mma_commit(&S.bar_u);
+            mma_out = true;
+        }
+        // (2) gates: b (fp32 table), rho = max(b_15, -60), decay of the stored adjoint
+        const int gf = tid & 127, gq = tid >> 7;
+        {
+            const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + vG);
+            float bt[8];
+            float run = 0.0f;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+                const int tt = 8 * gq + t;
+                run += tt < n ? log_sigmoid_f(__bfloat162float(sg[tt * 128 + gf])) : 0.0f;
+                bt[t] = run;
+            }
+            xa[gq * 128 + gf] = run;
+            __syncthreads();
+            const float g0 = xa[gf], g1 = xa[128 + gf], g2 = xa[256 + gf];
+            const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? g0 + g1 : (g0 + g1) + g2;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) btab[(8 * gq + t) * 128 + gf] = bt[t] + off;
+        }
+        __syncthreads();
+        // (3) S' = e^{bl - rho + rho_next} (.) S, as high and low bf16 parts for the
+        //     key-side products; z' likewise
+        {
+            const int f = row;
+            const float bl = btab[31 * 128 + f], rh = fmaxf(btab[15 * 128 + f], -60.0f);
+            const float fac = __expf(bl - rh + S.rho_next[f]);
+            const int col = 32 * part;
+            float v[32];
+            tmem_ld32(tb + lane_off + vS + col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) v[k] *= fac;
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const uint32_t off = (col / 64) * 16384 + sw128(f, (col & 63) / 8 + ch);
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split2(v[8 * ch + 2 * e], v[8 * ch + 2 * e + 1], hi[e], lo[e]);
+                st_shared_v4(base + vR1 + off, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(base + vR1 + 32768 + off, lo[0], lo[1], lo[2], lo[3]);
+            }
+            tmem_st32(tb + lane_off + vS + col, v);
+            tmem_wait_st();
+            if (part == 0) {
+                S.z[f] *= fac;
+                S.rho[f] = rh;
+            }
+        }
+        ok = fw_wait2(&S.bar_u, ph_u, S.abort, hdr, 71);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0) mma_out = false;
+        if (quad == 0 && part < 2) {
+            float w[32];
+            tmem_ld32(tb + lane_off + vUk + 32 * part, w);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(suk + lane * 64 + 32 * part + k) =
+                    make_float4(w[k], w[k + 1], w[k + 2], w[k + 3]);
+        }
+        // phi(q) of this thread's 16 u-values (features 16 part + k of both halves)
+        float php[16], phn[16];
+        {
+            float u[16];
+            tmem_ld8(tb + lane_off + vUq + 16 * part, u);
+            tmem_ld8(tb + lane_off + vUq + 16 * part + 8, u + 8);
+            tmem_wait_ld();
+            float mx = -INFINITY, mn = -INFINITY;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                mx = fmaxf(mx, u[k]);
+                mn = fmaxf(mn, -u[k]);
+            }
+            xa[part * 128 + row] = mx;
+            xb[part * 128 + row] = mn;
+            quad_sync(quad);
+            mx = fmaxf(fmaxf(xa[row], xa[128 + row]), fmaxf(xa[256 + row], xa[384 + row]));
+            mn = fmaxf(fmaxf(xb[row], xb[128 + row]), fmaxf(xb[256 + row], xb[384 + row]));
+            float sp = 0.0f, sn = 0.0f;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                php[k] = __expf(u[k] - mx);
+                phn[k] = __expf(-u[k] - mn);
+                sp += php[k];
+                sn += phn[k];
+            }
+            quad_sync(quad);
+            xa[part * 128 + row] = sp;
+            xb[part * 128 + row] = sn;
+            quad_sync(quad);
+            sp = (xa[row] + xa[128 + row]) + (xa[256 + row] + xa[384 + row]);
+            sn = (xb[row] + xb[128 + row]) + (xb[256 + row] + xb[384 + row]);
+            const float ip = 1.0f / sp, in = 1.0f / sn;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                php[k] *= ip;
+                phn[k] *= in;
+            }
+        }
+        __syncthreads();
+        // (4) phi of the delayed keys (fp32, 16 threads per key) and k^ = phi e^{rho - b_t}
+        //     (bf16, into R2: the query tile is consumed)
+        {
+            const int t = tid >> 4, sub = tid & 15;
+            const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
+            const float4 u4 = *reinterpret_cast<const float4*>(suk + t * 64 + 4 * sub);
+            const float u[4] = {u4.x, u4.y, u4.z, u4.w};
+            float mx = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
+            float mn = fminf(fminf(u[0], u[1]), fminf(u[2], u[3]));
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            }
+            float ep[4], en[4], sp = 0.0f, sn = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                ep[e] = __expf(u[e] - mx);
+                en[e] = __expf(mn - u[e]);
+                sp += ep[e];
+                sn += en[e];
+            }
+#pragma unroll
+            for (int o = 1; o < 16; o <<= 1) {
+                sp += __shfl_xor_sync(0xffffffffu, sp, o);
+                sn += __shfl_xor_sync(0xffffffffu, sn, o);
+            }
+            const float ip = dvalid ? 1.0f / sp : 0.0f, in = dvalid ? 1.0f / sn : 0.0f;
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb) {
+                const int f0 = 64 * kb + 4 * sub;
+                float ph[4], kh[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    ph[e] = kb == 0 ? ep[e] * ip : en[e] * in;
+                    kh[e] = ph[e] * __expf(clamp80f(S.rho[f0 + e] - btab[t * 128 + f0 + e]));
+                }
+                *reinterpret_cast<float4*>(pk + t * 128 + f0) = make_float4(ph[0], ph[1], ph[2], ph[3]);
+                const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + vR2 + off),
+                             "r"(pack_bf16(kh[0], kh[1])), "r"(pack_bf16(kh[2], kh[3]))
+                             : "memory");
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // (5) G = S' V_d^T (high + low); dv'^T = S'^T k^^T
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                const uint32_t kdoff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + vGc, dS1h + koff, dVk + kdoff, idesc_bf16(128, 32, false, false), j > 0);
+                mma_bf16(tb + vGc, dS1l + koff, dVk + kdoff, idesc_bf16(128, 32, false, false), 1);
+                mma_bf16(tb + vDV, dS1hm + ((j * 2048) >> 4), dKh + kdoff,
+                         idesc_bf16(128, 32, true, false), j > 0);
+            }
+            mma_commit(&S.bar_g);
+            mma_out = true;
+        }
+        // (6) q^ = phi(q) a e^{b_i - rho} (high, low) into R1 once S' is read; c (high, low)
+        const int ti = row >> 2;
+        const int64_t ridx = (b * p.L + t0 + ti) * p.Hq + kv * GQ + (row & 3);
+        const bool rv = ti < n;
+        const float ar = rv ? rows[ridx] : 0.0f, dl = rv ? rows[nrow + ridx] : 0.0f;
+        ok = fw_wait2(&S.bar_g, ph_g, S.abort, hdr, 72);
+        if (!ok) break;
+        tc_fence_after();
+        {
+            const int fp = 16 * part, fn = 64 + 16 * part;
+            uint32_t hp[8], lp[8], hn[8], ln[8];
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+                float qp[2], qn[2];
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int f1 = fp + k + h, f2 = fn + k + h;
+                    qp[h] = php[k + h] * ar * __expf(clamp80f(btab[ti * 128 + f1] - S.rho[f1]));
+                    qn[h] = phn[k + h] * ar * __expf(clamp80f(btab[ti * 128 + f2] - S.rho[f2]));
+                }
+                split2(qp[0], qp[1], hp[k / 2], lp[k / 2]);
+                split2(qn[0], qn[1], hn[k / 2], ln[k / 2]);
+            }
+            // [f half][128 rows][64 f]: features fp.. are half 0, chunks 2 part, 2 part + 1
+#pragma unroll
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const uint32_t o0 = h2 * 16384 + sw128(row, 2 * part),
+                               o1 = h2 * 16384 + sw128(row, 2 * part + 1);
+                const uint32_t* H = h2 == 0 ? hp : hn;
+                const uint32_t* Lw = h2 == 0 ? lp : ln;
+                st_shared_v4(base + vR1 + o0, H[0], H[1], H[2], H[3]);
+                st_shared_v4(base + vR1 + o1, H[4], H[5], H[6], H[7]);
+                st_shared_v4(base + vR1 + 32768 + o0, Lw[0], Lw[1], Lw[2], Lw[3]);
+                st_shared_v4(base + vR1 + 32768 + o1, Lw[4], Lw[5], Lw[6], Lw[7]);
+            }
+            // c_it = dy_i . v'_t - delta_i for delayed keys t <= i, stored key-major
+            float cv[8];
+            tmem_ld8(tb + lane_off + vC + 8 * part, cv);
+            tmem_wait_ld();
+            __nv_bfloat16* ch = (__nv_bfloat16*)(sm + vR2 + 8192);
+            __nv_bfloat16* cl = (__nv_bfloat16*)(sm + vR2 + 16384);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * part + e;
+                const bool valid = rv && t <= ti && (t0 + t - WIN >= 0);
+                const float x = valid ? cv[e] - dl : 0.0f;
+                const __nv_bfloat16 xh = __float2bfloat16_rn(x);
+                const uint32_t o = kt_off(t, row) / 2;
+                ch[o] = xh;
+                cl[o] = __float2bfloat16_rn(x - __bfloat162float(xh));
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // (7) A = q^ k^^T; G += q^^T c (three parts); S += q^^T dY (two parts)
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+                const uint32_t kdoff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + vA, dQhk + koff, dKh + kdoff, idesc_bf16(128, 32, false, false), j > 0);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t ro = (j * 2048) >> 4;
+                const uint32_t co = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+                mma_bf16(tb + vGc, dQhm + ro, dCh + co, idesc_bf16(128, 32, true, false), 1);
+                mma_bf16(tb + vGc, dQhm + ro, dCl + co, idesc_bf16(128, 32, true, false), 1);
+                mma_bf16(tb + vGc, dQlm + ro, dCh + co, idesc_bf16(128, 32, true, false), 1);
+                mma_bf16(tb + vS, dQhm + ro, dDm + ro, idesc_bf16(128, 128, true, true), 1);
+                mma_bf16(tb + vS, dQlm + ro, dDm + ro, idesc_bf16(128, 128, true, true), 1);
+            }
+            mma_commit(&S.bar_a);
+        }
+        // z <- z' - sum_rows q^ delta (from the bf16 parts the MMA reads)
+        {
+            const int f = tid & 127, gq2 = tid >> 7;
+            const __nv_bfloat16* qh = (const __nv_bfloat16*)(sm + vR1);
+            const __nv_bfloat16* ql = (const __nv_bfloat16*)(sm + vR1 + 32768);
+            float zsum = 0.0f;
+            for (int r = 32 * gq2; r < 32 * gq2 + 32; ++r) {
+                const uint32_t o = ((f >> 6) * 16384 + sw128(r, (f & 63) >> 3) + (f & 7) * 2) / 2;
+                const int tr = r >> 2;
+                const float d_r = tr < n ? rows[nrow + (b * p.L + t0 + tr) * p.Hq + kv * GQ + (r & 3)] : 0.0f;
+                zsum = fmaf(__bfloat162float(qh[o]) + __bfloat162float(ql[o]), d_r, zsum);
+            }
+            xa[gq2 * 128 + f] = zsum;
+        }
+        ok = fw_wait2(&S.bar_a, ph_a, S.abort, hdr, 73);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid < 128) {
+            const float zr = (xa[tid] + xa[128 + tid]) + (xa[256 + tid] + xa[384 + tid]);
+            xb[tid] = S.z[tid];  // z' for dphi(k')
+            S.z[tid] -= zr;
+        }
+        // (8) A^ (masked i >= t) key-major for dv' += dY^T A^
+        {
+            float av[8];
+            tmem_ld8(tb + lane_off + vA + 8 * part, av);
+            tmem_wait_ld();
+            __nv_bfloat16* ah = (__nv_bfloat16*)(sm + vR2 + 24576);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * part + e;
+                const bool valid = rv && t <= ti && (t0 + t - WIN >= 0);
+                ah[kt_off(t, row) / 2] = __float2bfloat16_rn(valid ? av[e] : 0.0f);
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                mma_bf16(tb + vDV, dDm + ((j * 2048) >> 4),
+                         dAh + ((((j >> 2) * 4096 + (j & 3) * 32)) >> 4),
+                         idesc_bf16(128, 32, true, false), 1);
+            mma_commit(&S.bar_v);
+        }
+        // (9) dphi(k') = e^{rho - b_t} (.) (G + z') for feature `row`, keys 8 part .. + 7;
+        //     phi(k')-side of dB with the reverse cumulative sum; du'
+        float dphi[8], phk[8];
+        {
+            const int f = row;
+            float gv[8];
+            tmem_ld8(tb + lane_off + vGc + 8 * part, gv);
+            tmem_wait_ld();
+            const float zp = xb[f];
+            float loc[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * part + e;
+                phk[e] = pk[t * 128 + f];
+                dphi[e] = __expf(clamp80f(S.rho[f] - btab[t * 128 + f])) * (gv[e] + zp);
+                loc[e] = t < n ? dB[((b * p.L + t0 + t) * p.Hkv + kv) * 128 + f] - phk[e] * dphi[e]
+                               : 0.0f;
+            }
+            // suffix sums inside the part (keys descending), then across parts
+            float suf[8];
+            float run = 0.0f;
+#pragma unroll
+            for (int e = 7; e >= 0; --e) {
+                run += loc[e];
+                suf[e] = run;
+            }
+            xa[part * 128 + f] = run;  // part totals [4][128]
+            __syncthreads();
+            float cin = S.carry[f];
+            for (int p2 = 3; p2 > part; --p2) cin += xa[p2 * 128 + f];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * part + e;
+                if (t < n) dB[((b * p.L + t0 + t) * p.Hkv + kv) * 128 + f] = cin + suf[e];
+            }
+            __syncthreads();
+            if (part == 0)
+                S.carry[f] += (xa[f] + xa[128 + f]) + (xa[256 + f] + xa[384 + f]);
+            // feature-map backward: per key, S_half = sum over the half of phi dphi
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                float x = phk[e] * dphi[e];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+                if (lane == 0) tn[2048 + quad * 32 + 8 * part + e] = x;  // [4 quads][32 keys]
+            }
+            __syncthreads();
+        }
+        {
+            const int f = row;
+            const int h = quad >> 1;  // 0: softmax(+u) half, 1: softmax(-u) half
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * part + e;
+                const float Sh = tn[2048 + (2 * h) * 32 + t] + tn[2048 + (2 * h + 1) * 32 + t];
+                const float term = phk[e] * (dphi[e] - Sh);
+                if (h == 1) tn[(f - 64) * 32 + t] = term;
+                else dphi[e] = term;  // quads 0, 1 keep the + term
+            }
+            __syncthreads();
+            if (h == 0) {
+                __nv_bfloat16* du = (__nv_bfloat16*)(sm + vDU);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int t = 8 * part + e;
+                    const float v = dphi[e] - tn[f * 32 + t];
+                    du[(sw128(t, f >> 3) + (f & 7) * 2) / 2] = __float2bfloat16_rn(v);
+                }
+            }
+        }
+        fence_async_smem();
+        tc_fence_before();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after();
+            // (10) dk'^T = Wf du'^T; dWf += k'^T du'
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                mma_bf16(tb + vDK, dWk + ((j * 32) >> 4), dDUk + ((j * 32) >> 4),
+                         idesc_bf16(128, 32, false, false), j > 0);
+#pragma unroll
+            for (int j = 0; j < 2; ++j)
+                mma_bf16(tb + vDW, dKm + ((j * 2048) >> 4), dDUm + ((j * 2048) >> 4),
+                         idesc_bf16(128, 64, true, true), (dw_init || j > 0) ? 1u : 0u);
+            mma_commit(&S.bar_k);
+        }
+        dw_init = true;
+        ok = fw_wait2(&S.bar_v, ph_v, S.abort, hdr, 74);
+        if (!ok) break;
+        ok = fw_wait2(&S.bar_k, ph_k, S.abort, hdr, 75);
+        if (!ok) break;
+        tc_fence_after();
+        if (tid == 0) {
+            mma_out = false;
+            if (more) {
+                // every tile of this step is consumed: the previous step's copies start
+                mbar_arrive_expect_tx(&S.bar_tma, kStepBytes);
+                load_delayed(sm + vK, &tmK, &S.bar_tma, kv, c - 1, b);
+                load_delayed(sm + vV, &tmV, &S.bar_tma, kv, c - 1, b);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb) {
+                    tma_load_4d(sm + vR2 + kb * 16384, &tmQ, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                                (int)((c - 1) * CT), (int)b);
+                    tma_load_4d(sm + vR3 + kb * 16384, &tmDY, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                                (int)((c - 1) * CT), (int)b);
+                }
+                tma_load_4d(sm + vG, &tmG, &S.bar_tma, 0, (int)kv, (int)((c - 1) * CT), (int)b);
+                tma_out = true;
+            }
+        }
+        // (11) dk, dv of the delayed keys (lane = d, keys 8 part .. + 7)
+        {
+            float kv8[8], vv8[8];
+            tmem_ld8(tb + lane_off + vDK + 8 * part, kv8);
+            tmem_ld8(tb + lane_off + vDV + 8 * part, vv8);
+            tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int t = 8 * part + e;
+                const int64_t j = t0 + t - WIN;
+                if (t < n && j >= 0) {
+                    const int64_t o = ((b * p.L + j) * p.Hkv + kv) * DH + row;
+                    ((__nv_bfloat16*)a.dk)[o] = __float2bfloat16_rn(kv8[e]);
+                    ((__nv_bfloat16*)a.dv)[o] = __float2bfloat16_rn(vv8[e]);
+                }
+            }
+        }
+        if (tid < 128) S.rho_next[tid] = S.rho[tid];
+        tc_fence_before();
+        __syncthreads();
+    }
+
+    if (ok) {
+        float v[16];
+        tmem_ld8(tb + lane_off + vDW + 16 * part, v);
+        tmem_ld8(tb + lane_off + vDW + 16 * part + 8, v + 8);
+        tmem_wait_ld();
+        float* dst = dWp + ((size_t)(p.Pmax + seg) * (size_t)U + (size_t)unit) * (size_t)(DH * 64) +
+                     row * 64 + 16 * part;
+#pragma unroll
+        for (int k = 0; k < 16; k += 4)
+            *reinterpret_cast<float4*>(dst + k) =
+                dw_init ? make_float4(v[k], v[k + 1], v[k + 2], v[k + 3])
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (tid < 128) totp[((size_t)seg * (size_t)U + (size_t)unit) * 128 + tid] = S.carry[tid];
+    } else if (tid == 0) {
+        if (mma_out) {
+            mma_commit(&S.bar_fin);
+            mbar_wait(&S.bar_fin, 0, kTimeout);
+        }
+        if (tma_out) mbar_wait(&S.bar_tma, ph_tma, kTimeout);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+        tc_fence_after();
+        tmem_dealloc(tb, 512);
+    }
+}
+
 }  // namespace
 
 bool bwd_win_tc_supported(const Plan& p) {
@@ -1453,6 +2084,47 @@ cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, siz
     bwd_fwalk_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemFW, s>>>(
         mq, md, mk, mv, mw, mg, p, a, wsf + o_rows, wsf + o_fwd, wsf + o_dB, wsf + o_dW,
         wsf + o_dt);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_bwd_rwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
+                                size_t o_rev, size_t o_dB, size_t o_dW, size_t o_tot,
+                                cudaStream_t s) {
+    alignas(64) CUtensorMap mq, md, mk, mv, mw, mg;
+    const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
+                     Hkv = (cuuint64_t)p.Hkv;
+    {
+        const cuuint64_t dims[4] = {DH, Hq, L, B};
+        const cuuint64_t str[3] = {DH * 2, Hq * DH * 2, L * Hq * DH * 2};
+        const cuuint32_t box[4] = {64, GQ, CT, 1};
+        if (!tc::make_map(&mq, a.q, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!tc::make_map(&md, a.dy, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {DH, Hkv, L, B};
+        const cuuint64_t str[3] = {DH * 2, Hkv * DH * 2, L * Hkv * DH * 2};
+        const cuuint32_t box[4] = {64, 1, CT, 1};
+        if (!tc::make_map(&mk, a.k, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!tc::make_map(&mv, a.v, 4, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[4] = {128, Hkv, L, B};
+        const cuuint64_t str[3] = {128 * 2, Hkv * 128 * 2, L * Hkv * 128 * 2};
+        const cuuint32_t box[4] = {128, 1, CT, 1};
+        if (!tc::make_map(&mg, a.g, 4, dims, str, box, false)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {64, DH, Hkv};
+        const cuuint64_t str[2] = {64 * 2, DH * 64 * 2};
+        const cuuint32_t box[3] = {64, DH, 1};
+        if (!tc::make_map(&mw, a.Wf, 3, dims, str, box)) return cudaErrorInvalidValue;
+    }
+    cudaError_t e = cudaFuncSetAttribute(bwd_rwalk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)kSmemRW);
+    if (e != cudaSuccess) return e;
+    bwd_rwalk_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemRW, s>>>(
+        mq, md, mk, mv, mw, mg, p, a, wsf + o_rows, wsf + o_rev, wsf + o_dB, wsf + o_dW,
+        wsf + o_tot);
     return cudaGetLastError();
 }
 

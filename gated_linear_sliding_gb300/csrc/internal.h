@@ -85,6 +85,11 @@ struct BwdArgs {
 size_t bwd_workspace_bytes(const Plan& p);
 bool bwd_win_tc_supported(const Plan& p);
 bool bwd_rev_local_tc_supported(const Plan& p);
+// Reverse-direction walk of the backward on the tensor cores (state parts of dk, dv,
+// phi(k')-side of dB with its reverse cumulative sum, dWf and segment totals).
+cudaError_t launch_bwd_rwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
+                                size_t o_rev, size_t o_dB, size_t o_dW, size_t o_tot,
+                                cudaStream_t s);
 // Forward-direction walk of the backward on the tensor cores (state part of dq, phi(q)-side of
 // dB, dWf and dt partials); offsets are in floats from the workspace start.
 cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
