@@ -205,7 +205,19 @@ __global__ void bwd_row_table(Plan p, BwdArgs a, BwdWs ws) {
     const T* yr = (const T*)a.y + r * DH;
     const T* dr = (const T*)a.dy + r * DH;
     float dl = 0.0f;
-    for (int c = lane; c < DH; c += 32) dl = fmaf(ld(yr + c), ld(dr + c), dl);
+    if constexpr (sizeof(T) == 2 && DH == 128) {
+        // four bf16 per lane in one 8-byte load
+        const uint2 yv = reinterpret_cast<const uint2*>(yr)[lane];
+        const uint2 dv = reinterpret_cast<const uint2*>(dr)[lane];
+        const uint32_t yw[2] = {yv.x, yv.y}, dw[2] = {dv.x, dv.y};
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            dl = fmaf(__uint_as_float(yw[k] << 16), __uint_as_float(dw[k] << 16), dl);
+            dl = fmaf(__uint_as_float(yw[k] & 0xFFFF0000u), __uint_as_float(dw[k] & 0xFFFF0000u), dl);
+        }
+    } else {
+        for (int c = lane; c < DH; c += 32) dl = fmaf(ld(yr + c), ld(dr + c), dl);
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
     if (lane == 0) {
@@ -544,16 +556,26 @@ __global__ void bwd_reverse_scan(Plan p, float* rec0) {
     if (e >= nE) return;
     const int64_t f = e < p.D * p.d ? e / p.d : e - p.D * p.d;
     const int64_t U = p.B * p.Hkv;
+    // records are read eight at a time before any is overwritten (one round trip per group)
+    constexpr int KG = 8;
     float carry = 0.0f;
-    for (int64_t s = p.P - 1; s >= 0; --s) {
-        float* rec = rec0 + ((size_t)s * U + unit) * p.rec_floats;
-        float dH = 0.0f, lam = 0.0f;
-        if (s >= 1) {
-            dH = rec[e];
-            lam = rec[p.D * p.d + p.D + f];
+    for (int64_t s0 = p.P - 1; s0 >= 0; s0 -= KG) {
+        float dH[KG], lam[KG];
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+            const int64_t sg = s0 - k;
+            const float* rec = rec0 + ((size_t)(sg >= 0 ? sg : 0) * U + unit) * p.rec_floats;
+            dH[k] = sg >= 1 ? rec[e] : 0.0f;
+            lam[k] = sg >= 1 ? rec[p.D * p.d + p.D + f] : 0.0f;
         }
-        rec[e] = carry;
-        carry = expf(lam) * carry + dH;
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+            const int64_t sg = s0 - k;
+            if (sg >= 0) {
+                rec0[((size_t)sg * U + unit) * p.rec_floats + e] = carry;
+                carry = expf(lam[k]) * carry + dH[k];
+            }
+        }
     }
 }
 
@@ -865,10 +887,24 @@ __global__ void bwd_gates(Plan p, BwdArgs a, BwdWs ws) {
     const int64_t seg = i / p.seg_len;
     const int64_t U = p.B * p.Hkv, unit = b * p.Hkv + kv;
     const float* wsf = (const float*)a.ws;
-    float s = wsf[ws.dB + e];
-    for (int64_t sg = seg + 1; sg < p.P; ++sg) s += wsf[ws.tot + ((size_t)sg * U + unit) * p.D + f];
+    // tot holds, per segment, the sum of dB over all later segments (bwd_tot_suffix)
+    const float s = wsf[ws.dB + e] + wsf[ws.tot + ((size_t)seg * U + unit) * p.D + f];
     const float gam = sigmoidf_(ld((const T*)a.g + e));
     st((T*)a.dg + e, s * (1.0f - gam));
+}
+
+// Segment totals of dB -> exclusive suffix sums over the segments (later segments first).
+__global__ void bwd_tot_suffix(Plan p, float* tot) {
+    const int64_t U = p.B * p.Hkv;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // unit * D + f
+    if (e >= U * p.D) return;
+    float run = 0.0f;
+    for (int64_t sg = p.P - 1; sg >= 0; --sg) {
+        float* x = tot + (size_t)sg * U * p.D + e;
+        const float t = *x;
+        *x = run;
+        run += t;
+    }
 }
 
 // dWf[kv] = sum over batch, segments and both walks (fixed order); dsinks likewise.
@@ -978,6 +1014,7 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     }
     // 6. dg, then the reductions
     const int64_t ng = p.B * p.L * p.Hkv * p.D;
+    bwd_tot_suffix<<<(unsigned)((U * p.D + 255) / 256), 256, 0, s>>>(p, wsf + ws.tot);
     bwd_gates<T><<<(unsigned)((ng + 255) / 256), 256, 0, s>>>(p, a, ws);
     const int64_t nr = max64(p.Hkv * p.d * (p.D / 2), p.Hq * p.M);
     bwd_reduce<<<(unsigned)((nr + 255) / 256), 256, 0, s>>>(p, a, ws);
