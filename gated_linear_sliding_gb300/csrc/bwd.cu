@@ -877,20 +877,28 @@ __global__ void __launch_bounds__(NT) bwd_window_keys(Plan p, BwdArgs a, BwdWs w
 // later segments add their totals.
 template <typename T>
 __global__ void bwd_gates(Plan p, BwdArgs a, BwdWs ws) {
-    const int64_t total = p.B * p.L * p.Hkv * p.D;
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= total) return;
-    const int64_t f = e % p.D;
-    const int64_t kv = (e / p.D) % p.Hkv;
-    const int64_t i = (e / (p.D * p.Hkv)) % p.L;
-    const int64_t b = e / (p.D * p.Hkv * p.L);
+    // eight consecutive features of one (batch, token, KV head) row per thread
+    const int64_t total8 = p.B * p.L * p.Hkv * p.D / 8;
+    const int64_t e8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e8 >= total8) return;
+    const int64_t e = e8 * 8;
+    const int64_t rowi = e / p.D;                   // (b L + i) Hkv + kv
+    const int f0 = (int)(e - rowi * p.D);
+    const int64_t kv = rowi % p.Hkv, bi = rowi / p.Hkv;
+    const int64_t i = bi % p.L, b = bi / p.L;
     const int64_t seg = i / p.seg_len;
     const int64_t U = p.B * p.Hkv, unit = b * p.Hkv + kv;
     const float* wsf = (const float*)a.ws;
     // tot holds, per segment, the sum of dB over all later segments (bwd_tot_suffix)
-    const float s = wsf[ws.dB + e] + wsf[ws.tot + ((size_t)seg * U + unit) * p.D + f];
-    const float gam = sigmoidf_(ld((const T*)a.g + e));
-    st((T*)a.dg + e, s * (1.0f - gam));
+    const float* tot = wsf + ws.tot + ((size_t)seg * U + unit) * p.D + f0;
+    const float4 d0 = *reinterpret_cast<const float4*>(wsf + ws.dB + e);
+    const float4 d1 = *reinterpret_cast<const float4*>(wsf + ws.dB + e + 4);
+    const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float gam = sigmoidf_(ld((const T*)a.g + e + k));
+        st((T*)a.dg + e + k, (dv[k] + tot[k]) * (1.0f - gam));
+    }
 }
 
 // Segment totals of dB -> exclusive suffix sums over the segments (later segments first).
@@ -1015,7 +1023,7 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     // 6. dg, then the reductions
     const int64_t ng = p.B * p.L * p.Hkv * p.D;
     bwd_tot_suffix<<<(unsigned)((U * p.D + 255) / 256), 256, 0, s>>>(p, wsf + ws.tot);
-    bwd_gates<T><<<(unsigned)((ng + 255) / 256), 256, 0, s>>>(p, a, ws);
+    bwd_gates<T><<<(unsigned)((ng / 8 + 255) / 256), 256, 0, s>>>(p, a, ws);
     const int64_t nr = max64(p.Hkv * p.d * (p.D / 2), p.Hq * p.M);
     bwd_reduce<<<(unsigned)((nr + 255) / 256), 256, 0, s>>>(p, a, ws);
     return cudaGetLastError();

@@ -495,9 +495,9 @@ __global__ void __launch_bounds__(NT, 1)
 // weighted feature rows q^ = phi(q) e^{b} a form the A operand (features are the MMA rows)
 // of dH += q^^T dY.
 constexpr uint32_t rQ = 0, rD = 32768, rQh = 65536, rW = 98304, rG = 114688,
-                   rE = rG + 8192;                 // e^{b_t} bf16 [32][EPR]
-constexpr int EPR = 136;                           // padded row pitch of the decay table
-constexpr uint32_t rX = rE + 32 * EPR * 2;         // exchanges [4][128] x 4, -delta [128]
+                   rE = rG + 8192;                 // e^{b_t} fp32 [32][EPR]
+constexpr int EPR = 132;                           // padded row pitch (floats) of the decay table
+constexpr uint32_t rX = rE + 32 * EPR * 4;         // exchanges [4][128] x 4, -delta [128]
 constexpr uint32_t rBars = rX + 9216;
 struct RSmall {
     uint64_t bar_q, bar_d, bar_g, bar_u, bar_h, bar_fin;
@@ -505,7 +505,9 @@ struct RSmall {
     volatile int abort;
     float dz[128], el[128];
 };
-constexpr uint32_t kSmemRev = rBars + (uint32_t)sizeof(RSmall) + 1024;
+constexpr uint32_t rQl = 151552;                    // low bf16 part of q^ (same layout)
+static_assert(rBars + sizeof(RSmall) <= rQl, "reverse-pass layout");
+constexpr uint32_t kSmemRev = rQl + 32768 + 1024;
 static_assert(kSmemRev <= 232448, "shared memory budget");
 
 __device__ __forceinline__ bool rev_wait(uint64_t* bar, uint32_t& ph, RSmall& S, WsHeader* hdr,
@@ -611,7 +613,8 @@ __global__ void __launch_bounds__(NT, 1)
     tc_fence_before();
     __syncthreads();
     const uint64_t dQ = kdesc(base + rQ), dW = mndesc(base + rW, 16384);
-    const uint64_t dQh = mndesc(base + rQh, 16384), dD = mndesc(base + rD, 16384);
+    const uint64_t dQh = mndesc(base + rQh, 16384), dD = mndesc(base + rD, 16384),
+                   dQl = mndesc(base + rQl, 16384);
     uint32_t ph_q = 0, ph_d = 0, ph_g = 0, ph_u = 0, ph_h = 0;
     float lam_tot = 0.0f;
     bool ok = true;
@@ -654,10 +657,11 @@ __global__ void __launch_bounds__(NT, 1)
             const float g0 = gpart[gf], g1 = gpart[128 + gf], g2 = gpart[256 + gf],
                         g3 = gpart[384 + gf];
             const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? g0 + g1 : (g0 + g1) + g2;
-            __nv_bfloat16* Eb = (__nv_bfloat16*)(sm + rE);
+            // kept in fp32: the adjoint records feed the gate gradient, a difference of two
+            // nearly equal sums that bf16 weights would not cancel consistently
+            float* Eb = (float*)(sm + rE);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                Eb[(8 * gq + j) * EPR + gf] = __float2bfloat16_rn(ex2f((bt[j] + off) * kLog2e));
+            for (int j = 0; j < 8; ++j) Eb[(8 * gq + j) * EPR + gf] = ex2f((bt[j] + off) * kLog2e);
             if (gq == 0) {
                 const float blast = (g0 + g1) + (g2 + g3);
                 S.el[gf] = ex2f(blast * kLog2e);
@@ -732,15 +736,18 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 const int f0 = 32 * part + 8 * ch;
-                uint32_t w0, w1, w2, w3;
-                ld_shared_v4(base + rE + (uint32_t)(t * EPR + f0) * 2u, w0, w1, w2, w3);
-                float eb[8], qh[8];
-                unpack8(w0, w1, w2, w3, eb);
+                const float4* ep = reinterpret_cast<const float4*>(sm + rE + (size_t)(t * EPR + f0) * 4u);
+                const float4 e0 = ep[0], e1 = ep[1];
+                const float eb[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+                float qh[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) qh[e] = uv[8 * ch + e] * sc * eb[e];
-                st_shared_v4(base + rQh + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
-                             pack_bf16(qh[0], qh[1]), pack_bf16(qh[2], qh[3]),
-                             pack_bf16(qh[4], qh[5]), pack_bf16(qh[6], qh[7]));
+                uint32_t hi[4], lo[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split2(qh[2 * e], qh[2 * e + 1], hi[e], lo[e]);
+                const uint32_t o = (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch);
+                st_shared_v4(base + rQh + o, hi[0], hi[1], hi[2], hi[3]);
+                st_shared_v4(base + rQl + o, lo[0], lo[1], lo[2], lo[3]);
             }
         }
         fence_async_smem();
@@ -756,9 +763,12 @@ __global__ void __launch_bounds__(NT, 1)
                 d_out = false;
                 tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < 8; ++j) {
                     mma_bf16(tb + cH, dQh + ((j * 2048) >> 4), dD + ((j * 2048) >> 4),
                              idesc_bf16(128, 128, true, true), 1);
+                    mma_bf16(tb + cH, dQl + ((j * 2048) >> 4), dD + ((j * 2048) >> 4),
+                             idesc_bf16(128, 128, true, true), 1);
+                }
                 mma_commit(&S.bar_h);
                 mma_out = true;
             }
@@ -767,10 +777,11 @@ __global__ void __launch_bounds__(NT, 1)
             // dz_f += sum_rows q^[row][f] (-delta_row), from the bf16 tile the MMA reads
             const int f = tid & 127, gq = tid >> 7;
             const __nv_bfloat16* qh = (const __nv_bfloat16*)(sm + rQh);
+            const __nv_bfloat16* ql = (const __nv_bfloat16*)(sm + rQl);
             float zs = 0.0f;
             for (int r = 32 * gq; r < 32 * gq + 32; ++r) {
-                const uint32_t off = (f >> 6) * 16384 + sw128(r, (f & 63) >> 3) + (f & 7) * 2;
-                zs = fmaf(__bfloat162float(qh[off / 2]), zq[512 + r], zs);
+                const uint32_t off = ((f >> 6) * 16384 + sw128(r, (f & 63) >> 3) + (f & 7) * 2) / 2;
+                zs = fmaf(__bfloat162float(qh[off]) + __bfloat162float(ql[off]), zq[512 + r], zs);
             }
             zq[gq * 128 + f] = zs;
         }
@@ -873,12 +884,6 @@ __device__ __forceinline__ bool fw_wait(uint64_t* bar, uint32_t& ph, WSmall& S, 
 
 __device__ __forceinline__ float clamp80f(float x) { return fminf(fmaxf(x, -80.0f), 80.0f); }
 
-// Split x into a bf16 high part and the bf16 rounding of the remainder.
-__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-    float h0 = x0, h1 = x1;
-    hi = round_pair(h0, h1);
-    lo = pack_bf16(x0 - h0, x1 - h1);
-}
 
 // Delayed keys or values of chunk c (two 64-column halves of 32 rows, 4 KB apart).
 __device__ __forceinline__ void load_delayed(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar,
@@ -974,7 +979,7 @@ __global__ void __launch_bounds__(NT, 1)
     const uint64_t dWm = mndesc(base + wW, 16384), dVm = mndesc(base + wV, 4096),
                    dKih = mndesc(base + wKih, 4096), dKil = mndesc(base + wKil, 4096),
                    dKum = mndesc(base + wKu, 4096), dQm = mndesc(base + wQ, 16384),
-                   dDUm = mndesc(base + wKih, 16384);
+                   dDUm = mndesc(base + wKih, 16384), dKulm = mndesc(base + wD, 4096);
     uint32_t ph_tma = 0, ph_u = 0, ph_d1 = 0, ph_d2 = 0, ph_q = 0;
     bool ok = true, dw_init = false;
     float dts_acc = 0.0f;
@@ -1125,6 +1130,8 @@ __global__ void __launch_bounds__(NT, 1)
         }
         __syncthreads();
         // (6) phi of the delayed keys -> k~i = phi e^{r - b_t} (high, low), k~u = k~i e^{b_31 - r}
+        //     (high now; the low part goes into the dY tile once D and C have read it)
+        uint32_t kul[2][2];
         {
             const int t = tid >> 4, sub = tid & 15;
             const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
@@ -1171,8 +1178,11 @@ __global__ void __launch_bounds__(NT, 1)
                 asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + wKil + off), "r"(l0),
                              "r"(l1)
                              : "memory");
-                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + wKu + off),
-                             "r"(pack_bf16(ku[0], ku[1])), "r"(pack_bf16(ku[2], ku[3]))
+                uint32_t uh0, uh1;
+                split2(ku[0], ku[1], uh0, kul[kb][0]);
+                split2(ku[2], ku[3], uh1, kul[kb][1]);
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + wKu + off), "r"(uh0),
+                             "r"(uh1)
                              : "memory");
             }
         }
@@ -1182,17 +1192,6 @@ __global__ void __launch_bounds__(NT, 1)
             // the gate tile and the staged U_k rows are consumed
             tma_load_4d(sm + wG, &tmG, &S.bar_tma, 0, (int)kv, (int)((c + 1) * CT), (int)b);
         }
-        // z <- e^{b_31} z + sum_t k~u_t
-        if (tid < 128) {
-            const int f = tid;
-            float zsum = 0.0f;
-            const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + wKu);
-            for (int t = 0; t < CT; ++t) {
-                const uint32_t off = (f >> 6) * 4096 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
-                zsum += __bfloat162float(ku[off / 2]);
-            }
-            S.z[f] = fmaf(S.cf[f] * S.zs[f], 1.0f, zsum);
-        }
         // (7) c_it = C_it - delta_i for delayed keys t <= i (8 keys per part), high and low
         const int ti = row >> 2;
         const int64_t ridx = (b * p.L + t0 + ti) * p.Hq + kv * GQ + (row & 3);
@@ -1201,12 +1200,16 @@ __global__ void __launch_bounds__(NT, 1)
         ok = fw_wait(&S.bar_d1, ph_d1, S, hdr, 62);
         if (!ok) break;
         tc_fence_after();
-        if (tid == 0 && more) {
-            // dY is consumed
+        {
+            // low part of k~u into the consumed dY tile (same layout as the high part)
+            const int t = tid >> 4, sub = tid & 15;
 #pragma unroll
-            for (int kb = 0; kb < 2; ++kb)
-                tma_load_4d(sm + wD + kb * 16384, &tmDY, &S.bar_tma, 64 * kb, (int)(kv * GQ),
-                            (int)((c + 1) * CT), (int)b);
+            for (int kb = 0; kb < 2; ++kb) {
+                const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
+                asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + wD + off),
+                             "r"(kul[kb][0]), "r"(kul[kb][1])
+                             : "memory");
+            }
         }
         {
             float cv[8];
@@ -1228,6 +1231,7 @@ __global__ void __launch_bounds__(NT, 1)
             tmem_st4(tb + lane_off + fCl + 4 * part, cl);
             tmem_wait_st();
         }
+        fence_async_smem();
         tc_fence_before();
         __syncthreads();
         if (tid == 0) {
@@ -1241,17 +1245,36 @@ __global__ void __launch_bounds__(NT, 1)
                 mma_bf16_ts(tb + fD, tb + fCl + 8 * j, dKih + bo, idesc_bf16(128, 128, false, true), 1);
             }
 #pragma unroll
-            for (int j = 0; j < 2; ++j)
+            for (int j = 0; j < 2; ++j) {
                 mma_bf16(tb + fH, dKum + ((j * 2048) >> 4), dVm + ((j * 2048) >> 4),
                          idesc_bf16(128, 128, true, true), 1);
+                mma_bf16(tb + fH, dKulm + ((j * 2048) >> 4), dVm + ((j * 2048) >> 4),
+                         idesc_bf16(128, 128, true, true), 1);
+            }
             mma_commit(&S.bar_d2);
+        }
+        // z <- e^{b_31} z + sum_t k~u_t (high + low parts the MMA reads)
+        if (tid < 128) {
+            const int f = tid;
+            float zsum = 0.0f;
+            const __nv_bfloat16* kuh = (const __nv_bfloat16*)(sm + wKu);
+            const __nv_bfloat16* kul2 = (const __nv_bfloat16*)(sm + wD);
+            for (int t = 0; t < CT; ++t) {
+                const uint32_t off = ((f >> 6) * 4096 + sw128(t, (f & 63) >> 3) + (f & 7) * 2) / 2;
+                zsum += __bfloat162float(kuh[off]) + __bfloat162float(kul2[off]);
+            }
+            S.z[f] = fmaf(S.cf[f] * S.zs[f], 1.0f, zsum);
         }
         ok = fw_wait(&S.bar_d2, ph_d2, S, hdr, 63);
         if (!ok) break;
         tc_fence_after();
         if (tid == 0 && more) {
-            // the delayed values are consumed
+            // the delayed values, dY and the low part of k~u are consumed
             load_delayed(sm + wV, &tmV, &S.bar_tma, kv, c + 1, b);
+#pragma unroll
+            for (int kb = 0; kb < 2; ++kb)
+                tma_load_4d(sm + wD + kb * 16384, &tmDY, &S.bar_tma, 64 * kb, (int)(kv * GQ),
+                            (int)((c + 1) * CT), (int)b);
         }
         // (9) dphi(q), the phi(q)-side of dB, du
         {
@@ -1432,7 +1455,7 @@ struct VSmall {
     uint64_t bar_tma, bar_u, bar_g, bar_a, bar_v, bar_k, bar_fin;
     uint32_t tmem;
     volatile int abort;
-    float z[128], rho_next[128], carry[128], rho[128];
+    float z[128], rho_next[128], carry[128], rho[128], dlr[128];
 };
 constexpr uint32_t kSmemRW = vSm + (uint32_t)sizeof(VSmall) + 1024;
 static_assert(kSmemRW <= 232448, "shared memory budget");
@@ -1480,7 +1503,7 @@ __global__ void __launch_bounds__(NT, 1)
     VSmall& S = *reinterpret_cast<VSmall*>(sm + vSm);
     float* xa = reinterpret_cast<float*>(sm + vX);    // [4][128]
     float* xb = xa + 512;                             // [4][128]
-    float* tn = xb + 512;                             // [64 f][32 keys]
+    float* tn = xb + 512;                             // [32 keys][64 f]
     static_assert(vX + 4 * (512 + 512 + 2048 + 128) <= vSm, "exchange area");
     float* suk = reinterpret_cast<float*>(sm + vG);   // staged U_k rows [32][64]
     float* btab = reinterpret_cast<float*>(sm + vB);  // cumulative log-gates [32][128]
@@ -1761,6 +1784,7 @@ __global__ void __launch_bounds__(NT, 1)
         const int64_t ridx = (b * p.L + t0 + ti) * p.Hq + kv * GQ + (row & 3);
         const bool rv = ti < n;
         const float ar = rv ? rows[ridx] : 0.0f, dl = rv ? rows[nrow + ridx] : 0.0f;
+        if (part == 0) S.dlr[row] = dl;  // delta per row for the z column sums
         ok = fw_wait2(&S.bar_g, ph_g, S.abort, hdr, 72);
         if (!ok) break;
         tc_fence_after();
@@ -1840,9 +1864,7 @@ __global__ void __launch_bounds__(NT, 1)
             float zsum = 0.0f;
             for (int r = 32 * gq2; r < 32 * gq2 + 32; ++r) {
                 const uint32_t o = ((f >> 6) * 16384 + sw128(r, (f & 63) >> 3) + (f & 7) * 2) / 2;
-                const int tr = r >> 2;
-                const float d_r = tr < n ? rows[nrow + (b * p.L + t0 + tr) * p.Hq + kv * GQ + (r & 3)] : 0.0f;
-                zsum = fmaf(__bfloat162float(qh[o]) + __bfloat162float(ql[o]), d_r, zsum);
+                zsum = fmaf(__bfloat162float(qh[o]) + __bfloat162float(ql[o]), S.dlr[r], zsum);
             }
             xa[gq2 * 128 + f] = zsum;
         }
@@ -1935,7 +1957,7 @@ __global__ void __launch_bounds__(NT, 1)
                 const int t = 8 * part + e;
                 const float Sh = tn[2048 + (2 * h) * 32 + t] + tn[2048 + (2 * h + 1) * 32 + t];
                 const float term = phk[e] * (dphi[e] - Sh);
-                if (h == 1) tn[(f - 64) * 32 + t] = term;
+                if (h == 1) tn[t * 64 + (f - 64)] = term;
                 else dphi[e] = term;  // quads 0, 1 keep the + term
             }
             __syncthreads();
@@ -1944,7 +1966,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int t = 8 * part + e;
-                    const float v = dphi[e] - tn[f * 32 + t];
+                    const float v = dphi[e] - tn[t * 64 + f];
                     du[(sw128(t, f >> 3) + (f & 7) * 2) / 2] = __float2bfloat16_rn(v);
                 }
             }

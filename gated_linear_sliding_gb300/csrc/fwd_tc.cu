@@ -808,9 +808,10 @@ constexpr uint32_t lV = 32768;     // delayed values, same layout, read MN-major
 constexpr uint32_t lG = 65536;     // gate logits [128 tokens][128 features] bf16
 constexpr uint32_t lW = 98304;     // Wf, MN-major B
 constexpr uint32_t lKu = 114688;   // k~ = phi(k) e^{b_end - b_t}, [2 halves][128 tokens][64 f]
-constexpr uint32_t lE = 147456;    // e^{b_end - b_t} bf16 [128 tokens][EKR] (padded rows)
-constexpr int EKR = DF + 8;        // row pitch of lE: rows land in distinct bank groups
-constexpr uint32_t lX = lE + 128 * EKR * 2;  // exchanges: u-extreme, u-sum, gate and z quarters
+constexpr uint32_t lE = 147456;    // e^{b_end - b_t} fp32 [128 tokens][EKR] (padded rows)
+constexpr int EKR = DF + 4;        // row pitch (floats) of lE: rows land in distinct bank groups
+constexpr uint32_t lKul = lE;      // low bf16 part of k~ (layout of lKu), over lE once it is read
+constexpr uint32_t lX = lE + 128 * EKR * 4;  // exchanges: u-extreme, u-sum, gate and z quarters
 constexpr uint32_t lSmall = lX + 8192;
 
 struct LSmall {
@@ -819,7 +820,8 @@ struct LSmall {
     volatile int abort;
     float z[DF], el[DF];
 };
-constexpr uint32_t kLocalSmem = lSmall + (uint32_t)sizeof(LSmall) + 1024;
+static_assert(lKul % 1024 == 0 && 32768 <= 128 * EKR * 4, "segment-pass layout");
+constexpr uint32_t kLocalSmem = lSmall + sizeof(LSmall) + 1024;
 static_assert(kLocalSmem <= 232448, "shared memory budget");
 constexpr int NL = 512;  // threads of the segment pass
 
@@ -899,7 +901,7 @@ __global__ void __launch_bounds__(NL, 1)
     const uint32_t cHl = 0, cUl = 128;  // TMEM: H [0,128), U_k [128,192)
     const uint64_t dK = kdesc(base + lK);
     const uint64_t dW = mndesc(base + lW, 16384), dV = mndesc(base + lV, 16384),
-                   dKu = mndesc(base + lKu, 16384);
+                   dKu = mndesc(base + lKu, 16384), dKul = mndesc(base + lKul, 16384);
     {
         float v[32];
 #pragma unroll
@@ -970,10 +972,11 @@ __global__ void __launch_bounds__(NL, 1)
             const float blast = (g0 + g1) + (g2 + g3);
             const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? g0 + g1 : (g0 + g1) + g2;
             const float cst = (blast - off) * kLog2e;
-            __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + lE);
+            // kept in fp32: the state records feed the gate gradient, a difference of two
+            // nearly equal sums that bf16 weights would not cancel consistently
+            float* Ek = (float*)(sm + lE);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
-                Ek[(32 * gq + j) * EKR + gf] = __float2bfloat16_rn(ex2f(fmaf(-bt[j], kLog2e, cst)));
+            for (int j = 0; j < 32; ++j) Ek[(32 * gq + j) * EKR + gf] = ex2f(fmaf(-bt[j], kLog2e, cst));
             if (gq == 0) {
                 S.el[gf] = ex2f(blast * kLog2e);
                 lam_tot += blast;
@@ -1037,18 +1040,30 @@ __global__ void __launch_bounds__(NL, 1)
             quad_sync(quad);
             const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
             const float inv = dvalid ? 1.0f / (xus[part * 128 + t] + xus[sib * 128 + t]) : 0.0f;
+            // high and low bf16 parts: the state these records start segments from must carry
+            // fp32-like precision (the backward differentiates through it); the low parts go
+            // over the decay table once every thread has read its rows of it
+            uint32_t lo[16];
 #pragma unroll
             for (int ch = 0; ch < 4; ++ch) {
                 const int f0 = 32 * part + 8 * ch;
-                uint32_t w0, w1, w2, w3;
-                ld_shared_v4(base + lE + (uint32_t)(t * EKR + f0) * 2u, w0, w1, w2, w3);
-                float ek[8], kv8[8];
-                unpack8(w0, w1, w2, w3, ek);
+                const float4* ep = reinterpret_cast<const float4*>(sm + lE + (size_t)(t * EKR + f0) * 4u);
+                const float4 e0 = ep[0], e1 = ep[1];
+                const float ek[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+                float kv8[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) kv8[e] = uv[8 * ch + e] * inv * ek[e];
-                st_shared_v4(base + lKu + (part >> 1) * 16384 + sw128(t, 4 * (part & 1) + ch),
-                             pack_bf16(kv8[0], kv8[1]), pack_bf16(kv8[2], kv8[3]),
-                             pack_bf16(kv8[4], kv8[5]), pack_bf16(kv8[6], kv8[7]));
+                uint32_t hi[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) split2(kv8[2 * e], kv8[2 * e + 1], hi[e], lo[4 * ch + e]);
+                const uint32_t o = (part >> 1) * 16384 + sw128(t, 4 * (part & 1) + ch);
+                st_shared_v4(base + lKu + o, hi[0], hi[1], hi[2], hi[3]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) {
+                const uint32_t o = (part >> 1) * 16384 + sw128(t, 4 * (part & 1) + ch);
+                st_shared_v4(base + lKul + o, lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
             }
         }
         fence_async_smem();
@@ -1064,9 +1079,12 @@ __global__ void __launch_bounds__(NL, 1)
                 v_out = false;
                 tc_fence_after();
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
+                for (int j = 0; j < 8; ++j) {
                     mma_bf16(tb + cHl, dKu + ((j * 2048) >> 4), dV + ((j * 2048) >> 4),
                              idesc_bf16(128, 128, true, true), 1);
+                    mma_bf16(tb + cHl, dKul + ((j * 2048) >> 4), dV + ((j * 2048) >> 4),
+                             idesc_bf16(128, 128, true, true), 1);
+                }
                 mma_commit(&S.bar_h);
                 mma_out = true;
             }
@@ -1075,10 +1093,11 @@ __global__ void __launch_bounds__(NL, 1)
             // z <- e^{b_last} z + sum_t k~_t, from the bf16 tile the MMA reads
             const int f = tid & (DF - 1), gq = tid >> 7;
             const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + lKu);
+            const __nv_bfloat16* kul = (const __nv_bfloat16*)(sm + lKul);
             float zs = 0.0f;
             for (int t = 32 * gq; t < 32 * gq + 32; ++t) {
-                const uint32_t off = (f >> 6) * 16384 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
-                zs += __bfloat162float(ku[off / 2]);
+                const uint32_t off = ((f >> 6) * 16384 + sw128(t, (f & 63) >> 3) + (f & 7) * 2) / 2;
+                zs += __bfloat162float(ku[off]) + __bfloat162float(kul[off]);
             }
             zq[gq * DF + f] = zs;
         }

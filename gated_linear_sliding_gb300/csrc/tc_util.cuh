@@ -30,6 +30,14 @@ __device__ __forceinline__ uint32_t round_pair(float& lo, float& hi) {
     return w;
 }
 
+// Split a pair into bf16 high parts and the bf16 rounding of the remainders (packed, lo
+// element in the low half): hi + lo carries about 16 bits of mantissa.
+__device__ __forceinline__ void split2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+    float h0 = x0, h1 = x1;
+    hi = round_pair(h0, h1);
+    lo = sm100::pack_bf16(x0 - h0, x1 - h1);
+}
+
 __device__ __forceinline__ void unpack8(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
                                         float* o) {
     const uint32_t w[4] = {w0, w1, w2, w3};

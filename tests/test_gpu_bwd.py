@@ -111,3 +111,21 @@ def test_bwd_deterministic(lz):
     b = gpu_fwd_bwd(lz, inp, wl)
     for n in a:
         np.testing.assert_array_equal(a[n], b[n], err_msg=n)
+
+
+def test_bwd_ragged_length_tensor_core_path(lz, oracle_mod):
+    """L = 1000 is not a multiple of the 32-token steps: the last step of the tensor-core
+    walks and window kernels is partial, and the sequence is cut into several segments."""
+    wl = I.MISTRAL_7B_TRAIN
+    inp = I.make_inputs(wl, L=1000, B=1, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16")
+
+
+def test_bwd_strong_decay_gates(lz, oracle_mod):
+    """Gates drawn from the long-context stress mixture (30 % strongly decaying): the decay
+    references and clamps of the tensor-core walks see cumulative log-gates far below zero."""
+    wl = I.STRESS_L64K
+    inp = I.make_inputs(wl, L=700, B=1, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16")
