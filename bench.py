@@ -373,7 +373,7 @@ def run_ours(args, rank, world, device):
                                        "parallelism": "replicas" if world > 1 else "1 GPU"}),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "traffic": traffic,
-                     "kernel": ("fwd_tc_kernel<main> (tcgen05 chunk walk)" if path == 1
+                     "kernel": ("fwd_tc_kernel (tcgen05 chunk walk)" if path == 1
                                 else "fwd_simt_main (SIMT chunk walk)"),
                      "kernel_ms": kern_ms,
                      "algorithmic_bytes": alg_bytes, "peak_source": peak_src,

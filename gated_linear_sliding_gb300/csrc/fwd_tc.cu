@@ -24,10 +24,11 @@
 //   O_i   = q~_i (e^{r} (.) H) + P_win V_ring + [q~ k~^T (.) causal] V_delayed
 //   H    <- e^{b_31} (.) H + (phi(k_{t-w}) e^{b_31 - b_t})^T V_delayed
 //   y_i   = O_i / (sum P_win + sum P_intra + q~_i.(e^{r} z) + sum_m e^{t_m - m_i})
-// Every gate factor is e^{difference of cumulative log-gates}; relative to the
-// sub-chunk midpoint r each factor stays within the log-decay of 16 tokens, so no
-// factor leaves the fp32/bf16 range unless 16 consecutive gates decay by more than
-// e^-80 (exponents are clamped to +-80 there).
+// Every gate factor is e^{difference of cumulative log-gates}, formed as a running product of
+// Gamma = sigmoid(g) or 1/Gamma = 1 + e^{-g} over the tokens in between; relative to the
+// sub-chunk midpoint r each factor stays within the decay of 16 tokens, so no factor leaves
+// the fp32/bf16 range unless 16 consecutive gates decay by more than e^-80 (factors are
+// clamped to [e^-80, e^80] there).
 //
 // TMEM columns: H [0,128)  scores S [128,256) (intra scores A reuse [128,160))
 //               U_q [256,320)  U_k [320,384) (then P_win, bf16 pairs)  O [384,512).
@@ -81,10 +82,11 @@ struct Small {
     uint32_t tmem;
     volatile int abort;
     float z[DF], zs[DF], cf[DF];
-    float gpart[4][DF];            // per-quarter gate sums of each feature
+    float gpart[4][DF];            // per-quarter products of Gamma (later: z partial sums)
+    float gipart[4][DF];           // per-quarter products of 1/Gamma
     float ps[4][128], pg[4][128];  // per-part window and state denominators of each row
-    float tmax[GQ];
-    float sinks[GQ][MMAX];
+    float tmax[GQ];                // max(t_m) log2(e) per head (at least the minimum shift)
+    float sexp[GQ];                // sum_m 2^{t_m log2(e) - tmax} per head
 };
 constexpr uint32_t kSmemBytes = oSmall + (uint32_t)sizeof(Small) + 1024;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -96,7 +98,12 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 // step's projections can run while the epilogue still reads O.
 constexpr uint32_t cH = 0, cS = 128, cA = 128, cUq = 256, cUk = 320, cPw = 320, cO = 384;
 
-__device__ __forceinline__ float clamp80(float x) { return fminf(fmaxf(x, -80.0f), 80.0f); }
+constexpr float kE80 = 5.5406223843935100e34f;   // e^80
+constexpr float kEm80 = 1.8048513878454153e-35f;  // e^-80
+
+// Decay tables [32 tokens][128 features] bf16: the 16-byte chunks of token t's row are
+// XOR-swizzled by t, so rows read by neighbouring tokens fall in different banks.
+__device__ __forceinline__ int eidx(int t, int f) { return t * DF + (((f >> 3) ^ (t & 7)) << 3) + (f & 7); }
 
 // log sigmoid(x) = min(x, 0) - log(1 + e^{-|x|}); the argument of the log is in (1, 2].
 __device__ __forceinline__ float log_sigmoid_fast(float x) {
@@ -161,14 +168,10 @@ __device__ __forceinline__ bool ctl_wait(uint64_t* bar, uint32_t& ph, Small& S, 
 }
 
 // Bytes one step's copies bring: key and value slots, the gate tile (and the query tile).
-template <bool MAIN>
-constexpr uint32_t step_bytes() {
-    return MAIN ? 16384u + 8192u + 32768u : 16384u + 8192u;
-}
+constexpr uint32_t kStepBytes = 16384u + 8192u + 32768u;
 
 // Key/value slot of chunk c (and its query tile), on a barrier phase that expects `expect`
 // bytes in all (the gate tile follows separately).
-template <bool MAIN>
 __device__ __forceinline__ void issue_kvq_loads(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmQ,
                                                 const CUtensorMap* tmK, const CUtensorMap* tmV,
                                                 int64_t c, int64_t kv, int64_t b, uint32_t expect) {
@@ -179,8 +182,7 @@ __device__ __forceinline__ void issue_kvq_loads(uint8_t* sm, uint64_t* bar, cons
     for (int kb = 0; kb < 2; ++kb) {
         sm100::tma_load_4d(sm + oK + kb * 16384 + slot * 4096, tmK, bar, 64 * kb, (int)kv, t0, (int)b);
         sm100::tma_load_4d(sm + oV + kb * 16384 + slot * 4096, tmV, bar, 64 * kb, (int)kv, t0, (int)b);
-        if (MAIN)
-            sm100::tma_load_4d(sm + oQ + kb * 16384, tmQ, bar, 64 * kb, (int)(kv * 4), t0, (int)b);
+        sm100::tma_load_4d(sm + oQ + kb * 16384, tmQ, bar, 64 * kb, (int)(kv * 4), t0, (int)b);
     }
 }
 
@@ -193,7 +195,6 @@ __device__ __forceinline__ void issue_gate_load(uint8_t* sm, uint64_t* bar, cons
 // hands each result to the math warps through an mbarrier.  The next step's query tile and
 // ring slot are loaded as soon as this step's projections have read theirs, its gate tile
 // once the delayed keys' feature map has consumed the staged U_k rows.
-template <bool MAIN>
 __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_t tb, Small& S,
                                              WsHeader* hdr, const CUtensorMap* tmQ,
                                              const CUtensorMap* tmK, const CUtensorMap* tmV,
@@ -209,8 +210,8 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
     if (c_begin < c_end) {
         // the first step's operands, Wf and the two chunks before the segment (zero-filled
         // before the sequence start), all on one phase
-        issue_kvq_loads<MAIN>(sm, &S.bar_tma, tmQ, tmK, tmV, c_begin, kv, b,
-                              step_bytes<MAIN>() + 16384u + 2u * 16384u);
+        issue_kvq_loads(sm, &S.bar_tma, tmQ, tmK, tmV, c_begin, kv, b,
+                        kStepBytes + 16384u + 2u * 16384u);
         issue_gate_load(sm, &S.bar_tma, tmG, c_begin, kv, b);
         tma_load_3d(sm + oW, tmW, &S.bar_tma, 0, 0, (int)kv);
         for (int64_t cc = c_begin - 2; cc < c_begin; ++cc) {
@@ -238,17 +239,15 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
             const uint32_t koff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
             const uint64_t bw = dW + ((j * 2048) >> 4);
             mma_bf16(tb + cUk, dK + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
-            if (MAIN) {
-                mma_bf16(tb + cUq, dQ + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
-                mma_bf16(tb + cS, dQ + koff, dK + koff, idesc_bf16(128, 128, false, false), j > 0);
-            }
+            mma_bf16(tb + cUq, dQ + koff, bw, idesc_bf16(128, 64, false, true), j > 0);
+            mma_bf16(tb + cS, dQ + koff, dK + koff, idesc_bf16(128, 128, false, false), j > 0);
         }
         mma_commit(&S.bar_u);
         mma_out = true;
         if (!ctl_wait(&S.bar_u, ph_u, S, hdr, 9)) break;
         // the query tile and the ring slot of chunk c-3 are free: next step's copies start
         if (more) {
-            issue_kvq_loads<MAIN>(sm, &S.bar_tma, tmQ, tmK, tmV, c + 1, kv, b, step_bytes<MAIN>());
+            issue_kvq_loads(sm, &S.bar_tma, tmQ, tmK, tmV, c + 1, kv, b, kStepBytes);
             tma_out = true;
             gate_due = c + 1;
         }
@@ -259,40 +258,39 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
             gate_due = -1;
         }
         const uint64_t dVd = dV + ((slot_d * 4096) >> 4);
-        if (MAIN) {
-            // intra-step scores A = q~ k~^T
+        // intra-step scores A = q~ k~^T
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t qoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
-                const uint32_t koff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
-                mma_bf16(tb + cA, dQt + qoff, dKi + koff, idesc_bf16(128, 32, false, false), j > 0);
-            }
-            mma_commit(&S.bar_a);
-            if (!ctl_wait(&S.bar_p, ph_p, S, hdr, 7)) break;
-            tc_fence_after();
-            // O = q~ H_s + P_win V_ring + P_intra V_delayed
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
-                mma_bf16(tb + cO, dQt + aoff, dHs + ((j * 2048) >> 4),
-                         idesc_bf16(128, 128, false, true), j > 0);
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                if ((j >> 1) == slot_x) continue;  // P_win is zero there; the slot is reloading
-                mma_bf16_ts(tb + cO, tb + cPw + 8 * j, dV + ((j * 2048) >> 4),
-                            idesc_bf16(128, 128, false, true), 1);
-            }
-#pragma unroll
-            for (int j = 0; j < 2; ++j)
-                mma_bf16(tb + cO, dE + ((j * 32) >> 4), dVd + ((j * 2048) >> 4),
-                         idesc_bf16(128, 128, false, true), 1);
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t qoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+            const uint32_t koff = ((j >> 2) * 4096 + (j & 3) * 32) >> 4;
+            mma_bf16(tb + cA, dQt + qoff, dKi + koff, idesc_bf16(128, 32, false, false), j > 0);
         }
-        // H += k~u^T V_delayed
+        mma_commit(&S.bar_a);
+        // the parts of O that do not wait for P_intra: q~ H_s + P_win V_ring, and the state
+        // update H += k~u^T V_delayed, run while the math warps mask A
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t aoff = ((j >> 2) * 16384 + (j & 3) * 32) >> 4;
+            mma_bf16(tb + cO, dQt + aoff, dHs + ((j * 2048) >> 4), idesc_bf16(128, 128, false, true),
+                     j > 0);
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if ((j >> 1) == slot_x) continue;  // P_win is zero there; the slot is reloading
+            mma_bf16_ts(tb + cO, tb + cPw + 8 * j, dV + ((j * 2048) >> 4),
+                        idesc_bf16(128, 128, false, true), 1);
+        }
 #pragma unroll
         for (int j = 0; j < 2; ++j)
             mma_bf16(tb + cH, dKu + ((j * 2048) >> 4), dVd + ((j * 2048) >> 4),
                      idesc_bf16(128, 128, true, true), 1);
+        if (!ctl_wait(&S.bar_p, ph_p, S, hdr, 7)) break;
+        tc_fence_after();
+        // O += P_intra V_delayed
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+            mma_bf16(tb + cO, dE + ((j * 32) >> 4), dVd + ((j * 2048) >> 4),
+                     idesc_bf16(128, 128, false, true), 1);
         mma_commit(&S.bar_o);
         if (!ctl_wait(&S.bar_o, ph_o, S, hdr, 8)) break;
         mma_out = false;
@@ -310,7 +308,6 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
     }
 }
 
-template <bool MAIN>
 __global__ void __launch_bounds__(NT, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmW,
@@ -359,50 +356,64 @@ __global__ void __launch_bounds__(NT, 1)
         prefetch_tmap(&tmV);
         prefetch_tmap(&tmW);
         prefetch_tmap(&tmG);
-        if (MAIN) {
-            prefetch_tmap(&tmQ);
-            prefetch_tmap(&tmY);
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmY);
+    }
+    if (tid < GQ) {
+        const float* t = a.sinks + (kv * GQ + tid) * p.M;
+        float tm = kMinShift;
+        for (int mm = 0; mm < p.M; ++mm) tm = fmaxf(tm, t[mm]);
+        float se = 0.0f;
+        for (int mm = 0; mm < p.M; ++mm) se += ex2f((t[mm] - tm) * kLog2e);
+        S.tmax[tid] = tm * kLog2e;
+        S.sexp[tid] = se;
+    }
+    // The starting state passes through shared memory (the rings' bytes, zeroed afterwards):
+    // coalesced 16-byte loads, and each row's 16-byte chunks XOR-swizzled by the row so the
+    // per-row reads below are free of bank conflicts.
+    const float* rec =
+        seg > 0 ? a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats : nullptr;
+    if (rec != nullptr) {
+        for (int e = tid; e < DF * DH / 4; e += NT) {
+            const int r = e >> 5, c = e & 31;
+            *reinterpret_cast<float4*>(sm + oK + r * 512 + ((c & ~7) | ((c ^ r) & 7)) * 16) =
+                reinterpret_cast<const float4*>(rec)[e];
         }
     }
-    if (MAIN) {
-        for (int e = tid; e < GQ * MMAX; e += NT) {
-            const int hh = e / MMAX, mm = e % MMAX;
-            S.sinks[hh][mm] = mm < p.M ? a.sinks[(kv * GQ + hh) * p.M + mm] : 0.0f;
-        }
-        if (tid < GQ) {
-            float tm = kMinShift;
-            for (int mm = 0; mm < p.M; ++mm) tm = fmaxf(tm, a.sinks[(kv * GQ + tid) * p.M + mm]);
-            S.tmax[tid] = tm * kLog2e;
-        }
-    }
-    // zero both rings: P_win is 0 on masked keys, but 0 times non-finite stale bits is NaN
-    for (int e = tid; e < 65536 / 16; e += NT) st_shared_v4(base + oK + e * 16, 0u, 0u, 0u, 0u);
-    fence_async_smem();
-    const float* rec = (MAIN && seg > 0)
-                           ? a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats
-                           : nullptr;
     if (tid < DF) S.z[tid] = rec ? rec[DF * DH + tid] : 0.0f;
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = S.tmem;
+    if (warp < NW) {
+        // starting state H into TMEM (fp32 master copy), lane = feature f, column = d
+        float v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int c = 8 * part + j;
+            const float4 x = rec ? *reinterpret_cast<const float4*>(
+                                       sm + oK + row * 512 + ((c & ~7) | ((c ^ row) & 7)) * 16)
+                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            v[4 * j] = x.x;
+            v[4 * j + 1] = x.y;
+            v[4 * j + 2] = x.z;
+            v[4 * j + 3] = x.w;
+        }
+        tmem_st32(tb + lane_off + cH + 32 * part, v);
+        tmem_wait_st();
+    }
+    __syncthreads();
+    // zero both rings: P_win is 0 on masked keys, but 0 times non-finite stale bits is NaN
+    for (int e = tid; e < 65536 / 16; e += NT) st_shared_v4(base + oK + e * 16, 0u, 0u, 0u, 0u);
+    fence_async_smem();
+    __syncthreads();
 
     if (warp == NW) {
         if (lane == 0)
-            control_loop<MAIN>(sm, base, tb, S, hdr, &tmQ, &tmK, &tmV, &tmW, &tmG, c_begin, c_end,
+            control_loop(sm, base, tb, S, hdr, &tmQ, &tmK, &tmV, &tmW, &tmG, c_begin, c_end,
                                kv, b);
         __syncwarp();
     } else {
-        // starting state H into TMEM (fp32 master copy), lane = feature f, column = d
-        {
-            float v[32];
-            const int col = 32 * part;
-#pragma unroll
-            for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + col + k] : 0.0f;
-            tmem_st32(tb + lane_off + cH + col, v);
-            tmem_wait_st();
-        }
         uint32_t ph_tma = 0, ph_u = 0, ph_a = 0, ph_o = 0;
-        float lam_tot = 0.0f;
         bool ok = true;
 
         for (int64_t c = c_begin; c < c_end; ++c) {
@@ -415,44 +426,56 @@ __global__ void __launch_bounds__(NT, 1)
             ok = math_wait(&S.bar_tma, ph_tma, S, hdr, 2);
             if (!ok) break;
 
-            // (2) gates: cumulative log-sigmoid per feature; four threads per feature, one per
-            //     8-token quarter; the reference r = b_15 is the first two quarters' total
+            // (2) gates: four threads per feature, one per 8-token quarter.  Every decay factor
+            //     of the step relative to r = b_15 is a running product of Gamma = sigmoid(g) or
+            //     of 1/Gamma = 1 + e^{-g} over the tokens between (no logarithm), clamped to
+            //     [e^-80, e^80] as the exponents are
             const int gf = tid & (DF - 1), gq = tid >> 7;
-            float bt[CT / 4];
+            float ig[CT / 4];  // 1/Gamma of the thread's tokens (Gamma itself is rcp of it)
             {
                 const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + oG);
-                float run = 0.0f;
+                float pig = 1.0f;
 #pragma unroll
                 for (int t = 0; t < CT / 4; ++t) {
                     const int tt = (CT / 4) * gq + t;
-                    const float lam =
-                        tt < n ? log_sigmoid_fast(__bfloat162float(sg[tt * DF + gf])) : 0.0f;
-                    run += lam;
-                    bt[t] = run;
+                    const float x = __bfloat162float(sg[tt * DF + gf]);
+                    ig[t] = tt < n ? 1.0f + ex2f(-x * kLog2e) : 1.0f;  // past the end: Gamma = 1
+                    pig *= ig[t];
                 }
-                S.gpart[gq][gf] = run;
+                S.gpart[gq][gf] = rcpf(pig);
+                S.gipart[gq][gf] = pig;
             }
-            // the previous step's y tile has left the q~ buffer before anyone writes q~ again
-            if (MAIN && tid == 0) bulk_wait_read();
             math_sync();
             {
-                const float g0 = S.gpart[0][gf], g1 = S.gpart[1][gf], g2 = S.gpart[2][gf],
-                            g3 = S.gpart[3][gf];
-                const float bref = g0 + g1, blast = bref + g2 + g3;
-                const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? bref : bref + g2;
                 __nv_bfloat16* Eq = (__nv_bfloat16*)(sm + oE);
                 __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + oE + 8192);
+                if (gq < 2) {
+                    // t < 16: Eq = prod_{s=t+1..15} 1/Gamma_s, Ek = prod_{s=t+1..15} Gamma_s
+                    float sq = gq == 0 ? S.gipart[1][gf] : 1.0f, sk = gq == 0 ? S.gpart[1][gf] : 1.0f;
 #pragma unroll
-                for (int t = 0; t < CT / 4; ++t) {
-                    const int tt = (CT / 4) * gq + t;
-                    const float btt = bt[t] + off;
-                    if (MAIN) Eq[tt * DF + gf] = __float2bfloat16_rn(__expf(clamp80(btt - bref)));
-                    Ek[tt * DF + gf] = __float2bfloat16_rn(__expf(clamp80(bref - btt)));
+                    for (int t = CT / 4 - 1; t >= 0; --t) {
+                        const int tt = (CT / 4) * gq + t;
+                        Eq[eidx(tt, gf)] = __float2bfloat16_rn(fminf(sq, kE80));
+                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(fmaxf(sk, kEm80));
+                        sq *= ig[t];
+                        sk *= rcpf(ig[t]);
+                    }
+                } else {
+                    // t >= 16: Eq = prod_{s=16..t} Gamma_s, Ek = prod_{s=16..t} 1/Gamma_s
+                    float pq = gq == 3 ? S.gpart[2][gf] : 1.0f, pk = gq == 3 ? S.gipart[2][gf] : 1.0f;
+#pragma unroll
+                    for (int t = 0; t < CT / 4; ++t) {
+                        const int tt = (CT / 4) * gq + t;
+                        pq *= rcpf(ig[t]);
+                        pk *= ig[t];
+                        Eq[eidx(tt, gf)] = __float2bfloat16_rn(fmaxf(pq, kEm80));
+                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(fminf(pk, kE80));
+                    }
                 }
                 if (gq == 0) {
-                    S.cf[gf] = __expf(blast - bref);
-                    S.zs[gf] = __expf(bref) * S.z[gf];
-                    lam_tot += blast;
+                    const float g0 = S.gpart[0][gf], g1 = S.gpart[1][gf];
+                    S.cf[gf] = S.gpart[2][gf] * S.gpart[3][gf];  // e^{b_31 - r}
+                    S.zs[gf] = (g0 * g1) * S.z[gf];               // e^{r} z
                 }
             }
 
@@ -460,29 +483,29 @@ __global__ void __launch_bounds__(NT, 1)
             //     decayed by e^{b_31} (TMEM columns no MMA in flight touches)
             {
                 const int f = row;
-                const float g0 = S.gpart[0][f], g1 = S.gpart[1][f], g2 = S.gpart[2][f],
-                            g3 = S.gpart[3][f];
-                const float er = __expf(g0 + g1), el = __expf(g0 + g1 + g2 + g3);
+                const float er = S.gpart[0][f] * S.gpart[1][f];
+                const float el = er * (S.gpart[2][f] * S.gpart[3][f]);
                 const int col = 32 * part;
                 float v[32];
                 tmem_ld32(tb + lane_off + cH + col, v);
                 tmem_wait_ld();
-                if (MAIN) {
 #pragma unroll
-                    for (int ch = 0; ch < 4; ++ch) {
-                        const int nchunk = (col & 63) / 8 + ch;
-                        st_shared_v4(base + oHs + (col / 64) * 16384 + sw128(f, nchunk),
-                                     pack_bf16(er * v[8 * ch], er * v[8 * ch + 1]),
-                                     pack_bf16(er * v[8 * ch + 2], er * v[8 * ch + 3]),
-                                     pack_bf16(er * v[8 * ch + 4], er * v[8 * ch + 5]),
-                                     pack_bf16(er * v[8 * ch + 6], er * v[8 * ch + 7]));
-                    }
+                for (int ch = 0; ch < 4; ++ch) {
+                    const int nchunk = (col & 63) / 8 + ch;
+                    st_shared_v4(base + oHs + (col / 64) * 16384 + sw128(f, nchunk),
+                                 pack_bf16(er * v[8 * ch], er * v[8 * ch + 1]),
+                                 pack_bf16(er * v[8 * ch + 2], er * v[8 * ch + 3]),
+                                 pack_bf16(er * v[8 * ch + 4], er * v[8 * ch + 5]),
+                                 pack_bf16(er * v[8 * ch + 6], er * v[8 * ch + 7]));
                 }
 #pragma unroll
                 for (int k = 0; k < 32; ++k) v[k] *= el;
                 tmem_st32(tb + lane_off + cH + col, v);
                 tmem_wait_st();
             }
+            // the previous step's y tile has left the q~ buffer before anyone writes q~ again
+            // (the barrier of the wait below orders this before the q~ writes of phase (4))
+            if (tid == 0) bulk_wait_read();
             ok = math_wait(&S.bar_u, ph_u, S, hdr, 3);
             if (!ok) break;
             tc_fence_after();
@@ -502,7 +525,7 @@ __global__ void __launch_bounds__(NT, 1)
                     *reinterpret_cast<float4*>(suk + lane * 64 + 32 * part + k) =
                         make_float4(w[k], w[k + 1], w[k + 2], w[k + 3]);
             }
-            if (MAIN) {
+            {
                 // keys of ring slot `part` are tokens 32 (c - age) + u; the slot that is three
                 // steps old, and slots before the sequence start, hold no key of the window
                 const int age = (int)((c - part) & 3);
@@ -597,7 +620,7 @@ __global__ void __launch_bounds__(NT, 1)
                 for (int ch = 0; ch < 4; ++ch) {
                     const int f0 = 32 * part + 8 * ch;
                     uint32_t w0, w1, w2, w3;
-                    ld_shared_v4(base + oE + (uint32_t)(i * DF + f0) * 2u, w0, w1, w2, w3);
+                    ld_shared_v4(base + oE + (uint32_t)eidx(i, f0) * 2u, w0, w1, w2, w3);
                     float eq[8], qv8[8];
                     unpack8(w0, w1, w2, w3, eq);
                     const float4 za = *reinterpret_cast<const float4*>(&S.zs[f0]);
@@ -652,19 +675,24 @@ __global__ void __launch_bounds__(NT, 1)
                     sn += __shfl_xor_sync(0xffffffffu, sn, o);
                 }
                 const float ip = dvalid ? 1.0f / sp : 0.0f, in = dvalid ? 1.0f / sn : 0.0f;
-                const __nv_bfloat16* Ek = (const __nv_bfloat16*)(sm + oE + 8192);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb) {
                     const int f0 = 64 * kb + 4 * sub;  // features f0..f0+3 (kb 0: softmax(u), 1: -u)
+                    // the four decay factors are 8 contiguous bytes of the swizzled table
+                    const uint2 e2 = *reinterpret_cast<const uint2*>(sm + oE + 8192 + eidx(t, f0) * 2);
+                    const float ek[4] = {__uint_as_float(e2.x << 16), __uint_as_float(e2.x & 0xffff0000u),
+                                         __uint_as_float(e2.y << 16), __uint_as_float(e2.y & 0xffff0000u)};
+                    const float4 cf4 = *reinterpret_cast<const float4*>(&S.cf[f0]);
+                    const float cf[4] = {cf4.x, cf4.y, cf4.z, cf4.w};
                     float ki[4], ku[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float ph = kb == 0 ? ep[e] * ip : en[e] * in;
-                        ki[e] = ph * __bfloat162float(Ek[t * DF + f0 + e]);
-                        ku[e] = ki[e] * S.cf[f0 + e];
+                        ki[e] = ph * ek[e];
+                        ku[e] = ki[e] * cf[e];
                     }
                     const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
-                    if (MAIN) {
+                    {
                         const uint32_t a0 = pack_bf16(ki[0], ki[1]), a1 = pack_bf16(ki[2], ki[3]);
                         asm volatile("st.shared.v2.b32 [%0], {%1, %2};" ::"r"(base + oKi + off),
                                      "r"(a0), "r"(a1)
@@ -681,22 +709,32 @@ __global__ void __launch_bounds__(NT, 1)
             math_sync();
             if (tid == 0) mbar_arrive(&S.bar_q);
 
-            // z <- e^{b_31} z + sum_t k~u_t (read back from the bf16 tile the MMA uses)
-            if (tid < DF) {
-                const int f = tid;
+            // z <- e^{b_31} z + sum_t k~u_t (read back from the bf16 tile the MMA uses): four
+            // threads per feature sum 8 tokens each into the quarter slots phase (3) has read
+            {
+                const int f = tid & (DF - 1), zq = tid >> 7;
                 float zsum = 0.0f;
                 const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + oKu);
-                for (int t = 0; t < CT; ++t) {
+#pragma unroll
+                for (int t = 8 * zq; t < 8 * zq + 8; ++t) {
                     const uint32_t off = (f >> 6) * 4096 + sw128(t, (f & 63) >> 3) + (f & 7) * 2;
                     zsum += __bfloat162float(ku[off / 2]);
                 }
-                S.z[f] = fmaf(S.cf[f] * S.zs[f], 1.0f, zsum);  // e^{b_31} z = e^{b_31-r} e^{r} z
+                S.gpart[zq][f] = zsum;
             }
+            // the parts of this row's shared normaliser known before P_intra: window, state
+            // and sink terms (while the intra-score MMA runs)
+            const float den0 = (S.ps[0][row] + S.ps[1][row]) + (S.ps[2][row] + S.ps[3][row]) +
+                               (S.pg[0][row] + S.pg[1][row]) + (S.pg[2][row] + S.pg[3][row]) +
+                               ex2f(S.tmax[hh] - m2) * S.sexp[hh];  // sum_m e^{t_m - m}
             float inv = 0.0f;
-            if (MAIN) {
+            {
                 ok = math_wait(&S.bar_a, ph_a, S, hdr, 4);
                 if (!ok) break;
                 tc_fence_after();
+                if (tid < DF)  // e^{b_31} z = e^{b_31 - r} e^{r} z
+                    S.z[tid] = fmaf(S.cf[tid], S.zs[tid],
+                                    (S.gpart[0][tid] + S.gpart[1][tid]) + (S.gpart[2][tid] + S.gpart[3][tid]));
                 // (6) P_intra: columns t in [8 part, 8 part + 8)
                 float av[8];
                 tmem_ld8(tb + lane_off + cA + 8 * part, av);
@@ -719,13 +757,7 @@ __global__ void __launch_bounds__(NT, 1)
                 if (tid == 0) mbar_arrive(&S.bar_p);
                 // the shared normaliser of this row, while the output MMAs run
                 if (qv) {
-                    float ssum = 0.0f;
-                    for (int mm = 0; mm < p.M; ++mm)
-                        ssum += ex2f(fmaf(S.sinks[hh][mm], kLog2e, -m2));
-                    const float den = (S.ps[0][row] + S.ps[1][row]) + (S.ps[2][row] + S.ps[3][row]) +
-                                      (S.pg[0][row] + S.pg[1][row]) + (S.pg[2][row] + S.pg[3][row]) +
-                                      (spi[row] + spi[128 + row]) + (spi[256 + row] + spi[384 + row]) +
-                                      ssum;
+                    const float den = den0 + ((spi[row] + spi[128 + row]) + (spi[256 + row] + spi[384 + row]));
                     inv = 1.0f / den;
                     if (part == 0 && a.lse != nullptr)
                         a.lse[(b * p.L + qa) * p.Hq + kv * GQ + hh] = m2 * kLn2 + __logf(den);
@@ -737,7 +769,7 @@ __global__ void __launch_bounds__(NT, 1)
 
             // (7) epilogue: y = O / den over columns [32 part, 32 part + 32) into the y tile
             //     (q~'s buffer, free once the output MMAs are done), then one TMA store
-            if (MAIN) {
+            {
                 float ov[32];
                 const int col = 32 * part;
                 tmem_ld32(tb + lane_off + cO + col, ov);
@@ -759,22 +791,13 @@ __global__ void __launch_bounds__(NT, 1)
                 }
             }
         }
-        if (MAIN && tid == 0) bulk_wait_all();
+        if (tid == 0) bulk_wait_all();
 
-        if (ok) {
-            // final state of the segment: the local record (segment pass) or the decode hand-off
-            float* dstH = nullptr;
-            float* dstz = nullptr;
-            if (!MAIN) {
-                float* r = a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats;
-                dstH = r;
-                dstz = r + DF * DH;
-                if (tid < DF) r[DF * DH + DF + tid] = lam_tot;
-            } else if (a.S_out != nullptr && s1 == p.L) {
-                dstH = a.S_out + unit * DF * DH;
-                dstz = a.z_out + unit * DF;
-            }
-            if (dstH != nullptr) {
+        if (ok && a.S_out != nullptr && s1 == p.L) {
+            // final state of the last segment: the decode hand-off
+            float* dstH = a.S_out + unit * DF * DH;
+            float* dstz = a.z_out + unit * DF;
+            {
                 float v[32];
                 const int col = 32 * part;
                 tmem_ld32(tb + lane_off + cH + col, v);
@@ -1231,7 +1254,7 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
         if (!make_map(&mw, a.Wf, 3, dims, str, box)) return cudaErrorInvalidValue;
     }
     cudaError_t e;
-    e = cudaFuncSetAttribute(fwd_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const unsigned U = (unsigned)(p.B * p.Hkv);
@@ -1240,7 +1263,7 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     if (a.ev_before) cudaEventRecord(a.ev_before, s);
-    fwd_tc_kernel<true><<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, my, p,
+    fwd_tc_kernel<<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, my, p,
                                                                         a);
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
     return cudaGetLastError();

@@ -22,6 +22,13 @@ __device__ __forceinline__ float ex2f(float x) {
     return y;
 }
 
+// 1/x on the special-function unit (1/inf gives +0)
+__device__ __forceinline__ float rcpf(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Round a pair to bf16 (nearest even) in place and return it packed (lo in the low half).
 __device__ __forceinline__ uint32_t round_pair(float& lo, float& hi) {
     const uint32_t w = sm100::pack_bf16(lo, hi);
