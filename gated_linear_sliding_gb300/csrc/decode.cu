@@ -2,7 +2,8 @@
 //
 // Lizard summary (gist.science/ko/paper/2507.09025), sec. 2-A-1: inference keeps a
 // constant-size state updated token by token instead of a growing KV cache;
-// sec. 4: generation at 32K keeps constant memory.  One step at position pos:
+// sec. 4: generation at 32K keeps constant memory.  One step at position pos (one position
+// for the batch, or one per sequence read from device memory):
 //   S <- Gamma_pos (.) S + phi(k_{pos-w}) v_{pos-w}^T,  z likewise (pos >= w),
 //   y  = [phi(q) S + sum_{j in (pos-w, pos]} e^{s q.k_j} v_j]
 //      / [phi(q).z + sum_j e^{s q.k_j} + sum_m e^{t_m}],
@@ -81,7 +82,11 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
     const int64_t unit = blockIdx.x;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
     const int G = (int)p.G;
-    const int64_t w = p.w, R = w + 1, pos = a.pos;
+    const int64_t w = p.w, R = w + 1, pos = a.pos_dev != nullptr ? a.pos_dev[b] : a.pos;
+    if (pos < 0) {  // a negative per-sequence position: recorded, the sequence is left untouched
+        if (threadIdx.x == 0) report((WsHeader*)a.header, LIZARD_ERR_INVALID_ARG, 40);
+        return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = tid % DH, rg = tid / DH;
     const bool admit = pos >= w;

@@ -60,6 +60,7 @@ cudaError_t launch_ring_fill(const Plan& p, const void* k, const void* v, void* 
 
 struct DecodeArgs {
     int64_t pos;
+    const int64_t* pos_dev;  // per-sequence positions [B] on the device, or null (use pos)
     const void *q, *k, *v, *g, *Wf;
     const float* sinks;
     void* y;

@@ -226,10 +226,12 @@ size_t lizard_decode_workspace(const lizard_dims* dims) {
     return kHeaderBytes;
 }
 
-lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const void* q,
-                                 const void* k, const void* v, const void* g, const void* Wf,
-                                 const float* sinks, void* y, float* S, float* z, void* kcache,
-                                 void* vcache, void* workspace, size_t ws_bytes, void* stream) {
+// Both decode entry points: one position for the batch (pos_dev null) or one per sequence.
+static lizard_status decode_step(const lizard_dims* dims, int64_t pos, const int64_t* pos_dev,
+                                 const void* q, const void* k, const void* v, const void* g,
+                                 const void* Wf, const float* sinks, void* y, float* S, float* z,
+                                 void* kcache, void* vcache, void* workspace, size_t ws_bytes,
+                                 void* stream) {
     if (dims == nullptr) return LIZARD_ERR_INVALID_ARG;
     lizard_dims d1 = *dims;
     d1.L = 1;
@@ -246,6 +248,7 @@ lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const voi
     if (st != LIZARD_OK) return st;
     DecodeArgs a;
     a.pos = pos;
+    a.pos_dev = pos_dev;
     a.q = q;
     a.k = k;
     a.v = v;
@@ -259,6 +262,25 @@ lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const voi
     a.vc = vcache;
     a.header = workspace;
     return from_cuda(launch_decode(p, a, (cudaStream_t)stream));
+}
+
+lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const void* q,
+                                 const void* k, const void* v, const void* g, const void* Wf,
+                                 const float* sinks, void* y, float* S, float* z, void* kcache,
+                                 void* vcache, void* workspace, size_t ws_bytes, void* stream) {
+    return decode_step(dims, pos, nullptr, q, k, v, g, Wf, sinks, y, S, z, kcache, vcache,
+                       workspace, ws_bytes, stream);
+}
+
+lizard_status lizard_decode_step_positions(const lizard_dims* dims, const int64_t* pos,
+                                           const void* q, const void* k, const void* v,
+                                           const void* g, const void* Wf, const float* sinks,
+                                           void* y, float* S, float* z, void* kcache,
+                                           void* vcache, void* workspace, size_t ws_bytes,
+                                           void* stream) {
+    if (pos == nullptr || ((uintptr_t)pos & 7u) != 0) return LIZARD_ERR_INVALID_ARG;
+    return decode_step(dims, 0, pos, q, k, v, g, Wf, sinks, y, S, z, kcache, vcache, workspace,
+                       ws_bytes, stream);
 }
 
 lizard_status lizard_read_device_status(void* workspace, void* stream) {

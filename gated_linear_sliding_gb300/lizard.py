@@ -25,7 +25,8 @@ LIZARD_BF16 = 1
 
 EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_fwd",
             "lizard_attn_bwd_workspace", "lizard_attn_bwd", "lizard_decode_workspace",
-            "lizard_decode_step", "lizard_read_device_status", "lizard_status_string",
+            "lizard_decode_step", "lizard_decode_step_positions", "lizard_read_device_status",
+            "lizard_status_string",
             "lizard_profile_events", "lizard_version", "lizard_attn_fwd_noalloc",
             "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout"]
 
@@ -78,6 +79,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_attn_bwd.restype = ctypes.c_int
     lib.lizard_decode_step.argtypes = [_DP, ctypes.c_int64] + [_VP] * 12 + [ctypes.c_size_t, _VP]
     lib.lizard_decode_step.restype = ctypes.c_int
+    lib.lizard_decode_step_positions.argtypes = [_DP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
+    lib.lizard_decode_step_positions.restype = ctypes.c_int
     lib.lizard_read_device_status.argtypes = [_VP, _VP]
     lib.lizard_read_device_status.restype = ctypes.c_int
     lib.lizard_status_string.argtypes = [ctypes.c_int]
@@ -310,4 +313,34 @@ def lizard_decode_step(pos: int, q, k, v, g, Wf, sinks, S, z, kcache, vcache, w:
                                    _p(Wf), _p(sinks), _p(y), _p(S), _p(z), _p(kcache),
                                    _p(vcache), _p(workspace), workspace.numel(), _stream(stream))
     _check(st, "lizard_decode_step")
+    return y
+
+
+def lizard_decode_step_positions(pos, q, k, v, g, Wf, sinks, S, z, kcache, vcache, w: int, *,
+                                 scale: float = 0.0, y=None, workspace=None, stream=None):
+    """One decode step with a position per sequence: pos is an int64 device tensor [B],
+    read when the kernel runs.  A negative entry is reported through the workspace status
+    (lizard_read_device_status) and leaves that sequence untouched."""
+    B, Hq, d = q.shape
+    Hkv, D, M = k.shape[1], g.shape[-1], sinks.shape[1]
+    dt = q.dtype
+    _need(pos, "pos", (B,), torch.int64)
+    _need(k, "k", (B, Hkv, d), dt)
+    _need(v, "v", (B, Hkv, d), dt)
+    _need(g, "g", (B, Hkv, D), dt)
+    _need(Wf, "Wf", (Hkv, d, D // 2), dt)
+    _need(sinks, "sinks", (Hq, M), torch.float32)
+    _need(S, "S", (B, Hkv, D, d), torch.float32)
+    _need(z, "z", (B, Hkv, D), torch.float32)
+    _need(kcache, "kcache", (B, Hkv, w + 1, d), dt)
+    _need(vcache, "vcache", (B, Hkv, w + 1, d), dt)
+    y = torch.empty_like(q) if y is None else y
+    dims = lizard_dims(B, 1, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    if workspace is None:
+        workspace = new_workspace(lizard_decode_workspace(dims), q.device, stream)
+    st = load().lizard_decode_step_positions(ctypes.byref(dims), _p(pos), _p(q), _p(k), _p(v),
+                                             _p(g), _p(Wf), _p(sinks), _p(y), _p(S), _p(z),
+                                             _p(kcache), _p(vcache), _p(workspace),
+                                             workspace.numel(), _stream(stream))
+    _check(st, "lizard_decode_step_positions")
     return y

@@ -162,6 +162,23 @@ lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const voi
                                  const float* sinks, void* y, float* S, float* z, void* kcache,
                                  void* vcache, void* workspace, size_t ws_bytes, void* stream);
 
+/* The same step with one position per sequence, for batches whose sequences have
+ * different lengths (continuous batching).
+ *   pos: DEVICE array [B] of int64, 8-byte aligned, read by the kernel when it runs (so a
+ *   captured CUDA graph may be replayed after the positions are advanced on the device);
+ *   sequence b is at position pos[b]: its state, ring slots and output follow
+ *   lizard_decode_step at that position.  The library does not own or modify pos.
+ *   A negative pos[b] records LIZARD_ERR_INVALID_ARG in the workspace status word (read it
+ *   with lizard_read_device_status) and leaves sequence b's y, state and caches untouched;
+ *   the other sequences are computed.  Host-side errors are those of lizard_decode_step,
+ *   plus LIZARD_ERR_INVALID_ARG for a null or misaligned pos. */
+lizard_status lizard_decode_step_positions(const lizard_dims* dims, const int64_t* pos,
+                                           const void* q, const void* k, const void* v,
+                                           const void* g, const void* Wf, const float* sinks,
+                                           void* y, float* S, float* z, void* kcache,
+                                           void* vcache, void* workspace, size_t ws_bytes,
+                                           void* stream);
+
 /* Synchronise `stream`, read the device status word of `workspace` and clear it.
  * Returns LIZARD_OK or the first error a kernel recorded (e.g. LIZARD_ERR_TIMEOUT). */
 lizard_status lizard_read_device_status(void* workspace, void* stream);

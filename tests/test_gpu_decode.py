@@ -150,3 +150,141 @@ def test_decode_b64_full_size_sampled(lz, oracle_mod):
         ref = oracle_mod.fwd(**seq, w=w)["y"][0, T0:]          # [steps, Hq, d]
         got = Y[:, b].float().cpu().numpy().astype(np.float64)
         assert_parity(got, ref, "bf16", f"decode b{b}")
+
+
+def _prefill_rows(lz, t, wl, lens, S, z, kc, vc):
+    """State and ring caches of each sequence b after its first lens[b] tokens, one B=1
+    forward per sequence writing into row b (rows of a sequence that has not started stay
+    zero)."""
+    S.zero_()
+    z.zero_()
+    kc.zero_()
+    vc.zero_()
+    for b, L0 in enumerate(lens):
+        if L0 == 0:
+            continue
+        pre = {n: t[n][b:b + 1, :L0].contiguous() for n in ("q", "k", "v", "g")}
+        lz.lizard_attn_fwd(pre["q"], pre["k"], pre["v"], pre["g"], t["Wf"], t["sinks"], wl.w,
+                           S_out=S[b:b + 1], z_out=z[b:b + 1], kcache_out=kc[b:b + 1],
+                           vcache_out=vc[b:b + 1])
+
+
+def _token(t, lens, i):
+    """The new token of every sequence at step i (sequence b is at position lens[b] + i)."""
+    return {n: torch.stack([t[n][b, L0 + i] for b, L0 in enumerate(lens)]).contiguous()
+            for n in ("q", "k", "v", "g")}
+
+
+def _per_sequence_ref(oracle_mod, inp, wl, lens, steps):
+    """Oracle outputs of each sequence at its own positions lens[b] .. lens[b] + steps - 1."""
+    out = []
+    for b, L0 in enumerate(lens):
+        one = {n: (a[b:b + 1, :L0 + steps] if n in ("q", "k", "v", "g") else a)
+               for n, a in inp.items()}
+        out.append(oracle_mod.fwd(**one, w=wl.w)["y"][0, L0:L0 + steps])
+    return np.stack(out)
+
+
+def test_decode_positions_per_sequence(lz, oracle_mod):
+    """Sequences of one batch at different positions (a fresh one, one inside the first
+    window, one at the window edge, one long): each follows its own prefill, token by token."""
+    wl = I.DECODE_B64.replace(B=4)
+    lens, steps = [0, 5, 63, 700], 3
+    inp = I.make_inputs(wl.replace(L=max(lens) + steps))
+    ref = _per_sequence_ref(oracle_mod, inp, wl, lens, steps)
+    t = to_dev(inp, wl.dtype)
+    tdt = t["q"].dtype
+    S = torch.empty(wl.B, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.empty(wl.B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    kc = torch.empty(wl.B, wl.Hkv, wl.w + 1, wl.d, dtype=tdt, device="cuda")
+    vc = torch.empty_like(kc)
+    _prefill_rows(lz, t, wl, lens, S, z, kc, vc)
+    dims = lz.make_dims(wl.B, 1, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, tdt)
+    ws = lz.new_workspace(lz.lizard_decode_workspace(dims), "cuda")
+    ys = []
+    for i in range(steps):
+        pos = torch.tensor([L0 + i for L0 in lens], dtype=torch.int64, device="cuda")
+        tok = _token(t, lens, i)
+        ys.append(lz.lizard_decode_step_positions(pos, tok["q"], tok["k"], tok["v"], tok["g"],
+                                                  t["Wf"], t["sinks"], S, z, kc, vc, wl.w,
+                                                  workspace=ws))
+    torch.cuda.synchronize()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    assert_parity(to_np(torch.stack(ys, 1)), ref, wl.dtype, "per-sequence decode")
+
+
+def test_decode_positions_negative_entry_is_reported(lz, oracle_mod):
+    """A negative position is recorded in the workspace status and leaves that sequence's
+    output, state and caches untouched; the other sequences are computed."""
+    wl = I.DECODE_B64.replace(B=2)
+    lens = [10, 70]
+    inp = I.make_inputs(wl.replace(L=max(lens) + 1))
+    ref = _per_sequence_ref(oracle_mod, inp, wl, lens, 1)
+    t = to_dev(inp, wl.dtype)
+    tdt = t["q"].dtype
+    S = torch.empty(wl.B, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.empty(wl.B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    kc = torch.empty(wl.B, wl.Hkv, wl.w + 1, wl.d, dtype=tdt, device="cuda")
+    vc = torch.empty_like(kc)
+    _prefill_rows(lz, t, wl, lens, S, z, kc, vc)
+    before = [x[0].clone() for x in (S, z, kc, vc)]
+    tok = _token(t, lens, 0)
+    y = torch.full((wl.B, wl.Hq, wl.d), 7.0, dtype=tdt, device="cuda")
+    dims = lz.make_dims(wl.B, 1, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, tdt)
+    ws = lz.new_workspace(lz.lizard_decode_workspace(dims), "cuda")
+    pos = torch.tensor([-1, lens[1]], dtype=torch.int64, device="cuda")
+    lz.lizard_decode_step_positions(pos, tok["q"], tok["k"], tok["v"], tok["g"], t["Wf"],
+                                    t["sinks"], S, z, kc, vc, wl.w, y=y, workspace=ws)
+    torch.cuda.synchronize()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_ERR_INVALID_ARG
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK  # reading clears the word
+    assert bool((y[0] == 7.0).all())
+    for x, x0 in zip((S, z, kc, vc), before):
+        assert torch.equal(x[0], x0)
+    assert_parity(to_np(y[1:]), ref[1:, 0], wl.dtype, "the valid sequence")
+
+
+def test_decode_positions_graph_replay(lz, oracle_mod):
+    """The positions are read when the kernel runs: one captured step plus an on-device
+    position increment, replayed, walks every sequence forward."""
+    wl = I.DECODE_B64.replace(B=3)
+    lens, steps = [3, 66, 129], 5
+    inp = I.make_inputs(wl.replace(L=max(lens) + steps))
+    ref = _per_sequence_ref(oracle_mod, inp, wl, lens, steps)
+    t = to_dev(inp, wl.dtype)
+    tdt = t["q"].dtype
+    S = torch.empty(wl.B, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.empty(wl.B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    kc = torch.empty(wl.B, wl.Hkv, wl.w + 1, wl.d, dtype=tdt, device="cuda")
+    vc = torch.empty_like(kc)
+    _prefill_rows(lz, t, wl, lens, S, z, kc, vc)
+    dims = lz.make_dims(wl.B, 1, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, tdt)
+    ws = lz.new_workspace(lz.lizard_decode_workspace(dims), "cuda")
+    pos = torch.tensor(lens, dtype=torch.int64, device="cuda")
+    tok = _token(t, lens, 0)
+    y = torch.empty(wl.B, wl.Hq, wl.d, dtype=tdt, device="cuda")
+    state0 = [x.clone() for x in (S, z, kc, vc)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):  # first call (attribute setup) outside the capture
+        lz.lizard_decode_step_positions(pos, tok["q"], tok["k"], tok["v"], tok["g"], t["Wf"],
+                                        t["sinks"], S, z, kc, vc, wl.w, y=y, workspace=ws)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for x, x0 in zip((S, z, kc, vc), state0):
+        x.copy_(x0)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        lz.lizard_decode_step_positions(pos, tok["q"], tok["k"], tok["v"], tok["g"], t["Wf"],
+                                        t["sinks"], S, z, kc, vc, wl.w, y=y, workspace=ws)
+        pos.add_(1)
+    ys = []
+    for i in range(steps):
+        for n, x in _token(t, lens, i).items():
+            tok[n].copy_(x)
+        graph.replay()
+        ys.append(y.clone())
+    torch.cuda.synchronize()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    assert pos.tolist() == [L0 + steps for L0 in lens]
+    assert_parity(to_np(torch.stack(ys, 1)), ref, wl.dtype, "graph-replayed decode")
