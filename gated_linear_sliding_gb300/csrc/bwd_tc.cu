@@ -805,10 +805,10 @@ __global__ void __launch_bounds__(NT, 1)
         float v[32];
         tmem_ld32(tb + lane_off + cH + 32 * part, v);
         tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(r + row * DH + 32 * part + k) =
-                make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+        // through the (now idle) q and dY tiles, then coalesced to the record
+        staged_row_write(sm + rQ, row, part, v);
+        __syncthreads();
+        stage_record_out(r, sm + rQ);
         if (tid < 128) {
             r[128 * DH + tid] = S.dz[tid];
             r[128 * DH + 128 + tid] = lam_tot;
@@ -940,18 +940,20 @@ __global__ void __launch_bounds__(NT, 1)
                                : nullptr;
     if (tid < 128) S.z[tid] = rec ? rec[128 * DH + tid] : 0.0f;
     if (tid < 16) S.dts[tid >> 2][tid & 3] = 0.0f;
+    if (rec) stage_record_in(sm + wQ, rec);  // wQ, wD: the first step's copies land there later
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = S.tmem;
     {
         float v[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + 32 * part + k] : 0.0f;
+        staged_row_read(sm + wQ, rec != nullptr, row, part, v);
         tmem_st32(tb + lane_off + fH + 32 * part, v);
         tmem_wait_st();
     }
+    __syncthreads();  // the staged rows are read before the copies below overwrite them
     bool tma_out = false, mma_out = false;
     if (tid == 0 && c_begin < c_end) {
+        fence_async_smem();
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmDY);
         prefetch_tmap(&tmK);
@@ -1544,13 +1546,13 @@ __global__ void __launch_bounds__(NT, 1)
         S.rho_next[tid] = 0.0f;
         S.carry[tid] = 0.0f;
     }
+    if (rec) stage_record_in(sm + vR1, rec);  // vR1 is first written by the math threads
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = S.tmem;
     {
         float v[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = rec ? rec[row * DH + 32 * part + k] : 0.0f;
+        staged_row_read(sm + vR1, rec != nullptr, row, part, v);
         tmem_st32(tb + lane_off + vS + 32 * part, v);
         tmem_wait_st();
     }

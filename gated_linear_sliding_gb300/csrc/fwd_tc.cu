@@ -373,13 +373,7 @@ __global__ void __launch_bounds__(NT, 1)
     // per-row reads below are free of bank conflicts.
     const float* rec =
         seg > 0 ? a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats : nullptr;
-    if (rec != nullptr) {
-        for (int e = tid; e < DF * DH / 4; e += NT) {
-            const int r = e >> 5, c = e & 31;
-            *reinterpret_cast<float4*>(sm + oK + r * 512 + ((c & ~7) | ((c ^ r) & 7)) * 16) =
-                reinterpret_cast<const float4*>(rec)[e];
-        }
-    }
+    if (rec != nullptr) stage_record_in(sm + oK, rec);
     if (tid < DF) S.z[tid] = rec ? rec[DF * DH + tid] : 0.0f;
     __syncthreads();
     tc_fence_after();
@@ -387,17 +381,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (warp < NW) {
         // starting state H into TMEM (fp32 master copy), lane = feature f, column = d
         float v[32];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const int c = 8 * part + j;
-            const float4 x = rec ? *reinterpret_cast<const float4*>(
-                                       sm + oK + row * 512 + ((c & ~7) | ((c ^ row) & 7)) * 16)
-                                 : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-            v[4 * j] = x.x;
-            v[4 * j + 1] = x.y;
-            v[4 * j + 2] = x.z;
-            v[4 * j + 3] = x.w;
-        }
+        staged_row_read(sm + oK, rec != nullptr, row, part, v);
         tmem_st32(tb + lane_off + cH + 32 * part, v);
         tmem_wait_st();
     }
@@ -1145,10 +1129,10 @@ __global__ void __launch_bounds__(NL, 1)
         float v[32];
         tmem_ld32(tb + lane_off + cHl + 32 * part, v);
         tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; k += 4)
-            *reinterpret_cast<float4*>(r + row * DH + 32 * part + k) =
-                make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+        // through the (now idle) key and value tiles, then coalesced to the record
+        staged_row_write(sm + lK, row, part, v);
+        __syncthreads();
+        stage_record_out(r, sm + lK);
         if (tid < DF) {
             r[DF * DH + tid] = S.z[tid];
             r[DF * DH + DF + tid] = lam_tot;

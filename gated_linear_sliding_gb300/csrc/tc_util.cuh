@@ -89,5 +89,44 @@ inline bool make_map(CUtensorMap* m, const void* ptr, int rank, const cuuint64_t
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A [128][128] fp32 state record passes between global and shared memory through 64 KB of
+// shared memory with coalesced 16-byte accesses; each 512-byte row's 16-byte chunks are
+// XOR-swizzled by the row, so the per-thread row accesses (TMEM lane = row, 32 columns per
+// thread) are free of bank conflicts.
+__device__ __forceinline__ uint32_t rec_off(int r, int c) {
+    return (uint32_t)(r * 512 + ((c & ~7) | ((c ^ r) & 7)) * 16);
+}
+__device__ __forceinline__ void stage_record_in(uint8_t* dst, const float* rec) {
+    for (int e = threadIdx.x; e < 128 * 128 / 4; e += blockDim.x)
+        *reinterpret_cast<float4*>(dst + rec_off(e >> 5, e & 31)) =
+            reinterpret_cast<const float4*>(rec)[e];
+}
+__device__ __forceinline__ void stage_record_out(float* rec, const uint8_t* src) {
+    for (int e = threadIdx.x; e < 128 * 128 / 4; e += blockDim.x)
+        reinterpret_cast<float4*>(rec)[e] =
+            *reinterpret_cast<const float4*>(src + rec_off(e >> 5, e & 31));
+}
+// Columns [32 part, 32 part + 32) of staged row `row` (zeros when `have` is false) ...
+__device__ __forceinline__ void staged_row_read(const uint8_t* src, bool have, int row, int part,
+                                                float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float4 x = have ? *reinterpret_cast<const float4*>(src + rec_off(row, 8 * part + j))
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        v[4 * j] = x.x;
+        v[4 * j + 1] = x.y;
+        v[4 * j + 2] = x.z;
+        v[4 * j + 3] = x.w;
+    }
+}
+// ... and the same columns written.
+__device__ __forceinline__ void staged_row_write(uint8_t* dst, int row, int part,
+                                                 const float (&v)[32]) {
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        *reinterpret_cast<float4*>(dst + rec_off(row, 8 * part + j)) =
+            make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+
 }  // namespace tc
 }  // namespace lz
