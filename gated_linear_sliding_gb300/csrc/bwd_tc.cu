@@ -852,7 +852,7 @@ struct WSmall {
     uint64_t bar_tma, bar_u, bar_d1, bar_d2, bar_q, bar_fin;
     uint32_t tmem;
     volatile int abort;
-    float z[128], zs[128], cf[128], bref[128];
+    float z[128], zs[128], cf[128];
     float dts[4][4];
 };
 constexpr uint32_t kSmemFW = wSm + (uint32_t)sizeof(WSmall) + 1024;
@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(NT, 1)
     float* xa = reinterpret_cast<float*>(sm + wX);   // [4][128]
     float* xb = xa + 512;                            // [4][128]
     float* suk = reinterpret_cast<float*>(sm + wG);  // staged U_k rows [32][64]
-    float* btab = reinterpret_cast<float*>(sm + wB); // cumulative log-gates [32][128]
+    float* etab = reinterpret_cast<float*>(sm + wB); // e^{b_t - r} [32][128] fp32
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int quad = warp & 3, part = warp >> 2;
@@ -1025,12 +1025,14 @@ __global__ void __launch_bounds__(NT, 1)
             const float g0 = xa[gf], g1 = xa[128 + gf], g2 = xa[256 + gf], g3 = xa[384 + gf];
             const float bref = g0 + g1, blast = bref + g2 + g3;
             const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? bref : bref + g2;
+            // the decay factors of the step relative to r, once per (token, feature): the four
+            // heads of a token and the key-side phase read them from the table
 #pragma unroll
-            for (int t = 0; t < 8; ++t) btab[(8 * gq + t) * 128 + gf] = bt[t] + off;
+            for (int t = 0; t < 8; ++t)
+                etab[(8 * gq + t) * 128 + gf] = __expf(clamp80f(bt[t] + off - bref));
             if (gq == 0) {
                 S.cf[gf] = __expf(blast - bref);
                 S.zs[gf] = __expf(bref) * S.z[gf];
-                S.bref[gf] = bref;
             }
         }
         // (3) state copy e^{r} (.) H as high and low bf16 parts; master decayed by e^{b_31}
@@ -1167,7 +1169,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const float ph = kb == 0 ? ep[e] * ip : en[e] * in;
-                    ki[e] = ph * __expf(clamp80f(S.bref[f0 + e] - btab[t * 128 + f0 + e]));
+                    ki[e] = ph * rcpf(etab[t * 128 + f0 + e]);  // e^{r - b_t}
                     ku[e] = ki[e] * S.cf[f0 + e];
                 }
                 const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
@@ -1290,8 +1292,7 @@ __global__ void __launch_bounds__(NT, 1)
             float spd = 0.0f, snd = 0.0f;
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
-                const float eqp = __expf(clamp80f(btab[ti * 128 + fp + k] - S.bref[fp + k]));
-                const float eqn = __expf(clamp80f(btab[ti * 128 + fn + k] - S.bref[fn + k]));
+                const float eqp = etab[ti * 128 + fp + k], eqn = etab[ti * 128 + fn + k];
                 Dp[k] = ar * eqp * (Dp[k] - dl * S.zs[fp + k]);  // dphi+
                 Dn[k] = ar * eqn * (Dn[k] - dl * S.zs[fn + k]);  // dphi-
                 spd = fmaf(php[k], Dp[k], spd);
@@ -1457,7 +1458,7 @@ struct VSmall {
     uint64_t bar_tma, bar_u, bar_g, bar_a, bar_v, bar_k, bar_fin;
     uint32_t tmem;
     volatile int abort;
-    float z[128], rho_next[128], carry[128], rho[128], dlr[128];
+    float z[128], rho_next[128], carry[128], rho[128], dlr[128], bl[128];
 };
 constexpr uint32_t kSmemRW = vSm + (uint32_t)sizeof(VSmall) + 1024;
 static_assert(kSmemRW <= 232448, "shared memory budget");
@@ -1508,7 +1509,7 @@ __global__ void __launch_bounds__(NT, 1)
     float* tn = xb + 512;                             // [32 keys][64 f]
     static_assert(vX + 4 * (512 + 512 + 2048 + 128) <= vSm, "exchange area");
     float* suk = reinterpret_cast<float*>(sm + vG);   // staged U_k rows [32][64]
-    float* btab = reinterpret_cast<float*>(sm + vB);  // cumulative log-gates [32][128]
+    float* etab = reinterpret_cast<float*>(sm + vB);  // e^{b_t - rho} [32][128] fp32
     float* pk = reinterpret_cast<float*>(sm + vPK);   // phi(k') [32][128] fp32
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1632,18 +1633,26 @@ __global__ void __launch_bounds__(NT, 1)
             }
             xa[gq * 128 + gf] = run;
             __syncthreads();
-            const float g0 = xa[gf], g1 = xa[128 + gf], g2 = xa[256 + gf];
+            const float g0 = xa[gf], g1 = xa[128 + gf], g2 = xa[256 + gf], g3 = xa[384 + gf];
             const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? g0 + g1 : (g0 + g1) + g2;
+            // the decay factors of the step relative to rho, once per (token, feature): the
+            // four heads of a token and both key-side phases read them from the table
+            const float rh = fmaxf(g0 + g1, -60.0f);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) btab[(8 * gq + t) * 128 + gf] = bt[t] + off;
+            for (int t = 0; t < 8; ++t)
+                etab[(8 * gq + t) * 128 + gf] = __expf(clamp80f(bt[t] + off - rh));
+            if (gq == 0) {
+                S.bl[gf] = ((g0 + g1) + g2) + g3;
+                S.rho[gf] = rh;
+            }
         }
         __syncthreads();
         // (3) S' = e^{bl - rho + rho_next} (.) S, as high and low bf16 parts for the
         //     key-side products; z' likewise
         {
             const int f = row;
-            const float bl = btab[31 * 128 + f], rh = fmaxf(btab[15 * 128 + f], -60.0f);
-            const float fac = __expf(bl - rh + S.rho_next[f]);
+            const float rh = S.rho[f];
+            const float fac = __expf(S.bl[f] - rh + S.rho_next[f]);
             const int col = 32 * part;
             float v[32];
             tmem_ld32(tb + lane_off + vS + col, v);
@@ -1661,10 +1670,7 @@ __global__ void __launch_bounds__(NT, 1)
             }
             tmem_st32(tb + lane_off + vS + col, v);
             tmem_wait_st();
-            if (part == 0) {
-                S.z[f] *= fac;
-                S.rho[f] = rh;
-            }
+            if (part == 0) S.z[f] *= fac;
         }
         ok = fw_wait2(&S.bar_u, ph_u, S.abort, hdr, 71);
         if (!ok) break;
@@ -1754,7 +1760,7 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     ph[e] = kb == 0 ? ep[e] * ip : en[e] * in;
-                    kh[e] = ph[e] * __expf(clamp80f(S.rho[f0 + e] - btab[t * 128 + f0 + e]));
+                    kh[e] = ph[e] * rcpf(etab[t * 128 + f0 + e]);  // e^{rho - b_t}
                 }
                 *reinterpret_cast<float4*>(pk + t * 128 + f0) = make_float4(ph[0], ph[1], ph[2], ph[3]);
                 const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
@@ -1799,8 +1805,8 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                 for (int h = 0; h < 2; ++h) {
                     const int f1 = fp + k + h, f2 = fn + k + h;
-                    qp[h] = php[k + h] * ar * __expf(clamp80f(btab[ti * 128 + f1] - S.rho[f1]));
-                    qn[h] = phn[k + h] * ar * __expf(clamp80f(btab[ti * 128 + f2] - S.rho[f2]));
+                    qp[h] = php[k + h] * ar * etab[ti * 128 + f1];
+                    qn[h] = phn[k + h] * ar * etab[ti * 128 + f2];
                 }
                 split2(qp[0], qp[1], hp[k / 2], lp[k / 2]);
                 split2(qn[0], qn[1], hn[k / 2], ln[k / 2]);
@@ -1833,6 +1839,14 @@ __global__ void __launch_bounds__(NT, 1)
                 ch[o] = xh;
                 cl[o] = __float2bfloat16_rn(x - __bfloat162float(xh));
             }
+        }
+        // this step's dB rows (from the forward-direction walk) for phase (9), requested now so
+        // the load overlaps the MMAs below
+        float dbp[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const int t = 8 * part + e;
+            dbp[e] = t < n ? dB[((b * p.L + t0 + t) * p.Hkv + kv) * 128 + row] : 0.0f;
         }
         fence_async_smem();
         tc_fence_before();
@@ -1917,9 +1931,8 @@ __global__ void __launch_bounds__(NT, 1)
             for (int e = 0; e < 8; ++e) {
                 const int t = 8 * part + e;
                 phk[e] = pk[t * 128 + f];
-                dphi[e] = __expf(clamp80f(S.rho[f] - btab[t * 128 + f])) * (gv[e] + zp);
-                loc[e] = t < n ? dB[((b * p.L + t0 + t) * p.Hkv + kv) * 128 + f] - phk[e] * dphi[e]
-                               : 0.0f;
+                dphi[e] = rcpf(etab[t * 128 + f]) * (gv[e] + zp);  // e^{rho - b_t} (G + z')
+                loc[e] = t < n ? dbp[e] - phk[e] * dphi[e] : 0.0f;
             }
             // suffix sums inside the part (keys descending), then across parts
             float suf[8];
