@@ -778,12 +778,13 @@ __global__ void __launch_bounds__(NT, 1)
             const int f = tid & 127, gq = tid >> 7;
             const __nv_bfloat16* qh = (const __nv_bfloat16*)(sm + rQh);
             const __nv_bfloat16* ql = (const __nv_bfloat16*)(sm + rQl);
-            float zs = 0.0f;
+            float zs[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains: the loads overlap
+#pragma unroll
             for (int r = 32 * gq; r < 32 * gq + 32; ++r) {
                 const uint32_t off = ((f >> 6) * 16384 + sw128(r, (f & 63) >> 3) + (f & 7) * 2) / 2;
-                zs = fmaf(__bfloat162float(qh[off]) + __bfloat162float(ql[off]), zq[512 + r], zs);
+                zs[r & 3] = fmaf(__bfloat162float(qh[off]) + __bfloat162float(ql[off]), zq[512 + r], zs[r & 3]);
             }
-            zq[gq * 128 + f] = zs;
+            zq[gq * 128 + f] = (zs[0] + zs[1]) + (zs[2] + zs[3]);
         }
         __syncthreads();
         if (tid < 128)
@@ -1877,12 +1878,13 @@ __global__ void __launch_bounds__(NT, 1)
             const int f = tid & 127, gq2 = tid >> 7;
             const __nv_bfloat16* qh = (const __nv_bfloat16*)(sm + vR1);
             const __nv_bfloat16* ql = (const __nv_bfloat16*)(sm + vR1 + 32768);
-            float zsum = 0.0f;
+            float zsum[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains: the loads overlap
+#pragma unroll
             for (int r = 32 * gq2; r < 32 * gq2 + 32; ++r) {
                 const uint32_t o = ((f >> 6) * 16384 + sw128(r, (f & 63) >> 3) + (f & 7) * 2) / 2;
-                zsum = fmaf(__bfloat162float(qh[o]) + __bfloat162float(ql[o]), S.dlr[r], zsum);
+                zsum[r & 3] = fmaf(__bfloat162float(qh[o]) + __bfloat162float(ql[o]), S.dlr[r], zsum[r & 3]);
             }
-            xa[gq2 * 128 + f] = zsum;
+            xa[gq2 * 128 + f] = (zsum[0] + zsum[1]) + (zsum[2] + zsum[3]);
         }
         ok = fw_wait2(&S.bar_a, ph_a, S.abort, hdr, 73);
         if (!ok) break;

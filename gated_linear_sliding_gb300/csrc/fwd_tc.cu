@@ -1101,12 +1101,13 @@ __global__ void __launch_bounds__(NL, 1)
             const int f = tid & (DF - 1), gq = tid >> 7;
             const __nv_bfloat16* ku = (const __nv_bfloat16*)(sm + lKu);
             const __nv_bfloat16* kul = (const __nv_bfloat16*)(sm + lKul);
-            float zs = 0.0f;
+            float zs[4] = {0.0f, 0.0f, 0.0f, 0.0f};  // four chains: the loads overlap
+#pragma unroll
             for (int t = 32 * gq; t < 32 * gq + 32; ++t) {
                 const uint32_t off = ((f >> 6) * 16384 + sw128(t, (f & 63) >> 3) + (f & 7) * 2) / 2;
-                zs += __bfloat162float(ku[off]) + __bfloat162float(kul[off]);
+                zs[t & 3] += __bfloat162float(ku[off]) + __bfloat162float(kul[off]);
             }
-            zq[gq * DF + f] = zs;
+            zq[gq * DF + f] = (zs[0] + zs[1]) + (zs[2] + zs[3]);
         }
         __syncthreads();
         if (tid < DF)
