@@ -113,6 +113,22 @@ __device__ __forceinline__ void add_store_row(__nv_bfloat16* dst, const float* v
     }
 }
 
+// The same with the bf16 row already loaded (requested early, so its latency is hidden).
+__device__ __forceinline__ void add_store_loaded(__nv_bfloat16* dst, const float* v,
+                                                 const uint4 (&old)[4]) {
+#pragma unroll
+    for (int ch = 0; ch < 4; ++ch) {
+        float o[8];
+        unpack8(old[ch].x, old[ch].y, old[ch].z, old[ch].w, o);
+        uint4 w;
+        w.x = pack_bf16(o[0] + v[8 * ch], o[1] + v[8 * ch + 1]);
+        w.y = pack_bf16(o[2] + v[8 * ch + 2], o[3] + v[8 * ch + 3]);
+        w.z = pack_bf16(o[4] + v[8 * ch + 4], o[5] + v[8 * ch + 5]);
+        w.w = pack_bf16(o[6] + v[8 * ch + 6], o[7] + v[8 * ch + 7]);
+        *reinterpret_cast<uint4*>(dst + 8 * ch) = w;
+    }
+}
+
 // ---------------------------------------------------------------------------------------
 // dk, dv window parts: keys [j0, j0 + 128) against the query tiles that can see them.
 constexpr uint32_t aK = 0, aV = 32768, aQ = 65536, aD = 131072, aRow = 196608,
@@ -185,15 +201,23 @@ __global__ void __launch_bounds__(NT, 1)
     bool ok = all_wait(&S.bar_kv, 0, S, hdr, 30);
     const float s2 = p.scale * kLog2e;
 
+    // lse and delta of tile n's rows (the columns of S^T), requested one tile ahead
+    float nls = 0.0f, ndl = 0.0f;
+    auto row_vals = [&](int64_t cc) {
+        const int64_t i = cc * CT + (tid >> 2);
+        const int64_t idx = (b * p.L + i) * p.Hq + kv * GQ + (tid & 3);
+        nls = i < p.L ? a.lse[idx] : 0.0f;
+        ndl = i < p.L ? rows[nrow + idx] : 0.0f;
+    };
+    if (tid < 128 && nq > 0) row_vals(c_first);
+
     for (int n = 0; ok && n < nq; ++n) {
         const int buf = n & 1;
         const int64_t c = c_first + n, q0 = c * CT;
-        // rows of this tile: lse and delta (columns of S^T)
         if (tid < 128) {
-            const int64_t i = q0 + (tid >> 2);
-            const int64_t idx = (b * p.L + i) * p.Hq + kv * GQ + (tid & 3);
-            slse[buf * 128 + tid] = i < p.L ? a.lse[idx] * kLog2e : 0.0f;
-            sdel[buf * 128 + tid] = i < p.L ? rows[nrow + idx] : 0.0f;
+            slse[buf * 128 + tid] = nls * kLog2e;
+            sdel[buf * 128 + tid] = ndl;
+            if (n + 1 < nq) row_vals(c + 1);
         }
         ok = all_wait(&S.bar_in[buf], ph_in[buf], S, hdr, 31);
         if (!ok) break;
@@ -380,8 +404,29 @@ __global__ void __launch_bounds__(NT, 1)
     const float s2 = p.scale * kLog2e;
     const uint64_t dQ = kdesc(base + bQ), dD = kdesc(base + bD);
 
+    // this thread's row: lse and delta requested one tile ahead, the dq row (holding the
+    // state part) at the top of its tile; both are used late in the tile
+    float nls = 0.0f, ndl = 0.0f;
+    auto row_vals = [&](int64_t cc) {
+        const int64_t i = cc * CT + (row >> 2);
+        const int64_t idx = (b * p.L + i) * p.Hq + kv * GQ + (row & 3);
+        nls = i < p.L ? a.lse[idx] : 0.0f;
+        ndl = i < p.L ? rows[nrow + idx] : 0.0f;
+    };
+    if (nq > 0) row_vals(c0);
+
     for (int n = 0; ok && n < nq; ++n) {
         const int64_t c = c0 + n, q0 = c * CT;
+        const float ls = nls * kLog2e, dl = ndl;
+        if (n + 1 < nq) row_vals(c + 1);
+        uint4 oldq[4];
+        {
+            const int64_t i = q0 + (row >> 2);
+            const int64_t idx = (b * p.L + i) * p.Hq + kv * GQ + (row & 3);
+            const uint4* src = reinterpret_cast<const uint4*>((const __nv_bfloat16*)a.dq + idx * DH + 32 * part);
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) oldq[ch] = i < p.L ? src[ch] : make_uint4(0u, 0u, 0u, 0u);
+        }
         ok = all_wait(&S.bar_in[0], ph_in, S, hdr, 41);
         if (!ok) break;
         ph_in ^= 1u;
@@ -412,8 +457,6 @@ __global__ void __launch_bounds__(NT, 1)
         const int64_t i = q0 + (row >> 2);
         const int64_t idx = (b * p.L + i) * p.Hq + kv * GQ + (row & 3);
         const bool rv = i < p.L;
-        const float ls = rv ? a.lse[idx] * kLog2e : 0.0f;
-        const float dl = rv ? rows[nrow + idx] : 0.0f;
         uint32_t dw[16];
         {
             const int64_t kbase = (c - 2 + part) * CT;
@@ -470,7 +513,7 @@ __global__ void __launch_bounds__(NT, 1)
         float v[32];
         tmem_ld32(tb + lane_off + cDQ + 32 * part, v);
         tmem_wait_ld();
-        if (rv) add_store_row((__nv_bfloat16*)a.dq + idx * DH + 32 * part, v, true);
+        if (rv) add_store_loaded((__nv_bfloat16*)a.dq + idx * DH + 32 * part, v, oldq);
         tc_fence_before();
         __syncthreads();  // S, dP, dQ columns are free for the next tile
     }
