@@ -205,25 +205,51 @@ __global__ void bwd_row_table(Plan p, BwdArgs a, BwdWs ws) {
     const T* yr = (const T*)a.y + r * DH;
     const T* dr = (const T*)a.dy + r * DH;
     float dl = 0.0f;
-    if constexpr (sizeof(T) == 2 && DH == 128) {
-        // four bf16 per lane in one 8-byte load
-        const uint2 yv = reinterpret_cast<const uint2*>(yr)[lane];
-        const uint2 dv = reinterpret_cast<const uint2*>(dr)[lane];
-        const uint32_t yw[2] = {yv.x, yv.y}, dw[2] = {dv.x, dv.y};
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            dl = fmaf(__uint_as_float(yw[k] << 16), __uint_as_float(dw[k] << 16), dl);
-            dl = fmaf(__uint_as_float(yw[k] & 0xFFFF0000u), __uint_as_float(dw[k] & 0xFFFF0000u), dl);
-        }
-    } else {
-        for (int c = lane; c < DH; c += 32) dl = fmaf(ld(yr + c), ld(dr + c), dl);
-    }
+    for (int c = lane; c < DH; c += 32) dl = fmaf(ld(yr + c), ld(dr + c), dl);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
     if (lane == 0) {
         float* rows = (float*)a.ws + ws.rows;
         rows[r] = expf(-a.lse[r]);
         rows[nrow + r] = dl;
+    }
+}
+
+// bf16, d = 128: 16 lanes per row (8 elements each, 16-byte loads), 8 rows per warp with every
+// load of the warp issued before the first use, so each warp keeps 4 KB in flight.
+constexpr int kRowsPerWarp = 8;
+__global__ void bwd_row_table_bf16(Plan p, BwdArgs a, BwdWs ws) {
+    const int64_t nrow = p.B * p.L * p.Hq;
+    const int64_t r0 = ((int64_t)blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5)) * kRowsPerWarp;
+    const int lane = threadIdx.x & 31, half = lane >> 4, sub = lane & 15;
+    uint4 yv[kRowsPerWarp / 2], dv[kRowsPerWarp / 2];
+    float ls[kRowsPerWarp / 2];
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp / 2; ++k) {
+        const int64_t r = r0 + 2 * k + half;
+        const bool in = r < nrow;
+        yv[k] = in ? reinterpret_cast<const uint4*>((const __nv_bfloat16*)a.y + r * 128)[sub] : make_uint4(0u, 0u, 0u, 0u);
+        dv[k] = in ? reinterpret_cast<const uint4*>((const __nv_bfloat16*)a.dy + r * 128)[sub] : make_uint4(0u, 0u, 0u, 0u);
+        ls[k] = in && sub == 0 ? a.lse[r] : 0.0f;
+    }
+    float* rows = (float*)a.ws + ws.rows;
+#pragma unroll
+    for (int k = 0; k < kRowsPerWarp / 2; ++k) {
+        const uint32_t yw[4] = {yv[k].x, yv[k].y, yv[k].z, yv[k].w};
+        const uint32_t dw[4] = {dv[k].x, dv[k].y, dv[k].z, dv[k].w};
+        float dl = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            dl = fmaf(__uint_as_float(yw[e] << 16), __uint_as_float(dw[e] << 16), dl);
+            dl = fmaf(__uint_as_float(yw[e] & 0xFFFF0000u), __uint_as_float(dw[e] & 0xFFFF0000u), dl);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) dl += __shfl_xor_sync(0xffffffffu, dl, o);
+        const int64_t r = r0 + 2 * k + half;
+        if (sub == 0 && r < nrow) {
+            rows[r] = expf(-ls[k]);
+            rows[nrow + r] = dl;
+        }
     }
 }
 
@@ -893,11 +919,28 @@ __global__ void bwd_gates(Plan p, BwdArgs a, BwdWs ws) {
     const float* tot = wsf + ws.tot + ((size_t)seg * U + unit) * p.D + f0;
     const float4 d0 = *reinterpret_cast<const float4*>(wsf + ws.dB + e);
     const float4 d1 = *reinterpret_cast<const float4*>(wsf + ws.dB + e + 4);
-    const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+    const float4 t0 = *reinterpret_cast<const float4*>(tot);
+    const float4 t1 = *reinterpret_cast<const float4*>(tot + 4);
+    const float dv[8] = {d0.x + t0.x, d0.y + t0.y, d0.z + t0.z, d0.w + t0.w,
+                         d1.x + t1.x, d1.y + t1.y, d1.z + t1.z, d1.w + t1.w};
+    if constexpr (sizeof(T) == 2) {
+        // d log sigmoid(g)/dg = 1 - sigmoid(g) = 1 / (1 + e^g), which keeps its relative
+        // precision for large g; eight gates in one 16-byte load
+        const uint4 gw = *reinterpret_cast<const uint4*>((const __nv_bfloat16*)a.g + e);
+        const uint32_t w[4] = {gw.x, gw.y, gw.z, gw.w};
+        uint32_t o[4];
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float gam = sigmoidf_(ld((const T*)a.g + e + k));
-        st((T*)a.dg + e + k, (dv[k] + tot[k]) * (1.0f - gam));
+        for (int k = 0; k < 4; ++k) {
+            const float g0 = __uint_as_float(w[k] << 16), g1 = __uint_as_float(w[k] & 0xFFFF0000u);
+            const __nv_bfloat162 h =
+                __floats2bfloat162_rn(dv[2 * k] / (1.0f + expf(g0)), dv[2 * k + 1] / (1.0f + expf(g1)));
+            o[k] = *reinterpret_cast<const uint32_t*>(&h);
+        }
+        *reinterpret_cast<uint4*>((__nv_bfloat16*)a.dg + e) = make_uint4(o[0], o[1], o[2], o[3]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            st((T*)a.dg + e + k, dv[k] / (1.0f + expf(ld((const T*)a.g + e + k))));
     }
 }
 
@@ -965,7 +1008,10 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     // 0. per-row a = e^{-lse} and delta = dy . y
     {
         const int64_t nrow = p.B * p.L * p.Hq;
-        bwd_row_table<T, DH><<<(unsigned)((nrow + 7) / 8), 256, 0, s>>>(p, a, ws);
+        if constexpr (sizeof(T) == 2 && DH == 128)
+            bwd_row_table_bf16<<<(unsigned)((nrow + 8 * kRowsPerWarp - 1) / (8 * kRowsPerWarp)), 256, 0, s>>>(p, a, ws);
+        else
+            bwd_row_table<T, DH><<<(unsigned)((nrow + 7) / 8), 256, 0, s>>>(p, a, ws);
     }
     // 1. forward segment states (segment pass + scan) into the first record region
     if (p.P > 1) {
