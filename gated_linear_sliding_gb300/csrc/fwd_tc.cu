@@ -1205,9 +1205,13 @@ cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s
     return launch_local_and_scan(p, a, mw, s);
 }
 
+// Segments are cut so that the last wave of (batch, KV head, segment) CTAs is as full as the
+// others: a second, mostly empty wave would cost a whole segment's walk.
+void fwd_tc_plan(Plan* p) { plan_segments_waves(p, 152); }
+
 cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     Plan p = p0;
-    plan_segments(&p, 152);
+    fwd_tc_plan(&p);
     alignas(64) CUtensorMap mq, mk, mv, mw, my;
     const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
                      Hkv = (cuuint64_t)p.Hkv;

@@ -54,6 +54,8 @@ cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s);
 bool fwd_tc_supported(const Plan& p);
 cudaError_t launch_fwd_tc(const Plan& p, const FwdArgs& a, cudaStream_t s);
 // Segment-start states only (tensor-core segment pass + scan into a.seg), for the backward.
+// The segmentation the tensor-core forward runs with (fewest segment-waves on 152 SMs).
+void fwd_tc_plan(Plan* p);
 cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_ring_fill(const Plan& p, const void* k, const void* v, void* kc, void* vc,
                              cudaStream_t s);

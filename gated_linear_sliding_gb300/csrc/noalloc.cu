@@ -54,6 +54,16 @@ extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const 
                                                  void* stream) {
     Plan p;
     if (!make_plan(dims, &p)) return LIZARD_ERR_INVALID_ARG;
+    // scratch this problem needs (checked first: it depends on the dimensions only): the
+    // status word, plus one boundary-state record per (segment, batch x KV head) when the
+    // sequence is split into several segments, counted with the segmentation the launch
+    // below will use
+    Plan pl = p;
+    if (fwd_tc_supported(p)) fwd_tc_plan(&pl);
+    const size_t need =
+        kHeaderBytes +
+        (pl.P > 1 ? sizeof(float) * (size_t)pl.P * (size_t)(p.B * p.Hkv) * p.rec_floats : 0);
+    if (need > kNoAllocScratchBytes) return LIZARD_ERR_WORKSPACE;
     if (!q || !k || !v || !g || !Wf || !y || (p.M > 0 && !sinks)) return LIZARD_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, g, Wf, sinks, y, lse, S_out, z_out, kcache_out, vcache_out};
     for (const void* ptr : ptrs)
@@ -63,12 +73,6 @@ extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const 
     if (!((p.d == 64 || p.d == 128) && (p.D == 64 || p.D == 128) && p.B * p.Hkv <= 65535 &&
           p.B * p.Hq <= ((int64_t)1 << 30)))
         return LIZARD_ERR_UNSUPPORTED;
-    // scratch this problem needs: the status word, plus one boundary-state record per
-    // (segment, batch x KV head) when the sequence is split into several segments
-    const size_t need =
-        kHeaderBytes +
-        (p.P > 1 ? sizeof(float) * (size_t)p.P * (size_t)(p.B * p.Hkv) * p.rec_floats : 0);
-    if (need > kNoAllocScratchBytes) return LIZARD_ERR_WORKSPACE;
 
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return LIZARD_ERR_CUDA;

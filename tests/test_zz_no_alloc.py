@@ -51,11 +51,14 @@ def test_noalloc_matches_workspace_entry_point(lz, wl, L):
 
 
 def test_noalloc_rejects_problems_beyond_its_scratch(lz):
-    """37 x 8 units cut into 2 segments need 2 * 296 * 66,560 bytes of boundary states,
-    more than the 32 MiB array: the call must refuse before launching anything."""
+    """fp32, 37 x 8 units cut into 2 segments: 2 * 296 * 66,560 bytes of boundary states,
+    more than the 32 MiB array.  The size is checked before the pointers, so the call reports
+    it with every pointer null; with null pointers no call of this test can launch."""
     lib = lz.load()
-    dims = lz.make_dims(37, 4096, 32, 8, 128, 128, 64, 4, lz.LIZARD_BF16)
-    fake = ctypes.c_void_p(0x100000)
-    st = lib.lizard_attn_fwd_noalloc(ctypes.byref(dims), *([fake] * 7), None, None, None, None,
-                                     None, None)
+    dims = lz.make_dims(37, 4096, 32, 8, 128, 128, 64, 4, torch.float32)
+    st = lib.lizard_attn_fwd_noalloc(ctypes.byref(dims), *([None] * 13))
     assert st == lz.LIZARD_ERR_WORKSPACE
+    # a problem that fits is refused for its null pointers, again before any launch
+    small = lz.make_dims(1, 256, 4, 2, 128, 128, 64, 4, torch.bfloat16)
+    st = lib.lizard_attn_fwd_noalloc(ctypes.byref(small), *([None] * 13))
+    assert st == lz.LIZARD_ERR_INVALID_ARG
