@@ -32,6 +32,12 @@ __device__ __forceinline__ void cp16(void* dst, const void* src) {
                  "l"(src)
                  : "memory");
 }
+__device__ __forceinline__ void cp4(void* dst, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
 __device__ __forceinline__ void cp_wait_all() {
     asm volatile("cp.async.wait_all;" ::: "memory");
 }
@@ -58,7 +64,8 @@ struct DecLay {
     static constexpr int oS = oGam + DF * 4;                     // window scores [G][WMAX]
     static constexpr int oRed = oS + GMAX * WMAX * 4;            // partials [NRG][G][DH]
     static constexpr int oRow = oRed + NRG * GMAX * DH * 4;      // per head m, l, den_gla, sinks
-    static constexpr int bytes = oRow + GMAX * 4 * 4;
+    static constexpr int oSk = oRow + GMAX * 4 * 4;              // sink logits [G][M]
+    static constexpr int bytes = oSk + GMAX * 64 * 4;
 };
 
 template <typename T, int DH, int DF, int WMAX>
@@ -78,6 +85,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
     float* sS = (float*)(sm + Ly::oS);
     float* sRed = (float*)(sm + Ly::oRed);
     float* sRow = (float*)(sm + Ly::oRow);
+    float* sSk = (float*)(sm + Ly::oSk);
 
     const int64_t unit = blockIdx.x;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
@@ -131,6 +139,8 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
         const float* zr = a.z + unit * DF;
         for (int e = tid; e < DF * 4 / 16; e += NT) cp16((char*)sZ + 16 * e, (const char*)zr + 16 * e);
     }
+    // the sink logits of the group's heads (read in step 6)
+    for (int e = tid; e < G * (int)p.M; e += NT) cp4(sSk + e, a.sinks + kv * G * p.M + e);
     cp_wait_all();
     __syncthreads();
 
@@ -277,9 +287,8 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
 
     // 6. per head: shift m, window weights, state denominator, sink sum (one warp per head)
     for (int hh = warp; hh < G; hh += NT / 32) {
-        const int64_t h = kv * G + hh;
         float m = kMinShift;
-        for (int mm = 0; mm < p.M; ++mm) m = fmaxf(m, a.sinks[h * p.M + mm]);
+        for (int mm = 0; mm < p.M; ++mm) m = fmaxf(m, sSk[hh * p.M + mm]);
         for (int jj = lane; jj < nkeys; jj += 32) m = fmaxf(m, sS[hh * WMAX + jj]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -297,7 +306,7 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
             gd += __shfl_xor_sync(0xffffffffu, gd, o);
         }
         float ssum = 0.0f;
-        for (int mm = 0; mm < p.M; ++mm) ssum += expf(a.sinks[h * p.M + mm] - m);
+        for (int mm = 0; mm < p.M; ++mm) ssum += expf(sSk[hh * p.M + mm] - m);
         if (lane == 0) {
             sRow[hh * 4 + 0] = m;
             sRow[hh * 4 + 1] = l;
@@ -341,13 +350,18 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
         st(yo + 1, (Em * num1 + wv1) * inv);
     }
 
-    // 8. the new token joins the ring (slot pos mod (w+1), never read in this step)
-    T* kco = (T*)a.kc;
-    T* vco = (T*)a.vc;
-    for (int cc = tid; cc < DH; cc += NT) {
-        const int64_t dst = (unit * R + pos % R) * DH + cc;
-        kco[dst] = knew[cc];
-        vco[dst] = vnew[cc];
+    // 8. the new token joins the ring (slot pos mod (w+1), never read in this step), from its
+    //    staged copy (the last key and value of the window)
+    {
+        constexpr int cpr = DH * E / 16;
+        const unsigned char* kn = sm + Ly::oK + (nkeys - 1) * Ly::KROW;
+        const unsigned char* vn = sm + Ly::oV + (nkeys - 1) * DH * E;
+        char* kd = (char*)((T*)a.kc + (unit * R + pos % R) * DH);
+        char* vd = (char*)((T*)a.vc + (unit * R + pos % R) * DH);
+        for (int ch = tid; ch < cpr; ch += NT) {
+            *reinterpret_cast<uint4*>(kd + 16 * ch) = *reinterpret_cast<const uint4*>(kn + 16 * ch);
+            *reinterpret_cast<uint4*>(vd + 16 * ch) = *reinterpret_cast<const uint4*>(vn + 16 * ch);
+        }
     }
 }
 
