@@ -327,6 +327,7 @@ def run_ours(args, rank, world, device):
     # --- end to end through the public API with host buffers
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = y.numel() * y.element_size()
+    # (a) one request alone: copy in, forward, copy out, one after the other
     ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(args.steps)]
     for _ in range(max(1, args.warmup // 2)):
@@ -346,7 +347,54 @@ def run_ours(args, rank, world, device):
         e1.record(stream)
     torch.cuda.synchronize()
     barrier()
-    e2e_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev2) / args.steps)
+    lat_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev2) / args.steps)
+    # (b) a stream of requests: each step's inputs copied in from pinned host memory and its
+    #     output copied back, every copy inside the timed region; the copies of neighbouring
+    #     steps overlap the forward on their own streams (two device buffer sets, so no copy
+    #     overwrites what a running forward reads).  Inputs and output of a step (185 MB) are
+    #     larger than L2, so no flush between steps.
+    s_in, s_out = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    devs = [dev, {n: torch.empty_like(t) for n, t in dev.items()}]
+    ys = [y, torch.empty_like(y)]
+    yhs = [y_host, torch.empty(y.shape, dtype=y.dtype).pin_memory()]
+
+    def requests(nsteps):
+        ev_in = [torch.cuda.Event() for _ in range(nsteps)]
+        ev_comp = [torch.cuda.Event() for _ in range(nsteps)]
+        ev_out = [torch.cuda.Event() for _ in range(nsteps)]
+        s_in.wait_stream(stream)
+        s_out.wait_stream(stream)
+        for i in range(nsteps):
+            bi = i & 1
+            with torch.cuda.stream(s_in):
+                if i >= 2:
+                    s_in.wait_event(ev_comp[i - 2])  # buffer set bi is no longer read
+                for n in host:
+                    devs[bi][n].copy_(host[n], non_blocking=True)
+                ev_in[i].record(s_in)
+            stream.wait_event(ev_in[i])
+            if i >= 2:
+                stream.wait_event(ev_out[i - 2])  # ys[bi] has been copied out
+            lz.lizard_attn_fwd(devs[bi]["q"], devs[bi]["k"], devs[bi]["v"], devs[bi]["g"],
+                               devs[bi]["Wf"], devs[bi]["sinks"], wl.w, y=ys[bi], workspace=ws)
+            ev_comp[i].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_comp[i])
+                yhs[bi].copy_(ys[bi], non_blocking=True)
+                ev_out[i].record(s_out)
+        stream.wait_stream(s_in)
+        stream.wait_stream(s_out)
+
+    requests(max(2, args.warmup))
+    torch.cuda.synchronize()
+    barrier()
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r0.record(stream)
+    requests(args.steps)
+    r1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    e2e_ms = max_over_ranks(r0.elapsed_time(r1) / args.steps)
 
     # --- decode at B=64 after a prefill, 1024 steps captured in one CUDA graph
     decode = None
@@ -380,7 +428,10 @@ def run_ours(args, rank, world, device):
                      "flops": fwd_algorithmic_flops(wl),
                      "tflops_achieved": fwd_algorithmic_flops(wl) / (kern_ms * 1e-3) / 1e12},
         "e2e": {"value": world * tokens / (e2e_ms * 1e-3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "mode": "a stream of requests through lizard_attn_fwd: pinned host inputs in, "
+                        "output back, copies of neighbouring steps overlapping the forward",
+                "single_request_ms": lat_ms},
         "gpu_launches": args.steps * launches_per_fwd,
         "clocks": clocks,
     }
