@@ -941,7 +941,7 @@ __global__ void __launch_bounds__(NT, 1)
     bwd_fwalk_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDY,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
-                 Plan p, BwdArgs a, const float* rows, const float* fwd_rec, float* dB, float* dWp,
+                 const __grid_constant__ CUtensorMap tmDQ, Plan p, BwdArgs a, const float* rows, const float* fwd_rec, float* dB, float* dWp,
                  float* dtp) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
@@ -1065,6 +1065,9 @@ __global__ void __launch_bounds__(NT, 1)
                 bt[t] = run;
             }
             xa[gq * 128 + gf] = run;
+            // the previous step's dq tile has left the state-copy buffer before phase (3)
+            // writes it again (the barrier orders this for every thread)
+            if (tid == 0) bulk_wait_read();
             __syncthreads();
             const float g0 = xa[gf], g1 = xa[128 + gf], g2 = xa[256 + gf], g3 = xa[384 + gf];
             const float bref = g0 + g1, blast = bref + g2 + g3;
@@ -1417,25 +1420,27 @@ __global__ void __launch_bounds__(NT, 1)
             }
         }
         {
+            // the dq tile (state part) through the idle state-copy buffer and one TMA store;
+            // rows past the end of the sequence fall outside the tensor and are dropped
             float v[32];
             tmem_ld32(tb + lane_off + fDQ + 32 * part, v);
             tmem_wait_ld();
-            if (rv) {
-                __nv_bfloat16* dq = (__nv_bfloat16*)a.dq + ridx * DH + 32 * part;
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint4 w;
-                    w.x = pack_bf16(v[8 * ch], v[8 * ch + 1]);
-                    w.y = pack_bf16(v[8 * ch + 2], v[8 * ch + 3]);
-                    w.z = pack_bf16(v[8 * ch + 4], v[8 * ch + 5]);
-                    w.w = pack_bf16(v[8 * ch + 6], v[8 * ch + 7]);
-                    *reinterpret_cast<uint4*>(dq + 8 * ch) = w;
-                }
-            }
+            for (int ch = 0; ch < 4; ++ch)
+                st_shared_v4(base + wHh + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                             pack_bf16(v[8 * ch], v[8 * ch + 1]), pack_bf16(v[8 * ch + 2], v[8 * ch + 3]),
+                             pack_bf16(v[8 * ch + 4], v[8 * ch + 5]), pack_bf16(v[8 * ch + 6], v[8 * ch + 7]));
         }
+        fence_async_smem();
         tc_fence_before();
         __syncthreads();
+        if (tid == 0) {
+            tma_store_4d(&tmDQ, sm + wHh, 0, (int)(kv * GQ), (int)t0, (int)b);
+            tma_store_4d(&tmDQ, sm + wHh + 16384, 64, (int)(kv * GQ), (int)t0, (int)b);
+            bulk_commit();
+        }
     }
+    if (tid == 0) bulk_wait_all();  // the last dq tiles have left shared memory
 
     if (ok) {
         // dWf partial of the segment (lane = d, 16 feature columns per part) and dt partials
@@ -2131,7 +2136,7 @@ bool bwd_win_tc_supported(const Plan& p) {
 cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
                                 size_t o_fwd, size_t o_dB, size_t o_dW, size_t o_dt,
                                 cudaStream_t s) {
-    alignas(64) CUtensorMap mq, md, mk, mv, mw, mg;
+    alignas(64) CUtensorMap mq, md, mk, mv, mw, mg, mdq;
     const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
                      Hkv = (cuuint64_t)p.Hkv;
     {
@@ -2140,6 +2145,7 @@ cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, siz
         const cuuint32_t box[4] = {64, GQ, CT, 1};
         if (!tc::make_map(&mq, a.q, 4, dims, str, box)) return cudaErrorInvalidValue;
         if (!tc::make_map(&md, a.dy, 4, dims, str, box)) return cudaErrorInvalidValue;
+        if (!tc::make_map(&mdq, a.dq, 4, dims, str, box)) return cudaErrorInvalidValue;
     }
     {
         const cuuint64_t dims[4] = {DH, Hkv, L, B};
@@ -2164,7 +2170,7 @@ cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, siz
                                          (int)kSmemFW);
     if (e != cudaSuccess) return e;
     bwd_fwalk_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemFW, s>>>(
-        mq, md, mk, mv, mw, mg, p, a, wsf + o_rows, wsf + o_fwd, wsf + o_dB, wsf + o_dW,
+        mq, md, mk, mv, mw, mg, mdq, p, a, wsf + o_rows, wsf + o_fwd, wsf + o_dB, wsf + o_dW,
         wsf + o_dt);
     return cudaGetLastError();
 }
