@@ -105,10 +105,6 @@ constexpr float kEm80 = 1.8048513878454153e-35f;  // e^-80
 // XOR-swizzled by t, so rows read by neighbouring tokens fall in different banks.
 __device__ __forceinline__ int eidx(int t, int f) { return t * DF + (((f >> 3) ^ (t & 7)) << 3) + (f & 7); }
 
-// log sigmoid(x) = min(x, 0) - log(1 + e^{-|x|}); the argument of the log is in (1, 2].
-__device__ __forceinline__ float log_sigmoid_fast(float x) {
-    return fminf(x, 0.0f) - __logf(1.0f + __expf(-fabsf(x)));
-}
 
 // Barrier among the 128 math threads (4 warps) that share one TMEM lane quadrant.
 __device__ __forceinline__ void quad_sync(int quad) {
@@ -957,36 +953,47 @@ __global__ void __launch_bounds__(NL, 1)
             mma_out = true;
         }
         // (2) gates: four threads per feature, 32 tokens each; decay of each token's key to the
-        //     step end, e^{b_last - b_t} (at most 1), and of the old state, e^{b_last}
+        //     step end, e^{b_last - b_t} (at most 1), and of the old state, e^{b_last}.  Both are
+        //     products of Gamma = 1 / (1 + e^{-g}): suffix products inside the thread's quarter
+        //     times the later quarters' products.  The step's log-decay (for the records) comes
+        //     from the quarter products renormalised every 4 tokens, one logarithm per thread.
         ok = local_wait(&S.bar_g, ph_g, S, hdr, 21);
         if (!ok) break;
         if (tid == 0) g_out = false;
         {
             const int gf = tid & (DF - 1), gq = tid >> 7;
             const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + lG);
-            float bt[32];
-            float run = 0.0f;
+            float suf[32];       // prod_{s = t+1 .. quarter end} Gamma_s
+            float sp = 1.0f;     // running suffix product
+            float mq = 1.0f;     // the same product, renormalised: mq 2^{eq}
+            int eq = 0;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 31; j >= 0; --j) {
                 const int tt = 32 * gq + j;
-                run += tt < n ? log_sigmoid_fast(__bfloat162float(sg[tt * DF + gf])) : 0.0f;
-                bt[j] = run;
+                const float gam =
+                    tt < n ? rcpf(1.0f + ex2f(-__bfloat162float(sg[tt * DF + gf]) * kLog2e)) : 1.0f;
+                suf[j] = sp;
+                sp *= gam;
+                mq *= gam;
+                if ((j & 3) == 0) {
+                    int e;
+                    mq = frexpf(mq, &e);
+                    eq += e;
+                }
             }
-            gpart[gq * DF + gf] = run;
+            gpart[gq * DF + gf] = sp;                                // the quarter's product
+            zq[gq * DF + gf] = (__log2f(mq) + (float)eq) * kLn2;     // and its logarithm
             __syncthreads();
-            const float g0 = gpart[gf], g1 = gpart[DF + gf], g2 = gpart[2 * DF + gf],
-                        g3 = gpart[3 * DF + gf];
-            const float blast = (g0 + g1) + (g2 + g3);
-            const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? g0 + g1 : (g0 + g1) + g2;
-            const float cst = (blast - off) * kLog2e;
+            const float q1 = gpart[DF + gf], q2 = gpart[2 * DF + gf], q3 = gpart[3 * DF + gf];
+            const float later = gq == 3 ? 1.0f : gq == 2 ? q3 : gq == 1 ? q2 * q3 : (q1 * q2) * q3;
             // kept in fp32: the state records feed the gate gradient, a difference of two
             // nearly equal sums that bf16 weights would not cancel consistently
             float* Ek = (float*)(sm + lE);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) Ek[(32 * gq + j) * EKR + gf] = ex2f(fmaf(-bt[j], kLog2e, cst));
+            for (int j = 0; j < 32; ++j) Ek[(32 * gq + j) * EKR + gf] = suf[j] * later;
             if (gq == 0) {
-                S.el[gf] = ex2f(blast * kLog2e);
-                lam_tot += blast;
+                S.el[gf] = gpart[gf] * ((q1 * q2) * q3);
+                lam_tot += (zq[gf] + zq[DF + gf]) + (zq[2 * DF + gf] + zq[3 * DF + gf]);
             }
         }
         __syncthreads();
