@@ -115,4 +115,4 @@ def test_kernel_path_query(lib):
     assert lz.lizard_attn_fwd_kernel(dims(Hq=30)) == -1
     assert lz.lizard_attn_fwd_kernel(dims(dtype=lz.LIZARD_F32)) == 0
     assert lz.lizard_attn_fwd_kernel(dims(w=32)) == 0
-    assert lz.lizard_attn_fwd_kernel(dims()) in (0, 1)  # 1 where the driver's TMA encoder exists
+    assert lz.lizard_attn_fwd_kernel(dims()) in (0, 1)  # 1 where the CUDA driver's TMA encoder exists
