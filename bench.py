@@ -395,6 +395,12 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     barrier()
     e2e_ms = max_over_ranks(r0.elapsed_time(r1) / args.steps)
+    # the overlapped requests must return exactly what a lone forward returns (the kernels are
+    # deterministic): a race between a copy and a running forward would show here
+    fwd()
+    torch.cuda.synchronize()
+    if not torch.equal(yhs[(args.steps - 1) & 1], y.cpu()):
+        raise RuntimeError("end-to-end requests returned a different y than a lone forward")
 
     # --- decode at B=64 after a prefill, 1024 steps captured in one CUDA graph
     decode = None
