@@ -368,7 +368,8 @@ __global__ void __launch_bounds__(NT, 1)
     // coalesced 16-byte loads, and each row's 16-byte chunks XOR-swizzled by the row so the
     // per-row reads below are free of bank conflicts.
     const float* rec =
-        seg > 0 ? a.seg + ((size_t)seg * (size_t)U + (size_t)unit) * p.rec_floats : nullptr;
+        seg > 0 ? a.seg + ((size_t)(seg * p.rec_step) * (size_t)U + (size_t)unit) * p.rec_floats
+                : nullptr;
     if (rec != nullptr) stage_record_in(sm + oK, rec);
     if (tid < DF) S.z[tid] = rec ? rec[DF * DH + tid] : 0.0f;
     __syncthreads();
@@ -1214,7 +1215,21 @@ cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s
 
 // Segments are cut so that the last wave of (batch, KV head, segment) CTAs is as full as the
 // others: a second, mostly empty wave would cost a whole segment's walk.
-void fwd_tc_plan(Plan* p) { plan_segments_waves(p, 152); }
+//
+// With few segments the segment pass (one CTA per unit and segment but the last) would leave
+// SMs idle, so its records are cut rec_step times finer while one wave still holds them: the
+// scan then yields the state at every finer boundary and the main walk reads every
+// rec_step-th record.
+void fwd_tc_plan(Plan* p) {
+    plan_segments_waves(p, 152);
+    p->rec_step = 1;
+    if (p->P <= 1) return;
+    const int64_t U = p->B * p->Hkv;
+    for (int64_t k = 2; k <= 8; ++k) {
+        if (U * k * (p->P - 1) > 152 || k * (p->P - 1) + 1 > p->Pmax) break;
+        if (p->seg_chunks % k == 0) p->rec_step = k;
+    }
+}
 
 cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     Plan p = p0;
@@ -1255,7 +1270,13 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const unsigned U = (unsigned)(p.B * p.Hkv);
     if (p.P > 1) {
-        e = launch_local_and_scan(p, a, mw, s);
+        // the segment pass and the scan over rec_step finer cuts of every segment but the last
+        Plan pl = p;
+        pl.seg_chunks = p.seg_chunks / p.rec_step;
+        pl.seg_len = pl.seg_chunks * kChunk;
+        pl.P = p.rec_step * (p.P - 1) + 1;
+        pl.rec_step = 1;
+        e = launch_local_and_scan(pl, a, mw, s);
         if (e != cudaSuccess) return e;
     }
     if (a.ev_before) cudaEventRecord(a.ev_before, s);

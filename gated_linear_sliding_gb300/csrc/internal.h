@@ -23,6 +23,7 @@ struct Plan {
     int dtype;
     int64_t nchunks, seg_chunks, seg_len, P, Pmax;
     size_t rec_floats;   // floats per (segment, unit) record: D*d + D + D
+    int64_t rec_step;    // boundary records per segment: the segment pass may cut finer
 };
 
 bool make_plan(const lizard_dims* dims, Plan* p);

@@ -37,6 +37,7 @@ bool make_plan(const lizard_dims* dims, Plan* p) {
     if (pmax > 64) pmax = 64;
     p->Pmax = pmax;
     p->rec_floats = (size_t)(d.D * d.d + 2 * d.D);
+    p->rec_step = 1;
     plan_segments(p, kTargetUnits);
     return true;
 }

@@ -62,7 +62,9 @@ extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const 
     if (fwd_tc_supported(p)) fwd_tc_plan(&pl);
     const size_t need =
         kHeaderBytes +
-        (pl.P > 1 ? sizeof(float) * (size_t)pl.P * (size_t)(p.B * p.Hkv) * p.rec_floats : 0);
+        (pl.P > 1 ? sizeof(float) * (size_t)(pl.rec_step * (pl.P - 1) + 1) *
+                        (size_t)(p.B * p.Hkv) * p.rec_floats
+                  : 0);
     if (need > kNoAllocScratchBytes) return LIZARD_ERR_WORKSPACE;
     if (!q || !k || !v || !g || !Wf || !y || (p.M > 0 && !sinks)) return LIZARD_ERR_INVALID_ARG;
     const void* ptrs[] = {q, k, v, g, Wf, sinks, y, lse, S_out, z_out, kcache_out, vcache_out};
