@@ -173,6 +173,57 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
     return from_cuda(e);
 }
 
+lizard_status lizard_attn_fwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,
+                                     const void* q, const void* k, const void* v, const void* g,
+                                     const void* Wf, const float* sinks, void* y, float* lse,
+                                     float* S_out, float* z_out, void* kcache_out,
+                                     void* vcache_out, void* workspace, size_t ws_bytes,
+                                     void* stream) {
+    if (dims == nullptr || cu_seqlens == nullptr || dims->B < 1 || dims->L < 0)
+        return LIZARD_ERR_INVALID_ARG;
+    const int64_t nseq = dims->B, T = dims->L;
+    if (cu_seqlens[0] != 0 || cu_seqlens[nseq] != T) return LIZARD_ERR_INVALID_ARG;
+    for (int64_t i = 0; i < nseq; ++i)
+        if (cu_seqlens[i + 1] < cu_seqlens[i]) return LIZARD_ERR_INVALID_ARG;
+    // every sequence is a B = 1 problem; its workspace does not depend on its length
+    lizard_dims d1 = *dims;
+    d1.B = 1;
+    d1.L = T > 0 ? T : 1;
+    Plan p;
+    if (!make_plan(&d1, &p)) return LIZARD_ERR_INVALID_ARG;
+    if (workspace == nullptr || ws_bytes < fwd_workspace_bytes(p)) return LIZARD_ERR_WORKSPACE;
+    const size_t E = d1.dtype == LIZARD_F32 ? 4 : 2;
+    const size_t qrow = (size_t)(d1.Hq * d1.d) * E, krow = (size_t)(d1.Hkv * d1.d) * E,
+                 grow = (size_t)(d1.Hkv * d1.D) * E;
+    const size_t Sun = (size_t)(d1.Hkv * d1.D * d1.d), zun = (size_t)(d1.Hkv * d1.D),
+                 cun = (size_t)(d1.Hkv * (d1.w + 1) * d1.d) * E;
+    cudaStream_t s = (cudaStream_t)stream;
+    for (int64_t i = 0; i < nseq; ++i) {
+        const int64_t t0 = cu_seqlens[i], n = cu_seqlens[i + 1] - t0;
+        float* Si = S_out ? S_out + (size_t)i * Sun : nullptr;
+        float* zi = z_out ? z_out + (size_t)i * zun : nullptr;
+        char* kci = kcache_out ? (char*)kcache_out + (size_t)i * cun : nullptr;
+        char* vci = vcache_out ? (char*)vcache_out + (size_t)i * cun : nullptr;
+        if (n == 0) {  // an empty sequence: zero state, empty caches
+            cudaError_t e = cudaSuccess;
+            if (Si) e = cudaMemsetAsync(Si, 0, Sun * sizeof(float), s);
+            if (e == cudaSuccess && zi) e = cudaMemsetAsync(zi, 0, zun * sizeof(float), s);
+            if (e == cudaSuccess && kci) e = cudaMemsetAsync(kci, 0, cun, s);
+            if (e == cudaSuccess && vci) e = cudaMemsetAsync(vci, 0, cun, s);
+            if (e != cudaSuccess) return from_cuda(e);
+            continue;
+        }
+        d1.L = n;
+        const lizard_status st = lizard_attn_fwd(
+            &d1, (const char*)q + t0 * qrow, (const char*)k + t0 * krow,
+            (const char*)v + t0 * krow, (const char*)g + t0 * grow, Wf, sinks,
+            (char*)y + t0 * qrow, lse ? lse + t0 * d1.Hq : nullptr, Si, zi, kci, vci, workspace,
+            ws_bytes, stream);
+        if (st != LIZARD_OK) return st;
+    }
+    return LIZARD_OK;
+}
+
 size_t lizard_attn_bwd_workspace(const lizard_dims* dims) {
     Plan p;
     if (!make_plan(dims, &p)) return 0;

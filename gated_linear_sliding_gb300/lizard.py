@@ -10,6 +10,8 @@ from __future__ import annotations
 import ctypes
 import os
 
+import numpy as np
+
 import torch
 
 from . import _build
@@ -28,7 +30,7 @@ EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_f
             "lizard_decode_step", "lizard_decode_step_positions", "lizard_read_device_status",
             "lizard_status_string",
             "lizard_profile_events", "lizard_version", "lizard_attn_fwd_noalloc",
-            "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout"]
+            "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout", "lizard_attn_fwd_varlen"]
 
 
 class lizard_dims(ctypes.Structure):
@@ -73,6 +75,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_workspace_init.restype = ctypes.c_int
     lib.lizard_attn_fwd.argtypes = [_DP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_fwd.restype = ctypes.c_int
+    lib.lizard_attn_fwd_varlen.argtypes = [_DP, _VP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
+    lib.lizard_attn_fwd_varlen.restype = ctypes.c_int
     lib.lizard_attn_fwd_noalloc.argtypes = [_DP] + [_VP] * 13
     lib.lizard_attn_fwd_noalloc.restype = ctypes.c_int
     lib.lizard_attn_bwd.argtypes = [_DP] + [_VP] * 16 + [ctypes.c_size_t, _VP]
@@ -229,6 +233,46 @@ def lizard_attn_fwd(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0, y=None
                                 _p(vcache_out), _p(workspace), workspace.numel(),
                                 _stream(stream))
     _check(st, "lizard_attn_fwd")
+    return y
+
+
+def lizard_attn_fwd_varlen(q, k, v, g, Wf, sinks, w: int, cu_seqlens, *, scale: float = 0.0,
+                           y=None, lse=None, S_out=None, z_out=None, kcache_out=None,
+                           vcache_out=None, workspace=None, stream=None):
+    """Forward over a packed batch: q [T, Hq, d], k, v [T, Hkv, d], g [T, Hkv, D], and
+    cu_seqlens (host integers, B + 1 offsets) delimiting B sequences.  Returns y [T, Hq, d];
+    S_out, z_out, kcache_out, vcache_out hold one entry per sequence."""
+    T, Hq, d = q.shape
+    Hkv, D, M = k.shape[1], g.shape[-1], sinks.shape[1]
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    nseq = cu.shape[0] - 1
+    dt = q.dtype
+    _need(q, "q", (T, Hq, d), dt)
+    _need(k, "k", (T, Hkv, d), dt)
+    _need(v, "v", (T, Hkv, d), dt)
+    _need(g, "g", (T, Hkv, D), dt)
+    _need(Wf, "Wf", (Hkv, d, D // 2), dt)
+    _need(sinks, "sinks", (Hq, M), torch.float32)
+    if y is None:
+        y = torch.empty_like(q)
+    _need(y, "y", (T, Hq, d), dt)
+    if lse is not None:
+        _need(lse, "lse", (T, Hq), torch.float32)
+    if S_out is not None:
+        _need(S_out, "S_out", (nseq, Hkv, D, d), torch.float32)
+        _need(z_out, "z_out", (nseq, Hkv, D), torch.float32)
+    if kcache_out is not None:
+        _need(kcache_out, "kcache_out", (nseq, Hkv, w + 1, d), dt)
+        _need(vcache_out, "vcache_out", (nseq, Hkv, w + 1, d), dt)
+    dims = lizard_dims(nseq, T, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    if workspace is None:
+        one = lizard_dims(1, max(T, 1), Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+        workspace = new_workspace(lizard_attn_fwd_workspace(one), q.device, stream)
+    st = load().lizard_attn_fwd_varlen(ctypes.byref(dims), cu.ctypes.data, _p(q), _p(k), _p(v),
+                                       _p(g), _p(Wf), _p(sinks), _p(y), _p(lse), _p(S_out),
+                                       _p(z_out), _p(kcache_out), _p(vcache_out), _p(workspace),
+                                       workspace.numel(), _stream(stream))
+    _check(st, "lizard_attn_fwd_varlen")
     return y
 
 

@@ -100,6 +100,28 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
                               void* y, float* lse, float* S_out, float* z_out, void* kcache_out,
                               void* vcache_out, void* workspace, size_t ws_bytes, void* stream);
 
+/* The forward over a packed batch of sequences of different lengths (variable-length
+ * batching).  dims.B is the number of sequences and dims.L the total number of tokens T;
+ * cu_seqlens is a HOST array of B + 1 offsets (cu_seqlens[0] = 0, non-decreasing,
+ * cu_seqlens[B] = T): sequence i is tokens [cu_seqlens[i], cu_seqlens[i+1]).
+ *   q, y [T, Hq, d]; k, v [T, Hkv, d]; g [T, Hkv, D]; lse (nullable) [T, Hq] fp32; the
+ *   packed layouts are those of lizard_attn_fwd with B = 1 and L = T.
+ *   S_out, z_out, kcache_out, vcache_out (nullable, in pairs) hold one entry per sequence:
+ *   [B, Hkv, D, d], [B, Hkv, D], [B, Hkv, w+1, d]; an empty sequence gets a zero state.
+ *   workspace, ws_bytes >= lizard_attn_fwd_workspace with dims.B = 1 (any L).
+ * Each sequence's results equal lizard_attn_fwd on that sequence alone: no state, window
+ * or token crosses a sequence boundary.  The sequences run one after another on `stream`,
+ * each cut into segments on its own, so long sequences fill the GPU and many short ones are
+ * bound by launches.  Every sequence's slice must meet lizard_attn_fwd's 16-byte alignment
+ * (for lse: Hq * 4 * cu_seqlens[i] a multiple of 16, true whenever Hq >= 4); errors are those
+ * of lizard_attn_fwd, plus LIZARD_ERR_INVALID_ARG for inconsistent offsets. */
+lizard_status lizard_attn_fwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,
+                                     const void* q, const void* k, const void* v, const void* g,
+                                     const void* Wf, const float* sinks, void* y, float* lse,
+                                     float* S_out, float* z_out, void* kcache_out,
+                                     void* vcache_out, void* workspace, size_t ws_bytes,
+                                     void* stream);
+
 /* The forward for callers that cannot allocate device memory.  The Lizard pages have
  * no counterpart to this entry point; it exists for the integration.
  *

@@ -116,3 +116,17 @@ def test_kernel_path_query(lib):
     assert lz.lizard_attn_fwd_kernel(dims(dtype=lz.LIZARD_F32)) == 0
     assert lz.lizard_attn_fwd_kernel(dims(w=32)) == 0
     assert lz.lizard_attn_fwd_kernel(dims()) in (0, 1)  # 1 where the CUDA driver's TMA encoder exists
+
+
+def test_varlen_offsets_validated_before_any_launch(lib):
+    """lizard_attn_fwd_varlen refuses inconsistent offsets on the host; every tensor pointer
+    here is null, so no call can reach a launch."""
+    d = dims(L=10)
+    d.B = 2
+    nul = [None] * 13
+    for cu in ([0, 4, 9], [1, 4, 10], [0, 6, 4, 10][:3], [0, 11, 10]):
+        arr = (ctypes.c_int64 * len(cu))(*cu)
+        st = lib.lizard_attn_fwd_varlen(ctypes.byref(d), arr, *nul, 1 << 30, None)
+        assert st == lz.LIZARD_ERR_INVALID_ARG
+    assert lib.lizard_attn_fwd_varlen(ctypes.byref(d), None, *nul, 1 << 30, None) == \
+        lz.LIZARD_ERR_INVALID_ARG
