@@ -270,6 +270,88 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* q, const void
     return from_cuda(launch_bwd(p, a, (cudaStream_t)stream));
 }
 
+// Packed-batch backward: dst = src (first sequence) or dst += src (the others), fixed order.
+__global__ void add_or_copy(float* dst, const float* src, size_t n, int first) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = first ? src[i] : dst[i] + src[i];
+}
+
+static bool varlen_offsets_ok(const lizard_dims* dims, const int64_t* cu) {
+    if (dims == nullptr || cu == nullptr || dims->B < 1 || dims->L < 0) return false;
+    if (cu[0] != 0 || cu[dims->B] != dims->L) return false;
+    for (int64_t i = 0; i < dims->B; ++i)
+        if (cu[i + 1] < cu[i]) return false;
+    return true;
+}
+
+// The largest B = 1 backward workspace over the sequences, 256-byte aligned, then the
+// per-sequence dWf and dsinks.
+static size_t bwd_varlen_main_bytes(const lizard_dims* dims, const int64_t* cu) {
+    lizard_dims d1 = *dims;
+    d1.B = 1;
+    d1.L = 1;
+    for (int64_t i = 0; i < dims->B; ++i) d1.L = cu[i + 1] - cu[i] > d1.L ? cu[i + 1] - cu[i] : d1.L;
+    Plan p;
+    if (!make_plan(&d1, &p)) return 0;
+    return (bwd_workspace_bytes(p) + 255) & ~(size_t)255;
+}
+
+size_t lizard_attn_bwd_varlen_workspace(const lizard_dims* dims, const int64_t* cu_seqlens) {
+    if (!varlen_offsets_ok(dims, cu_seqlens)) return 0;
+    const size_t main = bwd_varlen_main_bytes(dims, cu_seqlens);
+    if (main == 0) return 0;
+    const size_t nW = (size_t)(dims->Hkv * dims->d * (dims->D / 2)), nt = (size_t)(dims->Hq * dims->M);
+    return main + ((nW * 4 + 255) & ~(size_t)255) + ((nt * 4 + 255) & ~(size_t)255);
+}
+
+lizard_status lizard_attn_bwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,
+                                     const void* q, const void* k, const void* v, const void* g,
+                                     const void* Wf, const float* sinks, const void* y,
+                                     const float* lse, const void* dy, void* dq, void* dk,
+                                     void* dv, void* dg, float* dWf, float* dsinks,
+                                     void* workspace, size_t ws_bytes, void* stream) {
+    if (!varlen_offsets_ok(dims, cu_seqlens)) return LIZARD_ERR_INVALID_ARG;
+    const size_t need = lizard_attn_bwd_varlen_workspace(dims, cu_seqlens);
+    if (need == 0) return LIZARD_ERR_INVALID_ARG;
+    if (workspace == nullptr || ws_bytes < need) return LIZARD_ERR_WORKSPACE;
+    if (dWf == nullptr || (dims->M > 0 && dsinks == nullptr)) return LIZARD_ERR_INVALID_ARG;
+    const size_t main = bwd_varlen_main_bytes(dims, cu_seqlens);
+    const size_t nW = (size_t)(dims->Hkv * dims->d * (dims->D / 2)), nt = (size_t)(dims->Hq * dims->M);
+    float* tW = (float*)((char*)workspace + main);
+    float* tt = (float*)((char*)workspace + main + ((nW * 4 + 255) & ~(size_t)255));
+    lizard_dims d1 = *dims;
+    d1.B = 1;
+    const size_t E = d1.dtype == LIZARD_F32 ? 4 : 2;
+    const size_t qrow = (size_t)(d1.Hq * d1.d) * E, krow = (size_t)(d1.Hkv * d1.d) * E,
+                 grow = (size_t)(d1.Hkv * d1.D) * E;
+    cudaStream_t s = (cudaStream_t)stream;
+    bool first = true;
+    for (int64_t i = 0; i < dims->B; ++i) {
+        const int64_t t0 = cu_seqlens[i], n = cu_seqlens[i + 1] - t0;
+        if (n == 0) continue;  // no tokens: no gradient slice, nothing to add
+        d1.L = n;
+        const lizard_status st = lizard_attn_bwd(
+            &d1, (const char*)q + t0 * qrow, (const char*)k + t0 * krow,
+            (const char*)v + t0 * krow, (const char*)g + t0 * grow, Wf, sinks,
+            (const char*)y + t0 * qrow, lse + t0 * d1.Hq, (const char*)dy + t0 * qrow,
+            (char*)dq + t0 * qrow, (char*)dk + t0 * krow, (char*)dv + t0 * krow,
+            (char*)dg + t0 * grow, tW, dims->M > 0 ? tt : nullptr, workspace, main, stream);
+        if (st != LIZARD_OK) return st;
+        add_or_copy<<<(unsigned)((nW + 255) / 256), 256, 0, s>>>(dWf, tW, nW, first ? 1 : 0);
+        if (dims->M > 0)
+            add_or_copy<<<(unsigned)((nt + 255) / 256), 256, 0, s>>>(dsinks, tt, nt, first ? 1 : 0);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return from_cuda(e);
+        first = false;
+    }
+    if (first) {  // every sequence is empty: zero parameter gradients
+        cudaError_t e = cudaMemsetAsync(dWf, 0, nW * 4, s);
+        if (e == cudaSuccess && dims->M > 0) e = cudaMemsetAsync(dsinks, 0, nt * 4, s);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
+    return LIZARD_OK;
+}
+
 size_t lizard_decode_workspace(const lizard_dims* dims) {
     lizard_dims d1 = dims ? *dims : lizard_dims{};
     d1.L = 1;

@@ -30,7 +30,8 @@ EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_f
             "lizard_decode_step", "lizard_decode_step_positions", "lizard_read_device_status",
             "lizard_status_string",
             "lizard_profile_events", "lizard_version", "lizard_attn_fwd_noalloc",
-            "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout", "lizard_attn_fwd_varlen"]
+            "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout", "lizard_attn_fwd_varlen",
+            "lizard_attn_bwd_varlen_workspace", "lizard_attn_bwd_varlen"]
 
 
 class lizard_dims(ctypes.Structure):
@@ -77,6 +78,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_attn_fwd.restype = ctypes.c_int
     lib.lizard_attn_fwd_varlen.argtypes = [_DP, _VP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_fwd_varlen.restype = ctypes.c_int
+    lib.lizard_attn_bwd_varlen_workspace.argtypes = [_DP, _VP]
+    lib.lizard_attn_bwd_varlen_workspace.restype = ctypes.c_size_t
+    lib.lizard_attn_bwd_varlen.argtypes = [_DP, _VP] + [_VP] * 16 + [ctypes.c_size_t, _VP]
+    lib.lizard_attn_bwd_varlen.restype = ctypes.c_int
     lib.lizard_attn_fwd_noalloc.argtypes = [_DP] + [_VP] * 13
     lib.lizard_attn_fwd_noalloc.restype = ctypes.c_int
     lib.lizard_attn_bwd.argtypes = [_DP] + [_VP] * 16 + [ctypes.c_size_t, _VP]
@@ -331,6 +336,38 @@ def lizard_attn_bwd(q, k, v, g, Wf, sinks, y, lse, dy, w: int, *, scale: float =
                                 _p(dg), _p(dWf), _p(dsinks), _p(workspace), workspace.numel(),
                                 _stream(stream))
     _check(st, "lizard_attn_bwd")
+    return dict(dq=dq, dk=dk, dv=dv, dg=dg, dWf=dWf, dsinks=dsinks)
+
+
+def lizard_attn_bwd_varlen(q, k, v, g, Wf, sinks, y, lse, dy, w: int, cu_seqlens, *,
+                           scale: float = 0.0, workspace=None, stream=None):
+    """Gradients of lizard_attn_fwd_varlen's y against dy for a packed batch: dq, dk, dv,
+    dg packed like the inputs; dWf and dsinks summed over the sequences."""
+    T, Hq, d = q.shape
+    Hkv, D, M = k.shape[1], g.shape[-1], sinks.shape[1]
+    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    nseq = cu.shape[0] - 1
+    dt = q.dtype
+    for t, n, shp in ((q, "q", (T, Hq, d)), (k, "k", (T, Hkv, d)), (v, "v", (T, Hkv, d)),
+                      (g, "g", (T, Hkv, D)), (Wf, "Wf", (Hkv, d, D // 2)),
+                      (y, "y", (T, Hq, d)), (dy, "dy", (T, Hq, d))):
+        _need(t, n, shp, dt)
+    _need(sinks, "sinks", (Hq, M), torch.float32)
+    _need(lse, "lse", (T, Hq), torch.float32)
+    dq, dk, dv, dg = (torch.empty_like(x) for x in (q, k, v, g))
+    dWf = torch.empty(Hkv, d, D // 2, dtype=torch.float32, device=q.device)
+    dsinks = torch.empty(Hq, M, dtype=torch.float32, device=q.device)
+    dims = lizard_dims(nseq, T, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    if workspace is None:
+        nbytes = int(load().lizard_attn_bwd_varlen_workspace(ctypes.byref(dims), cu.ctypes.data))
+        if nbytes == 0:
+            raise ValueError("cu_seqlens: inconsistent offsets")
+        workspace = new_workspace(nbytes, q.device, stream)
+    st = load().lizard_attn_bwd_varlen(ctypes.byref(dims), cu.ctypes.data, _p(q), _p(k), _p(v),
+                                       _p(g), _p(Wf), _p(sinks), _p(y), _p(lse), _p(dy),
+                                       _p(dq), _p(dk), _p(dv), _p(dg), _p(dWf), _p(dsinks),
+                                       _p(workspace), workspace.numel(), _stream(stream))
+    _check(st, "lizard_attn_bwd_varlen")
     return dict(dq=dq, dk=dk, dv=dv, dg=dg, dWf=dWf, dsinks=dsinks)
 
 

@@ -165,6 +165,25 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* q, const void
                               void* dv, void* dg, float* dWf, float* dsinks, void* workspace,
                               size_t ws_bytes, void* stream);
 
+/* Bytes of device workspace lizard_attn_bwd_varlen needs for this packed batch (dims.B
+ * sequences, dims.L tokens in all, host offsets cu_seqlens as for lizard_attn_fwd_varlen):
+ * the largest single-sequence backward workspace plus the per-sequence dWf and dsinks;
+ * 0 for inconsistent offsets. */
+size_t lizard_attn_bwd_varlen_workspace(const lizard_dims* dims, const int64_t* cu_seqlens);
+
+/* Backward of lizard_attn_fwd_varlen: packed q, k, v, g, y, dy, dq, dk, dv, dg [T, ...] and
+ * lse [T, Hq] as in the forward; dWf [Hkv, d, D/2] and dsinks [Hq, M] fp32 are the sums over
+ * the sequences (added in sequence order, so the result is deterministic).  Each sequence's
+ * dq, dk, dv, dg equal lizard_attn_bwd on that sequence alone; sequences run one after
+ * another on `stream`.  workspace >= lizard_attn_bwd_varlen_workspace; errors as for
+ * lizard_attn_bwd, plus LIZARD_ERR_INVALID_ARG for inconsistent offsets. */
+lizard_status lizard_attn_bwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,
+                                     const void* q, const void* k, const void* v, const void* g,
+                                     const void* Wf, const float* sinks, const void* y,
+                                     const float* lse, const void* dy, void* dq, void* dk,
+                                     void* dv, void* dg, float* dWf, float* dsinks,
+                                     void* workspace, size_t ws_bytes, void* stream);
+
 /* Bytes of device workspace lizard_decode_step needs (the status word only). */
 size_t lizard_decode_workspace(const lizard_dims* dims);
 

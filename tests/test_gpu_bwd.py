@@ -129,3 +129,37 @@ def test_bwd_strong_decay_gates(lz, oracle_mod):
     inp = I.make_inputs(wl, L=700, B=1, with_dy=True)
     ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
     check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16")
+
+
+def test_bwd_varlen_packed_batch(lz, oracle_mod):
+    """Backward of a packed batch (sequences of 5, 0, 130 and 700 tokens, Mistral-shaped
+    heads): each sequence's gradients equal its own backward; dWf and dsinks are the sums."""
+    wl = I.MISTRAL_7B_TRAIN
+    lens = [5, 0, 130, 700]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T = int(cu[-1])
+    inp = I.make_inputs(wl.replace(B=1, L=T), with_dy=True)
+    t = to_dev(inp, wl.dtype)
+    pk = {n: t[n][0] for n in ("q", "k", "v", "g", "dy")}
+    lse = torch.empty(T, wl.Hq, dtype=torch.float32, device="cuda")
+    y = lz.lizard_attn_fwd_varlen(pk["q"], pk["k"], pk["v"], pk["g"], t["Wf"], t["sinks"], wl.w,
+                                  cu, lse=lse)
+    gr = lz.lizard_attn_bwd_varlen(pk["q"], pk["k"], pk["v"], pk["g"], t["Wf"], t["sinks"], y,
+                                   lse, pk["dy"], wl.w, cu)
+    torch.cuda.synchronize()
+    out = {n: to_np(v) for n, v in gr.items()}
+    dW = np.zeros_like(out["dWf"], dtype=np.float64)
+    dt = np.zeros_like(out["dsinks"], dtype=np.float64)
+    for i in range(len(lens)):
+        a, b = int(cu[i]), int(cu[i + 1])
+        if b == a:
+            continue
+        one = {n: (arr[:, a:b] if n in ("q", "k", "v", "g", "dy") else arr)
+               for n, arr in inp.items()}
+        ref = oracle_mod.bwd(**{n: x for n, x in one.items() if n != "dy"}, dy=one["dy"], w=wl.w)
+        for n in ("dq", "dk", "dv", "dg"):
+            assert_grad(out[n][a:b][None], ref[n], "bf16", f"{n} of sequence {i}")
+        dW += ref["dWf"]
+        dt += ref["dsinks"]
+    assert_grad(out["dWf"], dW, "bf16", "dWf (sum)")
+    assert_grad(out["dsinks"], dt, "bf16", "dsinks (sum)")
