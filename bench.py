@@ -220,10 +220,25 @@ def run_reference(args, rank, world):
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": workload_config(wl, {"parallelism": "host cores, OpenMP over batch x KV head"}),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                         "sample": sample},
+                         "sample": sample, "host": host_cpu()},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+def host_cpu() -> str:
+    """The host's logical CPU count and model, from /proc/cpuinfo where it names one."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    return f"{os.cpu_count()} logical CPUs" + (f", {model}" if model else "")
 
 
 def cpu_baseline(wl):
@@ -241,7 +256,7 @@ def cpu_baseline(wl):
     t = time.perf_counter() - t0
     return {"value": wl.B * Ls / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
             "sample": f"one float64 pass over the whole workload ({Ls} tokens, all heads; "
-                      f"{t:.1f} s wall)"}
+                      f"{t:.1f} s wall)", "host": host_cpu()}
 
 
 def run_ours(args, rank, world, device):
