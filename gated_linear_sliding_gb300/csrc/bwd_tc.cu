@@ -686,29 +686,41 @@ __global__ void __launch_bounds__(NT, 1)
         if (!ok) break;
         {
             const int gf = tid & 127, gq = tid >> 7;
+            // e^{b_t} = prod_{s <= t} Gamma_s with Gamma = 1 / (1 + e^{-g}): prefix products
+            // inside the thread's quarter times the earlier quarters' products; the step's
+            // log-decay (for the records) from the quarter products renormalised every 4
+            // tokens, one logarithm per thread
             const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + rG);
-            float bt[8];
-            float run = 0.0f;
+            float pre[8];
+            float pp = 1.0f, mq = 1.0f;
+            int eq = 0;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
                 const int tt = 8 * gq + j;
-                run += tt < n ? log_sigmoid_f(__bfloat162float(sg[tt * 128 + gf])) : 0.0f;
-                bt[j] = run;
+                const float gam =
+                    tt < n ? rcpf(1.0f + ex2f(-__bfloat162float(sg[tt * 128 + gf]) * kLog2e)) : 1.0f;
+                pp *= gam;
+                pre[j] = pp;
+                mq *= gam;
+                if ((j & 3) == 3) {
+                    int e;
+                    mq = frexpf(mq, &e);
+                    eq += e;
+                }
             }
-            gpart[gq * 128 + gf] = run;
+            gpart[gq * 128 + gf] = pp;
+            zq[gq * 128 + gf] = (__log2f(mq) + (float)eq) * kLn2;
             __syncthreads();
-            const float g0 = gpart[gf], g1 = gpart[128 + gf], g2 = gpart[256 + gf],
-                        g3 = gpart[384 + gf];
-            const float off = gq == 0 ? 0.0f : gq == 1 ? g0 : gq == 2 ? g0 + g1 : (g0 + g1) + g2;
+            const float q0 = gpart[gf], q1 = gpart[128 + gf], q2 = gpart[256 + gf];
+            const float before = gq == 0 ? 1.0f : gq == 1 ? q0 : gq == 2 ? q0 * q1 : (q0 * q1) * q2;
             // kept in fp32: the adjoint records feed the gate gradient, a difference of two
             // nearly equal sums that bf16 weights would not cancel consistently
             float* Eb = (float*)(sm + rE);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) Eb[(8 * gq + j) * EPR + gf] = ex2f((bt[j] + off) * kLog2e);
+            for (int j = 0; j < 8; ++j) Eb[(8 * gq + j) * EPR + gf] = pre[j] * before;
             if (gq == 0) {
-                const float blast = (g0 + g1) + (g2 + g3);
-                S.el[gf] = ex2f(blast * kLog2e);
-                lam_tot += blast;
+                S.el[gf] = ((q0 * q1) * q2) * gpart[384 + gf];
+                lam_tot += (zq[gf] + zq[128 + gf]) + (zq[256 + gf] + zq[384 + gf]);
             }
         }
         __syncthreads();
