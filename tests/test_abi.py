@@ -130,3 +130,24 @@ def test_varlen_offsets_validated_before_any_launch(lib):
         assert st == lz.LIZARD_ERR_INVALID_ARG
     assert lib.lizard_attn_fwd_varlen(ctypes.byref(d), None, *nul, 1 << 30, None) == \
         lz.LIZARD_ERR_INVALID_ARG
+
+
+def test_bwd_varlen_workspace_and_offsets(lib):
+    """The packed backward's workspace grows with the longest sequence, covers the parameter
+    gradient sums, and is 0 for inconsistent offsets (no device work involved)."""
+    d = dims(L=3000)
+    d.B = 3
+    ok = (ctypes.c_int64 * 4)(0, 1000, 1000, 3000)
+    short = (ctypes.c_int64 * 4)(0, 1000, 2000, 3000)
+    bad = (ctypes.c_int64 * 4)(0, 1000, 999, 3000)
+    lib.lizard_attn_bwd_varlen_workspace.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.lizard_attn_bwd_varlen_workspace.restype = ctypes.c_size_t
+    w_ok = lib.lizard_attn_bwd_varlen_workspace(ctypes.byref(d), ok)
+    w_short = lib.lizard_attn_bwd_varlen_workspace(ctypes.byref(d), short)
+    one = dims(L=2000)
+    assert w_ok > w_short > lz.lizard_attn_bwd_workspace(dims(L=1000))
+    assert w_ok >= lz.lizard_attn_bwd_workspace(one) + 128 * 64 * 8 * 4
+    assert lib.lizard_attn_bwd_varlen_workspace(ctypes.byref(d), bad) == 0
+    nul = [None] * 16
+    assert lib.lizard_attn_bwd_varlen(ctypes.byref(d), bad, *nul, 1 << 30, None) == \
+        lz.LIZARD_ERR_INVALID_ARG
