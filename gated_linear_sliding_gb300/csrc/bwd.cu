@@ -36,7 +36,7 @@ constexpr int KB = 16;  // window keys per tile in the query-side walk
 
 // Workspace regions (floats, each 64-float aligned)
 struct BwdWs {
-    size_t fwd_rec, rev_rec, dB, tot, dW, dt, rows, total;
+    size_t fwd_rec, rev_rec, dB, tot, dW, dt, rows, flags, total;
 };
 
 inline size_t al64(size_t x) { return (x + 63) & ~(size_t)63; }
@@ -59,6 +59,8 @@ BwdWs bwd_layout(const Plan& p) {
     off += al64((size_t)p.Pmax * U * (size_t)p.G);
     w.rows = off;  // per query row: a = e^{-lse}, delta = dy . y   [2][B*L*Hq]
     off += al64((size_t)2 * (size_t)(p.B * p.L * p.Hq));
+    w.flags = off;  // per (segment, unit): 1 if its gates close too hard for the factored walks
+    off += al64((size_t)p.Pmax * U);
     w.total = off * sizeof(float);
     return w;
 }
@@ -351,7 +353,8 @@ __device__ __forceinline__ void adjoint_add(float* sH, float* sz, float* sphq, c
 // Forward-direction walk: dq (state and window parts), phi(q)-side of dB, partials.
 // One CTA per (batch, KV head, segment); the G query heads are walked in turn.
 template <typename T, int DH, int DF, bool FAST>
-__global__ void __launch_bounds__(NT, 1) bwd_forward_walk(Plan p, BwdArgs a, BwdWs ws) {
+__global__ void __launch_bounds__(NT, 1) bwd_forward_walk(Plan p, BwdArgs a, BwdWs ws,
+                                                          int only_flagged) {
     using Ly = BLay<DH, DF>;
     constexpr int PF = Ly::PF, PH = Ly::PH, PW = Ly::PW, H2 = Ly::H2;
     constexpr int NC = DH / LPR, NF = DF / LPR;
@@ -369,6 +372,7 @@ __global__ void __launch_bounds__(NT, 1) bwd_forward_walk(Plan p, BwdArgs a, Bwd
     const int64_t s0 = seg * p.seg_len, s1 = min64(p.L, s0 + p.seg_len);
     const int tid = threadIdx.x, r = tid / LPR, cs = tid % LPR;
     float* wsf = (float*)a.ws;
+    if (only_flagged && ((const int*)wsf)[ws.flags + seg * U + unit] == 0) return;
     const T* W = (const T*)a.Wf + kv * DH * H2;
     for (int e = tid; e < DH * H2; e += NT) sW[(e / H2) * PW + e % H2] = ld(W + e);
     const float* rec = wsf + ws.fwd_rec + ((size_t)seg * U + unit) * p.rec_floats;
@@ -608,8 +612,12 @@ __global__ void bwd_reverse_scan(Plan p, float* rec0) {
 // ---------------------------------------------------------------------------------------
 // Reverse-direction walk: state parts of dk, dv (keys t - w of the delayed stream),
 // phi(k')-side of dB and the reverse cumulative sum of dB inside the segment, dWf partials.
+// Every decay is e^{difference of cumulative log-gates} taken per pair and arranged as
+// e^{non-positive}, so strongly closed gates (Lizard summary sec. 2-C: products that underflow)
+// cost nothing in accuracy.
 template <typename T, int DH, int DF, bool FAST>
-__global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, BwdWs ws) {
+__global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, BwdWs ws,
+                                                          int only_flagged) {
     using Ly = BLay<DH, DF>;
     constexpr int PF = Ly::PF, PH = Ly::PH, PW = Ly::PW, H2 = Ly::H2;
     constexpr int NC = DH / LPR, NF = DF / LPR;
@@ -619,18 +627,13 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
     float *sphk = sm + Ly::ophk, *sv = sm + Ly::ov, *sq = sm + Ly::oq, *sphq = sm + Ly::ophq;
     float *sdp = sm + Ly::odp, *sdy = sm + Ly::ody, *sA = sm + Ly::oA, *sA2 = sm + Ly::oA2;
     float* srow = sm + Ly::orow;
-    // decay tables in the window-tile area (unused by this walk)
-    float* sE = sm + Ly::otile;           // [TS][PF]
-    float* sK = sE + TS * PF;             // [TS][PF]
-    float* ser = sK + TS * PF;            // [DF]
-    float* sel = ser + DF;                // [DF]
-    static_assert(2 * TS * (DF + 1) + 2 * DF <= Ly::ntile, "tables fit");
     const int64_t unit = blockIdx.x, seg = blockIdx.y;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
     const int64_t U = p.B * p.Hkv;
     const int64_t s0 = seg * p.seg_len, s1 = min64(p.L, s0 + p.seg_len);
     const int tid = threadIdx.x, r = tid / LPR, cs = tid % LPR;
     float* wsf = (float*)a.ws;
+    if (only_flagged && ((const int*)wsf)[ws.flags + seg * U + unit] == 0) return;
     const T* W = (const T*)a.Wf + kv * DH * H2;
     for (int e = tid; e < DH * H2; e += NT) sW[(e / H2) * PW + e % H2] = ld(W + e);
     const float* rec = wsf + ws.rev_rec + ((size_t)seg * U + unit) * p.rec_floats;
@@ -652,19 +655,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
         load_rows_p<T, DH>((const T*)a.v, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n, sv);
         __syncthreads();
         phi_rows_p<DH, DF, FAST>(sq, sW, sphk, rlo, n);
-        // decay tables around the step's midpoint r = b_{TS/2-1}: sE = e^{b_t - r},
-        // sK = e^{r - b_t}, so e^{b_i - b_t} = sE_i sK_t without an exponential per pair;
-        // ser = e^{r}, sel = e^{bl - r}
-        for (int e = tid; e < TS * DF; e += NT) {
-            const int t = e / DF, f = e % DF;
-            const float d = sb[t * PF + f] - sb[(TS / 2 - 1) * PF + f];
-            sE[t * PF + f] = ex<FAST>(fminf(fmaxf(d, -80.0f), 80.0f));
-            sK[t * PF + f] = ex<FAST>(fminf(fmaxf(-d, -80.0f), 80.0f));
-        }
-        if (tid < DF) {
-            ser[tid] = ex<FAST>(sb[(TS / 2 - 1) * PF + tid]);
-            sel[tid] = ex<FAST>(sb[(TS - 1) * PF + tid] - sb[(TS / 2 - 1) * PF + tid]);
-        }
         __syncthreads();
         // terms through the step's end: dphk_t = e^{bl - b_t} (.) (dH v'_t + dz),
         // dv'_t = sum_f e^{bl_f - b_tf} phk_tf dH[f][.]   (row t = r, in registers)
@@ -677,16 +667,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
 #pragma unroll
                 for (int j = 0; j < NF; ++j) dk_acc[j] = fmaf(sH[(cs + LPR * j) * PH + c], vc, dk_acc[j]);
             }
-            // dk_acc holds e^{r - b_t} times the sum; the common factor sK is applied at the end
 #pragma unroll
             for (int j = 0; j < NF; ++j) {
                 const int f = cs + LPR * j;
-                dk_acc[j] = sel[f] * (dk_acc[j] + sz[f]);
+                dk_acc[j] = ex<FAST>(sb[(TS - 1) * PF + f] - sb[r * PF + f]) * (dk_acc[j] + sz[f]);
             }
             // weights e^{bl - b_t} phk_t of the end term, once per (row, feature) (sdp is free)
             for (int e = tid; e < TS * DF; e += NT) {
                 const int t = e / DF, f = e % DF;
-                sdp[t * PF + f] = sel[f] * sK[t * PF + f] * sphk[t * PF + f];
+                sdp[t * PF + f] = ex<FAST>(sb[(TS - 1) * PF + f] - sb[t * PF + f]) * sphk[t * PF + f];
             }
             __syncthreads();
 #pragma unroll
@@ -713,12 +702,6 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
             __syncthreads();
             phi_rows_p<DH, DF, FAST>(sq, sW, sphq, 0, n);
             __syncthreads();
-            // phq rows carry e^{b_i - r} from here on
-            for (int e = tid; e < TS * DF; e += NT) {
-                const int t = e / DF, f = e % DF;
-                sphq[t * PF + f] *= sE[t * PF + f];
-            }
-            __syncthreads();
             // c_it = a_i (v'_t.dy_i - delta_i); A_it a_i = a_i sum_f phq_if phk_tf e^{b_if - b_tf}
             {
                 const int i = r, t = cs;
@@ -729,7 +712,8 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
                     cv = srow[i] * (d - srow[TS + i]);
                     float s = 0.0f;
                     for (int f = 0; f < DF; ++f)
-                        s = fmaf(sphq[i * PF + f], sphk[t * PF + f] * sK[t * PF + f], s);
+                        s = fmaf(sphq[i * PF + f] * sphk[t * PF + f],
+                                 ex<FAST>(sb[i * PF + f] - sb[t * PF + f]), s);
                     av = s * srow[i];
                 }
                 sA[i * (TS + 1) + t] = cv;
@@ -740,8 +724,10 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
 #pragma unroll
             for (int j = 0; j < NF; ++j) {
                 const int f = cs + LPR * j;
+                const float bt = sb[r * PF + f];
                 float v = 0.0f;
-                for (int i = r; i < n; ++i) v = fmaf(sphq[i * PF + f], sA[i * (TS + 1) + r], v);
+                for (int i = r; i < n; ++i)
+                    v = fmaf(sphq[i * PF + f] * ex<FAST>(sb[i * PF + f] - bt), sA[i * (TS + 1) + r], v);
                 dk_acc[j] += v;
             }
 #pragma unroll
@@ -752,13 +738,12 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
                 dv_acc[j] += v;
             }
             __syncthreads();
-            adjoint_add<DH, DF, FAST>(sH, sz, sphq, sdy, sb, srow, n, ser);
+            adjoint_add<DH, DF, FAST>(sH, sz, sphq, sdy, sb, srow, n);
         }
-        // dphk into sdp (rows outside [rlo, n) are zero), with the factor e^{r - b_t}
+        // dphk into sdp (rows outside [rlo, n) are zero)
 #pragma unroll
         for (int j = 0; j < NF; ++j)
-            sdp[r * PF + cs + LPR * j] =
-                (r >= rlo && r < n) ? sK[r * PF + cs + LPR * j] * dk_acc[j] : 0.0f;
+            sdp[r * PF + cs + LPR * j] = (r >= rlo && r < n) ? dk_acc[j] : 0.0f;
         __syncthreads();
         // dB = (phi(q)-side, from the forward walk) - phk (.) dphk; reverse cumsum in place
         if (tid < DF) {
@@ -802,6 +787,26 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
     if (tid < DF) wsf[ws.tot + ((size_t)seg * U + unit) * DF + tid] = carry;
 }
 
+// Segments whose gates close too hard for the tensor-core walks' factored decays: flag
+// (segment, unit) when some feature's cumulative log-gate falls by more than 60 over one of
+// the 16-token halves of the walks' 32-token steps (Lizard summary sec. 2-C: products of such
+// gates underflow).  Four threads per feature, each summing every fourth half.
+__global__ void bwd_gate_flags(Plan p, const __nv_bfloat16* g, int* flags) {
+    const int64_t unit = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t s0 = seg * p.seg_len, s1 = min64(p.L, s0 + p.seg_len);
+    const int f = threadIdx.x & 127, gq = threadIdx.x >> 7;
+    bool closed = false;
+    for (int64_t h0 = s0 + 16 * gq; h0 < s1; h0 += 64) {
+        float lam = 0.0f;
+        const int64_t he = min64(s1, h0 + 16);
+        for (int64_t t = h0; t < he; ++t)
+            lam += log_sigmoid<true>(__bfloat162float(g[((b * p.L + t) * p.Hkv + kv) * 128 + f]));
+        closed |= !(lam >= -60.0f);
+    }
+    const int any = __syncthreads_or(closed);
+    if (threadIdx.x == 0) flags[seg * p.B * p.Hkv + unit] = any ? 1 : 0;
+}
 // ---------------------------------------------------------------------------------------
 // Window part of dk, dv, key-centric: keys j of a 32-key tile, queries i in [j, j + w).
 // Keys with j + w < L already hold their state parts; the window part is added to them.
@@ -1027,14 +1032,20 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
         e = fwd_tc_supported(p) ? launch_fwd_states_tc(p, fa, s) : launch_fwd_states(p, fa, s);
         if (e != cudaSuccess) return e;
     }
-    // 2. forward-direction walk
-    if (a.ev_before) cudaEventRecord(a.ev_before, s);
-    if (a.win_tc && bwd_rev_local_tc_supported(p)) {
-        e = launch_bwd_fwalk_tc(p, a, wsf, ws.rows, ws.fwd_rec, ws.dB, ws.dW, ws.dt, s);
-        if (e != cudaSuccess) return e;
-    } else {
-        bwd_forward_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
+    // 2. forward-direction walk.  The tensor-core walks leave the segments whose gates close
+    //    too hard for their factored decays to the exact SIMT walks (flags from one pass over g)
+    const bool tc_walks = a.win_tc && bwd_rev_local_tc_supported(p);
+    int* flags = (int*)(wsf + ws.flags);
+    if (tc_walks) {
+        if constexpr (sizeof(T) == 2 && DF == 128)
+            bwd_gate_flags<<<dim3(U, (unsigned)p.P), 512, 0, s>>>(p, (const __nv_bfloat16*)a.g, flags);
     }
+    if (a.ev_before) cudaEventRecord(a.ev_before, s);
+    if (tc_walks) {
+        e = launch_bwd_fwalk_tc(p, a, wsf, ws.rows, ws.fwd_rec, ws.dB, ws.dW, ws.dt, flags, s);
+        if (e != cudaSuccess) return e;
+    }
+    bwd_forward_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws, tc_walks ? 1 : 0);
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
     // window part of dq on the tensor cores (the walk above wrote the state part)
     if (a.win_tc) {
@@ -1043,7 +1054,7 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     }
     // 3. reverse segment pass and scan
     if (p.P > 1) {
-        if (a.win_tc && bwd_rev_local_tc_supported(p)) {
+        if (tc_walks) {
             e = launch_bwd_rev_local_tc(p, a, wsf + ws.rows, wsf + ws.rev_rec, s);
             if (e != cudaSuccess) return e;
         } else {
@@ -1053,12 +1064,11 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
         bwd_reverse_scan<<<dim3((nE + 255) / 256, U), 256, 0, s>>>(p, wsf + ws.rev_rec);
     }
     // 4. reverse-direction walk
-    if (a.win_tc && bwd_rev_local_tc_supported(p)) {
-        e = launch_bwd_rwalk_tc(p, a, wsf, ws.rows, ws.rev_rec, ws.dB, ws.dW, ws.tot, s);
+    if (tc_walks) {
+        e = launch_bwd_rwalk_tc(p, a, wsf, ws.rows, ws.rev_rec, ws.dB, ws.dW, ws.tot, flags, s);
         if (e != cudaSuccess) return e;
-    } else {
-        bwd_reverse_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws);
     }
+    bwd_reverse_walk<T, DH, DF, FAST><<<dim3(U, (unsigned)p.P), NT, smem, s>>>(p, a, ws, tc_walks ? 1 : 0);
     // 5. window parts of dk, dv
     if (a.win_tc) {
         e = launch_bwd_win_tc(p, a, wsf + ws.rows, true, s);

@@ -953,8 +953,8 @@ __global__ void __launch_bounds__(NT, 1)
     bwd_fwalk_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDY,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
-                 const __grid_constant__ CUtensorMap tmDQ, Plan p, BwdArgs a, const float* rows, const float* fwd_rec, float* dB, float* dWp,
-                 float* dtp) {
+                 const __grid_constant__ CUtensorMap tmDQ, Plan p, BwdArgs a, const float* rows,
+                 const float* fwd_rec, float* dB, float* dWp, float* dtp, const int* flags) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -977,6 +977,8 @@ __global__ void __launch_bounds__(NT, 1)
     WsHeader* hdr = (WsHeader*)a.ws;
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
     constexpr uint32_t kStepBytes = 2 * kTile + 8192u + 8192u + 8192u;  // q, dY, k', v', gates
+    // a segment whose gates close too hard for the factored decays is the SIMT walk's
+    if (flags[seg * U + unit] != 0) return;
 
     if (warp == 0) {
         tmem_alloc(&S.tmem, 512);
@@ -1559,7 +1561,7 @@ __global__ void __launch_bounds__(NT, 1)
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
                  Plan p, BwdArgs a, const float* rows, const float* rev_rec, float* dB,
-                 float* dWp, float* totp) {
+                 float* dWp, float* totp, const int* flags) {
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -1585,6 +1587,8 @@ __global__ void __launch_bounds__(NT, 1)
     WsHeader* hdr = (WsHeader*)a.ws;
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
     constexpr uint32_t kStepBytes = 2 * kTile + 8192u + 8192u + 8192u;  // q, dY, k', v', gates
+    // a segment whose gates close too hard for the factored decays is the SIMT walk's
+    if (flags[seg * U + unit] != 0) return;
 
     if (warp == 0) {
         tmem_alloc(&S.tmem, 512);
@@ -2147,7 +2151,7 @@ bool bwd_win_tc_supported(const Plan& p) {
 
 cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
                                 size_t o_fwd, size_t o_dB, size_t o_dW, size_t o_dt,
-                                cudaStream_t s) {
+                                const int* flags, cudaStream_t s) {
     alignas(64) CUtensorMap mq, md, mk, mv, mw, mg, mdq;
     const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
                      Hkv = (cuuint64_t)p.Hkv;
@@ -2183,13 +2187,13 @@ cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, siz
     if (e != cudaSuccess) return e;
     bwd_fwalk_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemFW, s>>>(
         mq, md, mk, mv, mw, mg, mdq, p, a, wsf + o_rows, wsf + o_fwd, wsf + o_dB, wsf + o_dW,
-        wsf + o_dt);
+        wsf + o_dt, flags);
     return cudaGetLastError();
 }
 
 cudaError_t launch_bwd_rwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
                                 size_t o_rev, size_t o_dB, size_t o_dW, size_t o_tot,
-                                cudaStream_t s) {
+                                const int* flags, cudaStream_t s) {
     alignas(64) CUtensorMap mq, md, mk, mv, mw, mg;
     const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
                      Hkv = (cuuint64_t)p.Hkv;
@@ -2224,7 +2228,7 @@ cudaError_t launch_bwd_rwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, siz
     if (e != cudaSuccess) return e;
     bwd_rwalk_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemRW, s>>>(
         mq, md, mk, mv, mw, mg, p, a, wsf + o_rows, wsf + o_rev, wsf + o_dB, wsf + o_dW,
-        wsf + o_tot);
+        wsf + o_tot, flags);
     return cudaGetLastError();
 }
 

@@ -94,29 +94,25 @@ __global__ void fwd_seg_scan(Plan p, float* seg) {
     }
 }
 
+// One query head h of batch entry b over tokens [s0, s1), starting from the state in `rec`
+// ([D][d] then [D]; null: the zero state).  s0 is a multiple of the 32-token step.
 template <typename T, int DH, int DF, bool FAST>
-__global__ void __launch_bounds__(NT, 1) fwd_simt_main(Plan p, FwdArgs a) {
+__device__ __forceinline__ void walk_head(const Plan& p, const FwdArgs& a, int64_t b, int64_t h,
+                                          int64_t s0, int64_t s1, const float* rec, float* sm) {
     using Ly = Lay<DH, DF>;
     constexpr int PF = Ly::PF, PH = Ly::PH, NC = DH / 8;
-    extern __shared__ float sm[];
     float *sH = sm + Ly::oH, *sz = sm + Ly::oz, *sW = sm + Ly::oW, *sb = sm + Ly::ob;
     float *sphk = sm + Ly::ophk, *sv = sm + Ly::ov, *sq = sm + Ly::oq, *sphq = sm + Ly::ophq;
     float *sA = sm + Ly::oA, *sR = sm + Ly::oR, *sP = sm + Ly::oP;
-    const int64_t bh = blockIdx.x, seg = blockIdx.y;
-    const int64_t b = bh / p.Hq, h = bh % p.Hq, kv = h / p.G;
-    const int64_t s0 = seg * p.seg_len;
-    if (s0 >= p.L) return;
-    const int64_t s1 = min64(p.L, s0 + p.seg_len);
+    const int64_t kv = h / p.G;
     const int64_t unit = b * p.Hkv + kv;
     const int tid = threadIdx.x;
     const T* W = (const T*)a.Wf + kv * DH * (DF / 2);
     for (int e = tid; e < DH * (DF / 2); e += NT) sW[e] = ld(W + e);
-    if (seg == 0) {
+    if (rec == nullptr) {
         for (int e = tid; e < DF * DH; e += NT) sH[e] = 0.0f;
         if (tid < DF) sz[tid] = 0.0f;
     } else {
-        const float* rec = a.seg + ((size_t)seg * (size_t)(p.B * p.Hkv) + (size_t)unit) *
-                                       p.rec_floats;
         for (int e = tid; e < DF * DH; e += NT) sH[e] = rec[e];
         if (tid < DF) sz[tid] = rec[DF * DH + tid];
     }
@@ -255,6 +251,44 @@ __global__ void __launch_bounds__(NT, 1) fwd_simt_main(Plan p, FwdArgs a) {
     }
 }
 
+template <typename T, int DH, int DF, bool FAST>
+__global__ void __launch_bounds__(NT, 1) fwd_simt_main(Plan p, FwdArgs a) {
+    extern __shared__ float sm[];
+    const int64_t bh = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = bh / p.Hq, h = bh % p.Hq, kv = h / p.G;
+    const int64_t s0 = seg * p.seg_len;
+    if (s0 >= p.L) return;
+    const int64_t s1 = min64(p.L, s0 + p.seg_len);
+    const int64_t unit = b * p.Hkv + kv;
+    const float* rec =
+        seg == 0 ? nullptr
+                 : a.seg + ((size_t)seg * (size_t)(p.B * p.Hkv) + (size_t)unit) * p.rec_floats;
+    walk_head<T, DH, DF, FAST>(p, a, b, h, s0, s1, rec, sm);
+}
+
+// The rest of a segment that the tensor-core main walk handed over at a step whose gates close
+// too hard for its factored decays (Lizard summary sec. 2-C: the cumulative gate product of
+// such a stretch underflows).  One CTA per (batch x KV head, segment) of the tensor-core plan:
+// the CTA's record slot (slot seg * rec_step) holds the state before that step and, in its
+// first log-decay word, the step (-1: the segment is complete).  The group's query heads are
+// walked one after another from that state, with exact per-pair decays.
+template <typename T, int DH, int DF, bool FAST>
+__global__ void __launch_bounds__(NT, 1) fwd_simt_tail(Plan p, FwdArgs a) {
+    extern __shared__ float sm[];
+    const int64_t unit = blockIdx.x, seg = blockIdx.y;
+    const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
+    const float* ho =
+        a.seg + ((size_t)(seg * p.rec_step) * (size_t)(p.B * p.Hkv) + (size_t)unit) * p.rec_floats;
+    const int stop = __float_as_int(ho[DF * DH + DF]);
+    if (stop < 0) return;
+    const int64_t s0 = (int64_t)stop * TS;
+    const int64_t s1 = min64(p.L, seg * p.seg_len + p.seg_len);
+    for (int64_t hh = 0; hh < p.G; ++hh) {
+        walk_head<T, DH, DF, FAST>(p, a, b, kv * p.G + hh, s0, s1, ho, sm);
+        __syncthreads();
+    }
+}
+
 template <typename T>
 __global__ void ring_fill_kernel(Plan p, const T* k, const T* v, T* kc, T* vc) {
     const int64_t nt = min64(p.L, p.w);
@@ -336,6 +370,17 @@ cudaError_t launch_fwd_simt(const Plan& p, const FwdArgs& a, cudaStream_t s) {
 cudaError_t launch_fwd_states(const Plan& p, const FwdArgs& a, cudaStream_t s) {
     if (p.dtype == LIZARD_F32) return states_dims<float, false>(p, a, s);
     return states_dims<__nv_bfloat16, true>(p, a, s);
+}
+
+cudaError_t launch_fwd_tail(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+    if (p.dtype != LIZARD_BF16 || p.d != 128 || p.D != 128) return cudaErrorInvalidValue;
+    using Ly = Lay<128, 128>;
+    auto kern = fwd_simt_tail<__nv_bfloat16, 128, 128, true>;
+    const cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ly::bytes);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, Ly::bytes, s>>>(p, a);
+    return cudaGetLastError();
 }
 
 cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s) {

@@ -26,9 +26,13 @@
 //   y_i   = O_i / (sum P_win + sum P_intra + q~_i.(e^{r} z) + sum_m e^{t_m - m_i})
 // Every gate factor is e^{difference of cumulative log-gates}, formed as a running product of
 // Gamma = sigmoid(g) or 1/Gamma = 1 + e^{-g} over the tokens in between; relative to the
-// sub-chunk midpoint r each factor stays within the decay of 16 tokens, so no factor leaves
-// the fp32/bf16 range unless 16 consecutive gates decay by more than e^-80 (factors are
-// clamped to [e^-80, e^80] there).
+// step midpoint r each factor stays within the decay of one 16-token half.  That factored form
+// is exact only while no half decays too far (a factor e^{b_i - r} of a half that decays by
+// e^-200 does not exist in fp32).  A step on which some 8-token quarter of some feature
+// decays by more than e^-36 therefore leaves this kernel: the CTA writes the state it would
+// start that step from into its own record slot, marks the slot with the step, and stops; the
+// exact SIMT tail walk (fwd_simt_tail) finishes the segment from there.  On the steps this
+// kernel does run, every factor lies in [e^-72, e^72].
 //
 // TMEM columns: H [0,128)  scores S [128,256) (intra scores A reuse [128,160))
 //               U_q [256,320)  U_k [320,384) (then P_win, bf16 pairs)  O [384,512).
@@ -98,8 +102,12 @@ static_assert(kSmemBytes <= 232448, "shared memory budget");
 // step's projections can run while the epilogue still reads O.
 constexpr uint32_t cH = 0, cS = 128, cA = 128, cUq = 256, cUk = 320, cPw = 320, cO = 384;
 
-constexpr float kE80 = 5.5406223843935100e34f;   // e^80
-constexpr float kEm80 = 1.8048513878454153e-35f;  // e^-80
+// Largest product of 1/Gamma over an 8-token quarter of a step this kernel runs (e^36): the
+// midpoint factors of its steps then stay within [e^-72, e^72].
+constexpr float kQuarterMax = 4.311231547115195e15f;
+// Lower bound of the row shift m in this kernel: q~ = phi(q) e^{-m} e^{b_i - r} / sum stays
+// below e^{8} e^{72}, inside the bf16 range.
+constexpr float kTcMinShift = -8.0f;
 
 // Decay tables [32 tokens][128 features] bf16: the 16-byte chunks of token t's row are
 // XOR-swizzled by t, so rows read by neighbouring tokens fall in different banks.
@@ -357,7 +365,7 @@ __global__ void __launch_bounds__(NT, 1)
     }
     if (tid < GQ) {
         const float* t = a.sinks + (kv * GQ + tid) * p.M;
-        float tm = kMinShift;
+        float tm = kTcMinShift;
         for (int mm = 0; mm < p.M; ++mm) tm = fmaxf(tm, t[mm]);
         float se = 0.0f;
         for (int mm = 0; mm < p.M; ++mm) se += ex2f((t[mm] - tm) * kLog2e);
@@ -396,6 +404,7 @@ __global__ void __launch_bounds__(NT, 1)
     } else {
         uint32_t ph_tma = 0, ph_u = 0, ph_a = 0, ph_o = 0;
         bool ok = true;
+        int64_t stop = -1;  // the step handed to the exact tail walk, if any
 
         for (int64_t c = c_begin; c < c_end; ++c) {
             const int64_t t0 = c * CT;
@@ -409,13 +418,12 @@ __global__ void __launch_bounds__(NT, 1)
 
             // (2) gates: four threads per feature, one per 8-token quarter.  Every decay factor
             //     of the step relative to r = b_15 is a running product of Gamma = sigmoid(g) or
-            //     of 1/Gamma = 1 + e^{-g} over the tokens between (no logarithm), clamped to
-            //     [e^-80, e^80] as the exponents are
+            //     of 1/Gamma = 1 + e^{-g} over the tokens between (no logarithm)
             const int gf = tid & (DF - 1), gq = tid >> 7;
             float ig[CT / 4];  // 1/Gamma of the thread's tokens (Gamma itself is rcp of it)
+            float pig = 1.0f;
             {
                 const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + oG);
-                float pig = 1.0f;
 #pragma unroll
                 for (int t = 0; t < CT / 4; ++t) {
                     const int tt = (CT / 4) * gq + t;
@@ -426,7 +434,13 @@ __global__ void __launch_bounds__(NT, 1)
                 S.gpart[gq][gf] = rcpf(pig);
                 S.gipart[gq][gf] = pig;
             }
-            math_sync();
+            // a quarter that decays by more than e^-36 (or a non-finite product) on any feature:
+            // the step goes to the exact tail walk, before anything of it is written
+            if (math_any(!(pig <= kQuarterMax))) {
+                stop = c;
+                if (tid == 0) S.abort = 2;  // releases the control warp without an error
+                break;
+            }
             {
                 __nv_bfloat16* Eq = (__nv_bfloat16*)(sm + oE);
                 __nv_bfloat16* Ek = (__nv_bfloat16*)(sm + oE + 8192);
@@ -436,8 +450,8 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
                     for (int t = CT / 4 - 1; t >= 0; --t) {
                         const int tt = (CT / 4) * gq + t;
-                        Eq[eidx(tt, gf)] = __float2bfloat16_rn(fminf(sq, kE80));
-                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(fmaxf(sk, kEm80));
+                        Eq[eidx(tt, gf)] = __float2bfloat16_rn(sq);
+                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(sk);
                         sq *= ig[t];
                         sk *= rcpf(ig[t]);
                     }
@@ -449,8 +463,8 @@ __global__ void __launch_bounds__(NT, 1)
                         const int tt = (CT / 4) * gq + t;
                         pq *= rcpf(ig[t]);
                         pk *= ig[t];
-                        Eq[eidx(tt, gf)] = __float2bfloat16_rn(fmaxf(pq, kEm80));
-                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(fminf(pk, kE80));
+                        Eq[eidx(tt, gf)] = __float2bfloat16_rn(pq);
+                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(pk);
                     }
                 }
                 if (gq == 0) {
@@ -774,7 +788,24 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (tid == 0) bulk_wait_all();
 
-        if (ok && a.S_out != nullptr && s1 == p.L) {
+        // Record slot of this CTA (the one it read its starting state from, or slot 0): the
+        // state handed to the tail walk, and in the first log-decay word the step it starts at
+        // (-1: nothing to finish).  Written on every call, so no earlier call's mark survives.
+        float* ho = a.seg + ((size_t)(seg * p.rec_step) * (size_t)U + (size_t)unit) * p.rec_floats;
+        if (ok && stop >= 0) {
+            float v[32];
+            const int col = 32 * part;
+            tmem_ld32(tb + lane_off + cH + col, v);
+            tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 32; k += 4)
+                *reinterpret_cast<float4*>(ho + row * DH + col + k) =
+                    make_float4(v[k], v[k + 1], v[k + 2], v[k + 3]);
+            if (tid < DF) ho[DF * DH + tid] = S.z[tid];
+        }
+        if (tid == 0) ho[DF * DH + DF] = __int_as_float(ok && stop >= 0 ? (int)stop : -1);
+
+        if (ok && stop < 0 && a.S_out != nullptr && s1 == p.L) {
             // final state of the last segment: the decode hand-off
             float* dstH = a.S_out + unit * DF * DH;
             float* dstz = a.z_out + unit * DF;
@@ -1283,7 +1314,10 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     fwd_tc_kernel<<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, my, p,
                                                                         a);
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
-    return cudaGetLastError();
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    // segments handed over at a strongly closed step are finished by the exact walk
+    return launch_fwd_tail(p, a, s);
 }
 
 }  // namespace lz

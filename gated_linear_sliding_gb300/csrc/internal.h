@@ -27,6 +27,20 @@ struct Plan {
 };
 
 bool make_plan(const lizard_dims* dims, Plan* p);
+// Host-side checks shared by every forward entry point (sizes, pointers, alignment, pairs of
+// optional outputs, compiled shapes), in this order; fills *p.  Nothing is launched.
+lizard_status fwd_check(const lizard_dims* dims, Plan* p, const void* q, const void* k,
+                        const void* v, const void* g, const void* Wf, const float* sinks,
+                        const void* y, const float* lse, const float* S_out, const float* z_out,
+                        const void* kcache_out, const void* vcache_out);
+// LIZARD_OK on an sm_103 device, LIZARD_ERR_UNSUPPORTED on another, LIZARD_ERR_CUDA if the
+// query fails.
+lizard_status device_status();
+// Boundary-state records (each rec_floats floats per unit) the forward's launch uses.
+size_t fwd_records_used(const Plan& p);
+struct FwdArgs;
+// The forward's kernels (tensor-core or SIMT path, then the ring caches) on stream s.
+cudaError_t fwd_launch(const Plan& p, const FwdArgs& a, cudaStream_t s);
 // Re-cut the segments for a kernel that wants about `target` (unit, segment) CTAs;
 // never more than Pmax segments, so the workspace size stays valid.
 void plan_segments(Plan* p, int64_t target);
@@ -54,6 +68,9 @@ cudaError_t launch_fwd_states(const Plan& p, const FwdArgs& a, cudaStream_t s);
 cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s);
 bool fwd_tc_supported(const Plan& p);
 cudaError_t launch_fwd_tc(const Plan& p, const FwdArgs& a, cudaStream_t s);
+// Exact SIMT walk of the segments the tensor-core main walk handed over at a strongly closed
+// step (bf16, d = D = 128; p is the tensor-core plan).  Segments not handed over return at once.
+cudaError_t launch_fwd_tail(const Plan& p, const FwdArgs& a, cudaStream_t s);
 // Segment-start states only (tensor-core segment pass + scan into a.seg), for the backward.
 // The segmentation the tensor-core forward runs with (fewest segment-waves on 152 SMs).
 void fwd_tc_plan(Plan* p);
@@ -91,14 +108,15 @@ bool bwd_win_tc_supported(const Plan& p);
 bool bwd_rev_local_tc_supported(const Plan& p);
 // Reverse-direction walk of the backward on the tensor cores (state parts of dk, dv,
 // phi(k')-side of dB with its reverse cumulative sum, dWf and segment totals).
+// Segments whose flag is set (flags[seg * B * Hkv + unit] != 0) are left to the SIMT walks.
 cudaError_t launch_bwd_rwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
                                 size_t o_rev, size_t o_dB, size_t o_dW, size_t o_tot,
-                                cudaStream_t s);
+                                const int* flags, cudaStream_t s);
 // Forward-direction walk of the backward on the tensor cores (state part of dq, phi(q)-side of
 // dB, dWf and dt partials); offsets are in floats from the workspace start.
 cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, size_t o_rows,
                                 size_t o_fwd, size_t o_dB, size_t o_dW, size_t o_dt,
-                                cudaStream_t s);
+                                const int* flags, cudaStream_t s);
 // Reverse segment pass on the tensor cores: each segment's contribution to the state adjoint
 // at its start (records as the forward's) into rev_rec.
 cudaError_t launch_bwd_rev_local_tc(const Plan& p, const BwdArgs& a, const float* rows,
@@ -108,5 +126,9 @@ cudaError_t launch_bwd_rev_local_tc(const Plan& p, const BwdArgs& a, const float
 cudaError_t launch_bwd_win_tc(const Plan& p, const BwdArgs& a, const float* rows, bool keys,
                               cudaStream_t s);
 cudaError_t launch_bwd(const Plan& p, const BwdArgs& a, cudaStream_t s);
+
+// Device address of the status header of lizard_attn_fwd_noalloc's fixed scratch on the
+// current device (looked up once per device).
+cudaError_t noalloc_header(void** out);
 
 }  // namespace lz

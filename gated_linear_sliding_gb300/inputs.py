@@ -88,6 +88,19 @@ def gla_sensitive(wl: Workload) -> Workload:
     return wl.replace(name=wl.name + "_glasens", gate=("normal", 8.0, 1.0), wf_std=1.0)
 
 
+def closed_gates(wl: Workload, per_1k: float = 2.0) -> Workload:
+    """Variant whose gate logits hold runs of strongly closed gates.
+
+    The Lizard summary (sec. 2-C) builds its chunk algorithm around cumulative gate
+    products that underflow.  Here the workload's gate stream is broken, about per_1k
+    times per 1000 tokens of each (batch, KV head), by a run of 16 to 48 consecutive tokens
+    whose logits are N(-12, 1) (a quarter of the runs: N(-30, 1)), on every feature or on a
+    random half of them.  Such a run closes the gates: 16 tokens at -12 decay the state by
+    about e^-190.
+    """
+    return wl.replace(name=wl.name + "_closed", gate=("runs", wl.gate, per_1k, 16, 48, 0.25))
+
+
 def round_to(a: np.ndarray, dtype: str) -> np.ndarray:
     """Round fp32 values to the storage dtype and return them as fp32."""
     a = np.ascontiguousarray(a, dtype=np.float32)
@@ -112,6 +125,24 @@ def _gates(rng: np.random.Generator, shape, spec) -> np.ndarray:
         u = rng.random(shape, dtype=np.float32)
         first = u < p1
         return np.where(first, mu1 + s1 * a, mu2 + s2 * a).astype(np.float32)
+    if spec[0] == "runs":
+        _, base, per_1k, lo, hi, p_deep = spec
+        out = _gates(rng, shape, base)
+        B, L, H, D = shape
+        nrun = max(1, int(round(L * per_1k / 1000.0)))
+        for b in range(B):
+            for h in range(H):
+                starts = rng.integers(0, L, size=nrun)
+                lens = rng.integers(lo, hi + 1, size=nrun)
+                deep = rng.random(nrun) < p_deep
+                every = rng.random(nrun) < 0.5
+                for s0, n, dp, ev in zip(starts, lens, deep, every):
+                    feats = np.arange(D) if ev else np.sort(rng.permutation(D)[: D // 2])
+                    e = min(L, int(s0) + int(n))
+                    vals = rng.standard_normal((e - int(s0), len(feats)), dtype=np.float32)
+                    view = out[b, int(s0):e, h]
+                    view[:, feats] = (-30.0 if dp else -12.0) + vals
+        return out
     raise ValueError(spec)
 
 

@@ -163,3 +163,33 @@ def test_bwd_varlen_packed_batch(lz, oracle_mod):
         dt += ref["dsinks"]
     assert_grad(out["dWf"], dW, "bf16", "dWf (sum)")
     assert_grad(out["dsinks"], dt, "bf16", "dsinks (sum)")
+
+
+@pytest.mark.parametrize("gla", [False, True])
+def test_bwd_closed_gate_runs_mistral(lz, oracle_mod, gla):
+    """Runs of strongly closed gates (logits N(-12, 1) and N(-30, 1)) inside the Mistral-shaped
+    workload's gates: the segments they fall in take the exact SIMT walks, the others the
+    tensor-core walks; all six gradients match the oracle."""
+    wl = I.MISTRAL_7B_TRAIN
+    if gla:
+        wl = I.gla_sensitive(wl)
+    wl = I.closed_gates(wl, per_1k=1.0)
+    inp = I.make_inputs(wl, L=2048, B=2, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w,
+                         scale=wl.scale)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16")
+
+
+def test_bwd_closed_gate_runs_llama(lz, oracle_mod):
+    wl = I.closed_gates(I.LLAMA3_8B_L8K, per_1k=0.5)
+    inp = I.make_inputs(wl, L=4096, B=1, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16")
+
+
+def test_bwd_closed_gates_f32(lz, oracle_mod):
+    """The fp32 path (SIMT walks only) under the same runs."""
+    wl = I.closed_gates(I.TINY_F32.replace(L=400, B=2, Hq=4, Hkv=2, w=16), per_1k=5.0)
+    inp = I.make_inputs(wl, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "f32")

@@ -204,3 +204,69 @@ def test_varlen_packed_batch_bf16(lz, oracle_mod):
 
 def test_varlen_packed_batch_f32(lz, oracle_mod):
     _varlen_case(lz, oracle_mod, I.TINY_F32.replace(Hq=4, Hkv=2), [40, 3, 129, 64])
+
+
+def _closed_quarters(g) -> int:
+    """Number of (batch, 8-token quarter, KV head, feature) cells whose gates decay by more
+    than e^-36: the cells that take the tensor-core forward's exact tail walk."""
+    B, L, H, D = g.shape
+    ls = -np.logaddexp(0.0, -np.asarray(g, np.float64))
+    n = L // 8 * 8
+    return int((ls[:, :n].reshape(B, n // 8, 8, H, D).sum(2) < -36.0).sum())
+
+
+@pytest.mark.parametrize("base,L,B,gla", [
+    ("llama", 8192, 1, False),   # LLaMA-shaped heads, runs inside N(3, 1.5) gates
+    ("llama", 1000, 1, True),    # ragged length, state term large (closing it matters)
+    ("mistral", 2048, 2, False),
+    ("mistral", 2048, 2, True),
+])
+def test_closed_gate_runs(lz, oracle_mod, base, L, B, gla):
+    """Runs of 16-48 tokens whose gate logits are N(-12, 1) or N(-30, 1) (Lizard summary
+    sec. 2-C: cumulative gate products that underflow).  The tensor-core walk hands each such
+    step to the exact tail walk; y, lse, the final state and z match the oracle."""
+    wl = {"llama": I.LLAMA3_8B_L8K, "mistral": I.MISTRAL_7B_TRAIN}[base]
+    if gla:
+        wl = I.gla_sensitive(wl)
+    wl = I.closed_gates(wl)
+    inp = I.make_inputs(wl, L=L, B=B)
+    assert _closed_quarters(inp["g"]) > 0
+    out = gpu_fwd(lz, inp, wl, lse=True, state=True)
+    ref = oracle_fwd(oracle_mod, inp, wl, parts=True, state=True)
+    assert_parity(out["y"], ref["y"], "bf16", "y")
+    assert rel_l2(out["lse"], np.log(ref["den"])) < 1e-3
+    assert_parity(out["S_out"], ref["S"], "bf16", "S")
+    assert_parity(out["z_out"], ref["z"], "bf16", "z")
+
+
+def test_closed_gates_every_step(lz, oracle_mod):
+    """Every gate strongly closed (logits N(-20, 1)): the whole sequence runs on the exact
+    walk from its first step; the state holds only the key that just left the window."""
+    wl = I.LLAMA3_8B_L8K.replace(gate=("normal", -20.0, 1.0))
+    inp = I.make_inputs(wl, L=700)
+    out = gpu_fwd(lz, inp, wl, lse=True, state=True)
+    ref = oracle_fwd(oracle_mod, inp, wl, parts=True, state=True)
+    assert_parity(out["y"], ref["y"], "bf16", "y")
+    assert_parity(out["S_out"], ref["S"], "bf16", "S")
+
+
+def test_closed_gates_repeat_bitwise(lz):
+    """The hand-off marks live in the workspace: a second call with open gates on the same
+    workspace is unaffected by the first call's marks, and repeats are bit-identical."""
+    wl = I.closed_gates(I.LLAMA3_8B_L8K)
+    tc = to_dev(I.make_inputs(wl, L=4096), wl.dtype)
+    to = to_dev(I.make_inputs(I.LLAMA3_8B_L8K, L=4096), wl.dtype)
+    dims = lz.dims_of(tc["q"], tc["k"], tc["g"], tc["sinks"], wl.w)
+    ws = lz.new_workspace(lz.lizard_attn_fwd_workspace(dims), "cuda")
+    run = lambda t: lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"],
+                                       wl.w, workspace=ws)
+    yc1 = run(tc)
+    yo1 = run(to)
+    yc2 = run(tc)
+    yo2 = run(to)
+    torch.cuda.synchronize()
+    assert torch.equal(yc1, yc2) and torch.equal(yo1, yo2)
+    fresh = lz.lizard_attn_fwd(to["q"], to["k"], to["v"], to["g"], to["Wf"], to["sinks"], wl.w)
+    torch.cuda.synchronize()
+    assert torch.equal(yo1, fresh)
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK

@@ -147,6 +147,38 @@ def test_gates_one_no_sinks_is_window_softmax_plus_linear(oracle_mod):
     assert rel(y, expect) < 1e-13
 
 
+def test_closed_gates_state_holds_only_the_leaving_key(oracle_mod):
+    """Every gate shut (g = -200, Gamma ~ 1e-87): each step's decay wipes the state, so it
+    holds only the key that has just left the window.  y_i is then a softmax-like average
+    over the w window keys and key i - w, the latter weighted by phi(q_i).phi(k_{i-w}) instead
+    of e^{s q.k}, with the sinks in the denominator (Lizard summary sec. 2-A-1, 2-A-2)."""
+    wl = small(w=3, L=20)
+    inp = f64(I.make_inputs(wl))
+    inp["g"][:] = -200.0
+    y = oracle_mod.fwd(**inp, w=wl.w)["y"]
+    q, k, v, Wf, t = inp["q"], inp["k"], inp["v"], inp["Wf"], inp["sinks"]
+    B, L, Hq, d = q.shape
+    G = Hq // wl.Hkv
+    expect = np.zeros_like(y)
+    for b in range(B):
+        for h in range(Hq):
+            kv = h // G
+            pq, pk = forms.phi(q[b, :, h], Wf[kv]), forms.phi(k[b, :, kv], Wf[kv])
+            for i in range(L):
+                num = np.zeros(d)
+                den = np.exp(t[h]).sum()
+                for j in range(max(0, i - wl.w + 1), i + 1):
+                    e = math.exp(q[b, i, h] @ k[b, j, kv] / math.sqrt(d))
+                    num += e * v[b, j, kv]
+                    den += e
+                if i >= wl.w:
+                    a = pq[i] @ pk[i - wl.w]
+                    num += a * v[b, i - wl.w, kv]
+                    den += a
+                expect[b, i, h] = num / den
+    assert rel(y, expect) < 1e-13
+
+
 def test_full_window_no_sinks_is_causal_softmax_attention(oracle_mod):
     """w >= L and no sinks: y is textbook causal softmax attention (torch SDPA, fp64)."""
     import torch
