@@ -80,6 +80,38 @@ size_t fwd_workspace_bytes(const Plan& p) {
 
 static bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
 
+lizard_status fwd_check(const lizard_dims* dims, Plan* p, const void* q, const void* k,
+                        const void* v, const void* g, const void* Wf, const float* sinks,
+                        const void* y, const float* lse, const float* S_out, const float* z_out,
+                        const void* kcache_out, const void* vcache_out) {
+    if (!make_plan(dims, p)) return LIZARD_ERR_INVALID_ARG;
+    if (!q || !k || !v || !g || !Wf || !y || (p->M > 0 && !sinks)) return LIZARD_ERR_INVALID_ARG;
+    const void* ptrs[] = {q, k, v, g, Wf, sinks, y, lse, S_out, z_out, kcache_out, vcache_out};
+    for (const void* ptr : ptrs)
+        if (ptr && !aligned16(ptr)) return LIZARD_ERR_INVALID_ARG;
+    if ((S_out == nullptr) != (z_out == nullptr)) return LIZARD_ERR_INVALID_ARG;
+    if ((kcache_out == nullptr) != (vcache_out == nullptr)) return LIZARD_ERR_INVALID_ARG;
+    if (!shapes_compiled(*p)) return LIZARD_ERR_UNSUPPORTED;
+    return LIZARD_OK;
+}
+
+size_t fwd_records_used(const Plan& p) {
+    if (fwd_tc_supported(p)) {
+        Plan pl = p;
+        fwd_tc_plan(&pl);
+        // every CTA of the tensor-core walk marks its record slot (hand-off to the tail walk)
+        return pl.P > 1 ? (size_t)(pl.rec_step * (pl.P - 1) + 1) : 1;
+    }
+    return p.P > 1 ? (size_t)p.P : 0;
+}
+
+cudaError_t fwd_launch(const Plan& p, const FwdArgs& a, cudaStream_t s) {
+    cudaError_t e = fwd_tc_supported(p) ? launch_fwd_tc(p, a, s) : launch_fwd_simt(p, a, s);
+    if (e == cudaSuccess && a.kcache_out != nullptr)
+        e = launch_ring_fill(p, a.k, a.v, a.kcache_out, a.vcache_out, s);
+    return e;
+}
+
 // 1 if the current device is sm_103, 0 if not, -1 if the query failed.
 static int device_ok() {
     int dev = 0;
@@ -95,7 +127,7 @@ static int device_ok() {
     return ok;
 }
 
-static lizard_status device_status() {
+lizard_status device_status() {
     const int ok = device_ok();
     if (ok < 0) {
         cudaGetLastError();
@@ -137,17 +169,12 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
                               void* y, float* lse, float* S_out, float* z_out, void* kcache_out,
                               void* vcache_out, void* workspace, size_t ws_bytes, void* stream) {
     Plan p;
-    if (!make_plan(dims, &p)) return LIZARD_ERR_INVALID_ARG;
-    if (!q || !k || !v || !g || !Wf || !y || (p.M > 0 && !sinks)) return LIZARD_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, Wf, sinks, y, lse, S_out, z_out, kcache_out, vcache_out,
-                          workspace};
-    for (const void* ptr : ptrs)
-        if (ptr && !aligned16(ptr)) return LIZARD_ERR_INVALID_ARG;
-    if ((S_out == nullptr) != (z_out == nullptr)) return LIZARD_ERR_INVALID_ARG;
-    if ((kcache_out == nullptr) != (vcache_out == nullptr)) return LIZARD_ERR_INVALID_ARG;
-    if (!shapes_compiled(p)) return LIZARD_ERR_UNSUPPORTED;
+    lizard_status st = fwd_check(dims, &p, q, k, v, g, Wf, sinks, y, lse, S_out, z_out,
+                                 kcache_out, vcache_out);
+    if (st != LIZARD_OK) return st;
+    if (workspace != nullptr && !aligned16(workspace)) return LIZARD_ERR_INVALID_ARG;
     if (workspace == nullptr || ws_bytes < fwd_workspace_bytes(p)) return LIZARD_ERR_WORKSPACE;
-    lizard_status st = device_status();
+    st = device_status();
     if (st != LIZARD_OK) return st;
     cudaStream_t s = (cudaStream_t)stream;
     FwdArgs a;
@@ -167,10 +194,7 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
     a.seg = (float*)((char*)workspace + kHeaderBytes);
     a.ev_before = g_ev_before;
     a.ev_after = g_ev_after;
-    cudaError_t e = fwd_tc_supported(p) ? launch_fwd_tc(p, a, s) : launch_fwd_simt(p, a, s);
-    if (e == cudaSuccess && kcache_out != nullptr)
-        e = launch_ring_fill(p, k, v, kcache_out, vcache_out, s);
-    return from_cuda(e);
+    return from_cuda(fwd_launch(p, a, s));
 }
 
 lizard_status lizard_attn_fwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,

@@ -39,12 +39,27 @@ cudaError_t noalloc_scratch(void** out) {
     return cudaSuccess;
 }
 
-bool aligned16_na(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
+// Scratch bytes a call needs: the status word, then the boundary-state records its launch
+// uses (the same count as in a caller's workspace).
+size_t noalloc_need(const Plan& p) {
+    return kHeaderBytes +
+           sizeof(float) * fwd_records_used(p) * (size_t)(p.B * p.Hkv) * p.rec_floats;
+}
 
 }  // namespace
+
+// The status header (first 256 bytes) of the array, for the failure-path self-test.
+cudaError_t noalloc_header(void** out) { return noalloc_scratch(out); }
+
 }  // namespace lz
 
 using namespace lz;
+
+extern "C" size_t lizard_attn_fwd_noalloc_scratch(const lizard_dims* dims) {
+    Plan p;
+    if (!make_plan(dims, &p)) return 0;
+    return noalloc_need(p);
+}
 
 extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const void* q,
                                                  const void* k, const void* v, const void* g,
@@ -53,41 +68,18 @@ extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const 
                                                  void* kcache_out, void* vcache_out,
                                                  void* stream) {
     Plan p;
-    if (!make_plan(dims, &p)) return LIZARD_ERR_INVALID_ARG;
-    // scratch this problem needs (checked first: it depends on the dimensions only): the
-    // status word, plus one boundary-state record per (segment, batch x KV head) when the
-    // sequence is split into several segments, counted with the segmentation the launch
-    // below will use
-    Plan pl = p;
-    if (fwd_tc_supported(p)) fwd_tc_plan(&pl);
-    const size_t need =
-        kHeaderBytes +
-        (pl.P > 1 ? sizeof(float) * (size_t)(pl.rec_step * (pl.P - 1) + 1) *
-                        (size_t)(p.B * p.Hkv) * p.rec_floats
-                  : 0);
-    if (need > kNoAllocScratchBytes) return LIZARD_ERR_WORKSPACE;
-    if (!q || !k || !v || !g || !Wf || !y || (p.M > 0 && !sinks)) return LIZARD_ERR_INVALID_ARG;
-    const void* ptrs[] = {q, k, v, g, Wf, sinks, y, lse, S_out, z_out, kcache_out, vcache_out};
-    for (const void* ptr : ptrs)
-        if (ptr && !aligned16_na(ptr)) return LIZARD_ERR_INVALID_ARG;
-    if ((S_out == nullptr) != (z_out == nullptr)) return LIZARD_ERR_INVALID_ARG;
-    if ((kcache_out == nullptr) != (vcache_out == nullptr)) return LIZARD_ERR_INVALID_ARG;
-    if (!((p.d == 64 || p.d == 128) && (p.D == 64 || p.D == 128) && p.B * p.Hkv <= 65535 &&
-          p.B * p.Hq <= ((int64_t)1 << 30)))
-        return LIZARD_ERR_UNSUPPORTED;
-
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return LIZARD_ERR_CUDA;
-    int major = 0, minor = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-        return LIZARD_ERR_CUDA;
-    if (!(major == 10 && minor == 3)) return LIZARD_ERR_UNSUPPORTED;
+    lizard_status st = fwd_check(dims, &p, q, k, v, g, Wf, sinks, y, lse, S_out, z_out,
+                                 kcache_out, vcache_out);
+    if (st != LIZARD_OK) return st;
+    if (noalloc_need(p) > kNoAllocScratchBytes) return LIZARD_ERR_WORKSPACE;
+    st = device_status();
+    if (st != LIZARD_OK) return st;
 
     void* scratch = nullptr;
     if (noalloc_scratch(&scratch) != cudaSuccess) return LIZARD_ERR_CUDA;
     cudaStream_t s = (cudaStream_t)stream;
     // the array keeps the previous call's contents: the status word must start at zero
+    // (boundary records and hand-off marks are always written before they are read)
     if (cudaMemsetAsync(scratch, 0, kHeaderBytes, s) != cudaSuccess) return LIZARD_ERR_CUDA;
 
     FwdArgs a;
@@ -107,8 +99,11 @@ extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const 
     a.seg = (float*)((char*)scratch + kHeaderBytes);
     a.ev_before = nullptr;
     a.ev_after = nullptr;
-    cudaError_t e = fwd_tc_supported(p) ? launch_fwd_tc(p, a, s) : launch_fwd_simt(p, a, s);
-    if (e == cudaSuccess && kcache_out != nullptr)
-        e = launch_ring_fill(p, k, v, kcache_out, vcache_out, s);
-    return e == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA;
+    return fwd_launch(p, a, s) == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA;
+}
+
+extern "C" lizard_status lizard_read_noalloc_status(void* stream) {
+    void* scratch = nullptr;
+    if (noalloc_scratch(&scratch) != cudaSuccess) return LIZARD_ERR_CUDA;
+    return lizard_read_device_status(scratch, stream);
 }

@@ -40,9 +40,14 @@ using namespace lz;
 
 extern "C" lizard_status lizard_selftest_wait_timeout(void* workspace, size_t ws_bytes,
                                                        long long limit_cycles, void* stream) {
-    if (workspace == nullptr || ((uintptr_t)workspace & 15u) != 0) return LIZARD_ERR_INVALID_ARG;
-    if (ws_bytes < kHeaderBytes) return LIZARD_ERR_WORKSPACE;
     if (limit_cycles < 0 || limit_cycles > 4000000000LL) return LIZARD_ERR_INVALID_ARG;
+    if (workspace == nullptr) {
+        // the status word of lizard_attn_fwd_noalloc's fixed scratch (current device)
+        if (noalloc_header(&workspace) != cudaSuccess) return LIZARD_ERR_CUDA;
+        ws_bytes = kHeaderBytes;
+    }
+    if (((uintptr_t)workspace & 15u) != 0) return LIZARD_ERR_INVALID_ARG;
+    if (ws_bytes < kHeaderBytes) return LIZARD_ERR_WORKSPACE;
     int dev = 0, major = 0, minor = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||

@@ -31,7 +31,8 @@ EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_f
             "lizard_status_string",
             "lizard_profile_events", "lizard_version", "lizard_attn_fwd_noalloc",
             "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout", "lizard_attn_fwd_varlen",
-            "lizard_attn_bwd_varlen_workspace", "lizard_attn_bwd_varlen"]
+            "lizard_attn_bwd_varlen_workspace", "lizard_attn_bwd_varlen",
+            "lizard_attn_fwd_noalloc_scratch", "lizard_read_noalloc_status"]
 
 
 class lizard_dims(ctypes.Structure):
@@ -84,6 +85,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_attn_bwd_varlen.restype = ctypes.c_int
     lib.lizard_attn_fwd_noalloc.argtypes = [_DP] + [_VP] * 13
     lib.lizard_attn_fwd_noalloc.restype = ctypes.c_int
+    lib.lizard_attn_fwd_noalloc_scratch.argtypes = [_DP]
+    lib.lizard_attn_fwd_noalloc_scratch.restype = ctypes.c_size_t
+    lib.lizard_read_noalloc_status.argtypes = [_VP]
+    lib.lizard_read_noalloc_status.restype = ctypes.c_int
     lib.lizard_attn_bwd.argtypes = [_DP] + [_VP] * 16 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_bwd.restype = ctypes.c_int
     lib.lizard_decode_step.argtypes = [_DP, ctypes.c_int64] + [_VP] * 12 + [ctypes.c_size_t, _VP]
@@ -196,10 +201,21 @@ def lizard_profile_events(before=None, after=None):
     _check(load().lizard_profile_events(*handles), "lizard_profile_events")
 
 
-def lizard_selftest_wait_timeout(workspace: torch.Tensor, limit_cycles: int, stream=None):
-    """Run the bounded-wait failure path once (see include/lizard.h)."""
-    _check(load().lizard_selftest_wait_timeout(_p(workspace), workspace.numel(), int(limit_cycles),
+def lizard_selftest_wait_timeout(workspace, limit_cycles: int, stream=None):
+    """Run the bounded-wait failure path once (see include/lizard.h).  workspace None targets
+    the status word of lizard_attn_fwd_noalloc's fixed array."""
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(load().lizard_selftest_wait_timeout(_p(workspace), nbytes, int(limit_cycles),
                                                _stream(stream)), "lizard_selftest_wait_timeout")
+
+
+def lizard_read_noalloc_status(stream=None) -> int:
+    """Synchronise the stream, read and clear lizard_attn_fwd_noalloc's status word."""
+    return int(load().lizard_read_noalloc_status(_stream(stream)))
+
+
+def lizard_attn_fwd_noalloc_scratch(dims) -> int:
+    return int(load().lizard_attn_fwd_noalloc_scratch(ctypes.byref(dims)))
 
 
 def lizard_read_device_status(workspace: torch.Tensor, stream=None) -> int:

@@ -128,25 +128,41 @@ lizard_status lizard_attn_fwd_varlen(const lizard_dims* dims, const int64_t* cu_
  * Some callers hold only pointers to their inputs and outputs: a plugin handed tensors
  * by a host framework that owns every device allocation, or a latency-critical loop that
  * must not call cudaMalloc/cudaFree because those can synchronise the whole device.  This
- * call takes no workspace.  It computes exactly what lizard_attn_fwd computes, with the
- * same arguments minus the workspace, and allocates nothing: its scratch (the status
- * word and the per-segment boundary states) is one 32 MiB array in device memory that
- * the library defines at file scope, so every GPU that loads the library holds those
- * 32 MiB until the process exits.
- *   - A problem whose scratch exceeds 32 MiB (256 bytes plus, when the sequence is cut
- *     into P > 1 segments, P * B * Hkv * (D*d + 2*D) * 4 bytes) is rejected with
- *     LIZARD_ERR_WORKSPACE before anything is launched.
+ * call takes no workspace.  It computes exactly what lizard_attn_fwd computes (the same
+ * kernels in the same order, so the results are bit-identical), with the same arguments
+ * minus the workspace and the same argument checks, and allocates nothing: its scratch (the
+ * status word and the per-segment boundary states) is one 32 MiB array in device memory that
+ * the library defines at file scope, so every GPU that loads the library holds those 32 MiB
+ * until the process exits.
+ *   - lizard_attn_fwd_noalloc_scratch(dims) gives the bytes of that array a call needs; a
+ *     problem needing more than 32 MiB is rejected with LIZARD_ERR_WORKSPACE before anything
+ *     is launched.
  *   - The first call on a device looks up the array's device address (with that device
  *     current) and caches it; make that first call before any stream capture.
- *   - All calls share the one array and it keeps the last call's contents (each call
- *     clears the status word on `stream` before its kernels).  Calls whose work overlaps
- *     on the GPU (different streams, or different host threads) race on the array:
- *     order them on one stream. */
+ *   - All calls share the one array and it keeps the last call's contents: each call clears
+ *     the status word on `stream` before its kernels, and every boundary record is written
+ *     before it is read.  Calls whose work overlaps on the GPU (different streams, or
+ *     different host threads) race on the array: order them on one stream.
+ *   - A device-side error of a call (a bounded wait that gave up) is recorded in the array's
+ *     status word; read it with lizard_read_noalloc_status after the call and before the
+ *     next one (the next call clears it). */
 lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const void* q, const void* k,
                                       const void* v, const void* g, const void* Wf,
                                       const float* sinks, void* y, float* lse, float* S_out,
                                       float* z_out, void* kcache_out, void* vcache_out,
                                       void* stream);
+
+/* Bytes of lizard_attn_fwd_noalloc's 32 MiB array that a call with these sizes uses: 256
+ * (status word) plus the boundary-state records of its launch, R * B * Hkv * (D*d + 2*D) * 4,
+ * with R the number of records its segmentation writes (at least 1 on the tensor-core path,
+ * 0 on the SIMT path when the sequence is one segment).  0 for invalid sizes.  Pure host
+ * query; no counterpart on the Lizard pages. */
+size_t lizard_attn_fwd_noalloc_scratch(const lizard_dims* dims);
+
+/* Synchronise `stream`, read and clear the status word of lizard_attn_fwd_noalloc's array on
+ * the current device.  Returns LIZARD_OK or the error a kernel of the last call recorded
+ * (e.g. LIZARD_ERR_TIMEOUT).  No counterpart on the Lizard pages. */
+lizard_status lizard_read_noalloc_status(void* stream);
 
 /* Bytes of device workspace lizard_attn_bwd needs: segment records whose size depends on
  * B, Hkv, d and D only, plus one fp32 per gate element (B * L * Hkv * D * 4 bytes) holding
@@ -228,7 +244,8 @@ lizard_status lizard_read_device_status(void* workspace, void* stream);
  * gives up after limit_cycles SM cycles (at most 4e9, about two seconds) exactly like the
  * tensor-core kernels' waits, records LIZARD_ERR_TIMEOUT in the workspace status word,
  * frees its TMEM and returns.  No fault, no hang: the context stays usable.  Read the
- * result with lizard_read_device_status. */
+ * result with lizard_read_device_status.  workspace NULL targets the status word of
+ * lizard_attn_fwd_noalloc's array instead (read it with lizard_read_noalloc_status). */
 lizard_status lizard_selftest_wait_timeout(void* workspace, size_t ws_bytes,
                                            long long limit_cycles, void* stream);
 

@@ -1,8 +1,11 @@
 """The C ABI: the library loads, exports what include/lizard.h declares, and rejects bad
 arguments on the host before touching the GPU (no compute call here)."""
 import ctypes
+import json
 import os
 import re
+import subprocess
+import sys
 
 import pytest
 
@@ -73,42 +76,61 @@ def test_invalid_dims_rejected(lib, bad):
     assert st == lz.LIZARD_ERR_INVALID_ARG
 
 
+def _no_device_calls():
+    """Run tests/_abi_calls.py with no visible CUDA device and return its status codes."""
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    script = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_abi_calls.py")
+    r = subprocess.run([sys.executable, script], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr
+    return json.loads(r.stdout.strip().splitlines()[-1])
+
+
 def test_null_and_misaligned_pointers_rejected(lib):
-    d = dims(L=128)
-    fake = ctypes.c_void_p(0x10000)  # never dereferenced: validation fails first
-    mis = ctypes.c_void_p(0x10004)
-    args = [fake] * 6 + [fake] + [None] * 5 + [fake]
-    st = lib.lizard_attn_fwd(ctypes.byref(d), None, *args[1:], 1 << 30, None)
-    assert st == lz.LIZARD_ERR_INVALID_ARG
-    args2 = list(args)
-    args2[2] = mis
-    st = lib.lizard_attn_fwd(ctypes.byref(d), *args2, 1 << 30, None)
-    assert st == lz.LIZARD_ERR_INVALID_ARG
-    # S_out without z_out
-    args3 = list(args)
-    args3[8] = fake
-    st = lib.lizard_attn_fwd(ctypes.byref(d), *args3, 1 << 30, None)
-    assert st == lz.LIZARD_ERR_INVALID_ARG
+    """Null, misaligned and unpaired pointers, unsupported sizes and a short workspace are
+    refused on the host.  The calls that need non-null pointers get host buffers, in a child
+    process that sees no CUDA device, so none of them can launch anything."""
+    st = _no_device_calls()
+    bad = lz.LIZARD_ERR_INVALID_ARG
+    for case in ("fwd_null_q", "fwd_misaligned_v", "fwd_S_without_z", "fwd_misaligned_ws",
+                 "noalloc_misaligned", "dec_neg_pos", "dec_misaligned"):
+        assert st[case] == bad, (case, st[case])
+    assert st["fwd_unsupported"] == lz.LIZARD_ERR_UNSUPPORTED
+    assert st["fwd_small_ws"] == lz.LIZARD_ERR_WORKSPACE
+    assert st["dec_w300"] == lz.LIZARD_ERR_UNSUPPORTED
+    assert st["dec_G16"] == lz.LIZARD_ERR_UNSUPPORTED
+    assert st["fwd_no_device"] == lz.LIZARD_ERR_CUDA
 
 
-def test_unsupported_and_workspace_errors(lib):
-    fake = ctypes.c_void_p(0x10000)
-    d = dims(d=96, D=96)
-    args = [fake] * 7 + [None] * 5 + [fake]
-    assert lib.lizard_attn_fwd(ctypes.byref(d), *args, 1 << 30, None) == \
-        lz.LIZARD_ERR_UNSUPPORTED
+def test_null_pointer_checks_in_process(lib):
+    """With every tensor pointer null the forward, backward and decode entry points refuse the
+    call before any device work."""
     d = dims(L=128)
-    need = lz.lizard_attn_fwd_workspace(d)
-    assert lib.lizard_attn_fwd(ctypes.byref(d), *args, need - 16, None) == \
-        lz.LIZARD_ERR_WORKSPACE
-    # decode: window beyond the staged maximum, and G beyond 8
-    nul = [fake] * 12
-    assert lib.lizard_decode_step(ctypes.byref(dims(w=300)), 0, *nul, 256, None) == \
-        lz.LIZARD_ERR_UNSUPPORTED
-    assert lib.lizard_decode_step(ctypes.byref(dims(Hq=32, Hkv=2)), 0, *nul, 256, None) == \
-        lz.LIZARD_ERR_UNSUPPORTED
-    assert lib.lizard_decode_step(ctypes.byref(dims()), -1, *nul, 256, None) == \
+    nul = [None] * 13
+    assert lib.lizard_attn_fwd(ctypes.byref(d), *nul, 1 << 30, None) == lz.LIZARD_ERR_INVALID_ARG
+    assert lib.lizard_attn_fwd_noalloc(ctypes.byref(d), *([None] * 13)) == \
         lz.LIZARD_ERR_INVALID_ARG
+    assert lib.lizard_attn_bwd(ctypes.byref(d), *([None] * 16), 1 << 30, None) == \
+        lz.LIZARD_ERR_INVALID_ARG
+    assert lib.lizard_decode_step(ctypes.byref(d), 0, *([None] * 12), 256, None) == \
+        lz.LIZARD_ERR_INVALID_ARG
+
+
+def test_noalloc_scratch_query(lib):
+    """The fixed array's use: 256 bytes plus one 66,560-byte boundary record per unit and
+    record of the launch (tensor-core shape: at least one record)."""
+    rec = (128 * 128 + 2 * 128) * 4
+    small = lz.lizard_attn_fwd_noalloc_scratch(dims(L=64))
+    assert (small - 256) % (8 * rec) == 0
+    # the tensor-core path needs the driver's TMA encoder; without it the one-segment SIMT
+    # launch uses no record
+    tc = lz.lizard_attn_fwd_kernel(dims(L=64)) == 1
+    assert small == 256 + 8 * rec if tc else small == 256
+    if tc:
+        assert lz.lizard_attn_fwd_noalloc_scratch(dims(B=64, L=64)) > 32 << 20
+    f32 = lz.lizard_attn_fwd_noalloc_scratch(dims(B=37, L=4096, dtype=lz.LIZARD_F32))
+    assert f32 > 32 << 20 and (f32 - 256) % (37 * 8 * rec) == 0
+    assert lz.lizard_attn_fwd_noalloc_scratch(dims(Hq=30)) == 0
 
 
 def test_kernel_path_query(lib):
