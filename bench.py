@@ -38,6 +38,7 @@ def parse():
     ap.add_argument("--decode-prefill", type=int, default=32768)
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-train", action="store_true")
+    ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -75,6 +76,17 @@ def decode_algorithmic_bytes(wl) -> int:
     unit = 2 * wl.D * wl.d * 4 + 2 * wl.D * 4 + 2 * wl.w * wl.d * e + 2 * wl.d * e
     per_b = wl.Hkv * unit + 2 * wl.Hq * wl.d * e + 2 * wl.Hkv * wl.d * e + wl.Hkv * wl.D * e
     return wl.B * per_b + wl.Hkv * wl.d * (wl.D // 2) * e
+
+
+def bwd_algorithmic_bytes(wl) -> int:
+    """One read of q, k, v, g, Wf, sinks, y, dy and lse and one write of dq, dk, dv, dg, dWf
+    and dsinks."""
+    e = 2 if wl.dtype == "bf16" else 4
+    toks = wl.B * wl.L
+    per_tok = (3 * wl.Hq * wl.d + 2 * wl.Hkv * wl.d + wl.Hkv * wl.D) * e + wl.Hq * 4  # in
+    per_tok += (wl.Hq * wl.d + 2 * wl.Hkv * wl.d + wl.Hkv * wl.D) * e                # out
+    params = wl.Hkv * wl.d * (wl.D // 2) * (e + 4) + wl.Hq * wl.M * 8
+    return toks * per_tok + params
 
 
 def load_peaks():
@@ -299,13 +311,14 @@ def run_ours(args, rank, world, device):
                            wl.w, y=y, workspace=ws)
 
     # launches per forward call: segment pass + scan (when the sequence is split) + chunk walk
+    # + the exact tail walk (its CTAs return at once unless a step was handed to it)
     import math
     U = wl.B * wl.Hkv
     pmax = min(64, max(1, math.ceil(304 / U)))
     nch = math.ceil(wl.L / 64)
     segc = math.ceil(nch / pmax)
     plan_p = math.ceil(nch / segc)
-    launches_per_fwd = 3 if plan_p > 1 else 1
+    launches_per_fwd = (3 if plan_p > 1 else 1) + 1
 
     sampler = ClockSampler(smi_id(device.index or 0))
     sampler.start()
@@ -424,6 +437,9 @@ def run_ours(args, rank, world, device):
     train = None
     if not args.no_train:
         train = run_train(args, device, lz, I)
+    long = None
+    if not args.no_long:
+        long = run_long(args, device, lz, I)
     clocks = sampler.stop()
 
     tokens = wl.B * wl.L
@@ -460,6 +476,8 @@ def run_ours(args, rank, world, device):
         out["decode"] = decode
     if train is not None:
         out["train"] = train
+    if long is not None:
+        out["long_context"] = long
     return out
 
 
@@ -504,9 +522,62 @@ def run_train(args, device, lz, I):
     torch.cuda.synchronize()
     fwd_ms = sum(a.elapsed_time(b) for a, b, _ in evs) / n
     bwd_ms = sum(b.elapsed_time(c) for _, b, c in evs) / n
+    hbm_peak, _, peak_src = load_peaks()
+    fb, bb = fwd_algorithmic_bytes(wl) + B * L * Hq * 4, bwd_algorithmic_bytes(wl)
     return {"workload": wl.name, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
             "step_ms": fwd_ms + bwd_ms, "tokens_per_s": B * L / ((fwd_ms + bwd_ms) * 1e-3),
-            "timing": "CUDA events, 512 MiB L2 flush before each step, mean of 3"}
+            "timing": "CUDA events, 512 MiB L2 flush before each step, mean of 3",
+            "roofline": {"bound": "hbm", "peak": hbm_peak, "unit": "GB/s",
+                         "peak_source": peak_src,
+                         "fwd_algorithmic_bytes": fb, "bwd_algorithmic_bytes": bb,
+                         "bwd_achieved": bb / (bwd_ms * 1e-3) / 1e9,
+                         "bwd_frac": bb / (bwd_ms * 1e-3) / 1e9 / hbm_peak,
+                         "step_frac": (fb + bb) / ((fwd_ms + bwd_ms) * 1e-3) / 1e9 / hbm_peak}}
+
+
+def run_long(args, device, lz, I):
+    """The L = 65536 stress workload (gate mixture 0.7 N(4,1) + 0.3 N(-3,1)): forward tokens/s
+    and the workspace, which holds the same number of boundary records as at L = 8192."""
+    import torch
+
+    wl = I.STRESS_L64K
+    t = I.make_device_inputs(wl, device)
+    y = torch.empty_like(t["q"])
+    dims = lz.dims_of(t["q"], t["k"], t["g"], t["sinks"], wl.w)
+    ws_bytes = lz.lizard_attn_fwd_workspace(dims)
+    ws = lz.new_workspace(ws_bytes, device)
+    short = lz.make_dims(wl.B, 8192, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, torch.bfloat16)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def fwd():
+        lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w, y=y,
+                           workspace=ws)
+
+    for _ in range(2):
+        fwd()
+    torch.cuda.synchronize()
+    n = 5
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n)]
+    for e0, e1 in evs:
+        flush.zero_()
+        e0.record()
+        fwd()
+        e1.record()
+    torch.cuda.synchronize()
+    ms = sum(a.elapsed_time(b) for a, b in evs) / n
+    st = lz.lizard_read_device_status(ws)
+    if st != lz.LIZARD_OK:
+        raise RuntimeError(f"long forward device status {lz.status_string(st)}")
+    hbm_peak, _, peak_src = load_peaks()
+    ab = fwd_algorithmic_bytes(wl)
+    return {"workload": wl.name, "ms": ms, "tokens_per_s": wl.B * wl.L / (ms * 1e-3),
+            "workspace_bytes": ws_bytes,
+            "workspace_bytes_at_L8192": lz.lizard_attn_fwd_workspace(short),
+            "roofline": {"bound": "hbm", "achieved": ab / (ms * 1e-3) / 1e9, "peak": hbm_peak,
+                         "frac": ab / (ms * 1e-3) / 1e9 / hbm_peak, "algorithmic_bytes": ab,
+                         "peak_source": peak_src, "scope": "whole forward"},
+            "timing": "CUDA events, 512 MiB L2 flush before each call, mean of 5"}
 
 
 def run_decode(args, device, lz, I, hbm_peak, peak_src):
@@ -587,12 +658,15 @@ def run_decode(args, device, lz, I, hbm_peak, peak_src):
     bytes_step = decode_algorithmic_bytes(wl)
     achieved = bytes_step / (ms_cold * 1e-3) / 1e9
     return {"workload": wl.name, "prefill": T0, "steps": steps,
-            "steps_per_s": 1e3 / ms_graph, "tokens_per_s": B * 1e3 / ms_graph,
-            "ms_per_step": ms_graph,
-            "timing": "1024 consecutive steps replayed as one CUDA graph (state L2-resident "
-                      "across steps, as in a decode loop); roofline from per-step events with "
-                      "a 512 MiB L2 flush before each step",
+            "steps_per_s": 1e3 / ms_cold, "tokens_per_s": B * 1e3 / ms_cold,
+            "ms_per_step": ms_cold,
+            "timing": "per-step CUDA events with a 512 MiB L2 flush before each step (the "
+                      "state streams from HBM, as in a model whose layers' states do not all "
+                      "fit in L2); also 1024 consecutive steps replayed as one CUDA graph "
+                      "with the 86 MB state L2-resident across steps",
             "ms_per_step_l2_flushed": ms_cold,
+            "ms_per_step_graph_l2_resident": ms_graph,
+            "steps_per_s_graph_l2_resident": 1e3 / ms_graph,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                          "frac": achieved / hbm_peak, "algorithmic_bytes": bytes_step,
                          "peak_source": peak_src, "kernel": "decode step"}}

@@ -39,6 +39,29 @@ __host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return
 // state terms' factor e^{-m} below e^{60}.
 constexpr float kMinShift = -60.0f;
 
+// Programmatic dependent launch.  A kernel launched with launch_dependent() may start while
+// the previous kernel of the stream still runs: it must call grid_dep_wait() before it reads
+// anything that kernel writes (a no-op when the launch carried no such dependency).  A kernel
+// calls grid_dep_launch() to let the next one be launched before it completes.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t s, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 // Device status word at the head of every workspace.
 struct WsHeader {
     unsigned int status;

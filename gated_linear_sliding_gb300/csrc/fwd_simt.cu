@@ -64,6 +64,8 @@ __global__ void __launch_bounds__(NT, 1) fwd_simt_seglocal(Plan p, FwdArgs a) {
 
 // Exclusive scan over segments, in place: record p becomes the state before segment p.
 __global__ void fwd_seg_scan(Plan p, float* seg) {
+    grid_dep_wait();  // the segment records of the pass before
+    grid_dep_launch();
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     const int64_t unit = blockIdx.y;
     const int64_t nE = p.D * p.d + p.D;
@@ -275,6 +277,7 @@ __global__ void __launch_bounds__(NT, 1) fwd_simt_main(Plan p, FwdArgs a) {
 template <typename T, int DH, int DF, bool FAST>
 __global__ void __launch_bounds__(NT, 1) fwd_simt_tail(Plan p, FwdArgs a) {
     extern __shared__ float sm[];
+    grid_dep_wait();  // the main walk's marks and hand-off states
     const int64_t unit = blockIdx.x, seg = blockIdx.y;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
     const float* ho =
@@ -379,13 +382,15 @@ cudaError_t launch_fwd_tail(const Plan& p, const FwdArgs& a, cudaStream_t s) {
     const cudaError_t e =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Ly::bytes);
     if (e != cudaSuccess) return e;
-    kern<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, Ly::bytes, s>>>(p, a);
-    return cudaGetLastError();
+    return launch_dependent(kern, dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), dim3(NT),
+                            Ly::bytes, s, p, a);
 }
 
-cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s) {
+cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s, bool dependent) {
     const unsigned nE = (unsigned)(p.D * p.d + p.D);
-    fwd_seg_scan<<<dim3((nE + 255) / 256, (unsigned)(p.B * p.Hkv)), 256, 0, s>>>(p, seg);
+    const dim3 grid((nE + 255) / 256, (unsigned)(p.B * p.Hkv));
+    if (dependent) return launch_dependent(fwd_seg_scan, grid, dim3(256), 0, s, p, seg);
+    fwd_seg_scan<<<grid, 256, 0, s>>>(p, seg);
     return cudaGetLastError();
 }
 

@@ -344,6 +344,7 @@ __global__ void __launch_bounds__(NT, 1)
         tmem_alloc(&S.tmem, 512);
         tmem_relinquish();
     }
+    grid_dep_launch();  // the tail walk may be launched now (it waits for this grid's end)
     if (tid == 0) {
         mbar_init(&S.bar_tma, 1);
         mbar_init(&S.bar_u, 1);
@@ -378,6 +379,7 @@ __global__ void __launch_bounds__(NT, 1)
     const float* rec =
         seg > 0 ? a.seg + ((size_t)(seg * p.rec_step) * (size_t)U + (size_t)unit) * p.rec_floats
                 : nullptr;
+    grid_dep_wait();  // the records come from the scan launched just before
     if (rec != nullptr) stage_record_in(sm + oK, rec);
     if (tid < DF) S.z[tid] = rec ? rec[DF * DH + tid] : 0.0f;
     __syncthreads();
@@ -930,6 +932,7 @@ __global__ void __launch_bounds__(NL, 1)
         S.abort = 0;
     }
     if (tid < DF) S.z[tid] = 0.0f;
+    grid_dep_launch();  // the scan may be launched now (it waits for this grid's end)
     __syncthreads();
     tc_fence_after();
     const uint32_t tb = S.tmem;
@@ -1220,7 +1223,9 @@ cudaError_t launch_local_and_scan(const Plan& p, const FwdArgs& a, const CUtenso
                                          (int)kLocalSmem);
     if (e != cudaSuccess) return e;
     fwd_tc_local<<<dim3(U, (unsigned)(p.P - 1)), NL, kLocalSmem, s>>>(lk, lv, mw, lg, p, a);
-    return launch_seg_scan(p, a.seg, s);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    return launch_seg_scan(p, a.seg, s, true);
 }
 
 bool make_wf_map(CUtensorMap* mw, const void* Wf, int64_t Hkv) {
@@ -1311,10 +1316,14 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
         if (e != cudaSuccess) return e;
     }
     if (a.ev_before) cudaEventRecord(a.ev_before, s);
-    fwd_tc_kernel<<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, my, p,
-                                                                        a);
+    if (p.P > 1 && a.ev_before == nullptr)  // starts while the scan finishes
+        e = launch_dependent(fwd_tc_kernel, dim3(U, (unsigned)p.P), dim3(NT), kSmemBytes, s, mq,
+                             mk, mv, mw, mg, my, p, a);
+    else
+        fwd_tc_kernel<<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, my, p,
+                                                                            a);
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
-    e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     // segments handed over at a strongly closed step are finished by the exact walk
     return launch_fwd_tail(p, a, s);

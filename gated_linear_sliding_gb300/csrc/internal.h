@@ -64,8 +64,9 @@ struct FwdArgs {
 cudaError_t launch_fwd_simt(const Plan& p, const FwdArgs& a, cudaStream_t s);
 // Segment-start states only (segment pass + scan into a.seg), for the backward.
 cudaError_t launch_fwd_states(const Plan& p, const FwdArgs& a, cudaStream_t s);
-// fp32 exclusive scan over the segment records (in place).
-cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s);
+// fp32 exclusive scan over the segment records (in place).  dependent: launched to start while
+// the kernel before it (the one writing the records) finishes.
+cudaError_t launch_seg_scan(const Plan& p, float* seg, cudaStream_t s, bool dependent = false);
 bool fwd_tc_supported(const Plan& p);
 cudaError_t launch_fwd_tc(const Plan& p, const FwdArgs& a, cudaStream_t s);
 // Exact SIMT walk of the segments the tensor-core main walk handed over at a strongly closed
