@@ -172,6 +172,26 @@ def make_inputs(wl: Workload, L: int | None = None, B: int | None = None,
     return out
 
 
+def make_proj_inputs(wl: Workload, dm: int, L: int | None = None, B: int | None = None,
+                     with_grads: bool = False, seed_offset: int = 100) -> dict:
+    """Inputs of the projections in front of the mixer: the layer input x [B, L, dm] ~ N(0, 1)
+    and the stacked weight W [N, dm] ~ N(0, 1/dm), N = Hq d + 2 Hkv d + Hkv D (rows q, k, v,
+    gate), rounded to the workload's dtype; optionally upstream gradients dq, dk, dv, dg ~
+    N(0, 1).  Own stream: seed = 1000 * (workload seed + seed_offset)."""
+    L = wl.L if L is None else L
+    B = wl.B if B is None else B
+    rng = np.random.Generator(np.random.PCG64(1000 * (wl.seed + seed_offset)))
+    N = wl.Hq * wl.d + 2 * wl.Hkv * wl.d + wl.Hkv * wl.D
+    x = rng.standard_normal((B, L, dm), dtype=np.float32)
+    W = rng.standard_normal((N, dm), dtype=np.float32) * np.float32(1.0 / math.sqrt(dm))
+    out = {"x": round_to(x, wl.dtype), "W": round_to(W, wl.dtype)}
+    if with_grads:
+        for n, h, e in (("dq", wl.Hq, wl.d), ("dk", wl.Hkv, wl.d), ("dv", wl.Hkv, wl.d),
+                        ("dg", wl.Hkv, wl.D)):
+            out[n] = round_to(rng.standard_normal((B, L, h, e), dtype=np.float32), wl.dtype)
+    return out
+
+
 def make_decode_inputs(wl: Workload, batch_index: int, T: int) -> dict:
     """Inputs of one sequence of a decode workload: T = prefill + steps tokens.
 

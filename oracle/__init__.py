@@ -6,6 +6,8 @@ and this package imports nothing from the product package.
 
 The main oracle is the token-by-token recurrence in `lizard_oracle.c` (plain C,
 fp64, OpenMP over (batch, KV head) units), loaded here with ctypes.  The
+projections in front of the mixer (q, k, v and the gate logits from the layer
+input) are plain fp64 matrix products, `qkvg_proj` and `qkvg_proj_bwd`.  The
 alternate forms in `forms.py` (brute force, quadratic-parallel, chunked with
 explicit products, chunked in log space) exist to pin it.
 
@@ -142,3 +144,31 @@ def bwd(q, k, v, g, Wf, sinks, dy, w: int, scale: float | None = None) -> dict:
     if rc != 0:
         raise ValueError("ora_bwd rejected its arguments")
     return out
+
+
+def qkvg_proj(x, W, Hq: int, Hkv: int, d: int, D: int) -> dict:
+    """The projections in front of the mixer, in fp64: [q | k | v | g] = x W^T.
+
+    Lizard summary sec. 2-A-1: the gate logits are a learned projection of the layer input
+    (Gamma_i = sigmoid(W_gamma x_i)), next to the attention projections of q, k and v.
+    x [B, L, dm]; W [N, dm] with N = Hq d + 2 Hkv d + Hkv D, its rows in the order q, k, v, g.
+    Returns q [B, L, Hq, d], k, v [B, L, Hkv, d], g [B, L, Hkv, D]."""
+    x = np.asarray(x, np.float64)
+    W = np.asarray(W, np.float64)
+    B, L, dm = x.shape
+    y = x.reshape(B * L, dm) @ W.T
+    n = np.cumsum([0, Hq * d, Hkv * d, Hkv * d, Hkv * D])
+    shapes = [(Hq, d), (Hkv, d), (Hkv, d), (Hkv, D)]
+    return {name: y[:, n[i]:n[i + 1]].reshape(B, L, *shapes[i])
+            for i, name in enumerate(("q", "k", "v", "g"))}
+
+
+def qkvg_proj_bwd(x, W, dq, dk, dv, dg) -> dict:
+    """Gradients of qkvg_proj: with dY = [dq | dk | dv | dg] (flattened per token),
+    dx = dY W and dW = dY^T x, in fp64."""
+    x = np.asarray(x, np.float64)
+    W = np.asarray(W, np.float64)
+    B, L, dm = x.shape
+    dY = np.concatenate([np.asarray(t, np.float64).reshape(B * L, -1) for t in (dq, dk, dv, dg)],
+                        axis=1)
+    return {"dx": (dY @ W).reshape(B, L, dm), "dW": dY.T @ x.reshape(B * L, dm)}
