@@ -39,6 +39,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-train", action="store_true")
     ap.add_argument("--no-long", action="store_true")
+    ap.add_argument("--no-proj", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -440,6 +441,9 @@ def run_ours(args, rank, world, device):
     long = None
     if not args.no_long:
         long = run_long(args, device, lz, I)
+    proj = None
+    if not args.no_proj:
+        proj = run_proj(args, device, lz, I)
     clocks = sampler.stop()
 
     tokens = wl.B * wl.L
@@ -478,6 +482,8 @@ def run_ours(args, rank, world, device):
         out["train"] = train
     if long is not None:
         out["long_context"] = long
+    if proj is not None:
+        out["projection"] = proj
     return out
 
 
@@ -533,6 +539,59 @@ def run_train(args, device, lz, I):
                          "bwd_achieved": bb / (bwd_ms * 1e-3) / 1e9,
                          "bwd_frac": bb / (bwd_ms * 1e-3) / 1e9 / hbm_peak,
                          "step_frac": (fb + bb) / ((fwd_ms + bwd_ms) * 1e-3) / 1e9 / hbm_peak}}
+
+
+def run_proj(args, device, lz, I):
+    """The projections in front of the mixer at the LLaMA-3-8B layer: x [8192, 4096] times the
+    stacked q, k, v, gate weight [7168, 4096] (one tcgen05 GEMM), and its backward (dx, dW)."""
+    import torch
+
+    wl = I.LLAMA3_8B_L8K
+    dm, T = 4096, wl.B * wl.L
+    N = wl.Hq * wl.d + 2 * wl.Hkv * wl.d + wl.Hkv * wl.D
+    gen = torch.Generator(device=device)
+    gen.manual_seed(1234)
+    x = torch.randn(wl.B, wl.L, dm, generator=gen, device=device).to(torch.bfloat16)
+    W = (torch.randn(N, dm, generator=gen, device=device) / dm ** 0.5).to(torch.bfloat16)
+    q = torch.empty(wl.B, wl.L, wl.Hq, wl.d, dtype=torch.bfloat16, device=device)
+    k = torch.empty(wl.B, wl.L, wl.Hkv, wl.d, dtype=torch.bfloat16, device=device)
+    v = torch.empty_like(k)
+    g = torch.empty(wl.B, wl.L, wl.Hkv, wl.D, dtype=torch.bfloat16, device=device)
+    dx = torch.empty_like(x)
+    dW = torch.empty(N, dm, dtype=torch.float32, device=device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def fwd():
+        lz.lizard_qkvg_proj(x, W, wl.Hq, wl.Hkv, wl.d, wl.D, q=q, k=k, v=v, g=g)
+
+    def bwd():
+        lz.lizard_qkvg_proj_bwd(x, W, q, k, v, g, dx=dx, dW=dW)
+
+    def timed(fn, n=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / n
+
+    f_ms, b_ms = timed(fwd), timed(bwd)
+    _, tc_peak, peak_src = load_peaks()
+    flops = 2.0 * T * N * dm
+    return {"workload": f"qkvg_proj_T{T}_dm{dm}_N{N}", "fwd_ms": f_ms, "bwd_ms": b_ms,
+            "roofline": {"bound": "tensor", "unit": "TFLOP/s", "peak": tc_peak,
+                         "peak_source": peak_src + " (bf16 burst)",
+                         "fwd_achieved": flops / (f_ms * 1e-3) / 1e12,
+                         "fwd_frac": flops / (f_ms * 1e-3) / 1e12 / tc_peak,
+                         "bwd_achieved": 2 * flops / (b_ms * 1e-3) / 1e12,
+                         "bwd_frac": 2 * flops / (b_ms * 1e-3) / 1e12 / tc_peak},
+            "timing": "CUDA events, 512 MiB L2 flush before each call, mean of 5"}
 
 
 def run_long(args, device, lz, I):

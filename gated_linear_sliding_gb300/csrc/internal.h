@@ -128,6 +128,15 @@ cudaError_t launch_bwd_win_tc(const Plan& p, const BwdArgs& a, const float* rows
                               cudaStream_t s);
 cudaError_t launch_bwd(const Plan& p, const BwdArgs& a, cudaStream_t s);
 
+// The projections in front of the mixer (tcgen05 GEMMs).  proj_supported: bf16, dm a multiple
+// of 64, each of Hq d, Hkv d, Hkv D a multiple of 128; *bn is the output tile width.
+bool proj_supported(const Plan& p, int64_t dm, int* bn);
+cudaError_t launch_proj_fwd(const Plan& p, int64_t dm, const void* x, const void* W, void* q,
+                            void* k, void* v, void* g, void* hdr, cudaStream_t s);
+cudaError_t launch_proj_bwd(const Plan& p, int64_t dm, const void* x, const void* W,
+                            const void* dq, const void* dk, const void* dv, const void* dg,
+                            void* dx, float* dW, void* hdr, cudaStream_t s);
+
 // Device address of the status header of lizard_attn_fwd_noalloc's fixed scratch on the
 // current device (looked up once per device).
 cudaError_t noalloc_header(void** out);

@@ -441,6 +441,43 @@ lizard_status lizard_decode_step_positions(const lizard_dims* dims, const int64_
                        ws_bytes, stream);
 }
 
+// Checks shared by the two projection entry points.
+static lizard_status proj_check(const lizard_dims* dims, int64_t dmodel, Plan* p,
+                                const void* const* ptrs, int n, void* workspace,
+                                size_t ws_bytes) {
+    if (!make_plan(dims, p) || dmodel < 1) return LIZARD_ERR_INVALID_ARG;
+    for (int i = 0; i < n; ++i)
+        if (ptrs[i] == nullptr || !aligned16(ptrs[i])) return LIZARD_ERR_INVALID_ARG;
+    if (workspace != nullptr && !aligned16(workspace)) return LIZARD_ERR_INVALID_ARG;
+    int bn = 0;
+    if (!proj_supported(*p, dmodel, &bn)) return LIZARD_ERR_UNSUPPORTED;
+    if (workspace != nullptr && ws_bytes < kHeaderBytes) return LIZARD_ERR_WORKSPACE;
+    return device_status();
+}
+
+lizard_status lizard_qkvg_proj(const lizard_dims* dims, int64_t dmodel, const void* x,
+                               const void* W, void* q, void* k, void* v, void* g,
+                               void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    const void* ptrs[] = {x, W, q, k, v, g};
+    const lizard_status st = proj_check(dims, dmodel, &p, ptrs, 6, workspace, ws_bytes);
+    if (st != LIZARD_OK) return st;
+    return from_cuda(launch_proj_fwd(p, dmodel, x, W, q, k, v, g, workspace,
+                                     (cudaStream_t)stream));
+}
+
+lizard_status lizard_qkvg_proj_bwd(const lizard_dims* dims, int64_t dmodel, const void* x,
+                                   const void* W, const void* dq, const void* dk,
+                                   const void* dv, const void* dg, void* dx, float* dW,
+                                   void* workspace, size_t ws_bytes, void* stream) {
+    Plan p;
+    const void* ptrs[] = {x, W, dq, dk, dv, dg, dx, dW};
+    const lizard_status st = proj_check(dims, dmodel, &p, ptrs, 8, workspace, ws_bytes);
+    if (st != LIZARD_OK) return st;
+    return from_cuda(launch_proj_bwd(p, dmodel, x, W, dq, dk, dv, dg, dx, dW, workspace,
+                                     (cudaStream_t)stream));
+}
+
 lizard_status lizard_read_device_status(void* workspace, void* stream) {
     if (workspace == nullptr || !aligned16(workspace)) return LIZARD_ERR_INVALID_ARG;
     cudaStream_t s = (cudaStream_t)stream;

@@ -32,7 +32,8 @@ EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_f
             "lizard_profile_events", "lizard_version", "lizard_attn_fwd_noalloc",
             "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout", "lizard_attn_fwd_varlen",
             "lizard_attn_bwd_varlen_workspace", "lizard_attn_bwd_varlen",
-            "lizard_attn_fwd_noalloc_scratch", "lizard_read_noalloc_status"]
+            "lizard_attn_fwd_noalloc_scratch", "lizard_read_noalloc_status",
+            "lizard_qkvg_proj", "lizard_qkvg_proj_bwd"]
 
 
 class lizard_dims(ctypes.Structure):
@@ -89,6 +90,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_attn_fwd_noalloc_scratch.restype = ctypes.c_size_t
     lib.lizard_read_noalloc_status.argtypes = [_VP]
     lib.lizard_read_noalloc_status.restype = ctypes.c_int
+    lib.lizard_qkvg_proj.argtypes = [_DP, ctypes.c_int64] + [_VP] * 7 + [ctypes.c_size_t, _VP]
+    lib.lizard_qkvg_proj.restype = ctypes.c_int
+    lib.lizard_qkvg_proj_bwd.argtypes = [_DP, ctypes.c_int64] + [_VP] * 9 + [ctypes.c_size_t, _VP]
+    lib.lizard_qkvg_proj_bwd.restype = ctypes.c_int
     lib.lizard_attn_bwd.argtypes = [_DP] + [_VP] * 16 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_bwd.restype = ctypes.c_int
     lib.lizard_decode_step.argtypes = [_DP, ctypes.c_int64] + [_VP] * 12 + [ctypes.c_size_t, _VP]
@@ -441,3 +446,54 @@ def lizard_decode_step_positions(pos, q, k, v, g, Wf, sinks, S, z, kcache, vcach
                                              workspace.numel(), _stream(stream))
     _check(st, "lizard_decode_step_positions")
     return y
+
+
+def lizard_qkvg_proj(x, W, Hq: int, Hkv: int, d: int, D: int, *, q=None, k=None, v=None,
+                     g=None, workspace=None, stream=None):
+    """[q | k | v | g] = x W^T on the tensor cores.  x [B, L, dm], W [N, dm] (bf16).
+    Returns (q, k, v, g) in the mixer's layouts (allocated if not given)."""
+    B, L, dm = x.shape
+    N = Hq * d + 2 * Hkv * d + Hkv * D
+    _need(x, "x", (B, L, dm), torch.bfloat16)
+    _need(W, "W", (N, dm), torch.bfloat16)
+    outs = []
+    for t, name, shape in ((q, "q", (B, L, Hq, d)), (k, "k", (B, L, Hkv, d)),
+                           (v, "v", (B, L, Hkv, d)), (g, "g", (B, L, Hkv, D))):
+        if t is None:
+            t = torch.empty(shape, dtype=torch.bfloat16, device=x.device)
+        _need(t, name, shape, torch.bfloat16)
+        outs.append(t)
+    dims = make_dims(B, L, Hq, Hkv, d, D, 1, 0, LIZARD_BF16)
+    nb = 0 if workspace is None else workspace.numel()
+    st = load().lizard_qkvg_proj(ctypes.byref(dims), dm, _p(x), _p(W), *[_p(t) for t in outs],
+                                 _p(workspace), nb, _stream(stream))
+    _check(st, "lizard_qkvg_proj")
+    return tuple(outs)
+
+
+def lizard_qkvg_proj_bwd(x, W, dq, dk, dv, dg, *, dx=None, dW=None, workspace=None,
+                         stream=None):
+    """dx = dY W (bf16) and dW = dY^T x (fp32) for dY = [dq | dk | dv | dg]."""
+    B, L, dm = x.shape
+    Hq, d = dq.shape[2], dq.shape[3]
+    Hkv, D = dg.shape[2], dg.shape[3]
+    N = Hq * d + 2 * Hkv * d + Hkv * D
+    _need(x, "x", (B, L, dm), torch.bfloat16)
+    _need(W, "W", (N, dm), torch.bfloat16)
+    _need(dq, "dq", (B, L, Hq, d), torch.bfloat16)
+    _need(dk, "dk", (B, L, Hkv, d), torch.bfloat16)
+    _need(dv, "dv", (B, L, Hkv, d), torch.bfloat16)
+    _need(dg, "dg", (B, L, Hkv, D), torch.bfloat16)
+    if dx is None:
+        dx = torch.empty_like(x)
+    if dW is None:
+        dW = torch.empty(N, dm, dtype=torch.float32, device=x.device)
+    _need(dx, "dx", (B, L, dm), torch.bfloat16)
+    _need(dW, "dW", (N, dm), torch.float32)
+    dims = make_dims(B, L, Hq, Hkv, d, D, 1, 0, LIZARD_BF16)
+    nb = 0 if workspace is None else workspace.numel()
+    st = load().lizard_qkvg_proj_bwd(ctypes.byref(dims), dm, _p(x), _p(W), _p(dq), _p(dk),
+                                     _p(dv), _p(dg), _p(dx), _p(dW), _p(workspace), nb,
+                                     _stream(stream))
+    _check(st, "lizard_qkvg_proj_bwd")
+    return dx, dW

@@ -200,6 +200,31 @@ lizard_status lizard_attn_bwd_varlen(const lizard_dims* dims, const int64_t* cu_
                                      void* dv, void* dg, float* dWf, float* dsinks,
                                      void* workspace, size_t ws_bytes, void* stream);
 
+/* The projections in front of the mixer (sec. 2-A-1: the gate is a learned projection of
+ * the layer input, Gamma_i = sigmoid(W_gamma x_i), next to the attention projections), as one
+ * tensor-core GEMM:  [q | k | v | g] = x W^T.
+ *   dims     the mixer's sizes (B, L, Hq, Hkv, d, D; the others are not used); dtype BF16;
+ *   dmodel   width of the layer input, a multiple of 64;
+ *   x        [B, L, dmodel] bf16;   W  [N, dmodel] bf16 with N = Hq d + 2 Hkv d + Hkv D, its rows
+ *            q (Hq d), k (Hkv d), v (Hkv d), gate logits (Hkv D), each head's rows contiguous;
+ *   q, k, v, g  outputs in the mixer's layouts ([B, L, Hq, d], [B, L, Hkv, d] x 2,
+ *            [B, L, Hkv, D]), overwritten;
+ *   workspace, ws_bytes  optional (NULL, 0): >= 256 bytes whose status word records a
+ *            device-side error (read it with lizard_read_device_status).
+ * Each of Hq d, Hkv d and Hkv D must be a multiple of 128, else LIZARD_ERR_UNSUPPORTED; fp32
+ * dims also give LIZARD_ERR_UNSUPPORTED.  fp32 accumulation, bf16 results. */
+lizard_status lizard_qkvg_proj(const lizard_dims* dims, int64_t dmodel, const void* x,
+                               const void* W, void* q, void* k, void* v, void* g,
+                               void* workspace, size_t ws_bytes, void* stream);
+
+/* Backward of lizard_qkvg_proj from the mixer's gradients dq, dk, dv, dg (dY = [dq|dk|dv|dg]):
+ *   dx [B, L, dmodel] bf16 = dY W,   dW [N, dmodel] fp32 = dY^T x   (both overwritten).
+ * Sizes, layouts, workspace and errors as for lizard_qkvg_proj. */
+lizard_status lizard_qkvg_proj_bwd(const lizard_dims* dims, int64_t dmodel, const void* x,
+                                   const void* W, const void* dq, const void* dk,
+                                   const void* dv, const void* dg, void* dx, float* dW,
+                                   void* workspace, size_t ws_bytes, void* stream);
+
 /* Bytes of device workspace lizard_decode_step needs (the status word only). */
 size_t lizard_decode_workspace(const lizard_dims* dims);
 

@@ -51,6 +51,14 @@ def main():
     out["dec_neg_pos"] = lib.lizard_decode_step(ctypes.byref(dims()), -1, *nul, 256, None)
     out["dec_misaligned"] = lib.lizard_decode_step(ctypes.byref(dims()), 0, mis, *nul[1:], 256,
                                                    None)
+    # the projections: bf16 only, dm a multiple of 64
+    six = [ok] * 6
+    out["proj_f32"] = lib.lizard_qkvg_proj(ctypes.byref(dims(dtype=lz.LIZARD_F32)), 256, *six,
+                                           None, 0, None)
+    out["proj_dm"] = lib.lizard_qkvg_proj(ctypes.byref(d), 200, *six, None, 0, None)
+    out["proj_null"] = lib.lizard_qkvg_proj(ctypes.byref(d), 256, None, *six[1:], None, 0, None)
+    out["proj_bwd_mis"] = lib.lizard_qkvg_proj_bwd(ctypes.byref(d), 256, *([ok] * 7), mis, None,
+                                                   0, None)
     # every check passes: the device query is what fails, with nothing launched
     out["fwd_no_device"] = lib.lizard_attn_fwd(ctypes.byref(d), *args, 1 << 30, None)
     print(json.dumps(out))

@@ -100,6 +100,10 @@ def test_null_and_misaligned_pointers_rejected(lib):
     assert st["dec_w300"] == lz.LIZARD_ERR_UNSUPPORTED
     assert st["dec_G16"] == lz.LIZARD_ERR_UNSUPPORTED
     assert st["fwd_no_device"] == lz.LIZARD_ERR_CUDA
+    assert st["proj_f32"] == lz.LIZARD_ERR_UNSUPPORTED
+    assert st["proj_dm"] == lz.LIZARD_ERR_UNSUPPORTED
+    assert st["proj_null"] == bad
+    assert st["proj_bwd_mis"] == bad
 
 
 def test_null_pointer_checks_in_process(lib):
