@@ -377,24 +377,27 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
 // heads per KV head, w <= 64).  The step reads and writes the fp32 state, 64 KB per (batch, KV
 // head) unit, and around it does about 190 K multiply-adds of small products per unit (u = x Wf,
 // window scores, window values, the readout phi(q).S).  One CTA per SM walks its units (unit =
-// CTA + i x grid) with two shared-memory buffers, so the copies of one unit overlap the compute
-// of the one before.  Thread 0 moves all data with the copy engine: the key and value rings
-// and the query rows by tensor-map loads in two 64-column halves with the 128-byte swizzle (a
-// row's 16-byte chunk c sits at chunk c ^ (row mod 8), so the eight rows an ldmatrix reads fall
-// in distinct bank groups), the new token's rows, gate logits and z by plain bulk copies, and
-// the state by tensor-map copies of four 32-column fp32 boxes with the same swizzle, in and,
-// once updated in place, out again (the stores drain while the next unit computes).  The copy
-// engine takes requests in order, so a unit's loads are issued before the store ahead of them.  The products run as warp-level tensor-core MMAs (mma.sync):
-// bf16 operands for u and the window scores; P V with the probabilities split into a bf16 head
-// and tail (so they keep about 16 bits); tf32 for the readout, whose B fragments are the very
-// state elements the lane has just updated, passed as fp32 bit patterns (the MMA reads their
-// upper 19 bits).  Rows of the 16-row A fragments beyond the query heads are zero.
-constexpr int ST = 512;      // threads: 16 warps
+// CTA + i x grid) as a two-stage pipeline of 8-warp groups: the front group computes u, the
+// window scores, the feature maps, the softmax and P V of unit i+1 while the back group updates
+// the state of unit i, writes it straight back to global memory from registers (each warp store
+// covers four whole 128-byte rows) and forms y.  They hand over through a double-buffered slot
+// of shared memory (feature maps, gates, v_{pos-w}, the window values, e^{-m} and the
+// normaliser), with mbarriers for each direction.  The copy engine brings everything in: the key
+// and value rings and the query rows by tensor-map loads in two 64-column halves with the
+// 128-byte swizzle (a row's 16-byte chunk c sits at chunk c ^ (row mod 8), so the eight rows an
+// ldmatrix reads fall in distinct bank groups), the new token's rows, gate logits and z by plain
+// bulk copies, and the state by four 32-column fp32 boxes with the same swizzle, two units
+// ahead.  The products run as warp-level tensor-core MMAs (mma.sync): bf16 operands for u and
+// the scores; P V with the probabilities rounded to bf16 (and the normaliser summing the same
+// rounded values); tf32 for the readout, whose B fragments are the very state elements the lane has just updated,
+// passed as fp32 bit patterns (the MMA reads their upper 19 bits).  Rows of the 16-row A
+// fragments beyond the query heads are zero.
+constexpr int ST = 512;      // threads: 16 warps, two groups of 8
 constexpr int SG = 4;        // query heads per KV head, at most
 constexpr int SW = 64;       // window, at most
 constexpr int RH = 9216;     // one 64-column half of a ring: (w+1) rows of 128 bytes, 1 KB-rounded
-struct alignas(1024) StreamBuf {
-    float S[4][128 * 32];             // state, columns 32 cg .. + 31 of all rows f (swizzled)
+// A unit's rows: the copy engine writes them, the front group alone reads them.
+struct alignas(1024) StreamRows {
     uint8_t kr[2][RH];                // key ring halves (swizzled)
     uint8_t vr[2][RH];                // value ring halves
     uint8_t q[2][1024];               // query rows of the group, halves
@@ -402,31 +405,40 @@ struct alignas(1024) StreamBuf {
     __nv_bfloat16 gl[128];            // its gate logits
     float z[128];
 };
+// What the front group hands the back group for one unit.
+struct StreamHand {
+    float phi[SG + 1][136];   // feature maps: query heads, then k_{pos-w} (rows padded by 8)
+    float gam[128];           // gates
+    float ve[128];            // v_{pos-w} (zero before token w)
+    float pv[SG][128];        // window values sum_j e^{s_j - m} v_j
+    float row[SG][2];         // e^{-m}, 1 / denominator
+};
 struct StreamSmem {
-    StreamBuf buf[2];
-    float u[SG + 1][64];           // x Wf: query rows, then k_{pos-w}
-    float phi[SG + 1][136];        // feature maps of the same rows (rows padded by 8 floats)
-    float gam[128];
-    float ps[SG][SW];              // window scores
-    __nv_bfloat16 ph[SG][72];      // window probabilities, bf16 head ...
-    __nv_bfloat16 pl[SG][72];      // ... and tail (p - head)
-    float xp[4][SG][128];          // readout partials of the four feature quarters
-    float pv[SG][128];             // window values
-    float row[SG][4];              // m, E_win + sinks, e^{-m}, 1 / denominator
+    float S[2][4][128 * 32];       // states: four 32-column boxes of 128 rows each (swizzled)
+    StreamRows rows[2];
+    StreamHand hand[2];
+    float u[SG + 1][64];           // front: x Wf of the query rows and k_{pos-w}
+    float ps[SG][SW];              // front: window scores
+    __nv_bfloat16 ph[SG][72];      // front: window probabilities (bf16)
+    float rowf[SG][2];             // front: m, E_win + sinks
+    float xp[SG][128];             // back: readout partials of features 64 .. 127
     __nv_bfloat16 zrow[128];       // zeros: the rows of fragments past the heads or the window
-    uint64_t bar_in[2], bar_s[2];
+    uint64_t full_in[2], full_s[2], front_done[2], back_done[2];
+    int abort;                     // set by a group that gave up waiting
 };
 constexpr size_t kStreamSmem = sizeof(StreamSmem) + 1024;
 static_assert(kStreamSmem <= 232448, "shared memory budget");
-static_assert(sizeof(StreamBuf) % 1024 == 0 && offsetof(StreamBuf, kr) % 1024 == 0 &&
-                  offsetof(StreamBuf, vr) % 1024 == 0 && offsetof(StreamBuf, q) % 1024 == 0 &&
-                  offsetof(StreamBuf, kn) % 16 == 0 && offsetof(StreamBuf, vn) % 16 == 0 &&
-                  offsetof(StreamBuf, gl) % 16 == 0 && offsetof(StreamBuf, z) % 16 == 0,
-              "buffer regions");
-static_assert(offsetof(StreamSmem, ph) % 16 == 0 && offsetof(StreamSmem, pl) % 16 == 0 &&
-                  offsetof(StreamSmem, xp) % 16 == 0 && offsetof(StreamSmem, pv) % 16 == 0 &&
+static_assert(sizeof(StreamRows) % 1024 == 0 && offsetof(StreamRows, kr) % 1024 == 0 &&
+                  offsetof(StreamRows, vr) % 1024 == 0 && offsetof(StreamRows, q) % 1024 == 0 &&
+                  offsetof(StreamRows, kn) % 16 == 0 && offsetof(StreamRows, vn) % 16 == 0 &&
+                  offsetof(StreamRows, gl) % 16 == 0 && offsetof(StreamRows, z) % 16 == 0,
+              "row regions");
+static_assert(offsetof(StreamSmem, rows) % 1024 == 0 && offsetof(StreamSmem, hand) % 16 == 0 &&
+                  sizeof(StreamHand) % 16 == 0 && offsetof(StreamSmem, ph) % 16 == 0 &&
+                  offsetof(StreamSmem, xp) % 16 == 0 &&
                   offsetof(StreamSmem, zrow) % 16 == 0 && offsetof(StreamSmem, u) % 16 == 0 &&
-                  offsetof(StreamSmem, ps) % 16 == 0 && (72 * 2) % 16 == 0,
+                  offsetof(StreamSmem, ps) % 16 == 0 && offsetof(StreamHand, pv) % 16 == 0 &&
+                  offsetof(StreamHand, ve) % 16 == 0 && offsetof(StreamHand, gam) % 16 == 0,
               "scratch rows");
 
 // Kernel parameters of the streaming step: tensor maps of the rings ([B Hkv (w+1)] rows of
@@ -452,10 +464,9 @@ __device__ __forceinline__ uint32_t chunk_addr(const SRow& r, int c) {
     return (c < 8 ? r.h0 : r.h1) + ((((uint32_t)c & 7u) ^ r.x) << 4);
 }
 
-// Thread 0 issues a unit's rings, query rows, token rows and z (no store reads them back, so
-// the buffer is free once the unit's compute is done) ...
+// The front leader issues a unit's rings, query rows, token rows and z ...
 __device__ __forceinline__ void stream_issue_in(const StreamMaps& mp, const Plan& p,
-                                                const DecodeArgs& a, StreamBuf& B, uint64_t* bar,
+                                                const DecodeArgs& a, StreamRows& B, uint64_t* bar,
                                                 int un) {
     const int Hkv = (int)p.Hkv, G = (int)p.G, R = (int)p.w + 1;
     const int b = un / Hkv, kv = un - b * Hkv;
@@ -470,11 +481,11 @@ __device__ __forceinline__ void stream_issue_in(const StreamMaps& mp, const Plan
     bulk_load(B.gl, (const __nv_bfloat16*)a.g + (int64_t)un * 128, 256u, bar);
     bulk_load(B.z, a.z + (int64_t)un * 128, 512u, bar);
 }
-// ... and its state (once the store of the unit that used the buffer before has read it out).
-__device__ __forceinline__ void stream_issue_s(const StreamMaps& mp, StreamBuf& B, uint64_t* bar,
-                                               int un) {
+// ... and the back leader its state, four 32-column boxes.
+__device__ __forceinline__ void stream_issue_s(const StreamMaps& mp, float (*S)[128 * 32],
+                                               uint64_t* bar, int un) {
     mbar_arrive_expect_tx(bar, 65536u);
-    for (int cg = 0; cg < 4; ++cg) tma_load_2d(B.S[cg], &mp.S, bar, 32 * cg, 128 * un);
+    for (int cg = 0; cg < 4; ++cg) tma_load_2d(S[cg], &mp.S, bar, 32 * cg, 128 * un);
 }
 
 // D += A B on a 16 x 8 tile: bf16 operands (K = 16) or tf32 operands (K = 8), fp32 accumulate.
@@ -510,6 +521,31 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t* r, uint32_t addr) {
                  : "r"(addr));
 }
 
+// Barrier of one 8-warp group (named barrier 1: front, 2: back); the _and form returns whether
+// every thread passed true.
+__device__ __forceinline__ void group_bar(int id) {
+    asm volatile("bar.sync %0, 256;" ::"r"(id) : "memory");
+}
+__device__ __forceinline__ bool group_bar_and(int id, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, 256, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id)
+        : "memory");
+    return r != 0;
+}
+// Bounded wait for a phase, also given up when the other group has aborted.
+__device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort != 0 || clock64() - t0 > kTimeout) return false;
+    }
+    return true;
+}
+
 __global__ void __launch_bounds__(ST, 1)
     decode_stream_kernel(Plan p, DecodeArgs a, const __grid_constant__ StreamMaps mp) {
     extern __shared__ uint8_t smem_raw[];
@@ -524,49 +560,58 @@ __global__ void __launch_bounds__(ST, 1)
     WsHeader* hdr = (WsHeader*)a.header;
     const int u0 = blockIdx.x, ustep = gridDim.x;
     if (u0 >= U) return;
-    float* const zg = a.z;
-    __nv_bfloat16* const yg = (__nv_bfloat16*)a.y;
-    __nv_bfloat16* const kcw = (__nv_bfloat16*)a.kc;
-    __nv_bfloat16* const vcw = (__nv_bfloat16*)a.vc;
-    const __nv_bfloat16* const wfg = (const __nv_bfloat16*)a.Wf;
-    const float* const sinks = a.sinks;
     const int64_t* const pos_dev = a.pos_dev;
     const int64_t pos_all = a.pos;
-    const int M = (int)p.M;
-    const float scale = p.scale;
+    volatile int* abort_flag = &sm.abort;
     if (tid == 0) {
         prefetch_tmap(&mp.kc);
         prefetch_tmap(&mp.vc);
         prefetch_tmap(&mp.q);
         prefetch_tmap(&mp.S);
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sm.bar_in[i], 1);
-            mbar_init(&sm.bar_s[i], 1);
+            mbar_init(&sm.full_in[i], 1);
+            mbar_init(&sm.full_s[i], 1);
+            mbar_init(&sm.front_done[i], 1);
+            mbar_init(&sm.back_done[i], 1);
         }
+        sm.abort = 0;
         fence_mbar_init();
-        stream_issue_in(mp, p, a, sm.buf[0], &sm.bar_in[0], u0);
-        stream_issue_s(mp, sm.buf[0], &sm.bar_s[0], u0);
-        if (u0 + ustep < U) stream_issue_in(mp, p, a, sm.buf[1], &sm.bar_in[1], u0 + ustep);
     }
     if (tid < 64) reinterpret_cast<uint32_t*>(sm.zrow)[tid] = 0u;
     __syncthreads();
-    uint32_t ph_in0 = 0u, ph_in1 = 0u, ph_s0 = 0u, ph_s1 = 0u;
-    bool out_in0 = true, out_in1 = u0 + ustep < U, out_s0 = true, out_s1 = false;  // in flight
-    bool ok = true, got = true, gs = true;
-    int bi = 0;
-    const SRow zr = srow_plain(sm.zrow);
-    // warps 0..7: B fragments of Wf (columns 8 warp .. + 7, all 128 inputs), kept in registers
-    // for the CTA's KV head (the same for all its units whenever the grid is a multiple of Hkv;
-    // reloaded when it changes); per head, max(t_m, kMinShift) and sum_m e^{t_m - that max}
-    uint32_t wb[8][2];
-    int kv_w = -1;
-    float tmx[SG], tse[SG];
-    for (int un = u0; un < U; un += ustep, bi ^= 1) {
-        StreamBuf& B = sm.buf[bi];
-        StreamBuf& Bn = sm.buf[bi ^ 1];
-        const int b = un / Hkv, kv = un - b * Hkv;
-        if (kv != kv_w) {
-            if (warp < 8) {
+
+    if (warp < 8) {
+        // ================= front: rows in; u, scores, feature maps, softmax, P V =================
+        uint32_t out_in = 0u;  // leader's row copies in flight, one bit per buffer
+        if (tid == 0) {
+            stream_issue_in(mp, p, a, sm.rows[0], &sm.full_in[0], u0);
+            out_in = 1u;
+            if (u0 + ustep < U) {
+                stream_issue_in(mp, p, a, sm.rows[1], &sm.full_in[1], u0 + ustep);
+                out_in |= 2u;
+            }
+        }
+        __nv_bfloat16* const kcw = (__nv_bfloat16*)a.kc;
+        __nv_bfloat16* const vcw = (__nv_bfloat16*)a.vc;
+        const __nv_bfloat16* const wfg = (const __nv_bfloat16*)a.Wf;
+        const int M = (int)p.M;
+        const float scale = p.scale;
+        // B fragments of Wf (columns 8 warp .. + 7, all 128 inputs), kept in registers for the
+        // CTA's KV head (the same for all its units whenever the grid is a multiple of Hkv;
+        // reloaded when it changes); per head, max(t_m, kMinShift) and sum_m e^{t_m - that max}
+        uint32_t wb[8][2];
+        int kv_w = -1;
+        // softmax rows: warps 5 and 6, one head per half-warp
+        float tm = kMinShift, ts = 0.0f;  // of that head
+        const int sh = warp == 5 || warp == 6 ? 2 * (warp - 5) + (lane >> 4) : -1;
+        int it = 0;
+        for (int un = u0; un < U; un += ustep, ++it) {
+            const int sl = it & 1;
+            const uint32_t par = (uint32_t)(it >> 1) & 1u;
+            StreamRows& B = sm.rows[sl];
+            StreamHand& H = sm.hand[sl];
+            const int b = un / Hkv, kv = un - b * Hkv;
+            if (kv != kv_w) {
                 const __nv_bfloat16* W = wfg + (int64_t)kv * 128 * 64 + 8 * warp + gq;
 #pragma unroll
                 for (int ks = 0; ks < 8; ++ks) {
@@ -574,306 +619,355 @@ __global__ void __launch_bounds__(ST, 1)
                     wb[ks][0] = pack2(W[k0 * 64], W[(k0 + 1) * 64]);
                     wb[ks][1] = pack2(W[(k0 + 8) * 64], W[(k0 + 9) * 64]);
                 }
-            }
-#pragma unroll
-            for (int x = 0; x < SG; ++x) {
-                float m = kMinShift, se = 0.0f;
-                if (x < G) {
-                    const float* t = sinks + (int64_t)(kv * G + x) * M;
-                    for (int mm = 0; mm < M; ++mm) m = fmaxf(m, t[mm]);
-                    for (int mm = 0; mm < M; ++mm) se += expf(t[mm] - m);
+                tm = kMinShift;
+                ts = 0.0f;
+                if (sh >= 0 && sh < G) {
+                    const float* t = a.sinks + (int64_t)(kv * G + sh) * M;
+                    for (int mm = 0; mm < M; ++mm) tm = fmaxf(tm, t[mm]);
+                    for (int mm = 0; mm < M; ++mm) ts += expf(t[mm] - tm);
                 }
-                tmx[x] = m;
-                tse[x] = se;
+                kv_w = kv;
             }
-            kv_w = kv;
-        }
-        const int64_t pos = pos_dev != nullptr ? pos_dev[b] : pos_all;
-        // (1) everything but the state (one thread waits; the others wait at the barrier)
-        if (tid == 0) got = mbar_wait(&sm.bar_in[bi], bi ? ph_in1 : ph_in0, kTimeout);
-        if (!__syncthreads_and(got)) {
-            if (tid == 0) report(hdr, LIZARD_ERR_TIMEOUT, 42);
-            ok = false;
-            break;
-        }
-        if (bi) ph_in1 ^= 1u;
-        else ph_in0 ^= 1u;
-        if (tid == 0) {
-            if (bi) out_in1 = false;
-            else out_in0 = false;
-        }
-        const bool run = pos >= 0;  // a negative per-sequence position leaves the unit untouched
-        if (!run && tid == 0) report(hdr, LIZARD_ERR_INVALID_ARG, 43);
-        const bool admit = pos >= w;
-        const int nkeys = run ? (pos + 1 < w ? (int)pos + 1 : w) : 1;
-        // ring slots: the new token goes to slot_n = pos mod (w+1); the key that leaves the
-        // window (token pos - w) sits in the slot after it; key jj of the window (token
-        // pos - nkeys + 1 + jj) in slot (slot0 + jj) mod (w+1), the last one being the new token
-        const int slot_n = run ? (pos <= 0x7fffffff ? (int)pos % R : (int)(pos % R)) : 0;
-        const int slot_e = slot_n + 1 == R ? 0 : slot_n + 1;
-        const int slot0 = slot_n - (nkeys - 1) < 0 ? slot_n - (nkeys - 1) + R : slot_n - (nkeys - 1);
-        // row of window key jj (the new token's own row for the last key; keys past the window
-        // read the zero row)
-        auto key_row = [&](const uint8_t (*ring)[RH], const __nv_bfloat16* cur, int jj) {
-            int sl = slot0 + jj;
-            if (sl >= R) sl -= R;
-            return jj < nkeys - 1 ? srow_swz(ring[0], ring[1], sl)
-                                  : jj == nkeys - 1 ? srow_plain(cur) : zr;
-        };
-        if (run) {
-            // A fragments of the query rows (rows 0..G-1), row SG the key that leaves (zero
-            // before token w), the others zero: two k-steps per ldmatrix
-            const SRow ar = lr < G ? srow_swz(B.q[0], B.q[1], lr)
-                          : (lr == SG && admit) ? srow_swz(B.kr[0], B.kr[1], slot_e) : zr;
-            if (warp < 8) {
-                // u = x Wf, columns 8 warp .. + 7
-                float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-                for (int kp = 0; kp < 4; ++kp) {
-                    uint32_t af[4];
-                    ldsm_x4(af, chunk_addr(ar, 4 * kp + lm));
-                    mma_bf16_16816(d0, af[0], 0u, af[1], 0u, wb[2 * kp][0], wb[2 * kp][1]);
-                    mma_bf16_16816(d1, af[2], 0u, af[3], 0u, wb[2 * kp + 1][0], wb[2 * kp + 1][1]);
+            const int64_t pos = pos_dev != nullptr ? pos_dev[b] : pos_all;
+            bool okw = true;
+            if (tid == 0) okw = stream_wait(&sm.full_in[sl], par, abort_flag);
+            if (!group_bar_and(1, okw)) {
+                if (tid == 0) {
+                    report(hdr, LIZARD_ERR_TIMEOUT, 42);
+                    sm.abort = 1;
                 }
-                if (gq <= SG)
-                    *reinterpret_cast<float2*>(&sm.u[gq][8 * warp + 2 * tq]) =
-                        make_float2(d0[0] + d1[0], d0[1] + d1[1]);
-                if (tid < 128) sm.gam[tid] = 1.0f / (1.0f + __expf(-__bfloat162float(B.gl[tid])));
-            } else {
-                // window scores of keys 8 (warp - 8) .. + 7 against the query rows
-                const SRow kr = key_row(B.kr, B.kn, 8 * (warp - 8) + lr);
-                float d0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, d1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                break;
+            }
+            if (tid == 0) out_in &= ~(1u << sl);
+            const bool run = pos >= 0;  // a negative per-sequence position: unit left untouched
+            if (!run && tid == 0) report(hdr, LIZARD_ERR_INVALID_ARG, 43);
+            const bool admit = pos >= w;
+            const int nkeys = run ? (pos + 1 < w ? (int)pos + 1 : w) : 1;
+            // ring slots: the new token goes to slot_n = pos mod (w+1); the key that leaves the
+            // window (token pos - w) sits in the slot after it; key jj of the window (token
+            // pos - nkeys + 1 + jj) in slot (slot0 + jj) mod (w+1), the last being the new token
+            const int slot_n = run ? (pos <= 0x7fffffff ? (int)pos % R : (int)(pos % R)) : 0;
+            const int slot_e = slot_n + 1 == R ? 0 : slot_n + 1;
+            const int slot0 =
+                slot_n - (nkeys - 1) < 0 ? slot_n - (nkeys - 1) + R : slot_n - (nkeys - 1);
+            const uint32_t zb = smem_u32(sm.zrow);
+            // row of window key jj (the new token's own row for the last key; keys past the
+            // window read the zero row, at chunks that keep the eight rows in distinct banks)
+            auto key_row = [&](const uint8_t (*ring)[RH], const __nv_bfloat16* cur, int jj) {
+                int sl2 = slot0 + jj;
+                if (sl2 >= R) sl2 -= R;
+                return jj < nkeys - 1 ? srow_swz(ring[0], ring[1], sl2)
+                       : jj == nkeys - 1 ? srow_plain(cur)
+                                         : SRow{zb, zb + 128u, (uint32_t)(jj & 7)};
+            };
+            if (run) {
+                // u = x Wf (columns 8 warp .. + 7) and the window scores of keys 8 warp .. + 7,
+                // both from the same A fragments: query rows 0..G-1, row SG the key that leaves
+                // (zero before token w), zero rows elsewhere
+                const SRow ar = lr < G ? srow_swz(B.q[0], B.q[1], lr)
+                                : (lr == SG && admit) ? srow_swz(B.kr[0], B.kr[1], slot_e)
+                                                      : SRow{zb, zb + 128u, (uint32_t)lr};
+                const SRow kr = key_row(B.kr, B.kn, 8 * warp + lr);
+                float du0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, du1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                float ds0[4] = {0.0f, 0.0f, 0.0f, 0.0f}, ds1[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
                 for (int kp = 0; kp < 4; ++kp) {
                     uint32_t af[4], bf[4];
                     ldsm_x4(af, chunk_addr(ar, 4 * kp + lm));
                     ldsm_x4(bf, chunk_addr(kr, 4 * kp + lm));
-                    mma_bf16_16816(d0, af[0], 0u, af[1], 0u, bf[0], bf[1]);
-                    mma_bf16_16816(d1, af[2], 0u, af[3], 0u, bf[2], bf[3]);
+                    mma_bf16_16816(du0, af[0], 0u, af[1], 0u, wb[2 * kp][0], wb[2 * kp][1]);
+                    mma_bf16_16816(ds0, af[0], 0u, af[1], 0u, bf[0], bf[1]);
+                    mma_bf16_16816(du1, af[2], 0u, af[3], 0u, wb[2 * kp + 1][0], wb[2 * kp + 1][1]);
+                    mma_bf16_16816(ds1, af[2], 0u, af[3], 0u, bf[2], bf[3]);
                 }
+                if (gq <= SG)
+                    *reinterpret_cast<float2*>(&sm.u[gq][8 * warp + 2 * tq]) =
+                        make_float2(du0[0] + du1[0], du0[1] + du1[1]);
                 if (gq < SG) {
-                    const int j0 = 8 * (warp - 8) + 2 * tq;
+                    const int j0 = 8 * warp + 2 * tq;
                     const bool hv = gq < G;
                     *reinterpret_cast<float2*>(&sm.ps[gq][j0]) =
-                        make_float2(hv && j0 < nkeys ? (d0[0] + d1[0]) * scale : -INFINITY,
-                                    hv && j0 + 1 < nkeys ? (d0[1] + d1[1]) * scale : -INFINITY);
+                        make_float2(hv && j0 < nkeys ? (ds0[0] + ds1[0]) * scale : -INFINITY,
+                                    hv && j0 + 1 < nkeys ? (ds0[1] + ds1[1]) * scale : -INFINITY);
                 }
             }
-            __syncthreads();
-            if (warp <= SG) {
-                // feature maps: one warp per row (query heads, then the key that leaves)
-                const int x = warp;
-                const float u0v = sm.u[x][lane], u1v = sm.u[x][lane + 32];
-                float mx = fmaxf(u0v, u1v), mn = fminf(u0v, u1v);
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            // the hand-off slot must be free (the back group done with unit it - 2)
+            bool okh = true;
+            if (tid == 0 && it >= 2) okh = stream_wait(&sm.back_done[sl], par ^ 1u, abort_flag);
+            if (!group_bar_and(1, okh)) {
+                if (tid == 0) {
+                    report(hdr, LIZARD_ERR_TIMEOUT, 45);
+                    sm.abort = 1;
                 }
-                const float p0 = __expf(u0v - mx), p1 = __expf(u1v - mx);
-                const float n0 = __expf(mn - u0v), n1 = __expf(mn - u1v);
-                float sp = p0 + p1, sn = n0 + n1;
+                break;
+            }
+            if (run) {
+                if (warp <= SG) {
+                    // feature maps: warps 0..3 the query heads, warp 4 the key that leaves
+                    const int x = warp;
+                    const float u0v = sm.u[x][lane], u1v = sm.u[x][lane + 32];
+                    float mx = fmaxf(u0v, u1v), mn = fminf(u0v, u1v);
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) {
-                    sp += __shfl_xor_sync(0xffffffffu, sp, o);
-                    sn += __shfl_xor_sync(0xffffffffu, sn, o);
+                    for (int o = 16; o > 0; o >>= 1) {
+                        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+                    }
+                    const float p0 = __expf(u0v - mx), p1 = __expf(u1v - mx);
+                    const float n0 = __expf(mn - u0v), n1 = __expf(mn - u1v);
+                    float sp = p0 + p1, sn = n0 + n1;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        sp += __shfl_xor_sync(0xffffffffu, sp, o);
+                        sn += __shfl_xor_sync(0xffffffffu, sn, o);
+                    }
+                    const bool zero = (x == SG && !admit) || (x < SG && x >= G);
+                    const float ip = zero ? 0.0f : 1.0f / sp, in = zero ? 0.0f : 1.0f / sn;
+                    H.phi[x][lane] = p0 * ip;
+                    H.phi[x][lane + 32] = p1 * ip;
+                    H.phi[x][64 + lane] = n0 * in;
+                    H.phi[x][96 + lane] = n1 * in;
                 }
-                const bool zero = (x == SG && !admit) || (x < SG && x >= G);
-                const float ip = zero ? 0.0f : 1.0f / sp, in = zero ? 0.0f : 1.0f / sn;
-                sm.phi[x][lane] = p0 * ip;
-                sm.phi[x][lane + 32] = p1 * ip;
-                sm.phi[x][64 + lane] = n0 * in;
-                sm.phi[x][96 + lane] = n1 * in;
-            } else if (warp >= 8 && warp < 8 + SG) {
-                // per head: shift, probabilities (split into bf16 head and tail for P V), their
-                // sum with the sinks'; heads beyond G get zero rows
-                const int hh = warp - 8;
-                const float tm = hh == 0 ? tmx[0] : hh == 1 ? tmx[1] : hh == 2 ? tmx[2] : tmx[3];
-                const float ts = hh == 0 ? tse[0] : hh == 1 ? tse[1] : hh == 2 ? tse[2] : tse[3];
-                const float s0 = sm.ps[hh][lane], s1 = sm.ps[hh][lane + 32];
-                float m = fmaxf(tm, fmaxf(s0, s1));
+                if (sh >= 0) {
+                    // softmax of head sh over a half-warp (keys l, l + 16, l + 32, l + 48):
+                    // shift, probabilities rounded to bf16 (the P V operand; the normaliser sums
+                    // the same rounded values, so y stays a weighted mean of the window's v),
+                    // their sum with the sinks'; heads beyond G get zero rows
+                    const int l = lane & 15;
+                    float sv[4], m = tm;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-                const float e0 = hh < G ? __expf(s0 - m) : 0.0f;
-                const float e1 = hh < G ? __expf(s1 - m) : 0.0f;
-                const __nv_bfloat16 h0 = __float2bfloat16_rn(e0), h1 = __float2bfloat16_rn(e1);
-                sm.ph[hh][lane] = h0;
-                sm.ph[hh][lane + 32] = h1;
-                sm.pl[hh][lane] = __float2bfloat16_rn(e0 - __bfloat162float(h0));
-                sm.pl[hh][lane + 32] = __float2bfloat16_rn(e1 - __bfloat162float(h1));
-                float es = e0 + e1;
+                    for (int k = 0; k < 4; ++k) {
+                        sv[k] = sm.ps[sh][l + 16 * k];
+                        m = fmaxf(m, sv[k]);
+                    }
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1) es += __shfl_xor_sync(0xffffffffu, es, o);
-                if (lane == 0) {
-                    sm.row[hh][0] = m;
-                    sm.row[hh][1] = es + ts * __expf(tm - m);  // window sum + sum_m e^{t_m - m}
+                    for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    float es = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const __nv_bfloat16 e = __float2bfloat16_rn(sh < G ? __expf(sv[k] - m) : 0.0f);
+                        sm.ph[sh][l + 16 * k] = e;
+                        es += __bfloat162float(e);
+                    }
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) es += __shfl_xor_sync(0xffffffffu, es, o);
+                    if (l == 0) {
+                        sm.rowf[sh][0] = m;
+                        sm.rowf[sh][1] = es + ts * __expf(tm - m);  // window + sum_m e^{t_m - m}
+                    }
+                } else if (warp == 7) {
+                    // the new token joins the ring (slot pos mod (w+1), read by no one here)
+                    __nv_bfloat16* dst = (lane < 16 ? kcw : vcw) + ((int64_t)un * R + slot_n) * 128;
+                    const __nv_bfloat16* src = lane < 16 ? B.kn : B.vn;
+                    *reinterpret_cast<uint4*>(dst + 8 * (lane & 15)) =
+                        *reinterpret_cast<const uint4*>(src + 8 * (lane & 15));
+                }
+                group_bar(1);
+                // window values N[h][c] = sum_j P[h][j] V[j][c], columns 16 warp .. + 15 (two
+                // n-tiles): V's B fragments by transposing ldmatrix (keys 32 kp + lane), P's A
+                // fragments (rows 0..SG-1 the heads, the others zero) by plain ldmatrix; the two
+                // k-steps of each ldmatrix accumulate apart
+                {
+                    float n0[2][4] = {}, n1[2][4] = {};
+                    const uint32_t prh = lr < SG ? smem_u32(sm.ph[lr]) : zb + 16u * lr;
+#pragma unroll
+                    for (int kp = 0; kp < 2; ++kp) {
+                        uint32_t bv0[4], bv1[4], ah[4];
+                        const SRow vrow = key_row(B.vr, B.vn, 32 * kp + lane);
+                        ldsm_x4_t(bv0, chunk_addr(vrow, 2 * warp));
+                        ldsm_x4_t(bv1, chunk_addr(vrow, 2 * warp + 1));
+                        ldsm_x4(ah, prh + 64 * kp + 16 * lm);
+                        mma_bf16_16816(n0[0], ah[0], 0u, ah[1], 0u, bv0[0], bv0[1]);
+                        mma_bf16_16816(n0[1], ah[0], 0u, ah[1], 0u, bv1[0], bv1[1]);
+                        mma_bf16_16816(n1[0], ah[2], 0u, ah[3], 0u, bv0[2], bv0[3]);
+                        mma_bf16_16816(n1[1], ah[2], 0u, ah[3], 0u, bv1[2], bv1[3]);
+                    }
+                    if (gq < SG) {
+#pragma unroll
+                        for (int t = 0; t < 2; ++t)
+                            *reinterpret_cast<float2*>(&H.pv[gq][16 * warp + 8 * t + 2 * tq]) =
+                                make_float2(n0[t][0] + n1[t][0], n0[t][1] + n1[t][1]);
+                    }
+                }
+                if (warp < G) {
+                    // phi(q).z with the new z = Gamma z + phi(k_{pos-w}), then e^{-m} and the
+                    // reciprocal of the denominator
+                    float dz = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        const int f = lane + 32 * k;
+                        const float gm = 1.0f / (1.0f + __expf(-__bfloat162float(B.gl[f])));
+                        dz = fmaf(H.phi[warp][f], fmaf(gm, B.z[f], H.phi[SG][f]), dz);
+                    }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) dz += __shfl_xor_sync(0xffffffffu, dz, o);
+                    if (lane == 0) {
+                        const float em = __expf(-sm.rowf[warp][0]);
+                        H.row[warp][0] = em;
+                        H.row[warp][1] = 1.0f / (em * dz + sm.rowf[warp][1]);
+                    }
+                } else if (warp == 4 || warp == 5) {
+                    // gates and the new z (features 64 (warp - 4) + lane, + 32)
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const int f = 64 * (warp - 4) + lane + 32 * k;
+                        const float gm = 1.0f / (1.0f + __expf(-__bfloat162float(B.gl[f])));
+                        H.gam[f] = gm;
+                        a.z[(int64_t)un * 128 + f] = fmaf(gm, B.z[f], H.phi[SG][f]);
+                    }
+                } else if (warp == 6) {
+                    // v_{pos-w} for the state update (columns 4 lane .. + 3)
+                    float4 vf = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    if (admit) {
+                        const SRow vrow = srow_swz(B.vr[0], B.vr[1], slot_e);
+                        const int c = 4 * lane;
+                        uint2 vv;
+                        asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
+                                     : "=r"(vv.x), "=r"(vv.y)
+                                     : "r"(chunk_addr(vrow, c >> 3) + 2 * (c & 7)));
+                        const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(&vv.x);
+                        const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(&vv.y);
+                        vf = make_float4(__low2float(v01), __high2float(v01), __low2float(v23),
+                                         __high2float(v23));
+                    }
+                    *reinterpret_cast<float4*>(&H.ve[4 * lane]) = vf;
                 }
             }
-            __syncthreads();
+            group_bar(1);  // the hand-off is written; this unit's rows are read
+            if (tid == 0) {
+                mbar_arrive(&sm.front_done[sl]);
+                if (un + 2 * ustep < U) {
+                    stream_issue_in(mp, p, a, B, &sm.full_in[sl], un + 2 * ustep);
+                    out_in |= 1u << sl;
+                }
+            }
         }
-        // the next unit's state goes to the other buffer once the store that buffer held (of
-        // the unit before this one) has been read out
-        if (tid == 0 && un + ustep < U) {
-            bulk_wait_read();
-            stream_issue_s(mp, Bn, &sm.bar_s[bi ^ 1], un + ustep);
-            if (bi) out_s0 = true;
-            else out_s1 = true;
-        }
-        if (run) {
-            // (2) window values N[h][c] = sum_j P[h][j] V[j][c], columns 8 warp .. + 7: V's B
-            //     fragments by transposing ldmatrix (keys 32 kp + lane), P's A fragments (rows
-            //     0..SG-1 the heads, the others the zero row) by plain ldmatrix
-            float nh[4] = {0.0f, 0.0f, 0.0f, 0.0f}, nl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            const uint32_t prh = lr < SG ? smem_u32(sm.ph[lr]) : smem_u32(sm.zrow);
-            const uint32_t prl = lr < SG ? smem_u32(sm.pl[lr]) : smem_u32(sm.zrow);
-#pragma unroll
-            for (int kp = 0; kp < 2; ++kp) {
-                uint32_t bv[4], ah[4], al[4];
-                ldsm_x4_t(bv, chunk_addr(key_row(B.vr, B.vn, 32 * kp + lane), warp));
-                ldsm_x4(ah, prh + 64 * kp + 16 * lm);
-                ldsm_x4(al, prl + 64 * kp + 16 * lm);
-                mma_bf16_16816(nh, ah[0], 0u, ah[1], 0u, bv[0], bv[1]);
-                mma_bf16_16816(nl, al[0], 0u, al[1], 0u, bv[0], bv[1]);
-                mma_bf16_16816(nh, ah[2], 0u, ah[3], 0u, bv[2], bv[3]);
-                mma_bf16_16816(nl, al[2], 0u, al[3], 0u, bv[2], bv[3]);
-            }
-            if (gq < SG)
-                *reinterpret_cast<float2*>(&sm.pv[gq][8 * warp + 2 * tq]) =
-                    make_float2(nh[0] + nl[0], nh[1] + nl[1]);
-            // the new token joins the ring (slot pos mod (w+1), read by no one in this step)
-            if (warp == 15) {
-                __nv_bfloat16* dst = (lane < 16 ? kcw : vcw) + ((int64_t)un * R + slot_n) * 128;
-                const __nv_bfloat16* src = lane < 16 ? B.kn : B.vn;
-                *reinterpret_cast<uint4*>(dst + 8 * (lane & 15)) =
-                    *reinterpret_cast<const uint4*>(src + 8 * (lane & 15));
-            }
-            // per head: phi(q).z with the new z = Gamma z + phi(k_{pos-w}), then e^{-m} and
-            // the reciprocal of the denominator
-            if (warp < G) {
-                float dz = 0.0f;
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int f = lane + 32 * k;
-                    dz = fmaf(sm.phi[warp][f], fmaf(sm.gam[f], B.z[f], sm.phi[SG][f]), dz);
+        if (tid == 0 && *abort_flag != 0) {  // let row copies still in flight land
+            for (int i = 0; i < 2; ++i)
+                if (out_in & (1u << i)) {  // (one of the two parities is the copy in flight)
+                    for (uint32_t ph = 0; ph < 2; ++ph) mbar_wait(&sm.full_in[i], ph, kTimeout / 8);
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) dz += __shfl_xor_sync(0xffffffffu, dz, o);
-                if (lane == 0) {
-                    const float em = __expf(-sm.row[warp][0]);
-                    sm.row[warp][2] = em;
-                    sm.row[warp][3] = 1.0f / (em * dz + sm.row[warp][1]);
+        }
+    } else {
+        // ================= back: state in; update, readout, y; state out =================
+        const int bt = tid - 256;  // thread within the group; 0 is the leader
+        const int wq = warp - 8, cg = wq & 3, kh = wq >> 2;
+        const int c0 = 32 * cg + 4 * gq;
+        uint32_t out_s = 0u;  // leader's state copies in flight, one bit per buffer
+        if (bt == 0) {
+            stream_issue_s(mp, sm.S[0], &sm.full_s[0], u0);
+            out_s = 1u;
+            if (u0 + ustep < U) {
+                stream_issue_s(mp, sm.S[1], &sm.full_s[1], u0 + ustep);
+                out_s |= 2u;
+            }
+        }
+        __nv_bfloat16* const yg = (__nv_bfloat16*)a.y;
+        int it = 0;
+        for (int un = u0; un < U; un += ustep, ++it) {
+            const int sl = it & 1;
+            const uint32_t par = (uint32_t)(it >> 1) & 1u;
+            const StreamHand& H = sm.hand[sl];
+            const int b = un / Hkv, kv = un - b * Hkv;
+            const int64_t pos = pos_dev != nullptr ? pos_dev[b] : pos_all;
+            const bool run = pos >= 0;
+            bool okw = true;
+            if (bt == 0)
+                okw = stream_wait(&sm.front_done[sl], par, abort_flag) &&
+                      stream_wait(&sm.full_s[sl], par, abort_flag);
+            if (!group_bar_and(2, okw)) {
+                if (bt == 0) {
+                    report(hdr, LIZARD_ERR_TIMEOUT, 44);
+                    sm.abort = 1;
                 }
+                break;
             }
-        }
-        // (3) the state, S <- Gamma S + phi(k_{pos-w}) v_{pos-w}^T in place, and the readout
-        //     partials phi(q) S over features 32 kg .. + 31 for columns 32 cg .. + 31.  The
-        //     lane holds columns 32 cg + 4 gq + j (the column gq of n-tile j, j = 0..3) of
-        //     feature rows f = 32 kg + 8 ks + 2 tq and f + 1: one 16-byte chunk of each, at
-        //     swizzled chunk gq ^ (f mod 8), so each 8-lane phase of a 128-bit access reads 8
-        //     distinct chunks.  Those are exactly its B fragments (k = tq, tq + 4; n = gq) of
-        //     the tf32 products, with feature f for k = tq and f + 1 for k = tq + 4.
-        if (tid == 0) gs = mbar_wait(&sm.bar_s[bi], bi ? ph_s1 : ph_s0, kTimeout);
-        if (!__syncthreads_and(gs)) {
-            if (tid == 0) report(hdr, LIZARD_ERR_TIMEOUT, 44);
-            ok = false;
-            break;
-        }
-        if (bi) ph_s1 ^= 1u;
-        else ph_s0 ^= 1u;
-        if (tid == 0) {
-            if (bi) out_s1 = false;
-            else out_s0 = false;
-        }
-        if (run) {
-            const int cg = warp & 3, kg = warp >> 2;
-            const int c0 = 32 * cg + 4 * gq;
-            float ve[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-            if (admit) {
-                const SRow vrow = srow_swz(B.vr[0], B.vr[1], slot_e);
-                uint2 vv;
-                asm volatile("ld.shared.v2.u32 {%0,%1}, [%2];"
-                             : "=r"(vv.x), "=r"(vv.y)
-                             : "r"(chunk_addr(vrow, c0 >> 3) + 2 * (c0 & 7)));
-                const __nv_bfloat162 v01 = *reinterpret_cast<const __nv_bfloat162*>(&vv.x);
-                const __nv_bfloat162 v23 = *reinterpret_cast<const __nv_bfloat162*>(&vv.y);
-                ve[0] = __low2float(v01);
-                ve[1] = __high2float(v01);
-                ve[2] = __low2float(v23);
-                ve[3] = __high2float(v23);
-            }
+            if (bt == 0) out_s &= ~(1u << sl);
+            // S <- Gamma S + phi(k_{pos-w}) v_{pos-w}^T, written straight to global memory, and
+            // the readout partials phi(q) S over features 64 kh .. + 63 for columns 32 cg .. + 31.
+            // The lane holds columns 32 cg + 4 gq + j (the column gq of n-tile j) of feature rows
+            // f = 64 kh + 8 ks + 2 tq and f + 1: one 16-byte chunk of each, at swizzled chunk
+            // gq ^ (f mod 8), so each 8-lane phase of a 128-bit access reads 8 distinct chunks.
+            // Those are exactly its B fragments (k = tq: feature f; k = tq + 4: f + 1) of the
+            // tf32 products, passed as fp32 bit patterns.
             float acc[4][4];
 #pragma unroll
             for (int j = 0; j < 4; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-            float* const Sq = B.S[cg];
-#pragma unroll
-            for (int ks = 0; ks < 4; ++ks) {
-                const int f0 = 32 * kg + 8 * ks + 2 * tq, f1 = f0 + 1;
-                float4* p0 = reinterpret_cast<float4*>(Sq + f0 * 32 + ((gq ^ (2 * tq)) << 2));
-                float4* p1 = reinterpret_cast<float4*>(Sq + f1 * 32 + ((gq ^ (2 * tq + 1)) << 2));
-                float4 s0 = *p0, s1 = *p1;
-                const float2 gg = *reinterpret_cast<const float2*>(&sm.gam[f0]);
-                const float2 kk = *reinterpret_cast<const float2*>(&sm.phi[SG][f0]);
-                const float g0 = gg.x, g1 = gg.y, k0 = kk.x, k1 = kk.y;
-                s0.x = fmaf(g0, s0.x, k0 * ve[0]);
-                s0.y = fmaf(g0, s0.y, k0 * ve[1]);
-                s0.z = fmaf(g0, s0.z, k0 * ve[2]);
-                s0.w = fmaf(g0, s0.w, k0 * ve[3]);
-                s1.x = fmaf(g1, s1.x, k1 * ve[0]);
-                s1.y = fmaf(g1, s1.y, k1 * ve[1]);
-                s1.z = fmaf(g1, s1.z, k1 * ve[2]);
-                s1.w = fmaf(g1, s1.w, k1 * ve[3]);
-                *p0 = s0;
-                *p1 = s1;
-                const float2 qq = gq < SG ? *reinterpret_cast<const float2*>(&sm.phi[gq][f0])
-                                          : make_float2(0.0f, 0.0f);
-                const uint32_t a0 = __float_as_uint(qq.x), a2 = __float_as_uint(qq.y);
-                mma_tf32_1688(acc[0], a0, 0u, a2, 0u, __float_as_uint(s0.x), __float_as_uint(s1.x));
-                mma_tf32_1688(acc[1], a0, 0u, a2, 0u, __float_as_uint(s0.y), __float_as_uint(s1.y));
-                mma_tf32_1688(acc[2], a0, 0u, a2, 0u, __float_as_uint(s0.z), __float_as_uint(s1.z));
-                mma_tf32_1688(acc[3], a0, 0u, a2, 0u, __float_as_uint(s0.w), __float_as_uint(s1.w));
-            }
-            // C rows gq (heads): n = 2 tq of tile j is column 32 cg + 8 tq + j, n = 2 tq + 1 is
-            // column 32 cg + 8 tq + 4 + j
-            if (gq < SG) {
-                float* xo = &sm.xp[kg][gq][32 * cg + 8 * tq];
-                *reinterpret_cast<float4*>(xo) = make_float4(acc[0][0], acc[1][0], acc[2][0], acc[3][0]);
-                *reinterpret_cast<float4*>(xo + 4) = make_float4(acc[0][1], acc[1][1], acc[2][1], acc[3][1]);
-            }
-            if (tid < 128) zg[(int64_t)un * 128 + tid] = fmaf(sm.gam[tid], B.z[tid], sm.phi[SG][tid]);
-        }
-        fence_async_smem();  // the state's generic writes, before the copy engine reads them
-        __syncthreads();
-        if (tid == 0) {
-            // this buffer's rows are free: the rows of the unit after next go in first, then
-            // the state goes back (one thread, one bulk group)
-            if (un + 2 * ustep < U) {
-                stream_issue_in(mp, p, a, B, &sm.bar_in[bi], un + 2 * ustep);
-                if (bi) out_in1 = true;
-                else out_in0 = true;
-            }
             if (run) {
-                for (int cg = 0; cg < 4; ++cg) tma_store_2d(&mp.S, B.S[cg], 32 * cg, 128 * un);
-                bulk_commit();
+                const float4 ve = *reinterpret_cast<const float4*>(&H.ve[c0]);
+                const float* const Sq = sm.S[sl][cg];
+                float* const Su = a.S + (int64_t)un * 128 * 128 + c0;
+#pragma unroll 4
+                for (int ks = 0; ks < 8; ++ks) {
+                    const int f0 = 64 * kh + 8 * ks + 2 * tq, f1 = f0 + 1;
+                    float4 s0 = *reinterpret_cast<const float4*>(Sq + f0 * 32 + ((gq ^ (2 * tq)) << 2));
+                    float4 s1 =
+                        *reinterpret_cast<const float4*>(Sq + f1 * 32 + ((gq ^ (2 * tq + 1)) << 2));
+                    const float2 gg = *reinterpret_cast<const float2*>(&H.gam[f0]);
+                    const float2 kk = *reinterpret_cast<const float2*>(&H.phi[SG][f0]);
+                    s0.x = fmaf(gg.x, s0.x, kk.x * ve.x);
+                    s0.y = fmaf(gg.x, s0.y, kk.x * ve.y);
+                    s0.z = fmaf(gg.x, s0.z, kk.x * ve.z);
+                    s0.w = fmaf(gg.x, s0.w, kk.x * ve.w);
+                    s1.x = fmaf(gg.y, s1.x, kk.y * ve.x);
+                    s1.y = fmaf(gg.y, s1.y, kk.y * ve.y);
+                    s1.z = fmaf(gg.y, s1.z, kk.y * ve.z);
+                    s1.w = fmaf(gg.y, s1.w, kk.y * ve.w);
+                    *reinterpret_cast<float4*>(Su + f0 * 128) = s0;
+                    *reinterpret_cast<float4*>(Su + f1 * 128) = s1;
+                    const float2 qq = gq < SG ? *reinterpret_cast<const float2*>(&H.phi[gq][f0])
+                                              : make_float2(0.0f, 0.0f);
+                    const uint32_t a0 = __float_as_uint(qq.x), a2 = __float_as_uint(qq.y);
+                    mma_tf32_1688(acc[0], a0, 0u, a2, 0u, __float_as_uint(s0.x), __float_as_uint(s1.x));
+                    mma_tf32_1688(acc[1], a0, 0u, a2, 0u, __float_as_uint(s0.y), __float_as_uint(s1.y));
+                    mma_tf32_1688(acc[2], a0, 0u, a2, 0u, __float_as_uint(s0.z), __float_as_uint(s1.z));
+                    mma_tf32_1688(acc[3], a0, 0u, a2, 0u, __float_as_uint(s0.w), __float_as_uint(s1.w));
+                }
+                // C rows gq (heads): n = 2 tq of tile j is column 32 cg + 8 tq + j, n = 2 tq + 1
+                // is column 32 cg + 8 tq + 4 + j; the upper feature half parks its partials
+                if (kh == 1 && gq < SG) {
+                    float* xo = &sm.xp[gq][32 * cg + 8 * tq];
+                    *reinterpret_cast<float4*>(xo) =
+                        make_float4(acc[0][0], acc[1][0], acc[2][0], acc[3][0]);
+                    *reinterpret_cast<float4*>(xo + 4) =
+                        make_float4(acc[0][1], acc[1][1], acc[2][1], acc[3][1]);
+                }
             }
-        }
-        if (!run) continue;  // the same for every thread; nothing else is written
-        {  // y: one (head, column) per thread
-            const int h = tid >> 7, c = tid & 127;
-            if (h < G) {
-                const float X = (sm.xp[0][h][c] + sm.xp[1][h][c]) + (sm.xp[2][h][c] + sm.xp[3][h][c]);
-                yg[((int64_t)b * Hq + kv * G + h) * 128 + c] =
-                    __float2bfloat16_rn(fmaf(sm.row[h][2], X, sm.pv[h][c]) * sm.row[h][3]);
+            group_bar(2);  // this state buffer is read; the partials are in
+            if (bt == 0 && un + 2 * ustep < U) {
+                stream_issue_s(mp, sm.S[sl], &sm.full_s[sl], un + 2 * ustep);
+                out_s |= 1u << sl;
             }
+            if (run && kh == 0 && gq < G) {
+                // y = (e^{-m} phi(q) S + N) / denominator for head gq, columns 32 cg + 8 tq + j
+                // and + 4 (j = 0..3), stored four bf16 at a time
+                const float em = H.row[gq][0], inv = H.row[gq][1];
+                const float* xo = &sm.xp[gq][32 * cg + 8 * tq];
+                const float* nv = &H.pv[gq][32 * cg + 8 * tq];
+                __nv_bfloat16* yo = yg + ((int64_t)b * Hq + kv * G + gq) * 128 + 32 * cg + 8 * tq;
+#pragma unroll
+                for (int hf = 0; hf < 2; ++hf) {
+                    const float4 xx = *reinterpret_cast<const float4*>(xo + 4 * hf);
+                    const float4 nn = *reinterpret_cast<const float4*>(nv + 4 * hf);
+                    const __nv_bfloat162 y01 =
+                        __floats2bfloat162_rn(fmaf(em, acc[0][hf] + xx.x, nn.x) * inv,
+                                              fmaf(em, acc[1][hf] + xx.y, nn.y) * inv);
+                    const __nv_bfloat162 y23 =
+                        __floats2bfloat162_rn(fmaf(em, acc[2][hf] + xx.z, nn.z) * inv,
+                                              fmaf(em, acc[3][hf] + xx.w, nn.w) * inv);
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<const uint32_t*>(&y01);
+                    pk.y = *reinterpret_cast<const uint32_t*>(&y23);
+                    *reinterpret_cast<uint2*>(yo + 4 * hf) = pk;
+                }
+            }
+            group_bar(2);  // the hand-off slot and the partials are read
+            if (bt == 0) mbar_arrive(&sm.back_done[sl]);
         }
-        __syncthreads();  // the scratch rows are reused by the next unit
-    }
-    if (tid == 0) {
-        bulk_wait_all();  // the last stores have completed
-        if (!ok) {        // let copies still in flight land before the CTA exits
-            if (out_in0) mbar_wait(&sm.bar_in[0], ph_in0, kTimeout);
-            if (out_in1) mbar_wait(&sm.bar_in[1], ph_in1, kTimeout);
-            if (out_s0) mbar_wait(&sm.bar_s[0], ph_s0, kTimeout);
-            if (out_s1) mbar_wait(&sm.bar_s[1], ph_s1, kTimeout);
+        if (bt == 0 && *abort_flag != 0) {  // let state copies still in flight land
+            for (int i = 0; i < 2; ++i)
+                if (out_s & (1u << i)) {  // (one of the two parities is the copy in flight)
+                    for (uint32_t ph = 0; ph < 2; ++ph) mbar_wait(&sm.full_s[i], ph, kTimeout / 8);
+                }
         }
     }
 }
