@@ -619,12 +619,28 @@ __global__ void __launch_bounds__(ST, 1)
                     wb[ks][0] = pack2(W[k0 * 64], W[(k0 + 1) * 64]);
                     wb[ks][1] = pack2(W[(k0 + 8) * 64], W[(k0 + 9) * 64]);
                 }
-                tm = kMinShift;
-                ts = 0.0f;
-                if (sh >= 0 && sh < G) {
+                if (sh >= 0) {
+                    // the head's sinks spread over its half-warp: one load per lane, then
+                    // max and sum across the 16 lanes
                     const float* t = a.sinks + (int64_t)(kv * G + sh) * M;
-                    for (int mm = 0; mm < M; ++mm) tm = fmaxf(tm, t[mm]);
-                    for (int mm = 0; mm < M; ++mm) ts += expf(t[mm] - tm);
+                    const int l = lane & 15;
+                    float tv[4];
+                    float mx = kMinShift;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {  // M <= 64 on this path
+                        const int mm = l + 16 * k;
+                        tv[k] = sh < G && mm < M ? t[mm] : -INFINITY;
+                        mx = fmaxf(mx, tv[k]);
+                    }
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                    float se = 0.0f;
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) se += expf(tv[k] - mx);
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) se += __shfl_xor_sync(0xffffffffu, se, o);
+                    tm = mx;
+                    ts = sh < G ? se : 0.0f;
                 }
                 kv_w = kv;
             }
@@ -978,7 +994,7 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
 // aligned and the tensor maps encode; otherwise the one-CTA-per-unit kernel runs.
 bool decode_stream_plan(const Plan& p, const DecodeArgs& a, StreamMaps* mp) {
     if (!(p.dtype == LIZARD_BF16 && p.d == 128 && p.D == 128 && p.G >= 1 && p.G <= SG &&
-          p.w >= 1 && p.w <= SW && p.B * p.Hkv * (p.w + 1) < (int64_t)1 << 31 &&
+          p.w >= 1 && p.w <= SW && p.M <= 64 && p.B * p.Hkv * (p.w + 1) < (int64_t)1 << 31 &&
           p.B * p.Hkv * 128 < (int64_t)1 << 31 && p.B * p.Hq < (int64_t)1 << 31))
         return false;
     if (!aligned16(a.kc) || !aligned16(a.vc) || !aligned16(a.q) || !aligned16(a.k) ||
