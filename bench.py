@@ -40,6 +40,7 @@ def parse():
     ap.add_argument("--no-train", action="store_true")
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--no-proj", action="store_true")
+    ap.add_argument("--no-varlen", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -444,6 +445,9 @@ def run_ours(args, rank, world, device):
     proj = None
     if not args.no_proj:
         proj = run_proj(args, device, lz, I)
+    varlen = None
+    if not args.no_varlen:
+        varlen = run_varlen(args, device, lz, I)
     clocks = sampler.stop()
 
     tokens = wl.B * wl.L
@@ -484,6 +488,8 @@ def run_ours(args, rank, world, device):
         out["long_context"] = long
     if proj is not None:
         out["projection"] = proj
+    if varlen is not None:
+        out["varlen"] = varlen
     return out
 
 
@@ -591,6 +597,61 @@ def run_proj(args, device, lz, I):
                          "fwd_frac": flops / (f_ms * 1e-3) / 1e12 / tc_peak,
                          "bwd_achieved": 2 * flops / (b_ms * 1e-3) / 1e12,
                          "bwd_frac": 2 * flops / (b_ms * 1e-3) / 1e12 / tc_peak},
+            "timing": "CUDA events, 512 MiB L2 flush before each call, mean of 5"}
+
+
+def run_varlen(args, device, lz, I):
+    """A packed batch of 64 LLaMA-shaped sequences of 128-4096 tokens (seeded lengths): the
+    forward as one launch over all sequences, and sequence after sequence (what a workspace
+    sized for one sequence gets), L2 flushed before each call."""
+    import numpy as np
+    import torch
+
+    lens = I.varlen_lengths()
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T = int(cu[-1])
+    wl = I.LLAMA3_8B_L8K
+    t = I.make_device_inputs(wl, device, L=T, B=1)
+    pk = {n: t[n][0] for n in ("q", "k", "v", "g")}
+    y = torch.empty_like(pk["q"])
+    dims = lz.make_dims(len(lens), T, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, torch.bfloat16)
+    one = lz.make_dims(1, T, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, torch.bfloat16)
+    ws_one_launch = lz.new_workspace(lz.lizard_attn_fwd_varlen_workspace(dims, cu), device)
+    ws_loop = lz.new_workspace(lz.lizard_attn_fwd_workspace(one), device)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+
+    def timed(ws, n=5):
+        def fwd():
+            lz.lizard_attn_fwd_varlen(pk["q"], pk["k"], pk["v"], pk["g"], t["Wf"], t["sinks"],
+                                      wl.w, cu, y=y, workspace=ws)
+        for _ in range(2):
+            fwd()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            fwd()
+            e1.record()
+        torch.cuda.synchronize()
+        st = lz.lizard_read_device_status(ws)
+        if st != lz.LIZARD_OK:
+            raise RuntimeError(f"varlen forward device status {lz.status_string(st)}")
+        return sum(a.elapsed_time(b) for a, b in evs) / n
+
+    ms_one, ms_loop = timed(ws_one_launch), timed(ws_loop)
+    hbm_peak, _, peak_src = load_peaks()
+    ab = fwd_algorithmic_bytes(wl.replace(L=T))
+    return {"workload": f"packed_{len(lens)}seq_len128-4096_T{T}_Hq32_Hkv8_d128_w64",
+            "sequences": len(lens), "tokens": T, "min_len": min(lens), "max_len": max(lens),
+            "ms_one_launch": ms_one, "tokens_per_s": T / (ms_one * 1e-3),
+            "ms_sequence_loop": ms_loop, "tokens_per_s_sequence_loop": T / (ms_loop * 1e-3),
+            "workspace_bytes_one_launch": int(ws_one_launch.numel()),
+            "roofline": {"bound": "hbm", "achieved": ab / (ms_one * 1e-3) / 1e9,
+                         "peak": hbm_peak, "frac": ab / (ms_one * 1e-3) / 1e9 / hbm_peak,
+                         "algorithmic_bytes": ab, "peak_source": peak_src,
+                         "scope": "whole forward"},
             "timing": "CUDA events, 512 MiB L2 flush before each call, mean of 5"}
 
 

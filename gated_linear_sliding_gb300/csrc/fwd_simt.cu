@@ -284,22 +284,49 @@ __global__ void __launch_bounds__(NT, 1) fwd_simt_tail(Plan p, FwdArgs a) {
         a.seg + ((size_t)(seg * p.rec_step) * (size_t)(p.B * p.Hkv) + (size_t)unit) * p.rec_floats;
     const int stop = __float_as_int(ho[DF * DH + DF]);
     if (stop < 0) return;
+    const int64_t len = seq_len(p, b);
     const int64_t s0 = (int64_t)stop * TS;
-    const int64_t s1 = min64(p.L, seg * p.seg_len + p.seg_len);
+    const int64_t s1 = min64(len, seg * p.seg_len + p.seg_len);
+    if (p.cu == nullptr) {
+        for (int64_t hh = 0; hh < p.G; ++hh) {
+            walk_head<T, DH, DF, FAST>(p, a, b, kv * p.G + hh, s0, s1, ho, sm);
+            __syncthreads();
+        }
+        return;
+    }
+    // a packed sequence is walked as batch 0 of a plan of its own length, on arrays that start
+    // at its first row (and at its state and z slots)
+    Plan ps = p;
+    ps.cu = nullptr;
+    ps.B = 1;
+    ps.L = len;
+    const int64_t r0 = seq_row0(p, b);
+    FwdArgs as = a;
+    as.q = (const T*)a.q + r0 * p.Hq * DH;
+    as.k = (const T*)a.k + r0 * p.Hkv * DH;
+    as.v = (const T*)a.v + r0 * p.Hkv * DH;
+    as.g = (const T*)a.g + r0 * p.Hkv * DF;
+    as.y = (T*)a.y + r0 * p.Hq * DH;
+    as.lse = a.lse != nullptr ? a.lse + r0 * p.Hq : nullptr;
+    as.S_out = a.S_out != nullptr ? a.S_out + b * p.Hkv * DF * DH : nullptr;
+    as.z_out = a.z_out != nullptr ? a.z_out + b * p.Hkv * DF : nullptr;
     for (int64_t hh = 0; hh < p.G; ++hh) {
-        walk_head<T, DH, DF, FAST>(p, a, b, kv * p.G + hh, s0, s1, ho, sm);
+        walk_head<T, DH, DF, FAST>(ps, as, 0, kv * p.G + hh, s0, s1, ho, sm);
         __syncthreads();
     }
 }
 
 template <typename T>
 __global__ void ring_fill_kernel(Plan p, const T* k, const T* v, T* kc, T* vc) {
-    const int64_t nt = min64(p.L, p.w);
-    const int64_t t = p.L - nt + blockIdx.x;
     const int64_t unit = blockIdx.y, b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t len = seq_len(p, b);
+    const int64_t nt = min64(len, p.w);
+    if ((int64_t)blockIdx.x >= nt) return;  // (a shorter packed sequence)
+    const int64_t t = len - nt + blockIdx.x;
     const int64_t slot = t % (p.w + 1);
+    const int64_t r0 = seq_row0(p, b);
     for (int64_t c = threadIdx.x; c < p.d; c += blockDim.x) {
-        const int64_t src = ((b * p.L + t) * p.Hkv + kv) * p.d + c;
+        const int64_t src = ((r0 + t) * p.Hkv + kv) * p.d + c;
         const int64_t dst = (unit * (p.w + 1) + slot) * p.d + c;
         if (kc != nullptr) kc[dst] = k[src];
         if (vc != nullptr) vc[dst] = v[src];

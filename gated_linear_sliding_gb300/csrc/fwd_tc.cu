@@ -176,11 +176,14 @@ constexpr uint32_t kStepBytes = 16384u + 8192u + 32768u;
 
 // Key/value slot of chunk c (and its query tile), on a barrier phase that expects `expect`
 // bytes in all (the gate tile follows separately).
+// Token coordinates are tok0 + 32 c: tok0 is the first row of a packed sequence (its maps span
+// every row, batch coordinate bco = 0) or 0 in a dense batch (bco = b).
 __device__ __forceinline__ void issue_kvq_loads(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmQ,
                                                 const CUtensorMap* tmK, const CUtensorMap* tmV,
-                                                int64_t c, int64_t kv, int64_t b, uint32_t expect) {
+                                                int64_t c, int64_t kv, int64_t tok0, int64_t b,
+                                                uint32_t expect) {
     const int slot = (int)(c & 3);
-    const int t0 = (int)(c * 32);
+    const int t0 = (int)(tok0 + c * 32);
     sm100::mbar_arrive_expect_tx(bar, expect);
 #pragma unroll
     for (int kb = 0; kb < 2; ++kb) {
@@ -191,8 +194,8 @@ __device__ __forceinline__ void issue_kvq_loads(uint8_t* sm, uint64_t* bar, cons
 }
 
 __device__ __forceinline__ void issue_gate_load(uint8_t* sm, uint64_t* bar, const CUtensorMap* tmG,
-                                                int64_t c, int64_t kv, int64_t b) {
-    sm100::tma_load_4d(sm + oG, tmG, bar, 0, (int)kv, (int)(c * 32), (int)b);
+                                                int64_t c, int64_t kv, int64_t tok0, int64_t b) {
+    sm100::tma_load_4d(sm + oG, tmG, bar, 0, (int)kv, (int)(tok0 + c * 32), (int)b);
 }
 
 // The control warp: lane 0 issues the copies and the three MMA groups of every step and
@@ -203,7 +206,8 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
                                              WsHeader* hdr, const CUtensorMap* tmQ,
                                              const CUtensorMap* tmK, const CUtensorMap* tmV,
                                              const CUtensorMap* tmW, const CUtensorMap* tmG,
-                                             int64_t c_begin, int64_t c_end, int64_t kv, int64_t b) {
+                                             int64_t c_begin, int64_t c_end, int64_t kv,
+                                             int64_t tok0, int64_t b) {
     const uint64_t dQ = kdesc(base + oQ), dQt = kdesc(base + oQt), dK = kdesc(base + oK),
                    dKi = kdesc(base + oKi), dE = kdesc(base + oE);
     const uint64_t dW = mndesc(base + oW, 16384), dHs = mndesc(base + oHs, 16384),
@@ -212,20 +216,22 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
     bool tma_out = false, mma_out = false;
     int64_t gate_due = -1;  // chunk whose gate tile its barrier phase still waits for
     if (c_begin < c_end) {
-        // the first step's operands, Wf and the two chunks before the segment (zero-filled
-        // before the sequence start), all on one phase
-        issue_kvq_loads(sm, &S.bar_tma, tmQ, tmK, tmV, c_begin, kv, b,
-                        kStepBytes + 16384u + 2u * 16384u);
-        issue_gate_load(sm, &S.bar_tma, tmG, c_begin, kv, b);
+        // the first step's operands, Wf and the two chunks before the segment, all on one
+        // phase; chunks before the sequence start are not loaded (their ring slots keep the
+        // zeros written at entry)
+        const int64_t c_prev = c_begin - 2 > 0 ? c_begin - 2 : 0;
+        issue_kvq_loads(sm, &S.bar_tma, tmQ, tmK, tmV, c_begin, kv, tok0, b,
+                        kStepBytes + 16384u + (uint32_t)(c_begin - c_prev) * 16384u);
+        issue_gate_load(sm, &S.bar_tma, tmG, c_begin, kv, tok0, b);
         tma_load_3d(sm + oW, tmW, &S.bar_tma, 0, 0, (int)kv);
-        for (int64_t cc = c_begin - 2; cc < c_begin; ++cc) {
+        for (int64_t cc = c_prev; cc < c_begin; ++cc) {
             const int slot = (int)(cc & 3);
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
                 tma_load_4d(sm + oK + kb * 16384 + slot * 4096, tmK, &S.bar_tma, 64 * kb, (int)kv,
-                            (int)(cc * CT), (int)b);
+                            (int)(tok0 + cc * CT), (int)b);
                 tma_load_4d(sm + oV + kb * 16384 + slot * 4096, tmV, &S.bar_tma, 64 * kb, (int)kv,
-                            (int)(cc * CT), (int)b);
+                            (int)(tok0 + cc * CT), (int)b);
             }
         }
         tma_out = true;
@@ -251,14 +257,14 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
         if (!ctl_wait(&S.bar_u, ph_u, S, hdr, 9)) break;
         // the query tile and the ring slot of chunk c-3 are free: next step's copies start
         if (more) {
-            issue_kvq_loads(sm, &S.bar_tma, tmQ, tmK, tmV, c + 1, kv, b, kStepBytes);
+            issue_kvq_loads(sm, &S.bar_tma, tmQ, tmK, tmV, c + 1, kv, tok0, b, kStepBytes);
             tma_out = true;
             gate_due = c + 1;
         }
         if (!ctl_wait(&S.bar_q, ph_q, S, hdr, 6)) break;
         tc_fence_after();
         if (more) {
-            issue_gate_load(sm, &S.bar_tma, tmG, c + 1, kv, b);
+            issue_gate_load(sm, &S.bar_tma, tmG, c + 1, kv, tok0, b);
             gate_due = -1;
         }
         const uint64_t dVd = dV + ((slot_d * 4096) >> 4);
@@ -306,7 +312,7 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
             mbar_wait(&S.bar_fin, 0, kTimeout);
         }
         if (tma_out) {
-            if (gate_due >= 0) issue_gate_load(sm, &S.bar_tma, tmG, gate_due, kv, b);
+            if (gate_due >= 0) issue_gate_load(sm, &S.bar_tma, tmG, gate_due, kv, tok0, b);
             mbar_wait(&S.bar_tma, ph_tma, kTimeout);
         }
     }
@@ -334,11 +340,24 @@ __global__ void __launch_bounds__(NT, 1)
     const int64_t unit = blockIdx.x, seg = blockIdx.y;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
     const int64_t U = p.B * p.Hkv;
+    // sequence b: rows row0 .. row0 + len - 1; TMA coordinates (tok0 + t, bco)
+    const int64_t row0 = seq_row0(p, b), len = seq_len(p, b);
+    const int64_t tok0 = p.cu != nullptr ? row0 : 0, bco = p.cu != nullptr ? 0 : b;
     const int64_t s0 = seg * p.seg_len;
-    const int64_t s1 = min64(p.L, s0 + p.seg_len);
+    const int64_t s1 = min64(len, s0 + p.seg_len);
     WsHeader* hdr = (WsHeader*)a.header;
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
     const int64_t c_begin = s0 / CT, c_end = (s1 + CT - 1) / CT;
+    if (s0 >= len) {
+        // a segment past the end of a shorter packed sequence: nothing to walk; its record
+        // slot tells the tail walk so (after the scan, which writes the same slots)
+        grid_dep_launch();
+        grid_dep_wait();
+        if (tid == 0)
+            a.seg[((size_t)(seg * p.rec_step) * (size_t)U + (size_t)unit) * p.rec_floats + DF * DH +
+                  DF] = __int_as_float(-1);
+        return;
+    }
 
     if (warp == 0) {
         tmem_alloc(&S.tmem, 512);
@@ -401,7 +420,7 @@ __global__ void __launch_bounds__(NT, 1)
     if (warp == NW) {
         if (lane == 0)
             control_loop(sm, base, tb, S, hdr, &tmQ, &tmK, &tmV, &tmW, &tmG, c_begin, c_end,
-                               kv, b);
+                               kv, tok0, bco);
         __syncwarp();
     } else {
         uint32_t ph_tma = 0, ph_u = 0, ph_a = 0, ph_o = 0;
@@ -757,7 +776,7 @@ __global__ void __launch_bounds__(NT, 1)
                     const float den = den0 + ((spi[row] + spi[128 + row]) + (spi[256 + row] + spi[384 + row]));
                     inv = 1.0f / den;
                     if (part == 0 && a.lse != nullptr)
-                        a.lse[(b * p.L + qa) * p.Hq + kv * GQ + hh] = m2 * kLn2 + __logf(den);
+                        a.lse[(row0 + qa) * p.Hq + kv * GQ + hh] = m2 * kLn2 + __logf(den);
                 }
             }
             ok = math_wait(&S.bar_o, ph_o, S, hdr, 5);
@@ -765,25 +784,36 @@ __global__ void __launch_bounds__(NT, 1)
             tc_fence_after();
 
             // (7) epilogue: y = O / den over columns [32 part, 32 part + 32) into the y tile
-            //     (q~'s buffer, free once the output MMAs are done), then one TMA store
+            //     (q~'s buffer, free once the output MMAs are done), then one TMA store.  The
+            //     last, partial step of a packed sequence stores its valid rows directly: the
+            //     tile's other rows are the next sequence's.
             {
                 float ov[32];
                 const int col = 32 * part;
                 tmem_ld32(tb + lane_off + cO + col, ov);
                 tmem_wait_ld();
+                const bool direct = p.cu != nullptr && n < CT;
+                uint4* yrow = reinterpret_cast<uint4*>(
+                    (__nv_bfloat16*)a.y + ((row0 + qa) * p.Hq + kv * GQ + hh) * DH + col);
 #pragma unroll
-                for (int ch = 0; ch < 4; ++ch)
-                    st_shared_v4(base + oQt + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
-                                 pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv),
-                                 pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv),
-                                 pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv),
-                                 pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv));
+                for (int ch = 0; ch < 4; ++ch) {
+                    const uint32_t w0 = pack_bf16(ov[8 * ch] * inv, ov[8 * ch + 1] * inv),
+                                   w1 = pack_bf16(ov[8 * ch + 2] * inv, ov[8 * ch + 3] * inv),
+                                   w2 = pack_bf16(ov[8 * ch + 4] * inv, ov[8 * ch + 5] * inv),
+                                   w3 = pack_bf16(ov[8 * ch + 6] * inv, ov[8 * ch + 7] * inv);
+                    if (!direct)
+                        st_shared_v4(base + oQt + (part >> 1) * 16384 + sw128(row, 4 * (part & 1) + ch),
+                                     w0, w1, w2, w3);
+                    else if (qv)
+                        yrow[ch] = make_uint4(w0, w1, w2, w3);
+                }
                 fence_async_smem();
                 math_sync();
-                if (tid == 0) {
-                    // rows past the end of the sequence fall outside the tensor and are dropped
-                    tma_store_4d(&tmY, sm + oQt, 0, (int)(kv * GQ), (int)t0, (int)b);
-                    tma_store_4d(&tmY, sm + oQt + 16384, 64, (int)(kv * GQ), (int)t0, (int)b);
+                if (tid == 0 && !direct) {
+                    // rows past the end of a dense batch's sequence fall outside the tensor
+                    tma_store_4d(&tmY, sm + oQt, 0, (int)(kv * GQ), (int)(tok0 + t0), (int)bco);
+                    tma_store_4d(&tmY, sm + oQt + 16384, 64, (int)(kv * GQ), (int)(tok0 + t0),
+                                 (int)bco);
                     bulk_commit();
                 }
             }
@@ -807,7 +837,7 @@ __global__ void __launch_bounds__(NT, 1)
         }
         if (tid == 0) ho[DF * DH + DF] = __int_as_float(ok && stop >= 0 ? (int)stop : -1);
 
-        if (ok && stop < 0 && a.S_out != nullptr && s1 == p.L) {
+        if (ok && stop < 0 && a.S_out != nullptr && s1 == len) {
             // final state of the last segment: the decode hand-off
             float* dstH = a.S_out + unit * DF * DH;
             float* dstz = a.z_out + unit * DF;
@@ -883,6 +913,7 @@ __device__ __forceinline__ bool local_wait(uint64_t* bar, uint32_t& ph, LSmall& 
     return !__syncthreads_or(fail);
 }
 
+// Token t of a 128-row tile: absolute row coordinate t (tok0 added by the caller), batch b.
 __device__ __forceinline__ void local_load(uint8_t* dst, const CUtensorMap* tm, uint64_t* bar,
                                            int64_t kv, int64_t t, int64_t b) {
     mbar_arrive_expect_tx(bar, 32768u);
@@ -911,9 +942,15 @@ __global__ void __launch_bounds__(NL, 1)
     const int64_t unit = blockIdx.x, seg = blockIdx.y;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
     const int64_t U = p.B * p.Hkv;
+    const int64_t row0 = seq_row0(p, b), len = seq_len(p, b);
+    const int64_t tok0 = p.cu != nullptr ? row0 : 0, bco = p.cu != nullptr ? 0 : b;
     const int64_t s0 = seg * p.seg_len;
-    const int64_t s1 = min64(p.L, s0 + p.seg_len);
-    const int64_t nsteps = (s1 - s0 + LT - 1) / LT;
+    const int64_t s1 = min64(len, s0 + p.seg_len);
+    // (a segment past the end of a shorter packed sequence walks nothing: zero record)
+    const int64_t nsteps = s1 > s0 ? (s1 - s0 + LT - 1) / LT : 0;
+    // the first tile's delayed keys and values before a packed sequence's start are the
+    // previous sequence's rows: zeroed in shared memory (a dense batch reads zero fill there)
+    const bool zero_pre = p.cu != nullptr && s0 < WIN;
     WsHeader* hdr = (WsHeader*)a.header;
     const uint32_t lane_off = (uint32_t)(32 * quad) << 16;
 
@@ -956,10 +993,11 @@ __global__ void __launch_bounds__(NL, 1)
         tma_load_3d(sm + lW, &tmW, &S.bar_k, 0, 0, (int)kv);
 #pragma unroll
         for (int kb = 0; kb < 2; ++kb)
-            tma_load_4d(sm + lK + kb * 16384, &tmK, &S.bar_k, 64 * kb, (int)kv, (int)(s0 - WIN), (int)b);
+            tma_load_4d(sm + lK + kb * 16384, &tmK, &S.bar_k, 64 * kb, (int)kv,
+                        (int)(tok0 + s0 - WIN), (int)bco);
         mbar_arrive_expect_tx(&S.bar_g, 32768u);
-        tma_load_4d(sm + lG, &tmG, &S.bar_g, 0, (int)kv, (int)s0, (int)b);
-        local_load(sm + lV, &tmV, &S.bar_v, kv, s0 - WIN, b);
+        tma_load_4d(sm + lG, &tmG, &S.bar_g, 0, (int)kv, (int)(tok0 + s0), (int)bco);
+        local_load(sm + lV, &tmV, &S.bar_v, kv, tok0 + s0 - WIN, bco);
         k_out = v_out = g_out = true;
     }
     tc_fence_before();
@@ -975,6 +1013,17 @@ __global__ void __launch_bounds__(NL, 1)
         // (1) U_k = k Wf for the 128 delayed keys of the step
         ok = local_wait(&S.bar_k, ph_k, S, hdr, 20);
         if (!ok) break;
+        if (zero_pre && c == 0) {
+            // rows t < WIN - s0 of both 64-column halves (the swizzle permutes chunks within
+            // a row, so whole rows are zeroed)
+            const int nz = (int)(WIN - s0) * 2 * 8;
+            for (int e = tid; e < nz; e += NL) {
+                const int r = e >> 4, kb = (e >> 3) & 1, ch = e & 7;
+                st_shared_v4(base + lK + kb * 16384 + r * 128 + ch * 16, 0u, 0u, 0u, 0u);
+            }
+            fence_async_smem();
+            __syncthreads();
+        }
         if (tid == 0) {
             k_out = false;
             tc_fence_after();
@@ -1035,7 +1084,7 @@ __global__ void __launch_bounds__(NL, 1)
         // the gate tile is consumed: the next step's gates start loading
         if (tid == 0 && more) {
             mbar_arrive_expect_tx(&S.bar_g, 32768u);
-            tma_load_4d(sm + lG, &tmG, &S.bar_g, 0, (int)kv, (int)(t0 + LT), (int)b);
+            tma_load_4d(sm + lG, &tmG, &S.bar_g, 0, (int)kv, (int)(tok0 + t0 + LT), (int)bco);
             g_out = true;
         }
         // (3) decay the state by e^{b_last} (lane = feature, 32 columns per part)
@@ -1058,7 +1107,7 @@ __global__ void __launch_bounds__(NL, 1)
             mma_out = false;
             // the key tile is consumed: the next step's keys start loading
             if (more) {
-                local_load(sm + lK, &tmK, &S.bar_k, kv, t0 + LT - WIN, b);
+                local_load(sm + lK, &tmK, &S.bar_k, kv, tok0 + t0 + LT - WIN, bco);
                 k_out = true;
             }
         }
@@ -1115,6 +1164,16 @@ __global__ void __launch_bounds__(NL, 1)
                 st_shared_v4(base + lKul + o, lo[4 * ch], lo[4 * ch + 1], lo[4 * ch + 2], lo[4 * ch + 3]);
             }
         }
+        if (zero_pre && c == 0) {
+            // the value rows before the sequence start, as for the keys (every thread waits
+            // for the tile here; the issuing thread's wait below then returns at once)
+            mbar_wait(&S.bar_v, 0u, kTimeout);
+            const int nz = (int)(WIN - s0) * 2 * 8;
+            for (int e = tid; e < nz; e += NL) {
+                const int r = e >> 4, kb = (e >> 3) & 1, ch = e & 7;
+                st_shared_v4(base + lV + kb * 16384 + r * 128 + ch * 16, 0u, 0u, 0u, 0u);
+            }
+        }
         fence_async_smem();
         tc_fence_before();
         __syncthreads();
@@ -1161,7 +1220,7 @@ __global__ void __launch_bounds__(NL, 1)
             mma_out = false;
             // values and k~ are consumed: the next step's values start loading
             if (more) {
-                local_load(sm + lV, &tmV, &S.bar_v, kv, t0 + LT - WIN, b);
+                local_load(sm + lV, &tmV, &S.bar_v, kv, tok0 + t0 + LT - WIN, bco);
                 v_out = true;
             }
         }
@@ -1202,7 +1261,10 @@ __global__ void __launch_bounds__(NL, 1)
 // a.seg receives the state each segment starts from.
 cudaError_t launch_local_and_scan(const Plan& p, const FwdArgs& a, const CUtensorMap& mw,
                                   cudaStream_t s) {
-    const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hkv = (cuuint64_t)p.Hkv;
+    // packed sequences: maps over all T rows, batch extent 1
+    const cuuint64_t B = p.cu != nullptr ? 1 : (cuuint64_t)p.B,
+                     L = p.cu != nullptr ? (cuuint64_t)p.T : (cuuint64_t)p.L,
+                     Hkv = (cuuint64_t)p.Hkv;
     const unsigned U = (unsigned)(p.B * p.Hkv);
     // 128-token tiles of the delayed keys, values and gates
     alignas(64) CUtensorMap lk, lv, lg;
@@ -1239,7 +1301,8 @@ bool make_wf_map(CUtensorMap* mw, const void* Wf, int64_t Hkv) {
 
 bool fwd_tc_supported(const Plan& p) {
     return p.dtype == LIZARD_BF16 && p.d == DH && p.D == DF && p.G == GQ && p.w == WIN &&
-           p.M <= MMAX && p.L < ((int64_t)1 << 30) && encode_fn() != nullptr;
+           p.M <= MMAX && p.L < ((int64_t)1 << 30) && p.T < ((int64_t)1 << 30) &&
+           encode_fn() != nullptr;
 }
 
 cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s) {
@@ -1257,8 +1320,9 @@ cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s
 // scan then yields the state at every finer boundary and the main walk reads every
 // rec_step-th record.
 void fwd_tc_plan(Plan* p) {
-    plan_segments_waves(p, 152);
     p->rec_step = 1;
+    if (p->cu != nullptr) return;  // packed sequences come with their segments cut
+    plan_segments_waves(p, 152);
     if (p->P <= 1) return;
     const int64_t U = p->B * p->Hkv;
     for (int64_t k = 2; k <= 8; ++k) {
@@ -1271,8 +1335,10 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     Plan p = p0;
     fwd_tc_plan(&p);
     alignas(64) CUtensorMap mq, mk, mv, mw, my;
-    const cuuint64_t B = (cuuint64_t)p.B, L = (cuuint64_t)p.L, Hq = (cuuint64_t)p.Hq,
-                     Hkv = (cuuint64_t)p.Hkv;
+    // packed sequences: maps over all T rows, batch extent 1
+    const cuuint64_t B = p.cu != nullptr ? 1 : (cuuint64_t)p.B,
+                     L = p.cu != nullptr ? (cuuint64_t)p.T : (cuuint64_t)p.L,
+                     Hq = (cuuint64_t)p.Hq, Hkv = (cuuint64_t)p.Hkv;
     {
         const cuuint64_t dims[4] = {DH, Hq, L, B};
         const cuuint64_t str[3] = {DH * 2, Hq * DH * 2, L * Hq * DH * 2};

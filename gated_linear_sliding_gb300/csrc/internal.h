@@ -24,7 +24,18 @@ struct Plan {
     int64_t nchunks, seg_chunks, seg_len, P, Pmax;
     size_t rec_floats;   // floats per (segment, unit) record: D*d + D + D
     int64_t rec_step;    // boundary records per segment: the segment pass may cut finer
+    // Packed sequences (null: a dense batch): device offsets [B+1]; sequence b is rows
+    // [cu[b], cu[b+1]) of arrays with T rows in all, and L is the longest sequence.
+    const int64_t* cu = nullptr;
+    int64_t T = 0;
 };
+// Row of sequence b's first token and the sequence's length (dense batch: b L and L).
+__host__ __device__ __forceinline__ int64_t seq_row0(const Plan& p, int64_t b) {
+    return p.cu != nullptr ? p.cu[b] : b * p.L;
+}
+__host__ __device__ __forceinline__ int64_t seq_len(const Plan& p, int64_t b) {
+    return p.cu != nullptr ? p.cu[b + 1] - p.cu[b] : p.L;
+}
 
 bool make_plan(const lizard_dims* dims, Plan* p);
 // Host-side checks shared by every forward entry point (sizes, pointers, alignment, pairs of

@@ -1,6 +1,7 @@
 // C-ABI entry points of the Lizard token-mixer library: argument validation,
 // segment planning, workspace sizes and kernel dispatch.  Every check runs on the
 // host before any launch; there is no CPU fallback.
+#include <algorithm>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -197,18 +198,128 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
     return from_cuda(fwd_launch(p, a, s));
 }
 
+}  // extern "C"
+
+namespace lz {
+
+static bool packed_offsets_ok(const lizard_dims* dims, const int64_t* cu) {
+    if (dims == nullptr || cu == nullptr || dims->B < 1 || dims->L < 0) return false;
+    const int64_t nseq = dims->B, T = dims->L;
+    if (cu[0] != 0 || cu[nseq] != T) return false;
+    for (int64_t i = 0; i < nseq; ++i)
+        if (cu[i + 1] < cu[i]) return false;
+    return true;
+}
+
+// Plan of one launch over all sequences of a packed batch (tensor-core path): sequence b is
+// batch b of a plan whose L is the longest sequence.  Segments have one length for all, about
+// a quarter of one SM's share of the batch's tokens (whole 64-token chunks), so that CTAs of
+// every length even out over the SMs; a sequence's segments past its end walk nothing.  One
+// record per (sequence x KV head, segment).  False when the batch is empty or the shapes take
+// the SIMT path.
+static bool packed_plan(const lizard_dims* dims, const int64_t* cu, Plan* p) {
+    const int64_t nseq = dims->B, T = dims->L;
+    int64_t lmax = 0;
+    for (int64_t i = 0; i < nseq; ++i) lmax = std::max<int64_t>(lmax, cu[i + 1] - cu[i]);
+    if (lmax < 1) return false;
+    lizard_dims dv = *dims;
+    dv.B = nseq;
+    dv.L = lmax;
+    if (!make_plan(&dv, p)) return false;
+    p->T = T;
+    if (!fwd_tc_supported(*p)) return false;
+    const int64_t share = (T * p->Hkv + 151) / 152;
+    int64_t sc = (share / 4 + kChunk - 1) / kChunk;
+    sc = std::max<int64_t>(1, std::min<int64_t>(sc, p->nchunks));
+    p->seg_chunks = sc;
+    p->seg_len = sc * kChunk;
+    p->P = (p->nchunks + sc - 1) / sc;
+    p->Pmax = p->P;
+    p->rec_step = 1;
+    return true;
+}
+
+// Records, then the sequence offsets (copied to the device for the kernels).
+static size_t packed_ws_bytes(const Plan& p) {
+    return fwd_workspace_bytes(p) + (size_t)(p.B + 1) * sizeof(int64_t);
+}
+
+}  // namespace lz
+
+extern "C" {
+
+size_t lizard_attn_fwd_varlen_workspace(const lizard_dims* dims, const int64_t* cu_seqlens) {
+    if (!packed_offsets_ok(dims, cu_seqlens)) return 0;
+    Plan p;
+    if (packed_plan(dims, cu_seqlens, &p)) return packed_ws_bytes(p);
+    lizard_dims d1 = *dims;  // one sequence after another
+    d1.B = 1;
+    d1.L = dims->L > 0 ? dims->L : 1;
+    return make_plan(&d1, &p) ? fwd_workspace_bytes(p) : 0;
+}
+
 lizard_status lizard_attn_fwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,
                                      const void* q, const void* k, const void* v, const void* g,
                                      const void* Wf, const float* sinks, void* y, float* lse,
                                      float* S_out, float* z_out, void* kcache_out,
                                      void* vcache_out, void* workspace, size_t ws_bytes,
                                      void* stream) {
-    if (dims == nullptr || cu_seqlens == nullptr || dims->B < 1 || dims->L < 0)
-        return LIZARD_ERR_INVALID_ARG;
+    if (!packed_offsets_ok(dims, cu_seqlens)) return LIZARD_ERR_INVALID_ARG;
     const int64_t nseq = dims->B, T = dims->L;
-    if (cu_seqlens[0] != 0 || cu_seqlens[nseq] != T) return LIZARD_ERR_INVALID_ARG;
-    for (int64_t i = 0; i < nseq; ++i)
-        if (cu_seqlens[i + 1] < cu_seqlens[i]) return LIZARD_ERR_INVALID_ARG;
+    cudaStream_t s = (cudaStream_t)stream;
+    // one launch over every sequence (tensor-core shapes, workspace of
+    // lizard_attn_fwd_varlen_workspace); otherwise the sequences run one after another
+    Plan pv;
+    if (workspace != nullptr && aligned16(workspace) && packed_plan(dims, cu_seqlens, &pv) &&
+        ws_bytes >= packed_ws_bytes(pv)) {
+        lizard_dims dv = *dims;
+        dv.L = pv.L;
+        Plan chk;
+        lizard_status st = fwd_check(&dv, &chk, q, k, v, g, Wf, sinks, y, lse, S_out, z_out,
+                                     kcache_out, vcache_out);
+        if (st != LIZARD_OK) return st;
+        st = device_status();
+        if (st != LIZARD_OK) return st;
+        const size_t Sun = (size_t)(dims->Hkv * dims->D * dims->d), zun = (size_t)(dims->Hkv * dims->D),
+                     cun = (size_t)(dims->Hkv * (dims->w + 1) * dims->d) *
+                           (dims->dtype == LIZARD_F32 ? 4 : 2);
+        cudaError_t e = cudaSuccess;
+        for (int64_t i = 0; i < nseq && e == cudaSuccess; ++i) {
+            if (cu_seqlens[i + 1] > cu_seqlens[i]) continue;
+            // an empty sequence: zero state, empty caches (its segments walk nothing)
+            if (S_out) e = cudaMemsetAsync(S_out + (size_t)i * Sun, 0, Sun * sizeof(float), s);
+            if (e == cudaSuccess && z_out)
+                e = cudaMemsetAsync(z_out + (size_t)i * zun, 0, zun * sizeof(float), s);
+            if (e == cudaSuccess && kcache_out)
+                e = cudaMemsetAsync((char*)kcache_out + (size_t)i * cun, 0, cun, s);
+            if (e == cudaSuccess && vcache_out)
+                e = cudaMemsetAsync((char*)vcache_out + (size_t)i * cun, 0, cun, s);
+        }
+        int64_t* cu_dev = (int64_t*)((char*)workspace + fwd_workspace_bytes(pv));
+        if (e == cudaSuccess)  // (from pageable memory: staged before the call returns)
+            e = cudaMemcpyAsync(cu_dev, cu_seqlens, (size_t)(nseq + 1) * sizeof(int64_t),
+                                cudaMemcpyHostToDevice, s);
+        if (e != cudaSuccess) return from_cuda(e);
+        pv.cu = cu_dev;
+        FwdArgs a;
+        a.q = q;
+        a.k = k;
+        a.v = v;
+        a.g = g;
+        a.Wf = Wf;
+        a.sinks = sinks;
+        a.y = y;
+        a.lse = lse;
+        a.S_out = S_out;
+        a.z_out = z_out;
+        a.kcache_out = kcache_out;
+        a.vcache_out = vcache_out;
+        a.header = workspace;
+        a.seg = (float*)((char*)workspace + kHeaderBytes);
+        a.ev_before = g_ev_before;
+        a.ev_after = g_ev_after;
+        return from_cuda(fwd_launch(pv, a, s));
+    }
     // every sequence is a B = 1 problem; its workspace does not depend on its length
     lizard_dims d1 = *dims;
     d1.B = 1;
@@ -221,7 +332,6 @@ lizard_status lizard_attn_fwd_varlen(const lizard_dims* dims, const int64_t* cu_
                  grow = (size_t)(d1.Hkv * d1.D) * E;
     const size_t Sun = (size_t)(d1.Hkv * d1.D * d1.d), zun = (size_t)(d1.Hkv * d1.D),
                  cun = (size_t)(d1.Hkv * (d1.w + 1) * d1.d) * E;
-    cudaStream_t s = (cudaStream_t)stream;
     for (int64_t i = 0; i < nseq; ++i) {
         const int64_t t0 = cu_seqlens[i], n = cu_seqlens[i + 1] - t0;
         float* Si = S_out ? S_out + (size_t)i * Sun : nullptr;

@@ -218,6 +218,12 @@ def make_shared_params(wl: Workload) -> dict:
     return dict(Wf=round_to(Wf, wl.dtype), sinks=np.ascontiguousarray(sinks, np.float32))
 
 
+def varlen_lengths(n: int = 64, lo: int = 128, hi: int = 4096, seed: int = 5) -> list:
+    """Lengths of a packed serving batch: n sequences, lengths uniform on [lo, hi] (seeded)."""
+    rng = np.random.default_rng(seed)
+    return [int(x) for x in rng.integers(lo, hi + 1, size=n)]
+
+
 def make_device_inputs(wl: Workload, device, L: int | None = None, B: int | None = None,
                        with_dy: bool = False, seed_offset: int = 0) -> dict:
     """Same laws as make_inputs, drawn on the device with torch's Philox generator.

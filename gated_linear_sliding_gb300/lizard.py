@@ -31,6 +31,7 @@ EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_f
             "lizard_status_string",
             "lizard_profile_events", "lizard_version", "lizard_attn_fwd_noalloc",
             "lizard_attn_fwd_kernel", "lizard_selftest_wait_timeout", "lizard_attn_fwd_varlen",
+            "lizard_attn_fwd_varlen_workspace",
             "lizard_attn_bwd_varlen_workspace", "lizard_attn_bwd_varlen",
             "lizard_attn_fwd_noalloc_scratch", "lizard_read_noalloc_status",
             "lizard_qkvg_proj", "lizard_qkvg_proj_bwd"]
@@ -78,6 +79,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_workspace_init.restype = ctypes.c_int
     lib.lizard_attn_fwd.argtypes = [_DP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_fwd.restype = ctypes.c_int
+    lib.lizard_attn_fwd_varlen_workspace.argtypes = [_DP, _VP]
+    lib.lizard_attn_fwd_varlen_workspace.restype = ctypes.c_size_t
     lib.lizard_attn_fwd_varlen.argtypes = [_DP, _VP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_fwd_varlen.restype = ctypes.c_int
     lib.lizard_attn_bwd_varlen_workspace.argtypes = [_DP, _VP]
@@ -262,6 +265,12 @@ def lizard_attn_fwd(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0, y=None
     return y
 
 
+def lizard_attn_fwd_varlen_workspace(dims, cu_seqlens) -> int:
+    """Workspace bytes for one launch of lizard_attn_fwd_varlen over all sequences."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    return int(load().lizard_attn_fwd_varlen_workspace(ctypes.byref(dims), cu.ctypes.data))
+
+
 def lizard_attn_fwd_varlen(q, k, v, g, Wf, sinks, w: int, cu_seqlens, *, scale: float = 0.0,
                            y=None, lse=None, S_out=None, z_out=None, kcache_out=None,
                            vcache_out=None, workspace=None, stream=None):
@@ -270,7 +279,7 @@ def lizard_attn_fwd_varlen(q, k, v, g, Wf, sinks, w: int, cu_seqlens, *, scale: 
     S_out, z_out, kcache_out, vcache_out hold one entry per sequence."""
     T, Hq, d = q.shape
     Hkv, D, M = k.shape[1], g.shape[-1], sinks.shape[1]
-    cu = np.asarray(cu_seqlens, dtype=np.int64)
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
     nseq = cu.shape[0] - 1
     dt = q.dtype
     _need(q, "q", (T, Hq, d), dt)
@@ -291,9 +300,8 @@ def lizard_attn_fwd_varlen(q, k, v, g, Wf, sinks, w: int, cu_seqlens, *, scale: 
         _need(kcache_out, "kcache_out", (nseq, Hkv, w + 1, d), dt)
         _need(vcache_out, "vcache_out", (nseq, Hkv, w + 1, d), dt)
     dims = lizard_dims(nseq, T, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
-    if workspace is None:
-        one = lizard_dims(1, max(T, 1), Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
-        workspace = new_workspace(lizard_attn_fwd_workspace(one), q.device, stream)
+    if workspace is None:  # the size of one launch over all sequences
+        workspace = new_workspace(lizard_attn_fwd_varlen_workspace(dims, cu), q.device, stream)
     st = load().lizard_attn_fwd_varlen(ctypes.byref(dims), cu.ctypes.data, _p(q), _p(k), _p(v),
                                        _p(g), _p(Wf), _p(sinks), _p(y), _p(lse), _p(S_out),
                                        _p(z_out), _p(kcache_out), _p(vcache_out), _p(workspace),

@@ -100,6 +100,13 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
                               void* y, float* lse, float* S_out, float* z_out, void* kcache_out,
                               void* vcache_out, void* workspace, size_t ws_bytes, void* stream);
 
+/* Bytes of device workspace for one launch of lizard_attn_fwd_varlen over all sequences of
+ * this packed batch (dims.B sequences, dims.L tokens in all, host offsets cu_seqlens as
+ * below): the header, one boundary record of (D d + 2 D) floats per (sequence x KV head,
+ * segment) and the B + 1 offsets.  For shapes that run one sequence at a time it is the
+ * workspace of a single sequence.  0 for invalid dims or offsets. */
+size_t lizard_attn_fwd_varlen_workspace(const lizard_dims* dims, const int64_t* cu_seqlens);
+
 /* The forward over a packed batch of sequences of different lengths (variable-length
  * batching).  dims.B is the number of sequences and dims.L the total number of tokens T;
  * cu_seqlens is a HOST array of B + 1 offsets (cu_seqlens[0] = 0, non-decreasing,
@@ -108,11 +115,16 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
  *   packed layouts are those of lizard_attn_fwd with B = 1 and L = T.
  *   S_out, z_out, kcache_out, vcache_out (nullable, in pairs) hold one entry per sequence:
  *   [B, Hkv, D, d], [B, Hkv, D], [B, Hkv, w+1, d]; an empty sequence gets a zero state.
- *   workspace, ws_bytes >= lizard_attn_fwd_workspace with dims.B = 1 (any L).
+ *   workspace: ws_bytes >= lizard_attn_fwd_varlen_workspace(dims, cu_seqlens) gives one
+ *   launch over all sequences; a workspace of at least lizard_attn_fwd_workspace with
+ *   dims.B = 1 (any L) but below that runs the sequences one after another.
  * Each sequence's results equal lizard_attn_fwd on that sequence alone: no state, window
- * or token crosses a sequence boundary.  The sequences run one after another on `stream`,
- * each cut into segments on its own, so long sequences fill the GPU and many short ones are
- * bound by launches.  Every sequence's slice must meet lizard_attn_fwd's 16-byte alignment
+ * or token crosses a sequence boundary.  With the larger workspace and the tensor-core
+ * shapes (bf16, d = D = 128, four query heads per KV head, w = 64) every sequence is walked
+ * in the same launches: its tokens are cut into segments of one length for the whole batch,
+ * a (sequence x KV head, segment) CTA per segment, so a batch of many short sequences fills
+ * the GPU as one long one does; other shapes run one sequence after another, each cut into
+ * segments on its own.  Every sequence's slice must meet lizard_attn_fwd's 16-byte alignment
  * (for lse: Hq * 4 * cu_seqlens[i] a multiple of 16, true whenever Hq >= 4); errors are those
  * of lizard_attn_fwd, plus LIZARD_ERR_INVALID_ARG for inconsistent offsets. */
 lizard_status lizard_attn_fwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,

@@ -177,3 +177,24 @@ def test_bwd_varlen_workspace_and_offsets(lib):
     nul = [None] * 16
     assert lib.lizard_attn_bwd_varlen(ctypes.byref(d), bad, *nul, 1 << 30, None) == \
         lz.LIZARD_ERR_INVALID_ARG
+
+
+def test_fwd_varlen_workspace_query(lib):
+    """The packed forward's workspace: one launch over all sequences needs a boundary record per
+    (sequence x KV head, segment) plus the offsets, more than one sequence's workspace; where
+    the tensor-core path is unavailable it is the sequence loop's workspace; 0 for
+    inconsistent offsets (no device work involved)."""
+    d = dims(L=3000)
+    d.B = 3
+    ok = (ctypes.c_int64 * 4)(0, 1000, 1000, 3000)
+    bad = (ctypes.c_int64 * 4)(0, 1000, 999, 3000)
+    lib.lizard_attn_fwd_varlen_workspace.argtypes = [ctypes.c_void_p, ctypes.c_void_p]
+    lib.lizard_attn_fwd_varlen_workspace.restype = ctypes.c_size_t
+    w_ok = lib.lizard_attn_fwd_varlen_workspace(ctypes.byref(d), ok)
+    loop = lz.lizard_attn_fwd_workspace(dims(L=3000))
+    if lz.lizard_attn_fwd_kernel(dims(L=3000)) == 1:
+        rec = (128 * 128 + 2 * 128) * 4
+        assert w_ok >= 256 + 3 * 8 * rec + 4 * 8 and w_ok > loop
+    else:
+        assert w_ok == loop
+    assert lib.lizard_attn_fwd_varlen_workspace(ctypes.byref(d), bad) == 0

@@ -153,9 +153,9 @@ def test_decode_writes_stay_in_bounds(lz, oracle_mod, dtype):
     assert_parity(to_np(torch.stack(ys, 1)), ref, dtype, "decode y")
 
 
-@pytest.mark.parametrize("path", ["tc", "simt"])
+@pytest.mark.parametrize("path", ["tc", "tc_one_launch", "simt"])
 def test_varlen_writes_stay_in_bounds(lz, path):
-    wl = WORKLOADS[path]
+    wl = WORKLOADS["tc" if path == "tc_one_launch" else path]
     lens = [1, 33, 0, 517, 1100]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
     T = int(cu[-1])
@@ -172,7 +172,11 @@ def test_varlen_writes_stay_in_bounds(lz, path):
     kc = g.empty((n, wl.Hkv, wl.w + 1, wl.d), dt)
     vc = g.empty((n, wl.Hkv, wl.w + 1, wl.d), dt)
     one = lz.make_dims(1, T, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, dt)
-    ws = _ws(lz, g, lz.lizard_attn_fwd_workspace(one))
+    if path == "tc_one_launch":  # every sequence in one launch (direct stores of ragged ends)
+        dims = lz.make_dims(n, T, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, dt)
+        ws = _ws(lz, g, lz.lizard_attn_fwd_varlen_workspace(dims, cu))
+    else:  # one sequence after another
+        ws = _ws(lz, g, lz.lizard_attn_fwd_workspace(one))
     lz.lizard_attn_fwd_varlen(pk["q"], pk["k"], pk["v"], pk["g"], t["Wf"], t["sinks"], wl.w, cu,
                               y=y, lse=lse, S_out=S, z_out=z, kcache_out=kc, vcache_out=vc,
                               workspace=ws)

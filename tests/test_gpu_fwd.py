@@ -170,19 +170,26 @@ def test_workspace_reuse_and_determinism(lz):
     assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
 
 
+def _varlen_run(lz, wl, t, cu, workspace=None):
+    T, nseq = int(cu[-1]), len(cu) - 1
+    packed = {n: t[n][0] for n in ("q", "k", "v", "g")}
+    S = torch.empty(nseq, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.empty(nseq, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    lse = torch.empty(T, wl.Hq, dtype=torch.float32, device="cuda")
+    y = lz.lizard_attn_fwd_varlen(packed["q"], packed["k"], packed["v"], packed["g"], t["Wf"],
+                                  t["sinks"], wl.w, cu, lse=lse, S_out=S, z_out=z,
+                                  workspace=workspace)
+    return y, S, z, lse
+
+
 def _varlen_case(lz, oracle_mod, wl, lens):
     """A packed batch of sequences against the oracle run on each sequence alone."""
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
     T = int(cu[-1])
     inp = I.make_inputs(wl.replace(B=1, L=T))
     t = to_dev(inp, wl.dtype)
-    packed = {n: t[n][0] for n in ("q", "k", "v", "g")}
     nseq = len(lens)
-    S = torch.empty(nseq, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
-    z = torch.empty(nseq, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
-    lse = torch.empty(T, wl.Hq, dtype=torch.float32, device="cuda")
-    y = lz.lizard_attn_fwd_varlen(packed["q"], packed["k"], packed["v"], packed["g"], t["Wf"],
-                                  t["sinks"], wl.w, cu, lse=lse, S_out=S, z_out=z)
+    y, S, z, lse = _varlen_run(lz, wl, t, cu)
     torch.cuda.synchronize()
     y, S, z = to_np(y), to_np(S), to_np(z)
     for i in range(nseq):
@@ -204,6 +211,47 @@ def test_varlen_packed_batch_bf16(lz, oracle_mod):
 
 def test_varlen_packed_batch_f32(lz, oracle_mod):
     _varlen_case(lz, oracle_mod, I.TINY_F32.replace(Hq=4, Hkv=2), [40, 3, 129, 64])
+
+
+def test_varlen_one_launch_several_segments(lz, oracle_mod):
+    """One launch over sequences long enough to span several segments of the packed plan
+    (the segment pass, whose first tile reaches 64 tokens before each sequence start, the
+    scan and the main walk all cross packed boundaries), with ragged ends, a one-token and an
+    empty sequence; each sequence equals its own forward."""
+    _varlen_case(lz, oracle_mod, I.LLAMA3_8B_L8K, [2600, 33, 1, 0, 1500, 64, 2100])
+
+
+def test_varlen_one_launch_closed_gates(lz, oracle_mod):
+    """Strongly closed gates in a packed batch: steps handed to the exact tail walk, which
+    walks each packed sequence from its own rows."""
+    _varlen_case(lz, oracle_mod, I.closed_gates(I.LLAMA3_8B_L8K, per_1k=8.0), [1700, 300, 900])
+
+
+def test_varlen_one_launch_matches_sequence_loop(lz):
+    """The one-launch path and the sequence-by-sequence path (chosen by a workspace too small
+    for the first) agree.  They cut segments differently, so the state reaches each boundary
+    through different bf16-rounded update products: y within bf16 rounding, S, z and lse
+    within 1e-3 relative (each path also meets the oracle bounds, tested above)."""
+    wl = I.LLAMA3_8B_L8K
+    lens = [700, 129, 2000, 5, 1000]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T = int(cu[-1])
+    t = to_dev(I.make_inputs(wl.replace(B=1, L=T)), wl.dtype)
+    dims = lz.make_dims(len(lens), T, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, torch.bfloat16)
+    one = lz.make_dims(1, T, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, torch.bfloat16)
+    big, small = lz.lizard_attn_fwd_varlen_workspace(dims, cu), lz.lizard_attn_fwd_workspace(one)
+    assert big > small > 0
+    ws_big = lz.new_workspace(big, torch.device("cuda"))
+    ws_small = lz.new_workspace(small, torch.device("cuda"))
+    ya, Sa, za, la = _varlen_run(lz, wl, t, cu, ws_big)
+    yb, Sb, zb, lb = _varlen_run(lz, wl, t, cu, ws_small)
+    torch.cuda.synchronize()
+    assert lz.lizard_read_device_status(ws_big) == lz.LIZARD_OK
+    ya, yb = to_np(ya), to_np(yb)
+    assert np.abs(ya - yb).max() <= 2e-2 * np.sqrt(np.mean(yb * yb)) + 1e-30
+    for x, r in ((Sa, Sb), (za, zb), (la, lb)):
+        x, r = to_np(x), to_np(r)
+        assert np.linalg.norm(x - r) <= 1e-3 * np.linalg.norm(r)
 
 
 def _closed_quarters(g) -> int:
