@@ -2,6 +2,7 @@
 // segment planning, workspace sizes and kernel dispatch.  Every check runs on the
 // host before any launch; there is no CPU fallback.
 #include <algorithm>
+#include <vector>
 #include <math.h>
 #include <stdint.h>
 #include <string.h>
@@ -430,12 +431,80 @@ static size_t bwd_varlen_main_bytes(const lizard_dims* dims, const int64_t* cu) 
     return (bwd_workspace_bytes(p) + 255) & ~(size_t)255;
 }
 
+}  // extern "C"
+
+namespace lz {
+
+// The packed backward runs its sequences as independent backwards on kBwdLanes streams, forked
+// from the caller's stream and joined back before the call returns; each lane has its own
+// slice of the workspace (its own status word) and its own dWf, dsinks partials.
+constexpr int kBwdLanes = 4;
+
+struct LanePool {
+    int dev = -1;
+    cudaStream_t s[kBwdLanes];
+    cudaEvent_t done[kBwdLanes], fork;
+};
+static LanePool g_lanes;
+
+// The lanes' streams and events, made once for the first device that asks (null on another).
+static LanePool* lane_pool() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+    if (g_lanes.dev == dev) return &g_lanes;
+    if (g_lanes.dev != -1) return nullptr;
+    for (int k = 0; k < kBwdLanes; ++k) {
+        if (cudaStreamCreateWithFlags(&g_lanes.s[k], cudaStreamNonBlocking) != cudaSuccess ||
+            cudaEventCreateWithFlags(&g_lanes.done[k], cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+    }
+    if (cudaEventCreateWithFlags(&g_lanes.fork, cudaEventDisableTiming) != cudaSuccess)
+        return nullptr;
+    g_lanes.dev = dev;
+    return &g_lanes;
+}
+
+static size_t round256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// dst[i] = sum over the lanes in `mask`, lane 0 first, of src[k stride + i].
+__global__ void sum_lanes(float* dst, const float* src, size_t n, size_t stride, unsigned mask) {
+    const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    float acc = 0.0f;
+    bool first = true;
+    for (int k = 0; k < kBwdLanes; ++k) {
+        if (!((mask >> k) & 1u)) continue;
+        acc = first ? src[(size_t)k * stride + i] : acc + src[(size_t)k * stride + i];
+        first = false;
+    }
+    dst[i] = acc;
+}
+
+// The first error a lane recorded reaches the caller's status word; lane words are cleared.
+__global__ void merge_lane_status(WsHeader* head, char* ws, size_t lane_bytes) {
+    if (threadIdx.x != 0) return;
+    for (int k = 1; k < kBwdLanes; ++k) {
+        WsHeader* h = (WsHeader*)(ws + (size_t)k * lane_bytes);
+        if (h->status != 0u && head->status == 0u) {
+            head->status = h->status;
+            head->where = h->where;
+        }
+        h->status = 0u;
+        h->where = 0u;
+    }
+}
+
+}  // namespace lz
+
+extern "C" {
+
 size_t lizard_attn_bwd_varlen_workspace(const lizard_dims* dims, const int64_t* cu_seqlens) {
     if (!varlen_offsets_ok(dims, cu_seqlens)) return 0;
     const size_t main = bwd_varlen_main_bytes(dims, cu_seqlens);
     if (main == 0) return 0;
     const size_t nW = (size_t)(dims->Hkv * dims->d * (dims->D / 2)), nt = (size_t)(dims->Hq * dims->M);
-    return main + ((nW * 4 + 255) & ~(size_t)255) + ((nt * 4 + 255) & ~(size_t)255);
+    // per lane: a backward's workspace, the dWf and dsinks of one sequence, the lane's sums
+    return (size_t)kBwdLanes * (main + 2 * round256(nW * 4) + 2 * round256(nt * 4));
 }
 
 lizard_status lizard_attn_bwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,
@@ -445,14 +514,100 @@ lizard_status lizard_attn_bwd_varlen(const lizard_dims* dims, const int64_t* cu_
                                      void* dv, void* dg, float* dWf, float* dsinks,
                                      void* workspace, size_t ws_bytes, void* stream) {
     if (!varlen_offsets_ok(dims, cu_seqlens)) return LIZARD_ERR_INVALID_ARG;
-    const size_t need = lizard_attn_bwd_varlen_workspace(dims, cu_seqlens);
-    if (need == 0) return LIZARD_ERR_INVALID_ARG;
-    if (workspace == nullptr || ws_bytes < need) return LIZARD_ERR_WORKSPACE;
-    if (dWf == nullptr || (dims->M > 0 && dsinks == nullptr)) return LIZARD_ERR_INVALID_ARG;
+    const size_t need_lanes = lizard_attn_bwd_varlen_workspace(dims, cu_seqlens);
+    if (need_lanes == 0) return LIZARD_ERR_INVALID_ARG;
     const size_t main = bwd_varlen_main_bytes(dims, cu_seqlens);
     const size_t nW = (size_t)(dims->Hkv * dims->d * (dims->D / 2)), nt = (size_t)(dims->Hq * dims->M);
+    const size_t rW = round256(nW * 4), rt = round256(nt * 4);
+    // one backward at a time needs a single lane's share
+    if (workspace == nullptr || ws_bytes < main + rW + rt) return LIZARD_ERR_WORKSPACE;
+    if (dWf == nullptr || (dims->M > 0 && dsinks == nullptr)) return LIZARD_ERR_INVALID_ARG;
+    LanePool* pool = ws_bytes >= need_lanes && dims->B > 1 ? lane_pool() : nullptr;
+    if (pool != nullptr) {
+        cudaStream_t s = (cudaStream_t)stream;
+        char* ws = (char*)workspace;
+        char* temps = ws + (size_t)kBwdLanes * main;   // [lane] dWf, then [lane] dsinks of one sequence
+        char* sums = temps + (size_t)kBwdLanes * (rW + rt);  // the lanes' running sums, same layout
+        auto tW = [&](int ln) { return (float*)(temps + (size_t)ln * rW); };
+        auto tt = [&](int ln) { return (float*)(temps + (size_t)kBwdLanes * rW + (size_t)ln * rt); };
+        auto aW = [&](int ln) { return (float*)(sums + (size_t)ln * rW); };
+        auto at = [&](int ln) { return (float*)(sums + (size_t)kBwdLanes * rW + (size_t)ln * rt); };
+        // longest sequences first, each to the lane with the fewest tokens so far (ties: lower
+        // lane); each lane then runs its sequences in index order
+        const int64_t nseq = dims->B;
+        std::vector<int64_t> order(nseq);
+        for (int64_t i = 0; i < nseq; ++i) order[i] = i;
+        std::stable_sort(order.begin(), order.end(), [&](int64_t x, int64_t y) {
+            return cu_seqlens[x + 1] - cu_seqlens[x] > cu_seqlens[y + 1] - cu_seqlens[y];
+        });
+        std::vector<int> lane_of(nseq, 0);
+        int64_t load[kBwdLanes] = {};
+        for (int64_t i : order) {
+            int best = 0;
+            for (int ln = 1; ln < kBwdLanes; ++ln)
+                if (load[ln] < load[best]) best = ln;
+            lane_of[i] = best;
+            load[best] += cu_seqlens[i + 1] - cu_seqlens[i];
+        }
+        cudaError_t e = cudaSuccess;
+        for (int ln = 1; ln < kBwdLanes && e == cudaSuccess; ++ln)  // the lanes' status words
+            e = cudaMemsetAsync(ws + (size_t)ln * main, 0, kHeaderBytes, s);
+        if (e == cudaSuccess) e = cudaEventRecord(pool->fork, s);
+        for (int ln = 0; ln < kBwdLanes && e == cudaSuccess; ++ln)
+            e = cudaStreamWaitEvent(pool->s[ln], pool->fork, 0);
+        if (e != cudaSuccess) return from_cuda(e);
+        lizard_dims d1 = *dims;
+        d1.B = 1;
+        const size_t E = d1.dtype == LIZARD_F32 ? 4 : 2;
+        const size_t qrow = (size_t)(d1.Hq * d1.d) * E, krow = (size_t)(d1.Hkv * d1.d) * E,
+                     grow = (size_t)(d1.Hkv * d1.D) * E;
+        unsigned used = 0u;
+        lizard_status st = LIZARD_OK;
+        for (int64_t i = 0; i < nseq && st == LIZARD_OK; ++i) {
+            const int64_t t0 = cu_seqlens[i], n = cu_seqlens[i + 1] - t0;
+            if (n == 0) continue;  // no tokens: no gradient slice, nothing to add
+            const int ln = lane_of[i];
+            cudaStream_t ls = pool->s[ln];
+            d1.L = n;
+            st = lizard_attn_bwd(
+                &d1, (const char*)q + t0 * qrow, (const char*)k + t0 * krow,
+                (const char*)v + t0 * krow, (const char*)g + t0 * grow, Wf, sinks,
+                (const char*)y + t0 * qrow, lse + t0 * d1.Hq, (const char*)dy + t0 * qrow,
+                (char*)dq + t0 * qrow, (char*)dk + t0 * krow, (char*)dv + t0 * krow,
+                (char*)dg + t0 * grow, tW(ln), dims->M > 0 ? tt(ln) : nullptr,
+                ws + (size_t)ln * main, main, ls);
+            if (st != LIZARD_OK) break;
+            const int first = (used >> ln) & 1u ? 0 : 1;
+            add_or_copy<<<(unsigned)((nW + 255) / 256), 256, 0, ls>>>(aW(ln), tW(ln), nW, first);
+            if (dims->M > 0)
+                add_or_copy<<<(unsigned)((nt + 255) / 256), 256, 0, ls>>>(at(ln), tt(ln), nt, first);
+            if (cudaGetLastError() != cudaSuccess) st = LIZARD_ERR_CUDA;
+            used |= 1u << ln;
+        }
+        // every lane joins the caller's stream, whatever happened above
+        for (int ln = 0; ln < kBwdLanes; ++ln) {
+            if (cudaEventRecord(pool->done[ln], pool->s[ln]) != cudaSuccess ||
+                cudaStreamWaitEvent(s, pool->done[ln], 0) != cudaSuccess)
+                st = LIZARD_ERR_CUDA;
+        }
+        if (st != LIZARD_OK) return st;
+        if (used == 0u) {  // every sequence is empty: zero parameter gradients
+            e = cudaMemsetAsync(dWf, 0, nW * 4, s);
+            if (e == cudaSuccess && dims->M > 0) e = cudaMemsetAsync(dsinks, 0, nt * 4, s);
+        } else {
+            sum_lanes<<<(unsigned)((nW + 255) / 256), 256, 0, s>>>(dWf, aW(0), nW, rW / 4, used);
+            if (dims->M > 0)
+                sum_lanes<<<(unsigned)((nt + 255) / 256), 256, 0, s>>>(dsinks, at(0), nt, rt / 4, used);
+            e = cudaGetLastError();
+        }
+        if (e == cudaSuccess) {
+            merge_lane_status<<<1, 32, 0, s>>>((WsHeader*)ws, ws, main);
+            e = cudaGetLastError();
+        }
+        return from_cuda(e);
+    }
     float* tW = (float*)((char*)workspace + main);
-    float* tt = (float*)((char*)workspace + main + ((nW * 4 + 255) & ~(size_t)255));
+    float* tt = (float*)((char*)workspace + main + rW);
     lizard_dims d1 = *dims;
     d1.B = 1;
     const size_t E = d1.dtype == LIZARD_F32 ? 4 : 2;

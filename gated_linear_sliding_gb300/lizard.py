@@ -368,6 +368,12 @@ def lizard_attn_bwd(q, k, v, g, Wf, sinks, y, lse, dy, w: int, *, scale: float =
     return dict(dq=dq, dk=dk, dv=dv, dg=dg, dWf=dWf, dsinks=dsinks)
 
 
+def lizard_attn_bwd_varlen_workspace(dims, cu_seqlens) -> int:
+    """Workspace bytes of lizard_attn_bwd_varlen for this packed batch (0: bad offsets)."""
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    return int(load().lizard_attn_bwd_varlen_workspace(ctypes.byref(dims), cu.ctypes.data))
+
+
 def lizard_attn_bwd_varlen(q, k, v, g, Wf, sinks, y, lse, dy, w: int, cu_seqlens, *,
                            scale: float = 0.0, workspace=None, stream=None):
     """Gradients of lizard_attn_fwd_varlen's y against dy for a packed batch: dq, dk, dv,

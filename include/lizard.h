@@ -193,17 +193,23 @@ lizard_status lizard_attn_bwd(const lizard_dims* dims, const void* q, const void
                               void* dv, void* dg, float* dWf, float* dsinks, void* workspace,
                               size_t ws_bytes, void* stream);
 
-/* Bytes of device workspace lizard_attn_bwd_varlen needs for this packed batch (dims.B
+/* Bytes of device workspace for lizard_attn_bwd_varlen on this packed batch (dims.B
  * sequences, dims.L tokens in all, host offsets cu_seqlens as for lizard_attn_fwd_varlen):
- * the largest single-sequence backward workspace plus the per-sequence dWf and dsinks;
- * 0 for inconsistent offsets. */
+ * four lanes, each with the largest single-sequence backward workspace and room for one
+ * sequence's dWf and dsinks and the lane's sums of them; 0 for inconsistent offsets.  A
+ * quarter of it (one lane) is the least the call accepts. */
 size_t lizard_attn_bwd_varlen_workspace(const lizard_dims* dims, const int64_t* cu_seqlens);
 
 /* Backward of lizard_attn_fwd_varlen: packed q, k, v, g, y, dy, dq, dk, dv, dg [T, ...] and
  * lse [T, Hq] as in the forward; dWf [Hkv, d, D/2] and dsinks [Hq, M] fp32 are the sums over
- * the sequences (added in sequence order, so the result is deterministic).  Each sequence's
- * dq, dk, dv, dg equal lizard_attn_bwd on that sequence alone; sequences run one after
- * another on `stream`.  workspace >= lizard_attn_bwd_varlen_workspace; errors as for
+ * the sequences.  Each sequence's dq, dk, dv, dg equal lizard_attn_bwd on that sequence
+ * alone.  With the full lizard_attn_bwd_varlen_workspace the sequences run as independent
+ * backwards on four streams of the library's own, forked from `stream` and joined back to it
+ * before the call returns (longest sequences first, each to the lane with the fewest tokens
+ * so far); each lane sums its sequences' dWf, dsinks in sequence order and the lanes are added
+ * in lane order, so the result is deterministic for a given batch.  A workspace of one lane's
+ * share runs the sequences one after another on `stream`, summed in sequence order.  Device
+ * errors of every lane reach the status word at the head of `workspace`.  Errors as for
  * lizard_attn_bwd, plus LIZARD_ERR_INVALID_ARG for inconsistent offsets. */
 lizard_status lizard_attn_bwd_varlen(const lizard_dims* dims, const int64_t* cu_seqlens,
                                      const void* q, const void* k, const void* v, const void* g,
