@@ -7,6 +7,8 @@ Lengths are ragged (1, 33, 517, 1000, 1100 tokens) so that partial tiles, partia
 steps and partial TMA stores are written, on the tensor-core path (bf16, d = D = 128, four
 query heads per KV head, window 64) and on the SIMT path (fp32).
 """
+import ctypes
+
 import numpy as np
 import pytest
 
@@ -182,3 +184,37 @@ def test_varlen_writes_stay_in_bounds(lz, path):
                               workspace=ws)
     g.check()
     assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+
+
+def test_varlen_backward_writes_stay_in_bounds(lz):
+    """The packed backward on four streams: dq, dk, dv, dg of every ragged sequence, dWf, dsinks
+    and the workspace tail keep their slack untouched."""
+    wl = I.MISTRAL_7B_TRAIN
+    lens = [1, 33, 0, 517, 1100, 70]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T, n = int(cu[-1]), len(lens)
+    inp = I.make_inputs(wl.replace(B=1, L=T), with_dy=True)
+    t = to_dev(inp, wl.dtype)
+    pk = {k: t[k][0] for k in ("q", "k", "v", "g", "dy")}
+    dt = pk["q"].dtype
+    lse = torch.empty(T, wl.Hq, device="cuda")
+    y = lz.lizard_attn_fwd_varlen(pk["q"], pk["k"], pk["v"], pk["g"], t["Wf"], t["sinks"], wl.w,
+                                  cu, lse=lse)
+    g = Guarded()
+    out = dict(dq=g.empty((T, wl.Hq, wl.d), dt), dk=g.empty((T, wl.Hkv, wl.d), dt),
+               dv=g.empty((T, wl.Hkv, wl.d), dt), dg=g.empty((T, wl.Hkv, wl.D), dt),
+               dWf=g.empty((wl.Hkv, wl.d, wl.D // 2), torch.float32),
+               dsinks=g.empty((wl.Hq, wl.M), torch.float32))
+    dims = lz.make_dims(n, T, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, dt)
+    ws = _ws(lz, g, lz.lizard_attn_bwd_varlen_workspace(dims, cu))
+    lib = lz.load()
+    st = lib.lizard_attn_bwd_varlen(
+        ctypes.byref(dims), np.ascontiguousarray(cu).ctypes.data, *(lz._p(x) for x in (
+            pk["q"], pk["k"], pk["v"], pk["g"], t["Wf"], t["sinks"], y, lse, pk["dy"],
+            out["dq"], out["dk"], out["dv"], out["dg"], out["dWf"], out["dsinks"], ws)),
+        ws.numel(), None)
+    assert st == lz.LIZARD_OK
+    g.check()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    for k in ("dq", "dk", "dv", "dg", "dWf", "dsinks"):
+        assert bool(torch.isfinite(out[k].float()).all()), k
