@@ -44,8 +44,16 @@ def build(force: bool = False) -> str:
 
 
 class _Dims(ctypes.Structure):
-    _fields_ = [(n, ctypes.c_long) for n in ("B", "L", "Hq", "Hkv", "d", "D", "w", "M")] + [
-        ("scale", ctypes.c_double)]
+    _fields_ = [(n, ctypes.c_long) for n in ("B", "L", "Hq", "Hkv", "d", "D", "w", "M",
+                                             "reading")] + [("scale", ctypes.c_double)]
+
+
+# Readings of which gates decay a key that has left the window (the pages fix none):
+# the weight of key j <= i - w at query i is the product of Gamma_s over
+#   DELAYED  s = j+w+1 .. i   (the key enters the state undecayed as it leaves the window),
+#   MASKED   s = j+1 .. i     (full gated linear attention with the window masked out),
+#   LAGGED   s = j+1 .. i-w   (the query reads the state of token i-w).
+DELAYED, MASKED, LAGGED = 0, 1, 2
 
 
 _P = ctypes.POINTER(ctypes.c_double)
@@ -58,7 +66,7 @@ def _load():
         lib = ctypes.CDLL(_LIB_PATH)
         lib.ora_fwd.argtypes = [ctypes.POINTER(_Dims)] + [_P] * 14
         lib.ora_fwd.restype = ctypes.c_int
-        lib.ora_decode_step.argtypes = [ctypes.POINTER(_Dims), ctypes.c_long] + [_P] * 11
+        lib.ora_decode_step.argtypes = [ctypes.POINTER(_Dims), ctypes.c_long] + [_P] * 12
         lib.ora_decode_step.restype = ctypes.c_int
         lib.ora_bwd.argtypes = [ctypes.POINTER(_Dims)] + [_P] * 13
         lib.ora_bwd.restype = ctypes.c_int
@@ -74,23 +82,24 @@ def _ptr(a):
     return None if a is None else a.ctypes.data_as(_P)
 
 
-def _dims(q, k, g, sinks, w, scale):
+def _dims(q, k, g, sinks, w, scale, reading=DELAYED):
     B, L, Hq, d = q.shape
     Hkv = k.shape[2]
     D = g.shape[3]
     M = sinks.shape[1]
     if scale is None:
         scale = 1.0 / np.sqrt(d)
-    return _Dims(B, L, Hq, Hkv, d, D, w, M, float(scale))
+    return _Dims(B, L, Hq, Hkv, d, D, w, M, int(reading), float(scale))
 
 
 def fwd(q, k, v, g, Wf, sinks, w: int, scale: float | None = None, parts: bool = False,
-        state: bool = False) -> dict:
+        state: bool = False, reading: int = DELAYED) -> dict:
     """Recurrent fp64 forward.  Returns {"y"} and optionally the state (S, z) after
-    the last token and the parts num_gla, den_gla, num_win, den_win, den."""
+    the last token and the parts num_gla, den_gla, num_win, den_win, den.  `reading`
+    picks the decay reading (DELAYED, MASKED or LAGGED)."""
     lib = _load()
     q, k, v, g, Wf, sinks = map(_f64, (q, k, v, g, Wf, sinks))
-    p = _dims(q, k, g, sinks, w, scale)
+    p = _dims(q, k, g, sinks, w, scale, reading)
     B, L, Hq, d = q.shape
     Hkv, D = k.shape[2], g.shape[3]
     out = {"y": np.zeros_like(q)}
@@ -113,29 +122,33 @@ def fwd(q, k, v, g, Wf, sinks, w: int, scale: float | None = None, parts: bool =
 
 
 def decode_step(pos: int, q, k, v, g, Wf, sinks, S, z, kcache, vcache, w: int,
-                scale: float | None = None) -> np.ndarray:
+                scale: float | None = None, gcache=None, reading: int = DELAYED) -> np.ndarray:
     """One fp64 decode step.  q [B,Hq,d]; k, v [B,Hkv,d]; g [B,Hkv,D].  S, z,
-    kcache, vcache (float64, contiguous) are updated in place.  Returns y [B,Hq,d]."""
+    kcache, vcache (float64, contiguous) are updated in place, and so is gcache
+    [B,Hkv,w+1,D], the ring of gate logits the MASKED and LAGGED readings need.
+    Returns y [B,Hq,d]."""
     lib = _load()
     q, k, v, g, Wf, sinks = map(_f64, (q, k, v, g, Wf, sinks))
-    for a in (S, z, kcache, vcache):
+    for a in (S, z, kcache, vcache) + ((gcache,) if gcache is not None else ()):
         assert a.dtype == np.float64 and a.flags.c_contiguous
     B, Hq, d = q.shape
-    p = _Dims(B, 1, Hq, k.shape[1], d, g.shape[2], w, sinks.shape[1],
+    p = _Dims(B, 1, Hq, k.shape[1], d, g.shape[2], w, sinks.shape[1], int(reading),
               float(1.0 / np.sqrt(d) if scale is None else scale))
     y = np.zeros_like(q)
     rc = lib.ora_decode_step(ctypes.byref(p), pos, _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(Wf),
-                             _ptr(sinks), _ptr(y), _ptr(S), _ptr(z), _ptr(kcache), _ptr(vcache))
+                             _ptr(sinks), _ptr(y), _ptr(S), _ptr(z), _ptr(kcache), _ptr(vcache),
+                             _ptr(gcache))
     if rc != 0:
         raise ValueError("ora_decode_step rejected its arguments")
     return y
 
 
-def bwd(q, k, v, g, Wf, sinks, dy, w: int, scale: float | None = None) -> dict:
-    """Exact fp64 gradient of fwd()["y"] against the upstream gradient dy."""
+def bwd(q, k, v, g, Wf, sinks, dy, w: int, scale: float | None = None,
+        reading: int = DELAYED) -> dict:
+    """Exact fp64 gradient of fwd()["y"] (same reading) against the upstream gradient dy."""
     lib = _load()
     q, k, v, g, Wf, sinks, dy = map(_f64, (q, k, v, g, Wf, sinks, dy))
-    p = _dims(q, k, g, sinks, w, scale)
+    p = _dims(q, k, g, sinks, w, scale, reading)
     out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v),
                dg=np.zeros_like(g), dWf=np.zeros_like(Wf), dsinks=np.zeros_like(sinks))
     rc = lib.ora_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(Wf), _ptr(sinks),

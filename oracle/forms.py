@@ -9,6 +9,9 @@ weight
 
     phi(k_j)_f * prod_{s=j+w+1..i} Gamma_{s,f},      Gamma = sigmoid(g),
 
+(the delayed-key reading; `brute_force` and `quadratic_parallel` also take the
+masked reading, product over s = j+1..i, and the lagged reading, s = j+1..i-w)
+
 and a key inside the window (i - w < j <= i) with e^{scale q_i.k_j}; the
 meta-memory scalars add sum_m e^{t_m} to the denominator only.
 
@@ -38,13 +41,26 @@ def phi(x: np.ndarray, Wf_kv: np.ndarray) -> np.ndarray:
     return np.concatenate([sm(u), sm(-u)], axis=-1)
 
 
+def gate_range(reading: int, i: int, j: int, w: int) -> tuple[int, int]:
+    """First and last s of the gate product that weighs key j <= i - w at query i:
+    0 delayed key (j+w+1 .. i), 1 masked full GLA (j+1 .. i), 2 lagged state (j+1 .. i-w).
+    An empty range (first > last) is the product 1."""
+    if reading == 0:
+        return j + w + 1, i
+    if reading == 1:
+        return j + 1, i
+    if reading == 2:
+        return j + 1, i - w
+    raise ValueError(f"unknown reading {reading}")
+
+
 def _unpack(inp):
     q, k, v, g, Wf, sinks = (np.asarray(inp[n], np.float64)
                              for n in ("q", "k", "v", "g", "Wf", "sinks"))
     return q, k, v, g, Wf, sinks
 
 
-def brute_force(inp: dict, w: int, scale: float | None = None) -> np.ndarray:
+def brute_force(inp: dict, w: int, scale: float | None = None, reading: int = 0) -> np.ndarray:
     """Output y by the weight definition, one scalar product at a time (L <= 16)."""
     q, k, v, g, Wf, sinks = _unpack(inp)
     B, L, Hq, d = q.shape
@@ -62,9 +78,10 @@ def brute_force(inp: dict, w: int, scale: float | None = None) -> np.ndarray:
                 for j in range(0, i - w + 1):
                     pk = phi(k[b, j, kv], Wf[kv])
                     a = 0.0
+                    lo, hi = gate_range(reading, i, j, w)
                     for f in range(D):
                         prod = 1.0
-                        for s in range(j + w + 1, i + 1):
+                        for s in range(lo, hi + 1):
                             prod *= 1.0 / (1.0 + math.exp(-g[b, s, kv, f]))
                         a += pq[f] * pk[f] * prod
                     for c in range(d):
@@ -85,7 +102,8 @@ def brute_force(inp: dict, w: int, scale: float | None = None) -> np.ndarray:
     return y
 
 
-def quadratic_parallel(inp: dict, w: int, scale: float | None = None) -> np.ndarray:
+def quadratic_parallel(inp: dict, w: int, scale: float | None = None,
+                       reading: int = 0) -> np.ndarray:
     """Output y from the full L x L weight matrices (gated-linear part and window part)."""
     q, k, v, g, Wf, sinks = _unpack(inp)
     B, L, Hq, d = q.shape
@@ -100,13 +118,12 @@ def quadratic_parallel(inp: dict, w: int, scale: float | None = None) -> np.ndar
     for b in range(B):
         for kv in range(Hkv):
             pk = phi(k[b, :, kv], Wf[kv])                       # [L, D]
-            # decay[i, j, f] = prod_{s=j+w+1..i} Gamma_s,f for j <= i-w
+            # decay[i, j, f] = prod_{s=lo..hi} Gamma_s,f for j <= i-w (gate_range)
             decay = np.zeros((L, L, D))
             for i in range(w, L):
-                rc = np.cumprod(gam[b, i::-1, kv], axis=0)     # rc[n] = prod_{s=i-n..i}
                 for j in range(0, i - w + 1):
-                    n = i - (j + w + 1)
-                    decay[i, j] = 1.0 if n < 0 else rc[n]
+                    lo, hi = gate_range(reading, i, j, w)
+                    decay[i, j] = np.prod(gam[b, lo:hi + 1, kv], axis=0)  # 1 when empty
             for hh in range(G):
                 h = kv * G + hh
                 pq = phi(q[b, :, h], Wf[kv])                   # [L, D]

@@ -26,6 +26,18 @@
  *        S_i = Gamma_i (.) S_{i-1} + [i >= w] phi(k_{i-w}) v_{i-w}^T,
  *        z_i = Gamma_i (.) z_{i-1} + [i >= w] phi(k_{i-w});
  *     Gamma (.) S scales row f of S by Gamma_f;
+ *   - two other readings of which gates decay a past key are kept as a switch
+ *     (dims.reading; the pages fix none of the three), as weights of a key
+ *     j <= i-w at query i and as recurrences of the state S_i that query i reads:
+ *       0 delayed key (the default):  prod_{s=j+w+1..i} Gamma_s,
+ *           S_i = Gamma_i (.) S_{i-1} + phi(k_{i-w}) v_{i-w}^T;
+ *       1 masked full GLA:            prod_{s=j+1..i} Gamma_s,
+ *           S_i = Gamma_i (.) S_{i-1} + c_{i-w} (.) phi(k_{i-w}) v_{i-w}^T,
+ *           c_j = prod_{s=j+1..j+w} Gamma_s (the gates the key saw in the window);
+ *       2 lagged state:               prod_{s=j+1..i-w} Gamma_s,
+ *           S_i = Gamma_{i-w} (.) S_{i-1} + phi(k_{i-w}) v_{i-w}^T;
+ *     S_i = 0 for i < w in all three, and z follows S with phi(k) in place of
+ *     phi(k) v^T;
  *   - one Wf and one gate row per KV head; query head h uses KV head h / G;
  *   - the sinks are per query head and enter the denominator only.
  *
@@ -43,6 +55,7 @@
 
 typedef struct {
     long B, L, Hq, Hkv, d, D, w, M;
+    long reading; /* 0 delayed key, 1 masked full GLA, 2 lagged state */
     double scale;
 } ora_dims;
 
@@ -76,6 +89,21 @@ static void ora_phi(const double *x, const double *Wf, long d, long D, double *p
 
 static double ora_sigmoid(double x) { return 1.0 / (1.0 + exp(-x)); }
 
+/* Row of the gate that decays the state at step i (-1: no decay at this step). */
+static long decay_row(const ora_dims *p, long i) {
+    if (p->reading == 2) return i >= p->w ? i - p->w : -1;
+    return i;
+}
+
+/* c_f = prod_{s=i-w+1..i} sigmoid(g_{s,f}) for the key entering at step i under the
+ * masked reading; gate row s of the unit is gates + s * stride. */
+static void window_gate_product(const double *gates, long stride, long i, long w, long D,
+                                double *c) {
+    for (long f = 0; f < D; ++f) c[f] = 1.0;
+    for (long s = i - w + 1; s <= i; ++s)
+        for (long f = 0; f < D; ++f) c[f] *= ora_sigmoid(gates[s * stride + f]);
+}
+
 static double dot(const double *a, const double *b, long n) {
     double s = 0.0;
     for (long i = 0; i < n; ++i) s += a[i] * b[i];
@@ -95,7 +123,9 @@ int ora_fwd(const ora_dims *p, const double *q, const double *k, const double *v
             double *den_out) {
     const long B = p->B, L = p->L, Hq = p->Hq, Hkv = p->Hkv, d = p->d, D = p->D, w = p->w,
                M = p->M;
-    if (Hkv <= 0 || Hq % Hkv != 0 || D % 2 != 0 || w < 1) return 1;
+    if (Hkv <= 0 || Hq % Hkv != 0 || D % 2 != 0 || w < 1 || p->reading < 0 ||
+        p->reading > 2)
+        return 1;
     const long G = Hq / Hkv;
 #pragma omp parallel for schedule(dynamic, 1)
     for (long unit = 0; unit < B * Hkv; ++unit) {
@@ -105,12 +135,15 @@ int ora_fwd(const ora_dims *p, const double *q, const double *k, const double *v
         double *z = (double *)calloc((size_t)D, sizeof(double));
         double *phk = (double *)malloc(sizeof(double) * D);
         double *phq = (double *)malloc(sizeof(double) * D);
+        double *cf = (double *)malloc(sizeof(double) * D);
         double *num = (double *)malloc(sizeof(double) * d);
+        const double *gu = g + (b * L * Hkv + kv) * D; /* gate row s: gu + s * Hkv * D */
         for (long i = 0; i < L; ++i) {
-            const double *gi = g + ((b * L + i) * Hkv + kv) * D;
-            /* decay by Gamma_i = sigmoid(g_i), then admit the key leaving the window */
-            for (long f = 0; f < D; ++f) {
-                double gam = ora_sigmoid(gi[f]);
+            /* decay by the reading's gate (Gamma_i, or Gamma_{i-w} for the lagged state),
+             * then admit the key leaving the window */
+            const long gr = decay_row(p, i);
+            for (long f = 0; gr >= 0 && f < D; ++f) {
+                double gam = ora_sigmoid(gu[gr * Hkv * D + f]);
                 for (long c = 0; c < d; ++c) S[f * d + c] *= gam;
                 z[f] *= gam;
             }
@@ -118,6 +151,10 @@ int ora_fwd(const ora_dims *p, const double *q, const double *k, const double *v
                 const double *kx = k + ((b * L + (i - w)) * Hkv + kv) * d;
                 const double *vx = v + ((b * L + (i - w)) * Hkv + kv) * d;
                 ora_phi(kx, Wk, d, D, phk, NULL);
+                if (p->reading == 1) {
+                    window_gate_product(gu, Hkv * D, i, w, D, cf);
+                    for (long f = 0; f < D; ++f) phk[f] *= cf[f];
+                }
                 for (long f = 0; f < D; ++f) {
                     for (long c = 0; c < d; ++c) S[f * d + c] += phk[f] * vx[c];
                     z[f] += phk[f];
@@ -163,6 +200,7 @@ int ora_fwd(const ora_dims *p, const double *q, const double *k, const double *v
         free(z);
         free(phk);
         free(phq);
+        free(cf);
         free(num);
     }
     return 0;
@@ -172,12 +210,16 @@ int ora_fwd(const ora_dims *p, const double *q, const double *k, const double *v
  * constant-memory inference).  q [B,Hq,d]; k, v [B,Hkv,d]; g [B,Hkv,D] hold the
  * new token.  S [B,Hkv,D,d] and z [B,Hkv,D] hold the state after token pos-1 and
  * are updated in place.  kc, vc [B,Hkv,w+1,d] are ring caches: token t lives in
- * slot t mod (w+1); the new token is written to its slot.  y [B,Hq,d]. */
+ * slot t mod (w+1); the new token is written to its slot.  y [B,Hq,d].
+ * gc [B,Hkv,w+1,D] is the same ring for the gate logits, which the masked and lagged
+ * readings need (they decay or weigh with gates of tokens already in the window); it
+ * may be NULL under the delayed-key reading. */
 int ora_decode_step(const ora_dims *p, long pos, const double *q, const double *k,
                     const double *v, const double *g, const double *Wf, const double *sinks,
-                    double *y, double *S, double *z, double *kc, double *vc) {
+                    double *y, double *S, double *z, double *kc, double *vc, double *gc) {
     const long B = p->B, Hq = p->Hq, Hkv = p->Hkv, d = p->d, D = p->D, w = p->w, M = p->M;
     if (Hkv <= 0 || Hq % Hkv != 0 || D % 2 != 0 || w < 1 || pos < 0) return 1;
+    if (p->reading < 0 || p->reading > 2 || (p->reading != 0 && gc == NULL)) return 1;
     const long G = Hq / Hkv, R = w + 1;
 #pragma omp parallel for schedule(dynamic, 1)
     for (long unit = 0; unit < B * Hkv; ++unit) {
@@ -185,18 +227,27 @@ int ora_decode_step(const ora_dims *p, long pos, const double *q, const double *
         const double *Wk = Wf + kv * d * (D / 2);
         double *Su = S + unit * D * d, *zu = z + unit * D;
         double *kcu = kc + unit * R * d, *vcu = vc + unit * R * d;
+        double *gcu = gc ? gc + unit * R * D : NULL;
         const double *gi = g + unit * D;
         double *phk = (double *)malloc(sizeof(double) * D);
         double *phq = (double *)malloc(sizeof(double) * D);
         double *num = (double *)malloc(sizeof(double) * d);
-        for (long f = 0; f < D; ++f) {
-            double gam = ora_sigmoid(gi[f]);
+        /* the gate of this step: Gamma_pos, or Gamma_{pos-w} from the ring (lagged state) */
+        const double *gd = gi;
+        if (p->reading == 2) gd = pos >= w ? gcu + ((pos - w) % R) * D : NULL;
+        for (long f = 0; gd != NULL && f < D; ++f) {
+            double gam = ora_sigmoid(gd[f]);
             for (long c = 0; c < d; ++c) Su[f * d + c] *= gam;
             zu[f] *= gam;
         }
         if (pos >= w) {
             const long slot = (pos - w) % R;
             ora_phi(kcu + slot * d, Wk, d, D, phk, NULL);
+            if (p->reading == 1) /* c = prod of the gates of tokens pos-w+1 .. pos */
+                for (long s = pos - w + 1; s <= pos; ++s) {
+                    const double *gs = s == pos ? gi : gcu + (s % R) * D;
+                    for (long f = 0; f < D; ++f) phk[f] *= ora_sigmoid(gs[f]);
+                }
             for (long f = 0; f < D; ++f) {
                 for (long c = 0; c < d; ++c) Su[f * d + c] += phk[f] * vcu[slot * d + c];
                 zu[f] += phk[f];
@@ -205,6 +256,7 @@ int ora_decode_step(const ora_dims *p, long pos, const double *q, const double *
         /* the new token joins the ring before the window is read */
         memcpy(kcu + (pos % R) * d, k + unit * d, sizeof(double) * d);
         memcpy(vcu + (pos % R) * d, v + unit * d, sizeof(double) * d);
+        if (gcu) memcpy(gcu + (pos % R) * D, gi, sizeof(double) * D);
         for (long hh = 0; hh < G; ++hh) {
             const long h = kv * G + hh;
             const double *qi = q + (b * Hq + h) * d;
@@ -254,6 +306,32 @@ static void ora_phi_bwd(const double *x, const double *Wk, long d, long D, const
     free(du);
 }
 
+/* Transition of step i on one unit's augmented state [S | z] (D x (d+1)), under the
+ * dims' reading: cur = gamma (.) prev + [i >= w] a (.) phi(k_{i-w}) [v_{i-w} | 1], with gamma
+ * the gate of decay_row(i) (1 when there is none) and a = c_{i-w} (masked reading) or 1.
+ * gu: gate row 0 of the unit (row s at gu + s * gstride); kx, vx: key and value i-w.
+ * cur may be prev.  phk, cf: scratch [D]. */
+static void ora_transition(const ora_dims *p, const double *gu, long gstride, const double *kx,
+                           const double *vx, const double *Wk, long i, const double *prev,
+                           double *cur, double *phk, double *cf) {
+    const long d = p->d, D = p->D, w = p->w, E = d + 1;
+    const long gr = decay_row(p, i);
+    for (long f = 0; f < D; ++f) {
+        double gam = gr >= 0 ? ora_sigmoid(gu[gr * gstride + f]) : 1.0;
+        for (long c = 0; c < E; ++c) cur[f * E + c] = gam * prev[f * E + c];
+    }
+    if (i < w) return;
+    ora_phi(kx, Wk, d, D, phk, NULL);
+    if (p->reading == 1) {
+        window_gate_product(gu, gstride, i, w, D, cf);
+        for (long f = 0; f < D; ++f) phk[f] *= cf[f];
+    }
+    for (long f = 0; f < D; ++f) {
+        for (long c = 0; c < d; ++c) cur[f * E + c] += phk[f] * vx[c];
+        cur[f * E + d] += phk[f];
+    }
+}
+
 /* Exact gradient of ora_fwd (the pages give no backward; this is the adjoint of
  * the same recurrence).  The augmented state [S | z] (D x (d+1)) is checkpointed
  * every 64 tokens and recomputed one block at a time in the reverse sweep.
@@ -264,7 +342,9 @@ int ora_bwd(const ora_dims *p, const double *q, const double *k, const double *v
             double *dq, double *dk, double *dv, double *dg, double *dWf, double *dsinks) {
     const long B = p->B, L = p->L, Hq = p->Hq, Hkv = p->Hkv, d = p->d, D = p->D, w = p->w,
                M = p->M;
-    if (Hkv <= 0 || Hq % Hkv != 0 || D % 2 != 0 || w < 1) return 1;
+    if (Hkv <= 0 || Hq % Hkv != 0 || D % 2 != 0 || w < 1 || p->reading < 0 ||
+        p->reading > 2)
+        return 1;
     const long G = Hq / Hkv, E = d + 1, CK = 64;
     const long nblk = (L + CK - 1) / CK;
     const long wsz = d * (D / 2);
@@ -286,21 +366,13 @@ int ora_bwd(const ora_dims *p, const double *q, const double *k, const double *v
         double *ck = (double *)calloc((size_t)(nblk * D * E), sizeof(double));
         double *St = (double *)calloc((size_t)(D * E), sizeof(double));
         double *phk = (double *)malloc(sizeof(double) * D);
+        double *cf = (double *)malloc(sizeof(double) * D);
+        const double *gu = g + GIDX(0);
+        const long gs = Hkv * D;
         for (long i = 0; i < L; ++i) {
             if (i % CK == 0) memcpy(ck + (i / CK) * D * E, St, sizeof(double) * D * E);
-            const double *gi = g + GIDX(i);
-            for (long f = 0; f < D; ++f) {
-                double gam = ora_sigmoid(gi[f]);
-                for (long c = 0; c < E; ++c) St[f * E + c] *= gam;
-            }
-            if (i >= w) {
-                ora_phi(k + KIDX(i - w), Wk, d, D, phk, NULL);
-                const double *vx = v + KIDX(i - w);
-                for (long f = 0; f < D; ++f) {
-                    for (long c = 0; c < d; ++c) St[f * E + c] += phk[f] * vx[c];
-                    St[f * E + d] += phk[f];
-                }
-            }
+            const long j = i >= w ? i - w : 0;
+            ora_transition(p, gu, gs, k + KIDX(j), v + KIDX(j), Wk, i, St, St, phk, cf);
         }
         /* reverse sweep; Gb = gradient w.r.t. the augmented state after token i */
         double *Gb = (double *)calloc((size_t)(D * E), sizeof(double));
@@ -316,23 +388,11 @@ int ora_bwd(const ora_dims *p, const double *q, const double *k, const double *v
             memcpy(blk, ck + bi * D * E, sizeof(double) * D * E);
             for (long i = i0; i < i1; ++i) {
                 double *prev = blk + (i - i0) * D * E, *cur = prev + D * E;
-                const double *gi = g + GIDX(i);
-                for (long f = 0; f < D; ++f) {
-                    double gam = ora_sigmoid(gi[f]);
-                    for (long c = 0; c < E; ++c) cur[f * E + c] = gam * prev[f * E + c];
-                }
-                if (i >= w) {
-                    ora_phi(k + KIDX(i - w), Wk, d, D, phk, NULL);
-                    const double *vx = v + KIDX(i - w);
-                    for (long f = 0; f < D; ++f) {
-                        for (long c = 0; c < d; ++c) cur[f * E + c] += phk[f] * vx[c];
-                        cur[f * E + d] += phk[f];
-                    }
-                }
+                const long j = i >= w ? i - w : 0;
+                ora_transition(p, gu, gs, k + KIDX(j), v + KIDX(j), Wk, i, prev, cur, phk, cf);
             }
             for (long i = i1 - 1; i >= i0; --i) {
                 const double *prev = blk + (i - i0) * D * E, *cur = prev + D * E;
-                const double *gi = g + GIDX(i);
                 /* outputs of token i */
                 for (long hh = 0; hh < G; ++hh) {
                     const long h = kv * G + hh;
@@ -387,31 +447,49 @@ int ora_bwd(const ora_dims *p, const double *q, const double *k, const double *v
                     }
                     ora_phi_bwd(qi, Wk, d, D, dph, dqi, dWk);
                 }
-                /* state update of token i: cur = Gamma (.) prev + [i>=w] phi(k_{i-w}) [v | 1] */
-                double *dgi = dg + GIDX(i);
-                for (long f = 0; f < D; ++f) {
-                    double gam = ora_sigmoid(gi[f]);
-                    double s = 0.0;
-                    for (long c = 0; c < E; ++c) s += Gb[f * E + c] * prev[f * E + c];
-                    dgi[f] = s * gam * (1.0 - gam);
+                /* state update of token i: cur = gamma (.) prev + [i>=w] a (.) phi(k_{i-w}) [v | 1]
+                 * (ora_transition); gamma's gate row gets dgamma gamma (1 - gamma) */
+                const long gr = decay_row(p, i);
+                if (gr >= 0) {
+                    const double *gg = g + GIDX(gr);
+                    double *dgr = dg + GIDX(gr);
+                    for (long f = 0; f < D; ++f) {
+                        double gam = ora_sigmoid(gg[f]);
+                        double s = 0.0;
+                        for (long c = 0; c < E; ++c) s += Gb[f * E + c] * prev[f * E + c];
+                        dgr[f] += s * gam * (1.0 - gam);
+                    }
                 }
                 if (i >= w) {
                     const double *kx = k + KIDX(i - w), *vx = v + KIDX(i - w);
                     double *dvx = dv + KIDX(i - w), *dkx = dk + KIDX(i - w);
                     ora_phi(kx, Wk, d, D, phk, NULL);
+                    for (long f = 0; f < D; ++f) cf[f] = 1.0;
+                    if (p->reading == 1) window_gate_product(gu, gs, i, w, D, cf);
                     for (long f = 0; f < D; ++f) {
+                        /* s = d/d(a phi_f); the value sees a phi_f */
                         double s = Gb[f * E + d];
                         for (long c = 0; c < d; ++c) {
                             s += Gb[f * E + c] * vx[c];
-                            dvx[c] += Gb[f * E + c] * phk[f];
+                            dvx[c] += Gb[f * E + c] * cf[f] * phk[f];
                         }
-                        dph[f] = s;
+                        dph[f] = cf[f] * s;
+                        /* masked reading: a_f = prod_{u=i-w+1..i} Gamma_u, so each of those
+                         * gates gets (a phi_f s) (1 - Gamma_u) */
+                        if (p->reading == 1) {
+                            const double da = cf[f] * phk[f] * s;
+                            for (long u = i - w + 1; u <= i; ++u)
+                                dg[GIDX(u) + f] += da * (1.0 - ora_sigmoid(g[GIDX(u) + f]));
+                        }
                     }
                     ora_phi_bwd(kx, Wk, d, D, dph, dkx, dWk);
                 }
-                for (long f = 0; f < D; ++f) {
-                    double gam = ora_sigmoid(gi[f]);
-                    for (long c = 0; c < E; ++c) Gb[f * E + c] *= gam;
+                if (gr >= 0) {
+                    const double *gg = g + GIDX(gr);
+                    for (long f = 0; f < D; ++f) {
+                        double gam = ora_sigmoid(gg[f]);
+                        for (long c = 0; c < E; ++c) Gb[f * E + c] *= gam;
+                    }
                 }
             }
         }
@@ -420,6 +498,7 @@ int ora_bwd(const ora_dims *p, const double *q, const double *k, const double *v
         free(ck);
         free(St);
         free(phk);
+        free(cf);
         free(Gb);
         free(blk);
         free(phq);
