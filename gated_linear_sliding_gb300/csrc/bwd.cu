@@ -36,7 +36,9 @@ constexpr int KB = 16;  // window keys per tile in the query-side walk
 
 // Workspace regions (floats, each 64-float aligned)
 struct BwdWs {
-    size_t fwd_rec, rev_rec, dB, tot, dW, dt, rows, flags, total;
+    size_t fwd_rec, rev_rec, dB, tot, dW, dt, rows, flags;
+    size_t gl, kd, kk;  // decay readings: moved gates (LAGGED); key log products and gate terms (MASKED)
+    size_t total;
 };
 
 inline size_t al64(size_t x) { return (x + 63) & ~(size_t)63; }
@@ -61,6 +63,13 @@ BwdWs bwd_layout(const Plan& p) {
     off += al64((size_t)2 * (size_t)(p.B * p.L * p.Hq));
     w.flags = off;  // per (segment, unit): 1 if its gates close too hard for the factored walks
     off += al64((size_t)p.Pmax * U);
+    const size_t ng = (size_t)(p.B * p.L * p.Hkv) * (size_t)p.D;
+    w.gl = off;  // LAGGED: g moved w tokens later, in the input's dtype
+    if (p.decay == LIZARD_DECAY_LAGGED) off += al64((ng * (p.dtype == LIZARD_F32 ? 4 : 2) + 3) / 4);
+    w.kd = off;  // MASKED: log product of the w gates after each key
+    if (p.decay == LIZARD_DECAY_MASKED) off += al64(ng);
+    w.kk = off;  // MASKED: phi(k') (.) dphi(k') of each key, at the key's own row
+    if (p.decay == LIZARD_DECAY_MASKED) off += al64(ng);
     w.total = off * sizeof(float);
     return w;
 }
@@ -392,6 +401,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_forward_walk(Plan p, BwdArgs a, Bwd
         __syncthreads();
         phi_rows_p<DH, DF, FAST>(sq, sW, sphk, rlo, n);
         __syncthreads();
+        if (a.kdec != nullptr) {  // masked reading: the keys enter scaled by their gate products
+            simt::scale_entering_keys<DF, TS, NT, FAST>(sphk, a.kdec, b, p.L, p.Hkv, kv, i0 - p.w,
+                                                        rlo, n);
+            __syncthreads();
+        }
         for (int hh = 0; hh < p.G; ++hh) {
             const int64_t h = kv * p.G + hh;
             load_rows_p<T, DH>((const T*)a.q, b, p.L, p.Hq, h, i0, 0, n, sq);
@@ -656,6 +670,11 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
         __syncthreads();
         phi_rows_p<DH, DF, FAST>(sq, sW, sphk, rlo, n);
         __syncthreads();
+        if (a.kdec != nullptr) {  // masked reading: sphk holds c (.) phi(k'), the entering value
+            simt::scale_entering_keys<DF, TS, NT, FAST>(sphk, a.kdec, b, p.L, p.Hkv, kv, i0 - p.w,
+                                                        rlo, n);
+            __syncthreads();
+        }
         // terms through the step's end: dphk_t = e^{bl - b_t} (.) (dH v'_t + dz),
         // dv'_t = sum_f e^{bl_f - b_tf} phk_tf dH[f][.]   (row t = r, in registers)
         float dk_acc[NF], dv_acc[NC];
@@ -745,13 +764,33 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
         for (int j = 0; j < NF; ++j)
             sdp[r * PF + cs + LPR * j] = (r >= rlo && r < n) ? dk_acc[j] : 0.0f;
         __syncthreads();
-        // dB = (phi(q)-side, from the forward walk) - phk (.) dphk; reverse cumsum in place
+        // dB = (phi(q)-side, from the forward walk) - phk (.) dphk; reverse cumsum in place.
+        // Masked reading: the key's term belongs to its own row t - w (its factor
+        // e^{-b} is taken at the key's position), so it goes to the separate array kkey, and
+        // phi's backward takes the unscaled map with dphi = c (.) dphi(c phi).
         if (tid < DF) {
             const int f = tid;
             for (int t = n - 1; t >= 0; --t) {
                 float* src = wsf + ws.dB + ((b * p.L + i0 + t) * p.Hkv + kv) * DF + f;
-                carry += *src - sphk[t * PF + f] * sdp[t * PF + f];
+                carry += a.kkey != nullptr ? *src : *src - sphk[t * PF + f] * sdp[t * PF + f];
                 *src = carry;
+            }
+        }
+        if (a.kkey != nullptr) {
+            for (int e = tid; e < TS * DF; e += NT) {
+                const int t = e / DF, f = e % DF;
+                if (t >= rlo && t < n)
+                    a.kkey[((b * p.L + i0 + t - p.w) * p.Hkv + kv) * DF + f] =
+                        sphk[t * PF + f] * sdp[t * PF + f];
+            }
+            __syncthreads();
+            load_rows_p<T, DH>((const T*)a.k, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n, sq);
+            __syncthreads();
+            phi_rows_p<DH, DF, FAST>(sq, sW, sphk, rlo, n);
+            for (int e = tid; e < TS * DF; e += NT) {
+                const int t = e / DF, f = e % DF;
+                if (t >= rlo && t < n)
+                    sdp[t * PF + f] *= ex<FAST>(a.kdec[((b * p.L + i0 + t - p.w) * p.Hkv + kv) * DF + f]);
             }
         }
         __syncthreads();
@@ -927,7 +966,10 @@ __global__ void __launch_bounds__(NT) bwd_window_keys(Plan p, BwdArgs a, BwdWs w
 }
 
 // dg = (sum_{s >= u} dB_s) (1 - sigmoid(g_u)); the in-segment sums are in the scratch,
-// later segments add their totals.
+// later segments add their totals.  Decay readings: the lagged one ran every kernel on the
+// gates moved w tokens later, so gate j takes the adjoint of moved row j + w (and the gates
+// of the last w tokens, never used, get 0); the masked one subtracts the suffix sums of the
+// key-side terms kept at the keys' own rows.
 template <typename T>
 __global__ void bwd_gates(Plan p, BwdArgs a, BwdWs ws) {
     // eight consecutive features of one (batch, token, KV head) row per thread
@@ -935,25 +977,42 @@ __global__ void bwd_gates(Plan p, BwdArgs a, BwdWs ws) {
     const int64_t e8 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (e8 >= total8) return;
     const int64_t e = e8 * 8;
-    const int64_t rowi = e / p.D;                   // (b L + i) Hkv + kv
-    const int f0 = (int)(e - rowi * p.D);
-    const int64_t kv = rowi % p.Hkv, bi = rowi / p.Hkv;
-    const int64_t i = bi % p.L, b = bi / p.L;
+    const int64_t rowj = e / p.D;                   // (b L + j) Hkv + kv: the gate written
+    const int f0 = (int)(e - rowj * p.D);
+    const int64_t kv = rowj % p.Hkv, bj = rowj / p.Hkv;
+    const int64_t j = bj % p.L, b = bj / p.L;
+    const int64_t i = j + a.glag;                   // the row of the adjoint it takes
+    if (i >= p.L) {
+        if constexpr (sizeof(T) == 2)
+            *reinterpret_cast<uint4*>((__nv_bfloat16*)a.dg + e) = make_uint4(0u, 0u, 0u, 0u);
+        else
+#pragma unroll
+            for (int k = 0; k < 8; ++k) st((T*)a.dg + e + k, 0.0f);
+        return;
+    }
+    const int64_t ei = e + a.glag * p.Hkv * p.D;
     const int64_t seg = i / p.seg_len;
     const int64_t U = p.B * p.Hkv, unit = b * p.Hkv + kv;
     const float* wsf = (const float*)a.ws;
     // tot holds, per segment, the sum of dB over all later segments (bwd_tot_suffix)
     const float* tot = wsf + ws.tot + ((size_t)seg * U + unit) * p.D + f0;
-    const float4 d0 = *reinterpret_cast<const float4*>(wsf + ws.dB + e);
-    const float4 d1 = *reinterpret_cast<const float4*>(wsf + ws.dB + e + 4);
+    const float4 d0 = *reinterpret_cast<const float4*>(wsf + ws.dB + ei);
+    const float4 d1 = *reinterpret_cast<const float4*>(wsf + ws.dB + ei + 4);
     const float4 t0 = *reinterpret_cast<const float4*>(tot);
     const float4 t1 = *reinterpret_cast<const float4*>(tot + 4);
-    const float dv[8] = {d0.x + t0.x, d0.y + t0.y, d0.z + t0.z, d0.w + t0.w,
-                         d1.x + t1.x, d1.y + t1.y, d1.z + t1.z, d1.w + t1.w};
+    float dv[8] = {d0.x + t0.x, d0.y + t0.y, d0.z + t0.z, d0.w + t0.w,
+                   d1.x + t1.x, d1.y + t1.y, d1.z + t1.z, d1.w + t1.w};
+    if (a.kkey != nullptr) {
+        const float4 k0 = *reinterpret_cast<const float4*>(a.kkey + e);
+        const float4 k1 = *reinterpret_cast<const float4*>(a.kkey + e + 4);
+        const float kv8[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+        for (int k = 0; k < 8; ++k) dv[k] -= kv8[k];
+    }
     if constexpr (sizeof(T) == 2) {
         // d log sigmoid(g)/dg = 1 - sigmoid(g) = 1 / (1 + e^g), which keeps its relative
         // precision for large g; eight gates in one 16-byte load
-        const uint4 gw = *reinterpret_cast<const uint4*>((const __nv_bfloat16*)a.g + e);
+        const uint4 gw = *reinterpret_cast<const uint4*>((const __nv_bfloat16*)a.g + ei);
         const uint32_t w[4] = {gw.x, gw.y, gw.z, gw.w};
         uint32_t o[4];
 #pragma unroll
@@ -967,7 +1026,7 @@ __global__ void bwd_gates(Plan p, BwdArgs a, BwdWs ws) {
     } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            st((T*)a.dg + e + k, dv[k] / (1.0f + expf(ld((const T*)a.g + e + k))));
+            st((T*)a.dg + e + k, dv[k] / (1.0f + expf(ld((const T*)a.g + ei + k))));
     }
 }
 
@@ -1011,9 +1070,10 @@ __global__ void bwd_reduce(Plan p, BwdArgs a, BwdWs ws) {
 }
 
 template <typename T, int DH, int DF, bool FAST>
-cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
+cudaError_t bwd_impl(const Plan& p, const BwdArgs& a_in, cudaStream_t s) {
     using Ly = BLay<DH, DF>;
     const BwdWs ws = bwd_layout(p);
+    BwdArgs a = a_in;
     const size_t smem = Ly::bytes;
     cudaError_t e;
     e = cudaFuncSetAttribute(bwd_forward_walk<T, DH, DF, FAST>,
@@ -1032,6 +1092,19 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
     const unsigned U = (unsigned)(p.B * p.Hkv);
     float* wsf = (float*)a.ws;
+    // decay readings: every kernel below reads the moved gates (LAGGED), or the SIMT walks
+    // scale the entering keys and keep their gate terms apart (MASKED)
+    if (p.decay == LIZARD_DECAY_LAGGED) {
+        e = launch_gate_lag(p, a.g, wsf + ws.gl, s);
+        if (e != cudaSuccess) return e;
+        a.g = wsf + ws.gl;
+        a.glag = p.w;
+    } else if (p.decay == LIZARD_DECAY_MASKED) {
+        e = launch_key_decay(p, a.g, wsf + ws.kd, s);
+        if (e != cudaSuccess) return e;
+        a.kdec = wsf + ws.kd;
+        a.kkey = wsf + ws.kk;
+    }
     // 0. per-row a = e^{-lse} and delta = dy . y
     {
         const int64_t nrow = p.B * p.L * p.Hq;
@@ -1051,12 +1124,14 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
         fa.sinks = a.sinks;
         fa.seg = wsf + ws.fwd_rec;
         fa.header = a.ws;
+        fa.kdec = a.kdec;
         e = fwd_tc_supported(p) ? launch_fwd_states_tc(p, fa, s) : launch_fwd_states(p, fa, s);
         if (e != cudaSuccess) return e;
     }
     // 2. forward-direction walk.  The tensor-core walks leave the segments whose gates close
     //    too hard for their factored decays to the exact SIMT walks (flags from one pass over g)
-    const bool tc_walks = a.win_tc && bwd_rev_local_tc_supported(p);
+    const bool tc_walks =
+        a.win_tc && bwd_rev_local_tc_supported(p) && p.decay != LIZARD_DECAY_MASKED;
     int* flags = (int*)(wsf + ws.flags);
     if (tc_walks) {
         if constexpr (sizeof(T) == 2 && DF == 128)
@@ -1100,6 +1175,10 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a, cudaStream_t s) {
     }
     // 6. dg, then the reductions
     const int64_t ng = p.B * p.L * p.Hkv * p.D;
+    if (a.kkey != nullptr) {
+        e = launch_key_suffix(p, a.kkey, s);
+        if (e != cudaSuccess) return e;
+    }
     bwd_tot_suffix<<<(unsigned)((U * p.D + 255) / 256), 256, 0, s>>>(p, wsf + ws.tot);
     bwd_gates<T><<<(unsigned)((ng / 8 + 255) / 256), 256, 0, s>>>(p, a, ws);
     const int64_t nr = max64(p.Hkv * p.d * (p.D / 2), p.Hq * p.M);

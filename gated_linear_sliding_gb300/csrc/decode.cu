@@ -233,6 +233,12 @@ __global__ void __launch_bounds__(NT) decode_kernel(Plan p, DecodeArgs a) {
         }
     }
     __syncthreads();
+    // masked decay reading: the admitted key enters scaled by the product of the gates of
+    // tokens pos - w + 1 .. pos (its log, per feature, from the gate-ring step)
+    if (a.kdec != nullptr && admit) {
+        for (int f = tid; f < DF; f += NT) sPhi[G * DF + f] *= expf(a.kdec[unit * DF + f]);
+        __syncthreads();
+    }
 
     // 4. state update (rows [rg RPT, rg RPT + RPT) of column c) and partial readouts phi(q).S
     const float ve = admit ? ld(sVE + c) : 0.0f;
@@ -993,6 +999,7 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
 // The streaming step takes the LLaMA-3-8B-shaped heads when every buffer it copies is 16-byte
 // aligned and the tensor maps encode; otherwise the one-CTA-per-unit kernel runs.
 bool decode_stream_plan(const Plan& p, const DecodeArgs& a, StreamMaps* mp) {
+    if (a.kdec != nullptr) return false;  // the masked reading's key factors: SIMT kernel
     if (!(p.dtype == LIZARD_BF16 && p.d == 128 && p.D == 128 && p.G >= 1 && p.G <= SG &&
           p.w >= 1 && p.w <= SW && p.M <= 64 && p.B * p.Hkv * (p.w + 1) < (int64_t)1 << 31 &&
           p.B * p.Hkv * 128 < (int64_t)1 << 31 && p.B * p.Hq < (int64_t)1 << 31))
@@ -1062,7 +1069,18 @@ cudaError_t dispatch(const Plan& p, const DecodeArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-cudaError_t launch_decode(const Plan& p, const DecodeArgs& a, cudaStream_t s) {
+cudaError_t launch_decode(const Plan& p, const DecodeArgs& a_in, cudaStream_t s) {
+    DecodeArgs a = a_in;
+    if (p.decay != LIZARD_DECAY_DELAYED) {
+        // the gate-ring step: the lagged reading's decay gates (then the step runs as the
+        // delayed one on them) or the masked reading's key factors, after the status word
+        if (a.gc == nullptr) return cudaErrorInvalidValue;
+        void* out = (char*)a.header + kHeaderBytes;
+        const cudaError_t e = launch_decode_ring(p, a, out, s);
+        if (e != cudaSuccess) return e;
+        if (p.decay == LIZARD_DECAY_LAGGED) a.g = out;
+        else a.kdec = (const float*)out;
+    }
     StreamMaps mp;
     if (decode_stream_plan(p, a, &mp)) return launch_decode_stream(p, a, mp, s);
     if (p.dtype == LIZARD_F32) return dispatch<float>(p, a, s);

@@ -52,6 +52,10 @@ __global__ void __launch_bounds__(NT, 1) fwd_simt_seglocal(Plan p, FwdArgs a) {
         phi_rows<DH, DF, FAST>(sq, sW, sphk, rlo, n);
         if (threadIdx.x < DF) lam_tot += sb[(TS - 1) * Ly::PF + threadIdx.x];
         __syncthreads();
+        if (a.kdec != nullptr) {  // masked reading
+            scale_entering_keys<DF, TS, NT, FAST>(sphk, a.kdec, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n);
+            __syncthreads();
+        }
         state_update<DH, DF, FAST>(sH, sz, sphk, sv, sb);
     }
     float* rec = a.seg + ((size_t)seg * (size_t)(p.B * p.Hkv) + (size_t)unit) * p.rec_floats;
@@ -136,6 +140,10 @@ __device__ __forceinline__ void walk_head(const Plan& p, const FwdArgs& a, int64
         __syncthreads();
         phi_rows<DH, DF, FAST>(sq, sW, sphk, rlo, n);
         __syncthreads();
+        if (a.kdec != nullptr) {  // masked reading
+            scale_entering_keys<DF, TS, NT, FAST>(sphk, a.kdec, b, p.L, p.Hkv, kv, i0 - p.w, rlo, n);
+            __syncthreads();
+        }
         load_rows<T, DH>(q, b, p.L, p.Hq, h, i0, 0, n, sq, PH);
         __syncthreads();
         phi_rows<DH, DF, FAST>(sq, sW, sphq, 0, n);
@@ -306,6 +314,7 @@ __global__ void __launch_bounds__(NT, 1) fwd_simt_tail(Plan p, FwdArgs a) {
     as.k = (const T*)a.k + r0 * p.Hkv * DH;
     as.v = (const T*)a.v + r0 * p.Hkv * DH;
     as.g = (const T*)a.g + r0 * p.Hkv * DF;
+    as.kdec = a.kdec != nullptr ? a.kdec + r0 * p.Hkv * DF : nullptr;
     as.y = (T*)a.y + r0 * p.Hq * DH;
     as.lse = a.lse != nullptr ? a.lse + r0 * p.Hq : nullptr;
     as.S_out = a.S_out != nullptr ? a.S_out + b * p.Hkv * DF * DH : nullptr;

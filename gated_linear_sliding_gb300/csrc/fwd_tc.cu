@@ -1299,10 +1299,12 @@ bool make_wf_map(CUtensorMap* mw, const void* Wf, int64_t Hkv) {
 
 }  // namespace
 
+// The masked decay reading scales each entering key's phi by its own gate product, which
+// only the SIMT walks apply.
 bool fwd_tc_supported(const Plan& p) {
     return p.dtype == LIZARD_BF16 && p.d == DH && p.D == DF && p.G == GQ && p.w == WIN &&
            p.M <= MMAX && p.L < ((int64_t)1 << 30) && p.T < ((int64_t)1 << 30) &&
-           encode_fn() != nullptr;
+           p.decay != LIZARD_DECAY_MASKED && encode_fn() != nullptr;
 }
 
 cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s) {

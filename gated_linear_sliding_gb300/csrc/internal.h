@@ -28,6 +28,7 @@ struct Plan {
     // [cu[b], cu[b+1]) of arrays with T rows in all, and L is the longest sequence.
     const int64_t* cu = nullptr;
     int64_t T = 0;
+    int decay = LIZARD_DECAY_DELAYED;  // lizard_decay: which gates weigh a key past the window
 };
 // Row of sequence b's first token and the sequence's length (dense batch: b L and L).
 __host__ __device__ __forceinline__ int64_t seq_row0(const Plan& p, int64_t b) {
@@ -70,7 +71,28 @@ struct FwdArgs {
     float* seg;   // (Pmax, B*Hkv, rec_floats) segment records
     void* header;
     cudaEvent_t ev_before, ev_after;  // optional: bracket the dominant kernel
+    // MASKED and LAGGED readings: reading_scratch_bytes(p) bytes, 256-byte aligned, that
+    // fwd_launch fills (the moved gates, or the keys' log gate products)
+    void* rscratch = nullptr;
+    // MASKED reading: [rows, Hkv, D] log of the product of the w gates after each key (the
+    // SIMT walks scale the key's phi by its exponential as it enters the state); else null
+    const float* kdec = nullptr;
 };
+
+// Reading scratch of a forward (0 for DELAYED): LAGGED moves the gate logits w tokens later
+// (one dtype value per gate element), MASKED keeps the keys' log gate products (one fp32).
+size_t reading_scratch_bytes(const Plan& p);
+// g' = g moved w tokens later in each sequence (rows before w: an open gate, which only
+// decays the empty state); out has the layout of g.
+cudaError_t launch_gate_lag(const Plan& p, const void* g, void* out, cudaStream_t s);
+// kd[j] = sum_{s=j+1..min(j+w, len-1)} log sigmoid(g_s) per (row, KV head, feature).
+cudaError_t launch_key_decay(const Plan& p, const void* g, float* kd, cudaStream_t s);
+// Gate ring of a prefill: the last min(L, w) tokens' gate rows to slot t mod (w+1).
+cudaError_t launch_gate_ring_fill(const Plan& p, const void* g, void* gc, cudaStream_t s);
+// Reverse cumulative sum over the rows of each (batch, KV head, feature) column of the
+// MASKED backward's key-side gate terms, in place; rows past L - 1 - w (keys that never
+// enter the state, not written by the walk) count as zero.
+cudaError_t launch_key_suffix(const Plan& p, float* kk, cudaStream_t s);
 
 cudaError_t launch_fwd_simt(const Plan& p, const FwdArgs& a, cudaStream_t s);
 // Segment-start states only (segment pass + scan into a.seg), for the backward.
@@ -99,8 +121,16 @@ struct DecodeArgs {
     float *S, *z;
     void *kc, *vc;
     void* header;
+    void* gc = nullptr;           // gate-logit ring (MASKED and LAGGED readings)
+    const float* kdec = nullptr;  // MASKED: log factor of the admitted key [B, Hkv, D]
 };
+// Bytes after the status word of a decode workspace (the reading's per-step values).
+size_t decode_scratch_bytes(const Plan& p);
+// The decode step; for MASKED and LAGGED first the gate-ring step (the step's decay gates
+// or the admitted key's factors into the workspace after the status word, the new gate row
+// into the ring).
 cudaError_t launch_decode(const Plan& p, const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_ring(const Plan& p, const DecodeArgs& a, void* out, cudaStream_t s);
 
 struct BwdArgs {
     const void *q, *k, *v, *g, *Wf;
@@ -114,6 +144,11 @@ struct BwdArgs {
     size_t ws_bytes;
     cudaEvent_t ev_before, ev_after;
     int win_tc;  // window parts of dq, dk, dv on the tensor cores (set by launch_bwd)
+    // set by launch_bwd for the readings: the gate row whose adjoint dg row j takes (LAGGED:
+    // j + w), the keys' log gate products and their gate terms (MASKED)
+    int64_t glag = 0;
+    const float* kdec = nullptr;
+    float* kkey = nullptr;
 };
 size_t bwd_workspace_bytes(const Plan& p);
 bool bwd_win_tc_supported(const Plan& p);

@@ -21,6 +21,7 @@ bool make_plan(const lizard_dims* dims, Plan* p) {
     if (!(d.chunk == 0 || d.chunk == kChunk)) return false;
     if (!(d.dtype == LIZARD_F32 || d.dtype == LIZARD_BF16)) return false;
     if (!(d.scale >= 0.0f) || !isfinite(d.scale)) return false;
+    if (d.decay < LIZARD_DECAY_DELAYED || d.decay > LIZARD_DECAY_LAGGED) return false;
     p->B = d.B;
     p->L = d.L;
     p->Hq = d.Hq;
@@ -32,6 +33,7 @@ bool make_plan(const lizard_dims* dims, Plan* p) {
     p->G = d.Hq / d.Hkv;
     p->scale = d.scale > 0.0f ? d.scale : 1.0f / sqrtf((float)d.d);
     p->dtype = d.dtype;
+    p->decay = d.decay;
     const int64_t U = d.B * d.Hkv;
     p->nchunks = (d.L + kChunk - 1) / kChunk;
     int64_t pmax = (2 * kTargetUnits + U - 1) / U;
@@ -76,8 +78,21 @@ static bool shapes_compiled(const Plan& p) {
            p.B * p.Hq <= (int64_t)1 << 30;
 }
 
-size_t fwd_workspace_bytes(const Plan& p) {
+static size_t fwd_base_bytes(const Plan& p) {
     return kHeaderBytes + sizeof(float) * (size_t)p.Pmax * (size_t)(p.B * p.Hkv) * p.rec_floats;
+}
+
+static size_t al256(size_t n) { return (n + 255) & ~(size_t)255; }
+
+// The header and the records, then (MASKED and LAGGED readings) the reading's scratch.
+size_t fwd_workspace_bytes(const Plan& p) {
+    const size_t r = reading_scratch_bytes(p);
+    return r == 0 ? fwd_base_bytes(p) : al256(fwd_base_bytes(p)) + r;
+}
+
+static void* fwd_reading_scratch(const Plan& p, void* workspace) {
+    if (reading_scratch_bytes(p) == 0) return nullptr;
+    return (char*)workspace + al256(fwd_base_bytes(p));
 }
 
 static bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15u) == 0; }
@@ -108,7 +123,22 @@ size_t fwd_records_used(const Plan& p) {
 }
 
 cudaError_t fwd_launch(const Plan& p, const FwdArgs& a, cudaStream_t s) {
-    cudaError_t e = fwd_tc_supported(p) ? launch_fwd_tc(p, a, s) : launch_fwd_simt(p, a, s);
+    // the readings first fill their scratch: the lagged one runs every kernel on the gates
+    // moved w tokens later, the masked one gives the SIMT walks the keys' log gate products
+    FwdArgs b = a;
+    cudaError_t e = cudaSuccess;
+    if (p.decay != LIZARD_DECAY_DELAYED) {
+        if (a.rscratch == nullptr) return cudaErrorInvalidValue;
+        if (p.decay == LIZARD_DECAY_LAGGED) {
+            e = launch_gate_lag(p, a.g, a.rscratch, s);
+            b.g = a.rscratch;
+        } else {
+            e = launch_key_decay(p, a.g, (float*)a.rscratch, s);
+            b.kdec = (const float*)a.rscratch;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    e = fwd_tc_supported(p) ? launch_fwd_tc(p, b, s) : launch_fwd_simt(p, b, s);
     if (e == cudaSuccess && a.kcache_out != nullptr)
         e = launch_ring_fill(p, a.k, a.v, a.kcache_out, a.vcache_out, s);
     return e;
@@ -196,6 +226,7 @@ lizard_status lizard_attn_fwd(const lizard_dims* dims, const void* q, const void
     a.seg = (float*)((char*)workspace + kHeaderBytes);
     a.ev_before = g_ev_before;
     a.ev_after = g_ev_after;
+    a.rscratch = fwd_reading_scratch(p, workspace);
     return from_cuda(fwd_launch(p, a, s));
 }
 
@@ -319,6 +350,7 @@ lizard_status lizard_attn_fwd_varlen(const lizard_dims* dims, const int64_t* cu_
         a.seg = (float*)((char*)workspace + kHeaderBytes);
         a.ev_before = g_ev_before;
         a.ev_after = g_ev_after;
+        a.rscratch = fwd_reading_scratch(pv, workspace);
         return from_cuda(fwd_launch(pv, a, s));
     }
     // every sequence is a B = 1 problem; its workspace does not depend on its length
@@ -646,15 +678,27 @@ size_t lizard_decode_workspace(const lizard_dims* dims) {
     d1.L = 1;
     Plan p;
     if (!make_plan(&d1, &p)) return 0;
-    return kHeaderBytes;
+    return kHeaderBytes + decode_scratch_bytes(p);
+}
+
+lizard_status lizard_gate_cache_fill(const lizard_dims* dims, const void* g, void* gcache,
+                                     void* stream) {
+    Plan p;
+    if (!make_plan(dims, &p) || g == nullptr || gcache == nullptr || !aligned16(g) ||
+        !aligned16(gcache))
+        return LIZARD_ERR_INVALID_ARG;
+    if (!shapes_compiled(p)) return LIZARD_ERR_UNSUPPORTED;
+    const lizard_status st = device_status();
+    if (st != LIZARD_OK) return st;
+    return from_cuda(launch_gate_ring_fill(p, g, gcache, (cudaStream_t)stream));
 }
 
 // Both decode entry points: one position for the batch (pos_dev null) or one per sequence.
 static lizard_status decode_step(const lizard_dims* dims, int64_t pos, const int64_t* pos_dev,
                                  const void* q, const void* k, const void* v, const void* g,
                                  const void* Wf, const float* sinks, void* y, float* S, float* z,
-                                 void* kcache, void* vcache, void* workspace, size_t ws_bytes,
-                                 void* stream) {
+                                 void* kcache, void* vcache, void* gcache, void* workspace,
+                                 size_t ws_bytes, void* stream) {
     if (dims == nullptr) return LIZARD_ERR_INVALID_ARG;
     lizard_dims d1 = *dims;
     d1.L = 1;
@@ -664,8 +708,12 @@ static lizard_status decode_step(const lizard_dims* dims, int64_t pos, const int
     for (const void* ptr : req)
         if (ptr == nullptr || !aligned16(ptr)) return LIZARD_ERR_INVALID_ARG;
     if (p.M > 0 && (!sinks || !aligned16(sinks))) return LIZARD_ERR_INVALID_ARG;
+    // the masked and lagged readings decay or weigh with gates of the window's tokens
+    if (p.decay != LIZARD_DECAY_DELAYED && (gcache == nullptr || !aligned16(gcache)))
+        return LIZARD_ERR_INVALID_ARG;
     if (!shapes_compiled(p) || p.G > 8 || p.w > 256) return LIZARD_ERR_UNSUPPORTED;
-    if (workspace == nullptr || !aligned16(workspace) || ws_bytes < kHeaderBytes)
+    if (workspace == nullptr || !aligned16(workspace) ||
+        ws_bytes < kHeaderBytes + decode_scratch_bytes(p))
         return LIZARD_ERR_WORKSPACE;
     lizard_status st = device_status();
     if (st != LIZARD_OK) return st;
@@ -684,26 +732,28 @@ static lizard_status decode_step(const lizard_dims* dims, int64_t pos, const int
     a.kc = kcache;
     a.vc = vcache;
     a.header = workspace;
+    a.gc = p.decay != LIZARD_DECAY_DELAYED ? gcache : nullptr;
     return from_cuda(launch_decode(p, a, (cudaStream_t)stream));
 }
 
 lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const void* q,
                                  const void* k, const void* v, const void* g, const void* Wf,
                                  const float* sinks, void* y, float* S, float* z, void* kcache,
-                                 void* vcache, void* workspace, size_t ws_bytes, void* stream) {
+                                 void* vcache, void* gcache, void* workspace, size_t ws_bytes,
+                                 void* stream) {
     return decode_step(dims, pos, nullptr, q, k, v, g, Wf, sinks, y, S, z, kcache, vcache,
-                       workspace, ws_bytes, stream);
+                       gcache, workspace, ws_bytes, stream);
 }
 
 lizard_status lizard_decode_step_positions(const lizard_dims* dims, const int64_t* pos,
                                            const void* q, const void* k, const void* v,
                                            const void* g, const void* Wf, const float* sinks,
                                            void* y, float* S, float* z, void* kcache,
-                                           void* vcache, void* workspace, size_t ws_bytes,
-                                           void* stream) {
+                                           void* vcache, void* gcache, void* workspace,
+                                           size_t ws_bytes, void* stream) {
     if (pos == nullptr || ((uintptr_t)pos & 7u) != 0) return LIZARD_ERR_INVALID_ARG;
-    return decode_step(dims, 0, pos, q, k, v, g, Wf, sinks, y, S, z, kcache, vcache, workspace,
-                       ws_bytes, stream);
+    return decode_step(dims, 0, pos, q, k, v, g, Wf, sinks, y, S, z, kcache, vcache, gcache,
+                       workspace, ws_bytes, stream);
 }
 
 // Checks shared by the two projection entry points.

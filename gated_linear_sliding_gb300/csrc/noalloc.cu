@@ -40,10 +40,16 @@ cudaError_t noalloc_scratch(void** out) {
 }
 
 // Scratch bytes a call needs: the status word, then the boundary-state records its launch
-// uses (the same count as in a caller's workspace).
-size_t noalloc_need(const Plan& p) {
+// uses (the same count as in a caller's workspace), then the reading's scratch (MASKED and
+// LAGGED) from the next 256-byte boundary.
+size_t noalloc_records_end(const Plan& p) {
     return kHeaderBytes +
            sizeof(float) * fwd_records_used(p) * (size_t)(p.B * p.Hkv) * p.rec_floats;
+}
+size_t noalloc_reading_offset(const Plan& p) { return (noalloc_records_end(p) + 255) & ~(size_t)255; }
+size_t noalloc_need(const Plan& p) {
+    const size_t r = reading_scratch_bytes(p);
+    return r == 0 ? noalloc_records_end(p) : noalloc_reading_offset(p) + r;
 }
 
 }  // namespace
@@ -99,6 +105,7 @@ extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const 
     a.seg = (float*)((char*)scratch + kHeaderBytes);
     a.ev_before = nullptr;
     a.ev_after = nullptr;
+    a.rscratch = reading_scratch_bytes(p) != 0 ? (char*)scratch + noalloc_reading_offset(p) : nullptr;
     return fwd_launch(p, a, s) == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA;
 }
 

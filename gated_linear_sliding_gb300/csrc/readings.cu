@@ -1,0 +1,209 @@
+// Kernels of the two other decay readings of the Lizard token mixer.
+//
+// Lizard summary (gist.science/ko/paper/2507.09025), sec. 2-A-1: a data-dependent gate
+// Gamma = sigmoid(g) decays a constant-size state of the tokens that have left the window.
+// The pages do not say which gates such a key has seen.  The default (delayed-key) reading
+// weighs key j <= i - w at query i with prod_{s=j+w+1..i} Gamma_s; the library also runs
+//   LAGGED  prod_{s=j+1..i-w} Gamma_s  = the delayed reading on the gates moved w tokens
+//           later (Gamma'_s = Gamma_{s-w}), so every delayed-reading kernel runs it on a
+//           moved copy of g and the backward moves dg back;
+//   MASKED  prod_{s=j+1..i} Gamma_s    = the delayed reading with each entering key's phi
+//           scaled by c_j = prod_{s=j+1..j+w} Gamma_s, the gates it saw in the window; the
+//           SIMT walks apply e^{kd_j}, kd_j = log c_j from key_decay_kernel.
+// Decode keeps the gate logits of the window in a ring like the keys and values: the
+// lagged step decays by the gate of token pos - w, the masked step admits token pos - w
+// scaled by the product of the gates of pos - w + 1 .. pos.
+#include <math.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace lz {
+namespace {
+
+// An open gate (sigmoid(30) rounds to 1 in fp32): the rows before w of a moved gate
+// sequence only decay the empty state.
+constexpr float kOpenGate = 30.0f;
+
+template <typename T>
+__device__ __forceinline__ uint4 open_chunk() {
+    if constexpr (sizeof(T) == 2) {
+        const uint32_t h = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(kOpenGate));
+        const uint32_t w = h | (h << 16);
+        return make_uint4(w, w, w, w);
+    } else {
+        const uint32_t w = __float_as_uint(kOpenGate);
+        return make_uint4(w, w, w, w);
+    }
+}
+
+// g' row i = g row i - w of the same sequence (i >= w), else an open gate.  One thread per
+// 16-byte chunk of a token row (Hkv D contiguous elements); grid.y = sequence.
+template <typename T>
+__global__ void gate_lag_kernel(Plan p, const T* __restrict__ g, T* __restrict__ out) {
+    const int64_t b = blockIdx.y;
+    const int64_t len = seq_len(p, b), r0 = seq_row0(p, b);
+    const int64_t per_row = p.Hkv * p.D * (int64_t)sizeof(T) / 16;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= len * per_row) return;
+    const int64_t i = e / per_row, c = e % per_row;
+    const uint4 val = i >= p.w
+                          ? reinterpret_cast<const uint4*>(g + (r0 + i - p.w) * p.Hkv * p.D)[c]
+                          : open_chunk<T>();
+    reinterpret_cast<uint4*>(out + (r0 + i) * p.Hkv * p.D)[c] = val;
+}
+
+// kd[j] = sum_{s=j+1..min(j+w, len-1)} log sigmoid(g_s) for KJ consecutive rows j of one
+// column (KV head x feature) per thread, a window sum slid one row at a time in fp64 (the
+// per-gate logarithms in fp32).  Threads of a block take consecutive columns, so every load
+// and store of a row is contiguous.  grid.x = column blocks x row blocks, grid.y = sequence.
+constexpr int KJ = 256;
+
+template <typename T>
+__global__ void __launch_bounds__(128) key_decay_kernel(Plan p, const T* __restrict__ g,
+                                                        float* __restrict__ kd) {
+    const int64_t b = blockIdx.y;
+    const int64_t len = seq_len(p, b), r0 = seq_row0(p, b);
+    const int64_t HD = p.Hkv * p.D, ncb = (HD + 127) / 128;
+    const int64_t cb = blockIdx.x % ncb, jb = blockIdx.x / ncb;
+    const int64_t col = cb * 128 + threadIdx.x;
+    const int64_t j0 = jb * KJ;
+    if (col >= HD || j0 >= len) return;
+    const int64_t j1 = min64(len, j0 + KJ), last = len - 1;
+    const T* gc = g + r0 * HD + col;
+    double acc = 0.0;
+    for (int64_t s = j0 + 1; s <= min64(j0 + p.w, last); ++s)
+        acc += (double)log_sigmoid<false>(ld(gc + s * HD));
+#pragma unroll 4
+    for (int64_t j = j0; j < j1; ++j) {
+        kd[(r0 + j) * HD + col] = (float)acc;
+        // the window of row j + 1 is s = j+2 .. j+1+w: gate j+1+w joins, gate j+1 leaves
+        const float in = j + 1 + p.w <= last ? log_sigmoid<false>(ld(gc + (j + 1 + p.w) * HD)) : 0.0f;
+        const float out = j + 1 <= last ? log_sigmoid<false>(ld(gc + (j + 1) * HD)) : 0.0f;
+        acc += (double)in - (double)out;
+    }
+}
+
+// The gate-ring step of a MASKED or LAGGED decode, one thread per (unit, feature): reads the
+// ring before the new gate goes to slot pos mod (w+1) (the slots read are other slots).
+template <typename T>
+__global__ void decode_ring_kernel(Plan p, int64_t pos_all, const int64_t* pos_dev,
+                                   const T* __restrict__ g, T* __restrict__ gc, void* out) {
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= p.B * p.Hkv * p.D) return;
+    const int64_t unit = e / p.D, f = e % p.D, b = unit / p.Hkv;
+    const int64_t pos = pos_dev != nullptr ? pos_dev[b] : pos_all;
+    if (pos < 0) return;  // the decode kernel reports it and leaves the sequence untouched
+    const int64_t w = p.w, R = w + 1;
+    T* gu = gc + unit * R * p.D + f;
+    const T gnew = g[e];
+    if (p.decay == LIZARD_DECAY_LAGGED) {
+        // the step decays by the gate of token pos - w; before that the state is empty
+        if (pos >= w) ((T*)out)[e] = gu[((pos - w) % R) * p.D];
+        else st((T*)out + e, kOpenGate);
+    } else {
+        // token pos - w enters scaled by prod_{s=pos-w+1..pos} Gamma_s
+        float acc = 0.0f;
+        if (pos >= w) {
+            for (int64_t s = pos - w + 1; s < pos; ++s) acc += log_sigmoid<false>(ld(gu + (s % R) * p.D));
+            acc += log_sigmoid<false>(ld(&gnew));
+        }
+        ((float*)out)[e] = acc;
+    }
+    gu[(pos % R) * p.D] = gnew;
+}
+
+template <typename T>
+__global__ void gate_ring_fill_kernel(Plan p, const T* __restrict__ g, T* __restrict__ gc) {
+    const int64_t unit = blockIdx.y, b = unit / p.Hkv, kv = unit % p.Hkv;
+    const int64_t nt = min64(p.L, p.w);
+    if ((int64_t)blockIdx.x >= nt) return;
+    const int64_t t = p.L - nt + blockIdx.x;
+    const int64_t slot = t % (p.w + 1);
+    for (int64_t c = threadIdx.x; c < p.D; c += blockDim.x)
+        gc[(unit * (p.w + 1) + slot) * p.D + c] = g[((b * p.L + t) * p.Hkv + kv) * p.D + c];
+}
+
+// Reverse cumulative sum of a column of key-side gate terms (rows past L - 1 - w are zero).
+__global__ void key_suffix_kernel(Plan p, float* kk) {
+    const int64_t HD = p.Hkv * p.D;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= p.B * HD) return;
+    const int64_t b = e / HD, col = e % HD;
+    float* x = kk + b * p.L * HD + col;
+    float run = 0.0f;
+#pragma unroll 4
+    for (int64_t j = p.L - 1; j >= 0; --j) {
+        if (j <= p.L - 1 - p.w) run += x[j * HD];
+        x[j * HD] = run;
+    }
+}
+
+size_t elem(const Plan& p) { return p.dtype == LIZARD_F32 ? 4 : 2; }
+
+}  // namespace
+
+size_t reading_scratch_bytes(const Plan& p) {
+    const size_t n = (size_t)(p.T > 0 ? p.T : p.B * p.L) * (size_t)(p.Hkv * p.D);
+    if (p.decay == LIZARD_DECAY_LAGGED) return (n * elem(p) + 255) & ~(size_t)255;
+    if (p.decay == LIZARD_DECAY_MASKED) return (n * 4 + 255) & ~(size_t)255;
+    return 0;
+}
+
+size_t decode_scratch_bytes(const Plan& p) {
+    const size_t n = (size_t)(p.B * p.Hkv * p.D);
+    if (p.decay == LIZARD_DECAY_LAGGED) return (n * elem(p) + 255) & ~(size_t)255;
+    if (p.decay == LIZARD_DECAY_MASKED) return (n * 4 + 255) & ~(size_t)255;
+    return 0;
+}
+
+cudaError_t launch_gate_lag(const Plan& p, const void* g, void* out, cudaStream_t s) {
+    const int64_t per_row = p.Hkv * p.D * (int64_t)elem(p) / 16;
+    const dim3 grid((unsigned)((p.L * per_row + 255) / 256), (unsigned)p.B);
+    if (p.dtype == LIZARD_F32)
+        gate_lag_kernel<float><<<grid, 256, 0, s>>>(p, (const float*)g, (float*)out);
+    else
+        gate_lag_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(p, (const __nv_bfloat16*)g,
+                                                            (__nv_bfloat16*)out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_key_decay(const Plan& p, const void* g, float* kd, cudaStream_t s) {
+    const int64_t ncb = (p.Hkv * p.D + 127) / 128, njb = (p.L + KJ - 1) / KJ;
+    const dim3 grid((unsigned)(ncb * njb), (unsigned)p.B);
+    if (p.dtype == LIZARD_F32)
+        key_decay_kernel<float><<<grid, 128, 0, s>>>(p, (const float*)g, kd);
+    else
+        key_decay_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(p, (const __nv_bfloat16*)g, kd);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_ring(const Plan& p, const DecodeArgs& a, void* out, cudaStream_t s) {
+    const int64_t n = p.B * p.Hkv * p.D;
+    const unsigned grid = (unsigned)((n + 255) / 256);
+    if (p.dtype == LIZARD_F32)
+        decode_ring_kernel<float><<<grid, 256, 0, s>>>(p, a.pos, a.pos_dev, (const float*)a.g,
+                                                       (float*)a.gc, out);
+    else
+        decode_ring_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+            p, a.pos, a.pos_dev, (const __nv_bfloat16*)a.g, (__nv_bfloat16*)a.gc, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_gate_ring_fill(const Plan& p, const void* g, void* gc, cudaStream_t s) {
+    const dim3 grid((unsigned)min64(p.L, p.w), (unsigned)(p.B * p.Hkv));
+    if (p.dtype == LIZARD_F32)
+        gate_ring_fill_kernel<float><<<grid, 128, 0, s>>>(p, (const float*)g, (float*)gc);
+    else
+        gate_ring_fill_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(p, (const __nv_bfloat16*)g,
+                                                                  (__nv_bfloat16*)gc);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_key_suffix(const Plan& p, float* kk, cudaStream_t s) {
+    const int64_t n = p.B * p.Hkv * p.D;
+    key_suffix_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, kk);
+    return cudaGetLastError();
+}
+
+}  // namespace lz

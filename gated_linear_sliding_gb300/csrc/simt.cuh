@@ -121,6 +121,20 @@ __device__ __forceinline__ void gates_cumsum(const T* g, int64_t b, int64_t L, i
     __syncthreads();
 }
 
+// Masked decay reading: the delayed keys of rows [rlo, n) (row t holds key tok0 + t of a
+// sequence with L rows) enter the state with phi scaled by e^{kd}, kd = the log product of
+// the w gates each key saw inside the window (rows of kd [B, L, Hkv, DF]).
+template <int DF, int TSZ, int NTH, bool FAST>
+__device__ __forceinline__ void scale_entering_keys(float* sphk, const float* kd, int64_t b,
+                                                    int64_t L, int64_t Hkv, int64_t kv,
+                                                    int64_t tok0, int rlo, int n) {
+    constexpr int PF = DF + 1;
+    for (int e = threadIdx.x; e < TSZ * DF; e += NTH) {
+        const int t = e / DF, f = e % DF;
+        if (t >= rlo && t < n) sphk[t * PF + f] *= ex<FAST>(kd[((b * L + tok0 + t) * Hkv + kv) * DF + f]);
+    }
+}
+
 // H <- e^{b_last} (.) H + sum_t (phk_t e^{b_last - b_t}) v_t^T, z likewise.
 // Overwrites sphk with the decayed keys.
 template <int DH, int DF, bool FAST>

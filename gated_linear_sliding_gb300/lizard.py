@@ -24,6 +24,10 @@ LIZARD_ERR_CUDA = 4
 LIZARD_ERR_TIMEOUT = 5
 LIZARD_F32 = 0
 LIZARD_BF16 = 1
+# decay readings (include/lizard.h, lizard_decay)
+LIZARD_DECAY_DELAYED = 0
+LIZARD_DECAY_MASKED = 1
+LIZARD_DECAY_LAGGED = 2
 
 EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_fwd",
             "lizard_attn_bwd_workspace", "lizard_attn_bwd", "lizard_decode_workspace",
@@ -34,14 +38,14 @@ EXPORTED = ["lizard_attn_fwd_workspace", "lizard_workspace_init", "lizard_attn_f
             "lizard_attn_fwd_varlen_workspace",
             "lizard_attn_bwd_varlen_workspace", "lizard_attn_bwd_varlen",
             "lizard_attn_fwd_noalloc_scratch", "lizard_read_noalloc_status",
-            "lizard_qkvg_proj", "lizard_qkvg_proj_bwd"]
+            "lizard_qkvg_proj", "lizard_qkvg_proj_bwd", "lizard_gate_cache_fill"]
 
 
 class lizard_dims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("L", ctypes.c_int64), ("Hq", ctypes.c_int64),
                 ("Hkv", ctypes.c_int64), ("d", ctypes.c_int64), ("D", ctypes.c_int64),
                 ("w", ctypes.c_int64), ("M", ctypes.c_int64), ("chunk", ctypes.c_int64),
-                ("scale", ctypes.c_float), ("dtype", ctypes.c_int32)]
+                ("scale", ctypes.c_float), ("dtype", ctypes.c_int32), ("decay", ctypes.c_int32)]
 
 
 class LizardError(RuntimeError):
@@ -99,10 +103,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.lizard_qkvg_proj_bwd.restype = ctypes.c_int
     lib.lizard_attn_bwd.argtypes = [_DP] + [_VP] * 16 + [ctypes.c_size_t, _VP]
     lib.lizard_attn_bwd.restype = ctypes.c_int
-    lib.lizard_decode_step.argtypes = [_DP, ctypes.c_int64] + [_VP] * 12 + [ctypes.c_size_t, _VP]
+    lib.lizard_decode_step.argtypes = [_DP, ctypes.c_int64] + [_VP] * 13 + [ctypes.c_size_t, _VP]
     lib.lizard_decode_step.restype = ctypes.c_int
-    lib.lizard_decode_step_positions.argtypes = [_DP] + [_VP] * 13 + [ctypes.c_size_t, _VP]
+    lib.lizard_decode_step_positions.argtypes = [_DP] + [_VP] * 14 + [ctypes.c_size_t, _VP]
     lib.lizard_decode_step_positions.restype = ctypes.c_int
+    lib.lizard_gate_cache_fill.argtypes = [_DP, _VP, _VP, _VP]
+    lib.lizard_gate_cache_fill.restype = ctypes.c_int
     lib.lizard_read_device_status.argtypes = [_VP, _VP]
     lib.lizard_read_device_status.restype = ctypes.c_int
     lib.lizard_status_string.argtypes = [ctypes.c_int]
@@ -146,17 +152,19 @@ def _dtype_code(t: torch.Tensor) -> int:
     raise TypeError(f"unsupported dtype {t.dtype}")
 
 
-def make_dims(B, L, Hq, Hkv, d, D, w, M, dtype, scale: float = 0.0, chunk: int = 0) -> lizard_dims:
+def make_dims(B, L, Hq, Hkv, d, D, w, M, dtype, scale: float = 0.0, chunk: int = 0,
+              decay: int = LIZARD_DECAY_DELAYED) -> lizard_dims:
     code = dtype if isinstance(dtype, int) else _dtype_code(torch.empty(0, dtype=dtype))
-    return lizard_dims(B, L, Hq, Hkv, d, D, w, M, chunk, float(scale), code)
+    return lizard_dims(B, L, Hq, Hkv, d, D, w, M, chunk, float(scale), code, int(decay))
 
 
-def dims_of(q, k, g, sinks, w: int, scale: float = 0.0) -> lizard_dims:
+def dims_of(q, k, g, sinks, w: int, scale: float = 0.0,
+            decay: int = LIZARD_DECAY_DELAYED) -> lizard_dims:
     B, L, Hq, d = q.shape
     Hkv = k.shape[2]
     D = g.shape[-1]
     M = sinks.shape[1]
-    return lizard_dims(B, L, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    return lizard_dims(B, L, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q), int(decay))
 
 
 def _need(t, name, shape, dtype):
@@ -232,8 +240,9 @@ def lizard_read_device_status(workspace: torch.Tensor, stream=None) -> int:
 
 def lizard_attn_fwd(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0, y=None, lse=None,
                     S_out=None, z_out=None, kcache_out=None, vcache_out=None, workspace=None,
-                    stream=None):
-    """Forward over L tokens.  Returns y [B, L, Hq, d] (allocated if not given)."""
+                    stream=None, decay: int = LIZARD_DECAY_DELAYED):
+    """Forward over L tokens.  Returns y [B, L, Hq, d] (allocated if not given).  `decay`
+    selects the decay reading (LIZARD_DECAY_*)."""
     B, L, Hq, d = q.shape
     Hkv, D, M = k.shape[2], g.shape[-1], sinks.shape[1]
     dt = q.dtype
@@ -254,7 +263,7 @@ def lizard_attn_fwd(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0, y=None
     if kcache_out is not None:
         _need(kcache_out, "kcache_out", (B, Hkv, w + 1, d), dt)
         _need(vcache_out, "vcache_out", (B, Hkv, w + 1, d), dt)
-    dims = dims_of(q, k, g, sinks, w, scale)
+    dims = dims_of(q, k, g, sinks, w, scale, decay)
     if workspace is None:
         workspace = new_workspace(lizard_attn_fwd_workspace(dims), q.device, stream)
     st = load().lizard_attn_fwd(ctypes.byref(dims), _p(q), _p(k), _p(v), _p(g), _p(Wf),
@@ -273,7 +282,8 @@ def lizard_attn_fwd_varlen_workspace(dims, cu_seqlens) -> int:
 
 def lizard_attn_fwd_varlen(q, k, v, g, Wf, sinks, w: int, cu_seqlens, *, scale: float = 0.0,
                            y=None, lse=None, S_out=None, z_out=None, kcache_out=None,
-                           vcache_out=None, workspace=None, stream=None):
+                           vcache_out=None, workspace=None, stream=None,
+                           decay: int = LIZARD_DECAY_DELAYED):
     """Forward over a packed batch: q [T, Hq, d], k, v [T, Hkv, d], g [T, Hkv, D], and
     cu_seqlens (host integers, B + 1 offsets) delimiting B sequences.  Returns y [T, Hq, d];
     S_out, z_out, kcache_out, vcache_out hold one entry per sequence."""
@@ -299,7 +309,7 @@ def lizard_attn_fwd_varlen(q, k, v, g, Wf, sinks, w: int, cu_seqlens, *, scale: 
     if kcache_out is not None:
         _need(kcache_out, "kcache_out", (nseq, Hkv, w + 1, d), dt)
         _need(vcache_out, "vcache_out", (nseq, Hkv, w + 1, d), dt)
-    dims = lizard_dims(nseq, T, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    dims = lizard_dims(nseq, T, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q), int(decay))
     if workspace is None:  # the size of one launch over all sequences
         workspace = new_workspace(lizard_attn_fwd_varlen_workspace(dims, cu), q.device, stream)
     st = load().lizard_attn_fwd_varlen(ctypes.byref(dims), cu.ctypes.data, _p(q), _p(k), _p(v),
@@ -312,7 +322,7 @@ def lizard_attn_fwd_varlen(q, k, v, g, Wf, sinks, w: int, cu_seqlens, *, scale: 
 
 def lizard_attn_fwd_noalloc(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0, y=None,
                             lse=None, S_out=None, z_out=None, kcache_out=None, vcache_out=None,
-                            stream=None):
+                            stream=None, decay: int = LIZARD_DECAY_DELAYED):
     """The forward without a workspace, for callers that cannot allocate device memory.
 
     Same arguments and result as lizard_attn_fwd; the library keeps the scratch in a
@@ -330,7 +340,7 @@ def lizard_attn_fwd_noalloc(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0
     if y is None:
         y = torch.empty_like(q)
     _need(y, "y", (B, L, Hq, d), dt)
-    dims = dims_of(q, k, g, sinks, w, scale)
+    dims = dims_of(q, k, g, sinks, w, scale, decay)
     st = load().lizard_attn_fwd_noalloc(ctypes.byref(dims), _p(q), _p(k), _p(v), _p(g), _p(Wf),
                                         _p(sinks), _p(y), _p(lse), _p(S_out), _p(z_out),
                                         _p(kcache_out), _p(vcache_out), _stream(stream))
@@ -340,8 +350,9 @@ def lizard_attn_fwd_noalloc(q, k, v, g, Wf, sinks, w: int, *, scale: float = 0.0
 
 def lizard_attn_bwd(q, k, v, g, Wf, sinks, y, lse, dy, w: int, *, scale: float = 0.0,
                     dq=None, dk=None, dv=None, dg=None, dWf=None, dsinks=None, workspace=None,
-                    stream=None):
-    """Gradients (dq, dk, dv, dg, dWf, dsinks) of y against dy."""
+                    stream=None, decay: int = LIZARD_DECAY_DELAYED):
+    """Gradients (dq, dk, dv, dg, dWf, dsinks) of y against dy (same decay reading as the
+    forward that made y)."""
     B, L, Hq, d = q.shape
     Hkv, D, M = k.shape[2], g.shape[-1], sinks.shape[1]
     dt = q.dtype
@@ -357,7 +368,7 @@ def lizard_attn_bwd(q, k, v, g, Wf, sinks, y, lse, dy, w: int, *, scale: float =
     dg = torch.empty_like(g) if dg is None else dg
     dWf = torch.empty(Hkv, d, D // 2, dtype=torch.float32, device=q.device) if dWf is None else dWf
     dsinks = torch.empty(Hq, M, dtype=torch.float32, device=q.device) if dsinks is None else dsinks
-    dims = dims_of(q, k, g, sinks, w, scale)
+    dims = dims_of(q, k, g, sinks, w, scale, decay)
     if workspace is None:
         workspace = new_workspace(lizard_attn_bwd_workspace(dims), q.device, stream)
     st = load().lizard_attn_bwd(ctypes.byref(dims), _p(q), _p(k), _p(v), _p(g), _p(Wf),
@@ -375,7 +386,8 @@ def lizard_attn_bwd_varlen_workspace(dims, cu_seqlens) -> int:
 
 
 def lizard_attn_bwd_varlen(q, k, v, g, Wf, sinks, y, lse, dy, w: int, cu_seqlens, *,
-                           scale: float = 0.0, workspace=None, stream=None):
+                           scale: float = 0.0, workspace=None, stream=None,
+                           decay: int = LIZARD_DECAY_DELAYED):
     """Gradients of lizard_attn_fwd_varlen's y against dy for a packed batch: dq, dk, dv,
     dg packed like the inputs; dWf and dsinks summed over the sequences."""
     T, Hq, d = q.shape
@@ -392,7 +404,7 @@ def lizard_attn_bwd_varlen(q, k, v, g, Wf, sinks, y, lse, dy, w: int, cu_seqlens
     dq, dk, dv, dg = (torch.empty_like(x) for x in (q, k, v, g))
     dWf = torch.empty(Hkv, d, D // 2, dtype=torch.float32, device=q.device)
     dsinks = torch.empty(Hq, M, dtype=torch.float32, device=q.device)
-    dims = lizard_dims(nseq, T, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    dims = lizard_dims(nseq, T, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q), int(decay))
     if workspace is None:
         nbytes = int(load().lizard_attn_bwd_varlen_workspace(ctypes.byref(dims), cu.ctypes.data))
         if nbytes == 0:
@@ -406,9 +418,7 @@ def lizard_attn_bwd_varlen(q, k, v, g, Wf, sinks, y, lse, dy, w: int, cu_seqlens
     return dict(dq=dq, dk=dk, dv=dv, dg=dg, dWf=dWf, dsinks=dsinks)
 
 
-def lizard_decode_step(pos: int, q, k, v, g, Wf, sinks, S, z, kcache, vcache, w: int, *,
-                       scale: float = 0.0, y=None, workspace=None, stream=None):
-    """One decode step at position pos; S, z, kcache, vcache are updated in place."""
+def _decode_common(q, k, v, g, Wf, sinks, S, z, kcache, vcache, gcache, w, decay):
     B, Hq, d = q.shape
     Hkv, D, M = k.shape[1], g.shape[-1], sinks.shape[1]
     dt = q.dtype
@@ -421,45 +431,61 @@ def lizard_decode_step(pos: int, q, k, v, g, Wf, sinks, S, z, kcache, vcache, w:
     _need(z, "z", (B, Hkv, D), torch.float32)
     _need(kcache, "kcache", (B, Hkv, w + 1, d), dt)
     _need(vcache, "vcache", (B, Hkv, w + 1, d), dt)
+    if decay != LIZARD_DECAY_DELAYED or gcache is not None:
+        _need(gcache, "gcache", (B, Hkv, w + 1, D), dt)
+    return B, Hq, Hkv, d, D, M
+
+
+def lizard_decode_step(pos: int, q, k, v, g, Wf, sinks, S, z, kcache, vcache, w: int, *,
+                       scale: float = 0.0, y=None, workspace=None, stream=None, gcache=None,
+                       decay: int = LIZARD_DECAY_DELAYED):
+    """One decode step at position pos; S, z, kcache, vcache (and gcache, the gate ring the
+    MASKED and LAGGED readings need) are updated in place."""
+    B, Hq, Hkv, d, D, M = _decode_common(q, k, v, g, Wf, sinks, S, z, kcache, vcache, gcache,
+                                         w, decay)
     y = torch.empty_like(q) if y is None else y
-    dims = lizard_dims(B, 1, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    dims = lizard_dims(B, 1, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q), int(decay))
     if workspace is None:
         workspace = new_workspace(lizard_decode_workspace(dims), q.device, stream)
     st = load().lizard_decode_step(ctypes.byref(dims), int(pos), _p(q), _p(k), _p(v), _p(g),
                                    _p(Wf), _p(sinks), _p(y), _p(S), _p(z), _p(kcache),
-                                   _p(vcache), _p(workspace), workspace.numel(), _stream(stream))
+                                   _p(vcache), _p(gcache), _p(workspace), workspace.numel(),
+                                   _stream(stream))
     _check(st, "lizard_decode_step")
     return y
 
 
 def lizard_decode_step_positions(pos, q, k, v, g, Wf, sinks, S, z, kcache, vcache, w: int, *,
-                                 scale: float = 0.0, y=None, workspace=None, stream=None):
+                                 scale: float = 0.0, y=None, workspace=None, stream=None,
+                                 gcache=None, decay: int = LIZARD_DECAY_DELAYED):
     """One decode step with a position per sequence: pos is an int64 device tensor [B],
     read when the kernel runs.  A negative entry is reported through the workspace status
     (lizard_read_device_status) and leaves that sequence untouched."""
-    B, Hq, d = q.shape
-    Hkv, D, M = k.shape[1], g.shape[-1], sinks.shape[1]
-    dt = q.dtype
+    B = q.shape[0]
     _need(pos, "pos", (B,), torch.int64)
-    _need(k, "k", (B, Hkv, d), dt)
-    _need(v, "v", (B, Hkv, d), dt)
-    _need(g, "g", (B, Hkv, D), dt)
-    _need(Wf, "Wf", (Hkv, d, D // 2), dt)
-    _need(sinks, "sinks", (Hq, M), torch.float32)
-    _need(S, "S", (B, Hkv, D, d), torch.float32)
-    _need(z, "z", (B, Hkv, D), torch.float32)
-    _need(kcache, "kcache", (B, Hkv, w + 1, d), dt)
-    _need(vcache, "vcache", (B, Hkv, w + 1, d), dt)
+    B, Hq, Hkv, d, D, M = _decode_common(q, k, v, g, Wf, sinks, S, z, kcache, vcache, gcache,
+                                         w, decay)
     y = torch.empty_like(q) if y is None else y
-    dims = lizard_dims(B, 1, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q))
+    dims = lizard_dims(B, 1, Hq, Hkv, d, D, w, M, 0, float(scale), _dtype_code(q), int(decay))
     if workspace is None:
         workspace = new_workspace(lizard_decode_workspace(dims), q.device, stream)
     st = load().lizard_decode_step_positions(ctypes.byref(dims), _p(pos), _p(q), _p(k), _p(v),
                                              _p(g), _p(Wf), _p(sinks), _p(y), _p(S), _p(z),
-                                             _p(kcache), _p(vcache), _p(workspace),
+                                             _p(kcache), _p(vcache), _p(gcache), _p(workspace),
                                              workspace.numel(), _stream(stream))
     _check(st, "lizard_decode_step_positions")
     return y
+
+
+def lizard_gate_cache_fill(g, gcache, w: int, *, stream=None):
+    """Gate ring of a prefill: the gate rows of the last min(L, w) tokens of g [B, L, Hkv, D]
+    go to slot t mod (w+1) of gcache [B, Hkv, w+1, D] (same dtype)."""
+    B, L, Hkv, D = g.shape
+    _need(g, "g", (B, L, Hkv, D), g.dtype)
+    _need(gcache, "gcache", (B, Hkv, w + 1, D), g.dtype)
+    dims = lizard_dims(B, L, Hkv, Hkv, D, D, w, 0, 0, 0.0, _dtype_code(g))
+    _check(load().lizard_gate_cache_fill(ctypes.byref(dims), _p(g), _p(gcache), _stream(stream)),
+           "lizard_gate_cache_fill")
 
 
 def lizard_qkvg_proj(x, W, Hq: int, Hkv: int, d: int, D: int, *, q=None, k=None, v=None,

@@ -19,6 +19,19 @@
  * is decayed by every later gate.  Query head h uses KV head h / (Hq / Hkv),
  * which owns Wf, the gate logits, S and z.
  *
+ * The pages say only that the gate decays a state of the tokens outside the
+ * window (sec. 2-A-1), not which gates a key that has left the window has seen.
+ * The recurrence above is the default reading; dims.decay selects one of two
+ * others, as the gate product that weighs key j <= i - w at query i:
+ *   LIZARD_DECAY_DELAYED (0)  prod_{s=j+w+1..i} Gamma_s  (the recurrence above);
+ *   LIZARD_DECAY_MASKED  (1)  prod_{s=j+1..i}   Gamma_s  (full gated linear
+ *       attention with the window's keys masked out: the key enters the state
+ *       already decayed by the w gates it saw inside the window);
+ *   LIZARD_DECAY_LAGGED  (2)  prod_{s=j+1..i-w} Gamma_s  (the query reads the
+ *       gated state of token i - w: the delayed recurrence run on the gates of
+ *       w tokens earlier).
+ * All three coincide when every gate is 1.
+ *
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers to contiguous row-major arrays,
  *     16-byte aligned.  The caller allocates and owns every buffer, workspace
@@ -39,6 +52,7 @@
  *   sinks, dsinks [Hq, M] (fp32)       lse           [B, L, Hq] (fp32)
  *   S             [B, Hkv, D, d] fp32  z             [B, Hkv, D] fp32
  *   kcache/vcache [B, Hkv, w+1, d]     token t lives in slot t mod (w+1)
+ *   gcache        [B, Hkv, w+1, D]     gate logits, same slots (MASKED/LAGGED decode)
  */
 #ifndef LIZARD_H
 #define LIZARD_H
@@ -61,25 +75,45 @@ typedef enum {
 
 typedef enum { LIZARD_F32 = 0, LIZARD_BF16 = 1 } lizard_dtype;
 
+typedef enum {
+    LIZARD_DECAY_DELAYED = 0, /* key enters undecayed as it leaves the window (default) */
+    LIZARD_DECAY_MASKED = 1,  /* full gated linear attention, window masked out        */
+    LIZARD_DECAY_LAGGED = 2   /* the query reads the gated state of token i - w         */
+} lizard_decay;
+
 /* Problem sizes.  d, D in {64, 128}; D is the phi width (Wf is d x D/2);
  * Hq % Hkv == 0; w >= 1 (window of the w most recent tokens, self included);
  * 0 <= M <= 64 sinks per query head; chunk is 0 (default) or 64;
- * scale is the softmax scale applied to q.k, 0 selects 1/sqrt(d). */
+ * scale is the softmax scale applied to q.k, 0 selects 1/sqrt(d);
+ * decay is the reading of the gate decay (lizard_decay; 0, the default, in a
+ * zero-initialised struct).  How each reading runs:
+ *   DELAYED  every path below as described;
+ *   LAGGED   the same kernels on the gate logits moved w tokens later (a copy in
+ *            the workspace, B L Hkv D elements more than the DELAYED workspace; the
+ *            backward moves dg back); decode needs the gate ring (gcache);
+ *   MASKED   the SIMT walks only (forward and backward), with each entering key's
+ *            phi scaled by the product of the w gates it saw in the window (per-token
+ *            log products in the workspace, B L Hkv D fp32 more; the backward keeps the
+ *            key-side gate terms in a second such array); decode needs gcache.  The
+ *            window parts of the backward still run on the tensor cores. */
 typedef struct {
     int64_t B, L, Hq, Hkv, d, D, w, M;
     int64_t chunk;
     float scale;
     int32_t dtype; /* lizard_dtype */
+    int32_t decay; /* lizard_decay */
 } lizard_dims;
 
-/* Bytes of device workspace lizard_attn_fwd needs.  It depends on B, Hkv, d and
- * D only, never on L (the per-segment boundary states, sec. 2-A-1 constant
- * memory).  Returns 0 for invalid dims. */
+/* Bytes of device workspace lizard_attn_fwd needs.  Under the DELAYED reading it
+ * depends on B, Hkv, d and D only, never on L (the per-segment boundary states,
+ * sec. 2-A-1 constant memory); the MASKED and LAGGED readings add one value per gate
+ * element (see lizard_dims).  Returns 0 for invalid dims. */
 size_t lizard_attn_fwd_workspace(const lizard_dims* dims);
 
 /* Which forward kernel serves these sizes: 1 = the tensor-core (tcgen05) chunk walk
- * (bf16, d = D = 128, Hq = 4 Hkv, w = 64), 0 = the SIMT walk (fp32 and every other
- * shape), -1 = invalid sizes.  Pure host query. */
+ * (bf16, d = D = 128, Hq = 4 Hkv, w = 64, reading DELAYED or LAGGED), 0 = the SIMT walk
+ * (fp32, the MASKED reading and every other shape), -1 = invalid sizes.  Pure host
+ * query. */
 int lizard_attn_fwd_kernel(const lizard_dims* dims);
 
 /* Zero the device status word at the head of a workspace (async on stream).
@@ -179,7 +213,9 @@ lizard_status lizard_read_noalloc_status(void* stream);
 /* Bytes of device workspace lizard_attn_bwd needs: segment records whose size depends on
  * B, Hkv, d and D only, plus one fp32 per gate element (B * L * Hkv * D * 4 bytes) holding
  * the per-position gate gradient before its reverse cumulative sum, plus two fp32 per query
- * row (e^{-lse} and dy . y, B * L * Hq * 8 bytes). */
+ * row (e^{-lse} and dy . y, B * L * Hq * 8 bytes); the LAGGED reading adds one dtype value
+ * per gate element (the moved gates), the MASKED reading two fp32 (the keys' log gate
+ * products and their gate terms). */
 size_t lizard_attn_bwd_workspace(const lizard_dims* dims);
 
 /* Exact gradient of lizard_attn_fwd's y against an upstream gradient dy.  The
@@ -243,8 +279,19 @@ lizard_status lizard_qkvg_proj_bwd(const lizard_dims* dims, int64_t dmodel, cons
                                    const void* dv, const void* dg, void* dx, float* dW,
                                    void* workspace, size_t ws_bytes, void* stream);
 
-/* Bytes of device workspace lizard_decode_step needs (the status word only). */
+/* Bytes of device workspace lizard_decode_step needs: the status word, plus for the MASKED
+ * and LAGGED readings B Hkv D values (the step's decay gates or key factors). */
 size_t lizard_decode_workspace(const lizard_dims* dims);
+
+/* Fill the gate ring a MASKED or LAGGED decode continues from: the gate logits of the last
+ * min(L, w) tokens of a prefill go to slot t mod (w+1) of gcache [B, Hkv, w+1, D] (dtype),
+ * other slots untouched, as lizard_attn_fwd writes kcache_out and vcache_out.  g [B, L, Hkv,
+ * D] is the prefill's input.  The gates of the tokens in the window are what these two
+ * readings decay with later: the lagged state takes the gate of token pos - w at step pos,
+ * the masked reading the product of the gates of tokens pos - w + 1 .. pos.  Errors:
+ * LIZARD_ERR_INVALID_ARG for bad dims or null/misaligned pointers. */
+lizard_status lizard_gate_cache_fill(const lizard_dims* dims, const void* g, void* gcache,
+                                     void* stream);
 
 /* One constant-memory generation step for every sequence of the batch
  * (sec. 2-A-1: the state is updated incrementally, no growing KV cache;
@@ -256,11 +303,17 @@ size_t lizard_decode_workspace(const lizard_dims* dims);
  *   (decay by Gamma_pos, then admit token pos-w read from the ring);
  *   kcache, vcache: ring caches holding tokens pos-w .. pos-1; the new k, v are
  *   written to slot pos mod (w+1) IN PLACE;
+ *   gcache: the gate-logit ring of the same tokens (lizard_gate_cache_fill after a prefill),
+ *   the new g written to slot pos mod (w+1) IN PLACE; required for the MASKED and LAGGED
+ *   readings (LIZARD_ERR_INVALID_ARG when null), ignored and may be NULL for DELAYED.  The
+ *   lagged state decays by the gate of token pos - w (none while pos < w), the masked
+ *   reading admits token pos - w scaled by the product of the gates of pos - w + 1 .. pos;
  *   y [B, Hq, d]: the output of token pos. */
 lizard_status lizard_decode_step(const lizard_dims* dims, int64_t pos, const void* q,
                                  const void* k, const void* v, const void* g, const void* Wf,
                                  const float* sinks, void* y, float* S, float* z, void* kcache,
-                                 void* vcache, void* workspace, size_t ws_bytes, void* stream);
+                                 void* vcache, void* gcache, void* workspace, size_t ws_bytes,
+                                 void* stream);
 
 /* The same step with one position per sequence, for batches whose sequences have
  * different lengths (continuous batching).
@@ -276,8 +329,8 @@ lizard_status lizard_decode_step_positions(const lizard_dims* dims, const int64_
                                            const void* q, const void* k, const void* v,
                                            const void* g, const void* Wf, const float* sinks,
                                            void* y, float* S, float* z, void* kcache,
-                                           void* vcache, void* workspace, size_t ws_bytes,
-                                           void* stream);
+                                           void* vcache, void* gcache, void* workspace,
+                                           size_t ws_bytes, void* stream);
 
 /* Synchronise `stream`, read the device status word of `workspace` and clear it.
  * Returns LIZARD_OK or the first error a kernel recorded (e.g. LIZARD_ERR_TIMEOUT). */

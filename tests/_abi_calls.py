@@ -14,10 +14,11 @@ from gated_linear_sliding_gb300 import lizard as lz  # noqa: E402
 
 
 def dims(**kw):
-    base = dict(B=1, L=128, Hq=32, Hkv=8, d=128, D=128, w=64, M=4, dtype=lz.LIZARD_BF16)
+    base = dict(B=1, L=128, Hq=32, Hkv=8, d=128, D=128, w=64, M=4, dtype=lz.LIZARD_BF16,
+                decay=lz.LIZARD_DECAY_DELAYED)
     base.update(kw)
     return lz.make_dims(base["B"], base["L"], base["Hq"], base["Hkv"], base["d"], base["D"],
-                        base["w"], base["M"], base["dtype"])
+                        base["w"], base["M"], base["dtype"], decay=base["decay"])
 
 
 def main():
@@ -45,12 +46,28 @@ def main():
     need = lz.lizard_attn_fwd_workspace(d)
     out["fwd_small_ws"] = lib.lizard_attn_fwd(ctypes.byref(d), *args, need - 16, None)
     out["noalloc_misaligned"] = lib.lizard_attn_fwd_noalloc(ctypes.byref(d), *a2[:12], None)
-    nul = [ok] * 12
+    nul = [ok] * 13  # q .. vcache, gcache
     out["dec_w300"] = lib.lizard_decode_step(ctypes.byref(dims(w=300)), 0, *nul, 256, None)
     out["dec_G16"] = lib.lizard_decode_step(ctypes.byref(dims(Hq=32, Hkv=2)), 0, *nul, 256, None)
     out["dec_neg_pos"] = lib.lizard_decode_step(ctypes.byref(dims()), -1, *nul, 256, None)
     out["dec_misaligned"] = lib.lizard_decode_step(ctypes.byref(dims()), 0, mis, *nul[1:], 256,
                                                    None)
+    # decay readings: an unknown one, and a masked/lagged decode without its gate ring
+    out["fwd_bad_decay"] = lib.lizard_attn_fwd(ctypes.byref(dims(decay=3)), *args, 1 << 30, None)
+    for name, code in (("masked", lz.LIZARD_DECAY_MASKED), ("lagged", lz.LIZARD_DECAY_LAGGED)):
+        # nul[:11] = q .. vcache, then gcache, workspace, its size, the stream
+        out[f"dec_{name}_no_gcache"] = lib.lizard_decode_step(
+            ctypes.byref(dims(decay=code)), 0, *nul[:11], None, ok, 1 << 20, None)
+        out[f"dec_{name}_mis_gcache"] = lib.lizard_decode_step(
+            ctypes.byref(dims(decay=code)), 0, *nul[:11], mis, ok, 1 << 20, None)
+        out[f"dec_{name}_small_ws"] = lib.lizard_decode_step(
+            ctypes.byref(dims(decay=code)), 0, *nul, 256, None)
+    # the delayed reading ignores the ring: no device is what stops this call
+    out["dec_delayed_no_gcache"] = lib.lizard_decode_step(ctypes.byref(dims()), 0, *nul[:11],
+                                                          None, ok, 256, None)
+    out["gfill_null"] = lib.lizard_gate_cache_fill(ctypes.byref(dims()), None, ok, None)
+    out["gfill_mis"] = lib.lizard_gate_cache_fill(ctypes.byref(dims()), ok, mis, None)
+    out["gfill_bad_dims"] = lib.lizard_gate_cache_fill(ctypes.byref(dims(w=0)), ok, ok, None)
     # the projections: bf16 only, dm a multiple of 64
     six = [ok] * 6
     out["proj_f32"] = lib.lizard_qkvg_proj(ctypes.byref(dims(dtype=lz.LIZARD_F32)), 256, *six,

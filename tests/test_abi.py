@@ -51,7 +51,48 @@ def dims(**kw):
     base.update(kw)
     return lz.make_dims(base["B"], base["L"], base["Hq"], base["Hkv"], base["d"], base["D"],
                         base["w"], base["M"], base["dtype"], scale=kw.get("scale", 0.0),
-                        chunk=kw.get("chunk", 0))
+                        chunk=kw.get("chunk", 0), decay=kw.get("decay", 0))
+
+
+def test_dims_struct_layout(tmp_path):
+    """The Python mirror of lizard_dims has the layout the C compiler gives the header's
+    struct (size and every field offset)."""
+    src = tmp_path / "layout.c"
+    src.write_text('#include <stddef.h>\n#include <stdio.h>\n#include "lizard.h"\n'
+                   'int main(void) { printf("%zu", sizeof(lizard_dims));\n' +
+                   "".join(f'printf(" %zu", offsetof(lizard_dims, {n}));\n'
+                           for n, _ in lz.lizard_dims._fields_) + "return 0; }\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call(["gcc", "-I", os.path.dirname(HEADER), "-o", str(exe), str(src)])
+    got = [int(x) for x in subprocess.check_output([str(exe)], text=True).split()]
+    want = [ctypes.sizeof(lz.lizard_dims)] + [getattr(lz.lizard_dims, n).offset
+                                              for n, _ in lz.lizard_dims._fields_]
+    assert got == want
+
+
+@pytest.mark.parametrize("decay,elem", [(lz.LIZARD_DECAY_LAGGED, 2), (lz.LIZARD_DECAY_MASKED, 4)])
+def test_reading_workspaces(lib, decay, elem):
+    """The lagged reading adds one moved gate per gate element (dtype), the masked one an
+    fp32 log gate product per element (and, in the backward, its gate term too)."""
+    f1 = lz.lizard_attn_fwd_workspace(dims(L=2048, decay=decay))
+    f2 = lz.lizard_attn_fwd_workspace(dims(L=4096, decay=decay))
+    assert f2 - f1 == 2048 * 8 * 128 * elem
+    assert f1 > lz.lizard_attn_fwd_workspace(dims(L=2048))
+    b1 = lz.lizard_attn_bwd_workspace(dims(L=2048, B=8, decay=decay))
+    b2 = lz.lizard_attn_bwd_workspace(dims(L=4096, B=8, decay=decay))
+    per_gate = elem if decay == lz.LIZARD_DECAY_LAGGED else 2 * elem
+    assert b2 - b1 == 8 * 2048 * 8 * 128 * (4 + per_gate) + 2 * 8 * 2048 * 32 * 4
+    # decode: the status word plus one value per (sequence, KV head, feature)
+    assert lz.lizard_decode_workspace(dims(L=1, B=64, decay=decay)) == 256 + 64 * 8 * 128 * elem
+    assert lz.lizard_decode_workspace(dims(L=1, B=64)) == 256
+
+
+def test_tensor_core_path_by_reading(lib):
+    """The masked reading runs the SIMT walk; the lagged one keeps the tensor-core path."""
+    if lz.lizard_attn_fwd_kernel(dims()) != 1:
+        pytest.skip("the driver's TMA encoder is not available here")
+    assert lz.lizard_attn_fwd_kernel(dims(decay=lz.LIZARD_DECAY_LAGGED)) == 1
+    assert lz.lizard_attn_fwd_kernel(dims(decay=lz.LIZARD_DECAY_MASKED)) == 0
 
 
 def test_workspace_constant_in_L(lib):
@@ -67,7 +108,7 @@ def test_workspace_constant_in_L(lib):
 
 @pytest.mark.parametrize("bad", [dict(Hq=30), dict(D=127), dict(w=0), dict(M=-1), dict(M=65),
                                  dict(chunk=32), dict(dtype=7), dict(L=0), dict(B=0),
-                                 dict(scale=-1.0)])
+                                 dict(scale=-1.0), dict(decay=3), dict(decay=-1)])
 def test_invalid_dims_rejected(lib, bad):
     d = dims(**bad)
     assert lz.lizard_attn_fwd_workspace(d) == 0
@@ -93,8 +134,13 @@ def test_null_and_misaligned_pointers_rejected(lib):
     st = _no_device_calls()
     bad = lz.LIZARD_ERR_INVALID_ARG
     for case in ("fwd_null_q", "fwd_misaligned_v", "fwd_S_without_z", "fwd_misaligned_ws",
-                 "noalloc_misaligned", "dec_neg_pos", "dec_misaligned"):
+                 "noalloc_misaligned", "dec_neg_pos", "dec_misaligned", "fwd_bad_decay",
+                 "dec_masked_no_gcache", "dec_masked_mis_gcache", "dec_lagged_no_gcache",
+                 "dec_lagged_mis_gcache", "gfill_null", "gfill_mis", "gfill_bad_dims"):
         assert st[case] == bad, (case, st[case])
+    assert st["dec_masked_small_ws"] == lz.LIZARD_ERR_WORKSPACE
+    assert st["dec_lagged_small_ws"] == lz.LIZARD_ERR_WORKSPACE
+    assert st["dec_delayed_no_gcache"] == lz.LIZARD_ERR_CUDA  # passes every check
     assert st["fwd_unsupported"] == lz.LIZARD_ERR_UNSUPPORTED
     assert st["fwd_small_ws"] == lz.LIZARD_ERR_WORKSPACE
     assert st["dec_w300"] == lz.LIZARD_ERR_UNSUPPORTED
@@ -116,7 +162,7 @@ def test_null_pointer_checks_in_process(lib):
         lz.LIZARD_ERR_INVALID_ARG
     assert lib.lizard_attn_bwd(ctypes.byref(d), *([None] * 16), 1 << 30, None) == \
         lz.LIZARD_ERR_INVALID_ARG
-    assert lib.lizard_decode_step(ctypes.byref(d), 0, *([None] * 12), 256, None) == \
+    assert lib.lizard_decode_step(ctypes.byref(d), 0, *([None] * 13), 256, None) == \
         lz.LIZARD_ERR_INVALID_ARG
 
 

@@ -1,0 +1,271 @@
+"""Parity of the two other decay readings, through the C ABI, against the float64 oracle.
+
+The Lizard summary (gist.science 2507.09025, sec. 2-A-1) says the gate decays a state of the
+tokens outside the window, not which gates such a key has seen.  Beside the delayed-key
+reading the library runs the masked full-GLA reading (key j <= i - w weighed by
+prod_{s=j+1..i} Gamma_s) and the lagged state (prod_{s=j+1..i-w} Gamma_s), selected by
+lizard_dims.decay; the oracle's recurrence takes the same switch.  Forward (both paths),
+packed batches, strongly closed gates, backward and decode through the gate ring.
+"""
+import numpy as np
+import pytest
+
+from gated_linear_sliding_gb300 import inputs as I
+from helpers import assert_grad, assert_parity, rel_l2, to_dev, to_np
+from oracle import LAGGED, MASKED
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+READINGS = [pytest.param(MASKED, id="masked"), pytest.param(LAGGED, id="lagged")]
+
+
+@pytest.fixture(scope="module")
+def lz():
+    from gated_linear_sliding_gb300 import lizard
+
+    lizard.load()
+    return lizard
+
+
+def gpu_fwd(lz, inp, wl, reading, lse=False):
+    t = to_dev(inp, wl.dtype)
+    B, L, Hq, d = inp["q"].shape
+    kw = dict(S_out=torch.empty(B, wl.Hkv, wl.D, d, dtype=torch.float32, device="cuda"),
+              z_out=torch.empty(B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda"))
+    if lse:
+        kw["lse"] = torch.empty(B, L, Hq, dtype=torch.float32, device="cuda")
+    y = lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w,
+                           decay=reading, **kw)
+    torch.cuda.synchronize()
+    out = {"y": to_np(y)}
+    out.update({n: to_np(v) for n, v in kw.items()})
+    return out
+
+
+def check_fwd(lz, oracle_mod, wl, reading, L=None, B=None, scale=None):
+    inp = I.make_inputs(wl, L=L, B=B)
+    out = gpu_fwd(lz, inp, wl, reading)
+    ref = oracle_mod.fwd(**inp, w=wl.w, scale=scale, state=True, reading=reading)
+    sdt = "f32" if wl.dtype == "f32" else "bf16"
+    assert_parity(out["y"], ref["y"], wl.dtype, "y")
+    assert_parity(out["S_out"], ref["S"], sdt, "S")
+    assert_parity(out["z_out"], ref["z"], sdt, "z")
+    return inp, out, ref
+
+
+@pytest.mark.parametrize("reading", READINGS)
+@pytest.mark.parametrize("L,w", [(300, 8), (517, 64), (1100, 100), (40, 64)])
+def test_fwd_f32(lz, oracle_mod, reading, L, w):
+    check_fwd(lz, oracle_mod, I.TINY_F32.replace(L=L, w=w, Hq=4, Hkv=2, B=2), reading)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_fwd_f32_gla_sensitive_tells_readings_apart(lz, oracle_mod, reading):
+    """Slow gates and peaked phi: the state carries real weight, and each reading's output
+    differs from the delayed one's by more than ten times the fp32 tolerance (gates this
+    close to 1 bring the readings together: the lagged one differs by ~3e-4), so the parity
+    above is not vacuous."""
+    wl = I.gla_sensitive(I.TINY_F32.replace(L=640, Hq=4, Hkv=2, w=16))
+    inp, out, ref = check_fwd(lz, oracle_mod, wl, reading, scale=wl.scale)
+    other = oracle_mod.fwd(**inp, w=wl.w, scale=wl.scale)["y"]
+    assert rel_l2(ref["y"], other) > 10 * 1e-5
+    assert rel_l2(out["y"], other) > 10 * 1e-5
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_fwd_llama_shape(lz, oracle_mod, reading):
+    """LLaMA-shaped heads at L = 1100 (several segments, a ragged last step): the lagged
+    reading runs the tensor-core walk on the moved gates, the masked one the SIMT walk."""
+    wl = I.LLAMA3_8B_L8K
+    dims = lz.make_dims(1, 1100, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, lz.LIZARD_BF16,
+                        decay=reading)
+    assert lz.lizard_attn_fwd_kernel(dims) == (1 if reading == LAGGED else 0)
+    check_fwd(lz, oracle_mod, wl, reading, L=1100)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_fwd_llama_gla_sensitive(lz, oracle_mod, reading):
+    wl = I.gla_sensitive(I.LLAMA3_8B_L8K)
+    check_fwd(lz, oracle_mod, wl, reading, L=700, scale=wl.scale)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_fwd_closed_gates(lz, oracle_mod, reading):
+    """Runs of strongly closed gates: the lagged reading's moved gates take the tensor-core
+    walk's hand-over to the exact walk at the moved positions."""
+    check_fwd(lz, oracle_mod, I.closed_gates(I.LLAMA3_8B_L8K, per_1k=6.0), reading, L=1600)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_fwd_varlen_packed(lz, oracle_mod, reading):
+    """A packed batch: the gates move within each sequence (lagged: one launch over all
+    sequences; masked: the sequences one after another), each equals its own forward."""
+    wl = I.LLAMA3_8B_L8K
+    lens = [1, 77, 0, 300, 1000, 130]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T = int(cu[-1])
+    inp = I.make_inputs(wl.replace(B=1, L=T))
+    t = to_dev(inp, wl.dtype)
+    nseq = len(lens)
+    S = torch.empty(nseq, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.empty(nseq, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    y = lz.lizard_attn_fwd_varlen(t["q"][0], t["k"][0], t["v"][0], t["g"][0], t["Wf"],
+                                  t["sinks"], wl.w, cu, S_out=S, z_out=z, decay=reading)
+    torch.cuda.synchronize()
+    y, S = to_np(y), to_np(S)
+    for i in range(nseq):
+        a, b = int(cu[i]), int(cu[i + 1])
+        if a == b:
+            assert not S[i].any()
+            continue
+        one = {n: (arr[:, a:b] if n in ("q", "k", "v", "g") else arr) for n, arr in inp.items()}
+        ref = oracle_mod.fwd(**one, w=wl.w, state=True, reading=reading)
+        assert_parity(y[a:b][None], ref["y"], "bf16", f"y of sequence {i}")
+        assert_parity(S[i][None], ref["S"], "bf16", f"S of sequence {i}")
+
+
+def test_noalloc_lagged_bit_identical(lz):
+    """The no-allocation forward runs the same kernels on the same moved gates."""
+    wl = I.LLAMA3_8B_L8K
+    t = to_dev(I.make_inputs(wl, L=900), wl.dtype)
+    args = (t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w)
+    a = lz.lizard_attn_fwd(*args, decay=LAGGED)
+    b = lz.lizard_attn_fwd_noalloc(*args, decay=LAGGED)
+    torch.cuda.synchronize()
+    assert lz.lizard_read_noalloc_status() == lz.LIZARD_OK
+    assert torch.equal(a, b)
+
+
+def gpu_fwd_bwd(lz, inp, wl, reading):
+    t = to_dev(inp, wl.dtype)
+    B, L, Hq, d = inp["q"].shape
+    lse = torch.empty(B, L, Hq, dtype=torch.float32, device="cuda")
+    y = lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w, lse=lse,
+                           decay=reading)
+    g = lz.lizard_attn_bwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], y, lse, t["dy"],
+                           wl.w, decay=reading)
+    torch.cuda.synchronize()
+    return {n: to_np(v) for n, v in g.items()}
+
+
+def check_bwd(lz, oracle_mod, wl, reading, L=None, B=None, scale=None):
+    inp = I.make_inputs(wl, L=L, B=B, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w,
+                         scale=scale, reading=reading)
+    out = gpu_fwd_bwd(lz, inp, wl, reading)
+    for n in ("dq", "dk", "dv", "dg", "dWf", "dsinks"):
+        assert_grad(out[n], ref[n], wl.dtype, n)
+    return out, ref
+
+
+@pytest.mark.parametrize("reading", READINGS)
+@pytest.mark.parametrize("L,w", [(300, 16), (257, 5), (100, 64)])
+def test_bwd_f32(lz, oracle_mod, reading, L, w):
+    check_bwd(lz, oracle_mod, I.TINY_F32.replace(L=L, w=w, B=2, Hq=4, Hkv=2), reading)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_bwd_f32_gla_sensitive(lz, oracle_mod, reading):
+    wl = I.gla_sensitive(I.TINY_F32.replace(L=400, Hq=4, Hkv=2, w=16))
+    out, ref = check_bwd(lz, oracle_mod, wl, reading, scale=wl.scale)
+    assert np.abs(ref["dg"]).max() > 1e-3
+    if reading == LAGGED:  # the last w gates decay nothing a query reads
+        assert not out["dg"][:, wl.L - wl.w:].any()
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_bwd_mistral_shape(lz, oracle_mod, reading):
+    check_bwd(lz, oracle_mod, I.MISTRAL_7B_TRAIN, reading, L=520, B=2)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_bwd_mistral_gla_sensitive(lz, oracle_mod, reading):
+    wl = I.gla_sensitive(I.MISTRAL_7B_TRAIN)
+    check_bwd(lz, oracle_mod, wl, reading, L=640, B=1, scale=wl.scale)
+
+
+def test_bwd_lagged_closed_gates(lz, oracle_mod):
+    """Closed-gate runs under the lagged reading: the tensor-core walks leave the flagged
+    segments (flagged on the moved gates) to the exact SIMT walks."""
+    check_bwd(lz, oracle_mod, I.closed_gates(I.MISTRAL_7B_TRAIN, per_1k=6.0), LAGGED, L=900, B=1)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+@pytest.mark.parametrize("dtype,d,D,G,w", [("f32", 64, 64, 2, 5), ("bf16", 128, 128, 4, 64)])
+def test_decode_after_prefill(lz, oracle_mod, reading, dtype, d, D, G, w):
+    """Prefill L0 tokens (state, k/v rings, gate ring), then decode the rest one token at a
+    time through the gate ring: every step equals the oracle's prefill of the whole
+    sequence under the same reading, and so does the final state."""
+    L0, L = 150, 230
+    base = I.LLAMA3_8B_L8K if dtype == "bf16" else I.TINY_F32
+    wl = base.replace(B=3, L=L, d=d, D=D, Hkv=2, Hq=2 * G, w=w, dtype=dtype)
+    inp = I.make_inputs(wl)
+    ref = oracle_mod.fwd(**inp, w=w, state=True, reading=reading)
+    t = to_dev(inp, dtype)
+    tdt = t["q"].dtype
+    pre = {n: (t[n][:, :L0].contiguous() if n in ("q", "k", "v", "g") else t[n]) for n in t}
+    S = torch.empty(wl.B, wl.Hkv, D, d, dtype=torch.float32, device="cuda")
+    z = torch.empty(wl.B, wl.Hkv, D, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(wl.B, wl.Hkv, w + 1, d, dtype=tdt, device="cuda")
+    vc = torch.zeros_like(kc)
+    gc = torch.zeros(wl.B, wl.Hkv, w + 1, D, dtype=tdt, device="cuda")
+    y0 = lz.lizard_attn_fwd(pre["q"], pre["k"], pre["v"], pre["g"], t["Wf"], t["sinks"], w,
+                            S_out=S, z_out=z, kcache_out=kc, vcache_out=vc, decay=reading)
+    lz.lizard_gate_cache_fill(pre["g"], gc, w)
+    dims = lz.make_dims(wl.B, 1, wl.Hq, wl.Hkv, d, D, w, wl.M, tdt, decay=reading)
+    ws = lz.new_workspace(lz.lizard_decode_workspace(dims), "cuda")
+    ys = []
+    for pos in range(L0, L):
+        ys.append(lz.lizard_decode_step(
+            pos, t["q"][:, pos].contiguous(), t["k"][:, pos].contiguous(),
+            t["v"][:, pos].contiguous(), t["g"][:, pos].contiguous(), t["Wf"], t["sinks"], S, z,
+            kc, vc, w, workspace=ws, gcache=gc, decay=reading))
+    torch.cuda.synchronize()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    assert_parity(to_np(y0), ref["y"][:, :L0], dtype, "prefill y")
+    assert_parity(to_np(torch.stack(ys, 1)), ref["y"][:, L0:], dtype, "decode y")
+    sdt = "f32" if dtype == "f32" else "bf16"
+    assert_parity(to_np(S), ref["S"], sdt, "S")
+    assert_parity(to_np(z), ref["z"], sdt, "z")
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_decode_positions_from_scratch(lz, oracle_mod, reading):
+    """Per-sequence positions (sequences started at different steps, one not yet started):
+    each sequence's outputs follow the oracle from its own position 0."""
+    wl = I.LLAMA3_8B_L8K.replace(B=3, L=90, Hq=8, Hkv=2)
+    inp = I.make_inputs(wl)
+    t = to_dev(inp, wl.dtype)
+    tdt = t["q"].dtype
+    B, w, d, D = wl.B, wl.w, wl.d, wl.D
+    S = torch.zeros(B, wl.Hkv, D, d, dtype=torch.float32, device="cuda")
+    z = torch.zeros(B, wl.Hkv, D, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(B, wl.Hkv, w + 1, d, dtype=tdt, device="cuda")
+    vc = torch.zeros_like(kc)
+    gc = torch.zeros(B, wl.Hkv, w + 1, D, dtype=tdt, device="cuda")
+    start = [0, 7, 20]  # sequence b decodes its token p at loop step start[b] + p
+    dims = lz.make_dims(B, 1, wl.Hq, wl.Hkv, d, D, w, wl.M, tdt, decay=reading)
+    ws = lz.new_workspace(lz.lizard_decode_workspace(dims), "cuda")
+    outs = {b: [] for b in range(B)}
+    for stepi in range(wl.L + max(start)):
+        p = [stepi - s for s in start]
+        # a sequence not started or already finished takes position -1: left untouched, the
+        # error noted in the status word
+        pos = torch.tensor([pp if 0 <= pp < wl.L else -1 for pp in p], dtype=torch.int64,
+                           device="cuda")
+        idx = [min(max(pp, 0), wl.L - 1) for pp in p]
+        tok = {n: torch.stack([t[n][b, idx[b]] for b in range(B)]).contiguous()
+               for n in ("q", "k", "v", "g")}
+        y = lz.lizard_decode_step_positions(pos, tok["q"], tok["k"], tok["v"], tok["g"], t["Wf"],
+                                            t["sinks"], S, z, kc, vc, w, workspace=ws, gcache=gc,
+                                            decay=reading)
+        for b in range(B):
+            if 0 <= p[b] < wl.L:
+                outs[b].append(y[b])
+    torch.cuda.synchronize()
+    lz.lizard_read_device_status(ws)  # clears the noted negative positions
+    ref = oracle_mod.fwd(**inp, w=w, reading=reading)["y"]
+    for b in range(B):
+        assert_parity(to_np(torch.stack(outs[b], 0))[None], ref[b:b + 1], "bf16", f"seq {b}")
