@@ -41,6 +41,7 @@ def parse():
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--no-proj", action="store_true")
     ap.add_argument("--no-varlen", action="store_true")
+    ap.add_argument("--no-readings", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -448,6 +449,9 @@ def run_ours(args, rank, world, device):
     varlen = None
     if not args.no_varlen:
         varlen = run_varlen(args, device, lz, I)
+    readings = None
+    if not args.no_readings:
+        readings = run_readings(args, device, lz, I)
     clocks = sampler.stop()
 
     tokens = wl.B * wl.L
@@ -494,6 +498,8 @@ def run_ours(args, rank, world, device):
         out["projection"] = proj
     if varlen is not None:
         out["varlen"] = varlen
+    if readings is not None:
+        out["decay_readings"] = readings
     return out
 
 
@@ -686,6 +692,118 @@ def run_varlen(args, device, lz, I):
                          "algorithmic_bytes": ab, "peak_source": peak_src,
                          "scope": "whole forward"},
             "timing": "CUDA events, 512 MiB L2 flush before each call, mean of 5"}
+
+
+def run_readings(args, device, lz, I):
+    """The two other decay readings next to the delayed-key one, on the same workloads: the
+    LLaMA-shaped forward (L = 8192), the Mistral-shaped forward + backward (B = 8, L = 2048)
+    and the B = 64 decode step (state and rings from a 2048-token prefill; a step's cost does
+    not depend on the context length).  L2 flushed before every timed call, mean of n."""
+    import torch
+
+    hbm_peak, _, peak_src = load_peaks()
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    names = {lz.LIZARD_DECAY_DELAYED: "delayed", lz.LIZARD_DECAY_MASKED: "masked",
+             lz.LIZARD_DECAY_LAGGED: "lagged"}
+
+    def timed(fn, n):
+        fn()
+        torch.cuda.synchronize()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for e0, e1 in evs:
+            flush.zero_()
+            e0.record()
+            fn()
+            e1.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / n
+
+    out = {"timing": "CUDA events, 512 MiB L2 flush before each call, mean of 5 (forward, "
+                     "decode) or 3 (backward)",
+           "peak_source": peak_src}
+    # forward, LLaMA-shaped
+    wl = I.LLAMA3_8B_L8K
+    t = I.make_device_inputs(wl, device)
+    y = torch.empty_like(t["q"])
+    fb = fwd_algorithmic_bytes(wl)
+    fwd = {}
+    for code, name in names.items():
+        dims = lz.dims_of(t["q"], t["k"], t["g"], t["sinks"], wl.w, decay=code)
+        ws = lz.new_workspace(lz.lizard_attn_fwd_workspace(dims), device)
+        ms = timed(lambda: lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"],
+                                              t["sinks"], wl.w, y=y, workspace=ws, decay=code), 5)
+        fwd[name] = {"ms": ms, "tokens_per_s": wl.B * wl.L / (ms * 1e-3),
+                     "path": "tcgen05" if lz.lizard_attn_fwd_kernel(dims) == 1 else "SIMT",
+                     "hbm_frac_whole_forward": fb / (ms * 1e-3) / 1e9 / hbm_peak}
+    out["forward"] = {"workload": wl.name, "algorithmic_bytes": fb, **fwd}
+    del t, y
+    # forward + backward, Mistral-shaped
+    wl = I.MISTRAL_7B_TRAIN
+    t = I.make_device_inputs(wl, device, with_dy=True)
+    y = torch.empty_like(t["q"])
+    lse = torch.empty(wl.B, wl.L, wl.Hq, dtype=torch.float32, device=device)
+    grads = dict(dq=torch.empty_like(t["q"]), dk=torch.empty_like(t["k"]),
+                 dv=torch.empty_like(t["v"]), dg=torch.empty_like(t["g"]),
+                 dWf=torch.empty(wl.Hkv, wl.d, wl.D // 2, device=device),
+                 dsinks=torch.empty(wl.Hq, wl.M, device=device))
+    bb = bwd_algorithmic_bytes(wl)
+    bwd = {}
+    for code, name in names.items():
+        dims = lz.dims_of(t["q"], t["k"], t["g"], t["sinks"], wl.w, decay=code)
+        wsf = lz.new_workspace(lz.lizard_attn_fwd_workspace(dims), device)
+        wsb = lz.new_workspace(lz.lizard_attn_bwd_workspace(dims), device)
+        lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w, y=y,
+                           lse=lse, workspace=wsf, decay=code)
+        ms_f = timed(lambda: lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"],
+                                                t["sinks"], wl.w, y=y, lse=lse, workspace=wsf,
+                                                decay=code), 3)
+        ms_b = timed(lambda: lz.lizard_attn_bwd(t["q"], t["k"], t["v"], t["g"], t["Wf"],
+                                                t["sinks"], y, lse, t["dy"], wl.w, workspace=wsb,
+                                                decay=code, **grads), 3)
+        bwd[name] = {"fwd_ms": ms_f, "bwd_ms": ms_b,
+                     "tokens_per_s": wl.B * wl.L / ((ms_f + ms_b) * 1e-3),
+                     "bwd_hbm_frac": bb / (ms_b * 1e-3) / 1e9 / hbm_peak}
+        del wsf, wsb
+    out["train"] = {"workload": wl.name, "bwd_algorithmic_bytes": bb, **bwd}
+    del t, y, lse, grads
+    # decode step, B = 64
+    wl = I.DECODE_B64
+    T0, n = 2048, 32
+    B, Hq, Hkv, d, D, w = wl.B, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w
+    pre = I.make_device_inputs(wl, device, L=T0, B=B)
+    nxt = I.make_device_inputs(wl, device, L=n + 1, B=B, seed_offset=1)
+    tok = {x: nxt[x].transpose(0, 1).contiguous() for x in ("q", "k", "v", "g")}
+    db = decode_algorithmic_bytes(wl)
+    dec = {}
+    for code, name in names.items():
+        S = torch.empty(B, Hkv, D, d, dtype=torch.float32, device=device)
+        z = torch.empty(B, Hkv, D, dtype=torch.float32, device=device)
+        kc = torch.zeros(B, Hkv, w + 1, d, dtype=torch.bfloat16, device=device)
+        vc = torch.zeros_like(kc)
+        gc = torch.zeros(B, Hkv, w + 1, D, dtype=torch.bfloat16, device=device)
+        lz.lizard_attn_fwd(pre["q"], pre["k"], pre["v"], pre["g"], pre["Wf"], pre["sinks"], w,
+                           S_out=S, z_out=z, kcache_out=kc, vcache_out=vc, decay=code)
+        lz.lizard_gate_cache_fill(pre["g"], gc, w)
+        dims = lz.make_dims(B, 1, Hq, Hkv, d, D, w, wl.M, torch.bfloat16, decay=code)
+        ws = lz.new_workspace(lz.lizard_decode_workspace(dims), device)
+        Y = torch.empty(B, Hq, d, dtype=torch.bfloat16, device=device)
+        pos = [T0]
+
+        def step():
+            i = pos[0] - T0
+            lz.lizard_decode_step(pos[0], tok["q"][i], tok["k"][i], tok["v"][i], tok["g"][i],
+                                  pre["Wf"], pre["sinks"], S, z, kc, vc, w, y=Y, workspace=ws,
+                                  gcache=gc, decay=code)
+            pos[0] += 1
+
+        ms = timed(step, n)
+        if lz.lizard_read_device_status(ws) != lz.LIZARD_OK:
+            raise RuntimeError(f"decode ({name}) device status")
+        dec[name] = {"ms_per_step": ms, "steps_per_s": 1e3 / ms,
+                     "hbm_frac": db / (ms * 1e-3) / 1e9 / hbm_peak}
+    out["decode"] = {"workload": wl.name, "prefill": T0, "algorithmic_bytes": db, **dec}
+    return out
 
 
 def run_long(args, device, lz, I):

@@ -84,33 +84,56 @@ __global__ void __launch_bounds__(128) key_decay_kernel(Plan p, const T* __restr
     }
 }
 
-// The gate-ring step of a MASKED or LAGGED decode, one thread per (unit, feature): reads the
-// ring before the new gate goes to slot pos mod (w+1) (the slots read are other slots).
+// The gate-ring step of a MASKED or LAGGED decode: one CTA per (sequence, KV head) unit, RP
+// threads per feature (thread = part * D + f).  The ring is read before the new gate row goes
+// to slot pos mod (w+1) (the slots read are other slots).  The masked reading's sum over the
+// window splits into RP contiguous runs of slots, added in a fixed order.
+constexpr int RP = 4;
+
 template <typename T>
 __global__ void decode_ring_kernel(Plan p, int64_t pos_all, const int64_t* pos_dev,
                                    const T* __restrict__ g, T* __restrict__ gc, void* out) {
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= p.B * p.Hkv * p.D) return;
-    const int64_t unit = e / p.D, f = e % p.D, b = unit / p.Hkv;
+    __shared__ float part_sum[RP][128];
+    const int64_t unit = blockIdx.x, b = unit / p.Hkv;
+    const int f = (int)(threadIdx.x % p.D), part = (int)(threadIdx.x / p.D);
     const int64_t pos = pos_dev != nullptr ? pos_dev[b] : pos_all;
     if (pos < 0) return;  // the decode kernel reports it and leaves the sequence untouched
-    const int64_t w = p.w, R = w + 1;
+    const int64_t w = p.w, R = w + 1, e = unit * p.D + f;
     T* gu = gc + unit * R * p.D + f;
     const T gnew = g[e];
     if (p.decay == LIZARD_DECAY_LAGGED) {
         // the step decays by the gate of token pos - w; before that the state is empty
-        if (pos >= w) ((T*)out)[e] = gu[((pos - w) % R) * p.D];
-        else st((T*)out + e, kOpenGate);
+        if (part == 0) {
+            if (pos >= w) ((T*)out)[e] = gu[((pos - w) % R) * p.D];
+            else st((T*)out + e, kOpenGate);
+        }
     } else {
-        // token pos - w enters scaled by prod_{s=pos-w+1..pos} Gamma_s
+        // token pos - w enters scaled by prod_{s=pos-w+1..pos} Gamma_s: this thread sums the
+        // slots of its run of tokens pos-w+1 .. pos-1, stepping the slot without a division
         float acc = 0.0f;
         if (pos >= w) {
-            for (int64_t s = pos - w + 1; s < pos; ++s) acc += log_sigmoid<false>(ld(gu + (s % R) * p.D));
-            acc += log_sigmoid<false>(ld(&gnew));
+            const int64_t n = w - 1, per = (n + RP - 1) / RP;
+            const int64_t s0 = pos - w + 1 + part * per, s1 = min64(pos, s0 + per);
+            int slot = s0 < s1 ? (int)(s0 % R) : 0;
+#pragma unroll 4
+            for (int64_t s = s0; s < s1; ++s) {
+                acc += log_sigmoid<false>(ld(gu + (int64_t)slot * p.D));
+                slot = slot + 1 == (int)R ? 0 : slot + 1;
+            }
         }
-        ((float*)out)[e] = acc;
+        part_sum[part][f] = acc;
+        __syncthreads();
+        if (part == 0) {
+            float tot = 0.0f;
+            if (pos >= w) {
+#pragma unroll
+                for (int k = 0; k < RP; ++k) tot += part_sum[k][f];
+                tot += log_sigmoid<false>(ld(&gnew));
+            }
+            ((float*)out)[e] = tot;
+        }
     }
-    gu[(pos % R) * p.D] = gnew;
+    if (part == 0) gu[(pos % R) * p.D] = gnew;
 }
 
 template <typename T>
@@ -179,13 +202,13 @@ cudaError_t launch_key_decay(const Plan& p, const void* g, float* kd, cudaStream
 }
 
 cudaError_t launch_decode_ring(const Plan& p, const DecodeArgs& a, void* out, cudaStream_t s) {
-    const int64_t n = p.B * p.Hkv * p.D;
-    const unsigned grid = (unsigned)((n + 255) / 256);
+    if (p.D > 128) return cudaErrorInvalidValue;  // the per-part sums hold 128 features
+    const unsigned grid = (unsigned)(p.B * p.Hkv), block = (unsigned)(RP * p.D);
     if (p.dtype == LIZARD_F32)
-        decode_ring_kernel<float><<<grid, 256, 0, s>>>(p, a.pos, a.pos_dev, (const float*)a.g,
-                                                       (float*)a.gc, out);
+        decode_ring_kernel<float><<<grid, block, 0, s>>>(p, a.pos, a.pos_dev, (const float*)a.g,
+                                                         (float*)a.gc, out);
     else
-        decode_ring_kernel<__nv_bfloat16><<<grid, 256, 0, s>>>(
+        decode_ring_kernel<__nv_bfloat16><<<grid, block, 0, s>>>(
             p, a.pos, a.pos_dev, (const __nv_bfloat16*)a.g, (__nv_bfloat16*)a.gc, out);
     return cudaGetLastError();
 }
