@@ -37,7 +37,8 @@ constexpr int KB = 16;  // window keys per tile in the query-side walk
 // Workspace regions (floats, each 64-float aligned)
 struct BwdWs {
     size_t fwd_rec, rev_rec, dB, tot, dW, dt, rows, flags;
-    size_t gl, kd, kk;  // decay readings: moved gates (LAGGED); key log products and gate terms (MASKED)
+    size_t gl, kd, kk, kt;  // decay readings: moved gates (LAGGED); key log products, their gate
+                            // terms and the terms' chunk totals (MASKED)
     size_t total;
 };
 
@@ -70,6 +71,8 @@ BwdWs bwd_layout(const Plan& p) {
     if (p.decay == LIZARD_DECAY_MASKED) off += al64(ng);
     w.kk = off;  // MASKED: phi(k') (.) dphi(k') of each key, at the key's own row
     if (p.decay == LIZARD_DECAY_MASKED) off += al64(ng);
+    w.kt = off;  // MASKED: chunk totals of those terms (their suffix sums)
+    if (p.decay == LIZARD_DECAY_MASKED) off += al64(key_suffix_scratch_floats(p));
     w.total = off * sizeof(float);
     return w;
 }
@@ -1044,28 +1047,41 @@ __global__ void bwd_tot_suffix(Plan p, float* tot) {
     }
 }
 
-// dWf[kv] = sum over batch, segments and both walks (fixed order); dsinks likewise.
-__global__ void bwd_reduce(Plan p, BwdArgs a, BwdWs ws) {
+// dWf[kv] = sum over batch, segments and both walks (fixed order); dsinks likewise.  Each
+// dWf entry takes four threads, thread `part` summing the segments sg = part mod 4 of both
+// walks (so four times as many loads are in flight), added in a fixed order.
+constexpr int kRedCols = 64, kRedParts = 4;
+
+__global__ void __launch_bounds__(kRedCols * kRedParts) bwd_reduce(Plan p, BwdArgs a, BwdWs ws) {
+    __shared__ float part_sum[kRedParts][kRedCols];
     const int64_t nW = p.d * (p.D / 2);
-    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const int col = threadIdx.x % kRedCols, part = threadIdx.x / kRedCols;
+    const int64_t e = (int64_t)blockIdx.x * kRedCols + col;
     const float* wsf = (const float*)a.ws;
     const int64_t U = p.B * p.Hkv;
-    if (e < p.Hkv * nW) {
+    const bool has = e < p.Hkv * nW;
+    float sum = 0.0f;
+    if (has) {
         const int64_t kv = e / nW, x = e % nW;
-        float s = 0.0f;
+        const size_t bs = (size_t)p.Hkv * (size_t)nW;
         for (int w2 = 0; w2 < 2; ++w2)
-            for (int64_t sg = 0; sg < p.P; ++sg)
-                for (int64_t b = 0; b < p.B; ++b)
-                    s += wsf[ws.dW + ((size_t)(w2 * p.Pmax + sg) * U + b * p.Hkv + kv) * nW + x];
-        a.dWf[e] = s;
+            for (int64_t sg = part; sg < p.P; sg += kRedParts) {
+                const float* src = wsf + ws.dW + ((size_t)(w2 * p.Pmax + sg) * U + kv) * nW + x;
+                for (int64_t b = 0; b < p.B; ++b) sum += src[b * bs];
+            }
     }
-    if (e < p.Hq * p.M && a.dsinks != nullptr) {
-        const int64_t h = e / p.M, kv = h / p.G, hh = h % p.G;
+    part_sum[part][col] = sum;
+    __syncthreads();
+    if (has && part == 0)
+        a.dWf[e] = (part_sum[0][col] + part_sum[1][col]) + (part_sum[2][col] + part_sum[3][col]);
+    const int64_t et = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (et < p.Hq * p.M && a.dsinks != nullptr) {
+        const int64_t h = et / p.M, kv = h / p.G, hh = h % p.G;
         float s = 0.0f;
         for (int64_t sg = 0; sg < p.P; ++sg)
             for (int64_t b = 0; b < p.B; ++b)
                 s += wsf[ws.dt + ((size_t)sg * U + b * p.Hkv + kv) * p.G + hh];
-        a.dsinks[e] = -expf(a.sinks[e]) * s;
+        a.dsinks[et] = -expf(a.sinks[et]) * s;
     }
 }
 
@@ -1176,13 +1192,16 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a_in, cudaStream_t s) {
     // 6. dg, then the reductions
     const int64_t ng = p.B * p.L * p.Hkv * p.D;
     if (a.kkey != nullptr) {
-        e = launch_key_suffix(p, a.kkey, s);
+        e = launch_key_suffix(p, a.kkey, wsf + ws.kt, s);
         if (e != cudaSuccess) return e;
     }
     bwd_tot_suffix<<<(unsigned)((U * p.D + 255) / 256), 256, 0, s>>>(p, wsf + ws.tot);
     bwd_gates<T><<<(unsigned)((ng / 8 + 255) / 256), 256, 0, s>>>(p, a, ws);
-    const int64_t nr = max64(p.Hkv * p.d * (p.D / 2), p.Hq * p.M);
-    bwd_reduce<<<(unsigned)((nr + 255) / 256), 256, 0, s>>>(p, a, ws);
+    // dWf: kRedCols entries per block; dsinks: one entry per thread of the same blocks
+    const int64_t nW = p.d * (p.D / 2);
+    const int64_t nb = max64((p.Hkv * nW + kRedCols - 1) / kRedCols,
+                             (p.Hq * p.M + kRedCols * kRedParts - 1) / (kRedCols * kRedParts));
+    bwd_reduce<<<(unsigned)nb, kRedCols * kRedParts, 0, s>>>(p, a, ws);
     return cudaGetLastError();
 }
 

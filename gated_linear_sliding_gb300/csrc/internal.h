@@ -91,8 +91,10 @@ cudaError_t launch_key_decay(const Plan& p, const void* g, float* kd, cudaStream
 cudaError_t launch_gate_ring_fill(const Plan& p, const void* g, void* gc, cudaStream_t s);
 // Reverse cumulative sum over the rows of each (batch, KV head, feature) column of the
 // MASKED backward's key-side gate terms, in place; rows past L - 1 - w (keys that never
-// enter the state, not written by the walk) count as zero.
-cudaError_t launch_key_suffix(const Plan& p, float* kk, cudaStream_t s);
+// enter the state, not written by the walk) count as zero.  kt: key_suffix_scratch_floats(p)
+// floats of chunk totals.
+size_t key_suffix_scratch_floats(const Plan& p);
+cudaError_t launch_key_suffix(const Plan& p, float* kk, float* kt, cudaStream_t s);
 
 cudaError_t launch_fwd_simt(const Plan& p, const FwdArgs& a, cudaStream_t s);
 // Segment-start states only (segment pass + scan into a.seg), for the backward.

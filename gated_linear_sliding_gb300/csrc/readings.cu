@@ -57,7 +57,7 @@ __global__ void gate_lag_kernel(Plan p, const T* __restrict__ g, T* __restrict__
 // column (KV head x feature) per thread, a window sum slid one row at a time in fp64 (the
 // per-gate logarithms in fp32).  Threads of a block take consecutive columns, so every load
 // and store of a row is contiguous.  grid.x = column blocks x row blocks, grid.y = sequence.
-constexpr int KJ = 256;
+constexpr int KJ = 64;
 
 template <typename T>
 __global__ void __launch_bounds__(128) key_decay_kernel(Plan p, const T* __restrict__ g,
@@ -147,16 +147,32 @@ __global__ void gate_ring_fill_kernel(Plan p, const T* __restrict__ g, T* __rest
         gc[(unit * (p.w + 1) + slot) * p.D + c] = g[((b * p.L + t) * p.Hkv + kv) * p.D + c];
 }
 
-// Reverse cumulative sum of a column of key-side gate terms (rows past L - 1 - w are zero).
-__global__ void key_suffix_kernel(Plan p, float* kk) {
-    const int64_t HD = p.Hkv * p.D;
+// Reverse cumulative sum of each column of key-side gate terms (rows past L - 1 - w are zero),
+// in chunks of KS rows: first every chunk's total, then each chunk adds the totals of the
+// chunks after it (last first) and scans its own rows in reverse.  Fixed order throughout.
+constexpr int KS = 64;
+
+__global__ void key_chunk_total_kernel(Plan p, const float* __restrict__ kk, float* __restrict__ kt) {
+    const int64_t HD = p.Hkv * p.D, nch = (p.L + KS - 1) / KS;
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-    if (e >= p.B * HD) return;
-    const int64_t b = e / HD, col = e % HD;
-    float* x = kk + b * p.L * HD + col;
+    if (e >= p.B * nch * HD) return;
+    const int64_t col = e % HD, r = e / HD, chunk = r % nch, b = r / nch;
+    const int64_t j0 = chunk * KS, j1 = min64(min64(p.L, j0 + KS), p.L - p.w);
+    float s = 0.0f;
+    for (int64_t j = j0; j < j1; ++j) s += kk[(b * p.L + j) * HD + col];
+    kt[e] = s;
+}
+
+__global__ void key_suffix_kernel(Plan p, float* __restrict__ kk, const float* __restrict__ kt) {
+    const int64_t HD = p.Hkv * p.D, nch = (p.L + KS - 1) / KS;
+    const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (e >= p.B * nch * HD) return;
+    const int64_t col = e % HD, r = e / HD, chunk = r % nch, b = r / nch;
     float run = 0.0f;
-#pragma unroll 4
-    for (int64_t j = p.L - 1; j >= 0; --j) {
+    for (int64_t c = nch - 1; c > chunk; --c) run += kt[(b * nch + c) * HD + col];
+    const int64_t j0 = chunk * KS, j1 = min64(p.L, j0 + KS);
+    float* x = kk + b * p.L * HD + col;
+    for (int64_t j = j1 - 1; j >= j0; --j) {
         if (j <= p.L - 1 - p.w) run += x[j * HD];
         x[j * HD] = run;
     }
@@ -223,9 +239,14 @@ cudaError_t launch_gate_ring_fill(const Plan& p, const void* g, void* gc, cudaSt
     return cudaGetLastError();
 }
 
-cudaError_t launch_key_suffix(const Plan& p, float* kk, cudaStream_t s) {
-    const int64_t n = p.B * p.Hkv * p.D;
-    key_suffix_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, kk);
+size_t key_suffix_scratch_floats(const Plan& p) {
+    return (size_t)(p.B * ((p.L + KS - 1) / KS) * p.Hkv * p.D);
+}
+
+cudaError_t launch_key_suffix(const Plan& p, float* kk, float* kt, cudaStream_t s) {
+    const int64_t n = (int64_t)key_suffix_scratch_floats(p);
+    key_chunk_total_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, kk, kt);
+    key_suffix_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(p, kk, kt);
     return cudaGetLastError();
 }
 
