@@ -269,3 +269,138 @@ def test_decode_positions_from_scratch(lz, oracle_mod, reading):
     ref = oracle_mod.fwd(**inp, w=w, reading=reading)["y"]
     for b in range(B):
         assert_parity(to_np(torch.stack(outs[b], 0))[None], ref[b:b + 1], "bf16", f"seq {b}")
+
+
+# --- out-of-bounds write guard (the plain stand-in for the closed sanitizer) --------------
+
+from test_gpu_canary import Guarded, _ws  # noqa: E402
+
+
+@pytest.mark.parametrize("reading", READINGS)
+@pytest.mark.parametrize("path,L", [("tc", 33), ("tc", 1100), ("simt", 517)])
+def test_forward_writes_stay_in_bounds(lz, oracle_mod, reading, path, L):
+    """Every output and the workspace (its reading scratch included, at exactly the queried
+    size) sit in sentinel-filled slack that must stay untouched."""
+    wl = I.LLAMA3_8B_L8K if path == "tc" else I.TINY_F32.replace(Hq=4, Hkv=2, B=2)
+    inp = I.make_inputs(wl, L=L)
+    t = to_dev(inp, wl.dtype)
+    B, Hq, Hkv, d, D = inp["q"].shape[0], wl.Hq, wl.Hkv, wl.d, wl.D
+    dt = t["q"].dtype
+    g = Guarded()
+    y = g.empty((B, L, Hq, d), dt)
+    lse = g.empty((B, L, Hq), torch.float32)
+    S = g.empty((B, Hkv, D, d), torch.float32)
+    z = g.empty((B, Hkv, D), torch.float32)
+    kc = g.empty((B, Hkv, wl.w + 1, d), dt, like=torch.zeros(B, Hkv, wl.w + 1, d, dtype=dt))
+    vc = g.empty((B, Hkv, wl.w + 1, d), dt, like=torch.zeros(B, Hkv, wl.w + 1, d, dtype=dt))
+    dims = lz.dims_of(t["q"], t["k"], t["g"], t["sinks"], wl.w, decay=reading)
+    ws = _ws(lz, g, lz.lizard_attn_fwd_workspace(dims))
+    lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w, y=y, lse=lse,
+                       S_out=S, z_out=z, kcache_out=kc, vcache_out=vc, workspace=ws,
+                       decay=reading)
+    g.check()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    ref = oracle_mod.fwd(**inp, w=wl.w, state=True, reading=reading)
+    assert_parity(to_np(y), ref["y"], wl.dtype, "y")
+
+
+@pytest.mark.parametrize("reading", READINGS)
+@pytest.mark.parametrize("path,L", [("tc", 33), ("tc", 1000), ("simt", 517)])
+def test_backward_writes_stay_in_bounds(lz, oracle_mod, reading, path, L):
+    wl = I.MISTRAL_7B_TRAIN if path == "tc" else I.TINY_F32.replace(Hq=4, Hkv=2)
+    inp = I.make_inputs(wl, L=L, B=1, with_dy=True)
+    t = to_dev(inp, wl.dtype)
+    B, Hq, Hkv, d, D, M = 1, wl.Hq, wl.Hkv, wl.d, wl.D, wl.M
+    dt = t["q"].dtype
+    lse = torch.empty(B, L, Hq, device="cuda")
+    y = lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w, lse=lse,
+                           decay=reading)
+    g = Guarded()
+    out = dict(dq=g.empty((B, L, Hq, d), dt), dk=g.empty((B, L, Hkv, d), dt),
+               dv=g.empty((B, L, Hkv, d), dt), dg=g.empty((B, L, Hkv, D), dt),
+               dWf=g.empty((Hkv, d, D // 2), torch.float32),
+               dsinks=g.empty((Hq, M), torch.float32))
+    dims = lz.dims_of(t["q"], t["k"], t["g"], t["sinks"], wl.w, decay=reading)
+    ws = _ws(lz, g, lz.lizard_attn_bwd_workspace(dims))
+    lz.lizard_attn_bwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], y, lse, t["dy"],
+                       wl.w, workspace=ws, decay=reading, **out)
+    g.check()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w,
+                         reading=reading)
+    for n in ("dq", "dk", "dv", "dg", "dWf"):
+        assert_grad(to_np(out[n]), ref[n], wl.dtype, n)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_decode_writes_stay_in_bounds(lz, oracle_mod, reading):
+    """Decode from position 0 through and past the window (the gate ring wraps): the ring,
+    the state, y and the workspace at exactly the queried size stay in bounds."""
+    wl = I.LLAMA3_8B_L8K.replace(B=2, L=80, Hq=8, Hkv=2)
+    inp = I.make_inputs(wl)
+    t = to_dev(inp, wl.dtype)
+    B, Hq, Hkv, d, D, w = wl.B, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w
+    dt = t["q"].dtype
+    g = Guarded()
+    S = g.empty((B, Hkv, D, d), torch.float32, like=torch.zeros(B, Hkv, D, d))
+    z = g.empty((B, Hkv, D), torch.float32, like=torch.zeros(B, Hkv, D))
+    kc = g.empty((B, Hkv, w + 1, d), dt, like=torch.zeros(B, Hkv, w + 1, d, dtype=dt))
+    vc = g.empty((B, Hkv, w + 1, d), dt, like=torch.zeros(B, Hkv, w + 1, d, dtype=dt))
+    gc = g.empty((B, Hkv, w + 1, D), dt, like=torch.zeros(B, Hkv, w + 1, D, dtype=dt))
+    dims = lz.make_dims(B, 1, Hq, Hkv, d, D, w, wl.M, dt, decay=reading)
+    ws = _ws(lz, g, lz.lizard_decode_workspace(dims))
+    ys = []
+    for pos in range(wl.L):
+        y = g.empty((B, Hq, d), dt)
+        lz.lizard_decode_step(pos, t["q"][:, pos].contiguous(), t["k"][:, pos].contiguous(),
+                              t["v"][:, pos].contiguous(), t["g"][:, pos].contiguous(), t["Wf"],
+                              t["sinks"], S, z, kc, vc, w, y=y, workspace=ws, gcache=gc,
+                              decay=reading)
+        ys.append(y)
+    g.check()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    ref = oracle_mod.fwd(**inp, w=w, reading=reading)["y"]
+    assert_parity(to_np(torch.stack(ys, 1)), ref, "bf16", "decode y")
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_bwd_varlen_packed(lz, oracle_mod, reading):
+    """The packed backward under each reading: every sequence's gradients equal the oracle's
+    for that sequence alone; dWf sums over the sequences."""
+    wl = I.MISTRAL_7B_TRAIN
+    lens = [300, 0, 70, 513]
+    cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    T = int(cu[-1])
+    inp = I.make_inputs(wl.replace(B=1, L=T), with_dy=True)
+    t = to_dev(inp, wl.dtype)
+    packed = {n: t[n][0] for n in ("q", "k", "v", "g", "dy")}
+    lse = torch.empty(T, wl.Hq, dtype=torch.float32, device="cuda")
+    y = lz.lizard_attn_fwd_varlen(packed["q"], packed["k"], packed["v"], packed["g"], t["Wf"],
+                                  t["sinks"], wl.w, cu, lse=lse, decay=reading)
+    gr = lz.lizard_attn_bwd_varlen(packed["q"], packed["k"], packed["v"], packed["g"], t["Wf"],
+                                   t["sinks"], y, lse, packed["dy"], wl.w, cu, decay=reading)
+    torch.cuda.synchronize()
+    out = {n: to_np(v) for n, v in gr.items()}
+    dWf = np.zeros_like(out["dWf"])
+    for i in range(len(lens)):
+        a, b = int(cu[i]), int(cu[i + 1])
+        if a == b:
+            continue
+        one = {n: (arr[:, a:b] if n in ("q", "k", "v", "g", "dy") else arr)
+               for n, arr in inp.items()}
+        ref = oracle_mod.bwd(**{n: x for n, x in one.items() if n != "dy"}, dy=one["dy"],
+                             w=wl.w, reading=reading)
+        for n in ("dq", "dk", "dv", "dg"):
+            assert_grad(out[n][a:b][None], ref[n], "bf16", f"{n} of sequence {i}")
+        dWf += ref["dWf"]
+    assert_grad(out["dWf"], dWf, "bf16", "dWf")
+
+
+@pytest.mark.parametrize("reading", READINGS)
+@pytest.mark.parametrize("d,D,G,w", [(64, 128, 2, 1), (128, 64, 1, 3)])
+def test_fwd_bwd_small_windows_and_heads(lz, oracle_mod, reading, d, D, G, w):
+    """w = 1 (the lagged gates move one token; the masked factor is the next token's gate)
+    and the other compiled head sizes, forward and backward."""
+    wl = I.TINY_F32.replace(L=150, d=d, D=D, Hkv=2, Hq=2 * G, w=w, B=2)
+    check_fwd(lz, oracle_mod, wl, reading)
+    check_bwd(lz, oracle_mod, wl, reading)
