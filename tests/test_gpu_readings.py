@@ -404,3 +404,42 @@ def test_fwd_bwd_small_windows_and_heads(lz, oracle_mod, reading, d, D, G, w):
     wl = I.TINY_F32.replace(L=150, d=d, D=D, Hkv=2, Hq=2 * G, w=w, B=2)
     check_fwd(lz, oracle_mod, wl, reading)
     check_bwd(lz, oracle_mod, wl, reading)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_fwd_llama_full_size(lz, oracle_mod, reading):
+    """The bench's LLaMA-shaped forward at its full size (B = 1, L = 8192, all heads) in the
+    bench's launch configuration, every output against the oracle."""
+    wl = I.LLAMA3_8B_L8K
+    check_fwd(lz, oracle_mod, wl, reading)
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_stress_full_length_sampled_heads(lz, oracle_mod, reading):
+    """L = 65536 with the stress gate mixture: the GPU runs all heads, the oracle one KV group
+    (units are independent, so a head subset is an exact sub-problem)."""
+    wl = I.STRESS_L64K
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl, reading)
+    G, kv = wl.G, 3
+    sub = dict(q=inp["q"][:, :, kv * G:(kv + 1) * G], k=inp["k"][:, :, kv:kv + 1],
+               v=inp["v"][:, :, kv:kv + 1], g=inp["g"][:, :, kv:kv + 1],
+               Wf=inp["Wf"][kv:kv + 1], sinks=inp["sinks"][kv * G:(kv + 1) * G])
+    ref = oracle_mod.fwd(**sub, w=wl.w, state=True, reading=reading)
+    assert_parity(out["y"][:, :, kv * G:(kv + 1) * G], ref["y"], "bf16", f"y kv{kv}")
+    assert_parity(out["S_out"][:, kv:kv + 1], ref["S"], "bf16", f"S kv{kv}")
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_bwd_mistral_full_size_sampled(lz, oracle_mod, reading):
+    """B = 8, L = 2048 (the bench's training step): the GPU runs the whole batch; the oracle
+    checks one sequence's dq, dk, dv, dg (batch entries are independent)."""
+    wl = I.MISTRAL_7B_TRAIN
+    inp = I.make_inputs(wl, with_dy=True)
+    out = gpu_fwd_bwd(lz, inp, wl, reading)
+    b = 6
+    sub = {n: (a[b:b + 1] if n in ("q", "k", "v", "g", "dy") else a) for n, a in inp.items()}
+    ref = oracle_mod.bwd(**{n: a for n, a in sub.items() if n != "dy"}, dy=sub["dy"], w=wl.w,
+                         reading=reading)
+    for n in ("dq", "dk", "dv", "dg"):
+        assert_grad(out[n][b:b + 1], ref[n], "bf16", f"{n} b{b}")
