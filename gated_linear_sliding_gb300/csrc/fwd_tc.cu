@@ -318,6 +318,9 @@ __device__ __forceinline__ void control_loop(uint8_t* sm, uint32_t base, uint32_
     }
 }
 
+// KEYF: the masked decay reading (each entering key's factor e^{kd} folded into its decay
+// table); a separate instantiation, so the other readings' code is not touched by it.
+template <bool KEYF>
 __global__ void __launch_bounds__(NT, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmW,
@@ -443,6 +446,18 @@ __global__ void __launch_bounds__(NT, 1)
             const int gf = tid & (DF - 1), gq = tid >> 7;
             float ig[CT / 4];  // 1/Gamma of the thread's tokens (Gamma itself is rcp of it)
             float pig = 1.0f;
+            // masked decay reading: the delayed key of each of the thread's tokens enters with
+            // its phi scaled by the product of the w gates it saw in the window, e^{kd}, folded
+            // into its decay factor below.  Loaded first, so the gate products run while the
+            // loads are in flight.
+            float kl[CT / 4];  // log factors (0 for a token with no key entering)
+#pragma unroll
+            for (int t = 0; t < CT / 4; ++t) {
+                const int64_t j = t0 + (CT / 4) * gq + t - WIN;
+                kl[t] = KEYF && j >= 0 && (CT / 4) * gq + t < n
+                            ? a.kdec[((row0 + j) * p.Hkv + kv) * DF + gf]
+                            : 0.0f;
+            }
             {
                 const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + oG);
 #pragma unroll
@@ -472,7 +487,7 @@ __global__ void __launch_bounds__(NT, 1)
                     for (int t = CT / 4 - 1; t >= 0; --t) {
                         const int tt = (CT / 4) * gq + t;
                         Eq[eidx(tt, gf)] = __float2bfloat16_rn(sq);
-                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(sk);
+                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(KEYF ? sk * __expf(kl[t]) : sk);
                         sq *= ig[t];
                         sk *= rcpf(ig[t]);
                     }
@@ -485,7 +500,7 @@ __global__ void __launch_bounds__(NT, 1)
                         pq *= rcpf(ig[t]);
                         pk *= ig[t];
                         Eq[eidx(tt, gf)] = __float2bfloat16_rn(pq);
-                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(pk);
+                        Ek[eidx(tt, gf)] = __float2bfloat16_rn(KEYF ? pk * __expf(kl[t]) : pk);
                     }
                 }
                 if (gq == 0) {
@@ -922,6 +937,7 @@ __device__ __forceinline__ void local_load(uint8_t* dst, const CUtensorMap* tm, 
         tma_load_4d(dst + kb * 16384, tm, bar, 64 * kb, (int)kv, (int)t, (int)b);
 }
 
+template <bool KEYF>
 __global__ void __launch_bounds__(NL, 1)
     fwd_tc_local(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                  const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmG,
@@ -1075,6 +1091,17 @@ __global__ void __launch_bounds__(NL, 1)
             float* Ek = (float*)(sm + lE);
 #pragma unroll
             for (int j = 0; j < 32; ++j) Ek[(32 * gq + j) * EKR + gf] = suf[j] * later;
+            // masked decay reading: each delayed key enters scaled by the product of the w
+            // gates it saw in the window, e^{kd}, folded into its decay factor
+            if (KEYF) {
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const int64_t key = t0 + 32 * gq + j - WIN;
+                    if (key >= 0 && 32 * gq + j < n)
+                        Ek[(32 * gq + j) * EKR + gf] *=
+                            __expf(a.kdec[((row0 + key) * p.Hkv + kv) * DF + gf]);
+                }
+            }
             if (gq == 0) {
                 S.el[gf] = gpart[gf] * ((q1 * q2) * q3);
                 lam_tot += (zq[gf] + zq[DF + gf]) + (zq[2 * DF + gf] + zq[3 * DF + gf]);
@@ -1281,10 +1308,11 @@ cudaError_t launch_local_and_scan(const Plan& p, const FwdArgs& a, const CUtenso
         const cuuint32_t box[4] = {DF, 1, LT, 1};
         if (!make_map(&lg, a.g, 4, dims, str, box, false)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(fwd_tc_local, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto local = a.kdec != nullptr ? fwd_tc_local<true> : fwd_tc_local<false>;
+    cudaError_t e = cudaFuncSetAttribute(local, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kLocalSmem);
     if (e != cudaSuccess) return e;
-    fwd_tc_local<<<dim3(U, (unsigned)(p.P - 1)), NL, kLocalSmem, s>>>(lk, lv, mw, lg, p, a);
+    local<<<dim3(U, (unsigned)(p.P - 1)), NL, kLocalSmem, s>>>(lk, lv, mw, lg, p, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return launch_seg_scan(p, a.seg, s, true);
@@ -1299,12 +1327,10 @@ bool make_wf_map(CUtensorMap* mw, const void* Wf, int64_t Hkv) {
 
 }  // namespace
 
-// The masked decay reading scales each entering key's phi by its own gate product, which
-// only the SIMT walks apply.
 bool fwd_tc_supported(const Plan& p) {
     return p.dtype == LIZARD_BF16 && p.d == DH && p.D == DF && p.G == GQ && p.w == WIN &&
            p.M <= MMAX && p.L < ((int64_t)1 << 30) && p.T < ((int64_t)1 << 30) &&
-           p.decay != LIZARD_DECAY_MASKED && encode_fn() != nullptr;
+           encode_fn() != nullptr;
 }
 
 cudaError_t launch_fwd_states_tc(const Plan& p, const FwdArgs& a, cudaStream_t s) {
@@ -1369,8 +1395,8 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
         if (!make_map(&mw, a.Wf, 3, dims, str, box)) return cudaErrorInvalidValue;
     }
     cudaError_t e;
-    e = cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)kSmemBytes);
+    auto walk = a.kdec != nullptr ? fwd_tc_kernel<true> : fwd_tc_kernel<false>;
+    e = cudaFuncSetAttribute(walk, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes);
     if (e != cudaSuccess) return e;
     const unsigned U = (unsigned)(p.B * p.Hkv);
     if (p.P > 1) {
@@ -1385,11 +1411,10 @@ cudaError_t launch_fwd_tc(const Plan& p0, const FwdArgs& a, cudaStream_t s) {
     }
     if (a.ev_before) cudaEventRecord(a.ev_before, s);
     if (p.P > 1 && a.ev_before == nullptr)  // starts while the scan finishes
-        e = launch_dependent(fwd_tc_kernel, dim3(U, (unsigned)p.P), dim3(NT), kSmemBytes, s, mq,
-                             mk, mv, mw, mg, my, p, a);
+        e = launch_dependent(walk, dim3(U, (unsigned)p.P), dim3(NT), kSmemBytes, s, mq, mk, mv,
+                             mw, mg, my, p, a);
     else
-        fwd_tc_kernel<<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, my, p,
-                                                                            a);
+        walk<<<dim3(U, (unsigned)p.P), NT, kSmemBytes, s>>>(mq, mk, mv, mw, mg, my, p, a);
     if (a.ev_after) cudaEventRecord(a.ev_after, s);
     if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return e;

@@ -49,7 +49,10 @@ lizard_status fwd_check(const lizard_dims* dims, Plan* p, const void* q, const v
 // query fails.
 lizard_status device_status();
 // Boundary-state records (each rec_floats floats per unit) the forward's launch uses.
-size_t fwd_records_used(const Plan& p);
+// The forward's walk: the tensor-core one on its shapes, except a masked-reading call that
+// returns the final state (state_out), which takes the SIMT walk.
+bool fwd_uses_tc(const Plan& p, bool state_out);
+size_t fwd_records_used(const Plan& p, bool tc);
 struct FwdArgs;
 // The forward's kernels (tensor-core or SIMT path, then the ring caches) on stream s.
 cudaError_t fwd_launch(const Plan& p, const FwdArgs& a, cudaStream_t s);

@@ -112,8 +112,17 @@ lizard_status fwd_check(const lizard_dims* dims, Plan* p, const void* q, const v
     return LIZARD_OK;
 }
 
-size_t fwd_records_used(const Plan& p) {
-    if (fwd_tc_supported(p)) {
+bool fwd_uses_tc(const Plan& p, bool state_out) {
+    // the masked reading scales each feature row of the state by its keys' gate products, so
+    // the final state spans a wide range (max entry ~40x the RMS on the LLaMA-shaped layer);
+    // the tensor-core walk's bf16 update operands keep every row's relative error but not
+    // the error against the state's RMS, so a masked call returning the state takes the fp32
+    // SIMT walk
+    return fwd_tc_supported(p) && !(p.decay == LIZARD_DECAY_MASKED && state_out);
+}
+
+size_t fwd_records_used(const Plan& p, bool tc) {
+    if (tc) {
         Plan pl = p;
         fwd_tc_plan(&pl);
         // every CTA of the tensor-core walk marks its record slot (hand-off to the tail walk)
@@ -138,7 +147,8 @@ cudaError_t fwd_launch(const Plan& p, const FwdArgs& a, cudaStream_t s) {
         }
         if (e != cudaSuccess) return e;
     }
-    e = fwd_tc_supported(p) ? launch_fwd_tc(p, b, s) : launch_fwd_simt(p, b, s);
+    e = fwd_uses_tc(p, a.S_out != nullptr || a.z_out != nullptr) ? launch_fwd_tc(p, b, s)
+                                                                 : launch_fwd_simt(p, b, s);
     if (e == cudaSuccess && a.kcache_out != nullptr)
         e = launch_ring_fill(p, a.k, a.v, a.kcache_out, a.vcache_out, s);
     return e;
@@ -259,7 +269,8 @@ static bool packed_plan(const lizard_dims* dims, const int64_t* cu, Plan* p) {
     dv.L = lmax;
     if (!make_plan(&dv, p)) return false;
     p->T = T;
-    if (!fwd_tc_supported(*p)) return false;
+    // (a masked batch runs sequence by sequence: each call picks its walk, see fwd_uses_tc, by whether it returns the state)
+    if (!fwd_tc_supported(*p) || p->decay == LIZARD_DECAY_MASKED) return false;
     const int64_t share = (T * p->Hkv + 151) / 152;
     int64_t sc = (share / 4 + kChunk - 1) / kChunk;
     sc = std::max<int64_t>(1, std::min<int64_t>(sc, p->nchunks));

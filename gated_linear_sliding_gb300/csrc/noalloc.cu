@@ -42,14 +42,16 @@ cudaError_t noalloc_scratch(void** out) {
 // Scratch bytes a call needs: the status word, then the boundary-state records its launch
 // uses (the same count as in a caller's workspace), then the reading's scratch (MASKED and
 // LAGGED) from the next 256-byte boundary.
-size_t noalloc_records_end(const Plan& p) {
+size_t noalloc_records_end(const Plan& p, bool tc) {
     return kHeaderBytes +
-           sizeof(float) * fwd_records_used(p) * (size_t)(p.B * p.Hkv) * p.rec_floats;
+           sizeof(float) * fwd_records_used(p, tc) * (size_t)(p.B * p.Hkv) * p.rec_floats;
 }
-size_t noalloc_reading_offset(const Plan& p) { return (noalloc_records_end(p) + 255) & ~(size_t)255; }
-size_t noalloc_need(const Plan& p) {
+size_t noalloc_reading_offset(const Plan& p, bool tc) {
+    return (noalloc_records_end(p, tc) + 255) & ~(size_t)255;
+}
+size_t noalloc_need(const Plan& p, bool tc) {
     const size_t r = reading_scratch_bytes(p);
-    return r == 0 ? noalloc_records_end(p) : noalloc_reading_offset(p) + r;
+    return r == 0 ? noalloc_records_end(p, tc) : noalloc_reading_offset(p, tc) + r;
 }
 
 }  // namespace
@@ -64,7 +66,10 @@ using namespace lz;
 extern "C" size_t lizard_attn_fwd_noalloc_scratch(const lizard_dims* dims) {
     Plan p;
     if (!make_plan(dims, &p)) return 0;
-    return noalloc_need(p);
+    // the larger of the two walks' needs (a masked call returning the state takes the SIMT walk)
+    const size_t tc = noalloc_need(p, fwd_uses_tc(p, false));
+    const size_t st = noalloc_need(p, fwd_uses_tc(p, true));
+    return tc > st ? tc : st;
 }
 
 extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const void* q,
@@ -77,7 +82,8 @@ extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const 
     lizard_status st = fwd_check(dims, &p, q, k, v, g, Wf, sinks, y, lse, S_out, z_out,
                                  kcache_out, vcache_out);
     if (st != LIZARD_OK) return st;
-    if (noalloc_need(p) > kNoAllocScratchBytes) return LIZARD_ERR_WORKSPACE;
+    const bool tc = fwd_uses_tc(p, S_out != nullptr || z_out != nullptr);
+    if (noalloc_need(p, tc) > kNoAllocScratchBytes) return LIZARD_ERR_WORKSPACE;
     st = device_status();
     if (st != LIZARD_OK) return st;
 
@@ -105,7 +111,8 @@ extern "C" lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const 
     a.seg = (float*)((char*)scratch + kHeaderBytes);
     a.ev_before = nullptr;
     a.ev_after = nullptr;
-    a.rscratch = reading_scratch_bytes(p) != 0 ? (char*)scratch + noalloc_reading_offset(p) : nullptr;
+    a.rscratch =
+        reading_scratch_bytes(p) != 0 ? (char*)scratch + noalloc_reading_offset(p, tc) : nullptr;
     return fwd_launch(p, a, s) == cudaSuccess ? LIZARD_OK : LIZARD_ERR_CUDA;
 }
 

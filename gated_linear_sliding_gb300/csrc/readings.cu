@@ -9,7 +9,8 @@
 //           moved copy of g and the backward moves dg back;
 //   MASKED  prod_{s=j+1..i} Gamma_s    = the delayed reading with each entering key's phi
 //           scaled by c_j = prod_{s=j+1..j+w} Gamma_s, the gates it saw in the window; the
-//           SIMT walks apply e^{kd_j}, kd_j = log c_j from key_decay_kernel.
+//           forward walks (tensor-core and SIMT) and the SIMT backward walks apply e^{kd_j},
+//           kd_j = log c_j from key_decay_kernel.
 // Decode keeps the gate logits of the window in a ring like the keys and values: the
 // lagged step decays by the gate of token pos - w, the masked step admits token pos - w
 // scaled by the product of the gates of pos - w + 1 .. pos.
@@ -208,7 +209,8 @@ cudaError_t launch_gate_lag(const Plan& p, const void* g, void* out, cudaStream_
 }
 
 cudaError_t launch_key_decay(const Plan& p, const void* g, float* kd, cudaStream_t s) {
-    const int64_t ncb = (p.Hkv * p.D + 127) / 128, njb = (p.L + KJ - 1) / KJ;
+    const int64_t ncb = (p.Hkv * p.D + 127) / 128;
+    const int64_t njb = (p.L + KJ - 1) / KJ;
     const dim3 grid((unsigned)(ncb * njb), (unsigned)p.B);
     if (p.dtype == LIZARD_F32)
         key_decay_kernel<float><<<grid, 128, 0, s>>>(p, (const float*)g, kd);

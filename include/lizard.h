@@ -91,11 +91,13 @@ typedef enum {
  *   LAGGED   the same kernels on the gate logits moved w tokens later (a copy in
  *            the workspace, B L Hkv D elements more than the DELAYED workspace; the
  *            backward moves dg back); decode needs the gate ring (gcache);
- *   MASKED   the SIMT walks only (forward and backward), with each entering key's
- *            phi scaled by the product of the w gates it saw in the window (per-token
- *            log products in the workspace, B L Hkv D fp32 more; the backward keeps the
- *            key-side gate terms in a second such array); decode needs gcache.  The
- *            window parts of the backward still run on the tensor cores. */
+ *   MASKED   each entering key's phi scaled by the product of the w gates it saw in the
+ *            window (per-token log products in the workspace, B L Hkv D fp32 more): the
+ *            forward folds the factor into the keys' decay tables (tensor-core walk, or
+ *            the SIMT walk when the call returns the final state, see
+ *            lizard_attn_fwd_kernel; a packed batch runs sequence by sequence); the
+ *            backward runs the SIMT walks (the window parts stay on the tensor cores) and
+ *            keeps the key-side gate terms in a second such array; decode needs gcache. */
 typedef struct {
     int64_t B, L, Hq, Hkv, d, D, w, M;
     int64_t chunk;
@@ -111,9 +113,11 @@ typedef struct {
 size_t lizard_attn_fwd_workspace(const lizard_dims* dims);
 
 /* Which forward kernel serves these sizes: 1 = the tensor-core (tcgen05) chunk walk
- * (bf16, d = D = 128, Hq = 4 Hkv, w = 64, reading DELAYED or LAGGED), 0 = the SIMT walk
- * (fp32, the MASKED reading and every other shape), -1 = invalid sizes.  Pure host
- * query. */
+ * (bf16, d = D = 128, Hq = 4 Hkv, w = 64), 0 = the SIMT walk (fp32 and every other
+ * shape), -1 = invalid sizes.  Under the MASKED reading a call that returns the final state
+ * (S_out, z_out) takes the SIMT walk even on the tensor-core shapes: that state spans a wide
+ * range (each feature row scaled by its keys' gate products), which the tensor-core walk's
+ * bf16 update operands do not hold to the bf16 bound against its RMS.  Pure host query. */
 int lizard_attn_fwd_kernel(const lizard_dims* dims);
 
 /* Zero the device status word at the head of a workspace (async on stream).
@@ -201,8 +205,10 @@ lizard_status lizard_attn_fwd_noalloc(const lizard_dims* dims, const void* q, co
 /* Bytes of lizard_attn_fwd_noalloc's 32 MiB array that a call with these sizes uses: 256
  * (status word) plus the boundary-state records of its launch, R * B * Hkv * (D*d + 2*D) * 4,
  * with R the number of records its segmentation writes (at least 1 on the tensor-core path,
- * 0 on the SIMT path when the sequence is one segment).  0 for invalid sizes.  Pure host
- * query; no counterpart on the Lizard pages. */
+ * 0 on the SIMT path when the sequence is one segment), plus, from the next 256-byte
+ * boundary, the MASKED or LAGGED reading's scratch (one value per gate element); for the
+ * MASKED reading the larger of its two walks' needs (see lizard_attn_fwd_kernel).  0 for
+ * invalid sizes.  Pure host query; no counterpart on the Lizard pages. */
 size_t lizard_attn_fwd_noalloc_scratch(const lizard_dims* dims);
 
 /* Synchronise `stream`, read and clear the status word of lizard_attn_fwd_noalloc's array on

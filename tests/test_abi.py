@@ -90,11 +90,13 @@ def test_reading_workspaces(lib, decay, elem):
 
 
 def test_tensor_core_path_by_reading(lib):
-    """The masked reading runs the SIMT walk; the lagged one keeps the tensor-core path."""
+    """Both other readings keep the tensor-core forward on its shapes, and the SIMT walk on
+    the others."""
     if lz.lizard_attn_fwd_kernel(dims()) != 1:
         pytest.skip("the driver's TMA encoder is not available here")
-    assert lz.lizard_attn_fwd_kernel(dims(decay=lz.LIZARD_DECAY_LAGGED)) == 1
-    assert lz.lizard_attn_fwd_kernel(dims(decay=lz.LIZARD_DECAY_MASKED)) == 0
+    for code in (lz.LIZARD_DECAY_LAGGED, lz.LIZARD_DECAY_MASKED):
+        assert lz.lizard_attn_fwd_kernel(dims(decay=code)) == 1
+        assert lz.lizard_attn_fwd_kernel(dims(decay=code, dtype=lz.LIZARD_F32)) == 0
 
 
 def test_workspace_constant_in_L(lib):

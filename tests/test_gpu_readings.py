@@ -29,11 +29,13 @@ def lz():
     return lizard
 
 
-def gpu_fwd(lz, inp, wl, reading, lse=False):
+def gpu_fwd(lz, inp, wl, reading, lse=False, state=True):
     t = to_dev(inp, wl.dtype)
     B, L, Hq, d = inp["q"].shape
-    kw = dict(S_out=torch.empty(B, wl.Hkv, wl.D, d, dtype=torch.float32, device="cuda"),
-              z_out=torch.empty(B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda"))
+    kw = {}
+    if state:
+        kw = dict(S_out=torch.empty(B, wl.Hkv, wl.D, d, dtype=torch.float32, device="cuda"),
+                  z_out=torch.empty(B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda"))
     if lse:
         kw["lse"] = torch.empty(B, L, Hq, dtype=torch.float32, device="cuda")
     y = lz.lizard_attn_fwd(t["q"], t["k"], t["v"], t["g"], t["Wf"], t["sinks"], wl.w,
@@ -76,12 +78,13 @@ def test_fwd_f32_gla_sensitive_tells_readings_apart(lz, oracle_mod, reading):
 
 @pytest.mark.parametrize("reading", READINGS)
 def test_fwd_llama_shape(lz, oracle_mod, reading):
-    """LLaMA-shaped heads at L = 1100 (several segments, a ragged last step): the lagged
-    reading runs the tensor-core walk on the moved gates, the masked one the SIMT walk."""
+    """LLaMA-shaped heads at L = 1100 (several segments, a ragged last step), returning the
+    final state: the lagged reading runs the tensor-core walk on the moved gates, the masked
+    one (asked for the state) the SIMT walk."""
     wl = I.LLAMA3_8B_L8K
     dims = lz.make_dims(1, 1100, wl.Hq, wl.Hkv, wl.d, wl.D, wl.w, wl.M, lz.LIZARD_BF16,
                         decay=reading)
-    assert lz.lizard_attn_fwd_kernel(dims) == (1 if reading == LAGGED else 0)
+    assert lz.lizard_attn_fwd_kernel(dims) == 1
     check_fwd(lz, oracle_mod, wl, reading, L=1100)
 
 
@@ -93,15 +96,16 @@ def test_fwd_llama_gla_sensitive(lz, oracle_mod, reading):
 
 @pytest.mark.parametrize("reading", READINGS)
 def test_fwd_closed_gates(lz, oracle_mod, reading):
-    """Runs of strongly closed gates: the lagged reading's moved gates take the tensor-core
-    walk's hand-over to the exact walk at the moved positions."""
+    """Runs of strongly closed gates: the tensor-core walk hands such steps to the exact walk
+    (at the moved positions for the lagged reading; with the keys' factors for the masked)."""
     check_fwd(lz, oracle_mod, I.closed_gates(I.LLAMA3_8B_L8K, per_1k=6.0), reading, L=1600)
 
 
 @pytest.mark.parametrize("reading", READINGS)
 def test_fwd_varlen_packed(lz, oracle_mod, reading):
-    """A packed batch: the gates move within each sequence (lagged: one launch over all
-    sequences; masked: the sequences one after another), each equals its own forward."""
+    """A packed batch: the gates move (lagged, one launch over all sequences) or the keys'
+    factors are taken (masked, sequence by sequence) within each sequence; each sequence
+    equals its own forward."""
     wl = I.LLAMA3_8B_L8K
     lens = [1, 77, 0, 300, 1000, 130]
     cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
@@ -443,3 +447,25 @@ def test_bwd_mistral_full_size_sampled(lz, oracle_mod, reading):
                          reading=reading)
     for n in ("dq", "dk", "dv", "dg"):
         assert_grad(out[n][b:b + 1], ref[n], "bf16", f"{n} b{b}")
+
+
+@pytest.mark.parametrize("L", [1100, 8192])
+def test_fwd_masked_tensor_core_walk(lz, oracle_mod, L):
+    """The masked reading on the tensor-core walk (a call that does not return the state):
+    y and lse of the LLaMA-shaped layer against the oracle, up to the bench's full size."""
+    wl = I.LLAMA3_8B_L8K
+    inp = I.make_inputs(wl, L=L)
+    out = gpu_fwd(lz, inp, wl, MASKED, lse=True, state=False)
+    ref = oracle_mod.fwd(**inp, w=wl.w, parts=True, reading=MASKED)
+    assert_parity(out["y"], ref["y"], "bf16", "y")
+    assert rel_l2(out["lse"], np.log(ref["den"])) < 1e-3
+
+
+def test_fwd_masked_tensor_core_walk_closed_gates(lz, oracle_mod):
+    """Closed-gate runs on the masked tensor-core walk: the steps it hands to the exact walk
+    take the keys' factors there too."""
+    wl = I.closed_gates(I.LLAMA3_8B_L8K, per_1k=6.0)
+    inp = I.make_inputs(wl, L=1600)
+    out = gpu_fwd(lz, inp, wl, MASKED, state=False)
+    ref = oracle_mod.fwd(**inp, w=wl.w, reading=MASKED)
+    assert_parity(out["y"], ref["y"], "bf16", "y")
