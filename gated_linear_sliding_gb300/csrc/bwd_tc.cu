@@ -46,7 +46,7 @@ struct Bars {
     volatile int abort;
 };
 
-// Bounded wait by every thread; all return the same verdict.
+// Bounded wait by every thread; all return the same answer.
 __device__ __forceinline__ bool all_wait(uint64_t* bar, uint32_t ph, Bars& S, WsHeader* hdr,
                                          unsigned where) {
     bool fail = false;

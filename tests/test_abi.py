@@ -93,7 +93,7 @@ def test_tensor_core_path_by_reading(lib):
     """Both other readings keep the tensor-core forward on its shapes, and the SIMT walk on
     the others."""
     if lz.lizard_attn_fwd_kernel(dims()) != 1:
-        pytest.skip("the driver's TMA encoder is not available here")
+        pytest.skip("the CUDA driver's TMA encoder is not available here")
     for code in (lz.LIZARD_DECAY_LAGGED, lz.LIZARD_DECAY_MASKED):
         assert lz.lizard_attn_fwd_kernel(dims(decay=code)) == 1
         assert lz.lizard_attn_fwd_kernel(dims(decay=code, dtype=lz.LIZARD_F32)) == 0
@@ -176,7 +176,7 @@ def test_noalloc_scratch_query(lib):
     rec = (128 * 128 + 2 * 128) * 4
     small = lz.lizard_attn_fwd_noalloc_scratch(dims(L=64))
     assert (small - 256) % (8 * rec) == 0
-    # the tensor-core path needs the driver's TMA encoder; without it the one-segment SIMT
+    # the tensor-core path needs the CUDA driver's TMA encoder; without it the one-segment SIMT
     # launch uses no record
     tc = lz.lizard_attn_fwd_kernel(dims(L=64)) == 1
     assert small == 256 + 8 * rec if tc else small == 256
