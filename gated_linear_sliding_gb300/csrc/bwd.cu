@@ -1146,8 +1146,7 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a_in, cudaStream_t s) {
     }
     // 2. forward-direction walk.  The tensor-core walks leave the segments whose gates close
     //    too hard for their factored decays to the exact SIMT walks (flags from one pass over g)
-    const bool tc_walks =
-        a.win_tc && bwd_rev_local_tc_supported(p) && p.decay != LIZARD_DECAY_MASKED;
+    const bool tc_walks = a.win_tc && bwd_rev_local_tc_supported(p);
     int* flags = (int*)(wsf + ws.flags);
     if (tc_walks) {
         if constexpr (sizeof(T) == 2 && DF == 128)

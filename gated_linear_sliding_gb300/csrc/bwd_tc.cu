@@ -949,6 +949,10 @@ __device__ __forceinline__ void load_delayed(uint8_t* dst, const CUtensorMap* tm
         tma_load_4d(dst + kb * 4096, tm, bar, 64 * kb, (int)kv, (int)((c - 2) * CT), (int)b);
 }
 
+// KEYF: the masked decay reading (each delayed key enters with its phi scaled by the product
+// of the w gates it saw in the window, e^{kd} from a.kdec); a separate instantiation, so the
+// other readings' code is not touched by it.
+template <bool KEYF>
 __global__ void __launch_bounds__(NT, 1)
     bwd_fwalk_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDY,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -1226,10 +1230,18 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
                 const int f0 = 64 * kb + 4 * sub;
-                float ki[4], ku[4];
+                float ki[4], ku[4], kf[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+                if (KEYF && dvalid) {  // the delayed key's own factor (masked reading)
+                    const float4 c4 = *reinterpret_cast<const float4*>(
+                        a.kdec + ((b * p.L + t0 + t - WIN) * p.Hkv + kv) * 128 + f0);
+                    kf[0] = __expf(c4.x);
+                    kf[1] = __expf(c4.y);
+                    kf[2] = __expf(c4.z);
+                    kf[3] = __expf(c4.w);
+                }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
-                    const float ph = kb == 0 ? ep[e] * ip : en[e] * in;
+                    const float ph = (kb == 0 ? ep[e] * ip : en[e] * in) * kf[e];
                     ki[e] = ph * rcpf(etab[t * 128 + f0 + e]);  // e^{r - b_t}
                     ku[e] = ki[e] * S.cf[f0 + e];
                 }
@@ -1556,6 +1568,9 @@ __device__ __forceinline__ bool fw_wait2(uint64_t* bar, uint32_t& ph, volatile i
     return !__syncthreads_or(fail);
 }
 
+// KEYF: the masked decay reading, as for the forward walk; the delayed keys' gate terms then
+// go to a.kkey at the keys' own rows instead of into the reverse sum.
+template <bool KEYF>
 __global__ void __launch_bounds__(NT, 1)
     bwd_rwalk_tc(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDY,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -1821,11 +1836,19 @@ __global__ void __launch_bounds__(NT, 1)
 #pragma unroll
             for (int kb = 0; kb < 2; ++kb) {
                 const int f0 = 64 * kb + 4 * sub;
-                float ph[4], kh[4];
+                float ph[4], kh[4], kf[4] = {1.0f, 1.0f, 1.0f, 1.0f};
+                if (KEYF && dvalid) {  // the delayed key's own factor (masked reading)
+                    const float4 c4 = *reinterpret_cast<const float4*>(
+                        a.kdec + ((b * p.L + t0 + t - WIN) * p.Hkv + kv) * 128 + f0);
+                    kf[0] = __expf(c4.x);
+                    kf[1] = __expf(c4.y);
+                    kf[2] = __expf(c4.z);
+                    kf[3] = __expf(c4.w);
+                }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     ph[e] = kb == 0 ? ep[e] * ip : en[e] * in;
-                    kh[e] = ph[e] * rcpf(etab[t * 128 + f0 + e]);  // e^{rho - b_t}
+                    kh[e] = ph[e] * kf[e] * rcpf(etab[t * 128 + f0 + e]);  // e^{rho - b_t}
                 }
                 *reinterpret_cast<float4*>(pk + t * 128 + f0) = make_float4(ph[0], ph[1], ph[2], ph[3]);
                 const uint32_t off = kb * 4096 + sw128(t, sub >> 1) + (sub & 1) * 8;
@@ -1998,7 +2021,19 @@ __global__ void __launch_bounds__(NT, 1)
                 const int t = 8 * part + e;
                 phk[e] = pk[t * 128 + f];
                 dphi[e] = rcpf(etab[t * 128 + f]) * (gv[e] + zp);  // e^{rho - b_t} (G + z')
-                loc[e] = t < n ? dbp[e] - phk[e] * dphi[e] : 0.0f;
+                if (KEYF) {
+                    // masked reading: the key entered as c phi, so dphi = c (.) d(c phi); its
+                    // gate term phi dphi belongs to the key's own row (kept apart in kkey)
+                    const int64_t j = t0 + t - WIN;
+                    if (t < n && j >= 0) {
+                        const int64_t kidx = ((b * p.L + j) * p.Hkv + kv) * 128 + f;
+                        dphi[e] *= __expf(a.kdec[kidx]);
+                        a.kkey[kidx] = phk[e] * dphi[e];
+                    }
+                    loc[e] = t < n ? dbp[e] : 0.0f;
+                } else {
+                    loc[e] = t < n ? dbp[e] - phk[e] * dphi[e] : 0.0f;
+                }
             }
             // suffix sums inside the part (keys descending), then across parts
             float suf[8];
@@ -2182,10 +2217,11 @@ cudaError_t launch_bwd_fwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, siz
         const cuuint32_t box[3] = {64, DH, 1};
         if (!tc::make_map(&mw, a.Wf, 3, dims, str, box)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(bwd_fwalk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto walk = a.kdec != nullptr ? bwd_fwalk_tc<true> : bwd_fwalk_tc<false>;
+    cudaError_t e = cudaFuncSetAttribute(walk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemFW);
     if (e != cudaSuccess) return e;
-    bwd_fwalk_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemFW, s>>>(
+    walk<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemFW, s>>>(
         mq, md, mk, mv, mw, mg, mdq, p, a, wsf + o_rows, wsf + o_fwd, wsf + o_dB, wsf + o_dW,
         wsf + o_dt, flags);
     return cudaGetLastError();
@@ -2223,10 +2259,11 @@ cudaError_t launch_bwd_rwalk_tc(const Plan& p, const BwdArgs& a, float* wsf, siz
         const cuuint32_t box[3] = {64, DH, 1};
         if (!tc::make_map(&mw, a.Wf, 3, dims, str, box)) return cudaErrorInvalidValue;
     }
-    cudaError_t e = cudaFuncSetAttribute(bwd_rwalk_tc, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto walk = a.kdec != nullptr ? bwd_rwalk_tc<true> : bwd_rwalk_tc<false>;
+    cudaError_t e = cudaFuncSetAttribute(walk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kSmemRW);
     if (e != cudaSuccess) return e;
-    bwd_rwalk_tc<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemRW, s>>>(
+    walk<<<dim3((unsigned)(p.B * p.Hkv), (unsigned)p.P), NT, kSmemRW, s>>>(
         mq, md, mk, mv, mw, mg, p, a, wsf + o_rows, wsf + o_rev, wsf + o_dB, wsf + o_dW,
         wsf + o_tot, flags);
     return cudaGetLastError();

@@ -96,8 +96,8 @@ typedef enum {
  *            forward folds the factor into the keys' decay tables (tensor-core walk, or
  *            the SIMT walk when the call returns the final state, see
  *            lizard_attn_fwd_kernel; a packed batch runs sequence by sequence); the
- *            backward runs the SIMT walks (the window parts stay on the tensor cores) and
- *            keeps the key-side gate terms in a second such array; decode needs gcache. */
+ *            backward's state walks take the same factor and keep the key-side gate terms
+ *            in a second such array; decode needs gcache. */
 typedef struct {
     int64_t B, L, Hq, Hkv, d, D, w, M;
     int64_t chunk;
