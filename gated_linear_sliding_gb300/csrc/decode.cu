@@ -552,6 +552,9 @@ __device__ __forceinline__ bool stream_wait(uint64_t* bar, uint32_t parity, vola
     return true;
 }
 
+// KEYF: the masked decay reading (the admitted key's phi scaled by a.kdec's factor); a
+// separate instantiation, so the other readings' code is not touched by it.
+template <bool KEYF>
 __global__ void __launch_bounds__(ST, 1)
     decode_stream_kernel(Plan p, DecodeArgs a, const __grid_constant__ StreamMaps mp) {
     extern __shared__ uint8_t smem_raw[];
@@ -665,6 +668,16 @@ __global__ void __launch_bounds__(ST, 1)
             if (!run && tid == 0) report(hdr, LIZARD_ERR_INVALID_ARG, 43);
             const bool admit = pos >= w;
             const int nkeys = run ? (pos + 1 < w ? (int)pos + 1 : w) : 1;
+            // masked decay reading: the log factors of the admitted key, loaded now for warp SG,
+            // which forms that key's phi after the hand-off wait below
+            float kl[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+            if (KEYF && warp == SG && run && admit) {
+                const float* kr2 = a.kdec + (int64_t)un * 128;
+                kl[0] = kr2[lane];
+                kl[1] = kr2[lane + 32];
+                kl[2] = kr2[64 + lane];
+                kl[3] = kr2[96 + lane];
+            }
             // ring slots: the new token goes to slot_n = pos mod (w+1); the key that leaves the
             // window (token pos - w) sits in the slot after it; key jj of the window (token
             // pos - nkeys + 1 + jj) in slot (slot0 + jj) mod (w+1), the last being the new token
@@ -744,10 +757,17 @@ __global__ void __launch_bounds__(ST, 1)
                     }
                     const bool zero = (x == SG && !admit) || (x < SG && x >= G);
                     const float ip = zero ? 0.0f : 1.0f / sp, in = zero ? 0.0f : 1.0f / sn;
-                    H.phi[x][lane] = p0 * ip;
-                    H.phi[x][lane + 32] = p1 * ip;
-                    H.phi[x][64 + lane] = n0 * in;
-                    H.phi[x][96 + lane] = n1 * in;
+                    if (KEYF && x == SG) {  // the admitted key's factor (masked reading)
+                        H.phi[x][lane] = p0 * ip * __expf(kl[0]);
+                        H.phi[x][lane + 32] = p1 * ip * __expf(kl[1]);
+                        H.phi[x][64 + lane] = n0 * in * __expf(kl[2]);
+                        H.phi[x][96 + lane] = n1 * in * __expf(kl[3]);
+                    } else {
+                        H.phi[x][lane] = p0 * ip;
+                        H.phi[x][lane + 32] = p1 * ip;
+                        H.phi[x][64 + lane] = n0 * in;
+                        H.phi[x][96 + lane] = n1 * in;
+                    }
                 }
                 if (sh >= 0) {
                     // softmax of head sh over a half-warp (keys l, l + 16, l + 32, l + 48):
@@ -999,7 +1019,6 @@ bool aligned16(const void* ptr) { return ((uintptr_t)ptr & 15) == 0; }
 // The streaming step takes the LLaMA-3-8B-shaped heads when every buffer it copies is 16-byte
 // aligned and the tensor maps encode; otherwise the one-CTA-per-unit kernel runs.
 bool decode_stream_plan(const Plan& p, const DecodeArgs& a, StreamMaps* mp) {
-    if (a.kdec != nullptr) return false;  // the masked reading's key factors: SIMT kernel
     if (!(p.dtype == LIZARD_BF16 && p.d == 128 && p.D == 128 && p.G >= 1 && p.G <= SG &&
           p.w >= 1 && p.w <= SW && p.M <= 64 && p.B * p.Hkv * (p.w + 1) < (int64_t)1 << 31 &&
           p.B * p.Hkv * 128 < (int64_t)1 << 31 && p.B * p.Hq < (int64_t)1 << 31))
@@ -1033,12 +1052,13 @@ cudaError_t launch_decode_stream(const Plan& p, const DecodeArgs& a, const Strea
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(decode_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    auto kern = a.kdec != nullptr ? decode_stream_kernel<true> : decode_stream_kernel<false>;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)kStreamSmem);
     if (e != cudaSuccess) return e;
     const int64_t U = p.B * p.Hkv;
     const unsigned grid = (unsigned)(U < nsm ? U : nsm);
-    decode_stream_kernel<<<grid, ST, kStreamSmem, s>>>(p, a, mp);
+    kern<<<grid, ST, kStreamSmem, s>>>(p, a, mp);
     return cudaGetLastError();
 }
 
