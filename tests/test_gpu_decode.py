@@ -56,6 +56,25 @@ def test_decode_from_scratch(lz, oracle_mod, dtype, d, D, G, w):
     assert_parity(to_np(z), fin["z"], dtype, "z")
 
 
+@pytest.mark.parametrize("G,w,M", [(1, 1, 4), (2, 5, 0), (3, 17, 1), (4, 33, 64)])
+def test_decode_streaming_kernel_shapes(lz, oracle_mod, G, w, M):
+    """The streaming decode kernel's range (bf16, d = D = 128): one to four query heads per
+    KV head, windows from 1 to 33 keys (the ring copies' box height is w + 1), no sinks up to
+    64.  Decoded from position 0, so the window fills, wraps and the state starts admitting
+    keys at token w."""
+    wl = I.LLAMA3_8B_L8K.replace(B=3, L=110, Hkv=2, Hq=2 * G, w=w, M=M)
+    inp = I.make_inputs(wl)
+    ref = oracle_mod.fwd(**inp, w=w, state=True)
+    t = to_dev(inp, "bf16")
+    S = torch.zeros(wl.B, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.zeros(wl.B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(wl.B, wl.Hkv, w + 1, wl.d, dtype=torch.bfloat16, device="cuda")
+    vc = torch.zeros_like(kc)
+    y = decode_all(lz, t, wl, 0, wl.L, S, z, kc, vc)
+    assert_parity(y, ref["y"], "bf16", "decode y")
+    assert_parity(to_np(S), ref["S"], "bf16", "S")
+
+
 def test_prefill_then_decode_matches_longer_prefill(lz, oracle_mod):
     """The forward hands off (S, z, ring caches); decode continues; the result equals the
     oracle prefill of the whole sequence, token by token."""
