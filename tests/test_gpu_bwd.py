@@ -230,3 +230,13 @@ def test_bwd_varlen_lanes_match_sequence_loop(lz):
     for n in ("dWf", "dsinks"):
         x, r = to_np(a[n]), to_np(c[n])
         assert np.linalg.norm(x - r) <= 1e-5 * np.linalg.norm(r), n
+
+
+@pytest.mark.parametrize("M", [0, 64])
+def test_bwd_tensor_core_sink_counts(lz, oracle_mod, M):
+    """The tensor-core backward with no sinks and with 64 per head (dsinks [Hq, M])."""
+    wl = I.MISTRAL_7B_TRAIN.replace(M=M)
+    inp = I.make_inputs(wl, L=300, B=1, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    names = ("dq", "dk", "dv", "dg", "dWf") + (("dsinks",) if M > 0 else ())
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16", names)

@@ -318,3 +318,15 @@ def test_closed_gates_repeat_bitwise(lz):
     torch.cuda.synchronize()
     assert torch.equal(yo1, fresh)
     assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+
+
+@pytest.mark.parametrize("M", [0, 1, 64])
+def test_tensor_core_forward_sink_counts(lz, oracle_mod, M):
+    """The tensor-core walk with no sinks, one, and the most it takes (64 per head): the
+    sinks only enter the shared denominator (and lse)."""
+    wl = I.LLAMA3_8B_L8K.replace(M=M)
+    inp = I.make_inputs(wl, L=700)
+    out = gpu_fwd(lz, inp, wl, lse=True)
+    ref = oracle_fwd(oracle_mod, inp, wl, parts=True)
+    assert_parity(out["y"], ref["y"], "bf16", "y")
+    assert rel_l2(out["lse"], np.log(ref["den"])) < 1e-3
