@@ -269,9 +269,27 @@ def cpu_baseline(wl):
     t0 = time.perf_counter()
     oracle.fwd(**inp, w=wl.w)
     t = time.perf_counter() - t0
-    return {"value": wl.B * Ls / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-            "sample": f"one float64 pass over the whole workload ({Ls} tokens, all heads; "
-                      f"{t:.1f} s wall)", "host": host_cpu()}
+    out = {"value": wl.B * Ls / t, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+           "sample": f"one float64 pass over the whole workload ({Ls} tokens, all heads; "
+                     f"{t:.1f} s wall)", "host": host_cpu()}
+    # the same oracle on one core, over the first 1024 tokens (its cost per token does not
+    # depend on L): OpenMP's thread count set through the runtime the oracle links
+    try:
+        import ctypes
+
+        gomp = ctypes.CDLL("libgomp.so.1")
+        gomp.omp_set_num_threads(1)
+        L1 = 1024
+        sub = {n: (a[:, :L1] if n in ("q", "k", "v", "g") else a) for n, a in inp.items()}
+        t0 = time.perf_counter()
+        oracle.fwd(**sub, w=wl.w)
+        t1 = time.perf_counter() - t0
+        gomp.omp_set_num_threads(threads)
+        out["single_core"] = {"value": wl.B * L1 / t1, "unit": "tokens/s", "cores": 1,
+                              "sample": f"the first {L1} tokens, all heads ({t1:.1f} s wall)"}
+    except OSError:
+        out["single_core"] = None
+    return out
 
 
 def run_ours(args, rank, world, device):
@@ -343,6 +361,7 @@ def run_ours(args, rank, world, device):
     torch.cuda.synchronize()
     barrier()
     step_ms = max_over_ranks(sum(e0.elapsed_time(e1) for e0, e1 in ev) / args.steps)
+    step_med = max_over_ranks(float(np.median([e0.elapsed_time(e1) for e0, e1 in ev])))
     # the main walk's own duration, for the roofline: K more forwards under the same
     # conditions with the library's event hook around the walk (the hook's events sit between
     # the scan and the walk, which then starts after the scan instead of overlapping its end,
@@ -473,6 +492,7 @@ def run_ours(args, rank, world, device):
     out = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "ms_per_step_median": step_med,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded numpy PCG64, shapes and laws of the LLaMA-3-8B layer)",
         "config": workload_config(wl, {"l2": "flushed between timed steps (512 MiB write)",
