@@ -294,7 +294,9 @@ size_t lizard_decode_workspace(const lizard_dims* dims);
  * other slots untouched, as lizard_attn_fwd writes kcache_out and vcache_out.  g [B, L, Hkv,
  * D] is the prefill's input.  The gates of the tokens in the window are what these two
  * readings decay with later: the lagged state takes the gate of token pos - w at step pos,
- * the masked reading the product of the gates of tokens pos - w + 1 .. pos.  Errors:
+ * the masked reading the product of the gates of tokens pos - w + 1 .. pos.  After a packed
+ * prefill (lizard_attn_fwd_varlen), call it once per sequence with dims.B = 1, dims.L = the
+ * sequence's length, g at its first row and gcache at its ring.  Errors:
  * LIZARD_ERR_INVALID_ARG for bad dims or null/misaligned pointers. */
 lizard_status lizard_gate_cache_fill(const lizard_dims* dims, const void* g, void* gcache,
                                      void* stream);
