@@ -194,3 +194,22 @@ def test_backward_finite_differences(oracle_mod, reading):
     if reading == LAGGED:
         # the gates of the last w tokens never decay anything the queries read
         assert np.abs(gr["dg"][:, wl.L - wl.w:]).max() == 0.0
+
+
+def test_lagged_gradient_is_delayed_gradient_on_moved_gates(oracle_mod):
+    """The lagged reading is the delayed one on Gamma'_s = Gamma_{s-w}, so its gradients are
+    the delayed reading's on the moved gates, with dg moved back: dg[j] = dg'[j + w], and 0 for
+    the last w gates (they decay nothing a query reads).  Ties the lagged adjoint to the
+    delayed one, which the finite differences pin."""
+    wl = small(w=4, L=40, B=1)
+    inp = f64(I.make_inputs(wl))
+    dy = np.random.default_rng(23).standard_normal(inp["q"].shape)
+    lag = oracle_mod.bwd(**inp, dy=dy, w=wl.w, reading=LAGGED)
+    moved = dict(inp)
+    moved["g"] = np.concatenate([np.full_like(inp["g"][:, :wl.w], 5.0),
+                                 inp["g"][:, :wl.L - wl.w]], axis=1)
+    ref = oracle_mod.bwd(**moved, dy=dy, w=wl.w)
+    for n in ("dq", "dk", "dv", "dWf", "dsinks"):
+        assert rel(lag[n], ref[n]) < 1e-12, n
+    assert rel(lag["dg"][:, :wl.L - wl.w], ref["dg"][:, wl.w:]) < 1e-12
+    assert not lag["dg"][:, wl.L - wl.w:].any()
