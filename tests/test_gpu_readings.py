@@ -196,6 +196,13 @@ def test_bwd_lagged_closed_gates(lz, oracle_mod):
     check_bwd(lz, oracle_mod, I.closed_gates(I.MISTRAL_7B_TRAIN, per_1k=6.0), LAGGED, L=900, B=1)
 
 
+def test_bwd_masked_closed_gates(lz, oracle_mod):
+    """Closed-gate runs under the masked reading: flagged segments go to the SIMT walks and the
+    others stay on the tensor-core walks, both scaling the keys and writing their gate terms to
+    the same key-term array."""
+    check_bwd(lz, oracle_mod, I.closed_gates(I.MISTRAL_7B_TRAIN, per_1k=6.0), MASKED, L=900, B=2)
+
+
 @pytest.mark.parametrize("reading", READINGS)
 @pytest.mark.parametrize("dtype,d,D,G,w", [("f32", 64, 64, 2, 5), ("bf16", 128, 128, 4, 64)])
 def test_decode_after_prefill(lz, oracle_mod, reading, dtype, d, D, G, w):
