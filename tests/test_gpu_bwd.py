@@ -240,3 +240,11 @@ def test_bwd_tensor_core_sink_counts(lz, oracle_mod, M):
     ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
     names = ("dq", "dk", "dv", "dg", "dWf") + (("dsinks",) if M > 0 else ())
     check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16", names)
+
+
+def test_bwd_tensor_core_batch_ragged(lz, oracle_mod):
+    """Three batch entries with a ragged length on the tensor-core backward."""
+    wl = I.MISTRAL_7B_TRAIN.replace(Hq=8, Hkv=2)
+    inp = I.make_inputs(wl, L=1000, B=3, with_dy=True)
+    ref = oracle_mod.bwd(**{n: a for n, a in inp.items() if n != "dy"}, dy=inp["dy"], w=wl.w)
+    check(gpu_fwd_bwd(lz, inp, wl), ref, "bf16")

@@ -330,3 +330,18 @@ def test_tensor_core_forward_sink_counts(lz, oracle_mod, M):
     ref = oracle_fwd(oracle_mod, inp, wl, parts=True)
     assert_parity(out["y"], ref["y"], "bf16", "y")
     assert rel_l2(out["lse"], np.log(ref["den"])) < 1e-3
+
+
+@pytest.mark.parametrize("L", [1000, 1100])
+def test_tensor_core_forward_batch_ragged(lz, oracle_mod, L):
+    """Several batch entries with a ragged length on the tensor-core walk: the (batch, KV
+    head) units and the segments of each entry, partial last steps, state and ring outputs."""
+    wl = I.LLAMA3_8B_L8K.replace(B=3, L=L, Hq=8, Hkv=2)
+    inp = I.make_inputs(wl)
+    out = gpu_fwd(lz, inp, wl, lse=True, state=True, cache=True)
+    ref = oracle_fwd(oracle_mod, inp, wl, parts=True, state=True)
+    assert_parity(out["y"], ref["y"], "bf16", "y")
+    assert rel_l2(out["lse"], np.log(ref["den"])) < 1e-3
+    assert_parity(out["S_out"], ref["S"], "bf16", "S")
+    for t in range(L - wl.w, L):
+        np.testing.assert_array_equal(out["kcache_out"][:, :, t % (wl.w + 1)], inp["k"][:, t])
