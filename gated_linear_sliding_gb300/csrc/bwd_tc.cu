@@ -1204,6 +1204,13 @@ __global__ void __launch_bounds__(NT, 1)
         {
             const int t = tid >> 4, sub = tid & 15;
             const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
+            float4 kd4[2] = {};  // the delayed key's own log factor (masked reading)
+            if (KEYF && dvalid) {
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+                    kd4[kb] = *reinterpret_cast<const float4*>(
+                        a.kdec + ((b * p.L + t0 + t - WIN) * p.Hkv + kv) * 128 + 64 * kb + 4 * sub);
+            }
             const float4 u4 = *reinterpret_cast<const float4*>(suk + t * 64 + 4 * sub);
             const float u[4] = {u4.x, u4.y, u4.z, u4.w};
             float mx = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
@@ -1231,13 +1238,11 @@ __global__ void __launch_bounds__(NT, 1)
             for (int kb = 0; kb < 2; ++kb) {
                 const int f0 = 64 * kb + 4 * sub;
                 float ki[4], ku[4], kf[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-                if (KEYF && dvalid) {  // the delayed key's own factor (masked reading)
-                    const float4 c4 = *reinterpret_cast<const float4*>(
-                        a.kdec + ((b * p.L + t0 + t - WIN) * p.Hkv + kv) * 128 + f0);
-                    kf[0] = __expf(c4.x);
-                    kf[1] = __expf(c4.y);
-                    kf[2] = __expf(c4.z);
-                    kf[3] = __expf(c4.w);
+                if (KEYF && dvalid) {
+                    kf[0] = __expf(kd4[kb].x);
+                    kf[1] = __expf(kd4[kb].y);
+                    kf[2] = __expf(kd4[kb].z);
+                    kf[3] = __expf(kd4[kb].w);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -1810,6 +1815,13 @@ __global__ void __launch_bounds__(NT, 1)
         {
             const int t = tid >> 4, sub = tid & 15;
             const bool dvalid = (t0 + t - WIN >= 0) && (t < n);
+            float4 kd4[2] = {};  // the delayed key's own log factor (masked reading)
+            if (KEYF && dvalid) {
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+                    kd4[kb] = *reinterpret_cast<const float4*>(
+                        a.kdec + ((b * p.L + t0 + t - WIN) * p.Hkv + kv) * 128 + 64 * kb + 4 * sub);
+            }
             const float4 u4 = *reinterpret_cast<const float4*>(suk + t * 64 + 4 * sub);
             const float u[4] = {u4.x, u4.y, u4.z, u4.w};
             float mx = fmaxf(fmaxf(u[0], u[1]), fmaxf(u[2], u[3]));
@@ -1837,13 +1849,11 @@ __global__ void __launch_bounds__(NT, 1)
             for (int kb = 0; kb < 2; ++kb) {
                 const int f0 = 64 * kb + 4 * sub;
                 float ph[4], kh[4], kf[4] = {1.0f, 1.0f, 1.0f, 1.0f};
-                if (KEYF && dvalid) {  // the delayed key's own factor (masked reading)
-                    const float4 c4 = *reinterpret_cast<const float4*>(
-                        a.kdec + ((b * p.L + t0 + t - WIN) * p.Hkv + kv) * 128 + f0);
-                    kf[0] = __expf(c4.x);
-                    kf[1] = __expf(c4.y);
-                    kf[2] = __expf(c4.z);
-                    kf[3] = __expf(c4.w);
+                if (KEYF && dvalid) {
+                    kf[0] = __expf(kd4[kb].x);
+                    kf[1] = __expf(kd4[kb].y);
+                    kf[2] = __expf(kd4[kb].z);
+                    kf[3] = __expf(kd4[kb].w);
                 }
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -2011,7 +2021,15 @@ __global__ void __launch_bounds__(NT, 1)
         float dphi[8], phk[8];
         {
             const int f = row;
-            float gv[8];
+            float gv[8], kdl[8];
+            if (KEYF) {  // the keys' log factors, every load issued before the first store
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int t = 8 * part + e;
+                    const int64_t j = t0 + t - WIN;
+                    kdl[e] = t < n && j >= 0 ? a.kdec[((b * p.L + j) * p.Hkv + kv) * 128 + f] : 0.0f;
+                }
+            }
             tmem_ld8(tb + lane_off + vGc + 8 * part, gv);
             tmem_wait_ld();
             const float zp = xb[f];
@@ -2027,7 +2045,7 @@ __global__ void __launch_bounds__(NT, 1)
                     const int64_t j = t0 + t - WIN;
                     if (t < n && j >= 0) {
                         const int64_t kidx = ((b * p.L + j) * p.Hkv + kv) * 128 + f;
-                        dphi[e] *= __expf(a.kdec[kidx]);
+                        dphi[e] *= __expf(kdl[e]);
                         a.kkey[kidx] = phk[e] * dphi[e];
                     }
                     loc[e] = t < n ? dbp[e] : 0.0f;

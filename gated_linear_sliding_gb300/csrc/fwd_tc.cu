@@ -1092,14 +1092,23 @@ __global__ void __launch_bounds__(NL, 1)
 #pragma unroll
             for (int j = 0; j < 32; ++j) Ek[(32 * gq + j) * EKR + gf] = suf[j] * later;
             // masked decay reading: each delayed key enters scaled by the product of the w
-            // gates it saw in the window, e^{kd}, folded into its decay factor
+            // gates it saw in the window, e^{kd}, folded into its decay factor; the loads of
+            // each batch of the thread's 32 rows are issued before its first product
+            // (kd = 0: no factor)
             if (KEYF) {
-#pragma unroll 8
-                for (int j = 0; j < 32; ++j) {
-                    const int64_t key = t0 + 32 * gq + j - WIN;
-                    if (key >= 0 && 32 * gq + j < n)
-                        Ek[(32 * gq + j) * EKR + gf] *=
-                            __expf(a.kdec[((row0 + key) * p.Hkv + kv) * DF + gf]);
+                constexpr int KB = 16;
+                const int64_t kstride = p.Hkv * DF;
+                const float* kcol = a.kdec + (row0 * p.Hkv + kv) * DF + gf;
+#pragma unroll 1
+                for (int j0 = 0; j0 < 32; j0 += KB) {
+                    float kdl[KB];
+#pragma unroll
+                    for (int j = 0; j < KB; ++j) {
+                        const int64_t key = t0 + 32 * gq + j0 + j - WIN;
+                        kdl[j] = key >= 0 && 32 * gq + j0 + j < n ? kcol[key * kstride] : 0.0f;
+                    }
+#pragma unroll
+                    for (int j = 0; j < KB; ++j) Ek[(32 * gq + j0 + j) * EKR + gf] *= __expf(kdl[j]);
                 }
             }
             if (gq == 0) {

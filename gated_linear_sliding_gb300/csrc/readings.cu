@@ -54,34 +54,193 @@ __global__ void gate_lag_kernel(Plan p, const T* __restrict__ g, T* __restrict__
     reinterpret_cast<uint4*>(out + (r0 + i) * p.Hkv * p.D)[c] = val;
 }
 
-// kd[j] = sum_{s=j+1..min(j+w, len-1)} log sigmoid(g_s) for KJ consecutive rows j of one
-// column (KV head x feature) per thread, a window sum slid one row at a time in fp64 (the
-// per-gate logarithms in fp32).  Threads of a block take consecutive columns, so every load
-// and store of a row is contiguous.  grid.x = column blocks x row blocks, grid.y = sequence.
+// log sigmoid(x) = min(x, 0) - log(1 + u), u = e^{-|x|} in (0, 1], for the window sums of
+// the masked reading: log(1 + u) = 2 artanh(s) with s = u / (2 + u) <= 1/3, from the odd
+// power series artanh(s) = s + s^3/3 + s^5/5 + ... taken through s^15 (the first term left
+// out is below 2e-9 of the sum).  No branch, so the independent evaluations of one thread
+// interleave; its error is a few fp32 ulp of log(1 + u) plus that of the hardware
+// exponential and quotient.
+__device__ __forceinline__ float log_sigmoid_series(float x) {
+    const float u = __expf(-fabsf(x));
+    const float s = __fdividef(u, 2.0f + u);
+    const float z = s * s;
+    float q = 1.0f / 15.0f;
+    q = fmaf(q, z, 1.0f / 13.0f);
+    q = fmaf(q, z, 1.0f / 11.0f);
+    q = fmaf(q, z, 1.0f / 9.0f);
+    q = fmaf(q, z, 1.0f / 7.0f);
+    q = fmaf(q, z, 1.0f / 5.0f);
+    q = fmaf(q, z, 1.0f / 3.0f);
+    q = fmaf(q, z, 1.0f);
+    return fminf(x, 0.0f) - 2.0f * s * q;
+}
+
+// kd[j] = sum_{s=j+1..min(j+w, len-1)} log sigmoid(g_s), one column (KV head x feature) per
+// thread.  Every term is <= 0, so a sum that only adds never cancels.  A run of n <= w rows
+// [a, a+n) has every window (j, j+w] straddle M = a + w: kd_j = (sum over (j, M]) + (sum over
+// (M, j+w]), the first grown downward from the middle run (a+n, M], the second upward from
+// M (kept per row in shared memory), both compensated fp32 sums; w + n - 1 logarithms per n
+// rows.  Threads of a block take consecutive columns, so every load and store of a row is
+// contiguous.  grid.x = column blocks x row blocks of KJ, grid.y = sequence.
 constexpr int KJ = 64;
+
+// s += x with the rounding error carried in c (Kahan).
+__device__ __forceinline__ void comp_add(float& s, float& c, float x) {
+    const float y = x - c;
+    const float t = s + y;
+    c = (t - s) - y;
+    s = t;
+}
 
 template <typename T>
 __global__ void __launch_bounds__(128) key_decay_kernel(Plan p, const T* __restrict__ g,
                                                         float* __restrict__ kd) {
+    __shared__ float up[KJ][128];  // the upward sums, row t of the run x thread
     const int64_t b = blockIdx.y;
     const int64_t len = seq_len(p, b), r0 = seq_row0(p, b);
     const int64_t HD = p.Hkv * p.D, ncb = (HD + 127) / 128;
     const int64_t cb = blockIdx.x % ncb, jb = blockIdx.x / ncb;
     const int64_t col = cb * 128 + threadIdx.x;
     const int64_t j0 = jb * KJ;
-    if (col >= HD || j0 >= len) return;
-    const int64_t j1 = min64(len, j0 + KJ), last = len - 1;
+    if (col >= HD || j0 >= len) return;  // no block barrier below
+    const int64_t j1 = min64(len, j0 + KJ), last = len - 1, w = p.w;
     const T* gc = g + r0 * HD + col;
-    double acc = 0.0;
-    for (int64_t s = j0 + 1; s <= min64(j0 + p.w, last); ++s)
-        acc += (double)log_sigmoid<false>(ld(gc + s * HD));
-#pragma unroll 4
-    for (int64_t j = j0; j < j1; ++j) {
-        kd[(r0 + j) * HD + col] = (float)acc;
-        // the window of row j + 1 is s = j+2 .. j+1+w: gate j+1+w joins, gate j+1 leaves
-        const float in = j + 1 + p.w <= last ? log_sigmoid<false>(ld(gc + (j + 1 + p.w) * HD)) : 0.0f;
-        const float out = j + 1 <= last ? log_sigmoid<false>(ld(gc + (j + 1) * HD)) : 0.0f;
-        acc += (double)in - (double)out;
+    float* upc = &up[0][threadIdx.x];
+    // each pass takes its gates KB rows at a time, every load of a batch issued first
+    constexpr int KB = 16;
+    for (int64_t a = j0; a < j1; a += w) {
+        const int n = (int)min64(w, j1 - a);
+        const int64_t M = a + w, top = min64(M, last);
+        float us = 0.0f, uc = 0.0f;
+        upc[0] = 0.0f;
+        for (int t0 = 1; t0 < n; t0 += KB) {  // upward: gates M+1 .. M+n-1
+            float x[KB];
+#pragma unroll
+            for (int k = 0; k < KB; ++k)
+                x[k] = t0 + k < n && M + t0 + k <= last ? ld(gc + (M + t0 + k) * HD) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < KB; ++k) {
+                if (t0 + k >= n) break;
+                if (M + t0 + k <= last) comp_add(us, uc, log_sigmoid_series(x[k]));
+                upc[(t0 + k) * 128] = us;
+            }
+        }
+        float ds = 0.0f, dc = 0.0f;
+        for (int64_t s0 = a + n + 1; s0 <= top; s0 += KB) {  // the middle run a+n+1 .. M
+            float x[KB];
+#pragma unroll
+            for (int k = 0; k < KB; ++k) x[k] = s0 + k <= top ? ld(gc + (s0 + k) * HD) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < KB; ++k)
+                if (s0 + k <= top) comp_add(ds, dc, log_sigmoid_series(x[k]));
+        }
+        for (int t0 = n - 1; t0 >= 0; t0 -= KB) {  // downward: gate a+t+1 joins row a+t
+            float x[KB];
+#pragma unroll
+            for (int k = 0; k < KB; ++k)
+                x[k] = t0 - k >= 0 && a + t0 - k + 1 <= last ? ld(gc + (a + t0 - k + 1) * HD) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < KB; ++k) {
+                const int t = t0 - k;
+                if (t < 0) break;
+                if (a + t + 1 <= last) comp_add(ds, dc, log_sigmoid_series(x[k]));
+                kd[(r0 + a + t) * HD + col] = ds + upc[t * 128];
+            }
+        }
+    }
+}
+
+// The same sums for windows of at most TW rows, from shared memory: a CTA copies rows
+// (j0, j0 + TR - 1 + w] of TC columns of g in with asynchronous 16-byte copies (all in
+// flight at once), takes their logarithms once (1 + (w - 1)/TR per output instead of about
+// 2), then each thread takes a (column, run of w rows) pair through the two passes above.
+// Needs HD a multiple of 16 bytes of T and g 16-byte aligned.  grid.x = column blocks x row
+// blocks of TR, grid.y = sequence; 128 threads.
+constexpr int TR = 256, TC = 32, TW = 64;
+constexpr size_t kKeyTileSmem = sizeof(float) * ((TR + TW) * TC + TW * 128);
+
+// Four consecutive elements of shared memory (8- or 16-byte aligned) as floats.
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 ld4(const __nv_bfloat16* p) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+}
+
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     (uint32_t)__cvta_generic_to_shared(dst)),
+                 "l"(src)
+                 : "memory");
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) key_decay_tiled(Plan p, const T* __restrict__ g,
+                                                       float* __restrict__ kd) {
+    extern __shared__ __align__(16) float ksm[];
+    float* lam = ksm;                  // [TR + w - 1][TC]: log sigmoid of row j0 + 1 + r
+    float* up = ksm + (TR + TW) * TC;  // [TW][128]: upward sums of the thread's run
+    // the raw rows: in place of their logarithms (fp32) or in the upward sums' space (bf16)
+    T* stage = sizeof(T) == 4 ? reinterpret_cast<T*>(lam) : reinterpret_cast<T*>(up);
+    const int64_t b = blockIdx.y;
+    const int64_t len = seq_len(p, b), r0 = seq_row0(p, b);
+    const int64_t HD = p.Hkv * p.D, ncb = (HD + TC - 1) / TC;
+    const int64_t cb = blockIdx.x % ncb, jb = blockIdx.x / ncb;
+    const int64_t j0 = jb * TR, c0 = cb * TC;
+    if (j0 >= len) return;  // the whole block leaves together
+    const int64_t j1 = min64(len, j0 + TR), last = len - 1, w = p.w;
+    const int tid = threadIdx.x, nrow = (int)(TR + w - 1);
+    // (1) the tile of logarithms; rows past the sequence's end and columns past HD hold 0
+    {
+        constexpr int CH = 16 / (int)sizeof(T), NCH = TC / CH;  // elements, chunks per row
+        const T* gt = g + (r0 + j0 + 1) * HD + c0;
+        for (int e = tid; e < nrow * NCH; e += 128) {
+            const int r = e / NCH, ch = e % NCH;
+            if (j0 + 1 + r <= last && c0 + ch * CH < HD)
+                cp_async16(stage + r * TC + ch * CH, gt + (int64_t)r * HD + ch * CH);
+        }
+        asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+        __syncthreads();
+        // four columns per thread (HD is a multiple of 4, so a quad is wholly in or out)
+        for (int e = tid; e < nrow * (TC / 4); e += 128) {
+            const int r = e / (TC / 4), c = 4 * (e % (TC / 4));
+            float4 l = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            if (j0 + 1 + r <= last && c0 + c < HD) {
+                const float4 x = ld4(stage + r * TC + c);
+                l = make_float4(log_sigmoid_series(x.x), log_sigmoid_series(x.y),
+                                log_sigmoid_series(x.z), log_sigmoid_series(x.w));
+            }
+            *reinterpret_cast<float4*>(lam + r * TC + c) = l;  // (fp32: the same elements)
+        }
+    }
+    __syncthreads();
+    // (2) runs [a, a + n) of w rows, kd_j = (sum over (j, a + w]) + (sum over (a + w, j + w])
+    const int64_t nrun = (j1 - j0 + w - 1) / w;
+    float* upt = up + tid;
+    for (int64_t pr = tid; pr < nrun * TC; pr += 128) {
+        const int c = (int)(pr % TC);
+        const int64_t a = j0 + (pr / TC) * w;
+        if (c0 + c >= HD) continue;
+        const int n = (int)min64(w, j1 - a);
+        const float* lc = lam + c;
+        const int mrow = (int)(a + w - j0 - 1);  // tile row of gate a + w (= M)
+        float us = 0.0f, uc = 0.0f;
+        upt[0] = 0.0f;
+#pragma unroll 8
+        for (int t = 1; t < n; ++t) {  // upward: gates M+1 .. M+n-1
+            comp_add(us, uc, lc[(mrow + t) * TC]);
+            upt[t * 128] = us;
+        }
+        float ds = 0.0f, dc = 0.0f;
+#pragma unroll 8
+        for (int r = (int)(a - j0) + n; r <= mrow; ++r) comp_add(ds, dc, lc[r * TC]);  // middle
+        float* out = kd + (r0 + a) * HD + c0 + c;
+#pragma unroll 8
+        for (int t = n - 1; t >= 0; --t) {  // downward: gate a+t+1 joins row a+t
+            comp_add(ds, dc, lc[((int)(a - j0) + t) * TC]);
+            out[(int64_t)t * HD] = ds + upt[t * 128];
+        }
     }
 }
 
@@ -92,8 +251,9 @@ __global__ void __launch_bounds__(128) key_decay_kernel(Plan p, const T* __restr
 constexpr int RP = 4;
 
 template <typename T>
-__global__ void decode_ring_kernel(Plan p, int64_t pos_all, const int64_t* pos_dev,
-                                   const T* __restrict__ g, T* __restrict__ gc, void* out) {
+__global__ void __launch_bounds__(RP * 128, 3)
+decode_ring_kernel(Plan p, int64_t pos_all, const int64_t* pos_dev,
+                   const T* __restrict__ g, T* __restrict__ gc, void* out) {
     __shared__ float part_sum[RP][128];
     const int64_t unit = blockIdx.x, b = unit / p.Hkv;
     const int f = (int)(threadIdx.x % p.D), part = (int)(threadIdx.x / p.D);
@@ -110,16 +270,24 @@ __global__ void decode_ring_kernel(Plan p, int64_t pos_all, const int64_t* pos_d
         }
     } else {
         // token pos - w enters scaled by prod_{s=pos-w+1..pos} Gamma_s: this thread sums the
-        // slots of its run of tokens pos-w+1 .. pos-1, stepping the slot without a division
+        // slots of its run of tokens pos-w+1 .. pos-1, RB slots at a time with every load of
+        // a batch issued before the first logarithm, stepping the slot without a division
+        constexpr int RB = 8;
         float acc = 0.0f;
         if (pos >= w) {
             const int64_t n = w - 1, per = (n + RP - 1) / RP;
             const int64_t s0 = pos - w + 1 + part * per, s1 = min64(pos, s0 + per);
             int slot = s0 < s1 ? (int)(s0 % R) : 0;
-#pragma unroll 4
-            for (int64_t s = s0; s < s1; ++s) {
-                acc += log_sigmoid<false>(ld(gu + (int64_t)slot * p.D));
-                slot = slot + 1 == (int)R ? 0 : slot + 1;
+            for (int64_t c0 = s0; c0 < s1; c0 += RB) {
+                float x[RB];
+#pragma unroll
+                for (int k = 0; k < RB; ++k) {
+                    x[k] = c0 + k < s1 ? ld(gu + (int64_t)slot * p.D) : 0.0f;
+                    slot = slot + 1 == (int)R ? 0 : slot + 1;
+                }
+#pragma unroll
+                for (int k = 0; k < RB; ++k)
+                    if (c0 + k < s1) acc += log_sigmoid_series(x[k]);
             }
         }
         part_sum[part][f] = acc;
@@ -129,7 +297,7 @@ __global__ void decode_ring_kernel(Plan p, int64_t pos_all, const int64_t* pos_d
             if (pos >= w) {
 #pragma unroll
                 for (int k = 0; k < RP; ++k) tot += part_sum[k][f];
-                tot += log_sigmoid<false>(ld(&gnew));
+                tot += log_sigmoid_series(ld(&gnew));
             }
             ((float*)out)[e] = tot;
         }
@@ -209,6 +377,21 @@ cudaError_t launch_gate_lag(const Plan& p, const void* g, void* out, cudaStream_
 }
 
 cudaError_t launch_key_decay(const Plan& p, const void* g, float* kd, cudaStream_t s) {
+    if (p.w <= TW && (p.Hkv * p.D * (int64_t)elem(p)) % 16 == 0 && ((uintptr_t)g & 15u) == 0) {
+        const int64_t ncb = (p.Hkv * p.D + TC - 1) / TC, njb = (p.L + TR - 1) / TR;
+        const dim3 grid((unsigned)(ncb * njb), (unsigned)p.B);
+        auto k = p.dtype == LIZARD_F32 ? (void*)key_decay_tiled<float>
+                                       : (void*)key_decay_tiled<__nv_bfloat16>;
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)kKeyTileSmem);
+        if (e != cudaSuccess) return e;
+        if (p.dtype == LIZARD_F32)
+            key_decay_tiled<float><<<grid, 128, kKeyTileSmem, s>>>(p, (const float*)g, kd);
+        else
+            key_decay_tiled<__nv_bfloat16><<<grid, 128, kKeyTileSmem, s>>>(
+                p, (const __nv_bfloat16*)g, kd);
+        return cudaGetLastError();
+    }
     const int64_t ncb = (p.Hkv * p.D + 127) / 128;
     const int64_t njb = (p.L + KJ - 1) / KJ;
     const dim3 grid((unsigned)(ncb * njb), (unsigned)p.B);
