@@ -1051,6 +1051,11 @@ __global__ void __launch_bounds__(NT, 1)
     for (int64_t c = c_begin; c < c_end; ++c) {
         const int64_t t0 = c * CT;
         const int n = (int)min64(CT, s1 - t0);
+        if (KEYF && tid < 128) {  // the next step's key factors (32 rows), into L2
+            const int64_t tn = t0 + CT + (tid >> 2);
+            if (tn - WIN >= 0 && tn < s1)
+                prefetch_l2(a.kdec + ((b * p.L + tn - WIN) * p.Hkv + kv) * 128 + 32 * (tid & 3));
+        }
         const bool more = c + 1 < c_end;
         ok = fw_wait(&S.bar_tma, ph_tma, S, hdr, 60);
         if (!ok) break;
@@ -1686,6 +1691,11 @@ __global__ void __launch_bounds__(NT, 1)
         const int64_t t0 = c * CT;
         const int n = (int)min64(CT, s1 - t0);
         const bool more = c > c_first;
+        if (KEYF && more && tid < 128) {  // the next step's key factors (32 rows), into L2
+            const int64_t tn = t0 - CT + (tid >> 2);
+            if (tn - WIN >= 0 && tn < s1)
+                prefetch_l2(a.kdec + ((b * p.L + tn - WIN) * p.Hkv + kv) * 128 + 32 * (tid & 3));
+        }
         ok = fw_wait2(&S.bar_tma, ph_tma, S.abort, hdr, 70);
         if (!ok) break;
         if (tid == 0) {

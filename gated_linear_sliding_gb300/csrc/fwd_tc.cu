@@ -435,21 +435,11 @@ __global__ void __launch_bounds__(NT, 1)
             const int n = (int)min64(CT, s1 - t0);
             const int slot_d = (int)((c - 2) & 3);
 
-            // (1) this step's keys, values, gates (and queries) have landed; the control warp
-            //     has started the feature-map projections and window scores
-            ok = math_wait(&S.bar_tma, ph_tma, S, hdr, 2);
-            if (!ok) break;
-
-            // (2) gates: four threads per feature, one per 8-token quarter.  Every decay factor
-            //     of the step relative to r = b_15 is a running product of Gamma = sigmoid(g) or
-            //     of 1/Gamma = 1 + e^{-g} over the tokens between (no logarithm)
-            const int gf = tid & (DF - 1), gq = tid >> 7;
-            float ig[CT / 4];  // 1/Gamma of the thread's tokens (Gamma itself is rcp of it)
-            float pig = 1.0f;
+            const int gf = tid & (DF - 1), gq = tid >> 7;  // phase (2): feature, quarter
             // masked decay reading: the delayed key of each of the thread's tokens enters with
             // its phi scaled by the product of the w gates it saw in the window, e^{kd}, folded
-            // into its decay factor below.  Loaded first, so the gate products run while the
-            // loads are in flight.
+            // into its decay factor in phase (2).  Loaded before the wait for the step's tiles,
+            // and the next step's factors are fetched into L2 meanwhile.
             float kl[CT / 4];  // log factors (0 for a token with no key entering)
 #pragma unroll
             for (int t = 0; t < CT / 4; ++t) {
@@ -458,6 +448,25 @@ __global__ void __launch_bounds__(NT, 1)
                             ? a.kdec[((row0 + j) * p.Hkv + kv) * DF + gf]
                             : 0.0f;
             }
+            if (KEYF) {
+#pragma unroll
+                for (int t = 0; t < CT / 4; ++t) {
+                    const int64_t j = t0 + CT + (CT / 4) * gq + t - WIN;
+                    if (j >= 0 && j + WIN < s1)
+                        prefetch_l2(a.kdec + ((row0 + j) * p.Hkv + kv) * DF + gf);
+                }
+            }
+
+            // (1) this step's keys, values, gates (and queries) have landed; the control warp
+            //     has started the feature-map projections and window scores
+            ok = math_wait(&S.bar_tma, ph_tma, S, hdr, 2);
+            if (!ok) break;
+
+            // (2) gates: four threads per feature, one per 8-token quarter.  Every decay factor
+            //     of the step relative to r = b_15 is a running product of Gamma = sigmoid(g) or
+            //     of 1/Gamma = 1 + e^{-g} over the tokens between (no logarithm)
+            float ig[CT / 4];  // 1/Gamma of the thread's tokens (Gamma itself is rcp of it)
+            float pig = 1.0f;
             {
                 const __nv_bfloat16* sg = (const __nv_bfloat16*)(sm + oG);
 #pragma unroll
@@ -1109,6 +1118,12 @@ __global__ void __launch_bounds__(NL, 1)
                     }
 #pragma unroll
                     for (int j = 0; j < KB; ++j) Ek[(32 * gq + j0 + j) * EKR + gf] *= __expf(kdl[j]);
+                }
+                // the next step's factors, into L2 while this step computes
+#pragma unroll 8
+                for (int j = 0; j < 32; ++j) {
+                    const int64_t key = t0 + LT + 32 * gq + j - WIN;
+                    if (key >= 0 && key + WIN < s1) prefetch_l2(kcol + key * kstride);
                 }
             }
             if (gq == 0) {
