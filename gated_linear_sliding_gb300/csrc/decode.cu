@@ -588,6 +588,9 @@ __global__ void __launch_bounds__(ST, 1)
     }
     if (tid < 64) reinterpret_cast<uint32_t*>(sm.zrow)[tid] = 0u;
     __syncthreads();
+    // after a gate-ring step this grid may start while that step still runs: nothing it
+    // wrote (the step's gates or key factors) is read before here
+    grid_dep_wait();
 
     if (warp < 8) {
         // ================= front: rows in; u, scores, feature maps, softmax, P V =================
@@ -1058,6 +1061,9 @@ cudaError_t launch_decode_stream(const Plan& p, const DecodeArgs& a, const Strea
     if (e != cudaSuccess) return e;
     const int64_t U = p.B * p.Hkv;
     const unsigned grid = (unsigned)(U < nsm ? U : nsm);
+    // after the other readings' gate-ring step: a dependent launch, overlapping its start
+    if (p.decay != LIZARD_DECAY_DELAYED)
+        return launch_dependent(kern, dim3(grid), dim3(ST), kStreamSmem, s, p, a, mp);
     kern<<<grid, ST, kStreamSmem, s>>>(p, a, mp);
     return cudaGetLastError();
 }

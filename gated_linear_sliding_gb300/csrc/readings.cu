@@ -255,6 +255,7 @@ __global__ void __launch_bounds__(RP * 128, 3)
 decode_ring_kernel(Plan p, int64_t pos_all, const int64_t* pos_dev,
                    const T* __restrict__ g, T* __restrict__ gc, void* out) {
     __shared__ float part_sum[RP][128];
+    grid_dep_launch();  // the decode step may be launched now (it waits for this grid's end)
     const int64_t unit = blockIdx.x, b = unit / p.Hkv;
     const int f = (int)(threadIdx.x % p.D), part = (int)(threadIdx.x / p.D);
     const int64_t pos = pos_dev != nullptr ? pos_dev[b] : pos_all;
@@ -404,7 +405,9 @@ cudaError_t launch_key_decay(const Plan& p, const void* g, float* kd, cudaStream
 
 cudaError_t launch_decode_ring(const Plan& p, const DecodeArgs& a, void* out, cudaStream_t s) {
     if (p.D > 128) return cudaErrorInvalidValue;  // the per-part sums hold 128 features
-    const unsigned grid = (unsigned)(p.B * p.Hkv), block = (unsigned)(RP * p.D);
+    // (the lagged step copies one gate row per unit: one thread per feature)
+    const unsigned grid = (unsigned)(p.B * p.Hkv),
+                   block = (unsigned)((p.decay == LIZARD_DECAY_LAGGED ? 1 : RP) * p.D);
     if (p.dtype == LIZARD_F32)
         decode_ring_kernel<float><<<grid, block, 0, s>>>(p, a.pos, a.pos_dev, (const float*)a.g,
                                                          (float*)a.gc, out);
