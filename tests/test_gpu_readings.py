@@ -476,3 +476,66 @@ def test_fwd_masked_tensor_core_walk_closed_gates(lz, oracle_mod):
     out = gpu_fwd(lz, inp, wl, MASKED, state=False)
     ref = oracle_mod.fwd(**inp, w=wl.w, reading=MASKED)
     assert_parity(out["y"], ref["y"], "bf16", "y")
+
+
+@pytest.mark.parametrize("reading", READINGS)
+def test_decode_graph_replay_matches_eager(lz, reading):
+    """The gate-ring step and the streaming decode step after it (launched as the ring
+    step's programmatic dependent) captured in one CUDA graph: replays give the eager
+    steps' outputs, states and rings bit for bit."""
+    wl = I.DECODE_B64.replace(B=3)
+    L0, steps, w = 100, 4, wl.w
+    t = to_dev(I.make_inputs(wl.replace(L=L0 + steps)), wl.dtype)
+    tdt = t["q"].dtype
+    S = torch.empty(wl.B, wl.Hkv, wl.D, wl.d, dtype=torch.float32, device="cuda")
+    z = torch.empty(wl.B, wl.Hkv, wl.D, dtype=torch.float32, device="cuda")
+    kc = torch.zeros(wl.B, wl.Hkv, w + 1, wl.d, dtype=tdt, device="cuda")
+    vc = torch.zeros_like(kc)
+    gc = torch.zeros(wl.B, wl.Hkv, w + 1, wl.D, dtype=tdt, device="cuda")
+    pre = {n: t[n][:, :L0].contiguous() for n in ("q", "k", "v", "g")}
+    lz.lizard_attn_fwd(pre["q"], pre["k"], pre["v"], pre["g"], t["Wf"], t["sinks"], w,
+                       S_out=S, z_out=z, kcache_out=kc, vcache_out=vc, decay=reading)
+    lz.lizard_gate_cache_fill(pre["g"], gc, w)
+    dims = lz.make_dims(wl.B, 1, wl.Hq, wl.Hkv, wl.d, wl.D, w, wl.M, tdt, decay=reading)
+    ws = lz.new_workspace(lz.lizard_decode_workspace(dims), "cuda")
+    torch.cuda.synchronize()
+    states = (S, z, kc, vc, gc)
+    start = [x.clone() for x in states]
+    tok = {n: t[n][:, L0].contiguous() for n in ("q", "k", "v", "g")}
+    y = torch.empty(wl.B, wl.Hq, wl.d, dtype=tdt, device="cuda")
+    pos = torch.full((wl.B,), L0, dtype=torch.int64, device="cuda")
+
+    def step():
+        lz.lizard_decode_step_positions(pos, tok["q"], tok["k"], tok["v"], tok["g"], t["Wf"],
+                                        t["sinks"], S, z, kc, vc, w, y=y, workspace=ws,
+                                        gcache=gc, decay=reading)
+        pos.add_(1)
+
+    eager = []
+    for i in range(steps):
+        for n in tok:
+            tok[n].copy_(t[n][:, L0 + i])
+        step()
+        eager.append(y.clone())
+    torch.cuda.synchronize()
+    end = [x.clone() for x in states]
+    for x, x0 in zip(states, start):
+        x.copy_(x0)
+    pos.fill_(L0)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    replayed = []
+    for i in range(steps):
+        for n in tok:
+            tok[n].copy_(t[n][:, L0 + i])
+        graph.replay()
+        replayed.append(y.clone())
+    torch.cuda.synchronize()
+    assert lz.lizard_read_device_status(ws) == lz.LIZARD_OK
+    assert pos.tolist() == [L0 + steps] * wl.B
+    for i, (a_, b_) in enumerate(zip(eager, replayed)):
+        assert torch.equal(a_, b_), f"step {i}"
+    for name, x, x1 in zip(("S", "z", "kcache", "vcache", "gcache"), states, end):
+        assert torch.equal(x, x1), name
