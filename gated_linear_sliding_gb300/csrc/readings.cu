@@ -328,8 +328,18 @@ __global__ void key_chunk_total_kernel(Plan p, const float* __restrict__ kk, flo
     if (e >= p.B * nch * HD) return;
     const int64_t col = e % HD, r = e / HD, chunk = r % nch, b = r / nch;
     const int64_t j0 = chunk * KS, j1 = min64(min64(p.L, j0 + KS), p.L - p.w);
+    // rows taken KB at a time, every load of a batch issued before the first addition
+    constexpr int KB = 16;
+    const float* x = kk + b * p.L * HD + col;
     float s = 0.0f;
-    for (int64_t j = j0; j < j1; ++j) s += kk[(b * p.L + j) * HD + col];
+    for (int64_t jt = j0; jt < j1; jt += KB) {
+        float v[KB];
+#pragma unroll
+        for (int k = 0; k < KB; ++k) v[k] = jt + k < j1 ? x[(jt + k) * HD] : 0.0f;
+#pragma unroll
+        for (int k = 0; k < KB; ++k)
+            if (jt + k < j1) s += v[k];
+    }
     kt[e] = s;
 }
 
@@ -342,9 +352,21 @@ __global__ void key_suffix_kernel(Plan p, float* __restrict__ kk, const float* _
     for (int64_t c = nch - 1; c > chunk; --c) run += kt[(b * nch + c) * HD + col];
     const int64_t j0 = chunk * KS, j1 = min64(p.L, j0 + KS);
     float* x = kk + b * p.L * HD + col;
-    for (int64_t j = j1 - 1; j >= j0; --j) {
-        if (j <= p.L - 1 - p.w) run += x[j * HD];
-        x[j * HD] = run;
+    // rows read KB at a time before any of them is overwritten: the loads of a batch are in
+    // flight together instead of each waiting behind the store before it
+    constexpr int KB = 16;
+    for (int64_t jt = j1 - 1; jt >= j0; jt -= KB) {
+        float v[KB];
+#pragma unroll
+        for (int k = 0; k < KB; ++k) v[k] = jt - k >= j0 ? x[(jt - k) * HD] : 0.0f;
+#pragma unroll
+        for (int k = 0; k < KB; ++k) {
+            const int64_t j = jt - k;
+            if (j >= j0) {
+                if (j <= p.L - 1 - p.w) run += v[k];
+                x[j * HD] = run;
+            }
+        }
     }
 }
 
