@@ -1038,12 +1038,21 @@ __global__ void bwd_tot_suffix(Plan p, float* tot) {
     const int64_t U = p.B * p.Hkv;
     const int64_t e = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;  // unit * D + f
     if (e >= U * p.D) return;
+    // totals read eight at a time before any is overwritten (one round trip per group
+    // instead of one per segment)
+    constexpr int KG = 8;
     float run = 0.0f;
-    for (int64_t sg = p.P - 1; sg >= 0; --sg) {
-        float* x = tot + (size_t)sg * U * p.D + e;
-        const float t = *x;
-        *x = run;
-        run += t;
+    for (int64_t s0 = p.P - 1; s0 >= 0; s0 -= KG) {
+        float t[KG];
+#pragma unroll
+        for (int k = 0; k < KG; ++k) t[k] = s0 - k >= 0 ? tot[(size_t)(s0 - k) * U * p.D + e] : 0.0f;
+#pragma unroll
+        for (int k = 0; k < KG; ++k) {
+            if (s0 - k >= 0) {
+                tot[(size_t)(s0 - k) * U * p.D + e] = run;
+                run += t[k];
+            }
+        }
     }
 }
 
