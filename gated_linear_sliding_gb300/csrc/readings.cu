@@ -10,7 +10,7 @@
 //   MASKED  prod_{s=j+1..i} Gamma_s    = the delayed reading with each entering key's phi
 //           scaled by c_j = prod_{s=j+1..j+w} Gamma_s, the gates it saw in the window; the
 //           forward and backward walks (tensor-core and SIMT) apply e^{kd_j}, kd_j = log c_j
-//           from key_decay_kernel.
+//           from key_decay_tiled (windows up to 64) or key_decay_kernel.
 // Decode keeps the gate logits of the window in a ring like the keys and values: the
 // lagged step decays by the gate of token pos - w, the masked step admits token pos - w
 // scaled by the product of the gates of pos - w + 1 .. pos.
