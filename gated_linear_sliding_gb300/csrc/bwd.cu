@@ -832,12 +832,15 @@ __global__ void __launch_bounds__(NT, 1) bwd_reverse_walk(Plan p, BwdArgs a, Bwd
 // Segments whose gates close too hard for the tensor-core walks' factored decays: flag
 // (segment, unit) when some feature's cumulative log-gate falls by more than 60 over one of
 // the 16-token halves of the walks' 32-token steps (Lizard summary sec. 2-C: products of such
-// gates underflow).  Four threads per feature, each summing every fourth half.
-__global__ void bwd_gate_flags(Plan p, const __nv_bfloat16* g, int* flags) {
+// gates underflow).  128 threads: 16 per token row (8 features each) times 8 halves at a
+// time, so four CTAs fit an SM beside each other and one wave holds the grid.
+constexpr int kFlagThreads = 128;
+__global__ void __launch_bounds__(kFlagThreads) bwd_gate_flags(Plan p, const __nv_bfloat16* g,
+                                                               int* flags) {
     const int64_t unit = blockIdx.x, seg = blockIdx.y;
     const int64_t b = unit / p.Hkv, kv = unit % p.Hkv;
     const int64_t s0 = seg * p.seg_len, s1 = min64(p.L, s0 + p.seg_len);
-    // thread: features 8 c8 .. + 7 of the 16-token halves s0 + 16 hq, + 512, ...: one 16-byte
+    // thread: features 8 c8 .. + 7 of the 16-token halves s0 + 16 hq, + 128, ...: one 16-byte
     // load per token, the half's 16 loads in flight together.  A half's log-decay is
     // sum_t log sigmoid(g_t) = sum_t min(g_t, 0) - ln prod_t (1 + e^{-|g_t|}); every factor of
     // the product lies in (1, 2], so 16 of them stay finite and one logarithm per half does
@@ -845,7 +848,7 @@ __global__ void bwd_gate_flags(Plan p, const __nv_bfloat16* g, int* flags) {
     const int c8 = threadIdx.x & 15, hq = threadIdx.x >> 4;
     const int64_t stride = p.Hkv * 128;
     bool closed = false;
-    for (int64_t h0 = s0 + 16 * hq; h0 < s1; h0 += 16 * 32) {
+    for (int64_t h0 = s0 + 16 * hq; h0 < s1; h0 += 16 * (kFlagThreads / 16)) {
         const int nt = (int)min64(16, s1 - h0);
         const __nv_bfloat16* row = g + ((b * p.L + h0) * p.Hkv + kv) * 128 + 8 * c8;
         uint4 v[16];
@@ -1159,7 +1162,8 @@ cudaError_t bwd_impl(const Plan& p, const BwdArgs& a_in, cudaStream_t s) {
     int* flags = (int*)(wsf + ws.flags);
     if (tc_walks) {
         if constexpr (sizeof(T) == 2 && DF == 128)
-            bwd_gate_flags<<<dim3(U, (unsigned)p.P), 512, 0, s>>>(p, (const __nv_bfloat16*)a.g, flags);
+            bwd_gate_flags<<<dim3(U, (unsigned)p.P), kFlagThreads, 0, s>>>(
+                p, (const __nv_bfloat16*)a.g, flags);
     }
     if (a.ev_before) cudaEventRecord(a.ev_before, s);
     if (tc_walks) {
